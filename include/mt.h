@@ -1,0 +1,240 @@
+/* mt.h -- C ABI of the merged dynamic embedding table (GB300, sm_103a).
+ *
+ * The hot path of a dynamic hash embedding table as described in "MTGenRec:
+ * An Efficient Distributed Training System for Generative Recommendation
+ * Models in Meituan" (TL;DR and abstract: dynamic hash tables replacing
+ * static ones for real-time insertion and deletion, automated table merging,
+ * two-stage ID deduplication) and in "MTGR: Industrial-Scale Generative
+ * Recommendation Framework in Meituan" (section 5, Embedding Management: keys
+ * map to embedding vectors plus metadata; Embedding Lookup: IDs stay unique).
+ *
+ * Conventions that hold for every call:
+ *  - Plain C types only.  `mt_stream` is a cudaStream_t passed as void*
+ *    (NULL = the legacy default stream).
+ *  - The library never allocates device memory.  The caller provides the
+ *    table arena, every workspace and every output, as device pointers,
+ *    unless a parameter says "host".  Device buffers passed here must be
+ *    16-byte aligned; arenas and workspaces 256-byte aligned.
+ *  - Calls are asynchronous and stream-ordered on `stream`, except
+ *    mt_stats, mt_export and mt_get_error, which synchronise it.  One table
+ *    must be used from one stream at a time.
+ *  - A negative return value is an error detected on the host; nothing has
+ *    been enqueued.  Errors found on the device (an ID out of range, the
+ *    probe limit or the row pool exhausted) latch the first code into a
+ *    device error word that mt_stats / mt_get_error report; the affected
+ *    positions get row -1 and zero output, and the call otherwise completes.
+ *  - No kernel of this library waits on another block or another launch:
+ *    every probe loop is bounded by the table's probe limit.
+ */
+#ifndef MT_H
+#define MT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MT_ABI_VERSION 1
+
+/* Status codes. */
+enum {
+  MT_OK = 0,
+  MT_EINVAL = -1,   /* bad argument (even probe step, bad dim, bad offsets, ...) */
+  MT_ENOSPACE = -2, /* arena or workspace too small or misaligned */
+  MT_EFULL = -3,    /* device: probe limit reached or row pool exhausted */
+  MT_EKEY = -4,     /* device: an ID outside [0, 2^56) */
+  MT_ECUDA = -5     /* a CUDA runtime call failed */
+};
+
+/* Element types of rows and gradients. */
+enum { MT_F32 = 0, MT_BF16 = 1 };
+
+/* Merged key = (table_id << 56) | id with table_id in [0, 254] and id in
+ * [0, 2^56) ("automated table merging", MTGenRec TL;DR).  Table id 255 is
+ * reserved for the two slot sentinels. */
+#define MT_KEY_EMPTY 0xFFFFFFFFFFFFFFFFull
+#define MT_KEY_TOMBSTONE 0xFFFFFFFFFFFFFFFEull
+#define MT_MAX_FEATURES 256
+#define MT_MAX_DIM 1024
+#define MT_HIST_BINS 64
+
+typedef struct mt_table mt_table; /* opaque host handle, owned by the library */
+typedef void* mt_stream;
+
+/* Table configuration.
+ *  log2_slots  n: the key store has M = 2^n slots, 1 <= n <= 31.
+ *  dim         d: embedding width; a multiple of 4 (fp32 rows) or 8 (bf16
+ *              rows), 4 <= d <= MT_MAX_DIM.
+ *  row_dtype   MT_F32 or MT_BF16 storage of the embedding; the Adam moments
+ *              m and v are always fp32.
+ *  max_probes  probe limit per key; 0 means M.
+ *  probe_step  S of the probe sequence h_t = (h0 + t*S) mod M (MTGenRec,
+ *              Theorem 1).  Used mod M; it must be odd, which makes the
+ *              sequence visit every slot.  An even S is MT_EINVAL.
+ *  hash_seed   h0 = top n bits of splitmix64-finaliser(key ^ hash_seed).
+ *  init_seed   fresh rows: column j = scale * (2q - 2^24) / 2^24 with q the
+ *              top 24 bits of word j%4 of Philox4x64-10(counter (j/4,0,0,0),
+ *              key (merged key, init_seed)); m = v = 0.
+ *  init_scale  0 means fp32(1/sqrt(d)).
+ *  num_rows    R, rows in the row pool; 0 means M.  1 <= R <= M. */
+typedef struct {
+  uint32_t log2_slots;
+  uint32_t dim;
+  uint32_t row_dtype;
+  uint32_t max_probes;
+  uint64_t probe_step;
+  uint64_t hash_seed;
+  uint64_t init_seed;
+  float init_scale;
+  uint32_t flags; /* reserved, must be 0 */
+  int64_t num_rows;
+} mt_config;
+
+/* Per-batch result of mt_lookup; all pointers are device buffers of
+ * capacity n (the batch size) owned by the caller.  It stays valid for
+ * mt_backward_adam until the next mt_lookup or mt_erase on the table. */
+typedef struct {
+  uint64_t* unique_keys; /* [n]: first U entries: the distinct merged keys in first-occurrence order */
+  int32_t* inverse;      /* [n]: unique_keys[inverse[i]] is the key of position i; -1 for an invalid ID */
+  int32_t* counts;       /* [n]: first U entries: number of positions holding each unique key */
+  int32_t* unique_rows;  /* [n]: first U entries: row of each unique key, -1 when it has none */
+  int64_t* num_unique;   /* [1]: U */
+} mt_lookup_result;
+
+/* Adam hyper-parameters (Meituan TensorFlow article, section 3.2 names Adam;
+ * the update is Kingma & Ba's with bias correction, see mt_backward_adam). */
+typedef struct {
+  float lr, beta1, beta2, eps;
+} mt_adam;
+
+/* Occupancy of the key store (MTGenRec, Theorem 1 probe sequence). */
+typedef struct {
+  int64_t live;               /* slots holding a key */
+  int64_t tombstones;         /* slots holding MT_KEY_TOMBSTONE */
+  int64_t capacity;           /* M */
+  int64_t num_rows;           /* R */
+  int64_t rows_free;          /* rows on the free list */
+  int64_t step;               /* Adam steps taken (mt_backward_adam calls) */
+  int64_t total_displacement; /* sum over live keys of their probe index t */
+  double load_factor;         /* live / M */
+  int64_t probe_hist[MT_HIST_BINS]; /* live keys by probe index t; the last bin holds t >= 63 */
+  int32_t device_error;       /* first latched device error code, 0 if none */
+  int32_t reserved;
+} mt_stats_out;
+
+/* ---- table ------------------------------------------------------------- */
+
+/* Device bytes the table arena needs: a header, M 16-byte slots {key, row,
+ * insert step}, the row free list (R int32) and R row records
+ * [emb d x row dtype | m d x fp32 | v d x fp32], each padded to 16 bytes.
+ * Returns 0 for an invalid configuration. */
+size_t mt_table_bytes(const mt_config* cfg);
+
+/* Build a table in caller-owned device memory `dev_mem` (>= mt_table_bytes
+ * bytes, 256-byte aligned; owned by the caller and used by the table until
+ * it is destroyed).  Marks every slot EMPTY and every row free, enqueued on
+ * `stream`.  *out receives a host handle. */
+int mt_table_create(const mt_config* cfg, void* dev_mem, size_t bytes, mt_stream stream, mt_table** out);
+
+/* Free the host handle (not the arena). */
+int mt_table_destroy(mt_table* t);
+
+/* The configuration with defaults filled in (S reduced mod M, max_probes,
+ * init_scale, num_rows). */
+int mt_table_config(const mt_table* t, mt_config* out);
+
+/* ---- forward: encode, two-stage dedup, find/insert, gather -------------- */
+
+/* Workspace bytes mt_lookup needs for a batch of n IDs. */
+size_t mt_lookup_workspace_bytes(const mt_table* t, int64_t n);
+
+/* Lookup of one batch of n IDs (MTGenRec TL;DR: merged tables and two-stage
+ * ID deduplication; MTGR section 5, Embedding Lookup).
+ *  ids           device int64 [n]: raw feature IDs.
+ *  feat_offsets  host int64 [F+1]: positions [feat_offsets[f], feat_offsets[f+1])
+ *                belong to feature table f; 0 = off[0] <= ... <= off[F] = n.
+ *                NULL means F = 1 covering all n.
+ *  table_ids     host uint8 [F]: the table id of each feature, < 255.  NULL
+ *                means table id 0 for every feature.
+ *  insert_missing  1: absent keys are inserted with a fresh row ("real-time
+ *                insertions", MTGenRec abstract); 0: they get row -1.
+ *  out_rows      device [n, d] of the row dtype, or NULL to skip the gather:
+ *                out_rows[i] = embedding of key i (zeros for an invalid ID or
+ *                an absent key).
+ *  res           caller-owned result buffers (see mt_lookup_result).
+ *  ws, ws_bytes  device workspace of mt_lookup_workspace_bytes(t, n) bytes;
+ *                its contents are scratch and need no initialisation.
+ * Device errors: an ID outside [0, 2^56) latches MT_EKEY (inverse -1); a full
+ * chain or an empty row pool latches MT_EFULL (row -1). */
+int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_offsets, const uint8_t* table_ids,
+              int F, int insert_missing, void* out_rows, const mt_lookup_result* res, void* ws, size_t ws_bytes,
+              mt_stream stream);
+
+/* ---- backward: per-unique gradient sum + sparse row-wise Adam ------------ */
+
+/* Workspace bytes mt_backward_adam needs for a batch of n IDs. */
+size_t mt_backward_workspace_bytes(const mt_table* t, int64_t n);
+
+/* Backward of the lookup `res` (same n): g_u = sum of grads[i] over positions
+ * i with inverse[i] = u, accumulated in at least fp32 pair precision and
+ * rounded once to fp32; then, for every unique key with a row, one Adam step
+ * in fp32 with the table's step counter t (advanced once per call):
+ *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g*g;
+ *   w = w - lr * (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)
+ * (1-b1, 1-b2, 1-b1^t, 1-b2^t evaluated in double, then rounded to fp32).
+ * Rows absent from the batch are not touched.
+ *  grads      device [n, d] of grad_dtype (MT_F32 or MT_BF16).
+ *  gsum_out   device fp32 [n, d] or NULL: the first U rows receive g_u.
+ *  ws         device workspace of mt_backward_workspace_bytes(t, n) bytes. */
+int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const void* grads, int grad_dtype,
+                     const mt_adam* hp, float* gsum_out, void* ws, size_t ws_bytes, mt_stream stream);
+
+/* ---- deletion ------------------------------------------------------------ */
+
+/* Workspace bytes mt_erase needs for n keys. */
+size_t mt_erase_workspace_bytes(int64_t n);
+
+/* Delete n merged keys ("real-time deletions", MTGenRec abstract): a live
+ * key's slot becomes MT_KEY_TOMBSTONE, which later probes pass over and
+ * later inserts may reuse, and its row returns to the free list.  A key
+ * inserted again later starts from its initial row with m = v = 0.
+ *  keys   device uint64 [n] merged keys (duplicates allowed).
+ *  found  device uint8 [n] or NULL: 1 when the key was live before the call
+ *         (every duplicate of a live key reports 1). */
+int mt_erase(mt_table* t, const uint64_t* keys, int64_t n, uint8_t* found, void* ws, size_t ws_bytes,
+             mt_stream stream);
+
+/* ---- inspection ------------------------------------------------------------ */
+
+/* Scan the key store: live keys, tombstones, and each live key's probe index
+ * t = (slot - h0) * S^-1 mod M (S is odd, so S^-1 mod 2^n exists; MTGenRec
+ * Theorem 1).  Synchronises `stream`. */
+int mt_stats(mt_table* t, mt_stats_out* out, mt_stream stream);
+
+/* Copy up to `capacity` live (key, row) pairs into device buffers keys/rows
+ * (in no particular order) and the number of live keys into *count (host).
+ * Synchronises `stream`.  ("compact key scanning", MTGR section 5.) */
+int mt_export(mt_table* t, uint64_t* keys, int32_t* rows, int64_t capacity, int64_t* count, mt_stream stream);
+
+/* Read n rows (device int32 row indices; -1 gives zeros) as fp32 into device
+ * buffers emb, m, v ([n, d] each; any may be NULL). */
+int mt_read_rows(const mt_table* t, const int32_t* rows, int64_t n, float* emb, float* m, float* v,
+                 mt_stream stream);
+
+/* The first latched device error (0 if none) into *device_error (host);
+ * clears it when `clear` is non-zero.  Synchronises `stream`. */
+int mt_get_error(mt_table* t, int32_t* device_error, int clear, mt_stream stream);
+
+/* Adam steps taken so far (host-side count of mt_backward_adam calls). */
+int64_t mt_step(const mt_table* t);
+
+const char* mt_strerror(int code);
+int mt_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MT_H */

@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "orc_erase": (None, [P, P, I64, P]),
             "orc_insert_keys": (I64, [P, P, I64]),
             "orc_get_row": (I32, [P, U64, P, P, P]),
+            "orc_get_rows": (None, [P, P, I64, P, P, P, P]),
             "orc_live_count": (I64, [P]),
             "orc_live_keys": (I64, [P, P, I64]),
             "orc_step": (I64, [P]),
@@ -216,6 +217,16 @@ class Table:
         v = np.zeros(self.dim, np.float32)
         ok = lib().orc_get_row(self.h, int(key), _p(e), _p(m), _p(v))
         return (e, m, v) if ok else None
+
+    def get_rows(self, keys):
+        """(emb, m, v, present) for an array of merged keys; absent keys give zero rows."""
+        k = _c(keys, np.uint64)
+        e = np.zeros((k.size, self.dim), np.float32)
+        m = np.zeros_like(e)
+        v = np.zeros_like(e)
+        pr = np.zeros(k.size, np.uint8)
+        lib().orc_get_rows(self.h, _p(k), k.size, _p(e), _p(m), _p(v), _p(pr))
+        return e, m, v, pr.astype(bool)
 
     def erase(self, keys):
         k = _c(keys, np.uint64)

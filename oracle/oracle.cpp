@@ -455,6 +455,25 @@ int orc_get_row(void* h, uint64_t key, float* emb, float* m, float* v) {
   return 1;
 }
 
+// orc_get_row for n keys: rows [n, dim] each (nullable); present[i] = 1 when
+// keys[i] is in the table (absent keys give zero rows).
+void orc_get_rows(void* h, const uint64_t* keys, int64_t n, float* emb, float* m, float* v, uint8_t* present) {
+  Table* t = (Table*)h;
+  const uint32_t d = t->dim;
+  for (int64_t i = 0; i < n; ++i) {
+    int ok = orc_get_row(h, keys[i], emb ? emb + (size_t)i * d : nullptr, m ? m + (size_t)i * d : nullptr,
+                         v ? v + (size_t)i * d : nullptr);
+    if (!ok) {
+      for (uint32_t j = 0; j < d; ++j) {
+        if (emb) emb[(size_t)i * d + j] = 0.0f;
+        if (m) m[(size_t)i * d + j] = 0.0f;
+        if (v) v[(size_t)i * d + j] = 0.0f;
+      }
+    }
+    if (present) present[i] = (uint8_t)ok;
+  }
+}
+
 int64_t orc_live_count(void* h) { return (int64_t)((Table*)h)->rows.size(); }
 
 int64_t orc_live_keys(void* h, uint64_t* out, int64_t cap) {

@@ -1,0 +1,116 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every
+symbol include/mt.h declares, and rejects bad arguments on the host (no
+compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import update_merged_table_gb300 as mt
+from update_merged_table_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return mt.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mt_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("mt_table_create", "mt_lookup", "mt_backward_adam", "mt_erase", "mt_stats"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) == set(mt.ABI_FUNCTIONS)
+
+
+def test_abi_version_and_strerror(lib):
+    assert lib.mt_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.mt_strerror(code)
+    assert lib.mt_strerror(-99) == b"unknown status"
+
+
+def _cfg(**kw):
+    base = dict(log2_slots=10, dim=16, row_dtype=mt.MT_F32, max_probes=0, probe_step=1, hash_seed=0, init_seed=0,
+                init_scale=0.0, flags=0, num_rows=0)
+    base.update(kw)
+    return mt._Config(*[base[f] for f, _ in mt._Config._fields_])
+
+
+def test_table_bytes_layout(lib):
+    c = _cfg(log2_slots=10, dim=16)
+    nb = lib.mt_table_bytes(ctypes.byref(c))
+    # header 1 KiB + 1024 slots x 16 B + 1024 x int32 free list + 1024 rows x (16 + 16 + 16) x 4 B
+    assert nb == 1024 + 1024 * 16 + 1024 * 4 + 1024 * 16 * 4 * 3
+    c = _cfg(log2_slots=10, dim=64, row_dtype=mt.MT_BF16, num_rows=100)
+    # 100 rows x (128 B bf16 emb + 256 B m + 256 B v); free list 400 B padded to 512
+    assert lib.mt_table_bytes(ctypes.byref(c)) == 1024 + 1024 * 16 + 512 + 100 * 640
+
+
+@pytest.mark.parametrize("kw", [
+    dict(probe_step=2),                 # Theorem 1: an even step does not cover the table
+    dict(probe_step=1024),              # == 0 mod M
+    dict(log2_slots=0), dict(log2_slots=32),
+    dict(dim=0), dict(dim=6), dict(dim=2048),
+    dict(row_dtype=mt.MT_BF16, dim=12),  # bf16 rows need dim % 8 == 0
+    dict(row_dtype=7),
+    dict(num_rows=-1), dict(num_rows=2048),
+    dict(flags=1),
+    dict(init_scale=float("nan")),
+])
+def test_invalid_configs_rejected_on_host(lib, kw):
+    c = _cfg(**kw)
+    assert lib.mt_table_bytes(ctypes.byref(c)) == 0
+    h = ctypes.c_void_p()
+    assert lib.mt_table_create(ctypes.byref(c), None, 0, None, ctypes.byref(h)) == mt.MT_EINVAL
+    assert not h.value
+
+
+def test_odd_steps_accepted(lib):
+    for S in (1, 3, 1023, 0x9E3779B97F4A7C15):
+        assert lib.mt_table_bytes(ctypes.byref(_cfg(probe_step=S))) > 0
+
+
+def test_create_needs_space(lib):
+    c = _cfg()
+    h = ctypes.c_void_p()
+    assert lib.mt_table_create(ctypes.byref(c), None, 1 << 20, None, ctypes.byref(h)) == mt.MT_ENOSPACE
+    # misaligned arena
+    assert lib.mt_table_create(ctypes.byref(c), 16, 1 << 30, None, ctypes.byref(h)) == mt.MT_ENOSPACE
+
+
+def test_null_handles_rejected(lib):
+    r = mt._Result(0, 0, 0, 0, 0)
+    assert lib.mt_lookup(None, None, 0, None, None, 1, 1, None, ctypes.byref(r), None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_backward_adam(None, ctypes.byref(r), 0, None, 0, None, None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_erase(None, None, 0, None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_stats(None, None, None) == mt.MT_EINVAL
+    assert lib.mt_table_destroy(None) == mt.MT_EINVAL
+    assert lib.mt_step(None) == -1
+    assert lib.mt_lookup_workspace_bytes(None, 10) == 0
+    assert lib.mt_erase_workspace_bytes(1000) >= 4000
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The package never imports the oracle and has no CPU path."""
+    pkg = os.path.join(ROOT, "update_merged_table_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text, f

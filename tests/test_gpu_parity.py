@@ -1,0 +1,352 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: unique keys, inverse indices, counts, key presence and gathered
+rows (fresh rows come from a counter-based generator keyed by the ID, and
+slot placement is not compared).  Within tolerance: gradient sums and
+Adam-updated rows (fp32 rows 1e-5 relative + 1e-6 absolute; bf16 rows within
+one bf16 ulp), as the table's specification fixes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import update_merged_table_gb300 as mt
+from update_merged_table_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+RTOL, ATOL = 1e-5, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from update_merged_table_gb300 import build_lib
+    build_lib.build()
+    mt.load_library()
+    oracle.build()
+
+
+def dev():
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+def bf16_bits_of(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+
+
+def assert_rows_close(got: np.ndarray, want: np.ndarray, row_dtype: str):
+    if row_dtype == "bf16":
+        # both sides hold bf16 values; allow one unit in the last place
+        gb = bf16_bits_of(got).astype(np.int32)
+        wb = bf16_bits_of(want).astype(np.int32)
+        same_sign = np.sign(got) == np.sign(want)
+        diff = np.where(same_sign, np.abs(gb - wb), np.abs(got - want) > 0)
+        bad = (diff > 1) & ~((np.abs(got) < 1e-30) & (np.abs(want) < 1e-30))
+        assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
+    else:
+        np.testing.assert_allclose(got, want, rtol=RTOL, atol=ATOL)
+
+
+def compare_lookup(res, r, gather=True):
+    U = res.U
+    assert U == r["U"]
+    n = res.n
+    uk = res.unique_keys[:U].cpu().numpy().view(np.uint64)
+    assert np.array_equal(uk, r["unique"])
+    assert np.array_equal(res.inverse[:n].cpu().numpy(), r["inverse"])
+    assert np.array_equal(res.counts[:U].cpu().numpy(), r["counts"])
+    present = res.unique_rows[:U].cpu().numpy() >= 0
+    assert np.array_equal(present, r["present"])
+    if gather and n:
+        got = res.rows.float().cpu().numpy()
+        assert np.array_equal(got, r["rows"])
+
+
+def compare_after_adam(tab, res, ref, r, row_dtype, gsum=None, ref_gsum=None):
+    U = r["U"]
+    if gsum is not None:
+        np.testing.assert_allclose(gsum[:U].cpu().numpy(), ref_gsum, rtol=RTOL, atol=ATOL)
+    emb, m, v = tab.read_rows(res.unique_rows[:U])
+    e2, m2, v2, pr = ref.get_rows(r["unique"])
+    pres = pr
+    assert_rows_close(emb.cpu().numpy()[pres], e2[pres], row_dtype)
+    np.testing.assert_allclose(m.cpu().numpy()[pres], m2[pres], rtol=RTOL, atol=ATOL)
+    np.testing.assert_allclose(v.cpu().numpy()[pres], v2[pres], rtol=RTOL, atol=1e-9)
+
+
+def grads_for(seed, n, d, dtype):
+    g = W.grads_normal(seed, n, d)
+    if dtype == "bf16":
+        gb = torch.from_numpy(g).to(torch.bfloat16)
+        return gb.to(dev()), gb.view(torch.int16).numpy().view(np.uint16), oracle.BF16
+    return to_dev(g), g, oracle.F32
+
+
+def run_steps(tab, ref, batches, row_dtype="f32", grad_dtype="f32", seed0=100, check_rows_every=1):
+    for k, b in enumerate(batches):
+        res = tab.lookup(to_dev(b.ids), b.feat_offsets, b.table_ids)
+        r = ref.lookup(b.ids, b.feat_offsets, b.table_ids)
+        compare_lookup(res, r)
+        gd, gh, gdt = grads_for(seed0 + k, b.n, tab.dim, grad_dtype)
+        gsum = tab.backward_adam(res, gd, want_gsum=True)
+        ref_gsum = ref.backward_adam(gh, grad_dtype=gdt, want_gsum=True)
+        if k % check_rows_every == 0:
+            compare_after_adam(tab, res, ref, r, row_dtype, gsum, ref_gsum)
+    assert tab.error() == 0 and ref.error == 0
+
+
+# ---------------------------------------------------------------------------
+# the workloads, at sizes the oracle finishes in seconds
+# ---------------------------------------------------------------------------
+
+def test_single_table_workload():
+    """M = 2^16, dim 16 fp32, 4096 IDs Zipf(1.1) over 1e5; lookup+insert then backward+Adam."""
+    b = W.single_table_batch(0)
+    tab = mt.Table(16, 16)
+    ref = oracle.Table(16, 16, simulate=True)
+    run_steps(tab, ref, [b])
+    st = tab.stats()
+    sim = ref.sim_stats()
+    assert st["live"] == sim["live"] == ref.live
+    assert st["total_displacement"] == sim["total_displacement"]  # insert-only: order-independent
+    assert st["step"] == 1 and tab.step == 1
+
+
+@pytest.mark.parametrize("probe_step", [1, 3, 0x9E3779B97F4A7C15])
+def test_merged_tables_steps(probe_step):
+    """8 feature tables merged by table id into one table, dim 32 fp32, several steps."""
+    tab = mt.Table(18, 32, probe_step=probe_step, hash_seed=7, init_seed=11)
+    ref = oracle.Table(18, 32, probe_step=probe_step, hash_seed=7, init_seed=11, simulate=True)
+    run_steps(tab, ref, [W.merged_batch(s, per_table=2048) for s in range(4)])
+    st, sim = tab.stats(), ref.sim_stats()
+    assert st["live"] == sim["live"] and st["total_displacement"] == sim["total_displacement"]
+
+
+def test_jagged_bf16_rows_and_grads():
+    """Jagged user sequences, 4 ID features, dim 64 bf16 rows, fp32 Adam state, bf16 grads."""
+    batches = [W.jagged_batch(s, users=96, lengths_seed=s) for s in range(3)]
+    tab = mt.Table(18, 64, row_dtype="bf16")
+    ref = oracle.Table(18, 64, row_dtype=oracle.BF16)
+    run_steps(tab, ref, batches, row_dtype="bf16", grad_dtype="bf16")
+
+
+def test_bf16_rows_fp32_grads_and_fp32_rows_bf16_grads():
+    b = W.merged_batch(3, per_table=512)
+    tab = mt.Table(16, 32, row_dtype="bf16")
+    ref = oracle.Table(16, 32, row_dtype=oracle.BF16)
+    run_steps(tab, ref, [b, b], row_dtype="bf16", grad_dtype="f32")
+    tab = mt.Table(16, 32)
+    ref = oracle.Table(16, 32)
+    run_steps(tab, ref, [b, b], row_dtype="f32", grad_dtype="bf16")
+
+
+def test_large_keyspace_prefilled():
+    """Zipf(1.05) over a 2^32 key space, dim 128 fp32, table prefilled to load 0.7."""
+    log2 = 16
+    tab = mt.Table(log2, 128)
+    ref = oracle.Table(log2, 128, simulate=True)
+    pre = W.large_table_prefill_ids(int(0.7 * (1 << log2)))
+    res = tab.lookup(to_dev(pre), gather=False)
+    ref.lookup(pre, gather=False)
+    assert res.U == pre.size
+    batches = [W.large_table_batch(s, n=8192) for s in range(2)]
+    run_steps(tab, ref, batches)
+    st, sim = tab.stats(), ref.sim_stats()
+    assert st["live"] == sim["live"] == ref.live
+    assert st["total_displacement"] == sim["total_displacement"]
+
+
+def test_churn_with_erase_and_stats():
+    """Per step: IDs with 10% never seen before, then erase of random earlier IDs (tombstones)."""
+    log2 = 14
+    cs = W.ChurnStream(0, hot=1 << 12, n=1 << 11, erase=1 << 9)
+    tab = mt.Table(log2, 64)
+    ref = oracle.Table(log2, 64, simulate=True)
+    pre = cs.prefill_ids()
+    tab.lookup(to_dev(pre), gather=False)
+    ref.lookup(pre, gather=False)
+    for k in range(12):
+        b, er = cs.step(k)
+        res = tab.lookup(to_dev(b.ids))
+        r = ref.lookup(b.ids)
+        compare_lookup(res, r)
+        gd, gh, _ = grads_for(500 + k, b.n, 64, "f32")
+        tab.backward_adam(res, gd)
+        ref.backward_adam(gh)
+        compare_after_adam(tab, res, ref, r, "f32")
+        found = tab.erase(to_dev(er.astype(np.int64)))
+        want = ref.erase(er.astype(np.uint64))
+        assert np.array_equal(found.cpu().numpy().astype(bool), want)
+        st = tab.stats()
+        assert st["live"] == ref.live
+        assert st["rows_free"] == (1 << log2) - ref.live
+        keys, rows = tab.export()
+        assert np.array_equal(np.sort(keys.cpu().numpy().view(np.uint64)), np.sort(ref.live_keys()))
+        assert np.unique(rows.cpu().numpy()).size == rows.numel()
+    sim = ref.sim_stats()
+    st = tab.stats()
+    # placement under churn depends on insertion order: tolerances
+    assert abs(st["tombstones"] - sim["tombstones"]) <= 0.05 * max(sim["tombstones"], 1) + 16
+    h1 = st["probe_hist"] / max(1, st["live"])
+    h2 = sim["hist"] / max(1, sim["live"])
+    assert np.abs(h1 - h2).sum() <= 0.05
+    assert abs(st["total_displacement"] - sim["total_displacement"]) <= 0.05 * sim["total_displacement"] + 64
+    assert tab.error() == 0
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [0, 1, 31, 2047, 2048, 2049, 5000])
+def test_ragged_sizes(n):
+    rng = np.random.default_rng(n)
+    ids = rng.integers(0, max(1, n // 2), size=n)
+    tab = mt.Table(14, 16)
+    ref = oracle.Table(14, 16)
+    b = W.single_feature(ids)
+    run_steps(tab, ref, [b, b])
+
+
+def test_all_positions_one_id():
+    ids = np.full(10000, 123456789, np.int64)
+    tab = mt.Table(10, 8, row_dtype="bf16")
+    ref = oracle.Table(10, 8, row_dtype=oracle.BF16)
+    run_steps(tab, ref, [W.single_feature(ids)], row_dtype="bf16")
+
+
+def test_empty_segments_and_table_ids():
+    ids = np.arange(300, dtype=np.int64) % 37
+    offs = [0, 0, 100, 100, 250, 300]
+    tids = [5, 254, 0, 7, 254]
+    tab = mt.Table(12, 16)
+    ref = oracle.Table(12, 16)
+    res = tab.lookup(to_dev(ids), offs, tids)
+    r = ref.lookup(ids, offs, tids)
+    compare_lookup(res, r)
+    assert (r["unique"] >> np.uint64(56)).max() == 254
+
+
+def test_invalid_ids_latch_ekey():
+    ids = np.array([5, -1, 7, 1 << 56, 5, (1 << 56) - 1], np.int64)
+    tab = mt.Table(10, 16)
+    ref = oracle.Table(10, 16)
+    res = tab.lookup(to_dev(ids))
+    r = ref.lookup(ids)
+    compare_lookup(res, r)
+    assert res.inverse[1].item() == -1 and res.inverse[3].item() == -1
+    assert tab.error() == mt.MT_EKEY == ref.error
+    assert tab.error(clear=True) == mt.MT_EKEY and tab.error() == 0
+    g = torch.ones((ids.size, 16), device=dev())
+    tab.backward_adam(res, g)  # invalid positions contribute nothing
+    ref.backward_adam(np.ones((ids.size, 16), np.float32))
+    compare_after_adam(tab, res, ref, r, "f32")
+
+
+def test_eval_mode_misses_give_zeros():
+    tab = mt.Table(12, 16)
+    ref = oracle.Table(12, 16)
+    a = np.arange(50, dtype=np.int64)
+    compare_lookup(tab.lookup(to_dev(a)), ref.lookup(a))
+    b = np.arange(25, 100, dtype=np.int64)
+    res = tab.lookup(to_dev(b), insert_missing=False)
+    r = ref.lookup(b, insert_missing=False)
+    compare_lookup(res, r)
+    assert tab.stats()["live"] == 50
+
+
+def test_row_pool_exhaustion_latches_full():
+    tab = mt.Table(10, 16, num_rows=100)
+    ids = np.arange(500, dtype=np.int64)
+    res = tab.lookup(to_dev(ids))
+    torch.cuda.synchronize()
+    rows = res.unique_rows[:500].cpu().numpy()
+    assert (rows >= 0).sum() == 100 and np.unique(rows[rows >= 0]).size == 100
+    assert tab.error() == mt.MT_EFULL
+    st = tab.stats()
+    assert st["live"] == 100 and st["rows_free"] == 0
+    got = res.rows.cpu().numpy()
+    for i in np.nonzero(rows >= 0)[0][:20]:
+        assert np.array_equal(got[i], oracle.init_row(i, 0, oracle.default_init_scale(16), 16))
+    assert np.all(got[rows < 0] == 0)
+
+
+def test_probe_limit_latches_full_without_hang():
+    tab = mt.Table(6, 8, max_probes=2)
+    ids = np.arange(64, dtype=np.int64)
+    res = tab.lookup(to_dev(ids))
+    rows = res.unique_rows[:64].cpu().numpy()
+    assert tab.error() == mt.MT_EFULL
+    placed = rows >= 0
+    assert 0 < placed.sum() < 64
+    again = tab.lookup(to_dev(ids), insert_missing=False)
+    assert np.array_equal(again.unique_rows[:64].cpu().numpy() >= 0, placed)
+    assert np.array_equal(again.unique_rows[:64].cpu().numpy()[placed], rows[placed])
+
+
+def test_erase_duplicates_and_reinsert():
+    tab = mt.Table(10, 16, init_seed=3)
+    ref = oracle.Table(10, 16, init_seed=3)
+    ids = np.arange(40, dtype=np.int64)
+    res = tab.lookup(to_dev(ids))
+    r = ref.lookup(ids)
+    tab.backward_adam(res, torch.ones((40, 16), device=dev()))
+    ref.backward_adam(np.ones((40, 16), np.float32))
+    er = np.array([3, 3, 99, 5, 3], np.int64)
+    found = tab.erase(to_dev(er)).cpu().numpy()
+    assert found.tolist() == [1, 1, 0, 1, 1] == ref.erase(er.astype(np.uint64)).astype(int).tolist()
+    st = tab.stats()
+    assert st["live"] == 38 and st["tombstones"] == 2 and st["rows_free"] == 1024 - 38
+    res = tab.lookup(to_dev(np.array([3, 4], np.int64)))
+    r = ref.lookup(np.array([3, 4], np.int64))
+    compare_lookup(res, r)  # key 3 is back at its initial row; key 4 keeps its trained row
+    st = tab.stats()
+    assert st["live"] == 39 and st["tombstones"] <= 2
+
+
+def test_step_counter_and_lazy_rows():
+    tab = mt.Table(10, 8)
+    ref = oracle.Table(10, 8)
+    a = W.single_feature(np.array([1, 2], np.int64))
+    b = W.single_feature(np.array([1], np.int64))
+    run_steps(tab, ref, [a, b, b])
+    emb, _, _ = tab.read_rows(tab.lookup(to_dev(np.array([2], np.int64))).unique_rows[:1])
+    assert np.allclose(emb.cpu().numpy()[0], ref.get_row(2)[0])
+    assert tab.stats()["step"] == 3 == ref.step
+
+
+def test_integer_grads_sum_exactly():
+    """Integer-valued gradients: every partial sum is exact, so the sums match bit for bit."""
+    b = W.merged_batch(5, per_table=4096)
+    tab = mt.Table(18, 32)
+    ref = oracle.Table(18, 32)
+    res = tab.lookup(to_dev(b.ids), b.feat_offsets, b.table_ids)
+    r = ref.lookup(b.ids, b.feat_offsets, b.table_ids)
+    g = W.grads_small_int(9, b.n, 32)
+    gsum = tab.backward_adam(res, to_dev(g), want_gsum=True)
+    want = ref.backward_adam(g, want_gsum=True)
+    assert np.array_equal(gsum[:r["U"]].cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------------------
+# full size, in the launch configuration the benchmark times
+# ---------------------------------------------------------------------------
+
+def test_full_size_jagged_two_steps():
+    """2048 users, lognormal(5, 1) lengths capped at 3000, 4 features, M = 2^24, dim 64 bf16."""
+    tab = mt.Table(24, 64, row_dtype="bf16")
+    ref = oracle.Table(24, 64, row_dtype=oracle.BF16)
+    batches = [W.jagged_batch(s, lengths_seed=0) for s in range(2)]
+    run_steps(tab, ref, batches, row_dtype="bf16", grad_dtype="bf16")
+
+
+def test_full_size_merged():
+    """8 tables, 65536 IDs, M = 2^22, dim 32 fp32, 3 steps."""
+    tab = mt.Table(22, 32)
+    ref = oracle.Table(22, 32)
+    run_steps(tab, ref, [W.merged_batch(s) for s in range(3)])

@@ -1,0 +1,330 @@
+"""Merged dynamic embedding table on GB300: thin Python binding of ``libmt.so``.
+
+The binding only marshals arguments: it allocates device memory with torch,
+passes raw pointers and the current CUDA stream to the C ABI declared in
+``include/mt.h``, and wraps the outputs as torch tensors.  Every step of the
+lookup and backward path runs in the library's CUDA kernels.  There is no CPU
+fallback: without the built library every call raises.
+
+The path follows "MTGenRec: An Efficient Distributed Training System for
+Generative Recommendation Models in Meituan" (TL;DR and abstract: dynamic
+hash embedding tables with real-time insertion and deletion, automated table
+merging, two-stage ID deduplication; Theorem 1: probing h_t = (h0 + t*S) mod
+2^n with odd S) and "MTGR" section 5 (Embedding Management, Embedding Lookup).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import numpy as np
+
+__all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "KEY_EMPTY", "KEY_TOMBSTONE",
+           "ABI_FUNCTIONS"]
+
+MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA = 0, -1, -2, -3, -4, -5
+MT_F32, MT_BF16 = 0, 1
+KEY_EMPTY = (1 << 64) - 1
+KEY_TOMBSTONE = (1 << 64) - 2
+HIST_BINS = 64
+MAX_FEATURES = 256
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmt.so")
+
+
+class MTError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: status {code} ({_strerror(code)})")
+        self.code = code
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("log2_slots", ctypes.c_uint32), ("dim", ctypes.c_uint32), ("row_dtype", ctypes.c_uint32),
+                ("max_probes", ctypes.c_uint32), ("probe_step", ctypes.c_uint64), ("hash_seed", ctypes.c_uint64),
+                ("init_seed", ctypes.c_uint64), ("init_scale", ctypes.c_float), ("flags", ctypes.c_uint32),
+                ("num_rows", ctypes.c_int64)]
+
+
+class _Result(ctypes.Structure):
+    _fields_ = [("unique_keys", ctypes.c_void_p), ("inverse", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("unique_rows", ctypes.c_void_p), ("num_unique", ctypes.c_void_p)]
+
+
+class _Adam(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float), ("eps", ctypes.c_float)]
+
+
+class _Stats(ctypes.Structure):
+    _fields_ = [("live", ctypes.c_int64), ("tombstones", ctypes.c_int64), ("capacity", ctypes.c_int64),
+                ("num_rows", ctypes.c_int64), ("rows_free", ctypes.c_int64), ("step", ctypes.c_int64),
+                ("total_displacement", ctypes.c_int64), ("load_factor", ctypes.c_double),
+                ("probe_hist", ctypes.c_int64 * HIST_BINS), ("device_error", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_P, _I64, _SZ, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+# name -> (restype, argtypes); every entry point of include/mt.h
+ABI_FUNCTIONS = {
+    "mt_abi_version": (_I32, []),
+    "mt_strerror": (ctypes.c_char_p, [_I32]),
+    "mt_table_bytes": (_SZ, [_P]),
+    "mt_table_create": (_I32, [_P, _P, _SZ, _P, _P]),
+    "mt_table_destroy": (_I32, [_P]),
+    "mt_table_config": (_I32, [_P, _P]),
+    "mt_lookup_workspace_bytes": (_SZ, [_P, _I64]),
+    "mt_lookup": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "mt_backward_workspace_bytes": (_SZ, [_P, _I64]),
+    "mt_backward_adam": (_I32, [_P, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "mt_erase_workspace_bytes": (_SZ, [_I64]),
+    "mt_erase": (_I32, [_P, _P, _I64, _P, _P, _SZ, _P]),
+    "mt_stats": (_I32, [_P, _P, _P]),
+    "mt_export": (_I32, [_P, _P, _P, _I64, _P, _P]),
+    "mt_read_rows": (_I32, [_P, _P, _I64, _P, _P, _P, _P]),
+    "mt_get_error": (_I32, [_P, _P, _I32, _P]),
+    "mt_step": (_I64, [_P]),
+}
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libmt.so (built by ``build_lib.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing (run update_merged_table_gb300.build_lib.build())")
+    L = ctypes.CDLL(p)
+    for name, (res, args) in ABI_FUNCTIONS.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    if L.mt_abi_version() != 1:
+        raise RuntimeError("libmt.so ABI version mismatch")
+    if path is None:
+        _lib = L
+    return L
+
+
+def _strerror(code: int) -> str:
+    try:
+        return load_library().mt_strerror(code).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def _check(rc: int, what: str):
+    if rc != MT_OK:
+        raise MTError(rc, what)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclasses.dataclass
+class LookupResult:
+    """Device outputs of one lookup (capacity n; the first U entries are valid)."""
+    unique_keys: "object"   # int64 [n] (bit pattern of the uint64 merged keys)
+    inverse: "object"       # int32 [n]
+    counts: "object"        # int32 [n]
+    unique_rows: "object"   # int32 [n]
+    num_unique: "object"    # int64 [1]
+    rows: "object" = None   # [n, dim] row dtype, or None
+    n: int = 0
+
+    def as_struct(self) -> _Result:
+        return _Result(_ptr(self.unique_keys), _ptr(self.inverse), _ptr(self.counts), _ptr(self.unique_rows),
+                       _ptr(self.num_unique))
+
+    @property
+    def U(self) -> int:
+        return int(self.num_unique.item())
+
+
+class Table:
+    """A merged dynamic embedding table held in one device arena.
+
+    Args mirror ``mt_config``: ``log2_slots`` (M = 2^n slots), ``dim``,
+    ``row_dtype`` ("f32" or "bf16"), ``probe_step`` (odd S), seeds,
+    ``init_scale`` (0 = 1/sqrt(dim)), ``max_probes`` (0 = M), ``num_rows``
+    (0 = M).
+    """
+
+    def __init__(self, log2_slots: int, dim: int, row_dtype: str = "f32", probe_step: int = 1, hash_seed: int = 0,
+                 init_seed: int = 0, init_scale: float = 0.0, max_probes: int = 0, num_rows: int = 0,
+                 device=None, stream=None):
+        torch = _torch()
+        self.lib = load_library()
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        dt = {"f32": MT_F32, "bf16": MT_BF16}[row_dtype]
+        self.row_dtype = row_dtype
+        self.torch_row_dtype = torch.float32 if dt == MT_F32 else torch.bfloat16
+        self.cfg = _Config(log2_slots, dim, dt, max_probes, probe_step, hash_seed, init_seed, init_scale, 0,
+                           num_rows)
+        nbytes = self.lib.mt_table_bytes(ctypes.byref(self.cfg))
+        if nbytes == 0:
+            raise MTError(MT_EINVAL, "mt_table_bytes")
+        self.arena = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self.h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(self.lib.mt_table_create(ctypes.byref(self.cfg), self.arena.data_ptr(), nbytes, _stream(stream),
+                                            ctypes.byref(self.h)), "mt_table_create")
+        out = _Config()
+        _check(self.lib.mt_table_config(self.h, ctypes.byref(out)), "mt_table_config")
+        self.cfg = out
+        self.dim = dim
+        self.log2_slots = log2_slots
+        self._ws = {}
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h and h.value:
+            try:
+                self.lib.mt_table_destroy(h)
+            except Exception:  # pragma: no cover
+                pass
+            self.h = None
+
+    @property
+    def config(self) -> dict:
+        c = self.cfg
+        return {f: getattr(c, f) for f, _ in c._fields_}
+
+    def _workspace(self, kind: str, nbytes: int):
+        torch = _torch()
+        buf = self._ws.get(kind)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self._ws[kind] = buf
+        return buf
+
+    def new_result(self, n: int, gather: bool = True) -> LookupResult:
+        torch = _torch()
+        dev = self.device
+        return LookupResult(
+            unique_keys=torch.empty(max(n, 1), dtype=torch.int64, device=dev),
+            inverse=torch.empty(max(n, 1), dtype=torch.int32, device=dev),
+            counts=torch.empty(max(n, 1), dtype=torch.int32, device=dev),
+            unique_rows=torch.empty(max(n, 1), dtype=torch.int32, device=dev),
+            num_unique=torch.empty(1, dtype=torch.int64, device=dev),
+            rows=torch.empty((n, self.dim), dtype=self.torch_row_dtype, device=dev) if gather else None,
+            n=n)
+
+    def lookup(self, ids, feat_offsets=None, table_ids=None, insert_missing: bool = True, gather: bool = True,
+               result: LookupResult | None = None, stream=None) -> LookupResult:
+        """Encode, deduplicate, find/insert and gather one batch.
+
+        ids: int64 CUDA tensor [n].  feat_offsets: host sequence of F+1 int64
+        (None = one feature).  table_ids: host sequence of F uint8 (None = 0).
+        """
+        torch = _torch()
+        if ids.dtype != torch.int64 or not ids.is_cuda or not ids.is_contiguous():
+            raise TypeError("ids must be a contiguous int64 CUDA tensor")
+        n = ids.numel()
+        res = result if result is not None else self.new_result(n, gather)
+        if res.n != n:
+            raise ValueError("result capacity differs from the batch size")
+        F = 1
+        fo_p = ti_p = None
+        if feat_offsets is not None:
+            fo = np.ascontiguousarray(feat_offsets, dtype=np.int64)
+            F = fo.size - 1
+            fo_p = fo.ctypes.data_as(ctypes.c_void_p)
+        if table_ids is not None:
+            ti = np.ascontiguousarray(table_ids, dtype=np.uint8)
+            if feat_offsets is None and ti.size != 1:
+                raise ValueError("table_ids without feat_offsets must have one entry")
+            ti_p = ti.ctypes.data_as(ctypes.c_void_p)
+        wsb = self.lib.mt_lookup_workspace_bytes(self.h, n)
+        ws = self._workspace("lookup", wsb)
+        st = res.as_struct()
+        _check(self.lib.mt_lookup(self.h, ids.data_ptr() if n else None, n, fo_p, ti_p, F, int(bool(insert_missing)),
+                                  _ptr(res.rows) if (gather and n) else None, ctypes.byref(st), ws.data_ptr(),
+                                  ws.numel(), _stream(stream)), "mt_lookup")
+        return res
+
+    def backward_adam(self, res: LookupResult, grads, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
+                      eps: float = 1e-8, want_gsum: bool = False, stream=None):
+        """Per-unique gradient sum and one sparse Adam step; returns gsum [n, dim] fp32 if asked."""
+        torch = _torch()
+        n = res.n
+        if grads.shape != (n, self.dim) or not grads.is_cuda or not grads.is_contiguous():
+            raise ValueError("grads must be a contiguous CUDA tensor [n, dim]")
+        gd = {torch.float32: MT_F32, torch.bfloat16: MT_BF16}.get(grads.dtype)
+        if gd is None:
+            raise TypeError("grads must be float32 or bfloat16")
+        gsum = torch.empty((max(n, 1), self.dim), dtype=torch.float32, device=self.device) if want_gsum else None
+        hp = _Adam(lr, beta1, beta2, eps)
+        wsb = self.lib.mt_backward_workspace_bytes(self.h, n)
+        ws = self._workspace("backward", wsb)
+        st = res.as_struct()
+        _check(self.lib.mt_backward_adam(self.h, ctypes.byref(st), n, grads.data_ptr() if n else None, gd,
+                                         ctypes.byref(hp), _ptr(gsum), ws.data_ptr(), ws.numel(), _stream(stream)),
+               "mt_backward_adam")
+        return gsum
+
+    def erase(self, keys, want_found: bool = True, stream=None):
+        """Delete merged keys (int64 CUDA tensor holding the uint64 bit patterns)."""
+        torch = _torch()
+        if keys.dtype != torch.int64 or not keys.is_cuda or not keys.is_contiguous():
+            raise TypeError("keys must be a contiguous int64 CUDA tensor")
+        n = keys.numel()
+        found = torch.empty(max(n, 1), dtype=torch.uint8, device=self.device) if want_found else None
+        ws = self._workspace("erase", self.lib.mt_erase_workspace_bytes(n))
+        _check(self.lib.mt_erase(self.h, keys.data_ptr() if n else None, n, _ptr(found), ws.data_ptr(), ws.numel(),
+                                 _stream(stream)), "mt_erase")
+        return found[:n] if want_found else None
+
+    def stats(self, stream=None) -> dict:
+        s = _Stats()
+        _check(self.lib.mt_stats(self.h, ctypes.byref(s), _stream(stream)), "mt_stats")
+        out = {f: getattr(s, f) for f, _ in s._fields_ if f not in ("probe_hist", "reserved")}
+        out["probe_hist"] = np.array(list(s.probe_hist), dtype=np.int64)
+        return out
+
+    def export(self, stream=None):
+        """(keys int64 [live], rows int32 [live]) of every live key, in no particular order."""
+        torch = _torch()
+        cap = int(self.stats(stream)["live"])
+        keys = torch.empty(max(cap, 1), dtype=torch.int64, device=self.device)
+        rows = torch.empty(max(cap, 1), dtype=torch.int32, device=self.device)
+        cnt = ctypes.c_int64()
+        _check(self.lib.mt_export(self.h, keys.data_ptr(), rows.data_ptr(), cap, ctypes.byref(cnt), _stream(stream)),
+               "mt_export")
+        c = min(int(cnt.value), cap)
+        return keys[:c], rows[:c]
+
+    def read_rows(self, rows, stream=None):
+        """(emb, m, v) as fp32 [n, dim] for int32 CUDA row indices (-1 gives zeros)."""
+        torch = _torch()
+        n = rows.numel()
+        emb = torch.empty((max(n, 1), self.dim), dtype=torch.float32, device=self.device)
+        m = torch.empty_like(emb)
+        v = torch.empty_like(emb)
+        _check(self.lib.mt_read_rows(self.h, rows.data_ptr() if n else None, n, emb.data_ptr(), m.data_ptr(),
+                                     v.data_ptr(), _stream(stream)), "mt_read_rows")
+        return emb[:n], m[:n], v[:n]
+
+    def error(self, clear: bool = False, stream=None) -> int:
+        e = ctypes.c_int32()
+        _check(self.lib.mt_get_error(self.h, ctypes.byref(e), int(bool(clear)), _stream(stream)), "mt_get_error")
+        return int(e.value)
+
+    @property
+    def step(self) -> int:
+        return int(self.lib.mt_step(self.h))

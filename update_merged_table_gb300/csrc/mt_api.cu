@@ -1,0 +1,339 @@
+// The C ABI (include/mt.h): argument validation, arena and workspace
+// carving, kernel launches.  No device memory is allocated here.
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "mt_kernels.cuh"
+
+struct mt_table {
+  mt_config cfg;
+  mt::TableDev dev;
+  size_t arena_bytes;
+  long long step;  // host-side count of backward calls
+};
+
+namespace {
+
+using mt::align_up;
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Fill defaults and check a configuration; returns MT_OK or MT_EINVAL.
+int normalise(const mt_config* in, mt_config* out) {
+  if (in == nullptr) return MT_EINVAL;
+  mt_config c = *in;
+  if (c.log2_slots < 1 || c.log2_slots > 31) return MT_EINVAL;
+  if (c.flags != 0) return MT_EINVAL;
+  if (c.row_dtype != MT_F32 && c.row_dtype != MT_BF16) return MT_EINVAL;
+  const uint32_t vec = c.row_dtype == MT_F32 ? 4 : 8;
+  if (c.dim < 4 || c.dim > MT_MAX_DIM || c.dim % vec != 0) return MT_EINVAL;
+  const uint64_t M = 1ull << c.log2_slots;
+  c.probe_step &= (M - 1);
+  if ((c.probe_step & 1ull) == 0) return MT_EINVAL;  // Theorem 1: only an odd step covers the table
+  if (c.max_probes == 0 || c.max_probes > M) c.max_probes = (uint32_t)(M > 0xFFFFFFFFull ? 0xFFFFFFFFull : M);
+  if (!(c.init_scale >= 0.0f) || std::isinf(c.init_scale)) return MT_EINVAL;
+  if (c.init_scale == 0.0f) c.init_scale = (float)(1.0 / std::sqrt((double)c.dim));
+  if (c.num_rows == 0) c.num_rows = (int64_t)M;
+  if (c.num_rows < 1 || (uint64_t)c.num_rows > M || c.num_rows > 0x7FFFFFFF) return MT_EINVAL;
+  *out = c;
+  return MT_OK;
+}
+
+struct ArenaLayout {
+  size_t hdr, slots, stack, rows, total;
+  uint32_t rec_bytes, emb_bytes, mv_bytes;
+};
+
+ArenaLayout arena_layout(const mt_config& c) {
+  ArenaLayout L{};
+  const uint64_t M = 1ull << c.log2_slots;
+  L.emb_bytes = c.dim * (c.row_dtype == MT_F32 ? 4u : 2u);
+  L.mv_bytes = c.dim * 4u;
+  L.rec_bytes = L.emb_bytes + 2u * L.mv_bytes;  // each part is a multiple of 16 bytes
+  size_t off = 0;
+  L.hdr = off;
+  off = align_up(off + mt::kHeaderBytes, 256);
+  L.slots = off;
+  off = align_up(off + (size_t)M * sizeof(mt::Slot), 256);
+  L.stack = off;
+  off = align_up(off + (size_t)c.num_rows * 4, 256);
+  L.rows = off;
+  off = align_up(off + (size_t)c.num_rows * L.rec_bytes, 256);
+  L.total = off;
+  return L;
+}
+
+// S^-1 mod 2^64 by Newton's iteration x <- x(2 - Sx); exact for odd S.
+uint64_t inverse_mod_2_64(uint64_t S) {
+  uint64_t x = S;  // correct to 3 bits for odd S
+  for (int i = 0; i < 6; ++i) x *= 2 - S * x;
+  return x;
+}
+
+cudaStream_t as_stream(mt_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MT_OK : MT_ECUDA; }
+
+bool valid_result(const mt_lookup_result* r) {
+  return r != nullptr && r->unique_keys && r->inverse && r->counts && r->unique_rows && r->num_unique &&
+         aligned(r->unique_keys, 16) && aligned(r->inverse, 16) && aligned(r->counts, 16) &&
+         aligned(r->unique_rows, 16) && aligned(r->num_unique, 8);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mt_abi_version(void) { return MT_ABI_VERSION; }
+
+const char* mt_strerror(int code) {
+  switch (code) {
+    case MT_OK: return "ok";
+    case MT_EINVAL: return "invalid argument";
+    case MT_ENOSPACE: return "arena or workspace too small or misaligned";
+    case MT_EFULL: return "probe limit reached or row pool exhausted";
+    case MT_EKEY: return "ID outside [0, 2^56)";
+    case MT_ECUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+size_t mt_table_bytes(const mt_config* cfg) {
+  mt_config c;
+  if (normalise(cfg, &c) != MT_OK) return 0;
+  return arena_layout(c).total;
+}
+
+int mt_table_create(const mt_config* cfg, void* dev_mem, size_t bytes, mt_stream stream, mt_table** out) {
+  if (out == nullptr) return MT_EINVAL;
+  *out = nullptr;
+  mt_config c;
+  const int rc = normalise(cfg, &c);
+  if (rc != MT_OK) return rc;
+  const ArenaLayout L = arena_layout(c);
+  if (dev_mem == nullptr || bytes < L.total || !aligned(dev_mem, 256)) return MT_ENOSPACE;
+  mt_table* t = new (std::nothrow) mt_table();
+  if (t == nullptr) return MT_ECUDA;
+  t->cfg = c;
+  t->arena_bytes = L.total;
+  t->step = 0;
+  char* base = static_cast<char*>(dev_mem);
+  mt::TableDev& T = t->dev;
+  T.hdr = reinterpret_cast<mt::Header*>(base + L.hdr);
+  T.slots = reinterpret_cast<mt::Slot*>(base + L.slots);
+  T.free_stack = reinterpret_cast<int32_t*>(base + L.stack);
+  T.rows = base + L.rows;
+  const uint64_t M = 1ull << c.log2_slots;
+  T.mask = M - 1;
+  T.S = c.probe_step;
+  T.hash_seed = c.hash_seed;
+  T.init_seed = c.init_seed;
+  T.Sinv = inverse_mod_2_64(c.probe_step) & (M - 1);
+  T.log2_slots = c.log2_slots;
+  T.max_probes = c.max_probes;
+  T.dim = c.dim;
+  T.rec_bytes = L.rec_bytes;
+  T.emb_bytes = L.emb_bytes;
+  T.mv_bytes = L.mv_bytes;
+  T.row_dtype = (int)c.row_dtype;
+  T.init_scale = c.init_scale;
+  T.num_rows = c.num_rows;
+  const cudaError_t e = mt::launch_table_init(T, as_stream(stream));
+  if (e != cudaSuccess) {
+    delete t;
+    return MT_ECUDA;
+  }
+  *out = t;
+  return MT_OK;
+}
+
+int mt_table_destroy(mt_table* t) {
+  if (t == nullptr) return MT_EINVAL;
+  delete t;
+  return MT_OK;
+}
+
+int mt_table_config(const mt_table* t, mt_config* out) {
+  if (t == nullptr || out == nullptr) return MT_EINVAL;
+  *out = t->cfg;
+  return MT_OK;
+}
+
+size_t mt_lookup_workspace_bytes(const mt_table* t, int64_t n) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF) return 0;
+  return mt::lookup_ws_layout(n).total;
+}
+
+int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_offsets, const uint8_t* table_ids,
+              int F, int insert_missing, void* out_rows, const mt_lookup_result* res, void* ws, size_t ws_bytes,
+              mt_stream stream) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF || !valid_result(res)) return MT_EINVAL;
+  if (n > 0 && (ids == nullptr || !aligned(ids, 8))) return MT_EINVAL;
+  if (out_rows != nullptr && !aligned(out_rows, 16)) return MT_EINVAL;
+  if (feat_offsets == nullptr) F = 1;
+  if (F < 1 || F > MT_MAX_FEATURES) return MT_EINVAL;
+  mt::LookupParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.T = t->dev;
+  p.ids = reinterpret_cast<const long long*>(ids);
+  p.n = n;
+  p.F = F;
+  p.insert_missing = insert_missing ? 1 : 0;
+  if (feat_offsets == nullptr) {
+    p.feat_off[0] = 0;
+    p.feat_off[1] = n;
+  } else {
+    if (feat_offsets[0] != 0 || feat_offsets[F] != n) return MT_EINVAL;
+    for (int f = 0; f <= F; ++f) {
+      if (f > 0 && feat_offsets[f] < feat_offsets[f - 1]) return MT_EINVAL;
+      p.feat_off[f] = feat_offsets[f];
+    }
+  }
+  for (int f = 0; f < F; ++f) {
+    const uint8_t tid = table_ids ? table_ids[f] : 0;
+    if (tid == 0xFF) return MT_EINVAL;  // table id 255 holds the sentinels
+    p.table_ids[f] = tid;
+  }
+  const mt::LookupWsLayout L = mt::lookup_ws_layout(n);
+  if (n > 0 && (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256))) return MT_ENOSPACE;
+  char* w = static_cast<char*>(ws);
+  p.out_rows = out_rows;
+  p.unique_keys = reinterpret_cast<unsigned long long*>(res->unique_keys);
+  p.inverse = res->inverse;
+  p.counts = res->counts;
+  p.unique_rows = res->unique_rows;
+  p.num_unique = reinterpret_cast<long long*>(res->num_unique);
+  if (n > 0) {
+    p.scratch = reinterpret_cast<mt::ScratchSlot*>(w + L.scratch);
+    p.scratch_mask = L.scratch_slots - 1;
+    p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
+    p.tile_owners = reinterpret_cast<int32_t*>(w + L.tile_owners);
+    p.tile_offset = reinterpret_cast<int32_t*>(w + L.tile_offset);
+    p.lfirst = reinterpret_cast<uint32_t*>(w + L.lfirst);
+    p.lsslot = reinterpret_cast<uint32_t*>(w + L.lsslot);
+    p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
+    p.ntiles = L.ntiles;
+  }
+  return cuda_status(mt::launch_lookup(p, as_stream(stream)));
+}
+
+size_t mt_backward_workspace_bytes(const mt_table* t, int64_t n) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF) return 0;
+  return mt::backward_ws_layout(n, t->cfg.dim).total;
+}
+
+int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const void* grads, int grad_dtype,
+                     const mt_adam* hp, float* gsum_out, void* ws, size_t ws_bytes, mt_stream stream) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF || !valid_result(res) || hp == nullptr) return MT_EINVAL;
+  if (grad_dtype != MT_F32 && grad_dtype != MT_BF16) return MT_EINVAL;
+  if (n > 0 && (grads == nullptr || !aligned(grads, 16))) return MT_EINVAL;
+  if (gsum_out != nullptr && !aligned(gsum_out, 16)) return MT_EINVAL;
+  if (!(hp->lr >= 0.0f) || !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) ||
+      !(hp->eps > 0.0f))
+    return MT_EINVAL;
+  const mt::BackwardWsLayout L = mt::backward_ws_layout(n, t->cfg.dim);
+  if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return MT_ENOSPACE;
+  char* w = static_cast<char*>(ws);
+  mt::BackwardParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.T = t->dev;
+  p.n = n;
+  p.inverse = res->inverse;
+  p.counts = res->counts;
+  p.unique_rows = res->unique_rows;
+  p.num_unique = reinterpret_cast<const long long*>(res->num_unique);
+  p.grads = grads;
+  p.grad_dtype = grad_dtype;
+  p.lr = hp->lr;
+  p.beta1 = hp->beta1;
+  p.beta2 = hp->beta2;
+  p.eps = hp->eps;
+  p.one_minus_b1 = (float)(1.0 - (double)hp->beta1);
+  p.one_minus_b2 = (float)(1.0 - (double)hp->beta2);
+  p.gsum_out = gsum_out;
+  p.bsum = reinterpret_cast<int32_t*>(w + L.bsum);
+  p.boff = reinterpret_cast<int32_t*>(w + L.boff);
+  p.cursor = reinterpret_cast<int32_t*>(w + L.cursor);
+  p.chunk_off = reinterpret_cast<int32_t*>(w + L.chunk_off);
+  p.heavy_idx = reinterpret_cast<int32_t*>(w + L.heavy_idx);
+  p.chunk_u = reinterpret_cast<int32_t*>(w + L.chunk_u);
+  p.pos_sorted = reinterpret_cast<int32_t*>(w + L.pos_sorted);
+  p.acc64 = reinterpret_cast<double*>(w + L.acc64);
+  p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
+  p.nblk = L.nblk;
+  p.ntiles = L.ntiles;
+  const int rc = cuda_status(mt::launch_backward(p, as_stream(stream)));
+  if (rc == MT_OK) t->step += 1;
+  return rc;
+}
+
+size_t mt_erase_workspace_bytes(int64_t n) {
+  if (n < 0) return 0;
+  return align_up((size_t)(n > 0 ? n : 1) * 4, 256);
+}
+
+int mt_erase(mt_table* t, const uint64_t* keys, int64_t n, uint8_t* found, void* ws, size_t ws_bytes,
+             mt_stream stream) {
+  if (t == nullptr || n < 0) return MT_EINVAL;
+  if (n > 0 && (keys == nullptr || !aligned(keys, 8))) return MT_EINVAL;
+  if (n > 0 && (ws == nullptr || ws_bytes < mt_erase_workspace_bytes(n) || !aligned(ws, 256))) return MT_ENOSPACE;
+  return cuda_status(mt::launch_erase(t->dev, reinterpret_cast<const unsigned long long*>(keys), n, found,
+                                      static_cast<int32_t*>(ws), as_stream(stream)));
+}
+
+int mt_stats(mt_table* t, mt_stats_out* out, mt_stream stream) {
+  if (t == nullptr || out == nullptr) return MT_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  if (mt::launch_stats(t->dev, s) != cudaSuccess) return MT_ECUDA;
+  mt::Header h;
+  if (cudaMemcpyAsync(&h, t->dev.hdr, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MT_ECUDA;
+  std::memset(out, 0, sizeof(*out));
+  out->live = (int64_t)h.live;
+  out->tombstones = (int64_t)h.tombs;
+  out->capacity = (int64_t)(t->dev.mask + 1);
+  out->num_rows = t->cfg.num_rows;
+  out->rows_free = h.free_top;
+  out->step = h.step;
+  out->total_displacement = (int64_t)h.disp;
+  out->load_factor = (double)h.live / (double)(t->dev.mask + 1);
+  for (int b = 0; b < MT_HIST_BINS; ++b) out->probe_hist[b] = (int64_t)h.hist[b];
+  out->device_error = h.error;
+  return MT_OK;
+}
+
+int mt_export(mt_table* t, uint64_t* keys, int32_t* rows, int64_t capacity, int64_t* count, mt_stream stream) {
+  if (t == nullptr || count == nullptr || capacity < 0) return MT_EINVAL;
+  if (capacity > 0 && (keys == nullptr || rows == nullptr)) return MT_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  if (mt::launch_export(t->dev, reinterpret_cast<unsigned long long*>(keys), rows, capacity, s) != cudaSuccess)
+    return MT_ECUDA;
+  long long c = 0;
+  if (cudaMemcpyAsync(&c, &t->dev.hdr->export_count, sizeof(c), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MT_ECUDA;
+  *count = c;
+  return MT_OK;
+}
+
+int mt_read_rows(const mt_table* t, const int32_t* rows, int64_t n, float* emb, float* m, float* v,
+                 mt_stream stream) {
+  if (t == nullptr || n < 0 || (n > 0 && rows == nullptr)) return MT_EINVAL;
+  return cuda_status(mt::launch_read_rows(t->dev, rows, n, emb, m, v, as_stream(stream)));
+}
+
+int mt_get_error(mt_table* t, int32_t* device_error, int clear, mt_stream stream) {
+  if (t == nullptr || device_error == nullptr) return MT_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  int32_t e = 0;
+  if (cudaMemcpyAsync(&e, &t->dev.hdr->error, sizeof(e), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MT_ECUDA;
+  if (clear && cudaMemsetAsync(&t->dev.hdr->error, 0, sizeof(int32_t), s) != cudaSuccess) return MT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MT_ECUDA;
+  *device_error = e;
+  return MT_OK;
+}
+
+int64_t mt_step(const mt_table* t) { return t == nullptr ? -1 : t->step; }
+
+}  // extern "C"

@@ -1,0 +1,227 @@
+// Internal declarations of the CUDA path of the merged dynamic embedding table.
+//
+// Layout of the table arena (all in one caller-owned device allocation):
+//   [Header 1 KiB][slots: M x Slot (16 B)][free stack: R x int32][rows: R x record]
+// A row record is [emb: d x row dtype][m: d x fp32][v: d x fp32], each part a
+// multiple of 16 bytes, so every part of a row is reached with 16-byte vector
+// accesses.  A slot {key, row, meta} maps a merged key to its row and keeps
+// the table step at which it was inserted ("keys map to embedding vectors and
+// metadata", MTGR section 5, Embedding Management); the key store is separate
+// from the rows, so it can be rebuilt without moving any embedding.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mt.h"
+
+namespace mt {
+
+constexpr unsigned long long kEmpty = MT_KEY_EMPTY;
+constexpr unsigned long long kTomb = MT_KEY_TOMBSTONE;
+constexpr unsigned long long kIdLimit = 1ull << 56;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct __align__(16) Slot {
+  unsigned long long key;
+  int32_t row;
+  uint32_t meta;  // table step at insertion
+};
+static_assert(sizeof(Slot) == 16, "slot is 16 bytes");
+
+// Device header at the start of the arena.
+struct __align__(256) Header {
+  int32_t error;           // first latched device error (0 = none)
+  int32_t pad0;
+  long long free_top;      // rows on the free stack
+  long long step;          // Adam steps taken
+  long long export_count;  // scratch for mt_export
+  long long pad1[4];
+  // mt_stats accumulators
+  unsigned long long live, tombs, disp;
+  unsigned long long hist[MT_HIST_BINS];
+};
+constexpr size_t kHeaderBytes = 1024;
+static_assert(sizeof(Header) <= kHeaderBytes, "header fits");
+
+// Everything a kernel needs to reach the table (passed by value).
+struct TableDev {
+  Header* hdr;
+  Slot* slots;
+  int32_t* free_stack;
+  char* rows;
+  unsigned long long mask;       // M - 1
+  unsigned long long S;          // odd probe step, reduced mod M
+  unsigned long long hash_seed;
+  unsigned long long init_seed;
+  unsigned long long Sinv;       // S^-1 mod M
+  uint32_t log2_slots;
+  uint32_t max_probes;
+  uint32_t dim;
+  uint32_t rec_bytes;            // bytes per row record
+  uint32_t emb_bytes;            // d x row element bytes
+  uint32_t mv_bytes;             // d x 4
+  int row_dtype;
+  float init_scale;
+  long long num_rows;
+};
+
+// ---- small device helpers -------------------------------------------------
+
+// splitmix64 output mixer (Steele, Lea, Flood, OOPSLA 2014).
+__device__ __forceinline__ unsigned long long mix64(unsigned long long z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Home slot h0 of a key in the table: the top n bits of the mixed key.
+__device__ __forceinline__ unsigned long long home_slot(const TableDev& T, unsigned long long key) {
+  return mix64(key ^ T.hash_seed) >> (64 - T.log2_slots);
+}
+
+__device__ __forceinline__ void latch_error(Header* h, int code) {
+  if (atomicCAS(&h->error, 0, code) == 0) { /* first error wins */ }
+}
+
+__device__ __forceinline__ unsigned long long load_key_relaxed(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ char* row_ptr(const TableDev& T, int32_t row) {
+  return T.rows + (size_t)row * T.rec_bytes;
+}
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 64x64->128 multiplies; the key is bumped by the golden-ratio and sqrt(3)-1
+// Weyl increments between rounds.
+__device__ __forceinline__ void philox4x64_10(unsigned long long c0, unsigned long long c1, unsigned long long c2,
+                                              unsigned long long c3, unsigned long long k0, unsigned long long k1,
+                                              unsigned long long out[4]) {
+  const unsigned long long M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    unsigned long long hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+    unsigned long long hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+    unsigned long long n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    k0 += 0x9E3779B97F4A7C15ull;
+    k1 += 0xBB67AE8584CAA73Bull;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+// Initial values of columns 4g .. 4g+3 of the row of `key`: the top 24 bits
+// q of each Philox word give (2q - 2^24) / 2^24 exactly; one fp32 multiply by
+// the scale is the only rounding.
+__device__ __forceinline__ void init_quad(const TableDev& T, unsigned long long key, uint32_t g, float v[4]) {
+  unsigned long long w[4];
+  philox4x64_10((unsigned long long)g, 0ull, 0ull, 0ull, key, T.init_seed, w);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    int q = (int)(w[k] >> 40);
+    float unit = (float)(2 * q - (1 << 24)) * (1.0f / 16777216.0f);
+    v[k] = __fmul_rn(unit, T.init_scale);
+  }
+}
+
+// Write a fresh row: emb = init(key), m = v = 0.  Cooperatively by `nl`
+// lanes (lane index `l` in [0, nl)), 16-byte stores.
+__device__ __forceinline__ void init_row_coop(const TableDev& T, int32_t row, unsigned long long key, int l, int nl) {
+  char* rec = row_ptr(T, row);
+  const uint32_t d = T.dim;
+  if (T.row_dtype == MT_F32) {
+    float4* e = reinterpret_cast<float4*>(rec);
+    for (uint32_t g = l; g < d / 4; g += nl) {
+      float v[4];
+      init_quad(T, key, g, v);
+      e[g] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+  } else {
+    uint4* e = reinterpret_cast<uint4*>(rec);
+    for (uint32_t g8 = l; g8 < d / 8; g8 += nl) {
+      float a[4], b[4];
+      init_quad(T, key, 2 * g8, a);
+      init_quad(T, key, 2 * g8 + 1, b);
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(a[0], a[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(a[2], a[3]);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(b[0], b[1]);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(b[2], b[3]);
+      uint4 u;
+      u.x = *reinterpret_cast<uint32_t*>(&p0);
+      u.y = *reinterpret_cast<uint32_t*>(&p1);
+      u.z = *reinterpret_cast<uint32_t*>(&p2);
+      u.w = *reinterpret_cast<uint32_t*>(&p3);
+      e[g8] = u;
+    }
+  }
+  float4* mv = reinterpret_cast<float4*>(rec + T.emb_bytes);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t g = l; g < 2 * d / 4; g += nl) mv[g] = z;
+}
+
+// Pop `k` rows from the free stack for the lanes in `mask` (warp-aggregated).
+// Returns this lane's row, or -1 when the pool ran out.
+__device__ __forceinline__ int32_t pop_row_warp(const TableDev& T, unsigned mask) {
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(mask) - 1;
+  const int k = __popc(mask);
+  const int rank = __popc(mask & ((1u << lane) - 1u));
+  long long old = 0;
+  if (lane == leader) old = atomicAdd((unsigned long long*)&T.hdr->free_top, (unsigned long long)(-(long long)k));
+  old = __shfl_sync(mask, old, leader);
+  const long long avail = old < 0 ? 0 : (old < k ? old : k);
+  if (lane == leader && avail < k) atomicAdd((unsigned long long*)&T.hdr->free_top, (unsigned long long)(k - avail));
+  if (rank < avail) return T.free_stack[old - 1 - rank];
+  return -1;
+}
+
+// Push rows back onto the free stack (warp-aggregated; lanes in `mask`).
+__device__ __forceinline__ void push_row_warp(const TableDev& T, unsigned mask, int32_t row) {
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(mask) - 1;
+  const int k = __popc(mask);
+  const int rank = __popc(mask & ((1u << lane) - 1u));
+  long long old = 0;
+  if (lane == leader) old = (long long)atomicAdd((unsigned long long*)&T.hdr->free_top, (unsigned long long)k);
+  old = __shfl_sync(mask, old, leader);
+  T.free_stack[old + rank] = row;
+}
+
+// Find `key` along its probe sequence h_t = (h0 + t*S) mod M (MTGenRec,
+// Theorem 1).  Returns the slot index, or -1 when an EMPTY slot or the probe
+// limit ends the chain first.  *t_end receives the probe index where the
+// search stopped and *t_tomb the first tombstone's probe index (or -1).
+__device__ __forceinline__ long long find_slot(const TableDev& T, unsigned long long key, long long* t_end,
+                                               long long* t_tomb) {
+  unsigned long long s = home_slot(T, key);
+  long long first_tomb = -1;
+  for (uint32_t t = 0; t < T.max_probes; ++t) {
+    const unsigned long long k = load_key_relaxed(&T.slots[s].key);
+    if (k == key) {
+      *t_end = t;
+      *t_tomb = first_tomb;
+      return (long long)s;
+    }
+    if (k == kEmpty) {
+      *t_end = t;
+      *t_tomb = first_tomb;
+      return -1;
+    }
+    if (k == kTomb && first_tomb < 0) first_tomb = t;
+    s = (s + T.S) & T.mask;
+  }
+  *t_end = T.max_probes;
+  *t_tomb = first_tomb;
+  return -1;
+}
+
+// ---- host-side launchers (defined in the kernel files) --------------------
+
+struct LookupWs;
+struct BackwardWs;
+
+}  // namespace mt

@@ -1,0 +1,117 @@
+// Kernel parameter blocks and host-side launchers shared by the kernel files
+// and the C ABI (mt_api.cu).
+#pragma once
+
+#include "mt_internal.cuh"
+
+namespace mt {
+
+// ---- forward ----------------------------------------------------------------
+
+constexpr int kTile = 2048;              // positions per lookup tile (one CTA)
+constexpr int kThreads = 256;            // threads per lookup CTA
+constexpr int kPPT = kTile / kThreads;   // positions per thread
+constexpr int kHS = 2 * kTile;           // shared-memory hash slots of stage 1
+constexpr uint16_t kNoIdx = 0xFFFF;
+
+// Stage-2 global scratch hash slot: key -> (first position, unique index).
+struct __align__(16) ScratchSlot {
+  unsigned long long key;
+  uint32_t minpos;
+  int32_t uidx;
+};
+
+struct LookupParams {
+  TableDev T;
+  const long long* ids;
+  long long n;
+  int F;
+  int insert_missing;
+  long long feat_off[MT_MAX_FEATURES + 1];
+  unsigned char table_ids[MT_MAX_FEATURES];
+  void* out_rows;
+  unsigned long long* unique_keys;
+  int32_t* inverse;
+  int32_t* counts;
+  int32_t* unique_rows;
+  long long* num_unique;
+  // workspace
+  ScratchSlot* scratch;
+  unsigned long long scratch_mask;
+  int32_t* tile_L;        // [ntiles] local uniques per tile
+  int32_t* tile_owners;   // [ntiles] global-first keys per tile
+  int32_t* tile_offset;   // [ntiles + 1] exclusive scan of tile_owners
+  uint32_t* lfirst;       // [ntiles * kTile] first global position of local unique l
+  uint32_t* lsslot;       // [ntiles * kTile] its scratch slot
+  uint16_t* lidx;         // [ntiles * kTile] local unique index of each position
+  int ntiles;
+};
+
+struct LookupWsLayout {
+  size_t scratch, tile_L, tile_owners, tile_offset, lfirst, lsslot, lidx, total;
+  unsigned long long scratch_slots;
+  int ntiles;
+};
+LookupWsLayout lookup_ws_layout(long long n);
+cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s);
+
+// ---- backward ---------------------------------------------------------------
+
+constexpr int kChunk = 32;          // positions per reduction chunk
+constexpr int kScanTile = 2048;     // uniques per scan block
+constexpr int kScanThreads = 256;
+
+struct BackwardParams {
+  TableDev T;
+  long long n;
+  const int32_t* inverse;
+  const int32_t* counts;
+  const int32_t* unique_rows;
+  const long long* num_unique;
+  const void* grads;
+  int grad_dtype;
+  float lr, beta1, beta2, eps;
+  float one_minus_b1, one_minus_b2;
+  float* gsum_out;
+  // workspace
+  int32_t* bsum;        // [nblk * 3] per scan block: sum of counts, chunks, heavy
+  int32_t* boff;        // [(nblk + 1) * 3] exclusive offsets (+ totals)
+  int32_t* cursor;      // [n] segment start, advanced to the segment end by the fill
+  int32_t* chunk_off;   // [n] first chunk of each unique
+  int32_t* heavy_idx;   // [n] index among multi-chunk uniques, or -1
+  int32_t* chunk_u;     // [n] unique of each chunk
+  int32_t* pos_sorted;  // [n] positions grouped by unique
+  double* acc64;        // [heavy_cap * d] cross-chunk sums of multi-chunk uniques
+  int32_t* arrive;      // [heavy_cap] chunks finished per multi-chunk unique
+  int nblk;
+  int ntiles;
+};
+
+struct BackwardWsLayout {
+  size_t bsum, boff, cursor, chunk_off, heavy_idx, chunk_u, pos_sorted, acc64, arrive, total;
+  long long heavy_cap;
+  int nblk, ntiles;
+};
+BackwardWsLayout backward_ws_layout(long long n, uint32_t dim);
+cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s);
+
+// ---- table maintenance --------------------------------------------------------
+
+cudaError_t launch_table_init(const TableDev& T, cudaStream_t s);
+cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long long n, unsigned char* found,
+                         int32_t* ws_slot, cudaStream_t s);
+cudaError_t launch_stats(const TableDev& T, cudaStream_t s);
+cudaError_t launch_export(const TableDev& T, unsigned long long* keys, int32_t* rows, long long capacity,
+                          cudaStream_t s);
+cudaError_t launch_read_rows(const TableDev& T, const int32_t* rows, long long n, float* emb, float* m, float* v,
+                             cudaStream_t s);
+
+// Single-block exclusive scan of `count` int32 triples/ints, used for the
+// tile-offset and scan-block-offset passes.  out[count] receives the total.
+// With total_to != nullptr the total is also stored there as int64.
+cudaError_t launch_scan_small(const int32_t* in, int32_t* out, int count, int width, long long* total_to,
+                              cudaStream_t s);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace mt

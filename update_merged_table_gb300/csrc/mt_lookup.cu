@@ -1,0 +1,466 @@
+// Forward path of the merged dynamic embedding table: merged-key encoding,
+// two-stage ID deduplication, find/insert with odd-step probing, and the
+// embedding gather.
+//
+// Pages: "MTGenRec" TL;DR and abstract (hash-based dynamic embedding table,
+// automated table merging, two-stage ID deduplication for faster lookup,
+// real-time insertions); Theorem 1 (probe sequence h_t = (h0 + t*S) mod 2^n
+// with S odd covers the table); "MTGR" section 5, Embedding Lookup (IDs stay
+// unique).
+//
+// Kernels, in launch order (one CTA per tile of kTile consecutive positions):
+//  k_dedup_claim     encode keys; stage 1: dedup inside the tile with a
+//                    shared-memory hash (warp match first, so a hot ID costs
+//                    one shared atomic per warp); stage 2: each tile-local
+//                    unique claims its key in a global scratch hash and
+//                    lowers the key's first position there (atomicMin).
+//  k_count_owners    a tile owns a key when its first position is the key's
+//                    global first position; count owners per tile.
+//  k_scan_small      tile offsets = exclusive scan of owner counts; U.
+//  k_assign_resolve  owners take unique indices in first-occurrence order,
+//                    publish them in the scratch hash, find or insert their
+//                    key in the table (odd-step probing, tombstone reuse,
+//                    warp-aggregated row pops) and initialise fresh rows.
+//  k_expand_gather   per position: inverse index; per tile-local unique:
+//                    counts; then the 16-byte vectorised row gather.
+#include "mt_kernels.cuh"
+
+namespace mt {
+
+namespace {
+
+__device__ __forceinline__ uint32_t stage1_hash(unsigned long long key) {
+  return (uint32_t)(mix64(key ^ 0x2545F4914F6CDD1Dull) >> 40) & (uint32_t)(kHS - 1);
+}
+
+__device__ __forceinline__ unsigned long long stage2_hash(unsigned long long key) {
+  return mix64(key ^ 0x9FB21C651E98DF25ull);
+}
+
+// Exclusive scan of one int per thread over a block of NT threads; *total
+// receives the block sum.  Contains __syncthreads (all threads must call).
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NT / 32 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < NT / 32) s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int r = (warp ? s_warp[warp - 1] : 0) + x - v;
+  *total = s_warp[NT / 32 - 1];
+  __syncthreads();
+  return r;
+}
+
+template <int NT>
+__device__ __forceinline__ int block_sum(int v, int* s_warp) {
+  int t;
+  block_exclusive_scan<NT>(v, s_warp, &t);
+  return t;
+}
+
+constexpr size_t kSmemA = kHS * 8 + kHS * 4 + kTile * 4 + kTile * 2 + (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
+
+__global__ void __launch_bounds__(kThreads) k_dedup_claim(const LookupParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHS] stage-1 hash keys
+  uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHS);              // [kHS] first local position, then local index
+  uint32_t* s_item = s_min + kHS;                                          // [kTile] (hash slot << 16) | first position of local unique l
+  uint16_t* s_pslot = reinterpret_cast<uint16_t*>(s_item + kTile);         // [kTile] hash slot of each position
+  long long* s_off = reinterpret_cast<long long*>(s_pslot + kTile);        // [F + 1]
+  unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
+  __shared__ int s_warp[kThreads / 32];
+
+  const int tile = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const long long base = (long long)tile * kTile;
+  const int cnt = (int)min((long long)kTile, p.n - base);
+
+  for (int i = tid; i < kHS; i += kThreads) {
+    s_key[i] = kEmpty;
+    s_min[i] = 0xFFFFFFFFu;
+  }
+  for (int i = tid; i <= p.F; i += kThreads) s_off[i] = p.feat_off[i];
+  for (int i = tid; i < p.F; i += kThreads) s_tid[i] = p.table_ids[i];
+  __syncthreads();
+
+  // ---- encode + stage 1 (tile-local dedup) ----
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int lp = k * kThreads + tid;  // a warp covers 32 consecutive positions
+    const bool in = lp < cnt;
+    unsigned long long key = kEmpty;
+    bool valid = false;
+    if (in) {
+      const long long i = base + lp;
+      const long long id = p.ids[i];
+      int lo = 0, hi = p.F;  // off[lo] <= i < off[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= i) lo = mid; else hi = mid;
+      }
+      valid = id >= 0 && (unsigned long long)id < kIdLimit;
+      key = ((unsigned long long)s_tid[lo] << 56) | (unsigned long long)id;
+      bad |= !valid;
+    }
+    const unsigned act = __ballot_sync(kFull, valid);
+    if (valid) {
+      const unsigned grp = __match_any_sync(act, key);
+      const int leader = __ffs(grp) - 1;
+      uint32_t slot = 0;
+      if (lane == leader) {  // the leader holds the group's smallest position
+        uint32_t h = stage1_hash(key);
+        for (int probe = 0; probe < kHS; ++probe) {
+          const unsigned long long prev = atomicCAS(&s_key[h], kEmpty, key);
+          if (prev == kEmpty || prev == key) break;
+          h = (h + 1) & (uint32_t)(kHS - 1);
+        }
+        slot = h;
+        atomicMin(&s_min[slot], (uint32_t)lp);
+      }
+      slot = __shfl_sync(grp, slot, leader);
+      s_pslot[lp] = (uint16_t)slot;
+    } else if (in) {
+      s_pslot[lp] = kNoIdx;
+    }
+  }
+  if (bad) latch_error(p.T.hdr, MT_EKEY);
+  __syncthreads();
+
+  // ---- local uniques in first-occurrence order (contiguous positions per thread) ----
+  uint32_t flags = 0;
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int lp = tid * kPPT + k;
+    if (lp < cnt) {
+      const uint16_t sl = s_pslot[lp];
+      if (sl != kNoIdx && s_min[sl] == (uint32_t)lp) {
+        flags |= 1u << k;
+        ++c;
+      }
+    }
+  }
+  int L;
+  int l = block_exclusive_scan<kThreads>(c, s_warp, &L);  // every s_min read above precedes its barriers
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    if (flags & (1u << k)) {
+      const int lp = tid * kPPT + k;
+      const uint16_t sl = s_pslot[lp];
+      s_min[sl] = (uint32_t)l;
+      s_item[l] = ((uint32_t)sl << 16) | (uint32_t)lp;
+      ++l;
+    }
+  }
+  __syncthreads();
+
+  uint16_t* lidx = p.lidx + base;
+  for (int lp = tid; lp < cnt; lp += kThreads) {
+    const uint16_t sl = s_pslot[lp];
+    lidx[lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
+  }
+
+  // ---- stage 2: claim every local unique in the global scratch hash ----
+  const size_t lb = (size_t)tile * kTile;
+  for (int li = tid; li < L; li += kThreads) {
+    const uint32_t it = s_item[li];
+    const unsigned long long key = s_key[it >> 16];
+    const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
+    unsigned long long h = stage2_hash(key) & p.scratch_mask;
+    for (unsigned long long probe = 0; probe <= p.scratch_mask; ++probe) {
+      unsigned long long cur = load_key_relaxed(&p.scratch[h].key);
+      if (cur == kEmpty) {
+        cur = atomicCAS(&p.scratch[h].key, kEmpty, key);
+        if (cur == kEmpty) cur = key;
+      }
+      if (cur == key) break;
+      h = (h + 1) & p.scratch_mask;
+    }
+    atomicMin(&p.scratch[h].minpos, gpos);
+    p.lfirst[lb + li] = gpos;
+    p.lsslot[lb + li] = (uint32_t)h;
+  }
+  if (tid == 0) p.tile_L[tile] = L;
+}
+
+__global__ void __launch_bounds__(kThreads) k_count_owners(const LookupParams p) {
+  __shared__ int s_warp[kThreads / 32];
+  const int tile = blockIdx.x;
+  const int L = p.tile_L[tile];
+  const size_t lb = (size_t)tile * kTile;
+  int c = 0;
+  for (int l = threadIdx.x; l < L; l += kThreads) c += p.scratch[p.lsslot[lb + l]].minpos == p.lfirst[lb + l];
+  const int tot = block_sum<kThreads>(c, s_warp);
+  if (threadIdx.x == 0) p.tile_owners[tile] = tot;
+}
+
+__global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams p) {
+  __shared__ int s_warp[kThreads / 32];
+  __shared__ uint32_t s_oslot[kTile];  // scratch slot of owner j
+  __shared__ int32_t s_orow[kTile];    // table row of owner j
+  __shared__ int32_t s_new[kTile];     // owners that inserted a fresh row
+  __shared__ int s_nnew;
+
+  const int tile = blockIdx.x, tid = threadIdx.x;
+  const int L = p.tile_L[tile];
+  const size_t lb = (size_t)tile * kTile;
+  const int off = p.tile_offset[tile];
+  if (tid == 0) s_nnew = 0;
+
+  // owners, in local (first-occurrence) order
+  uint32_t flags = 0;
+  uint32_t sl[kPPT];
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int l = tid * kPPT + k;
+    sl[k] = 0;
+    if (l < L) {
+      sl[k] = p.lsslot[lb + l];
+      if (p.scratch[sl[k]].minpos == p.lfirst[lb + l]) {
+        flags |= 1u << k;
+        ++c;
+      }
+    }
+  }
+  int O;
+  int j = block_exclusive_scan<kThreads>(c, s_warp, &O);
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    if (flags & (1u << k)) {
+      const int u = off + j;
+      ScratchSlot* ss = &p.scratch[sl[k]];
+      ss->uidx = u;
+      p.unique_keys[u] = ss->key;
+      p.counts[u] = 0;
+      s_oslot[j] = sl[k];
+      ++j;
+    }
+  }
+  __syncthreads();
+
+  // find or insert each owned key in the table
+  const uint32_t step = (uint32_t)p.T.hdr->step;
+  for (int j0 = 0; j0 < O; j0 += kThreads) {
+    const int jj = j0 + tid;
+    const bool act = jj < O;
+    int32_t row = -1;
+    bool claimed = false;
+    unsigned long long cs = 0;
+    if (act) {
+      const unsigned long long key = p.scratch[s_oslot[jj]].key;
+      long long t_end, t_tomb;
+      const long long s = find_slot(p.T, key, &t_end, &t_tomb);
+      if (s >= 0) {
+        row = p.T.slots[s].row;
+      } else if (p.insert_missing) {
+        // the key is absent and no other thread inserts it (it is unique in
+        // the batch): take the first tombstone of its chain, else the EMPTY
+        // slot that ended the chain, else the next free slot after them
+        long long t = t_tomb >= 0 ? t_tomb : t_end;
+        unsigned long long slot = (home_slot(p.T, key) + (unsigned long long)t * p.T.S) & p.T.mask;
+        for (; t < (long long)p.T.max_probes; ++t) {
+          const unsigned long long k = load_key_relaxed(&p.T.slots[slot].key);
+          if ((k == kEmpty || k == kTomb) && atomicCAS(&p.T.slots[slot].key, k, key) == k) {
+            claimed = true;
+            cs = slot;
+            break;
+          }
+          slot = (slot + p.T.S) & p.T.mask;
+        }
+        if (!claimed) latch_error(p.T.hdr, MT_EFULL);
+      }
+    }
+    const unsigned need = __ballot_sync(kFull, claimed);
+    if (claimed) {
+      row = pop_row_warp(p.T, need);
+      if (row < 0) {
+        atomicExch(&p.T.slots[cs].key, kTomb);  // give the slot back; the chain stays intact
+        latch_error(p.T.hdr, MT_EFULL);
+      } else {
+        p.T.slots[cs].row = row;
+        p.T.slots[cs].meta = step;
+        s_new[atomicAdd(&s_nnew, 1)] = jj;
+      }
+    }
+    if (act) {
+      p.unique_rows[off + jj] = row;
+      s_orow[jj] = row;
+    }
+  }
+  __syncthreads();
+
+  // initialise fresh rows, one team of lanes per row
+  const int nnew = s_nnew;
+  const uint32_t vecs = p.T.row_dtype == MT_F32 ? p.T.dim / 4 : p.T.dim / 8;
+  int team = 1;
+  while (team < 32 && team < (int)vecs) team <<= 1;
+  const int nteams = kThreads / team, my_team = tid / team, lt = tid % team;
+  for (int q = my_team; q < nnew; q += nteams) {
+    const int jj = s_new[q];
+    init_row_coop(p.T, s_orow[jj], p.scratch[s_oslot[jj]].key, lt, team);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_expand_gather(const LookupParams p) {
+  __shared__ int32_t s_lcnt[kTile];
+  __shared__ int32_t s_u[kTile];
+  __shared__ int32_t s_row[kTile];
+  __shared__ uint16_t s_pl[kTile];
+
+  const int tile = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  const long long base = (long long)tile * kTile;
+  const int cnt = (int)min((long long)kTile, p.n - base);
+  const int L = p.tile_L[tile];
+  const size_t lb = (size_t)tile * kTile;
+
+  for (int l = tid; l < L; l += kThreads) s_lcnt[l] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int lp = k * kThreads + tid;
+    const bool in = lp < cnt;
+    uint32_t li = kNoIdx;
+    if (in) {
+      li = p.lidx[base + lp];
+      s_pl[lp] = (uint16_t)li;
+    }
+    const bool v = in && li != kNoIdx;
+    const unsigned act = __ballot_sync(kFull, v);
+    if (v) {
+      const unsigned grp = __match_any_sync(act, li);
+      if (lane == __ffs(grp) - 1) atomicAdd(&s_lcnt[li], __popc(grp));
+    }
+  }
+  __syncthreads();
+  for (int l = tid; l < L; l += kThreads) {
+    const int32_t u = p.scratch[p.lsslot[lb + l]].uidx;
+    s_u[l] = u;
+    s_row[l] = p.unique_rows[u];
+    atomicAdd(&p.counts[u], s_lcnt[l]);
+  }
+  __syncthreads();
+  for (int lp = tid; lp < cnt; lp += kThreads) {
+    const uint16_t li = s_pl[lp];
+    p.inverse[base + lp] = li == kNoIdx ? -1 : s_u[li];
+  }
+  if (p.out_rows == nullptr) return;
+
+  // gather: 16-byte items (position, vector), consecutive threads on
+  // consecutive items, four independent items in flight per thread
+  const int vec16 = (int)(p.T.emb_bytes / 16);
+  const int vshift = (vec16 & (vec16 - 1)) == 0 ? __ffs(vec16) - 1 : -1;
+  const int total = cnt * vec16;
+  uint4* out = reinterpret_cast<uint4*>(p.out_rows) + (size_t)base * vec16;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  for (int i0 = tid; i0 < total; i0 += 4 * kThreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int it = i0 + k * kThreads;
+      v[k] = zero;
+      if (it < total) {
+        const int lp = vshift >= 0 ? (it >> vshift) : it / vec16;
+        const int cc = it - lp * vec16;
+        const uint16_t li = s_pl[lp];
+        const int32_t row = li == kNoIdx ? -1 : s_row[li];
+        if (row >= 0) v[k] = __ldg(reinterpret_cast<const uint4*>(row_ptr(p.T, row)) + cc);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int it = i0 + k * kThreads;
+      if (it < total) __stcs(out + it, v[k]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_scan_small(const int32_t* in, int32_t* out, int count, int width,
+                                                      long long* total_to) {
+  __shared__ int s_warp[32];
+  __shared__ int s_carry[4];
+  if (threadIdx.x < 4) s_carry[threadIdx.x] = 0;
+  __syncthreads();
+  for (int w = 0; w < width; ++w) {
+    for (int b = 0; b < count; b += 1024) {
+      const int i = b + (int)threadIdx.x;
+      const int v = i < count ? in[(size_t)i * width + w] : 0;
+      int tot;
+      const int ex = block_exclusive_scan<1024>(v, s_warp, &tot);
+      if (i < count) out[(size_t)i * width + w] = s_carry[w] + ex;
+      __syncthreads();
+      if (threadIdx.x == 0) s_carry[w] += tot;
+      __syncthreads();
+    }
+  }
+  if ((int)threadIdx.x < width) out[(size_t)count * width + threadIdx.x] = s_carry[threadIdx.x];
+  if (total_to != nullptr && threadIdx.x == 0) *total_to = s_carry[0];
+}
+
+}  // namespace
+
+LookupWsLayout lookup_ws_layout(long long n) {
+  LookupWsLayout L{};
+  L.ntiles = (int)((n + kTile - 1) / kTile);
+  unsigned long long ss = 1024;
+  while (ss < 2ull * (unsigned long long)n) ss <<= 1;
+  L.scratch_slots = ss;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t cap = (size_t)L.ntiles * kTile;
+  L.scratch = take(ss * sizeof(ScratchSlot));
+  L.tile_L = take((size_t)L.ntiles * 4);
+  L.tile_owners = take((size_t)L.ntiles * 4);
+  L.tile_offset = take(((size_t)L.ntiles + 1) * 4);
+  L.lfirst = take(cap * 4);
+  L.lsslot = take(cap * 4);
+  L.lidx = take(cap * 2);
+  L.total = off;
+  return L;
+}
+
+cudaError_t launch_scan_small(const int32_t* in, int32_t* out, int count, int width, long long* total_to,
+                              cudaStream_t s) {
+  k_scan_small<<<1, 1024, 0, s>>>(in, out, count, width, total_to);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
+  if (p.n == 0) return cudaMemsetAsync(p.num_unique, 0, sizeof(long long), s);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_dedup_claim, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaError_t e = cudaMemsetAsync(p.scratch, 0xFF, (p.scratch_mask + 1) * sizeof(ScratchSlot), s);
+  if (e != cudaSuccess) return e;
+  k_dedup_claim<<<p.ntiles, kThreads, kSmemA, s>>>(p);
+  k_count_owners<<<p.ntiles, kThreads, 0, s>>>(p);
+  k_scan_small<<<1, 1024, 0, s>>>(p.tile_owners, p.tile_offset, p.ntiles, 1, p.num_unique);
+  k_assign_resolve<<<p.ntiles, kThreads, 0, s>>>(p);
+  k_expand_gather<<<p.ntiles, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mt

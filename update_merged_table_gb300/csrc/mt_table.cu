@@ -1,0 +1,193 @@
+// Table maintenance kernels: arena initialisation, key deletion with
+// tombstones, the occupancy scan, live-key export and row read-back.
+//
+// Pages: "MTGenRec" abstract (real-time insertions and deletions in dynamic
+// hash tables) and Theorem 1 (probe sequence h_t = (h0 + t*S) mod 2^n, S odd);
+// "MTGR" section 5, Embedding Management (compact key scanning).
+#include "mt_kernels.cuh"
+
+namespace mt {
+
+namespace {
+
+__global__ void k_table_init(const TableDev T) {
+  const long long R = T.num_rows;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < R; i += (long long)gridDim.x * blockDim.x)
+    T.free_stack[i] = (int32_t)(R - 1 - i);  // pops hand out rows 0, 1, 2, ...
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    T.hdr->error = 0;
+    T.hdr->free_top = R;
+    T.hdr->step = 0;
+  }
+}
+
+// Pass 1 of an erase: every key is looked up while the store is unchanged,
+// so duplicates in the batch all see a live key.
+__global__ void k_erase_find(const TableDev T, const unsigned long long* keys, long long n, int32_t* ws_slot) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const unsigned long long key = keys[i];
+    long long s = -1;
+    if (key != kEmpty && key != kTomb) {
+      long long t_end, t_tomb;
+      s = find_slot(T, key, &t_end, &t_tomb);
+    }
+    ws_slot[i] = (int32_t)s;
+  }
+}
+
+// Pass 2: one CAS per found key turns its slot into a tombstone; the winner
+// returns the row to the free stack (warp-aggregated push).
+__global__ void k_erase_apply(const TableDev T, const unsigned long long* keys, long long n, const int32_t* ws_slot,
+                              unsigned char* found) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long n_round = (n + 31) / 32 * 32;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_round; i += stride) {
+    const bool in = i < n;
+    const int32_t s = in ? ws_slot[i] : -1;
+    bool won = false;
+    int32_t row = -1;
+    if (s >= 0) {
+      const unsigned long long key = keys[i];
+      row = T.slots[s].row;
+      won = atomicCAS(&T.slots[s].key, key, kTomb) == key;
+    }
+    if (in && found != nullptr) found[i] = s >= 0 ? 1 : 0;
+    const unsigned mask = __ballot_sync(kFull, won);
+    if (won) push_row_warp(T, mask, row);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_stats(const TableDev T) {
+  __shared__ unsigned long long s_hist[MT_HIST_BINS];
+  __shared__ unsigned long long s_live, s_tomb, s_disp;
+  for (int i = threadIdx.x; i < MT_HIST_BINS; i += blockDim.x) s_hist[i] = 0;
+  if (threadIdx.x == 0) s_live = s_tomb = s_disp = 0;
+  __syncthreads();
+  unsigned long long live = 0, tomb = 0, disp = 0;
+  const unsigned long long M = T.mask + 1;
+  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
+       s += (unsigned long long)gridDim.x * blockDim.x) {
+    const unsigned long long key = T.slots[s].key;
+    if (key == kTomb) {
+      ++tomb;
+    } else if (key != kEmpty) {
+      ++live;
+      // slot = h0 + t*S (mod M)  =>  t = (slot - h0) * S^-1 (mod M)
+      const unsigned long long t = ((s - home_slot(T, key)) & T.mask) * T.Sinv & T.mask;
+      disp += t;
+      atomicAdd(&s_hist[t < MT_HIST_BINS - 1 ? t : MT_HIST_BINS - 1], 1ull);
+    }
+  }
+  atomicAdd(&s_live, live);
+  atomicAdd(&s_tomb, tomb);
+  atomicAdd(&s_disp, disp);
+  __syncthreads();
+  for (int i = threadIdx.x; i < MT_HIST_BINS; i += blockDim.x)
+    if (s_hist[i]) atomicAdd(&T.hdr->hist[i], s_hist[i]);
+  if (threadIdx.x == 0) {
+    atomicAdd(&T.hdr->live, s_live);
+    atomicAdd(&T.hdr->tombs, s_tomb);
+    atomicAdd(&T.hdr->disp, s_disp);
+  }
+}
+
+__global__ void k_export(const TableDev T, unsigned long long* keys, int32_t* rows, long long capacity) {
+  const unsigned long long M = T.mask + 1;
+  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+  const unsigned long long M_round = (M + 31) / 32 * 32;
+  const int lane = threadIdx.x & 31;
+  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M_round; s += stride) {
+    bool live = false;
+    unsigned long long key = 0;
+    int32_t row = -1;
+    if (s < M) {
+      key = T.slots[s].key;
+      live = key != kEmpty && key != kTomb;
+      if (live) row = T.slots[s].row;
+    }
+    const unsigned mask = __ballot_sync(kFull, live);
+    if (mask == 0) continue;
+    const int leader = __ffs(mask) - 1;
+    long long base = 0;
+    if (lane == leader) base = (long long)atomicAdd((unsigned long long*)&T.hdr->export_count, (unsigned long long)__popc(mask));
+    base = __shfl_sync(kFull, base, leader);
+    if (live) {
+      const long long idx = base + __popc(mask & ((1u << lane) - 1u));
+      if (idx < capacity) {
+        keys[idx] = key;
+        rows[idx] = row;
+      }
+    }
+  }
+}
+
+__global__ void k_read_rows(const TableDev T, const int32_t* rows, long long n, float* emb, float* m, float* v) {
+  const long long d = T.dim;
+  const long long total = n * d;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const long long i = it / d, j = it - i * d;
+    const int32_t r = rows[i];
+    float e = 0.f, a = 0.f, b = 0.f;
+    if (r >= 0 && r < T.num_rows) {
+      const char* rec = row_ptr(T, r);
+      e = T.row_dtype == MT_F32 ? reinterpret_cast<const float*>(rec)[j]
+                                : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(rec)[j]);
+      a = reinterpret_cast<const float*>(rec + T.emb_bytes)[j];
+      b = reinterpret_cast<const float*>(rec + T.emb_bytes + T.mv_bytes)[j];
+    }
+    if (emb) emb[it] = e;
+    if (m) m[it] = a;
+    if (v) v[it] = b;
+  }
+}
+
+int grid_for(long long work, int threads) {
+  long long g = (work + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > 152 * 32) g = 152 * 32;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_table_init(const TableDev& T, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(T.hdr, 0, kHeaderBytes, s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(T.slots, 0xFF, (size_t)(T.mask + 1) * sizeof(Slot), s);
+  if (e != cudaSuccess) return e;
+  k_table_init<<<grid_for(T.num_rows, 256), 256, 0, s>>>(T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long long n, unsigned char* found,
+                         int32_t* ws_slot, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  k_erase_find<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot);
+  k_erase_apply<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot, found);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats(const TableDev& T, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(&T.hdr->live, 0, sizeof(unsigned long long) * (3 + MT_HIST_BINS), s);
+  if (e != cudaSuccess) return e;
+  k_stats<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export(const TableDev& T, unsigned long long* keys, int32_t* rows, long long capacity,
+                          cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(&T.hdr->export_count, 0, sizeof(long long), s);
+  if (e != cudaSuccess) return e;
+  k_export<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T, keys, rows, capacity);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_read_rows(const TableDev& T, const int32_t* rows, long long n, float* emb, float* m, float* v,
+                             cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  k_read_rows<<<grid_for(n * T.dim, 256), 256, 0, s>>>(T, rows, n, emb, m, v);
+  return cudaGetLastError();
+}
+
+}  // namespace mt
