@@ -1,0 +1,418 @@
+"""Benchmark of the merged dynamic embedding table hot path on GB300.
+
+One step = one lookup (encode, two-stage dedup, find/insert, gather) plus one
+backward (per-unique gradient sum + sparse Adam) over one batch of the GRM
+jagged-sequence workload: 2048 users with lognormal(5, 1) sequence lengths
+capped at 3000, 4 ID features per token (Zipf(1.1) over 1e6 IDs each, merged
+by table id), M = 2^24 slots, dim 64 bf16 rows, fp32 Adam state, bf16 grads.
+Synthetic, seeded inputs; every step's inputs (IDs 15 MB, grads 247 MB, output
+247 MB) exceed the 126 MB L2, so no flush is needed between steps.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from update_merged_table_gb300 import workloads as W  # noqa: E402
+
+METRIC = "unique+lookup+gather IDs/s and backward+Adam IDs/s; % of GB300 HBM roofline"
+UNIT = "IDs/s"
+WORKLOAD = "GRM jagged sequences: 2048 users, lognormal(5,1) lengths capped at 3000, 4 ID features, M=2^24, dim 64 bf16"
+LOG2_SLOTS, DIM, ROW_DTYPE = 24, 64, "bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(ids_local: float, secs_local: float, group=None):
+    """Whole-job totals over ranks: sum of IDs processed, max of elapsed seconds."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized():
+        return ids_local, secs_local
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([ids_local], dtype=torch.float64, device=dev)
+    s = torch.tensor([secs_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item()), float(s.item())
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d and d[k]:
+                    return float(d[k]), "measured"
+            for k, v in d.items():
+                if "hbm" in k.lower() and isinstance(v, (int, float)):
+                    return float(v), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (getattr(self, "out", "") or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_pool(pool: int, rank: int):
+    """`pool` jagged batches (seeds distinct per rank) plus bf16 grads."""
+    import torch
+    out = []
+    for k in range(pool):
+        seed = 1 + k + 1000 * rank
+        b = W.jagged_batch(seed)
+        g = torch.from_numpy(W.grads_normal(seed + 500_000, b.n, DIM)).to(torch.bfloat16)
+        keys = (b.table_ids[np.searchsorted(b.feat_offsets, np.arange(b.n), side="right") - 1].astype(np.uint64)
+                << np.uint64(56)) | b.ids.astype(np.uint64)
+        out.append(dict(batch=b, grads=g, U=int(np.unique(keys).size)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import update_merged_table_gb300 as mt
+    from update_merged_table_gb300 import build_lib
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    build_lib.build()
+    mt.load_library()
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+
+    tab = mt.Table(LOG2_SLOTS, DIM, row_dtype=ROW_DTYPE, device=dev)
+    pool = make_pool(args.pool, rank)
+    B = DIM * 2          # bytes per bf16 row
+    G = DIM * 2          # bytes per bf16 grad row
+    for e in pool:
+        b = e["batch"]
+        e["ids_d"] = torch.from_numpy(b.ids).to(dev)
+        e["grads_d"] = e["grads"].to(dev)
+        e["res"] = tab.new_result(b.n, gather=True)
+        e["ids_h"] = torch.from_numpy(b.ids).pin_memory()
+        e["grads_h"] = e["grads"].pin_memory()
+        e["u_h"] = torch.empty(1, dtype=torch.int64).pin_memory()
+
+    def step(e):
+        b = e["batch"]
+        tab.lookup(e["ids_d"], b.feat_offsets, b.table_ids, result=e["res"])
+        tab.backward_adam(e["res"], e["grads_d"])
+
+    # step 0: the cold batch (every key new) -- untimed
+    cold = W.jagged_batch(1000 * rank)
+    cres = tab.lookup(torch.from_numpy(cold.ids).to(dev), cold.feat_offsets, cold.table_ids)
+    tab.backward_adam(cres, torch.from_numpy(W.grads_normal(7, cold.n, DIM)).to(torch.bfloat16).to(dev))
+    del cres
+    for j in range(args.warmup):
+        step(pool[j % len(pool)])
+    torch.cuda.synchronize(dev)
+
+    graphs = None
+    launches_per_step = None
+    if args.graph:
+        graphs = []
+        c0 = mt.kernel_launches()
+        for e in pool:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(e)
+            graphs.append(g)
+        torch.cuda.synchronize(dev)
+        launches_per_step = (mt.kernel_launches() - c0) / len(pool)
+
+        def run(j):
+            graphs[j % len(pool)].replay()
+    else:
+        def run(j):
+            step(pool[j % len(pool)])
+
+    # -------- timed region: K steps, inputs resident in HBM --------
+    live0 = tab.stats()["live"]
+    n_ids = sum(pool[j % len(pool)]["batch"].n for j in range(args.steps))
+    launches0 = mt.kernel_launches()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for j in range(args.steps):
+            run(j)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    secs = ev0.elapsed_time(ev1) / 1e3
+    launches = mt.kernel_launches() - launches0
+    if launches_per_step is not None:  # graph replays launch the captured kernels
+        launches = int(round(launches_per_step * args.steps))
+    live1 = tab.stats()["live"]
+    tot_ids, tot_secs = aggregate(float(n_ids), secs)
+
+    # -------- per-direction and per-kernel device times (separate pass) --------
+    fwd_ms = bwd_ms = 0.0
+    npass = min(args.steps, 4 * len(pool))
+    pass_ids = 0
+    pass_U = 0
+    evs = []
+    for j in range(npass):
+        e = pool[j % len(pool)]
+        a, m_, z = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        tab.lookup(e["ids_d"], e["batch"].feat_offsets, e["batch"].table_ids, result=e["res"])
+        m_.record(stream)
+        tab.backward_adam(e["res"], e["grads_d"])
+        z.record(stream)
+        evs.append((a, m_, z))
+        pass_ids += e["batch"].n
+        pass_U += e["U"]
+    torch.cuda.synchronize(dev)
+    for a, m_, z in evs:
+        fwd_ms += a.elapsed_time(m_)
+        bwd_ms += m_.elapsed_time(z)
+    mt.profile_enable(True)
+    mt.profile_report(reset=True)
+    for j in range(npass):
+        step(pool[j % len(pool)])
+    torch.cuda.synchronize(dev)
+    prof = mt.profile_report(reset=True)
+    mt.profile_enable(False)
+
+    # algorithmic bytes (steady state; new keys counted from the live-key growth)
+    n_new_per_step = (live1 - live0) / max(1, args.steps)
+    N_avg = pass_ids / npass
+    U_avg = pass_U / npass
+    fwd_bytes = 8 * N_avg + 4 * N_avg + U_avg * (8 + 16) + U_avg * B + N_avg * B + n_new_per_step * (16 + B + 8 * DIM)
+    bwd_bytes = N_avg * G + 4 * N_avg + U_avg * (4 + 2 * B + 16 * DIM)
+    kernel_bytes = {
+        "k_bw_reduce_adam": N_avg * G + 4 * N_avg + U_avg * (2 * B + 16 * DIM + 16),
+        "k_expand_gather": N_avg * B + U_avg * B + 6 * N_avg,
+    }
+    peak, peak_kind = measured_hbm_peak()
+    tot_k = sum(v[1] for v in prof.values()) or 1.0
+    dom = max((k for k in prof if k in kernel_bytes), key=lambda k: prof[k][1])
+    dom_ms = prof[dom][1] / prof[dom][0]
+    achieved = kernel_bytes[dom] / (dom_ms / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(dom)
+        except Exception:
+            traffic = None
+
+    # -------- end to end through the public API with host buffers --------
+    e2e_steps = min(args.steps, 4 * len(pool))
+    h2d = d2h = 0
+    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ids = 0
+    torch.cuda.synchronize(dev)
+    ev2.record(stream)
+    for j in range(e2e_steps):
+        e = pool[j % len(pool)]
+        e["ids_d"].copy_(e["ids_h"], non_blocking=True)
+        e["grads_d"].copy_(e["grads_h"], non_blocking=True)
+        step(e)
+        e["u_h"].copy_(e["res"].num_unique, non_blocking=True)
+        h2d += e["ids_h"].numel() * 8 + e["grads_h"].numel() * 2
+        d2h += 8
+        e2e_ids += e["batch"].n
+    ev3.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_secs = ev2.elapsed_time(ev3) / 1e3
+    e2e_tot, e2e_max = aggregate(float(e2e_ids), e2e_secs)
+
+    err = tab.error()
+    if err != 0:
+        raise RuntimeError(f"device error {err} during the benchmark")
+
+    line = {
+        "metric": METRIC, "value": tot_ids / tot_secs, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot_secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "ids_per_step": N_avg, "unique_per_step": U_avg,
+                   "new_keys_per_step": n_new_per_step, "batch_pool": len(pool), "cuda_graph": bool(args.graph),
+                   "l2": "inputs larger than L2 (ids+grads+out ~0.5 GB per step), no flush",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "fwd_ids_per_s": pass_ids / (fwd_ms / 1e3), "bwd_ids_per_s": pass_ids / (bwd_ms / 1e3),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kernel_bytes[dom], "avg_launch_ms": dom_ms,
+                     "time_share": prof[dom][1] / tot_k},
+        "roofline_fwd": {"bytes_per_step": fwd_bytes, "achieved": fwd_bytes / (fwd_ms / npass / 1e3) / 1e9,
+                         "frac": fwd_bytes / (fwd_ms / npass / 1e3) / 1e9 / peak},
+        "roofline_bwd": {"bytes_per_step": bwd_bytes, "achieved": bwd_bytes / (bwd_ms / npass / 1e3) / 1e9,
+                         "frac": bwd_bytes / (bwd_ms / npass / 1e3) / 1e9 / peak},
+        "kernels": {k: {"launches": v[0], "avg_us": 1e3 * v[1] / v[0], "share": v[1] / tot_k} for k, v in prof.items()},
+        "e2e": {"value": e2e_tot / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d // e2e_steps,
+                "d2h_bytes_per_step": d2h // e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (reported baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(budget_s: float, users: int = 256):
+    """Oracle lookup+backward IDs/s on a bounded sample of the workload.
+
+    Sample: the first `users` users' worth of tokens per step (same length
+    distribution, same 4 features and table), cold step untimed, then steps
+    until about `budget_s` seconds of oracle time have been spent."""
+    import oracle
+    ref = oracle.Table(LOG2_SLOTS, DIM, row_dtype=oracle.BF16)
+    cold = W.jagged_batch(0, users=users)
+    ref.lookup(cold.ids, cold.feat_offsets, cold.table_ids)
+    gb = W.grads_normal(7, cold.n, DIM)
+    import torch
+    gbits = torch.from_numpy(gb).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref.backward_adam(gbits, grad_dtype=oracle.BF16)
+    ids_done, t_total, steps = 0, 0.0, 0
+    k = 1
+    while t_total < budget_s and steps < 10_000:
+        b = W.jagged_batch(k, users=users)
+        g = torch.from_numpy(W.grads_normal(k + 500_000, b.n, DIM)).to(torch.bfloat16).view(torch.int16).numpy()
+        g = g.view(np.uint16)
+        t0 = time.perf_counter()
+        ref.lookup(b.ids, b.feat_offsets, b.table_ids)
+        ref.backward_adam(g, grad_dtype=oracle.BF16)
+        t_total += time.perf_counter() - t0
+        ids_done += b.n
+        steps += 1
+        k += 1
+    return {"value": ids_done / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} steps of the first {users} users (avg {ids_done // max(1, steps)} IDs/step) "
+                      f"after one untimed cold step; single-threaded C++ oracle, {t_total:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cb = cpu_baseline(args.cpu_seconds)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD + " (bounded sample: 256 users per step)"},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pool", type=int, default=8, help="distinct pre-generated batches cycled through")
+    ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

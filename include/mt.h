@@ -230,6 +230,28 @@ int mt_get_error(mt_table* t, int32_t* device_error, int clear, mt_stream stream
 /* Adam steps taken so far (host-side count of mt_backward_adam calls). */
 int64_t mt_step(const mt_table* t);
 
+/* ---- tracing ------------------------------------------------------------- */
+
+/* Per-kernel device time, measured with CUDA events recorded on the
+ * launching stream around each kernel while profiling is on. */
+typedef struct {
+  char name[40];
+  int64_t launches;
+  double total_ms;
+} mt_kernel_time;
+
+/* Turn per-kernel event timing on or off for every table of the process
+ * (off by default; when on, each launch adds two event records). */
+int mt_profile_enable(int on);
+
+/* Synchronise the recorded events and return accumulated per-kernel totals
+ * (up to `capacity` entries; *count receives how many kernels have totals);
+ * clears the totals when `reset` is non-zero. */
+int mt_profile_report(mt_kernel_time* out, int capacity, int* count, int reset);
+
+/* Number of kernels this library has launched in the process. */
+int64_t mt_kernel_launches(void);
+
 const char* mt_strerror(int code);
 int mt_abi_version(void);
 

@@ -21,7 +21,7 @@ import os
 import numpy as np
 
 __all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "KEY_EMPTY", "KEY_TOMBSTONE",
-           "ABI_FUNCTIONS"]
+           "ABI_FUNCTIONS", "profile_enable", "profile_report", "kernel_launches"]
 
 MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA = 0, -1, -2, -3, -4, -5
 MT_F32, MT_BF16 = 0, 1
@@ -84,9 +84,36 @@ ABI_FUNCTIONS = {
     "mt_read_rows": (_I32, [_P, _P, _I64, _P, _P, _P, _P]),
     "mt_get_error": (_I32, [_P, _P, _I32, _P]),
     "mt_step": (_I64, [_P]),
+    "mt_profile_enable": (_I32, [_I32]),
+    "mt_profile_report": (_I32, [_P, _I32, _P, _I32]),
+    "mt_kernel_launches": (_I64, []),
 }
 
+class _KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
+
+
 _lib = None
+
+
+def profile_enable(on: bool = True) -> None:
+    """Per-kernel CUDA-event timing for every table of the process (off by default)."""
+    _check(load_library().mt_profile_enable(int(bool(on))), "mt_profile_enable")
+
+
+def profile_report(reset: bool = True) -> dict:
+    """{kernel name: (launches, total ms)} accumulated since the last reset; synchronises the events."""
+    L = load_library()
+    cap = 64
+    buf = (_KernelTime * cap)()
+    cnt = ctypes.c_int()
+    _check(L.mt_profile_report(buf, cap, ctypes.byref(cnt), int(bool(reset))), "mt_profile_report")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(min(cnt.value, cap))}
+
+
+def kernel_launches() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load_library().mt_kernel_launches())
 
 
 def load_library(path: str | None = None) -> ctypes.CDLL:

@@ -411,6 +411,7 @@ cudaError_t launch_reduce(const BackwardParams& p, int team_shift, cudaStream_t 
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_bw_reduce_adam<RD, GD>, 256, 0);
     grid = sms * (per > 0 ? per : 1);
   }
+  MT_LAUNCH("k_bw_reduce_adam", s);
   k_bw_reduce_adam<RD, GD><<<grid, 256, 0, s>>>(p, team_shift);
   return cudaGetLastError();
 }
@@ -444,11 +445,20 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
 }
 
 cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
-  k_bw_blocksum<<<p.nblk, kScanThreads, 0, s>>>(p);
+  {
+    MT_LAUNCH("k_bw_blocksum", s);
+    k_bw_blocksum<<<p.nblk, kScanThreads, 0, s>>>(p);
+  }
   cudaError_t e = launch_scan_small(p.bsum, p.boff, p.nblk, 3, nullptr, s);
   if (e != cudaSuccess) return e;
-  k_bw_offsets<<<p.nblk, kScanThreads, 0, s>>>(p);
-  if (p.ntiles > 0) k_bw_fill<<<p.ntiles, kThreads, 0, s>>>(p);
+  {
+    MT_LAUNCH("k_bw_offsets", s);
+    k_bw_offsets<<<p.nblk, kScanThreads, 0, s>>>(p);
+  }
+  if (p.ntiles > 0) {
+    MT_LAUNCH("k_bw_fill", s);
+    k_bw_fill<<<p.ntiles, kThreads, 0, s>>>(p);
+  }
   const int vec = p.T.row_dtype == MT_F32 ? 4 : 8;
   int team = 1, shift = 0;
   while (team < 32 && team * vec < (int)p.T.dim) {

@@ -112,6 +112,26 @@ cudaError_t launch_read_rows(const TableDev& T, const int32_t* rows, long long n
 cudaError_t launch_scan_small(const int32_t* in, int32_t* out, int count, int width, long long* total_to,
                               cudaStream_t s);
 
+// Counts every kernel launch of the library and, while profiling is on,
+// brackets it with CUDA events on its stream (mt_profile.cu).
+class LaunchScope {
+ public:
+  LaunchScope(const char* name, cudaStream_t s);
+  ~LaunchScope();
+  LaunchScope(const LaunchScope&) = delete;
+  LaunchScope& operator=(const LaunchScope&) = delete;
+
+ private:
+  const char* name_;
+  cudaStream_t stream_;
+  cudaEvent_t start_;
+};
+
+#define MT_CAT2(a, b) a##b
+#define MT_CAT(a, b) MT_CAT2(a, b)
+// Put at the start of a block that launches exactly one kernel.
+#define MT_LAUNCH(name, stream) ::mt::LaunchScope MT_CAT(mt_launch_scope_, __LINE__)(name, stream)
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace mt

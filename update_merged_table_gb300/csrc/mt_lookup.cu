@@ -441,7 +441,10 @@ LookupWsLayout lookup_ws_layout(long long n) {
 
 cudaError_t launch_scan_small(const int32_t* in, int32_t* out, int count, int width, long long* total_to,
                               cudaStream_t s) {
-  k_scan_small<<<1, 1024, 0, s>>>(in, out, count, width, total_to);
+  {
+    MT_LAUNCH("k_scan_small", s);
+    k_scan_small<<<1, 1024, 0, s>>>(in, out, count, width, total_to);
+  }
   return cudaGetLastError();
 }
 
@@ -455,11 +458,24 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
   }
   cudaError_t e = cudaMemsetAsync(p.scratch, 0xFF, (p.scratch_mask + 1) * sizeof(ScratchSlot), s);
   if (e != cudaSuccess) return e;
-  k_dedup_claim<<<p.ntiles, kThreads, kSmemA, s>>>(p);
-  k_count_owners<<<p.ntiles, kThreads, 0, s>>>(p);
-  k_scan_small<<<1, 1024, 0, s>>>(p.tile_owners, p.tile_offset, p.ntiles, 1, p.num_unique);
-  k_assign_resolve<<<p.ntiles, kThreads, 0, s>>>(p);
-  k_expand_gather<<<p.ntiles, kThreads, 0, s>>>(p);
+  {
+    MT_LAUNCH("k_dedup_claim", s);
+    k_dedup_claim<<<p.ntiles, kThreads, kSmemA, s>>>(p);
+  }
+  {
+    MT_LAUNCH("k_count_owners", s);
+    k_count_owners<<<p.ntiles, kThreads, 0, s>>>(p);
+  }
+  e = launch_scan_small(p.tile_owners, p.tile_offset, p.ntiles, 1, p.num_unique, s);
+  if (e != cudaSuccess) return e;
+  {
+    MT_LAUNCH("k_assign_resolve", s);
+    k_assign_resolve<<<p.ntiles, kThreads, 0, s>>>(p);
+  }
+  {
+    MT_LAUNCH("k_expand_gather", s);
+    k_expand_gather<<<p.ntiles, kThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -156,22 +156,34 @@ cudaError_t launch_table_init(const TableDev& T, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(T.slots, 0xFF, (size_t)(T.mask + 1) * sizeof(Slot), s);
   if (e != cudaSuccess) return e;
-  k_table_init<<<grid_for(T.num_rows, 256), 256, 0, s>>>(T);
+  {
+    MT_LAUNCH("k_table_init", s);
+    k_table_init<<<grid_for(T.num_rows, 256), 256, 0, s>>>(T);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long long n, unsigned char* found,
                          int32_t* ws_slot, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  k_erase_find<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot);
-  k_erase_apply<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot, found);
+  {
+    MT_LAUNCH("k_erase_find", s);
+    k_erase_find<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot);
+  }
+  {
+    MT_LAUNCH("k_erase_apply", s);
+    k_erase_apply<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot, found);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_stats(const TableDev& T, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(&T.hdr->live, 0, sizeof(unsigned long long) * (3 + MT_HIST_BINS), s);
   if (e != cudaSuccess) return e;
-  k_stats<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T);
+  {
+    MT_LAUNCH("k_stats", s);
+    k_stats<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T);
+  }
   return cudaGetLastError();
 }
 
@@ -179,14 +191,20 @@ cudaError_t launch_export(const TableDev& T, unsigned long long* keys, int32_t* 
                           cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(&T.hdr->export_count, 0, sizeof(long long), s);
   if (e != cudaSuccess) return e;
-  k_export<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T, keys, rows, capacity);
+  {
+    MT_LAUNCH("k_export", s);
+    k_export<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T, keys, rows, capacity);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_read_rows(const TableDev& T, const int32_t* rows, long long n, float* emb, float* m, float* v,
                              cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  k_read_rows<<<grid_for(n * T.dim, 256), 256, 0, s>>>(T, rows, n, emb, m, v);
+  {
+    MT_LAUNCH("k_read_rows", s);
+    k_read_rows<<<grid_for(n * T.dim, 256), 256, 0, s>>>(T, rows, n, emb, m, v);
+  }
   return cudaGetLastError();
 }
 
