@@ -128,18 +128,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def make_pool(pool: int, rank: int):
+def make_pool(pool: int, rank: int, users: int):
     """`pool` jagged batches (seeds distinct per rank) plus bf16 grads."""
     import torch
     out = []
     for k in range(pool):
         seed = 1 + k + 1000 * rank
-        b = W.jagged_batch(seed)
+        b = W.jagged_batch(seed, users=users)
         g = torch.from_numpy(W.grads_normal(seed + 500_000, b.n, DIM)).to(torch.bfloat16)
         keys = (b.table_ids[np.searchsorted(b.feat_offsets, np.arange(b.n), side="right") - 1].astype(np.uint64)
                 << np.uint64(56)) | b.ids.astype(np.uint64)
         out.append(dict(batch=b, grads=g, U=int(np.unique(keys).size)))
     return out
+
+
+def workload_name(args) -> str:
+    if args.users == 2048 and args.log2_slots == LOG2_SLOTS:
+        return WORKLOAD
+    return (f"GRM jagged sequences (reduced): {args.users} users, lognormal(5,1) lengths capped at 3000, "
+            f"4 ID features, M=2^{args.log2_slots}, dim 64 bf16")
 
 
 # ---------------------------------------------------------------------------
@@ -163,8 +170,8 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
 
-    tab = mt.Table(LOG2_SLOTS, DIM, row_dtype=ROW_DTYPE, device=dev)
-    pool = make_pool(args.pool, rank)
+    tab = mt.Table(args.log2_slots, DIM, row_dtype=ROW_DTYPE, device=dev)
+    pool = make_pool(args.pool, rank, args.users)
     B = DIM * 2          # bytes per bf16 row
     G = DIM * 2          # bytes per bf16 grad row
     for e in pool:
@@ -182,7 +189,7 @@ def run_ours(args):
         tab.backward_adam(e["res"], e["grads_d"])
 
     # step 0: the cold batch (every key new) -- untimed
-    cold = W.jagged_batch(1000 * rank)
+    cold = W.jagged_batch(1000 * rank, users=args.users)
     cres = tab.lookup(torch.from_numpy(cold.ids).to(dev), cold.feat_offsets, cold.table_ids)
     tab.backward_adam(cres, torch.from_numpy(W.grads_normal(7, cold.n, DIM)).to(torch.bfloat16).to(dev))
     del cres
@@ -314,7 +321,7 @@ def run_ours(args):
         "metric": METRIC, "value": tot_ids / tot_secs, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * tot_secs / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "ids_per_step": N_avg, "unique_per_step": U_avg,
+        "config": {"workload": workload_name(args), "ids_per_step": N_avg, "unique_per_step": U_avg,
                    "new_keys_per_step": n_new_per_step, "batch_pool": len(pool), "cuda_graph": bool(args.graph),
                    "l2": "inputs larger than L2 (ids+grads+out ~0.5 GB per step), no flush",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
@@ -405,6 +412,8 @@ def main():
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--users", type=int, default=2048, help="users per batch (smaller cases for profiling)")
+    ap.add_argument("--log2-slots", type=int, default=LOG2_SLOTS)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

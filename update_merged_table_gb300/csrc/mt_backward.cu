@@ -90,10 +90,23 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
 
 constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_offsets
 
+// Per unique: segment start (cursor).  Per chunk: a descriptor {start, end,
+// row, u or -(heavy index + 1)}, written cooperatively by the block so a hot
+// unique with thousands of chunks costs no single thread more than its share.
+// Per multi-chunk unique: {u, chunks}, a zero arrival count and zeroed fp64
+// accumulators.
 __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
+  __shared__ int s_chrel[kScanTile + 1];  // first chunk of each local unique, relative to the block
+  __shared__ int s_seg[kScanTile];        // segment start, relative to the block
+  __shared__ int s_cnt[kScanTile];
+  __shared__ int s_row[kScanTile];
+  __shared__ int s_hrel[kScanTile];       // multi-chunk index relative to the block, or -1
   const long long U = *p.num_unique;
-  const long long u0 = (long long)blockIdx.x * kScanTile + (long long)threadIdx.x * kUPT;
+  const long long ublk = (long long)blockIdx.x * kScanTile;
+  if (ublk >= U) return;  // uniform over the block
+  const int tid = threadIdx.x;
+  const long long u0 = ublk + (long long)tid * kUPT;
   int c[kUPT];
   int v[3] = {0, 0, 0};
 #pragma unroll
@@ -106,30 +119,49 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   }
   int ex[3], tot[3];
   block_scan3<kScanThreads>(v, ex, tot, s_warp);
-  int seg = ex[0] + p.boff[(size_t)blockIdx.x * 3 + 0];
-  int ch = ex[1] + p.boff[(size_t)blockIdx.x * 3 + 1];
-  int hv = ex[2] + p.boff[(size_t)blockIdx.x * 3 + 2];
-  const uint32_t d = p.T.dim;
+  const int seg_base = p.boff[(size_t)blockIdx.x * 3 + 0];
+  const int ch_base = p.boff[(size_t)blockIdx.x * 3 + 1];
+  const int hv_base = p.boff[(size_t)blockIdx.x * 3 + 2];
+  int seg = ex[0], ch = ex[1], hv = ex[2];
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
+    const int ul = tid * kUPT + k;
     const long long u = u0 + k;
-    if (u >= U) break;
     const int nc = nchunks(c[k]);
-    p.cursor[u] = seg;
-    p.chunk_off[u] = ch;
-    for (int q = 0; q < nc; ++q) p.chunk_u[ch + q] = (int32_t)u;
-    if (nc > 1) {
-      p.heavy_idx[u] = hv;
-      p.arrive[hv] = 0;
-      double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)hv * d);
-      for (uint32_t q = 0; q < d / 2; ++q) a[q] = make_double2(0.0, 0.0);
-      ++hv;
-    } else {
-      p.heavy_idx[u] = -1;
-    }
-    seg += c[k];
+    s_chrel[ul] = ch;
+    s_seg[ul] = seg;
+    s_cnt[ul] = c[k];
+    s_hrel[ul] = nc > 1 ? hv : -1;
+    s_row[ul] = u < U ? p.unique_rows[u] : -1;
+    if (u < U) p.cursor[u] = seg_base + seg;
     ch += nc;
+    seg += c[k];
+    hv += nc > 1;
   }
+  if (tid == 0) s_chrel[kScanTile] = tot[1];
+  __syncthreads();
+  for (int cc = tid; cc < tot[1]; cc += kScanThreads) {
+    int lo = 0, hi = kScanTile;  // s_chrel[lo] <= cc < s_chrel[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_chrel[mid] <= cc) lo = mid; else hi = mid;
+    }
+    const int k = cc - s_chrel[lo];
+    const int start = seg_base + s_seg[lo] + k * kChunk;
+    const int end = min(start + kChunk, seg_base + s_seg[lo] + s_cnt[lo]);
+    const int w = s_hrel[lo] < 0 ? (int)(ublk + lo) : -(hv_base + s_hrel[lo] + 1);
+    p.chunks[ch_base + cc] = make_int4(start, end, s_row[lo], w);
+  }
+  for (int ul = tid; ul < kScanTile; ul += kScanThreads) {
+    if (s_hrel[ul] >= 0) {
+      const int h = hv_base + s_hrel[ul];
+      p.heavy_info[h] = make_int2((int)(ublk + ul), nchunks(s_cnt[ul]));
+      p.arrive[h] = 0;
+    }
+  }
+  const int d2 = (int)p.T.dim / 2;
+  double2* acc = reinterpret_cast<double2*>(p.acc64 + (size_t)hv_base * p.T.dim);
+  for (int it = tid; it < tot[2] * d2; it += kScanThreads) acc[it] = make_double2(0.0, 0.0);
 }
 
 // Positions grouped by unique: each tile groups its positions by unique in
@@ -237,19 +269,21 @@ __device__ __forceinline__ void load_grad(const void* grads, long long pos, int 
   }
 }
 
-// One Adam step on columns [col, col + VEC) of a row, in the operation order
-// of the update rule, every operation rounded once.
+// Adam state of columns [col, col + VEC) of a row: w (as fp32), m, v.
 template <int RD, int VEC>
-__device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, int col, const float g[VEC],
-                                          float bc1, float bc2) {
-  char* rec = row_ptr(p.T, row);
-  float w[VEC];
+struct RowCols {
+  float w[VEC], m[VEC], v[VEC];
+};
+
+template <int RD, int VEC>
+__device__ __forceinline__ void load_row_cols(const TableDev& T, int32_t row, int col, RowCols<RD, VEC>& r) {
+  const char* rec = row_ptr(T, row);
   if (RD == MT_F32) {
-    float4* e = reinterpret_cast<float4*>(rec) + col / 4;
+    const float4* e = reinterpret_cast<const float4*>(rec) + col / 4;
 #pragma unroll
     for (int q = 0; q < VEC / 4; ++q) {
       const float4 t = e[q];
-      w[4 * q] = t.x; w[4 * q + 1] = t.y; w[4 * q + 2] = t.z; w[4 * q + 3] = t.w;
+      r.w[4 * q] = t.x; r.w[4 * q + 1] = t.y; r.w[4 * q + 2] = t.z; r.w[4 * q + 3] = t.w;
     }
   } else {
     const uint4 t = *(reinterpret_cast<const uint4*>(rec) + col / 8);
@@ -257,52 +291,76 @@ __device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, 
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[q]));
-      w[2 * q] = f.x;
-      w[2 * q + 1] = f.y;
+      r.w[2 * q] = f.x;
+      r.w[2 * q + 1] = f.y;
     }
   }
-  float4* mp = reinterpret_cast<float4*>(rec + p.T.emb_bytes) + col / 4;
-  float4* vp = reinterpret_cast<float4*>(rec + p.T.emb_bytes + p.T.mv_bytes) + col / 4;
-  float m[VEC], v[VEC];
+  const float4* mp = reinterpret_cast<const float4*>(rec + T.emb_bytes) + col / 4;
+  const float4* vp = reinterpret_cast<const float4*>(rec + T.emb_bytes + T.mv_bytes) + col / 4;
 #pragma unroll
   for (int q = 0; q < VEC / 4; ++q) {
     const float4 a = mp[q], b = vp[q];
-    m[4 * q] = a.x; m[4 * q + 1] = a.y; m[4 * q + 2] = a.z; m[4 * q + 3] = a.w;
-    v[4 * q] = b.x; v[4 * q + 1] = b.y; v[4 * q + 2] = b.z; v[4 * q + 3] = b.w;
+    r.m[4 * q] = a.x; r.m[4 * q + 1] = a.y; r.m[4 * q + 2] = a.z; r.m[4 * q + 3] = a.w;
+    r.v[4 * q] = b.x; r.v[4 * q + 1] = b.y; r.v[4 * q + 2] = b.z; r.v[4 * q + 3] = b.w;
   }
+}
+
+// One Adam step on the loaded columns, in the operation order of the update
+// rule with every operation rounded once, then the store.
+template <int RD, int VEC>
+__device__ __forceinline__ void adam_apply_store(const BackwardParams& p, int32_t row, int col, const float g[VEC],
+                                                 RowCols<RD, VEC>& r, float bc1, float bc2) {
 #pragma unroll
   for (int j = 0; j < VEC; ++j) {
-    m[j] = __fadd_rn(__fmul_rn(p.beta1, m[j]), __fmul_rn(p.one_minus_b1, g[j]));
-    v[j] = __fadd_rn(__fmul_rn(p.beta2, v[j]), __fmul_rn(p.one_minus_b2, __fmul_rn(g[j], g[j])));
-    const float mhat = __fdiv_rn(m[j], bc1);
-    const float vhat = __fdiv_rn(v[j], bc2);
+    r.m[j] = __fadd_rn(__fmul_rn(p.beta1, r.m[j]), __fmul_rn(p.one_minus_b1, g[j]));
+    r.v[j] = __fadd_rn(__fmul_rn(p.beta2, r.v[j]), __fmul_rn(p.one_minus_b2, __fmul_rn(g[j], g[j])));
+    const float mhat = __fdiv_rn(r.m[j], bc1);
+    const float vhat = __fdiv_rn(r.v[j], bc2);
     const float den = __fadd_rn(__fsqrt_rn(vhat), p.eps);
-    w[j] = __fsub_rn(w[j], __fmul_rn(p.lr, __fdiv_rn(mhat, den)));
+    r.w[j] = __fsub_rn(r.w[j], __fmul_rn(p.lr, __fdiv_rn(mhat, den)));
   }
+  char* rec = row_ptr(p.T, row);
+  float4* mp = reinterpret_cast<float4*>(rec + p.T.emb_bytes) + col / 4;
+  float4* vp = reinterpret_cast<float4*>(rec + p.T.emb_bytes + p.T.mv_bytes) + col / 4;
 #pragma unroll
   for (int q = 0; q < VEC / 4; ++q) {
-    mp[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
-    vp[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    mp[q] = make_float4(r.m[4 * q], r.m[4 * q + 1], r.m[4 * q + 2], r.m[4 * q + 3]);
+    vp[q] = make_float4(r.v[4 * q], r.v[4 * q + 1], r.v[4 * q + 2], r.v[4 * q + 3]);
   }
   if (RD == MT_F32) {
     float4* e = reinterpret_cast<float4*>(rec) + col / 4;
 #pragma unroll
-    for (int q = 0; q < VEC / 4; ++q) e[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    for (int q = 0; q < VEC / 4; ++q) e[q] = make_float4(r.w[4 * q], r.w[4 * q + 1], r.w[4 * q + 2], r.w[4 * q + 3]);
   } else {
     uint32_t ww[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(w[2 * q], w[2 * q + 1]);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(r.w[2 * q], r.w[2 * q + 1]);
       ww[q] = *reinterpret_cast<uint32_t*>(&b2);
     }
     *(reinterpret_cast<uint4*>(rec) + col / 8) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
   }
 }
 
+__device__ __forceinline__ void store_gsum(float* gsum_out, int u, int d, int col, const float* gs, int vec) {
+  float4* o = reinterpret_cast<float4*>(gsum_out + (size_t)u * d + col);
+  for (int r = 0; r < vec / 4; ++r) o[r] = make_float4(gs[4 * r], gs[4 * r + 1], gs[4 * r + 2], gs[4 * r + 3]);
+}
+
+constexpr int kMinTeamShift = 2;                              // teams of at least 4 lanes
+constexpr int kMaxTeams = 256 >> kMinTeamShift;               // per block
+
+// One team of 2^team_shift lanes per chunk descriptor.  The team stages the
+// chunk's positions in shared memory, prefetches the Adam row of a
+// single-chunk unique while the gradient rows load, accumulates in TwoSum
+// pairs, and either applies Adam (single-chunk unique) or adds its partial
+// sum to the unique's fp64 accumulator in L2, the last chunk applying Adam.
 template <int RD, int GD>
 __global__ void __launch_bounds__(256) k_bw_reduce_adam(const BackwardParams p, int team_shift) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;
+  constexpr int UNR = VEC == 8 ? 4 : 8;  // gradient rows in flight per lane
   __shared__ float s_bc[2];
+  __shared__ int s_pos[kMaxTeams * kChunk];
   if (threadIdx.x == 0) {
     const double t = (double)p.T.hdr->step;
     s_bc[0] = (float)(1.0 - pow((double)p.beta1, t));
@@ -315,87 +373,82 @@ __global__ void __launch_bounds__(256) k_bw_reduce_adam(const BackwardParams p, 
   const int lane = threadIdx.x & 31;
   const int lt = lane & (team - 1);
   const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << (lane & ~(team - 1)));
+  int* my_pos = s_pos + (threadIdx.x >> team_shift) * kChunk;
   const long long total_chunks = p.boff[(size_t)p.nblk * 3 + 1];
   const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
   const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
   const int d = (int)p.T.dim;
+  const bool one_pass = d <= team * VEC;
 
   for (long long c = gteam; c < total_chunks; c += nteam) {
-    const int u = p.chunk_u[c];
-    const int k = (int)(c - p.chunk_off[u]);
-    const int cntu = p.counts[u];
-    const int seg_end = p.cursor[u];  // the fill advanced the cursor to the segment end
-    const int start = seg_end - cntu + k * kChunk;
-    const int end = min(start + kChunk, seg_end);
-    const int nc = nchunks(cntu);
-    const int32_t row = p.unique_rows[u];
-    const int h = nc > 1 ? p.heavy_idx[u] : -1;
+    const int4 dsc = __ldg(&p.chunks[c]);
+    const int start = dsc.x, cnt = dsc.y - dsc.x, row = dsc.z;
+    const bool heavy = dsc.w < 0;
+    for (int q = lt; q < cnt; q += team) my_pos[q] = __ldg(&p.pos_sorted[start + q]);
+    RowCols<RD, VEC> rc;
+    const int col0 = lt * VEC;
+    if (one_pass && !heavy && row >= 0 && col0 < d) load_row_cols<RD, VEC>(p.T, row, col0, rc);
+    __syncwarp(team_mask);
 
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
-      const int col = c0 + lt * VEC;
+      const int col = c0 + col0;
       if (col >= d) continue;
       float hi[VEC], lo[VEC];
 #pragma unroll
       for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
-      int q = start;
-      for (; q + 4 <= end; q += 4) {
-        int pos[4];
+      for (int q0 = 0; q0 < cnt; q0 += UNR) {
+        float g[UNR][VEC];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) pos[r] = p.pos_sorted[q + r];
-        float g[4][VEC];
+        for (int r = 0; r < UNR; ++r)
+          if (q0 + r < cnt) load_grad<GD, VEC>(p.grads, my_pos[q0 + r], d, col, g[r]);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) load_grad<GD, VEC>(p.grads, pos[r], d, col, g[r]);
+        for (int r = 0; r < UNR; ++r)
+          if (q0 + r < cnt) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], g[r][j]);
+            for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], g[r][j]);
+          }
       }
-      for (; q < end; ++q) {
-        float g[VEC];
-        load_grad<GD, VEC>(p.grads, p.pos_sorted[q], d, col, g);
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], g[j]);
-      }
-      if (nc == 1) {
+      if (!heavy) {
         float gs[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
-        if (p.gsum_out != nullptr) {
-          float4* o = reinterpret_cast<float4*>(p.gsum_out + (size_t)u * d + col);
-#pragma unroll
-          for (int r = 0; r < VEC / 4; ++r) o[r] = make_float4(gs[4 * r], gs[4 * r + 1], gs[4 * r + 2], gs[4 * r + 3]);
+        if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
+        if (row >= 0) {
+          if (!one_pass) load_row_cols<RD, VEC>(p.T, row, col, rc);
+          adam_apply_store<RD, VEC>(p, row, col, gs, rc, bc1, bc2);
         }
-        if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, bc1, bc2);
       } else {
-        double* a = p.acc64 + (size_t)h * d + col;
+        double* a = p.acc64 + (size_t)(-dsc.w - 1) * d + col;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) atomicAdd(a + j, (double)hi[j] + (double)lo[j]);
       }
     }
-    if (nc > 1) {
+    if (heavy) {
+      const int h = -dsc.w - 1;
       __threadfence();
       __syncwarp(team_mask);
       int old = 0;
       if (lt == 0) old = atomicAdd(&p.arrive[h], 1);
       old = __shfl_sync(team_mask, old, 0, team);
-      if (old == nc - 1) {  // last chunk of this unique: every partial sum has landed
+      const int2 hinfo = __ldg(&p.heavy_info[h]);
+      if (old == hinfo.y - 1) {  // last chunk of this unique: every partial sum has landed
         __threadfence();
         for (int c0 = 0; c0 < d; c0 += team * VEC) {
-          const int col = c0 + lt * VEC;
+          const int col = c0 + col0;
           if (col >= d) continue;
           float gs[VEC];
           const double* a = p.acc64 + (size_t)h * d + col;
 #pragma unroll
           for (int j = 0; j < VEC; ++j) gs[j] = (float)__ldcg(a + j);
-          if (p.gsum_out != nullptr) {
-            float4* o = reinterpret_cast<float4*>(p.gsum_out + (size_t)u * d + col);
-#pragma unroll
-            for (int r = 0; r < VEC / 4; ++r) o[r] = make_float4(gs[4 * r], gs[4 * r + 1], gs[4 * r + 2], gs[4 * r + 3]);
+          if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
+          if (row >= 0) {
+            load_row_cols<RD, VEC>(p.T, row, col, rc);
+            adam_apply_store<RD, VEC>(p, row, col, gs, rc, bc1, bc2);
           }
-          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, bc1, bc2);
         }
       }
     }
+    __syncwarp(team_mask);  // my_pos is reused by the next chunk
   }
 }
 
@@ -434,9 +487,8 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
   L.bsum = take((size_t)L.nblk * 3 * 4);
   L.boff = take(((size_t)L.nblk + 1) * 3 * 4);
   L.cursor = take(nn * 4);
-  L.chunk_off = take(nn * 4);
-  L.heavy_idx = take(nn * 4);
-  L.chunk_u = take(nn * 4);
+  L.chunks = take(nn * 16);
+  L.heavy_info = take((size_t)L.heavy_cap * 8);
   L.pos_sorted = take(nn * 4);
   L.acc64 = take((size_t)L.heavy_cap * dim * 8);
   L.arrive = take((size_t)L.heavy_cap * 4);
@@ -460,7 +512,7 @@ cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
     k_bw_fill<<<p.ntiles, kThreads, 0, s>>>(p);
   }
   const int vec = p.T.row_dtype == MT_F32 ? 4 : 8;
-  int team = 1, shift = 0;
+  int team = 1 << kMinTeamShift, shift = kMinTeamShift;
   while (team < 32 && team * vec < (int)p.T.dim) {
     team <<= 1;
     ++shift;

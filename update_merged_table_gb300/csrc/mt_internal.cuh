@@ -194,16 +194,19 @@ __device__ __forceinline__ void push_row_warp(const TableDev& T, unsigned mask, 
 // Find `key` along its probe sequence h_t = (h0 + t*S) mod M (MTGenRec,
 // Theorem 1).  Returns the slot index, or -1 when an EMPTY slot or the probe
 // limit ends the chain first.  *t_end receives the probe index where the
-// search stopped and *t_tomb the first tombstone's probe index (or -1).
+// search stopped, *t_tomb the first tombstone's probe index (or -1) and
+// *row the row of a found key.  Each probe is one 16-byte load from L2.
 __device__ __forceinline__ long long find_slot(const TableDev& T, unsigned long long key, long long* t_end,
-                                               long long* t_tomb) {
+                                               long long* t_tomb, int32_t* row) {
   unsigned long long s = home_slot(T, key);
   long long first_tomb = -1;
   for (uint32_t t = 0; t < T.max_probes; ++t) {
-    const unsigned long long k = load_key_relaxed(&T.slots[s].key);
+    const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&T.slots[s]));
+    const unsigned long long k = sv.x;
     if (k == key) {
       *t_end = t;
       *t_tomb = first_tomb;
+      *row = (int32_t)(uint32_t)(sv.y & 0xFFFFFFFFull);
       return (long long)s;
     }
     if (k == kEmpty) {

@@ -74,12 +74,11 @@ struct BackwardParams {
   float one_minus_b1, one_minus_b2;
   float* gsum_out;
   // workspace
-  int32_t* bsum;        // [nblk * 3] per scan block: sum of counts, chunks, heavy
+  int32_t* bsum;        // [nblk * 3] per scan block: sum of counts, chunks, multi-chunk uniques
   int32_t* boff;        // [(nblk + 1) * 3] exclusive offsets (+ totals)
-  int32_t* cursor;      // [n] segment start, advanced to the segment end by the fill
-  int32_t* chunk_off;   // [n] first chunk of each unique
-  int32_t* heavy_idx;   // [n] index among multi-chunk uniques, or -1
-  int32_t* chunk_u;     // [n] unique of each chunk
+  int32_t* cursor;      // [n] segment start of each unique, advanced to its end by the fill
+  int4* chunks;         // [n] chunk descriptors {start, end, row, u or -(heavy index + 1)}
+  int2* heavy_info;     // [heavy_cap] {u, chunks} of each multi-chunk unique
   int32_t* pos_sorted;  // [n] positions grouped by unique
   double* acc64;        // [heavy_cap * d] cross-chunk sums of multi-chunk uniques
   int32_t* arrive;      // [heavy_cap] chunks finished per multi-chunk unique
@@ -88,7 +87,7 @@ struct BackwardParams {
 };
 
 struct BackwardWsLayout {
-  size_t bsum, boff, cursor, chunk_off, heavy_idx, chunk_u, pos_sorted, acc64, arrive, total;
+  size_t bsum, boff, cursor, chunks, heavy_info, pos_sorted, acc64, arrive, total;
   long long heavy_cap;
   int nblk, ntiles;
 };

@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   __shared__ uint32_t s_oslot[kTile];  // scratch slot of owner j
   __shared__ int32_t s_orow[kTile];    // table row of owner j
   __shared__ int32_t s_new[kTile];     // owners that inserted a fresh row
+  __shared__ unsigned long long s_okey[kTile];  // key of owner j
   __shared__ int s_nnew;
 
   const int tile = blockIdx.x, tid = threadIdx.x;
@@ -226,14 +227,18 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   // owners, in local (first-occurrence) order
   uint32_t flags = 0;
   uint32_t sl[kPPT];
+  unsigned long long key[kPPT];
   int c = 0;
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int l = tid * kPPT + k;
     sl[k] = 0;
+    key[k] = 0;
     if (l < L) {
       sl[k] = p.lsslot[lb + l];
-      if (p.scratch[sl[k]].minpos == p.lfirst[lb + l]) {
+      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.scratch[sl[k]]));
+      key[k] = sv.x;
+      if ((uint32_t)(sv.y & 0xFFFFFFFFull) == p.lfirst[lb + l]) {  // minpos == first position
         flags |= 1u << k;
         ++c;
       }
@@ -245,11 +250,11 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   for (int k = 0; k < kPPT; ++k) {
     if (flags & (1u << k)) {
       const int u = off + j;
-      ScratchSlot* ss = &p.scratch[sl[k]];
-      ss->uidx = u;
-      p.unique_keys[u] = ss->key;
+      p.scratch[sl[k]].uidx = u;
+      p.unique_keys[u] = key[k];
       p.counts[u] = 0;
       s_oslot[j] = sl[k];
+      s_okey[j] = key[k];
       ++j;
     }
   }
@@ -264,12 +269,10 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
     bool claimed = false;
     unsigned long long cs = 0;
     if (act) {
-      const unsigned long long key = p.scratch[s_oslot[jj]].key;
+      const unsigned long long key = s_okey[jj];
       long long t_end, t_tomb;
-      const long long s = find_slot(p.T, key, &t_end, &t_tomb);
-      if (s >= 0) {
-        row = p.T.slots[s].row;
-      } else if (p.insert_missing) {
+      const long long s = find_slot(p.T, key, &t_end, &t_tomb, &row);
+      if (s < 0 && p.insert_missing) {
         // the key is absent and no other thread inserts it (it is unique in
         // the batch): take the first tombstone of its chain, else the EMPTY
         // slot that ended the chain, else the next free slot after them
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   const int nteams = kThreads / team, my_team = tid / team, lt = tid % team;
   for (int q = my_team; q < nnew; q += nteams) {
     const int jj = s_new[q];
-    init_row_coop(p.T, s_orow[jj], p.scratch[s_oslot[jj]].key, lt, team);
+    init_row_coop(p.T, s_orow[jj], s_okey[jj], lt, team);
   }
 }
 

@@ -29,7 +29,8 @@ __global__ void k_erase_find(const TableDev T, const unsigned long long* keys, l
     long long s = -1;
     if (key != kEmpty && key != kTomb) {
       long long t_end, t_tomb;
-      s = find_slot(T, key, &t_end, &t_tomb);
+      int32_t row;
+      s = find_slot(T, key, &t_end, &t_tomb, &row);
     }
     ws_slot[i] = (int32_t)s;
   }
