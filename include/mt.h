@@ -182,8 +182,11 @@ size_t mt_backward_workspace_bytes(const mt_table* t, int64_t n);
  * rounded once to fp32; then, for every unique key with a row, one Adam step
  * in fp32 with the table's step counter t (advanced once per call):
  *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g*g;
- *   w = w - lr * (m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps)
- * (1-b1, 1-b2, 1-b1^t, 1-b2^t evaluated in double, then rounded to fp32).
+ *   w = w - step_size * (m / (sqrt(v) * inv_sqrt_bc2 + eps))
+ * with step_size = lr / (1-b1^t) and inv_sqrt_bc2 = 1 / sqrt(1-b2^t), i.e.
+ * Kingma & Ba's m_hat / (sqrt(v_hat) + eps) with the bias corrections folded
+ * into per-step scalars (1-b1, 1-b2 and both scalars evaluated in double,
+ * then rounded to fp32; every per-element operation rounds once).
  * Rows absent from the batch are not touched.
  *  grads      device [n, d] of grad_dtype (MT_F32 or MT_BF16).
  *  gsum_out   device fp32 [n, d] or NULL: the first U rows receive g_u.

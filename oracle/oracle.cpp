@@ -385,10 +385,16 @@ int orc_backward_adam(void* h, const void* grads, int grad_dtype, float lr, floa
   }
   t->step += 1;
   // Optimizer constants: computed in double, each rounded once to fp32.
+  // Kingma & Ba's m_hat / (sqrt(v_hat) + eps) with m_hat = m / (1 - b1^t) and
+  // sqrt(v_hat) = sqrt(v) / sqrt(1 - b2^t): the two bias corrections enter as
+  // the per-step scalars step_size = lr / (1 - b1^t) and
+  // inv_sqrt_bc2 = 1 / sqrt(1 - b2^t).
   const float omb1 = (float)(1.0 - (double)beta1);
   const float omb2 = (float)(1.0 - (double)beta2);
-  const float bc1 = (float)(1.0 - std::pow((double)beta1, (double)t->step));
-  const float bc2 = (float)(1.0 - std::pow((double)beta2, (double)t->step));
+  const double bc1 = 1.0 - std::pow((double)beta1, (double)t->step);
+  const double bc2 = 1.0 - std::pow((double)beta2, (double)t->step);
+  const float step_size = (float)((double)lr / bc1);
+  const float inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
   for (int64_t u = 0; u < U; ++u) {
     auto it = t->rows.find(t->last_uniq[u]);
     if (it != t->rows.end()) t->touch(t->last_uniq[u], it->second);
@@ -399,10 +405,8 @@ int orc_backward_adam(void* h, const void* grads, int grad_dtype, float lr, floa
       Row& r = it->second;
       float m = beta1 * r.m[j] + omb1 * g;
       float v = beta2 * r.v[j] + omb2 * (g * g);
-      float mhat = m / bc1;
-      float vhat = v / bc2;
-      float den = std::sqrt(vhat) + eps;
-      float upd = lr * (mhat / den);
+      float den = std::sqrt(v) * inv_sqrt_bc2 + eps;
+      float upd = step_size * (m / den);
       r.m[j] = m;
       r.v[j] = v;
       r.emb[j] = store_round(r.emb[j] - upd, t->dtype);
