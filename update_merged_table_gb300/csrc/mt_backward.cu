@@ -70,6 +70,8 @@ __device__ __forceinline__ void block_scan3(const int v[3], int ex[3], int tot[3
 
 __device__ __forceinline__ int nchunks(int c) { return (c + kChunk - 1) / kChunk; }
 
+// Sums over a block of uniques: positions, chunks of heavy (multi-chunk)
+// uniques, heavy uniques.  Block 0 advances the table's step counter.
 __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
   if (blockIdx.x == 0 && threadIdx.x == 0) p.T.hdr->step += 1;
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
     const int c = p.counts[u];
     const int nc = nchunks(c);
     v[0] += c;
-    v[1] += nc;
+    v[1] += nc > 1 ? nc : 0;
     v[2] += nc > 1;
   }
   int ex[3], tot[3];
@@ -90,23 +92,15 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
 
 constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_offsets
 
-// Per unique: segment start (cursor).  Per chunk: a descriptor {start, end,
-// row, u or -(heavy index + 1)}, written cooperatively by the block so a hot
-// unique with thousands of chunks costs no single thread more than its share.
-// Per multi-chunk unique: {u, chunks}, a zero arrival count and zeroed fp64
-// accumulators.
+// Per unique: segment start (cursor).  A light unique (one chunk) gets its
+// descriptor {start, end, row, u} at TH + its rank among light uniques (TH =
+// chunks of all heavy uniques, which come first); a heavy unique gets
+// {u, chunks, segment start, first chunk} for k_bw_heavy.
 __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
-  __shared__ int s_chrel[kScanTile + 1];  // first chunk of each local unique, relative to the block
-  __shared__ int s_seg[kScanTile];        // segment start, relative to the block
-  __shared__ int s_cnt[kScanTile];
-  __shared__ int s_row[kScanTile];
-  __shared__ int s_hrel[kScanTile];       // multi-chunk index relative to the block, or -1
   const long long U = *p.num_unique;
-  const long long ublk = (long long)blockIdx.x * kScanTile;
-  if (ublk >= U) return;  // uniform over the block
-  const int tid = threadIdx.x;
-  const long long u0 = ublk + (long long)tid * kUPT;
+  if ((long long)blockIdx.x * kScanTile >= U) return;  // uniform over the block
+  const long long u0 = (long long)blockIdx.x * kScanTile + (long long)threadIdx.x * kUPT;
   int c[kUPT];
   int v[3] = {0, 0, 0};
 #pragma unroll
@@ -114,54 +108,50 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
     c[k] = u0 + k < U ? p.counts[u0 + k] : 0;
     const int nc = nchunks(c[k]);
     v[0] += c[k];
-    v[1] += nc;
+    v[1] += nc > 1 ? nc : 0;
     v[2] += nc > 1;
   }
   int ex[3], tot[3];
   block_scan3<kScanThreads>(v, ex, tot, s_warp);
-  const int seg_base = p.boff[(size_t)blockIdx.x * 3 + 0];
-  const int ch_base = p.boff[(size_t)blockIdx.x * 3 + 1];
-  const int hv_base = p.boff[(size_t)blockIdx.x * 3 + 2];
-  int seg = ex[0], ch = ex[1], hv = ex[2];
+  int seg = ex[0] + p.boff[(size_t)blockIdx.x * 3 + 0];
+  int hch = ex[1] + p.boff[(size_t)blockIdx.x * 3 + 1];
+  int hv = ex[2] + p.boff[(size_t)blockIdx.x * 3 + 2];
+  const int TH = p.boff[(size_t)p.nblk * 3 + 1];
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
-    const int ul = tid * kUPT + k;
     const long long u = u0 + k;
+    if (u >= U) break;
     const int nc = nchunks(c[k]);
-    s_chrel[ul] = ch;
-    s_seg[ul] = seg;
-    s_cnt[ul] = c[k];
-    s_hrel[ul] = nc > 1 ? hv : -1;
-    s_row[ul] = u < U ? p.unique_rows[u] : -1;
-    if (u < U) p.cursor[u] = seg_base + seg;
-    ch += nc;
+    p.cursor[u] = seg;
+    if (nc == 1) {
+      p.chunks[TH + (int)(u - hv)] = make_int4(seg, seg + c[k], p.unique_rows[u], (int)u);
+    } else {
+      p.heavy_info[hv] = make_int4((int)u, nc, seg, hch);
+      ++hv;
+      hch += nc;
+    }
     seg += c[k];
-    hv += nc > 1;
   }
-  if (tid == 0) s_chrel[kScanTile] = tot[1];
-  __syncthreads();
-  for (int cc = tid; cc < tot[1]; cc += kScanThreads) {
-    int lo = 0, hi = kScanTile;  // s_chrel[lo] <= cc < s_chrel[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_chrel[mid] <= cc) lo = mid; else hi = mid;
+}
+
+// Descriptors of the heavy uniques' chunks, their zeroed fp64 accumulators
+// and arrival counts; one block per heavy unique at a time, so a unique with
+// thousands of chunks is written by a whole block.
+__global__ void __launch_bounds__(256) k_bw_heavy(const BackwardParams p) {
+  const int H = p.boff[(size_t)p.nblk * 3 + 2];
+  const int d = (int)p.T.dim;
+  for (int h = blockIdx.x; h < H; h += gridDim.x) {
+    const int4 hi = p.heavy_info[h];  // {u, chunks, segment start, first chunk}
+    const int cnt = p.counts[hi.x];
+    const int row = p.unique_rows[hi.x];
+    for (int k = threadIdx.x; k < hi.y; k += blockDim.x) {
+      const int start = hi.z + k * kChunk;
+      p.chunks[hi.w + k] = make_int4(start, min(start + kChunk, hi.z + cnt), row, -(h + 1));
     }
-    const int k = cc - s_chrel[lo];
-    const int start = seg_base + s_seg[lo] + k * kChunk;
-    const int end = min(start + kChunk, seg_base + s_seg[lo] + s_cnt[lo]);
-    const int w = s_hrel[lo] < 0 ? (int)(ublk + lo) : -(hv_base + s_hrel[lo] + 1);
-    p.chunks[ch_base + cc] = make_int4(start, end, s_row[lo], w);
+    double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)h * d);
+    for (int q = threadIdx.x; q < d / 2; q += blockDim.x) a[q] = make_double2(0.0, 0.0);
+    if (threadIdx.x == 0) p.arrive[h] = 0;
   }
-  for (int ul = tid; ul < kScanTile; ul += kScanThreads) {
-    if (s_hrel[ul] >= 0) {
-      const int h = hv_base + s_hrel[ul];
-      p.heavy_info[h] = make_int2((int)(ublk + ul), nchunks(s_cnt[ul]));
-      p.arrive[h] = 0;
-    }
-  }
-  const int d2 = (int)p.T.dim / 2;
-  double2* acc = reinterpret_cast<double2*>(p.acc64 + (size_t)hv_base * p.T.dim);
-  for (int it = tid; it < tot[2] * d2; it += kScanThreads) acc[it] = make_double2(0.0, 0.0);
 }
 
 // Positions grouped by unique: each tile groups its positions by unique in
@@ -233,113 +223,98 @@ __device__ __forceinline__ void two_sum_add(float& hi, float& lo, float x) {
   lo = __fadd_rn(lo, e);
 }
 
+// Raw gradient words of one lane's VEC columns: VEC fp32 words, or VEC/2
+// words holding two bf16 each.  Kept raw while in flight (fewer registers)
+// and widened to fp32 only when accumulated.
 template <int GD, int VEC>
-__device__ __forceinline__ void load_grad(const void* grads, long long pos, int d, int col, float g[VEC]) {
-  if (GD == MT_F32) {
-    const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(grads) + (size_t)pos * d + col);
+struct GradRaw {
+  static constexpr int W = GD == MT_F32 ? VEC : VEC / 2;
+  uint32_t w[W];
+};
+
+template <int GD, int VEC>
+__device__ __forceinline__ void load_grad_raw(const void* grads, long long pos, int d, int col, GradRaw<GD, VEC>& g) {
+  constexpr int W = GradRaw<GD, VEC>::W;
+  const char* base = reinterpret_cast<const char*>(grads) + ((size_t)pos * d + col) * (GD == MT_F32 ? 4 : 2);
+  if (W >= 4) {
 #pragma unroll
-    for (int q = 0; q < VEC / 4; ++q) {
-      const float4 t = __ldg(src + q);
-      g[4 * q + 0] = t.x;
-      g[4 * q + 1] = t.y;
-      g[4 * q + 2] = t.z;
-      g[4 * q + 3] = t.w;
+    for (int q = 0; q < W / 4; ++q) {
+      const uint4 t = __ldg(reinterpret_cast<const uint4*>(base) + q);
+      g.w[4 * q] = t.x; g.w[4 * q + 1] = t.y; g.w[4 * q + 2] = t.z; g.w[4 * q + 3] = t.w;
     }
   } else {
-    const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(grads) + (size_t)pos * d + col;
-    if (VEC == 8) {
-      const uint4 t = __ldg(reinterpret_cast<const uint4*>(b));
-      const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
-        g[2 * q] = f.x;
-        g[2 * q + 1] = f.y;
-      }
-    } else {
-      const uint2 t = __ldg(reinterpret_cast<const uint2*>(b));
-      const uint32_t w[2] = {t.x, t.y};
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[q]));
-        g[2 * q] = f.x;
-        g[2 * q + 1] = f.y;
-      }
-    }
+    const uint2 t = __ldg(reinterpret_cast<const uint2*>(base));
+    g.w[0] = t.x;
+    g.w[W - 1] = t.y;
   }
 }
 
-// Adam state of columns [col, col + VEC) of a row: w (as fp32), m, v.
-template <int RD, int VEC>
-struct RowCols {
-  float w[VEC], m[VEC], v[VEC];
-};
+template <int GD, int VEC>
+__device__ __forceinline__ float grad_value(const GradRaw<GD, VEC>& g, int j) {
+  if (GD == MT_F32) return __uint_as_float(g.w[j]);
+  const uint32_t w = g.w[j >> 1];
+  return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));  // bf16 -> fp32 is exact
+}
 
+// One Adam step on columns [col, col + VEC) of a row, every operation
+// rounded once: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+// w -= step_size * m / (sqrt(v) * inv_sqrt_bc2 + eps).  The moments are
+// streamed four columns at a time to keep few registers live.
 template <int RD, int VEC>
-__device__ __forceinline__ void load_row_cols(const TableDev& T, int32_t row, int col, RowCols<RD, VEC>& r) {
-  const char* rec = row_ptr(T, row);
+__device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, int col, const float g[VEC],
+                                          float step_size, float inv_sqrt_bc2) {
+  char* rec = row_ptr(p.T, row);
+  float w[VEC];
   if (RD == MT_F32) {
     const float4* e = reinterpret_cast<const float4*>(rec) + col / 4;
 #pragma unroll
     for (int q = 0; q < VEC / 4; ++q) {
       const float4 t = e[q];
-      r.w[4 * q] = t.x; r.w[4 * q + 1] = t.y; r.w[4 * q + 2] = t.z; r.w[4 * q + 3] = t.w;
+      w[4 * q] = t.x; w[4 * q + 1] = t.y; w[4 * q + 2] = t.z; w[4 * q + 3] = t.w;
     }
   } else {
     const uint4 t = *(reinterpret_cast<const uint4*>(rec) + col / 8);
     const uint32_t ww[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[q]));
-      r.w[2 * q] = f.x;
-      r.w[2 * q + 1] = f.y;
+      w[2 * q] = __uint_as_float(ww[q] << 16);
+      w[2 * q + 1] = __uint_as_float(ww[q] & 0xFFFF0000u);
     }
   }
-  const float4* mp = reinterpret_cast<const float4*>(rec + T.emb_bytes) + col / 4;
-  const float4* vp = reinterpret_cast<const float4*>(rec + T.emb_bytes + T.mv_bytes) + col / 4;
-#pragma unroll
-  for (int q = 0; q < VEC / 4; ++q) {
-    const float4 a = mp[q], b = vp[q];
-    r.m[4 * q] = a.x; r.m[4 * q + 1] = a.y; r.m[4 * q + 2] = a.z; r.m[4 * q + 3] = a.w;
-    r.v[4 * q] = b.x; r.v[4 * q + 1] = b.y; r.v[4 * q + 2] = b.z; r.v[4 * q + 3] = b.w;
-  }
-}
-
-// One Adam step on the loaded columns, in the operation order of the update
-// rule with every operation rounded once, then the store.
-template <int RD, int VEC>
-__device__ __forceinline__ void adam_apply_store(const BackwardParams& p, int32_t row, int col, const float g[VEC],
-                                                 RowCols<RD, VEC>& r, float bc1, float bc2) {
-#pragma unroll
-  for (int j = 0; j < VEC; ++j) {
-    r.m[j] = __fadd_rn(__fmul_rn(p.beta1, r.m[j]), __fmul_rn(p.one_minus_b1, g[j]));
-    r.v[j] = __fadd_rn(__fmul_rn(p.beta2, r.v[j]), __fmul_rn(p.one_minus_b2, __fmul_rn(g[j], g[j])));
-    const float mhat = __fdiv_rn(r.m[j], bc1);
-    const float vhat = __fdiv_rn(r.v[j], bc2);
-    const float den = __fadd_rn(__fsqrt_rn(vhat), p.eps);
-    r.w[j] = __fsub_rn(r.w[j], __fmul_rn(p.lr, __fdiv_rn(mhat, den)));
-  }
-  char* rec = row_ptr(p.T, row);
   float4* mp = reinterpret_cast<float4*>(rec + p.T.emb_bytes) + col / 4;
   float4* vp = reinterpret_cast<float4*>(rec + p.T.emb_bytes + p.T.mv_bytes) + col / 4;
 #pragma unroll
   for (int q = 0; q < VEC / 4; ++q) {
-    mp[q] = make_float4(r.m[4 * q], r.m[4 * q + 1], r.m[4 * q + 2], r.m[4 * q + 3]);
-    vp[q] = make_float4(r.v[4 * q], r.v[4 * q + 1], r.v[4 * q + 2], r.v[4 * q + 3]);
+    const float4 m4 = mp[q], v4 = vp[q];
+    float m[4] = {m4.x, m4.y, m4.z, m4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = 4 * q + k;
+      m[k] = __fadd_rn(__fmul_rn(p.beta1, m[k]), __fmul_rn(p.one_minus_b1, g[j]));
+      v[k] = __fadd_rn(__fmul_rn(p.beta2, v[k]), __fmul_rn(p.one_minus_b2, __fmul_rn(g[j], g[j])));
+      const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v[k]), inv_sqrt_bc2), p.eps);
+      w[j] = __fsub_rn(w[j], __fmul_rn(step_size, __fdiv_rn(m[k], den)));
+    }
+    mp[q] = make_float4(m[0], m[1], m[2], m[3]);
+    vp[q] = make_float4(v[0], v[1], v[2], v[3]);
   }
   if (RD == MT_F32) {
     float4* e = reinterpret_cast<float4*>(rec) + col / 4;
 #pragma unroll
-    for (int q = 0; q < VEC / 4; ++q) e[q] = make_float4(r.w[4 * q], r.w[4 * q + 1], r.w[4 * q + 2], r.w[4 * q + 3]);
+    for (int q = 0; q < VEC / 4; ++q) e[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   } else {
     uint32_t ww[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(r.w[2 * q], r.w[2 * q + 1]);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(w[2 * q], w[2 * q + 1]);
       ww[q] = *reinterpret_cast<uint32_t*>(&b2);
     }
     *(reinterpret_cast<uint4*>(rec) + col / 8) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
   }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
 __device__ __forceinline__ void store_gsum(float* gsum_out, int u, int d, int col, const float* gs, int vec) {
@@ -350,44 +325,54 @@ __device__ __forceinline__ void store_gsum(float* gsum_out, int u, int d, int co
 constexpr int kMinTeamShift = 2;                              // teams of at least 4 lanes
 constexpr int kMaxTeams = 256 >> kMinTeamShift;               // per block
 
-// One team of 2^team_shift lanes per chunk descriptor.  The team stages the
-// chunk's positions in shared memory, prefetches the Adam row of a
-// single-chunk unique while the gradient rows load, accumulates in TwoSum
-// pairs, and either applies Adam (single-chunk unique) or adds its partial
-// sum to the unique's fp64 accumulator in L2, the last chunk applying Adam.
+// One team of 2^team_shift lanes per chunk descriptor (the next descriptor
+// is loaded while the current chunk runs).  The team stages the chunk's
+// positions in shared memory and starts pulling the Adam row of a light
+// unique into L2, accumulates the gradient rows in TwoSum pairs, and either
+// applies Adam (light unique) or adds its partial sum to the unique's fp64
+// accumulator in L2, the last chunk of the unique applying Adam.
 template <int RD, int GD>
-__global__ void __launch_bounds__(256) k_bw_reduce_adam(const BackwardParams p, int team_shift) {
+__global__ void __launch_bounds__(256, 4) k_bw_reduce_adam(const BackwardParams p, int team_shift) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;
-  constexpr int UNR = VEC == 8 ? 4 : 8;  // gradient rows in flight per lane
-  __shared__ float s_bc[2];
+  constexpr int UNR = 16 / GradRaw<GD, VEC>::W;  // gradient rows in flight per lane (16 raw words)
+  __shared__ float s_scal[2];
   __shared__ int s_pos[kMaxTeams * kChunk];
   if (threadIdx.x == 0) {
     const double t = (double)p.T.hdr->step;
-    s_bc[0] = (float)(1.0 - pow((double)p.beta1, t));
-    s_bc[1] = (float)(1.0 - pow((double)p.beta2, t));
+    const double bc1 = 1.0 - pow((double)p.beta1, t);
+    const double bc2 = 1.0 - pow((double)p.beta2, t);
+    s_scal[0] = (float)((double)p.lr / bc1);
+    s_scal[1] = (float)(1.0 / sqrt(bc2));
   }
   __syncthreads();
-  const float bc1 = s_bc[0], bc2 = s_bc[1];
+  const float step_size = s_scal[0], inv_sqrt_bc2 = s_scal[1];
 
   const int team = 1 << team_shift;
   const int lane = threadIdx.x & 31;
   const int lt = lane & (team - 1);
   const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << (lane & ~(team - 1)));
   int* my_pos = s_pos + (threadIdx.x >> team_shift) * kChunk;
-  const long long total_chunks = p.boff[(size_t)p.nblk * 3 + 1];
+  const long long total_chunks =
+      (long long)p.boff[(size_t)p.nblk * 3 + 1] + (*p.num_unique - p.boff[(size_t)p.nblk * 3 + 2]);
   const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
   const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
   const int d = (int)p.T.dim;
   const bool one_pass = d <= team * VEC;
+  const int col0 = lt * VEC;
 
+  int4 next = gteam < total_chunks ? __ldg(&p.chunks[gteam]) : make_int4(0, 0, -1, 0);
   for (long long c = gteam; c < total_chunks; c += nteam) {
-    const int4 dsc = __ldg(&p.chunks[c]);
+    const int4 dsc = next;
+    if (c + nteam < total_chunks) next = __ldg(&p.chunks[c + nteam]);
     const int start = dsc.x, cnt = dsc.y - dsc.x, row = dsc.z;
     const bool heavy = dsc.w < 0;
+    if (!heavy && row >= 0 && col0 < d) {
+      const char* rec = row_ptr(p.T, row);
+      prefetch_l2(rec + (size_t)col0 * (RD == MT_F32 ? 4 : 2));
+      prefetch_l2(rec + p.T.emb_bytes + (size_t)col0 * 4);
+      prefetch_l2(rec + p.T.emb_bytes + p.T.mv_bytes + (size_t)col0 * 4);
+    }
     for (int q = lt; q < cnt; q += team) my_pos[q] = __ldg(&p.pos_sorted[start + q]);
-    RowCols<RD, VEC> rc;
-    const int col0 = lt * VEC;
-    if (one_pass && !heavy && row >= 0 && col0 < d) load_row_cols<RD, VEC>(p.T, row, col0, rc);
     __syncwarp(team_mask);
 
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
@@ -397,15 +382,15 @@ __global__ void __launch_bounds__(256) k_bw_reduce_adam(const BackwardParams p, 
 #pragma unroll
       for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
       for (int q0 = 0; q0 < cnt; q0 += UNR) {
-        float g[UNR][VEC];
+        GradRaw<GD, VEC> g[UNR];
 #pragma unroll
         for (int r = 0; r < UNR; ++r)
-          if (q0 + r < cnt) load_grad<GD, VEC>(p.grads, my_pos[q0 + r], d, col, g[r]);
+          if (q0 + r < cnt) load_grad_raw<GD, VEC>(p.grads, my_pos[q0 + r], d, col, g[r]);
 #pragma unroll
         for (int r = 0; r < UNR; ++r)
           if (q0 + r < cnt) {
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], g[r][j]);
+            for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g[r], j));
           }
       }
       if (!heavy) {
@@ -413,10 +398,7 @@ __global__ void __launch_bounds__(256) k_bw_reduce_adam(const BackwardParams p, 
 #pragma unroll
         for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
         if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
-        if (row >= 0) {
-          if (!one_pass) load_row_cols<RD, VEC>(p.T, row, col, rc);
-          adam_apply_store<RD, VEC>(p, row, col, gs, rc, bc1, bc2);
-        }
+        if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
       } else {
         double* a = p.acc64 + (size_t)(-dsc.w - 1) * d + col;
 #pragma unroll
@@ -430,7 +412,7 @@ __global__ void __launch_bounds__(256) k_bw_reduce_adam(const BackwardParams p, 
       int old = 0;
       if (lt == 0) old = atomicAdd(&p.arrive[h], 1);
       old = __shfl_sync(team_mask, old, 0, team);
-      const int2 hinfo = __ldg(&p.heavy_info[h]);
+      const int4 hinfo = __ldg(&p.heavy_info[h]);
       if (old == hinfo.y - 1) {  // last chunk of this unique: every partial sum has landed
         __threadfence();
         for (int c0 = 0; c0 < d; c0 += team * VEC) {
@@ -441,10 +423,7 @@ __global__ void __launch_bounds__(256) k_bw_reduce_adam(const BackwardParams p, 
 #pragma unroll
           for (int j = 0; j < VEC; ++j) gs[j] = (float)__ldcg(a + j);
           if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
-          if (row >= 0) {
-            load_row_cols<RD, VEC>(p.T, row, col, rc);
-            adam_apply_store<RD, VEC>(p, row, col, gs, rc, bc1, bc2);
-          }
+          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
         }
       }
     }
@@ -488,7 +467,7 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
   L.boff = take(((size_t)L.nblk + 1) * 3 * 4);
   L.cursor = take(nn * 4);
   L.chunks = take(nn * 16);
-  L.heavy_info = take((size_t)L.heavy_cap * 8);
+  L.heavy_info = take((size_t)L.heavy_cap * 16);
   L.pos_sorted = take(nn * 4);
   L.acc64 = take((size_t)L.heavy_cap * dim * 8);
   L.arrive = take((size_t)L.heavy_cap * 4);
@@ -506,6 +485,10 @@ cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
   {
     MT_LAUNCH("k_bw_offsets", s);
     k_bw_offsets<<<p.nblk, kScanThreads, 0, s>>>(p);
+  }
+  {
+    MT_LAUNCH("k_bw_heavy", s);
+    k_bw_heavy<<<4 * 152, 256, 0, s>>>(p);
   }
   if (p.ntiles > 0) {
     MT_LAUNCH("k_bw_fill", s);

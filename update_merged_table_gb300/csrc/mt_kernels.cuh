@@ -11,6 +11,8 @@ namespace mt {
 constexpr int kTile = 2048;              // positions per lookup tile (one CTA)
 constexpr int kThreads = 256;            // threads per lookup CTA
 constexpr int kPPT = kTile / kThreads;   // positions per thread
+constexpr int kThreadsA = 512;           // threads per dedup CTA (k_dedup_claim)
+constexpr int kPPTA = kTile / kThreadsA; // positions per dedup thread
 constexpr int kHS = 2 * kTile;           // shared-memory hash slots of stage 1
 constexpr uint16_t kNoIdx = 0xFFFF;
 
@@ -74,14 +76,15 @@ struct BackwardParams {
   float one_minus_b1, one_minus_b2;
   float* gsum_out;
   // workspace
-  int32_t* bsum;        // [nblk * 3] per scan block: sum of counts, chunks, multi-chunk uniques
+  int32_t* bsum;        // [nblk * 3] per scan block: sums of counts, heavy chunks, heavy uniques
   int32_t* boff;        // [(nblk + 1) * 3] exclusive offsets (+ totals)
   int32_t* cursor;      // [n] segment start of each unique, advanced to its end by the fill
-  int4* chunks;         // [n] chunk descriptors {start, end, row, u or -(heavy index + 1)}
-  int2* heavy_info;     // [heavy_cap] {u, chunks} of each multi-chunk unique
+  int4* chunks;         // [n] descriptors {start, end, row, u or -(heavy index + 1)}:
+                        //     the chunks of multi-chunk ("heavy") uniques first, then one per light unique
+  int4* heavy_info;     // [heavy_cap] {u, chunks, segment start, first chunk} of each heavy unique
   int32_t* pos_sorted;  // [n] positions grouped by unique
-  double* acc64;        // [heavy_cap * d] cross-chunk sums of multi-chunk uniques
-  int32_t* arrive;      // [heavy_cap] chunks finished per multi-chunk unique
+  double* acc64;        // [heavy_cap * d] cross-chunk sums of heavy uniques
+  int32_t* arrive;      // [heavy_cap] chunks finished per heavy unique
   int nblk;
   int ntiles;
 };

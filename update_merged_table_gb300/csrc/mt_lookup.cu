@@ -21,8 +21,10 @@
 //                    publish them in the scratch hash, find or insert their
 //                    key in the table (odd-step probing, tombstone reuse,
 //                    warp-aggregated row pops) and initialise fresh rows.
-//  k_expand_gather   per position: inverse index; per tile-local unique:
-//                    counts; then the 16-byte vectorised row gather.
+//  k_expand          per tile-local unique: its unique index and counts;
+//                    per position: the inverse index.
+//  k_gather          the 16-byte vectorised row gather, grid-stride over
+//                    the batch with four independent items per thread.
 #include "mt_kernels.cuh"
 
 namespace mt {
@@ -75,7 +77,7 @@ __device__ __forceinline__ int block_sum(int v, int* s_warp) {
 
 constexpr size_t kSmemA = kHS * 8 + kHS * 4 + kTile * 4 + kTile * 2 + (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
 
-__global__ void __launch_bounds__(kThreads) k_dedup_claim(const LookupParams p) {
+__global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHS] stage-1 hash keys
   uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHS);              // [kHS] first local position, then local index
@@ -83,26 +85,26 @@ __global__ void __launch_bounds__(kThreads) k_dedup_claim(const LookupParams p) 
   uint16_t* s_pslot = reinterpret_cast<uint16_t*>(s_item + kTile);         // [kTile] hash slot of each position
   long long* s_off = reinterpret_cast<long long*>(s_pslot + kTile);        // [F + 1]
   unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
-  __shared__ int s_warp[kThreads / 32];
+  __shared__ int s_warp[kThreadsA / 32];
 
   const int tile = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
   const long long base = (long long)tile * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
 
-  for (int i = tid; i < kHS; i += kThreads) {
+  for (int i = tid; i < kHS; i += kThreadsA) {
     s_key[i] = kEmpty;
     s_min[i] = 0xFFFFFFFFu;
   }
-  for (int i = tid; i <= p.F; i += kThreads) s_off[i] = p.feat_off[i];
-  for (int i = tid; i < p.F; i += kThreads) s_tid[i] = p.table_ids[i];
+  for (int i = tid; i <= p.F; i += kThreadsA) s_off[i] = p.feat_off[i];
+  for (int i = tid; i < p.F; i += kThreadsA) s_tid[i] = p.table_ids[i];
   __syncthreads();
 
   // ---- encode + stage 1 (tile-local dedup) ----
   bool bad = false;
 #pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    const int lp = k * kThreads + tid;  // a warp covers 32 consecutive positions
+  for (int k = 0; k < kPPTA; ++k) {
+    const int lp = k * kThreadsA + tid;  // a warp covers 32 consecutive positions
     const bool in = lp < cnt;
     unsigned long long key = kEmpty;
     bool valid = false;
@@ -146,8 +148,8 @@ __global__ void __launch_bounds__(kThreads) k_dedup_claim(const LookupParams p) 
   uint32_t flags = 0;
   int c = 0;
 #pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    const int lp = tid * kPPT + k;
+  for (int k = 0; k < kPPTA; ++k) {
+    const int lp = tid * kPPTA + k;
     if (lp < cnt) {
       const uint16_t sl = s_pslot[lp];
       if (sl != kNoIdx && s_min[sl] == (uint32_t)lp) {
@@ -157,11 +159,11 @@ __global__ void __launch_bounds__(kThreads) k_dedup_claim(const LookupParams p) 
     }
   }
   int L;
-  int l = block_exclusive_scan<kThreads>(c, s_warp, &L);  // every s_min read above precedes its barriers
+  int l = block_exclusive_scan<kThreadsA>(c, s_warp, &L);  // every s_min read above precedes its barriers
 #pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
+  for (int k = 0; k < kPPTA; ++k) {
     if (flags & (1u << k)) {
-      const int lp = tid * kPPT + k;
+      const int lp = tid * kPPTA + k;
       const uint16_t sl = s_pslot[lp];
       s_min[sl] = (uint32_t)l;
       s_item[l] = ((uint32_t)sl << 16) | (uint32_t)lp;
@@ -171,14 +173,14 @@ __global__ void __launch_bounds__(kThreads) k_dedup_claim(const LookupParams p) 
   __syncthreads();
 
   uint16_t* lidx = p.lidx + base;
-  for (int lp = tid; lp < cnt; lp += kThreads) {
+  for (int lp = tid; lp < cnt; lp += kThreadsA) {
     const uint16_t sl = s_pslot[lp];
     lidx[lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
   }
 
   // ---- stage 2: claim every local unique in the global scratch hash ----
   const size_t lb = (size_t)tile * kTile;
-  for (int li = tid; li < L; li += kThreads) {
+  for (int li = tid; li < L; li += kThreadsA) {
     const uint32_t it = s_item[li];
     const unsigned long long key = s_key[it >> 16];
     const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_expand_gather(const LookupParams p) {
+__global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
   __shared__ int32_t s_lcnt[kTile];
   __shared__ int32_t s_u[kTile];
   __shared__ int32_t s_row[kTile];
@@ -363,32 +365,44 @@ __global__ void __launch_bounds__(kThreads) k_expand_gather(const LookupParams p
     const uint16_t li = s_pl[lp];
     p.inverse[base + lp] = li == kNoIdx ? -1 : s_u[li];
   }
-  if (p.out_rows == nullptr) return;
+}
 
-  // gather: 16-byte items (position, vector), consecutive threads on
-  // consecutive items, four independent items in flight per thread
+// out[i] = row of unique inverse[i] (zeros for an invalid ID or an absent
+// key): 16-byte items (position, vector), consecutive threads on consecutive
+// items, four independent items in flight per thread, grid-stride over the
+// whole batch so every SM stays busy to the end.
+__global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
   const int vec16 = (int)(p.T.emb_bytes / 16);
   const int vshift = (vec16 & (vec16 - 1)) == 0 ? __ffs(vec16) - 1 : -1;
-  const int total = cnt * vec16;
-  uint4* out = reinterpret_cast<uint4*>(p.out_rows) + (size_t)base * vec16;
+  const long long total = p.n * vec16;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  uint4* out = reinterpret_cast<uint4*>(p.out_rows);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  for (int i0 = tid; i0 < total; i0 += 4 * kThreads) {
+  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+    int32_t row[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const long long it = i0 + k * stride;
+      row[k] = -1;
+      if (it < total) {
+        const long long i = vshift >= 0 ? (it >> vshift) : it / vec16;
+        const int32_t u = __ldg(&p.inverse[i]);
+        if (u >= 0) row[k] = __ldg(&p.unique_rows[u]);
+      }
+    }
     uint4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int it = i0 + k * kThreads;
+      const long long it = i0 + k * stride;
       v[k] = zero;
-      if (it < total) {
-        const int lp = vshift >= 0 ? (it >> vshift) : it / vec16;
-        const int cc = it - lp * vec16;
-        const uint16_t li = s_pl[lp];
-        const int32_t row = li == kNoIdx ? -1 : s_row[li];
-        if (row >= 0) v[k] = __ldg(reinterpret_cast<const uint4*>(row_ptr(p.T, row)) + cc);
+      if (it < total && row[k] >= 0) {
+        const long long i = vshift >= 0 ? (it >> vshift) : it / vec16;
+        v[k] = __ldg(reinterpret_cast<const uint4*>(row_ptr(p.T, row[k])) + (it - i * vec16));
       }
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int it = i0 + k * kThreads;
+      const long long it = i0 + k * stride;
       if (it < total) __stcs(out + it, v[k]);
     }
   }
@@ -463,7 +477,7 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_dedup_claim", s);
-    k_dedup_claim<<<p.ntiles, kThreads, kSmemA, s>>>(p);
+    k_dedup_claim<<<p.ntiles, kThreadsA, kSmemA, s>>>(p);
   }
   {
     MT_LAUNCH("k_count_owners", s);
@@ -476,8 +490,20 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
     k_assign_resolve<<<p.ntiles, kThreads, 0, s>>>(p);
   }
   {
-    MT_LAUNCH("k_expand_gather", s);
-    k_expand_gather<<<p.ntiles, kThreads, 0, s>>>(p);
+    MT_LAUNCH("k_expand", s);
+    k_expand<<<p.ntiles, kThreads, 0, s>>>(p);
+  }
+  if (p.out_rows != nullptr) {
+    static int grid = 0;
+    if (grid == 0) {
+      int dev = 0, sms = 0, per = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_gather, 256, 0);
+      grid = sms * (per > 0 ? per : 1);
+    }
+    MT_LAUNCH("k_gather", s);
+    k_gather<<<grid, 256, 0, s>>>(p);
   }
   return cudaGetLastError();
 }
