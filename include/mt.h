@@ -101,6 +101,9 @@ typedef struct {
   int32_t* counts;       /* [n]: first U entries: number of positions holding each unique key */
   int32_t* unique_rows;  /* [n]: first U entries: row of each unique key, -1 when it has none */
   int64_t* num_unique;   /* [1]: U */
+  int32_t* ranks;        /* [n] or NULL: rank of position i among the counts[inverse[i]] positions of its
+                            key, in an unspecified order (-1 for an invalid ID).  With ranks the backward
+                            groups positions by key without hashing them again. */
 } mt_lookup_result;
 
 /* Adam hyper-parameters (Meituan TensorFlow article, section 3.2 names Adam;

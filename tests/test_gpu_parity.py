@@ -350,3 +350,32 @@ def test_full_size_merged():
     tab = mt.Table(22, 32)
     ref = oracle.Table(22, 32)
     run_steps(tab, ref, [W.merged_batch(s) for s in range(3)])
+
+
+def test_ranks_are_a_permutation_per_key():
+    """ranks[i] enumerates the positions of each key: per key a permutation of 0..count-1."""
+    b = W.jagged_batch(4, users=64)
+    tab = mt.Table(16, 16)
+    res = tab.lookup(to_dev(b.ids), b.feat_offsets, b.table_ids)
+    U = res.U
+    inv = res.inverse[:b.n].cpu().numpy().astype(np.int64)
+    rk = res.ranks[:b.n].cpu().numpy().astype(np.int64)
+    cnt = res.counts[:U].cpu().numpy()
+    assert rk.min() >= 0 and np.all(rk < cnt[inv])
+    key = inv * (int(cnt.max()) + 1) + rk          # (unique, rank) pairs are all distinct
+    assert np.unique(key).size == b.n
+
+
+def test_backward_without_ranks_matches_with_ranks():
+    """Both ways of grouping positions by key give the same sums and rows."""
+    b = W.merged_batch(8, per_table=1024)
+    g = to_dev(W.grads_small_int(3, b.n, 32))
+    out = []
+    for ranks in (True, False):
+        tab = mt.Table(16, 32)
+        res = tab.new_result(b.n, ranks=ranks)
+        tab.lookup(to_dev(b.ids), b.feat_offsets, b.table_ids, result=res)
+        gs = tab.backward_adam(res, g, want_gsum=True)
+        emb, m, v = tab.read_rows(res.unique_rows[:res.U])
+        out.append((gs[:res.U].cpu().numpy(), emb.cpu().numpy()))
+    assert np.array_equal(out[0][0], out[1][0]) and np.array_equal(out[0][1], out[1][1])

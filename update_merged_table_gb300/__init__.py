@@ -49,7 +49,7 @@ class _Config(ctypes.Structure):
 
 class _Result(ctypes.Structure):
     _fields_ = [("unique_keys", ctypes.c_void_p), ("inverse", ctypes.c_void_p), ("counts", ctypes.c_void_p),
-                ("unique_rows", ctypes.c_void_p), ("num_unique", ctypes.c_void_p)]
+                ("unique_rows", ctypes.c_void_p), ("num_unique", ctypes.c_void_p), ("ranks", ctypes.c_void_p)]
 
 
 class _Adam(ctypes.Structure):
@@ -173,10 +173,11 @@ class LookupResult:
     num_unique: "object"    # int64 [1]
     rows: "object" = None   # [n, dim] row dtype, or None
     n: int = 0
+    ranks: "object" = None  # int32 [n] or None: rank of each position among its key's positions
 
     def as_struct(self) -> _Result:
         return _Result(_ptr(self.unique_keys), _ptr(self.inverse), _ptr(self.counts), _ptr(self.unique_rows),
-                       _ptr(self.num_unique))
+                       _ptr(self.num_unique), _ptr(self.ranks))
 
     @property
     def U(self) -> int:
@@ -240,7 +241,8 @@ class Table:
             self._ws[kind] = buf
         return buf
 
-    def new_result(self, n: int, gather: bool = True) -> LookupResult:
+    def new_result(self, n: int, gather: bool = True, ranks: bool = True) -> LookupResult:
+        """Result buffers for a batch of n IDs.  ranks=True lets the backward skip re-grouping positions."""
         torch = _torch()
         dev = self.device
         return LookupResult(
@@ -250,7 +252,8 @@ class Table:
             unique_rows=torch.empty(max(n, 1), dtype=torch.int32, device=dev),
             num_unique=torch.empty(1, dtype=torch.int64, device=dev),
             rows=torch.empty((n, self.dim), dtype=self.torch_row_dtype, device=dev) if gather else None,
-            n=n)
+            n=n,
+            ranks=torch.empty(max(n, 1), dtype=torch.int32, device=dev) if ranks else None)
 
     def lookup(self, ids, feat_offsets=None, table_ids=None, insert_missing: bool = True, gather: bool = True,
                result: LookupResult | None = None, stream=None) -> LookupResult:

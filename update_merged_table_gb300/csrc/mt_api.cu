@@ -78,7 +78,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MT_OK : MT_ECUDA; }
 bool valid_result(const mt_lookup_result* r) {
   return r != nullptr && r->unique_keys && r->inverse && r->counts && r->unique_rows && r->num_unique &&
          aligned(r->unique_keys, 16) && aligned(r->inverse, 16) && aligned(r->counts, 16) &&
-         aligned(r->unique_rows, 16) && aligned(r->num_unique, 8);
+         aligned(r->unique_rows, 16) && aligned(r->num_unique, 8) && aligned(r->ranks, 16);
 }
 
 }  // namespace
@@ -204,6 +204,7 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
   p.counts = res->counts;
   p.unique_rows = res->unique_rows;
   p.num_unique = reinterpret_cast<long long*>(res->num_unique);
+  p.ranks = res->ranks;
   if (n > 0) {
     p.scratch = reinterpret_cast<mt::ScratchSlot*>(w + L.scratch);
     p.scratch_mask = L.scratch_slots - 1;
@@ -240,6 +241,7 @@ int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const 
   p.T = t->dev;
   p.n = n;
   p.inverse = res->inverse;
+  p.ranks = res->ranks;
   p.counts = res->counts;
   p.unique_rows = res->unique_rows;
   p.num_unique = reinterpret_cast<const long long*>(res->num_unique);
@@ -262,6 +264,8 @@ int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const 
   p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
   p.nblk = L.nblk;
   p.ntiles = L.ntiles;
+  p.team_shift = mt::backward_team_shift(t->cfg.dim, (int)t->cfg.row_dtype);
+  p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
   const int rc = cuda_status(mt::launch_backward(p, as_stream(stream)));
   if (rc == MT_OK) t->step += 1;
   return rc;

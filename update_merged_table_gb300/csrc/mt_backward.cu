@@ -68,7 +68,9 @@ __device__ __forceinline__ void block_scan3(const int v[3], int ex[3], int tot[3
   __syncthreads();
 }
 
-__device__ __forceinline__ int nchunks(int c) { return (c + kChunk - 1) / kChunk; }
+// A unique with more than kChunk positions is "heavy": it is reduced in
+// warp-chunks of p.warp_chunk positions, each by one whole warp.
+__device__ __forceinline__ int warp_chunks(int c, int wc) { return c > kChunk ? (c + wc - 1) / wc : 0; }
 
 // Sums over a block of uniques: positions, chunks of heavy (multi-chunk)
 // uniques, heavy uniques.  Block 0 advances the table's step counter.
@@ -80,10 +82,9 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
   int v[3] = {0, 0, 0};
   for (long long u = u0 + threadIdx.x; u < U && u < u0 + kScanTile; u += kScanThreads) {
     const int c = p.counts[u];
-    const int nc = nchunks(c);
     v[0] += c;
-    v[1] += nc > 1 ? nc : 0;
-    v[2] += nc > 1;
+    v[1] += warp_chunks(c, p.warp_chunk);
+    v[2] += c > kChunk;
   }
   int ex[3], tot[3];
   block_scan3<kScanThreads>(v, ex, tot, s_warp);
@@ -92,10 +93,10 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
 
 constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_offsets
 
-// Per unique: segment start (cursor).  A light unique (one chunk) gets its
-// descriptor {start, end, row, u} at TH + its rank among light uniques (TH =
-// chunks of all heavy uniques, which come first); a heavy unique gets
-// {u, chunks, segment start, first chunk} for k_bw_heavy.
+// Per unique: segment start (cursor).  A light unique gets its team-chunk
+// descriptor {start, end, row, u} at HWC + its rank among light uniques (HWC
+// = warp-chunks of all heavy uniques, which come first); a heavy unique gets
+// {u, warp-chunks, segment start, first chunk} for k_bw_heavy.
 __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
   const long long U = *p.num_unique;
@@ -106,51 +107,51 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
     c[k] = u0 + k < U ? p.counts[u0 + k] : 0;
-    const int nc = nchunks(c[k]);
     v[0] += c[k];
-    v[1] += nc > 1 ? nc : 0;
-    v[2] += nc > 1;
+    v[1] += warp_chunks(c[k], p.warp_chunk);
+    v[2] += c[k] > kChunk;
   }
   int ex[3], tot[3];
   block_scan3<kScanThreads>(v, ex, tot, s_warp);
   int seg = ex[0] + p.boff[(size_t)blockIdx.x * 3 + 0];
   int hch = ex[1] + p.boff[(size_t)blockIdx.x * 3 + 1];
   int hv = ex[2] + p.boff[(size_t)blockIdx.x * 3 + 2];
-  const int TH = p.boff[(size_t)p.nblk * 3 + 1];
+  const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
     const long long u = u0 + k;
     if (u >= U) break;
-    const int nc = nchunks(c[k]);
     p.cursor[u] = seg;
-    if (nc == 1) {
-      p.chunks[TH + (int)(u - hv)] = make_int4(seg, seg + c[k], p.unique_rows[u], (int)u);
+    if (c[k] <= kChunk) {
+      p.chunks[HWC + (int)(u - hv)] = make_int4(seg, seg + c[k], p.unique_rows[u], (int)u);
     } else {
-      p.heavy_info[hv] = make_int4((int)u, nc, seg, hch);
+      const int nw = warp_chunks(c[k], p.warp_chunk);
+      p.heavy_info[hv] = make_int4((int)u, nw, seg, hch);
       ++hv;
-      hch += nc;
+      hch += nw;
     }
     seg += c[k];
   }
 }
 
-// Descriptors of the heavy uniques' chunks, their zeroed fp64 accumulators
-// and arrival counts; one block per heavy unique at a time, so a unique with
-// thousands of chunks is written by a whole block.
+// Warp-chunk descriptors of the heavy uniques, their zeroed fp64
+// accumulators and arrival counts; one block per heavy unique at a time.
 __global__ void __launch_bounds__(256) k_bw_heavy(const BackwardParams p) {
   const int H = p.boff[(size_t)p.nblk * 3 + 2];
   const int d = (int)p.T.dim;
   for (int h = blockIdx.x; h < H; h += gridDim.x) {
-    const int4 hi = p.heavy_info[h];  // {u, chunks, segment start, first chunk}
+    const int4 hi = p.heavy_info[h];  // {u, warp-chunks, segment start, first chunk}
     const int cnt = p.counts[hi.x];
     const int row = p.unique_rows[hi.x];
     for (int k = threadIdx.x; k < hi.y; k += blockDim.x) {
-      const int start = hi.z + k * kChunk;
-      p.chunks[hi.w + k] = make_int4(start, min(start + kChunk, hi.z + cnt), row, -(h + 1));
+      const int start = hi.z + k * p.warp_chunk;
+      p.chunks[hi.w + k] = make_int4(start, min(start + p.warp_chunk, hi.z + cnt), row, -(h + 1));
     }
-    double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)h * d);
-    for (int q = threadIdx.x; q < d / 2; q += blockDim.x) a[q] = make_double2(0.0, 0.0);
-    if (threadIdx.x == 0) p.arrive[h] = 0;
+    if (hi.y > 1) {
+      double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)h * d);
+      for (int q = threadIdx.x; q < d / 2; q += blockDim.x) a[q] = make_double2(0.0, 0.0);
+      if (threadIdx.x == 0) p.arrive[h] = 0;
+    }
   }
 }
 
@@ -325,14 +326,45 @@ __device__ __forceinline__ void store_gsum(float* gsum_out, int u, int d, int co
 constexpr int kMinTeamShift = 2;                              // teams of at least 4 lanes
 constexpr int kMaxTeams = 256 >> kMinTeamShift;               // per block
 
-// One team of 2^team_shift lanes per chunk descriptor (the next descriptor
-// is loaded while the current chunk runs).  The team stages the chunk's
-// positions in shared memory and starts pulling the Adam row of a light
-// unique into L2, accumulates the gradient rows in TwoSum pairs, and either
-// applies Adam (light unique) or adds its partial sum to the unique's fp64
-// accumulator in L2, the last chunk of the unique applying Adam.
+// Positions grouped by unique when the lookup recorded ranks: a plain
+// scatter, pos_sorted[segment start + rank] = position.
+__global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += (long long)gridDim.x * blockDim.x) {
+    const int u = __ldg(&p.inverse[i]);
+    if (u >= 0) p.pos_sorted[__ldg(&p.cursor[u]) + __ldg(&p.ranks[i])] = (int32_t)i;
+  }
+}
+
+// Sum of the gradient rows at positions pos[0 .. n) for one lane's VEC
+// columns, in TwoSum pairs, UNR rows in flight.
+template <int GD, int VEC, int UNR>
+__device__ __forceinline__ void accumulate(const BackwardParams& p, const int* pos, int n, int d, int col,
+                                           float hi[VEC], float lo[VEC]) {
+  for (int q0 = 0; q0 < n; q0 += UNR) {
+    GradRaw<GD, VEC> g[UNR];
+#pragma unroll
+    for (int r = 0; r < UNR; ++r)
+      if (q0 + r < n) load_grad_raw<GD, VEC>(p.grads, pos[q0 + r], d, col, g[r]);
+#pragma unroll
+    for (int r = 0; r < UNR; ++r)
+      if (q0 + r < n) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g[r], j));
+      }
+  }
+}
+
+// Phase 1: each warp takes a warp-chunk of a heavy unique; its teams split
+// the positions, and the teams' partial sums are combined by shuffles (lanes
+// with the same index in their team hold the same columns).  A heavy unique
+// with one warp-chunk applies Adam at once; otherwise the warp adds its sum
+// to the unique's fp64 accumulator in L2 and the last warp-chunk to arrive
+// applies Adam.
+// Phase 2: one team per light unique (at most kChunk positions): stage the
+// positions in shared memory, start pulling the Adam row into L2, sum the
+// gradient rows, apply Adam.  The next descriptor loads while a chunk runs.
 template <int RD, int GD>
-__global__ void __launch_bounds__(256, 4) k_bw_reduce_adam(const BackwardParams p, int team_shift) {
+__global__ void __launch_bounds__(256, 3) k_bw_reduce_adam(const BackwardParams p) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;
   constexpr int UNR = 16 / GradRaw<GD, VEC>::W;  // gradient rows in flight per lane (16 raw words)
   __shared__ float s_scal[2];
@@ -347,73 +379,72 @@ __global__ void __launch_bounds__(256, 4) k_bw_reduce_adam(const BackwardParams 
   __syncthreads();
   const float step_size = s_scal[0], inv_sqrt_bc2 = s_scal[1];
 
+  const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
+  const int tpw = 32 >> team_shift;  // teams per warp
   const int lane = threadIdx.x & 31;
   const int lt = lane & (team - 1);
+  const int tiw = lane >> team_shift;  // team index in the warp
   const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << (lane & ~(team - 1)));
   int* my_pos = s_pos + (threadIdx.x >> team_shift) * kChunk;
-  const long long total_chunks =
-      (long long)p.boff[(size_t)p.nblk * 3 + 1] + (*p.num_unique - p.boff[(size_t)p.nblk * 3 + 2]);
-  const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
-  const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
   const int d = (int)p.T.dim;
-  const bool one_pass = d <= team * VEC;
   const int col0 = lt * VEC;
+  const long long U = *p.num_unique;
+  const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
+  const long long light_end = (long long)HWC + (U - p.boff[(size_t)p.nblk * 3 + 2]);
 
-  int4 next = gteam < total_chunks ? __ldg(&p.chunks[gteam]) : make_int4(0, 0, -1, 0);
-  for (long long c = gteam; c < total_chunks; c += nteam) {
-    const int4 dsc = next;
-    if (c + nteam < total_chunks) next = __ldg(&p.chunks[c + nteam]);
-    const int start = dsc.x, cnt = dsc.y - dsc.x, row = dsc.z;
-    const bool heavy = dsc.w < 0;
-    if (!heavy && row >= 0 && col0 < d) {
-      const char* rec = row_ptr(p.T, row);
-      prefetch_l2(rec + (size_t)col0 * (RD == MT_F32 ? 4 : 2));
-      prefetch_l2(rec + p.T.emb_bytes + (size_t)col0 * 4);
-      prefetch_l2(rec + p.T.emb_bytes + p.T.mv_bytes + (size_t)col0 * 4);
-    }
-    for (int q = lt; q < cnt; q += team) my_pos[q] = __ldg(&p.pos_sorted[start + q]);
-    __syncwarp(team_mask);
-
+  // ---- phase 1: heavy warp-chunks, one warp each ----
+  const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long wc = gwarp; wc < HWC; wc += nwarp) {
+    const int4 dsc = __ldg(&p.chunks[wc]);
+    const int h = -dsc.w - 1, row = dsc.z;
+    const int4 hinfo = __ldg(&p.heavy_info[h]);  // {u, warp-chunks, ...}
+    const int share = (dsc.y - dsc.x + tpw - 1) / tpw;
+    const int tb = min(dsc.x + tiw * share, dsc.y), te = min(tb + share, dsc.y);
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + col0;
-      if (col >= d) continue;
+      const bool active = col < d;
       float hi[VEC], lo[VEC];
 #pragma unroll
       for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
-      for (int q0 = 0; q0 < cnt; q0 += UNR) {
-        GradRaw<GD, VEC> g[UNR];
-#pragma unroll
-        for (int r = 0; r < UNR; ++r)
-          if (q0 + r < cnt) load_grad_raw<GD, VEC>(p.grads, my_pos[q0 + r], d, col, g[r]);
-#pragma unroll
-        for (int r = 0; r < UNR; ++r)
-          if (q0 + r < cnt) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g[r], j));
-          }
+      for (int pb = tb; pb < te; pb += kChunk) {
+        const int nh = min(kChunk, te - pb);
+        for (int q = lt; q < nh; q += team) my_pos[q] = __ldg(&p.pos_sorted[pb + q]);
+        __syncwarp(team_mask);
+        if (active) accumulate<GD, VEC, UNR>(p, my_pos, nh, d, col, hi, lo);
+        __syncwarp(team_mask);
       }
-      if (!heavy) {
-        float gs[VEC];
+      for (int o = team; o < 32; o <<= 1) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
-        if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
-        if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
-      } else {
-        double* a = p.acc64 + (size_t)(-dsc.w - 1) * d + col;
+        for (int j = 0; j < VEC; ++j) {
+          const float h2 = __shfl_xor_sync(kFull, hi[j], o);
+          const float l2 = __shfl_xor_sync(kFull, lo[j], o);
+          two_sum_add(hi[j], lo[j], h2);
+          lo[j] = __fadd_rn(lo[j], l2);
+        }
+      }
+      if (tiw == 0 && active) {
+        if (hinfo.y == 1) {
+          float gs[VEC];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) atomicAdd(a + j, (double)hi[j] + (double)lo[j]);
+          for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
+          if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
+          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
+        } else {
+          double* a = p.acc64 + (size_t)h * d + col;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) atomicAdd(a + j, (double)hi[j] + (double)lo[j]);
+        }
       }
     }
-    if (heavy) {
-      const int h = -dsc.w - 1;
+    if (hinfo.y > 1) {
       __threadfence();
-      __syncwarp(team_mask);
+      __syncwarp();
       int old = 0;
-      if (lt == 0) old = atomicAdd(&p.arrive[h], 1);
-      old = __shfl_sync(team_mask, old, 0, team);
-      const int4 hinfo = __ldg(&p.heavy_info[h]);
-      if (old == hinfo.y - 1) {  // last chunk of this unique: every partial sum has landed
+      if (lane == 0) old = atomicAdd(&p.arrive[h], 1);
+      old = __shfl_sync(kFull, old, 0);
+      if (old == hinfo.y - 1 && tiw == 0) {  // last warp-chunk of this unique: every partial sum has landed
         __threadfence();
         for (int c0 = 0; c0 < d; c0 += team * VEC) {
           const int col = c0 + col0;
@@ -427,6 +458,39 @@ __global__ void __launch_bounds__(256, 4) k_bw_reduce_adam(const BackwardParams 
         }
       }
     }
+  }
+
+  // ---- phase 2: light uniques, one team each ----
+  const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
+  const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
+  const bool one_pass = d <= team * VEC;
+  long long c = HWC + gteam;
+  int4 next = c < light_end ? __ldg(&p.chunks[c]) : make_int4(0, 0, -1, 0);
+  for (; c < light_end; c += nteam) {
+    const int4 dsc = next;
+    if (c + nteam < light_end) next = __ldg(&p.chunks[c + nteam]);
+    const int cnt = dsc.y - dsc.x, row = dsc.z;
+    if (one_pass && row >= 0 && col0 < d) {
+      const char* rec = row_ptr(p.T, row);
+      prefetch_l2(rec + (size_t)col0 * (RD == MT_F32 ? 4 : 2));
+      prefetch_l2(rec + p.T.emb_bytes + (size_t)col0 * 4);
+      prefetch_l2(rec + p.T.emb_bytes + p.T.mv_bytes + (size_t)col0 * 4);
+    }
+    for (int q = lt; q < cnt; q += team) my_pos[q] = __ldg(&p.pos_sorted[dsc.x + q]);
+    __syncwarp(team_mask);
+    for (int c0 = 0; c0 < d; c0 += team * VEC) {
+      const int col = c0 + col0;
+      if (col >= d) continue;
+      float hi[VEC], lo[VEC];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
+      accumulate<GD, VEC, UNR>(p, my_pos, cnt, d, col, hi, lo);
+      float gs[VEC];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
+      if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
+      if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
+    }
     __syncwarp(team_mask);  // my_pos is reused by the next chunk
   }
 }
@@ -434,7 +498,7 @@ __global__ void __launch_bounds__(256, 4) k_bw_reduce_adam(const BackwardParams 
 int g_reduce_grid[4] = {0, 0, 0, 0};
 
 template <int RD, int GD>
-cudaError_t launch_reduce(const BackwardParams& p, int team_shift, cudaStream_t s) {
+cudaError_t launch_reduce(const BackwardParams& p, cudaStream_t s) {
   int& grid = g_reduce_grid[RD * 2 + GD];
   if (grid == 0) {
     int dev = 0, sms = 0, per = 0;
@@ -444,7 +508,7 @@ cudaError_t launch_reduce(const BackwardParams& p, int team_shift, cudaStream_t 
     grid = sms * (per > 0 ? per : 1);
   }
   MT_LAUNCH("k_bw_reduce_adam", s);
-  k_bw_reduce_adam<RD, GD><<<grid, 256, 0, s>>>(p, team_shift);
+  k_bw_reduce_adam<RD, GD><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -490,20 +554,30 @@ cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
     MT_LAUNCH("k_bw_heavy", s);
     k_bw_heavy<<<4 * 152, 256, 0, s>>>(p);
   }
-  if (p.ntiles > 0) {
+  if (p.ntiles > 0 && p.ranks != nullptr) {
+    MT_LAUNCH("k_bw_scatter", s);
+    const long long blocks = (p.n + 255) / 256;
+    k_bw_scatter<<<(int)(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, s>>>(p);
+  } else if (p.ntiles > 0) {
     MT_LAUNCH("k_bw_fill", s);
     k_bw_fill<<<p.ntiles, kThreads, 0, s>>>(p);
   }
-  const int vec = p.T.row_dtype == MT_F32 ? 4 : 8;
+  if (p.T.row_dtype == MT_F32) {
+    return p.grad_dtype == MT_F32 ? launch_reduce<MT_F32, MT_F32>(p, s) : launch_reduce<MT_F32, MT_BF16>(p, s);
+  }
+  return p.grad_dtype == MT_F32 ? launch_reduce<MT_BF16, MT_F32>(p, s) : launch_reduce<MT_BF16, MT_BF16>(p, s);
+}
+
+// Team size: the smallest power of two (>= 4 lanes, <= 32) whose lanes cover
+// the row at VEC columns each.
+int backward_team_shift(uint32_t dim, int row_dtype) {
+  const int vec = row_dtype == MT_F32 ? 4 : 8;
   int team = 1 << kMinTeamShift, shift = kMinTeamShift;
-  while (team < 32 && team * vec < (int)p.T.dim) {
+  while (team < 32 && team * vec < (int)dim) {
     team <<= 1;
     ++shift;
   }
-  if (p.T.row_dtype == MT_F32) {
-    return p.grad_dtype == MT_F32 ? launch_reduce<MT_F32, MT_F32>(p, shift, s) : launch_reduce<MT_F32, MT_BF16>(p, shift, s);
-  }
-  return p.grad_dtype == MT_F32 ? launch_reduce<MT_BF16, MT_F32>(p, shift, s) : launch_reduce<MT_BF16, MT_BF16>(p, shift, s);
+  return shift;
 }
 
 }  // namespace mt

@@ -37,6 +37,7 @@ struct LookupParams {
   int32_t* counts;
   int32_t* unique_rows;
   long long* num_unique;
+  int32_t* ranks;         // nullable
   // workspace
   ScratchSlot* scratch;
   unsigned long long scratch_mask;
@@ -59,7 +60,8 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s);
 
 // ---- backward ---------------------------------------------------------------
 
-constexpr int kChunk = 32;          // positions per reduction chunk
+constexpr int kChunk = 32;          // most positions a light unique has (one team-chunk)
+constexpr int kTeamShare = 128;     // positions per team in a heavy unique's warp-chunk
 constexpr int kScanTile = 2048;     // uniques per scan block
 constexpr int kScanThreads = 256;
 
@@ -67,6 +69,7 @@ struct BackwardParams {
   TableDev T;
   long long n;
   const int32_t* inverse;
+  const int32_t* ranks;  // nullable: rank of each position among its unique's positions
   const int32_t* counts;
   const int32_t* unique_rows;
   const long long* num_unique;
@@ -79,14 +82,16 @@ struct BackwardParams {
   int32_t* bsum;        // [nblk * 3] per scan block: sums of counts, heavy chunks, heavy uniques
   int32_t* boff;        // [(nblk + 1) * 3] exclusive offsets (+ totals)
   int32_t* cursor;      // [n] segment start of each unique, advanced to its end by the fill
-  int4* chunks;         // [n] descriptors {start, end, row, u or -(heavy index + 1)}:
-                        //     the chunks of multi-chunk ("heavy") uniques first, then one per light unique
-  int4* heavy_info;     // [heavy_cap] {u, chunks, segment start, first chunk} of each heavy unique
+  int4* chunks;         // [n] descriptors {start, end, row, u or -(heavy index + 1)}: the warp-chunks of
+                        //     heavy uniques (more than kChunk positions) first, then one team-chunk per light unique
+  int4* heavy_info;     // [heavy_cap] {u, warp-chunks, segment start, first chunk} of each heavy unique
   int32_t* pos_sorted;  // [n] positions grouped by unique
   double* acc64;        // [heavy_cap * d] cross-chunk sums of heavy uniques
   int32_t* arrive;      // [heavy_cap] chunks finished per heavy unique
   int nblk;
   int ntiles;
+  int team_shift;       // log2 lanes per team (one team covers VEC columns per lane)
+  int warp_chunk;       // positions per heavy warp-chunk: kTeamShare x teams per warp
 };
 
 struct BackwardWsLayout {
@@ -95,6 +100,7 @@ struct BackwardWsLayout {
   int nblk, ntiles;
 };
 BackwardWsLayout backward_ws_layout(long long n, uint32_t dim);
+int backward_team_shift(uint32_t dim, int row_dtype);
 cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s);
 
 // ---- table maintenance --------------------------------------------------------

@@ -324,10 +324,10 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
 }
 
 __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
-  __shared__ int32_t s_lcnt[kTile];
-  __shared__ int32_t s_u[kTile];
-  __shared__ int32_t s_row[kTile];
-  __shared__ uint16_t s_pl[kTile];
+  __shared__ int32_t s_lcnt[kTile];   // positions of local unique l in this tile, then its rank base
+  __shared__ int32_t s_u[kTile];      // unique index of local unique l
+  __shared__ uint16_t s_pl[kTile];    // local unique of each position
+  __shared__ uint16_t s_lrank[kTile]; // rank of each position among its local unique's positions
 
   const int tile = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const long long base = (long long)tile * kTile;
@@ -350,20 +350,26 @@ __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
     const unsigned act = __ballot_sync(kFull, v);
     if (v) {
       const unsigned grp = __match_any_sync(act, li);
-      if (lane == __ffs(grp) - 1) atomicAdd(&s_lcnt[li], __popc(grp));
+      const int leader = __ffs(grp) - 1;
+      int old = 0;
+      if (lane == leader) old = atomicAdd(&s_lcnt[li], __popc(grp));
+      old = __shfl_sync(grp, old, leader);
+      s_lrank[lp] = (uint16_t)(old + __popc(grp & ((1u << lane) - 1u)));
     }
   }
   __syncthreads();
+  // one atomic per (tile, unique): the old count is where this tile's
+  // positions start among all positions of the unique
   for (int l = tid; l < L; l += kThreads) {
     const int32_t u = p.scratch[p.lsslot[lb + l]].uidx;
     s_u[l] = u;
-    s_row[l] = p.unique_rows[u];
-    atomicAdd(&p.counts[u], s_lcnt[l]);
+    s_lcnt[l] = atomicAdd(&p.counts[u], s_lcnt[l]);
   }
   __syncthreads();
   for (int lp = tid; lp < cnt; lp += kThreads) {
     const uint16_t li = s_pl[lp];
     p.inverse[base + lp] = li == kNoIdx ? -1 : s_u[li];
+    if (p.ranks != nullptr) p.ranks[base + lp] = li == kNoIdx ? -1 : s_lcnt[li] + s_lrank[lp];
   }
 }
 
