@@ -138,7 +138,9 @@ def make_pool(pool: int, rank: int, users: int):
         g = torch.from_numpy(W.grads_normal(seed + 500_000, b.n, DIM)).to(torch.bfloat16)
         keys = (b.table_ids[np.searchsorted(b.feat_offsets, np.arange(b.n), side="right") - 1].astype(np.uint64)
                 << np.uint64(56)) | b.ids.astype(np.uint64)
-        out.append(dict(batch=b, grads=g, U=int(np.unique(keys).size)))
+        _, cnt = np.unique(keys, return_counts=True)
+        heavy = cnt > 32  # more positions than one team-chunk: reduced by whole warps
+        out.append(dict(batch=b, grads=g, U=int(cnt.size), H=int(heavy.sum()), NH=int(cnt[heavy].sum())))
     return out
 
 
@@ -255,6 +257,8 @@ def run_ours(args):
     npass = min(args.steps, 4 * len(pool))
     pass_ids = 0
     pass_U = 0
+    pass_H = 0
+    pass_NH = 0
     evs = []
     for j in range(npass):
         e = pool[j % len(pool)]
@@ -267,6 +271,8 @@ def run_ours(args):
         evs.append((a, m_, z))
         pass_ids += e["batch"].n
         pass_U += e["U"]
+        pass_H += e["H"]
+        pass_NH += e["NH"]
     torch.cuda.synchronize(dev)
     for a, m_, z in evs:
         fwd_ms += a.elapsed_time(m_)
@@ -285,8 +291,11 @@ def run_ours(args):
     U_avg = pass_U / npass
     fwd_bytes = 8 * N_avg + 4 * N_avg + U_avg * (8 + 16) + U_avg * B + N_avg * B + n_new_per_step * (16 + B + 8 * DIM)
     bwd_bytes = N_avg * G + 4 * N_avg + U_avg * (4 + 2 * B + 16 * DIM)
-    kernel_bytes = {
-        "k_bw_reduce_adam": N_avg * G + 4 * N_avg + U_avg * (2 * B + 16 * DIM + 16),
+    H_avg, NH_avg = pass_H / npass, pass_NH / npass
+    row_rw = 2 * B + 16 * DIM  # emb, m, v read and written
+    kernel_bytes = {  # algorithmic bytes per launch of the kernels that move the bulk
+        "k_bw_heavy_reduce": NH_avg * (G + 4) + H_avg * row_rw,
+        "k_bw_light_reduce": (N_avg - NH_avg) * (G + 4) + (U_avg - H_avg) * (row_rw + 16),
         "k_gather": N_avg * B + U_avg * B + 4 * N_avg,
     }
     peak, peak_kind = measured_hbm_peak()
@@ -336,6 +345,9 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (ids+grads+out ~0.5 GB per step), no flush",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "fwd_ids_per_s": pass_ids / (fwd_ms / 1e3), "bwd_ids_per_s": pass_ids / (bwd_ms / 1e3),
+        "kernel_rooflines": {k: {"GB/s": kernel_bytes[k] / (prof[k][1] / prof[k][0] / 1e3) / 1e9,
+                                 "frac": kernel_bytes[k] / (prof[k][1] / prof[k][0] / 1e3) / 1e9 / peak}
+                             for k in kernel_bytes if k in prof},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
                      "algorithmic_bytes_per_launch": kernel_bytes[dom], "avg_launch_ms": dom_ms,

@@ -267,17 +267,6 @@ int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const 
   p.ntiles = L.ntiles;
   p.team_shift = mt::backward_team_shift(t->cfg.dim, (int)t->cfg.row_dtype);
   p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
-  p.grad_row_bytes = (int)t->cfg.dim * (grad_dtype == MT_F32 ? 4 : 2);
-  {
-    // shared-memory batches for light uniques: about 36 KiB of row records and
-    // 56 KiB of gradient rows per block; rows too wide for that go team by team
-    const int bu = std::min(64, (36 << 10) / (int)t->dev.rec_bytes);
-    const int bp = std::min(1024, (56 << 10) / p.grad_row_bytes) / 4 * 4;  // keeps the staged rows 16-byte aligned
-    if (bu >= 4 && bp >= mt::kChunk) {
-      p.stage_bu = bu;
-      p.stage_bp = bp;
-    }
-  }
   const int rc = cuda_status(mt::launch_backward(p, as_stream(stream)));
   if (rc == MT_OK) t->step += 1;
   return rc;

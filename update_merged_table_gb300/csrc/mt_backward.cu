@@ -354,17 +354,116 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
   }
 }
 
-// Phase 1: each warp takes a warp-chunk of a heavy unique; its teams split
-// the positions, and the teams' partial sums are combined by shuffles (lanes
-// with the same index in their team hold the same columns).  A heavy unique
-// with one warp-chunk applies Adam at once; otherwise the warp adds its sum
-// to the unique's fp64 accumulator in L2 and the last warp-chunk to arrive
-// applies Adam.
-// Phase 2: one team per light unique (at most kChunk positions): stage the
-// positions in shared memory, start pulling the Adam row into L2, sum the
-// gradient rows, apply Adam.  The next descriptor loads while a chunk runs.
+// Heavy uniques (more than kChunk positions): each warp takes a warp-chunk;
+// its teams split the positions, UNR_H gradient rows in flight per lane, and
+// the teams' partial sums are combined by shuffles (lanes with the same
+// index in their team hold the same columns).  A heavy unique with one
+// warp-chunk applies Adam at once; otherwise the warp adds its sum to the
+// unique's fp64 accumulator in L2 and the last warp-chunk to arrive applies
+// Adam.
 template <int RD, int GD>
-__global__ void __launch_bounds__(256, 3) k_bw_reduce_adam(const BackwardParams p) {
+__global__ void __launch_bounds__(256, 2) k_bw_heavy_reduce(const BackwardParams p) {
+  constexpr int VEC = RD == MT_F32 ? 4 : 8;
+  constexpr int UNR = 64 / GradRaw<GD, VEC>::W;  // gradient rows in flight per lane (64 raw words)
+  __shared__ float s_scal[2];
+  __shared__ int s_pos[kMaxTeams * kTeamShare];
+  if (threadIdx.x == 0) {
+    const double t = (double)p.T.hdr->step;
+    const double bc1 = 1.0 - pow((double)p.beta1, t);
+    const double bc2 = 1.0 - pow((double)p.beta2, t);
+    s_scal[0] = (float)((double)p.lr / bc1);
+    s_scal[1] = (float)(1.0 / sqrt(bc2));
+  }
+  __syncthreads();
+  const float step_size = s_scal[0], inv_sqrt_bc2 = s_scal[1];
+
+  const int team_shift = p.team_shift;
+  const int team = 1 << team_shift;
+  const int tpw = 32 >> team_shift;  // teams per warp
+  const int lane = threadIdx.x & 31;
+  const int lt = lane & (team - 1);
+  const int tiw = lane >> team_shift;  // team index in the warp
+  const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << (lane & ~(team - 1)));
+  int* my_pos = s_pos + (threadIdx.x >> team_shift) * kTeamShare;
+  const int d = (int)p.T.dim;
+  const int col0 = lt * VEC;
+  const long long U = *p.num_unique;
+  const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
+  const long long light_end = (long long)HWC + (U - p.boff[(size_t)p.nblk * 3 + 2]);
+
+  // ---- phase 1: heavy warp-chunks, one warp each ----
+  const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long wc = gwarp; wc < HWC; wc += nwarp) {
+    const int4 dsc = __ldg(&p.chunks[wc]);
+    const int h = -dsc.w - 1, row = dsc.z;
+    const int4 hinfo = __ldg(&p.heavy_info[h]);  // {u, warp-chunks, ...}
+    const int share = (dsc.y - dsc.x + tpw - 1) / tpw;
+    const int tb = min(dsc.x + tiw * share, dsc.y), te = min(tb + share, dsc.y);
+    for (int c0 = 0; c0 < d; c0 += team * VEC) {
+      const int col = c0 + col0;
+      const bool active = col < d;
+      float hi[VEC], lo[VEC];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
+      if (c0 == 0) {  // this team's share of the warp-chunk (at most kTeamShare positions)
+        for (int q = lt; q < te - tb; q += team) my_pos[q] = __ldg(&p.pos_sorted[tb + q]);
+        __syncwarp(team_mask);
+      }
+      if (active) accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
+      for (int o = team; o < 32; o <<= 1) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          const float h2 = __shfl_xor_sync(kFull, hi[j], o);
+          const float l2 = __shfl_xor_sync(kFull, lo[j], o);
+          two_sum_add(hi[j], lo[j], h2);
+          lo[j] = __fadd_rn(lo[j], l2);
+        }
+      }
+      if (tiw == 0 && active) {
+        if (hinfo.y == 1) {
+          float gs[VEC];
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
+          if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
+          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
+        } else {
+          double* a = p.acc64 + (size_t)h * d + col;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) atomicAdd(a + j, (double)hi[j] + (double)lo[j]);
+        }
+      }
+    }
+    __syncwarp();  // my_pos is reused by the next warp-chunk
+    if (hinfo.y > 1) {
+      __threadfence();
+      int old = 0;
+      if (lane == 0) old = atomicAdd(&p.arrive[h], 1);
+      old = __shfl_sync(kFull, old, 0);
+      if (old == hinfo.y - 1 && tiw == 0) {  // last warp-chunk of this unique: every partial sum has landed
+        __threadfence();
+        for (int c0 = 0; c0 < d; c0 += team * VEC) {
+          const int col = c0 + col0;
+          if (col >= d) continue;
+          float gs[VEC];
+          const double* a = p.acc64 + (size_t)h * d + col;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) gs[j] = (float)__ldcg(a + j);
+          if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
+          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
+        }
+      }
+    }
+  }
+
+}
+
+// Light uniques (at most kChunk positions): one team per unique stages the
+// positions in shared memory, starts pulling the Adam row into L2, sums the
+// gradient rows (UNR in flight per lane) and applies Adam.  The next
+// descriptor loads while a chunk runs.
+template <int RD, int GD>
+__global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams p) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;
   constexpr int UNR = 16 / GradRaw<GD, VEC>::W;  // gradient rows in flight per lane (16 raw words)
   __shared__ float s_scal[2];
@@ -393,75 +492,6 @@ __global__ void __launch_bounds__(256, 3) k_bw_reduce_adam(const BackwardParams 
   const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
   const long long light_end = (long long)HWC + (U - p.boff[(size_t)p.nblk * 3 + 2]);
 
-  // ---- phase 1: heavy warp-chunks, one warp each ----
-  const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long wc = gwarp; wc < HWC; wc += nwarp) {
-    const int4 dsc = __ldg(&p.chunks[wc]);
-    const int h = -dsc.w - 1, row = dsc.z;
-    const int4 hinfo = __ldg(&p.heavy_info[h]);  // {u, warp-chunks, ...}
-    const int share = (dsc.y - dsc.x + tpw - 1) / tpw;
-    const int tb = min(dsc.x + tiw * share, dsc.y), te = min(tb + share, dsc.y);
-    for (int c0 = 0; c0 < d; c0 += team * VEC) {
-      const int col = c0 + col0;
-      const bool active = col < d;
-      float hi[VEC], lo[VEC];
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
-      for (int pb = tb; pb < te; pb += kChunk) {
-        const int nh = min(kChunk, te - pb);
-        for (int q = lt; q < nh; q += team) my_pos[q] = __ldg(&p.pos_sorted[pb + q]);
-        __syncwarp(team_mask);
-        if (active) accumulate<GD, VEC, UNR>(p, my_pos, nh, d, col, hi, lo);
-        __syncwarp(team_mask);
-      }
-      for (int o = team; o < 32; o <<= 1) {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          const float h2 = __shfl_xor_sync(kFull, hi[j], o);
-          const float l2 = __shfl_xor_sync(kFull, lo[j], o);
-          two_sum_add(hi[j], lo[j], h2);
-          lo[j] = __fadd_rn(lo[j], l2);
-        }
-      }
-      if (tiw == 0 && active) {
-        if (hinfo.y == 1) {
-          float gs[VEC];
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
-          if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
-          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
-        } else {
-          double* a = p.acc64 + (size_t)h * d + col;
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) atomicAdd(a + j, (double)hi[j] + (double)lo[j]);
-        }
-      }
-    }
-    if (hinfo.y > 1) {
-      __threadfence();
-      __syncwarp();
-      int old = 0;
-      if (lane == 0) old = atomicAdd(&p.arrive[h], 1);
-      old = __shfl_sync(kFull, old, 0);
-      if (old == hinfo.y - 1 && tiw == 0) {  // last warp-chunk of this unique: every partial sum has landed
-        __threadfence();
-        for (int c0 = 0; c0 < d; c0 += team * VEC) {
-          const int col = c0 + col0;
-          if (col >= d) continue;
-          float gs[VEC];
-          const double* a = p.acc64 + (size_t)h * d + col;
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) gs[j] = (float)__ldcg(a + j);
-          if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
-          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
-        }
-      }
-    }
-  }
-
-  // ---- phase 2: light uniques, one team each (unless k_bw_light_staged does them) ----
-  if (p.stage_bu > 0) return;
   const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
   const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
   const bool one_pass = d <= team * VEC;
@@ -496,205 +526,28 @@ __global__ void __launch_bounds__(256, 3) k_bw_reduce_adam(const BackwardParams 
   }
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Light uniques (at most kChunk positions each), a batch of stage_bu of them
-// per block at a time: descriptors and positions go to shared memory, then
-// every gradient row of the batch and every Adam row record arrive by
-// asynchronous 16-byte copies (cp.async) in one round trip; one team per
-// unique sums its rows from shared memory (TwoSum pairs) and applies Adam,
-// writing the row back to global memory.  A batch whose positions exceed
-// stage_bp is processed in several passes.
-template <int RD, int GD>
-__global__ void __launch_bounds__(256) k_bw_light_staged(const BackwardParams p) {
-  constexpr int VEC = RD == MT_F32 ? 4 : 8;
-  constexpr int GES = GD == MT_F32 ? 4 : 2;  // gradient element bytes
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int BU = p.stage_bu, BP = p.stage_bp;
-  const int G = p.grad_row_bytes, R = (int)p.T.rec_bytes;
-  int4* s_desc = reinterpret_cast<int4*>(smem);
-  int* s_poff = reinterpret_cast<int*>(s_desc + BU);
-  int* s_pos = s_poff + align16_ints(BU + 1);
-  char* s_grad = reinterpret_cast<char*>(s_pos + BP);
-  char* s_rows = s_grad + (size_t)BP * G;
-  __shared__ float s_scal[2];
-  __shared__ int s_nk, s_np;
-  if (threadIdx.x == 0) {
-    const double t = (double)p.T.hdr->step;
-    const double bc1 = 1.0 - pow((double)p.beta1, t);
-    const double bc2 = 1.0 - pow((double)p.beta2, t);
-    s_scal[0] = (float)((double)p.lr / bc1);
-    s_scal[1] = (float)(1.0 / sqrt(bc2));
-  }
-  __syncthreads();
-  const float step_size = s_scal[0], inv_sqrt_bc2 = s_scal[1];
-
-  const int tid = threadIdx.x;
-  const int team = 1 << p.team_shift;
-  const int lt = tid & (team - 1), team_id = tid >> p.team_shift, nteams = 256 >> p.team_shift;
-  const int d = (int)p.T.dim;
-  const int col0 = lt * VEC;
-  const long long U = *p.num_unique;
-  const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
-  const long long nlight = U - p.boff[(size_t)p.nblk * 3 + 2];
-  const long long nbatch = (nlight + BU - 1) / BU;
-  const int gv = G / 16, rv = R / 16;
-  const char* gbase = reinterpret_cast<const char*>(p.grads);
-
-  for (long long bt = blockIdx.x; bt < nbatch; bt += gridDim.x) {
-    const long long first = HWC + bt * BU;
-    const int nb = (int)min((long long)BU, nlight - bt * BU);
-    for (int k = tid; k < nb; k += 256) s_desc[k] = __ldg(&p.chunks[first + k]);
-    __syncthreads();
-    for (int k0 = 0; k0 < nb;) {
-      if (tid == 0) {  // the longest run of uniques from k0 whose rows fit in the batch
-        int acc = 0, k = k0;
-        s_poff[0] = 0;
-        while (k < nb && acc + (s_desc[k].y - s_desc[k].x) <= BP) {
-          acc += s_desc[k].y - s_desc[k].x;
-          ++k;
-          s_poff[k - k0] = acc;
-        }
-        s_nk = k - k0;
-        s_np = acc;
-      }
-      __syncthreads();
-      const int nk = s_nk, np = s_np;
-      for (int idx = tid; idx < np; idx += 256) {
-        int lo = 0, hi = nk;  // s_poff[lo] <= idx < s_poff[hi]
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (s_poff[mid] <= idx) lo = mid; else hi = mid;
-        }
-        s_pos[idx] = __ldg(&p.pos_sorted[s_desc[k0 + lo].x + (idx - s_poff[lo])]);
-      }
-      __syncthreads();
-      for (int it = tid; it < np * gv; it += 256) {
-        const int idx = it / gv, v = it - idx * gv;
-        cp_async16(s_grad + (size_t)idx * G + v * 16, gbase + (size_t)s_pos[idx] * G + v * 16);
-      }
-      for (int it = tid; it < nk * rv; it += 256) {
-        const int k = it / rv, v = it - k * rv;
-        const int row = s_desc[k0 + k].z;
-        if (row >= 0) cp_async16(s_rows + (size_t)k * R + v * 16, row_ptr(p.T, row) + v * 16);
-      }
-      cp_async_wait_all();
-      __syncthreads();
-      for (int k = team_id; k < nk; k += nteams) {
-        const int4 dsc = s_desc[k0 + k];
-        const int row = dsc.z;
-        const char* srow = s_rows + (size_t)k * R;
-        for (int c0 = 0; c0 < d; c0 += team * VEC) {
-          const int col = c0 + col0;
-          if (col >= d) continue;
-          float hi[VEC], lo[VEC];
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
-          for (int idx = s_poff[k]; idx < s_poff[k + 1]; ++idx) {
-            GradRaw<GD, VEC> g;
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(s_grad + (size_t)idx * G + (size_t)col * GES);
-#pragma unroll
-            for (int q = 0; q < GradRaw<GD, VEC>::W; ++q) g.w[q] = src[q];
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g, j));
-          }
-          float gs[VEC];
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
-          if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
-          if (row < 0) continue;
-          // Adam from the staged record; results go straight to global memory
-          float w[VEC];
-          if (RD == MT_F32) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) w[j] = reinterpret_cast<const float*>(srow)[col + j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j)
-              w[j] = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(srow)[col + j] << 16);
-          }
-          const float* sm_m = reinterpret_cast<const float*>(srow + p.T.emb_bytes) + col;
-          const float* sm_v = reinterpret_cast<const float*>(srow + p.T.emb_bytes + p.T.mv_bytes) + col;
-          char* rec = row_ptr(p.T, row);
-          float4* mp = reinterpret_cast<float4*>(rec + p.T.emb_bytes) + col / 4;
-          float4* vp = reinterpret_cast<float4*>(rec + p.T.emb_bytes + p.T.mv_bytes) + col / 4;
-#pragma unroll
-          for (int q = 0; q < VEC / 4; ++q) {
-            float m[4], v[4];
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const int j = 4 * q + kk;
-              m[kk] = __fadd_rn(__fmul_rn(p.beta1, sm_m[j]), __fmul_rn(p.one_minus_b1, gs[j]));
-              v[kk] = __fadd_rn(__fmul_rn(p.beta2, sm_v[j]), __fmul_rn(p.one_minus_b2, __fmul_rn(gs[j], gs[j])));
-              const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v[kk]), inv_sqrt_bc2), p.eps);
-              w[j] = __fsub_rn(w[j], __fmul_rn(step_size, __fdiv_rn(m[kk], den)));
-            }
-            mp[q] = make_float4(m[0], m[1], m[2], m[3]);
-            vp[q] = make_float4(v[0], v[1], v[2], v[3]);
-          }
-          if (RD == MT_F32) {
-            float4* e = reinterpret_cast<float4*>(rec) + col / 4;
-#pragma unroll
-            for (int q = 0; q < VEC / 4; ++q) e[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-          } else {
-            uint32_t ww[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(w[2 * q], w[2 * q + 1]);
-              ww[q] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            *(reinterpret_cast<uint4*>(rec) + col / 8) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-          }
-        }
-      }
-      __syncthreads();
-      k0 += nk;
-    }
-  }
-}
-
-int g_reduce_grid[4] = {0, 0, 0, 0};
-int g_staged_grid[4] = {0, 0, 0, 0};
-size_t g_staged_smem[4] = {0, 0, 0, 0};
+int g_heavy_grid[4] = {0, 0, 0, 0};
+int g_light_grid[4] = {0, 0, 0, 0};
 
 template <int RD, int GD>
 cudaError_t launch_reduce(const BackwardParams& p, cudaStream_t s) {
-  int& grid = g_reduce_grid[RD * 2 + GD];
-  if (grid == 0) {
-    int dev = 0, sms = 0, per = 0;
+  const int idx = RD * 2 + GD;
+  if (g_heavy_grid[idx] == 0) {
+    int dev = 0, sms = 0, per_h = 0, per_l = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_bw_reduce_adam<RD, GD>, 256, 0);
-    grid = sms * (per > 0 ? per : 1);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_h, k_bw_heavy_reduce<RD, GD>, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_l, k_bw_light_reduce<RD, GD>, 256, 0);
+    g_heavy_grid[idx] = sms * (per_h > 0 ? per_h : 1);
+    g_light_grid[idx] = sms * (per_l > 0 ? per_l : 1);
   }
   {
-    MT_LAUNCH("k_bw_reduce_adam", s);
-    k_bw_reduce_adam<RD, GD><<<grid, 256, 0, s>>>(p);
+    MT_LAUNCH("k_bw_heavy_reduce", s);
+    k_bw_heavy_reduce<RD, GD><<<g_heavy_grid[idx], 256, 0, s>>>(p);
   }
-  if (p.stage_bu > 0) {
-    const size_t smem = staged_smem_bytes(p.stage_bu, p.stage_bp, p.grad_row_bytes, (int)p.T.rec_bytes);
-    const int idx = RD * 2 + GD;
-    if (g_staged_smem[idx] < smem) {
-      cudaError_t e = cudaFuncSetAttribute(k_bw_light_staged<RD, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-      if (e != cudaSuccess) return e;
-      int dev = 0, sms = 0, per = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_bw_light_staged<RD, GD>, 256, smem);
-      g_staged_grid[idx] = sms * (per > 0 ? per : 1);
-      g_staged_smem[idx] = smem;
-    }
-    MT_LAUNCH("k_bw_light_staged", s);
-    k_bw_light_staged<RD, GD><<<g_staged_grid[idx], 256, smem, s>>>(p);
+  {
+    MT_LAUNCH("k_bw_light_reduce", s);
+    k_bw_light_reduce<RD, GD><<<g_light_grid[idx], 256, 0, s>>>(p);
   }
   return cudaGetLastError();
 }

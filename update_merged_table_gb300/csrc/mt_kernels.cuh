@@ -65,8 +65,6 @@ constexpr int kTeamShare = 128;     // positions per team in a heavy unique's wa
 constexpr int kScanTile = 2048;     // uniques per scan block
 constexpr int kScanThreads = 256;
 
-__host__ __device__ inline size_t align16_ints(size_t n) { return (n + 3) / 4 * 4; }
-
 struct BackwardParams {
   TableDev T;
   long long n;
@@ -94,17 +92,7 @@ struct BackwardParams {
   int ntiles;
   int team_shift;       // log2 lanes per team (one team covers VEC columns per lane)
   int warp_chunk;       // positions per heavy warp-chunk: kTeamShare x teams per warp
-  int grad_row_bytes;   // d x grad element bytes
-  int stage_bu;         // light uniques per shared-memory batch (0: light uniques go team by team)
-  int stage_bp;         // gradient rows per shared-memory batch
 };
-
-// Shared memory of the staged light-unique kernel for batches of bu uniques
-// and bp gradient rows.
-inline size_t staged_smem_bytes(int bu, int bp, int grad_row_bytes, int rec_bytes) {
-  const size_t a = (size_t)bu * 16 + align16_ints(bu + 1) * 4 + (size_t)bp * 4;
-  return a + (size_t)bp * grad_row_bytes + (size_t)bu * rec_bytes;
-}
 
 struct BackwardWsLayout {
   size_t bsum, boff, cursor, chunks, heavy_info, pos_sorted, acc64, arrive, total;
