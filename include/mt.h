@@ -45,7 +45,8 @@ enum {
   MT_ENOSPACE = -2, /* arena or workspace too small or misaligned */
   MT_EFULL = -3,    /* device: probe limit reached or row pool exhausted */
   MT_EKEY = -4,     /* device: an ID outside [0, 2^56) */
-  MT_ECUDA = -5     /* a CUDA runtime call failed */
+  MT_ECUDA = -5,    /* a CUDA runtime call failed */
+  MT_ETOOBIG = -6   /* batch larger than a fixed-size entry point allows (mt_lookup_static) */
 };
 
 /* Element types of rows and gradients. */
@@ -174,6 +175,25 @@ size_t mt_lookup_workspace_bytes(const mt_table* t, int64_t n);
 int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_offsets, const uint8_t* table_ids,
               int F, int insert_missing, void* out_rows, const mt_lookup_result* res, void* ws, size_t ws_bytes,
               mt_stream stream);
+
+/* The same lookup for callers that cannot allocate device memory when they
+ * call it (an operator or plugin interface that only passes its inputs and
+ * outputs, or a serving process whose memory budget is fixed at start-up):
+ * the workspace comes from a static device array inside the library instead
+ * of `ws`, so at most MT_LOOKUP_STATIC_MAX_IDS IDs per call; larger n returns
+ * MT_ETOOBIG with nothing enqueued.  The pages have no counterpart; this is
+ * an interface convenience, not part of the method.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every GPU that loads the library holds the array (3 MiB) until exit.
+ *  - All calls share the array: calls whose work overlaps on the GPU (other
+ *    streams or host threads) race on it.  The array keeps the last call's
+ *    contents; each call clears what it needs cleared.
+ *  - Otherwise identical to mt_lookup: same arguments, results and errors. */
+#define MT_LOOKUP_STATIC_MAX_IDS 65536
+int mt_lookup_static(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_offsets, const uint8_t* table_ids,
+                     int F, int insert_missing, void* out_rows, const mt_lookup_result* res, mt_stream stream);
 
 /* ---- backward: per-unique gradient sum + sparse row-wise Adam ------------ */
 

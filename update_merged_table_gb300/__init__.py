@@ -23,7 +23,8 @@ import numpy as np
 __all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "KEY_EMPTY", "KEY_TOMBSTONE",
            "ABI_FUNCTIONS", "profile_enable", "profile_report", "kernel_launches"]
 
-MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA = 0, -1, -2, -3, -4, -5
+MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA, MT_ETOOBIG = 0, -1, -2, -3, -4, -5, -6
+LOOKUP_STATIC_MAX_IDS = 65536
 MT_F32, MT_BF16 = 0, 1
 KEY_EMPTY = (1 << 64) - 1
 KEY_TOMBSTONE = (1 << 64) - 2
@@ -75,6 +76,7 @@ ABI_FUNCTIONS = {
     "mt_table_config": (_I32, [_P, _P]),
     "mt_lookup_workspace_bytes": (_SZ, [_P, _I64]),
     "mt_lookup": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "mt_lookup_static": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P]),
     "mt_backward_workspace_bytes": (_SZ, [_P, _I64]),
     "mt_backward_adam": (_I32, [_P, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "mt_erase_workspace_bytes": (_SZ, [_I64]),

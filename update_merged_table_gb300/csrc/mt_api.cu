@@ -96,6 +96,7 @@ const char* mt_strerror(int code) {
     case MT_EFULL: return "probe limit reached or row pool exhausted";
     case MT_EKEY: return "ID outside [0, 2^56)";
     case MT_ECUDA: return "CUDA runtime error";
+    case MT_ETOOBIG: return "batch larger than the fixed-size workspace allows";
     default: return "unknown status";
   }
 }
