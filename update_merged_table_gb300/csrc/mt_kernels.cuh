@@ -13,7 +13,9 @@ constexpr int kThreads = 256;            // threads per lookup CTA
 constexpr int kPPT = kTile / kThreads;   // positions per thread
 constexpr int kThreadsA = 512;           // threads per dedup CTA (k_dedup_claim)
 constexpr int kPPTA = kTile / kThreadsA; // positions per dedup thread
-constexpr int kHS = 2 * kTile;           // shared-memory hash slots of stage 1
+constexpr int kHS = 2 * kTile;           // shared-memory hash slots (backward fill)
+constexpr int kHSA = 3 * kTile / 2;      // shared-memory hash slots of stage 1 (load <= 2/3)
+constexpr int kMaxInBlockPrefix = 8192;  // tiles up to which each CTA sums its own tile offset
 constexpr uint16_t kNoIdx = 0xFFFF;
 
 // Stage-2 global scratch hash slot: key -> (first position, unique index).

@@ -31,8 +31,9 @@ namespace mt {
 
 namespace {
 
+// Home slot in the stage-1 shared hash of kHSA slots (multiply-shift range reduction).
 __device__ __forceinline__ uint32_t stage1_hash(unsigned long long key) {
-  return (uint32_t)(mix64(key ^ 0x2545F4914F6CDD1Dull) >> 40) & (uint32_t)(kHS - 1);
+  return (uint32_t)(((mix64(key ^ 0x2545F4914F6CDD1Dull) >> 32) * (unsigned long long)kHSA) >> 32);
 }
 
 __device__ __forceinline__ unsigned long long stage2_hash(unsigned long long key) {
@@ -75,30 +76,42 @@ __device__ __forceinline__ int block_sum(int v, int* s_warp) {
   return t;
 }
 
-constexpr size_t kSmemA = kHS * 8 + kHS * 4 + kTile * 4 + kTile * 2 + (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
+constexpr size_t kSmemA = kHSA * 8 + kHSA * 4 + kTile * 4 + kTile * 2 + (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
 
 __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
-  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHS] stage-1 hash keys
-  uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHS);              // [kHS] first local position, then local index
-  uint32_t* s_item = s_min + kHS;                                          // [kTile] (hash slot << 16) | first position of local unique l
+  unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHSA] stage-1 hash keys
+  uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHSA);             // [kHSA] first local position, then local index
+  uint32_t* s_item = s_min + kHSA;                                         // [kTile] (hash slot << 16) | first position of local unique l
   uint16_t* s_pslot = reinterpret_cast<uint16_t*>(s_item + kTile);         // [kTile] hash slot of each position
   long long* s_off = reinterpret_cast<long long*>(s_pslot + kTile);        // [F + 1]
   unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
   __shared__ int s_warp[kThreadsA / 32];
+  __shared__ int s_frange[2];  // features of the tile's first and last position
 
   const int tile = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
   const long long base = (long long)tile * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
 
-  for (int i = tid; i < kHS; i += kThreadsA) {
+  for (int i = tid; i < kHSA; i += kThreadsA) {
     s_key[i] = kEmpty;
     s_min[i] = 0xFFFFFFFFu;
   }
   for (int i = tid; i <= p.F; i += kThreadsA) s_off[i] = p.feat_off[i];
   for (int i = tid; i < p.F; i += kThreadsA) s_tid[i] = p.table_ids[i];
   __syncthreads();
+  if (tid < 2) {  // feature of position base (tid 0) and base + cnt - 1 (tid 1): last f with off[f] <= i
+    const long long i = base + (tid == 0 ? 0 : cnt - 1);
+    int lo = 0, hi = p.F;  // off[lo] <= i < off[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= i) lo = mid; else hi = mid;
+    }
+    s_frange[tid] = lo;
+  }
+  __syncthreads();
+  const int f_first = s_frange[0], f_last = s_frange[1];
 
   // ---- encode + stage 1 (tile-local dedup) ----
   bool bad = false;
@@ -111,7 +124,7 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
     if (in) {
       const long long i = base + lp;
       const long long id = p.ids[i];
-      int lo = 0, hi = p.F;  // off[lo] <= i < off[hi]
+      int lo = f_first, hi = f_last + 1;  // off[lo] <= i < off[hi]; one step when the tile has one feature
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (s_off[mid] <= i) lo = mid; else hi = mid;
@@ -127,10 +140,10 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
       uint32_t slot = 0;
       if (lane == leader) {  // the leader holds the group's smallest position
         uint32_t h = stage1_hash(key);
-        for (int probe = 0; probe < kHS; ++probe) {
+        for (int probe = 0; probe < kHSA; ++probe) {
           const unsigned long long prev = atomicCAS(&s_key[h], kEmpty, key);
           if (prev == kEmpty || prev == key) break;
-          h = (h + 1) & (uint32_t)(kHS - 1);
+          h = h + 1 == (uint32_t)kHSA ? 0u : h + 1;
         }
         slot = h;
         atomicMin(&s_min[slot], (uint32_t)lp);
@@ -223,7 +236,14 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   const int tile = blockIdx.x, tid = threadIdx.x;
   const int L = p.tile_L[tile];
   const size_t lb = (size_t)tile * kTile;
-  const int off = p.tile_offset[tile];
+  int off;
+  if (p.ntiles <= kMaxInBlockPrefix) {  // sum the owner counts of the earlier tiles (L2 reads, no scan launch)
+    int sum = 0;
+    for (int t = tid; t < tile; t += kThreads) sum += __ldg(&p.tile_owners[t]);
+    off = block_sum<kThreads>(sum, s_warp);
+  } else {
+    off = p.tile_offset[tile];
+  }
   if (tid == 0) s_nnew = 0;
 
   // owners, in local (first-occurrence) order
@@ -248,6 +268,7 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   }
   int O;
   int j = block_exclusive_scan<kThreads>(c, s_warp, &O);
+  if (tid == 0 && tile == p.ntiles - 1 && p.ntiles <= kMaxInBlockPrefix) *p.num_unique = off + O;
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     if (flags & (1u << k)) {
@@ -360,10 +381,26 @@ __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
   __syncthreads();
   // one atomic per (tile, unique): the old count is where this tile's
   // positions start among all positions of the unique
-  for (int l = tid; l < L; l += kThreads) {
-    const int32_t u = p.scratch[p.lsslot[lb + l]].uidx;
-    s_u[l] = u;
-    s_lcnt[l] = atomicAdd(&p.counts[u], s_lcnt[l]);
+  for (int l0 = tid; l0 < L; l0 += 4 * kThreads) {  // four independent atomics in flight per thread
+    int32_t u[4], old[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int l = l0 + k * kThreads;
+      u[k] = l < L ? __ldcg(&p.scratch[__ldg(&p.lsslot[lb + l])].uidx) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int l = l0 + k * kThreads;
+      if (l < L) old[k] = atomicAdd(&p.counts[u[k]], s_lcnt[l]);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int l = l0 + k * kThreads;
+      if (l < L) {
+        s_u[l] = u[k];
+        s_lcnt[l] = old[k];
+      }
+    }
   }
   __syncthreads();
   for (int lp = tid; lp < cnt; lp += kThreads) {
@@ -489,8 +526,10 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
     MT_LAUNCH("k_count_owners", s);
     k_count_owners<<<p.ntiles, kThreads, 0, s>>>(p);
   }
-  e = launch_scan_small(p.tile_owners, p.tile_offset, p.ntiles, 1, p.num_unique, s);
-  if (e != cudaSuccess) return e;
+  if (p.ntiles > kMaxInBlockPrefix) {
+    e = launch_scan_small(p.tile_owners, p.tile_offset, p.ntiles, 1, p.num_unique, s);
+    if (e != cudaSuccess) return e;
+  }
   {
     MT_LAUNCH("k_assign_resolve", s);
     k_assign_resolve<<<p.ntiles, kThreads, 0, s>>>(p);
