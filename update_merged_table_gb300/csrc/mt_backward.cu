@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
   const int tid = threadIdx.x, lane = tid & 31;
   const long long base = (long long)blockIdx.x * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
+  const long long U = *p.num_unique;
   for (int h = tid; h < kHS; h += kThreads) {
     s_hkey[h] = -1;
     s_hcnt[h] = 0;
@@ -174,7 +175,11 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int lp = k * kThreads + tid;
-    const int u = lp < cnt ? p.inverse[base + lp] : -1;
+    int u = lp < cnt ? p.inverse[base + lp] : -1;
+    if (u >= U) {  // not an index of this lookup's uniques: skip it, report it
+      latch_error(p.T.hdr, MT_EINVAL);
+      u = -1;
+    }
     const bool v = u >= 0;
     const unsigned act = __ballot_sync(kFull, v);
     if (v) {
@@ -327,12 +332,29 @@ constexpr int kMinTeamShift = 2;                              // teams of at lea
 constexpr int kMaxTeams = 256 >> kMinTeamShift;               // per block
 
 // Positions grouped by unique when the lookup recorded ranks: a plain
-// scatter, pos_sorted[segment start + rank] = position.
+// scatter, pos_sorted[segment start + rank] = position.  A rank or unique
+// index that does not belong to the lookup result (a caller passing some
+// other buffer) is skipped and latches MT_EINVAL instead of writing.
 __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
+  const long long U = *p.num_unique;
+  bool bad = false;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += (long long)gridDim.x * blockDim.x) {
     const int u = __ldg(&p.inverse[i]);
-    if (u >= 0) p.pos_sorted[__ldg(&p.cursor[u]) + __ldg(&p.ranks[i])] = (int32_t)i;
+    if (u < 0) continue;
+    const int r = __ldg(&p.ranks[i]);
+    if (u >= U || r < 0 || r >= __ldg(&p.counts[u])) {
+      bad = true;
+      continue;
+    }
+    p.pos_sorted[__ldg(&p.cursor[u]) + r] = (int32_t)i;
   }
+  if (bad) latch_error(p.T.hdr, MT_EINVAL);
+}
+
+// A grouped position, or -1 when it lies outside the batch (only possible
+// after the grouping kernels skipped inconsistent result buffers).
+__device__ __forceinline__ int valid_pos(const BackwardParams& p, int v) {
+  return (unsigned)v < (unsigned long long)p.n ? v : -1;
 }
 
 // Sum of the gradient rows at positions pos[0 .. n) for one lane's VEC
@@ -344,10 +366,10 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
     GradRaw<GD, VEC> g[UNR];
 #pragma unroll
     for (int r = 0; r < UNR; ++r)
-      if (q0 + r < n) load_grad_raw<GD, VEC>(p.grads, pos[q0 + r], d, col, g[r]);
+      if (q0 + r < n && pos[q0 + r] >= 0) load_grad_raw<GD, VEC>(p.grads, pos[q0 + r], d, col, g[r]);
 #pragma unroll
     for (int r = 0; r < UNR; ++r)
-      if (q0 + r < n) {
+      if (q0 + r < n && pos[q0 + r] >= 0) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g[r], j));
       }
@@ -407,7 +429,7 @@ __global__ void __launch_bounds__(256, 2) k_bw_heavy_reduce(const BackwardParams
 #pragma unroll
       for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
       if (c0 == 0) {  // this team's share of the warp-chunk (at most kTeamShare positions)
-        for (int q = lt; q < te - tb; q += team) my_pos[q] = __ldg(&p.pos_sorted[tb + q]);
+        for (int q = lt; q < te - tb; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[tb + q]));
         __syncwarp(team_mask);
       }
       if (active) accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
@@ -507,7 +529,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
       prefetch_l2(rec + p.T.emb_bytes + (size_t)col0 * 4);
       prefetch_l2(rec + p.T.emb_bytes + p.T.mv_bytes + (size_t)col0 * 4);
     }
-    for (int q = lt; q < cnt; q += team) my_pos[q] = __ldg(&p.pos_sorted[dsc.x + q]);
+    for (int q = lt; q < cnt; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[dsc.x + q]));
     __syncwarp(team_mask);
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + col0;
