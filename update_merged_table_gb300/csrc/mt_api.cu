@@ -208,7 +208,9 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
   p.num_unique = reinterpret_cast<long long*>(res->num_unique);
   p.ranks = res->ranks;
   if (n > 0) {
-    p.scratch = reinterpret_cast<mt::ScratchSlot*>(w + L.scratch);
+    p.sc_key = reinterpret_cast<unsigned long long*>(w + L.sc_key);
+    p.sc_minpos = reinterpret_cast<uint32_t*>(w + L.sc_minpos);
+    p.sc_uidx = reinterpret_cast<int32_t*>(w + L.sc_uidx);
     p.scratch_mask = L.scratch_slots - 1;
     p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
     p.tile_owners = reinterpret_cast<int32_t*>(w + L.tile_owners);
@@ -264,6 +266,7 @@ int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const 
   p.pos_sorted = reinterpret_cast<int32_t*>(w + L.pos_sorted);
   p.acc64 = reinterpret_cast<double*>(w + L.acc64);
   p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
+  p.work = reinterpret_cast<int32_t*>(w + L.work);
   p.nblk = L.nblk;
   p.ntiles = L.ntiles;
   p.team_shift = mt::backward_team_shift(t->cfg.dim, (int)t->cfg.row_dtype);

@@ -76,7 +76,10 @@ __device__ __forceinline__ int warp_chunks(int c, int wc) { return c > kChunk ? 
 // uniques, heavy uniques.  Block 0 advances the table's step counter.
 __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
-  if (blockIdx.x == 0 && threadIdx.x == 0) p.T.hdr->step += 1;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    p.T.hdr->step += 1;
+    p.work[0] = 0;
+  }
   const long long U = *p.num_unique;
   const long long u0 = (long long)blockIdx.x * kScanTile;
   int v[3] = {0, 0, 0};
@@ -413,10 +416,12 @@ __global__ void __launch_bounds__(256, 2) k_bw_heavy_reduce(const BackwardParams
   const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
   const long long light_end = (long long)HWC + (U - p.boff[(size_t)p.nblk * 3 + 2]);
 
-  // ---- phase 1: heavy warp-chunks, one warp each ----
-  const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarp = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long wc = gwarp; wc < HWC; wc += nwarp) {
+  // ---- heavy warp-chunks, handed to warps one at a time (they differ in size) ----
+  for (;;) {
+    int wc = 0;
+    if (lane == 0) wc = atomicAdd(&p.work[0], 1);
+    wc = __shfl_sync(kFull, wc, 0);
+    if (wc >= HWC) break;
     const int4 dsc = __ldg(&p.chunks[wc]);
     const int h = -dsc.w - 1, row = dsc.z;
     const int4 hinfo = __ldg(&p.heavy_info[h]);  // {u, warp-chunks, ...}
@@ -597,6 +602,7 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
   L.pos_sorted = take(nn * 4);
   L.acc64 = take((size_t)L.heavy_cap * dim * 8);
   L.arrive = take((size_t)L.heavy_cap * 4);
+  L.work = take(16);
   L.total = off;
   return L;
 }

@@ -18,13 +18,6 @@ constexpr int kHSA = 3 * kTile / 2;      // shared-memory hash slots of stage 1 
 constexpr int kMaxInBlockPrefix = 8192;  // tiles up to which each CTA sums its own tile offset
 constexpr uint16_t kNoIdx = 0xFFFF;
 
-// Stage-2 global scratch hash slot: key -> (first position, unique index).
-struct __align__(16) ScratchSlot {
-  unsigned long long key;
-  uint32_t minpos;
-  int32_t uidx;
-};
-
 struct LookupParams {
   TableDev T;
   const long long* ids;
@@ -41,7 +34,11 @@ struct LookupParams {
   long long* num_unique;
   int32_t* ranks;         // nullable
   // workspace
-  ScratchSlot* scratch;
+  // stage-2 global scratch hash, one array per field (keys and first
+  // positions start all-ones; unique indices are written before they are read)
+  unsigned long long* sc_key;
+  uint32_t* sc_minpos;
+  int32_t* sc_uidx;
   unsigned long long scratch_mask;
   int32_t* tile_L;        // [ntiles] local uniques per tile
   int32_t* tile_owners;   // [ntiles] global-first keys per tile
@@ -53,7 +50,7 @@ struct LookupParams {
 };
 
 struct LookupWsLayout {
-  size_t scratch, tile_L, tile_owners, tile_offset, lfirst, lsslot, lidx, total;
+  size_t sc_key, sc_minpos, sc_uidx, tile_L, tile_owners, tile_offset, lfirst, lsslot, lidx, total;
   unsigned long long scratch_slots;
   int ntiles;
 };
@@ -90,6 +87,7 @@ struct BackwardParams {
   int32_t* pos_sorted;  // [n] positions grouped by unique
   double* acc64;        // [heavy_cap * d] cross-chunk sums of heavy uniques
   int32_t* arrive;      // [heavy_cap] chunks finished per heavy unique
+  int32_t* work;        // [4] work counters (heavy warp-chunks handed out), zeroed per call
   int nblk;
   int ntiles;
   int team_shift;       // log2 lanes per team (one team covers VEC columns per lane)
@@ -97,7 +95,7 @@ struct BackwardParams {
 };
 
 struct BackwardWsLayout {
-  size_t bsum, boff, cursor, chunks, heavy_info, pos_sorted, acc64, arrive, total;
+  size_t bsum, boff, cursor, chunks, heavy_info, pos_sorted, acc64, arrive, work, total;
   long long heavy_cap;
   int nblk, ntiles;
 };

@@ -10,10 +10,10 @@
 //
 // Kernels, in launch order (one CTA per tile of kTile consecutive positions):
 //  k_dedup_claim     encode keys; stage 1: dedup inside the tile with a
-//                    shared-memory hash (warp match first, so a hot ID costs
-//                    one shared atomic per warp); stage 2: each tile-local
-//                    unique claims its key in a global scratch hash and
-//                    lowers the key's first position there (atomicMin).
+//                    shared-memory hash (CAS insert, atomicMin of the first
+//                    position); stage 2: each tile-local unique claims its
+//                    key in a global scratch hash and lowers the key's first
+//                    position there (atomicMin).
 //  k_count_owners    a tile owns a key when its first position is the key's
 //                    global first position; count owners per tile.
 //  k_scan_small      tile offsets = exclusive scan of owner counts; U.
@@ -133,23 +133,15 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
       key = ((unsigned long long)s_tid[lo] << 56) | (unsigned long long)id;
       bad |= !valid;
     }
-    const unsigned act = __ballot_sync(kFull, valid);
     if (valid) {
-      const unsigned grp = __match_any_sync(act, key);
-      const int leader = __ffs(grp) - 1;
-      uint32_t slot = 0;
-      if (lane == leader) {  // the leader holds the group's smallest position
-        uint32_t h = stage1_hash(key);
-        for (int probe = 0; probe < kHSA; ++probe) {
-          const unsigned long long prev = atomicCAS(&s_key[h], kEmpty, key);
-          if (prev == kEmpty || prev == key) break;
-          h = h + 1 == (uint32_t)kHSA ? 0u : h + 1;
-        }
-        slot = h;
-        atomicMin(&s_min[slot], (uint32_t)lp);
+      uint32_t h = stage1_hash(key);
+      for (int probe = 0; probe < kHSA; ++probe) {
+        const unsigned long long prev = atomicCAS(&s_key[h], kEmpty, key);
+        if (prev == kEmpty || prev == key) break;
+        h = h + 1 == (uint32_t)kHSA ? 0u : h + 1;
       }
-      slot = __shfl_sync(grp, slot, leader);
-      s_pslot[lp] = (uint16_t)slot;
+      atomicMin(&s_min[h], (uint32_t)lp);
+      s_pslot[lp] = (uint16_t)h;
     } else if (in) {
       s_pslot[lp] = kNoIdx;
     }
@@ -199,15 +191,15 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
     const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
     unsigned long long h = stage2_hash(key) & p.scratch_mask;
     for (unsigned long long probe = 0; probe <= p.scratch_mask; ++probe) {
-      unsigned long long cur = load_key_relaxed(&p.scratch[h].key);
+      unsigned long long cur = load_key_relaxed(&p.sc_key[h]);
       if (cur == kEmpty) {
-        cur = atomicCAS(&p.scratch[h].key, kEmpty, key);
+        cur = atomicCAS(&p.sc_key[h], kEmpty, key);
         if (cur == kEmpty) cur = key;
       }
       if (cur == key) break;
       h = (h + 1) & p.scratch_mask;
     }
-    atomicMin(&p.scratch[h].minpos, gpos);
+    atomicMin(&p.sc_minpos[h], gpos);
     p.lfirst[lb + li] = gpos;
     p.lsslot[lb + li] = (uint32_t)h;
   }
@@ -220,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) k_count_owners(const LookupParams p)
   const int L = p.tile_L[tile];
   const size_t lb = (size_t)tile * kTile;
   int c = 0;
-  for (int l = threadIdx.x; l < L; l += kThreads) c += p.scratch[p.lsslot[lb + l]].minpos == p.lfirst[lb + l];
+  for (int l = threadIdx.x; l < L; l += kThreads) c += __ldcg(&p.sc_minpos[p.lsslot[lb + l]]) == p.lfirst[lb + l];
   const int tot = block_sum<kThreads>(c, s_warp);
   if (threadIdx.x == 0) p.tile_owners[tile] = tot;
 }
@@ -258,9 +250,8 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
     key[k] = 0;
     if (l < L) {
       sl[k] = p.lsslot[lb + l];
-      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.scratch[sl[k]]));
-      key[k] = sv.x;
-      if ((uint32_t)(sv.y & 0xFFFFFFFFull) == p.lfirst[lb + l]) {  // minpos == first position
+      if (__ldcg(&p.sc_minpos[sl[k]]) == p.lfirst[lb + l]) {  // this tile holds the key's first position
+        key[k] = __ldcg(&p.sc_key[sl[k]]);
         flags |= 1u << k;
         ++c;
       }
@@ -273,7 +264,7 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   for (int k = 0; k < kPPT; ++k) {
     if (flags & (1u << k)) {
       const int u = off + j;
-      p.scratch[sl[k]].uidx = u;
+      p.sc_uidx[sl[k]] = u;
       p.unique_keys[u] = key[k];
       p.counts[u] = 0;
       s_oslot[j] = sl[k];
@@ -386,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int l = l0 + k * kThreads;
-      u[k] = l < L ? __ldcg(&p.scratch[__ldg(&p.lsslot[lb + l])].uidx) : 0;
+      u[k] = l < L ? __ldcg(&p.sc_uidx[__ldg(&p.lsslot[lb + l])]) : 0;
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -488,7 +479,9 @@ LookupWsLayout lookup_ws_layout(long long n) {
     return o;
   };
   const size_t cap = (size_t)L.ntiles * kTile;
-  L.scratch = take(ss * sizeof(ScratchSlot));
+  L.sc_key = take(ss * 8);
+  L.sc_minpos = take(ss * 4);
+  L.sc_uidx = take(ss * 4);
   L.tile_L = take((size_t)L.ntiles * 4);
   L.tile_owners = take((size_t)L.ntiles * 4);
   L.tile_offset = take(((size_t)L.ntiles + 1) * 4);
@@ -516,7 +509,10 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  cudaError_t e = cudaMemsetAsync(p.scratch, 0xFF, (p.scratch_mask + 1) * sizeof(ScratchSlot), s);
+  // keys EMPTY and first positions "none": sc_key and sc_minpos are adjacent
+  cudaError_t e = cudaMemsetAsync(p.sc_key, 0xFF, (p.scratch_mask + 1) * 8, s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(p.sc_minpos, 0xFF, (p.scratch_mask + 1) * 4, s);
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_dedup_claim", s);
