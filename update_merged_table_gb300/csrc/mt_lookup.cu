@@ -115,6 +115,12 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
 
   // ---- encode + stage 1 (tile-local dedup) ----
   bool bad = false;
+  long long idv[kPPTA];  // every ID load in flight before the shared-memory work
+#pragma unroll
+  for (int k = 0; k < kPPTA; ++k) {
+    const int lp = k * kThreadsA + tid;
+    idv[k] = lp < cnt ? __ldg(&p.ids[base + lp]) : 0;
+  }
 #pragma unroll
   for (int k = 0; k < kPPTA; ++k) {
     const int lp = k * kThreadsA + tid;  // a warp covers 32 consecutive positions
@@ -123,7 +129,7 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
     bool valid = false;
     if (in) {
       const long long i = base + lp;
-      const long long id = p.ids[i];
+      const long long id = idv[k];
       int lo = f_first, hi = f_last + 1;  // off[lo] <= i < off[hi]; one step when the tile has one feature
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -212,7 +218,17 @@ __global__ void __launch_bounds__(kThreads) k_count_owners(const LookupParams p)
   const int L = p.tile_L[tile];
   const size_t lb = (size_t)tile * kTile;
   int c = 0;
-  for (int l = threadIdx.x; l < L; l += kThreads) c += __ldcg(&p.sc_minpos[p.lsslot[lb + l]]) == p.lfirst[lb + l];
+  for (int l0 = threadIdx.x; l0 < L; l0 += kPPT * kThreads) {  // kPPT independent lookups in flight
+    uint32_t sl[kPPT], first[kPPT];
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+      const int l = l0 + k * kThreads;
+      sl[k] = l < L ? __ldg(&p.lsslot[lb + l]) : 0;
+      first[k] = l < L ? __ldg(&p.lfirst[lb + l]) : 0xFFFFFFFEu;  // matches no first position
+    }
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) c += __ldcg(&p.sc_minpos[sl[k]]) == first[k];
+  }
   const int tot = block_sum<kThreads>(c, s_warp);
   if (threadIdx.x == 0) p.tile_owners[tile] = tot;
 }
@@ -349,15 +365,18 @@ __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
 
   for (int l = tid; l < L; l += kThreads) s_lcnt[l] = 0;
   __syncthreads();
+  uint32_t liv[kPPT];  // every local-index load in flight before the warp-synchronous work
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int lp = k * kThreads + tid;
+    liv[k] = lp < cnt ? __ldg(&p.lidx[base + lp]) : kNoIdx;
+  }
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int lp = k * kThreads + tid;
     const bool in = lp < cnt;
-    uint32_t li = kNoIdx;
-    if (in) {
-      li = p.lidx[base + lp];
-      s_pl[lp] = (uint16_t)li;
-    }
+    const uint32_t li = liv[k];
+    if (in) s_pl[lp] = (uint16_t)li;
     const bool v = in && li != kNoIdx;
     const unsigned act = __ballot_sync(kFull, v);
     if (v) {
