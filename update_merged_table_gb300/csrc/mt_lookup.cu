@@ -218,17 +218,7 @@ __global__ void __launch_bounds__(kThreads) k_count_owners(const LookupParams p)
   const int L = p.tile_L[tile];
   const size_t lb = (size_t)tile * kTile;
   int c = 0;
-  for (int l0 = threadIdx.x; l0 < L; l0 += kPPT * kThreads) {  // kPPT independent lookups in flight
-    uint32_t sl[kPPT], first[kPPT];
-#pragma unroll
-    for (int k = 0; k < kPPT; ++k) {
-      const int l = l0 + k * kThreads;
-      sl[k] = l < L ? __ldg(&p.lsslot[lb + l]) : 0;
-      first[k] = l < L ? __ldg(&p.lfirst[lb + l]) : 0xFFFFFFFEu;  // matches no first position
-    }
-#pragma unroll
-    for (int k = 0; k < kPPT; ++k) c += __ldcg(&p.sc_minpos[sl[k]]) == first[k];
-  }
+  for (int l = threadIdx.x; l < L; l += kThreads) c += __ldcg(&p.sc_minpos[p.lsslot[lb + l]]) == p.lfirst[lb + l];
   const int tot = block_sum<kThreads>(c, s_warp);
   if (threadIdx.x == 0) p.tile_owners[tile] = tot;
 }
@@ -377,16 +367,7 @@ __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
     const bool in = lp < cnt;
     const uint32_t li = liv[k];
     if (in) s_pl[lp] = (uint16_t)li;
-    const bool v = in && li != kNoIdx;
-    const unsigned act = __ballot_sync(kFull, v);
-    if (v) {
-      const unsigned grp = __match_any_sync(act, li);
-      const int leader = __ffs(grp) - 1;
-      int old = 0;
-      if (lane == leader) old = atomicAdd(&s_lcnt[li], __popc(grp));
-      old = __shfl_sync(grp, old, leader);
-      s_lrank[lp] = (uint16_t)(old + __popc(grp & ((1u << lane) - 1u)));
-    }
+    if (in && li != kNoIdx) s_lrank[lp] = (uint16_t)atomicAdd(&s_lcnt[li], 1);
   }
   __syncthreads();
   // one atomic per (tile, unique): the old count is where this tile's
