@@ -379,3 +379,93 @@ def test_backward_without_ranks_matches_with_ranks():
         emb, m, v = tab.read_rows(res.unique_rows[:res.U])
         out.append((gs[:res.U].cpu().numpy(), emb.cpu().numpy()))
     assert np.array_equal(out[0][0], out[1][0]) and np.array_equal(out[0][1], out[1][1])
+
+
+def test_full_size_large_table():
+    """M = 2^26 slots, dim 128 fp32, prefilled with 0.7 M keys (46,976,204); a 2^20-ID batch Zipf(1.05)
+    over a 2^32 key space: unique/inverse/counts bit-exact, sampled gathered rows bit-exact (untouched
+    rows hold their initial values), sampled Adam rows within tolerance."""
+    log2, dim = 26, 128
+    tab = mt.Table(log2, dim)
+    pre_n = int(0.7 * (1 << log2))
+    pre = W.large_table_prefill_ids(pre_n)
+    for s0 in range(0, pre_n, 1 << 22):
+        tab.lookup(to_dev(pre[s0:s0 + (1 << 22)]), gather=False)
+    del pre
+    st = tab.stats()
+    assert st["live"] == pre_n and tab.error() == 0
+    b = W.large_table_batch(0)
+    res = tab.lookup(to_dev(b.ids))
+    keys, valid = oracle.encode(b.ids, b.feat_offsets, b.table_ids)
+    uq, inv, cnt = oracle.unique(keys, valid)
+    U = res.U
+    assert U == uq.size
+    assert np.array_equal(res.unique_keys[:U].cpu().numpy().view(np.uint64), uq)
+    assert np.array_equal(res.inverse[:b.n].cpu().numpy(), inv)
+    assert np.array_equal(res.counts[:U].cpu().numpy(), cnt)
+    assert (res.unique_rows[:U] >= 0).all()
+    rng = np.random.default_rng(0)
+    sample = rng.choice(b.n, size=2000, replace=False)
+    got = res.rows[torch.from_numpy(sample).to(dev())].cpu().numpy()
+    scale = oracle.default_init_scale(dim)
+    for r, i in enumerate(sample):
+        assert np.array_equal(got[r], oracle.init_row(int(keys[i]), 0, scale, dim))
+    # backward on the whole batch; the oracle sees the same keys fresh (same initial rows)
+    ref = oracle.Table(log2, dim)
+    ref.lookup(b.ids, b.feat_offsets, b.table_ids, gather=False)
+    g = W.grads_normal(5, b.n, dim)
+    gsum = tab.backward_adam(res, to_dev(g), want_gsum=True)
+    ref_gsum = ref.backward_adam(g, want_gsum=True)
+    np.testing.assert_allclose(gsum[:U].cpu().numpy(), ref_gsum, rtol=RTOL, atol=ATOL)
+    us = rng.choice(U, size=min(U, 20000), replace=False)
+    emb, m, v = tab.read_rows(res.unique_rows[torch.from_numpy(us).to(dev())])
+    e2, m2, v2, pr = ref.get_rows(uq[us])
+    assert pr.all()
+    np.testing.assert_allclose(emb.cpu().numpy(), e2, rtol=RTOL, atol=ATOL)
+    np.testing.assert_allclose(m.cpu().numpy(), m2, rtol=RTOL, atol=ATOL)
+    assert tab.error() == 0
+
+
+def test_full_size_online_churn():
+    """M = 2^24, dim 64 fp32, 2^23 prefilled keys; 200 steps of 2^18 IDs with 10% never seen before,
+    backward+Adam, and erase of 2^16 earlier IDs; live counts exact every step, rows and stats checked
+    every 20 steps against the oracle and its shadow open-addressing table."""
+    log2, dim = 24, 64
+    cs = W.ChurnStream(0)
+    tab = mt.Table(log2, dim)
+    ref = oracle.Table(log2, dim, simulate=True)
+    pre = cs.prefill_ids()
+    for s0 in range(0, pre.size, 1 << 22):
+        tab.lookup(to_dev(pre[s0:s0 + (1 << 22)]), gather=False)
+    ref.insert_keys(pre.astype(np.uint64))
+    for k in range(200):
+        b, er = cs.step(k)
+        res = tab.lookup(to_dev(b.ids))
+        r = ref.lookup(b.ids, gather=(k % 20 == 0))
+        gd, gh, _ = grads_for(900 + k, b.n, dim, "f32")
+        tab.backward_adam(res, gd)
+        ref.backward_adam(gh)
+        found = tab.erase(to_dev(er))
+        want = ref.erase(er.astype(np.uint64))
+        if k % 20 == 0:
+            compare_lookup(res, r)
+            assert np.array_equal(found.cpu().numpy().astype(bool), want)
+            st = tab.stats()
+            sim = ref.sim_stats()
+            assert st["live"] == ref.live == sim["live"]
+            assert abs(st["tombstones"] - sim["tombstones"]) <= 0.05 * sim["tombstones"] + 64
+            h1 = st["probe_hist"] / st["live"]
+            h2 = sim["hist"] / sim["live"]
+            assert np.abs(h1 - h2).sum() <= 0.05
+            # Adam rows of a sample of this step's keys
+            U = r["U"]
+            us = np.random.default_rng(k).choice(U, size=min(U, 5000), replace=False)
+            keys_now = r["unique"][us]
+            again = tab.lookup(to_dev(keys_now.astype(np.int64)), insert_missing=False)
+            rows_now = again.unique_rows[:again.U]
+            emb, m, v = tab.read_rows(rows_now)
+            e2, m2, v2, pr = ref.get_rows(keys_now)
+            assert np.array_equal(rows_now.cpu().numpy() >= 0, pr)
+            np.testing.assert_allclose(emb.cpu().numpy()[pr], e2[pr], rtol=RTOL, atol=ATOL)
+            np.testing.assert_allclose(v.cpu().numpy()[pr], v2[pr], rtol=RTOL, atol=1e-9)
+    assert tab.error() == 0 and ref.error == 0
