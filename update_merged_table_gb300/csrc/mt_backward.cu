@@ -522,20 +522,39 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
   const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
   const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
   const bool one_pass = d <= team * VEC;
+  const int gbytes = GD == MT_F32 ? 4 : 2;
+  // Software pipeline over this team's uniques: while unique c is reduced,
+  // the positions of the next one are in flight into registers and its Adam
+  // row and gradient rows are being pulled into L2.
+  constexpr int kPosRegs = kChunk >> kMinTeamShift;  // positions per lane of one team-chunk
   long long c = HWC + gteam;
-  int4 next = c < light_end ? __ldg(&p.chunks[c]) : make_int4(0, 0, -1, 0);
-  for (; c < light_end; c += nteam) {
-    const int4 dsc = next;
-    if (c + nteam < light_end) next = __ldg(&p.chunks[c + nteam]);
-    const int cnt = dsc.y - dsc.x, row = dsc.z;
-    if (one_pass && row >= 0 && col0 < d) {
-      const char* rec = row_ptr(p.T, row);
+  int4 dsc = c < light_end ? __ldg(&p.chunks[c]) : make_int4(0, 0, -1, 0);
+  if (c < light_end) {
+    for (int q = lt; q < dsc.y - dsc.x; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[dsc.x + q]));
+    if (one_pass && dsc.z >= 0 && col0 < d) {
+      const char* rec = row_ptr(p.T, dsc.z);
       prefetch_l2(rec + (size_t)col0 * (RD == MT_F32 ? 4 : 2));
       prefetch_l2(rec + p.T.emb_bytes + (size_t)col0 * 4);
       prefetch_l2(rec + p.T.emb_bytes + p.T.mv_bytes + (size_t)col0 * 4);
     }
-    for (int q = lt; q < cnt; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[dsc.x + q]));
-    __syncwarp(team_mask);
+  }
+  __syncwarp(team_mask);
+  for (; c < light_end; c += nteam) {
+    const int cnt = dsc.y - dsc.x, row = dsc.z;
+    const bool has_next = c + nteam < light_end;
+    const int4 nxt = has_next ? __ldg(&p.chunks[c + nteam]) : make_int4(0, 0, -1, 0);
+    int npos[kPosRegs];
+#pragma unroll
+    for (int k = 0; k < kPosRegs; ++k) {
+      const int q = lt + (k << team_shift);
+      npos[k] = q < nxt.y - nxt.x ? valid_pos(p, __ldg(&p.pos_sorted[nxt.x + q])) : -1;
+    }
+    if (one_pass && nxt.z >= 0 && col0 < d) {
+      const char* rec = row_ptr(p.T, nxt.z);
+      prefetch_l2(rec + (size_t)col0 * (RD == MT_F32 ? 4 : 2));
+      prefetch_l2(rec + p.T.emb_bytes + (size_t)col0 * 4);
+      prefetch_l2(rec + p.T.emb_bytes + p.T.mv_bytes + (size_t)col0 * 4);
+    }
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + col0;
       if (col >= d) continue;
@@ -543,13 +562,25 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
 #pragma unroll
       for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
       accumulate<GD, VEC, UNR>(p, my_pos, cnt, d, col, hi, lo);
+      if (c0 == 0) {  // the next unique's gradient rows (one 128-byte line per lane-position)
+#pragma unroll
+        for (int k = 0; k < kPosRegs; ++k)
+          if (npos[k] >= 0) prefetch_l2(reinterpret_cast<const char*>(p.grads) + (size_t)npos[k] * d * gbytes);
+      }
       float gs[VEC];
 #pragma unroll
       for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
       if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
       if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
     }
-    __syncwarp(team_mask);  // my_pos is reused by the next chunk
+    __syncwarp(team_mask);  // every lane is done with my_pos
+#pragma unroll
+    for (int k = 0; k < kPosRegs; ++k) {
+      const int q = lt + (k << team_shift);
+      if (q < nxt.y - nxt.x) my_pos[q] = npos[k];
+    }
+    __syncwarp(team_mask);
+    dsc = nxt;
   }
 }
 
