@@ -322,9 +322,6 @@ __device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, 
   }
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
-}
 
 __device__ __forceinline__ void store_gsum(float* gsum_out, int u, int d, int col, const float* gs, int vec) {
   float4* o = reinterpret_cast<float4*>(gsum_out + (size_t)u * d + col);
@@ -360,12 +357,24 @@ __device__ __forceinline__ int valid_pos(const BackwardParams& p, int v) {
   return (unsigned)v < (unsigned long long)p.n ? v : -1;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // Sum of the gradient rows at positions pos[0 .. n) for one lane's VEC
 // columns, in TwoSum pairs, UNR rows in flight.
-template <int GD, int VEC, int UNR>
+template <int GD, int VEC, int UNR, bool LOOKAHEAD = false>
 __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* pos, int n, int d, int col,
                                            float hi[VEC], float lo[VEC]) {
   for (int q0 = 0; q0 < n; q0 += UNR) {
+    if (LOOKAHEAD) {  // pull the next UNR rows toward L2 while these are summed
+#pragma unroll
+      for (int r = 0; r < UNR; ++r) {
+        const int q = q0 + UNR + r;
+        if (q < n && pos[q] >= 0)
+          prefetch_l2(reinterpret_cast<const char*>(p.grads) + ((size_t)pos[q] * d + col) * (GD == MT_F32 ? 4 : 2));
+      }
+    }
     GradRaw<GD, VEC> g[UNR];
 #pragma unroll
     for (int r = 0; r < UNR; ++r)
@@ -437,7 +446,7 @@ __global__ void __launch_bounds__(256, 2) k_bw_heavy_reduce(const BackwardParams
         for (int q = lt; q < te - tb; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[tb + q]));
         __syncwarp(team_mask);
       }
-      if (active) accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
+      if (active) accumulate<GD, VEC, UNR, true>(p, my_pos, te - tb, d, col, hi, lo);
       for (int o = team; o < 32; o <<= 1) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
