@@ -9,21 +9,21 @@
 // bias correction.
 //
 // Kernels, in launch order:
-//  k_bw_blocksum   per block of uniques: sums of counts, of chunks
-//                  (ceil(count / kChunk)) and of multi-chunk uniques; block
-//                  0 advances the table's step counter.
-//  k_scan_small    exclusive offsets of those sums over the blocks.
-//  k_bw_offsets    per unique: segment start (cursor), first chunk, index
-//                  among multi-chunk uniques; chunk -> unique map; zeroed
-//                  cross-chunk accumulators.
-//  k_bw_fill       positions grouped by unique (a counting sort): one
-//                  shared-memory group per unique per tile, one global
-//                  atomic per group to reserve its place in the segment.
-//  k_bw_reduce_adam  one team of lanes per chunk of <= kChunk positions sums
-//                  its gradient rows in fp32 pair (TwoSum) arithmetic.  A
-//                  single-chunk unique applies Adam at once; the chunks of a
-//                  larger unique add their partial sums in fp64 in L2 and
-//                  the last chunk to finish applies Adam.
+//  k_bw_blocksum     per block of uniques: sums of positions, of heavy
+//                    warp-chunks and of heavy uniques (more than kChunk
+//                    positions); block 0 advances the table's step counter.
+//  k_bw_offsets      per unique: segment start; per light unique one chunk
+//                    descriptor, per heavy unique its warp-chunk descriptors
+//                    and zeroed fp64 accumulators (each block sums the block
+//                    totals before it itself).
+//  k_bw_scatter      positions grouped by unique: segment start + the rank
+//                    the lookup recorded (k_bw_fill re-groups them with a
+//                    shared-memory hash when the lookup kept no ranks).
+//  k_bw_heavy_reduce heavy uniques: a warp per warp-chunk, 16 gradient rows
+//                    in flight per lane, TwoSum pairs, shuffle combine; the
+//                    last warp-chunk of a unique applies Adam.
+//  k_bw_light_reduce light uniques: a team of lanes per unique, software
+//                    pipelined across the team's uniques; Adam fused.
 #include "mt_kernels.cuh"
 
 namespace mt {
@@ -99,12 +99,41 @@ constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_of
 // Per unique: segment start (cursor).  A light unique gets its team-chunk
 // descriptor {start, end, row, u} at HWC + its rank among light uniques (HWC
 // = warp-chunks of all heavy uniques, which come first); a heavy unique gets
-// {u, warp-chunks, segment start, first chunk} for k_bw_heavy.
+// {u, warp-chunks, segment start, first chunk}, its warp-chunk descriptors,
+// zeroed fp64 accumulators and arrival count.  Each block adds up the sums
+// of the blocks before it itself (they are few), so no scan launch is needed.
 __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
+  __shared__ int s_base[3];
+  __shared__ int s_tot[3];
   const long long U = *p.num_unique;
-  if ((long long)blockIdx.x * kScanTile >= U) return;  // uniform over the block
-  const long long u0 = (long long)blockIdx.x * kScanTile + (long long)threadIdx.x * kUPT;
+  const int b = blockIdx.x;
+  {  // block offsets: sums over blocks < b; totals over all blocks
+    int pre[3] = {0, 0, 0}, all[3] = {0, 0, 0};
+    for (int q = threadIdx.x; q < p.nblk; q += kScanThreads) {
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        const int x = __ldg(&p.bsum[(size_t)q * 3 + c]);
+        all[c] += x;
+        if (q < b) pre[c] += x;
+      }
+    }
+    int ex[3], tot[3];
+    block_scan3<kScanThreads>(pre, ex, tot, s_warp);
+    if (threadIdx.x == 0) {
+      for (int c = 0; c < 3; ++c) s_base[c] = tot[c];
+    }
+    block_scan3<kScanThreads>(all, ex, tot, s_warp);
+    if (threadIdx.x == 0) {
+      for (int c = 0; c < 3; ++c) s_tot[c] = tot[c];
+      if (b == 0) {  // totals for the reduce kernels
+        for (int c = 0; c < 3; ++c) p.boff[(size_t)p.nblk * 3 + c] = tot[c];
+      }
+    }
+    __syncthreads();
+  }
+  if ((long long)b * kScanTile >= U) return;  // uniform over the block
+  const long long u0 = (long long)b * kScanTile + (long long)threadIdx.x * kUPT;
   int c[kUPT];
   int v[3] = {0, 0, 0};
 #pragma unroll
@@ -116,45 +145,35 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   }
   int ex[3], tot[3];
   block_scan3<kScanThreads>(v, ex, tot, s_warp);
-  int seg = ex[0] + p.boff[(size_t)blockIdx.x * 3 + 0];
-  int hch = ex[1] + p.boff[(size_t)blockIdx.x * 3 + 1];
-  int hv = ex[2] + p.boff[(size_t)blockIdx.x * 3 + 2];
-  const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
+  int seg = ex[0] + s_base[0];
+  int hch = ex[1] + s_base[1];
+  int hv = ex[2] + s_base[2];
+  const int HWC = s_tot[1];
+  const int d = (int)p.T.dim;
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
     const long long u = u0 + k;
     if (u >= U) break;
     p.cursor[u] = seg;
+    const int row = p.unique_rows[u];
     if (c[k] <= kChunk) {
-      p.chunks[HWC + (int)(u - hv)] = make_int4(seg, seg + c[k], p.unique_rows[u], (int)u);
+      p.chunks[HWC + (int)(u - hv)] = make_int4(seg, seg + c[k], row, (int)u);
     } else {
       const int nw = warp_chunks(c[k], p.warp_chunk);
       p.heavy_info[hv] = make_int4((int)u, nw, seg, hch);
+      for (int q = 0; q < nw; ++q) {
+        const int start = seg + q * p.warp_chunk;
+        p.chunks[hch + q] = make_int4(start, min(start + p.warp_chunk, seg + c[k]), row, -(hv + 1));
+      }
+      if (nw > 1) {
+        double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)hv * d);
+        for (int q = 0; q < d / 2; ++q) a[q] = make_double2(0.0, 0.0);
+        p.arrive[hv] = 0;
+      }
       ++hv;
       hch += nw;
     }
     seg += c[k];
-  }
-}
-
-// Warp-chunk descriptors of the heavy uniques, their zeroed fp64
-// accumulators and arrival counts; one block per heavy unique at a time.
-__global__ void __launch_bounds__(256) k_bw_heavy(const BackwardParams p) {
-  const int H = p.boff[(size_t)p.nblk * 3 + 2];
-  const int d = (int)p.T.dim;
-  for (int h = blockIdx.x; h < H; h += gridDim.x) {
-    const int4 hi = p.heavy_info[h];  // {u, warp-chunks, segment start, first chunk}
-    const int cnt = p.counts[hi.x];
-    const int row = p.unique_rows[hi.x];
-    for (int k = threadIdx.x; k < hi.y; k += blockDim.x) {
-      const int start = hi.z + k * p.warp_chunk;
-      p.chunks[hi.w + k] = make_int4(start, min(start + p.warp_chunk, hi.z + cnt), row, -(h + 1));
-    }
-    if (hi.y > 1) {
-      double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)h * d);
-      for (int q = threadIdx.x; q < d / 2; q += blockDim.x) a[q] = make_double2(0.0, 0.0);
-      if (threadIdx.x == 0) p.arrive[h] = 0;
-    }
   }
 }
 
@@ -337,16 +356,31 @@ constexpr int kMaxTeams = 256 >> kMinTeamShift;               // per block
 // other buffer) is skipped and latches MT_EINVAL instead of writing.
 __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
   const long long U = *p.num_unique;
+  const long long stride = (long long)gridDim.x * blockDim.x;
   bool bad = false;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += (long long)gridDim.x * blockDim.x) {
-    const int u = __ldg(&p.inverse[i]);
-    if (u < 0) continue;
-    const int r = __ldg(&p.ranks[i]);
-    if (u >= U || r < 0 || r >= __ldg(&p.counts[u])) {
-      bad = true;
-      continue;
+  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < p.n; i0 += 4 * stride) {
+    int u[4], r[4], cnt[4], cur[4];  // four positions' loads in flight
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const long long i = i0 + k * stride;
+      u[k] = i < p.n ? __ldg(&p.inverse[i]) : -1;
+      r[k] = i < p.n ? __ldg(&p.ranks[i]) : -1;
     }
-    p.pos_sorted[__ldg(&p.cursor[u]) + r] = (int32_t)i;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool ok = u[k] >= 0 && u[k] < U;
+      cnt[k] = ok ? __ldg(&p.counts[u[k]]) : 0;
+      cur[k] = ok ? __ldg(&p.cursor[u[k]]) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (u[k] < 0) continue;
+      if (u[k] >= U || r[k] < 0 || r[k] >= cnt[k]) {
+        bad = true;
+        continue;
+      }
+      p.pos_sorted[cur[k] + r[k]] = (int32_t)(i0 + k * stride);
+    }
   }
   if (bad) latch_error(p.T.hdr, MT_EINVAL);
 }
@@ -446,7 +480,7 @@ __global__ void __launch_bounds__(256, 2) k_bw_heavy_reduce(const BackwardParams
         for (int q = lt; q < te - tb; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[tb + q]));
         __syncwarp(team_mask);
       }
-      if (active) accumulate<GD, VEC, UNR, true>(p, my_pos, te - tb, d, col, hi, lo);
+      if (active) accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
       for (int o = team; o < 32; o <<= 1) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
@@ -652,15 +686,9 @@ cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
     MT_LAUNCH("k_bw_blocksum", s);
     k_bw_blocksum<<<p.nblk, kScanThreads, 0, s>>>(p);
   }
-  cudaError_t e = launch_scan_small(p.bsum, p.boff, p.nblk, 3, nullptr, s);
-  if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_bw_offsets", s);
     k_bw_offsets<<<p.nblk, kScanThreads, 0, s>>>(p);
-  }
-  {
-    MT_LAUNCH("k_bw_heavy", s);
-    k_bw_heavy<<<4 * 152, 256, 0, s>>>(p);
   }
   if (p.ntiles > 0 && p.ranks != nullptr) {
     MT_LAUNCH("k_bw_scatter", s);
