@@ -303,13 +303,13 @@ def run_ours(args):
     dom = max((k for k in prof if k in kernel_bytes), key=lambda k: prof[k][1])
     dom_ms = prof[dom][1] / prof[dom][0]
     achieved = kernel_bytes[dom] / (dom_ms / 1e3) / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    traffic = None  # DRAM bytes per launch from the committed ncu summary, scaled by the IDs of a launch
+    tpath = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
     if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get(dom)
-        except Exception:
-            traffic = None
+        for line in open(tpath):
+            f = line.split()
+            if len(f) == 2 and f[0] == dom:
+                traffic = float(f[1]) * N_avg
 
     # -------- end to end through the public API with host buffers --------
     e2e_steps = min(args.steps, 4 * len(pool))
