@@ -422,6 +422,69 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
   }
 }
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// accumulate() with the gradient rows brought in by asynchronous 16-byte
+// copies into a two-stage ring of HS rows in shared memory (this thread's
+// slots only, so no barrier is needed): the next HS rows are in flight while
+// these are summed, and no register holds a row in flight.
+template <int GD, int VEC, int HS>
+__device__ __forceinline__ void accumulate_async(const BackwardParams& p, const int* pos, int n, int d, int col,
+                                                 uint4* ring, float hi[VEC], float lo[VEC]) {
+  constexpr int W = GradRaw<GD, VEC>::W;
+  constexpr int Q = W / 4;  // 16-byte pieces of one lane's share of a row
+  const char* gbase = reinterpret_cast<const char*>(p.grads);
+  const size_t ges = GD == MT_F32 ? 4 : 2;
+  auto issue = [&](int st, int q0) {
+#pragma unroll
+    for (int r = 0; r < HS; ++r) {
+      const int qq = q0 + r;
+      if (qq < n && pos[qq] >= 0) {
+        const char* src = gbase + ((size_t)pos[qq] * d + col) * ges;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) cp_async16(ring + ((st * HS + r) * Q + q) * 256, src + 16 * q);
+      }
+    }
+    cp_async_commit();
+  };
+  issue(0, 0);
+  int st = 0;
+  for (int q0 = 0; q0 < n; q0 += HS, st ^= 1) {
+    if (q0 + HS < n) {
+      issue(st ^ 1, q0 + HS);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+#pragma unroll
+    for (int r = 0; r < HS; ++r) {
+      const int qq = q0 + r;
+      if (qq < n && pos[qq] >= 0) {
+        GradRaw<GD, VEC> g;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          const uint4 t = ring[((st * HS + r) * Q + q) * 256];
+          g.w[4 * q] = t.x; g.w[4 * q + 1] = t.y; g.w[4 * q + 2] = t.z; g.w[4 * q + 3] = t.w;
+        }
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g, j));
+      }
+    }
+  }
+}
+
+// Rows per ring stage of the heavy kernel (0: keep rows in registers).
+template <int RD, int GD>
+__host__ __device__ constexpr int heavy_stage_rows() {
+  return (GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W % 4) ? 0 : 6 / (GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W / 4);
+}
+
 // Heavy uniques (more than kChunk positions): each warp takes a warp-chunk;
 // its teams split the positions, UNR_H gradient rows in flight per lane, and
 // the teams' partial sums are combined by shuffles (lanes with the same
@@ -430,11 +493,15 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
 // unique's fp64 accumulator in L2 and the last warp-chunk to arrive applies
 // Adam.
 template <int RD, int GD>
-__global__ void __launch_bounds__(256, 2) k_bw_heavy_reduce(const BackwardParams p) {
+__global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams p) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;
-  constexpr int UNR = 64 / GradRaw<GD, VEC>::W;  // gradient rows in flight per lane (64 raw words)
+  constexpr int UNR = 32 / GradRaw<GD, VEC>::W;  // register path: gradient rows in flight per lane
+  constexpr int HS = heavy_stage_rows<RD, GD>();
+  constexpr int Q = GradRaw<GD, VEC>::W / 4;
+  extern __shared__ __align__(16) uint4 dsmem[];  // [2][HS][Q][256] ring, then positions
   __shared__ float s_scal[2];
-  __shared__ int s_pos[kMaxTeams * kTeamShare];
+  uint4* ring = dsmem + threadIdx.x;
+  int* s_pos = reinterpret_cast<int*>(dsmem + (HS > 0 ? 2 * HS * Q * 256 : 0));
   if (threadIdx.x == 0) {
     const double t = (double)p.T.hdr->step;
     const double bc1 = 1.0 - pow((double)p.beta1, t);
@@ -480,7 +547,10 @@ __global__ void __launch_bounds__(256, 2) k_bw_heavy_reduce(const BackwardParams
         for (int q = lt; q < te - tb; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[tb + q]));
         __syncwarp(team_mask);
       }
-      if (active) accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
+      if (active) {
+        if (HS > 0) accumulate_async<GD, VEC, (HS > 0 ? HS : 1)>(p, my_pos, te - tb, d, col, ring, hi, lo);
+        else accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
+      }
       for (int o = team; o < 32; o <<= 1) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
@@ -628,23 +698,31 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
 }
 
 int g_heavy_grid[4] = {0, 0, 0, 0};
+size_t g_heavy_smem[4] = {0, 0, 0, 0};
 int g_light_grid[4] = {0, 0, 0, 0};
 
 template <int RD, int GD>
 cudaError_t launch_reduce(const BackwardParams& p, cudaStream_t s) {
   const int idx = RD * 2 + GD;
-  if (g_heavy_grid[idx] == 0) {
+  constexpr int HS = heavy_stage_rows<RD, GD>();
+  constexpr int Q = GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W / 4;
+  const size_t heavy_smem = (size_t)(HS > 0 ? 2 * HS * Q * 256 : 0) * 16 + (size_t)(256 >> p.team_shift) * kTeamShare * 4;
+  if (g_heavy_grid[idx] == 0 || g_heavy_smem[idx] != heavy_smem) {
     int dev = 0, sms = 0, per_h = 0, per_l = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_h, k_bw_heavy_reduce<RD, GD>, 256, 0);
+    cudaError_t e = cudaFuncSetAttribute(k_bw_heavy_reduce<RD, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)heavy_smem);
+    if (e != cudaSuccess) return e;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_h, k_bw_heavy_reduce<RD, GD>, 256, heavy_smem);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_l, k_bw_light_reduce<RD, GD>, 256, 0);
     g_heavy_grid[idx] = sms * (per_h > 0 ? per_h : 1);
     g_light_grid[idx] = sms * (per_l > 0 ? per_l : 1);
+    g_heavy_smem[idx] = heavy_smem;
   }
   {
     MT_LAUNCH("k_bw_heavy_reduce", s);
-    k_bw_heavy_reduce<RD, GD><<<g_heavy_grid[idx], 256, 0, s>>>(p);
+    k_bw_heavy_reduce<RD, GD><<<g_heavy_grid[idx], 256, heavy_smem, s>>>(p);
   }
   {
     MT_LAUNCH("k_bw_light_reduce", s);
