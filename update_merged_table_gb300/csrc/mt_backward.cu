@@ -241,6 +241,24 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
 
 // ---- reduction + Adam -------------------------------------------------------
 
+// s + e = a + b exactly (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Add x and y (already an exact pair sum s + e of two rows) to the running
+// pair: the two rows' TwoSum does not depend on the running pair, so the
+// serial chain per column is one TwoSum per two rows.
+__device__ __forceinline__ void two_sum_add2(float& hi, float& lo, float x, float y) {
+  float s, e, s2, e2;
+  two_sum(x, y, s, e);
+  two_sum(hi, s, s2, e2);
+  hi = s2;
+  lo = __fadd_rn(lo, __fadd_rn(e2, e));
+}
+
 // a + b = s + e exactly (Knuth's TwoSum); the running pair (hi, lo) carries
 // the sum with about twice fp32's precision.
 __device__ __forceinline__ void two_sum_add(float& hi, float& lo, float x) {
@@ -414,11 +432,16 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
     for (int r = 0; r < UNR; ++r)
       if (q0 + r < n && pos[q0 + r] >= 0) load_grad_raw<GD, VEC>(p.grads, pos[q0 + r], d, col, g[r]);
 #pragma unroll
-    for (int r = 0; r < UNR; ++r)
-      if (q0 + r < n && pos[q0 + r] >= 0) {
+    for (int r = 0; r < UNR; r += 2) {
+      const bool ok0 = q0 + r < n && pos[q0 + r] >= 0;
+      const bool ok1 = r + 1 < UNR && q0 + r + 1 < n && pos[q0 + r + 1] >= 0;
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g[r], j));
+      for (int j = 0; j < VEC; ++j) {
+        const float x = ok0 ? grad_value<GD, VEC>(g[r], j) : 0.f;
+        const float y = ok1 ? grad_value<GD, VEC>(g[r + 1 < UNR ? r + 1 : r], j) : 0.f;
+        if (ok0 || ok1) two_sum_add2(hi[j], lo[j], x, y);
       }
+    }
   }
 }
 
@@ -463,17 +486,20 @@ __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const 
       cp_async_wait<0>();
     }
 #pragma unroll
-    for (int r = 0; r < HS; ++r) {
-      const int qq = q0 + r;
-      if (qq < n && pos[qq] >= 0) {
-        GradRaw<GD, VEC> g;
+    for (int r = 0; r < HS; r += 2) {
+      const bool ok0 = q0 + r < n && pos[q0 + r] >= 0;
+      const bool ok1 = r + 1 < HS && q0 + r + 1 < n && pos[q0 + r + 1] >= 0;
+      GradRaw<GD, VEC> g0, g1;
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-          const uint4 t = ring[((st * HS + r) * Q + q) * 256];
-          g.w[4 * q] = t.x; g.w[4 * q + 1] = t.y; g.w[4 * q + 2] = t.z; g.w[4 * q + 3] = t.w;
-        }
+      for (int q = 0; q < Q; ++q) {
+        const uint4 t0 = ok0 ? ring[((st * HS + r) * Q + q) * 256] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 t1 = ok1 ? ring[((st * HS + r + 1) * Q + q) * 256] : make_uint4(0u, 0u, 0u, 0u);
+        g0.w[4 * q] = t0.x; g0.w[4 * q + 1] = t0.y; g0.w[4 * q + 2] = t0.z; g0.w[4 * q + 3] = t0.w;
+        g1.w[4 * q] = t1.x; g1.w[4 * q + 1] = t1.y; g1.w[4 * q + 2] = t1.z; g1.w[4 * q + 3] = t1.w;
+      }
+      if (ok0 || ok1) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g, j));
+        for (int j = 0; j < VEC; ++j) two_sum_add2(hi[j], lo[j], grad_value<GD, VEC>(g0, j), grad_value<GD, VEC>(g1, j));
       }
     }
   }
