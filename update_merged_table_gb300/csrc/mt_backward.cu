@@ -432,16 +432,11 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
     for (int r = 0; r < UNR; ++r)
       if (q0 + r < n && pos[q0 + r] >= 0) load_grad_raw<GD, VEC>(p.grads, pos[q0 + r], d, col, g[r]);
 #pragma unroll
-    for (int r = 0; r < UNR; r += 2) {
-      const bool ok0 = q0 + r < n && pos[q0 + r] >= 0;
-      const bool ok1 = r + 1 < UNR && q0 + r + 1 < n && pos[q0 + r + 1] >= 0;
+    for (int r = 0; r < UNR; ++r)
+      if (q0 + r < n && pos[q0 + r] >= 0) {
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        const float x = ok0 ? grad_value<GD, VEC>(g[r], j) : 0.f;
-        const float y = ok1 ? grad_value<GD, VEC>(g[r + 1 < UNR ? r + 1 : r], j) : 0.f;
-        if (ok0 || ok1) two_sum_add2(hi[j], lo[j], x, y);
+        for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g[r], j));
       }
-    }
   }
 }
 
