@@ -217,7 +217,6 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
     p.tile_offset = reinterpret_cast<int32_t*>(w + L.tile_offset);
     p.lfirst = reinterpret_cast<uint32_t*>(w + L.lfirst);
     p.lsslot = reinterpret_cast<uint32_t*>(w + L.lsslot);
-    p.lrow = reinterpret_cast<int32_t*>(w + L.lrow);
     p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
     p.ntiles = L.ntiles;
   }

@@ -45,13 +45,12 @@ struct LookupParams {
   int32_t* tile_offset;   // [ntiles + 1] exclusive scan of tile_owners
   uint32_t* lfirst;       // [ntiles * kTile] first global position of local unique l
   uint32_t* lsslot;       // [ntiles * kTile] its scratch slot
-  int32_t* lrow;          // [ntiles * kTile] its table row as found by k_dedup_claim, -1 if absent
   uint16_t* lidx;         // [ntiles * kTile] local unique index of each position
   int ntiles;
 };
 
 struct LookupWsLayout {
-  size_t sc_key, sc_minpos, sc_uidx, tile_L, tile_owners, tile_offset, lfirst, lsslot, lrow, lidx, total;
+  size_t sc_key, sc_minpos, sc_uidx, tile_L, tile_owners, tile_offset, lfirst, lsslot, lidx, total;
   unsigned long long scratch_slots;
   int ntiles;
 };

@@ -189,17 +189,12 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
     lidx[lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
   }
 
-  // ---- stage 2: claim every local unique in the global scratch hash, and
-  // look it up in the table (read-only; nothing is inserted before
-  // k_assign_resolve, so the answer holds until then) ----
+  // ---- stage 2: claim every local unique in the global scratch hash ----
   const size_t lb = (size_t)tile * kTile;
   for (int li = tid; li < L; li += kThreadsA) {
     const uint32_t it = s_item[li];
     const unsigned long long key = s_key[it >> 16];
     const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
-    // the table's first probe is issued before the claim so both latencies overlap
-    const unsigned long long home = home_slot(p.T, key);
-    const ulonglong2 first = __ldcg(reinterpret_cast<const ulonglong2*>(&p.T.slots[home]));
     unsigned long long h = stage2_hash(key) & p.scratch_mask;
     for (unsigned long long probe = 0; probe <= p.scratch_mask; ++probe) {
       unsigned long long cur = load_key_relaxed(&p.sc_key[h]);
@@ -213,14 +208,6 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
     atomicMin(&p.sc_minpos[h], gpos);
     p.lfirst[lb + li] = gpos;
     p.lsslot[lb + li] = (uint32_t)h;
-    int32_t row = -1;
-    if (first.x == key) {
-      row = (int32_t)(uint32_t)(first.y & 0xFFFFFFFFull);
-    } else if (first.x != kEmpty) {  // the chain goes on past the home slot
-      long long t_end, t_tomb;
-      find_slot(p.T, key, &t_end, &t_tomb, &row);
-    }
-    p.lrow[lb + li] = row;
   }
   if (tid == 0) p.tile_L[tile] = L;
 }
@@ -261,7 +248,6 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   uint32_t flags = 0;
   uint32_t sl[kPPT];
   unsigned long long key[kPPT];
-  int32_t lrw[kPPT];
   int c = 0;
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
@@ -272,7 +258,6 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
       sl[k] = p.lsslot[lb + l];
       if (__ldcg(&p.sc_minpos[sl[k]]) == p.lfirst[lb + l]) {  // this tile holds the key's first position
         key[k] = __ldcg(&p.sc_key[sl[k]]);
-        lrw[k] = p.lrow[lb + l];
         flags |= 1u << k;
         ++c;
       }
@@ -290,7 +275,6 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
       p.counts[u] = 0;
       s_oslot[j] = sl[k];
       s_okey[j] = key[k];
-      s_orow[j] = lrw[k];
       ++j;
     }
   }
@@ -304,12 +288,11 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
     int32_t row = -1;
     bool claimed = false;
     unsigned long long cs = 0;
-    if (act) row = s_orow[jj];  // found by k_dedup_claim
-    if (act && row < 0 && p.insert_missing) {
+    if (act) {
       const unsigned long long key = s_okey[jj];
       long long t_end, t_tomb;
       const long long s = find_slot(p.T, key, &t_end, &t_tomb, &row);
-      if (s < 0) {
+      if (s < 0 && p.insert_missing) {
         // the key is absent and no other thread inserts it (it is unique in
         // the batch): take the first tombstone of its chain, else the EMPTY
         // slot that ended the chain, else the next free slot after them
@@ -504,7 +487,6 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.tile_offset = take(((size_t)L.ntiles + 1) * 4);
   L.lfirst = take(cap * 4);
   L.lsslot = take(cap * 4);
-  L.lrow = take(cap * 4);
   L.lidx = take(cap * 2);
   L.total = off;
   return L;
