@@ -1,12 +1,15 @@
 """Benchmark of the merged dynamic embedding table hot path on GB300.
 
 One step = one lookup (encode, two-stage dedup, find/insert, gather) plus one
-backward (per-unique gradient sum + sparse Adam) over one batch of the GRM
-jagged-sequence workload: 2048 users with lognormal(5, 1) sequence lengths
-capped at 3000, 4 ID features per token (Zipf(1.1) over 1e6 IDs each, merged
-by table id), M = 2^24 slots, dim 64 bf16 rows, fp32 Adam state, bf16 grads.
-Synthetic, seeded inputs; every step's inputs (IDs 15 MB, grads 247 MB, output
-247 MB) exceed the 126 MB L2, so no flush is needed between steps.
+backward (per-unique gradient sum + sparse Adam) over one batch, plus the
+erase of that step's deletions for the online-churn workload.  The default
+workload (``--config 3``) is the GRM jagged-sequence batch: 2048 users with
+lognormal(5, 1) sequence lengths capped at 3000, 4 ID features per token
+(Zipf(1.1) over 1e6 IDs each, merged by table id), M = 2^24 slots, dim 64
+bf16 rows, fp32 Adam state, bf16 grads.  Synthetic, seeded inputs; every
+step's inputs and outputs exceed the 126 MB L2, so no flush is needed between
+steps.  ``--config 1, 2, 4, 5`` time the single-table, merged-tables,
+large-table and online-churn workloads the same way.
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle on a bounded
 sample of the same workload instead.
@@ -30,9 +33,83 @@ from update_merged_table_gb300 import workloads as W  # noqa: E402
 
 METRIC = "unique+lookup+gather IDs/s and backward+Adam IDs/s; % of GB300 HBM roofline"
 UNIT = "IDs/s"
-WORKLOAD = "GRM jagged sequences: 2048 users, lognormal(5,1) lengths capped at 3000, 4 ID features, M=2^24, dim 64 bf16"
-LOG2_SLOTS, DIM, ROW_DTYPE = 24, 64, "bf16"
 FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class Workload:
+    """Table shape, batch generator and (for the oracle sample) a smaller batch generator."""
+
+    def __init__(self, cfg: int, users: int = 2048, log2_slots: int | None = None):
+        self.cfg = cfg
+        self.users = users
+        self.prefill_ids = None
+        self.churn = None
+        if cfg == 1:
+            self.name = "single table: M=2^16, dim 16 fp32, 4096 IDs Zipf(1.1) over 1e5"
+            self.log2, self.dim, self.row, self.grad = 16, 16, "f32", "f32"
+        elif cfg == 2:
+            self.name = ("merged tables: 8 features (vocab 1e4..1e6, Zipf s 0.8..1.3) in one M=2^22 table, "
+                         "dim 32 fp32, 65536 IDs")
+            self.log2, self.dim, self.row, self.grad = 22, 32, "f32", "f32"
+        elif cfg == 3:
+            self.log2, self.dim, self.row, self.grad = 24, 64, "bf16", "bf16"
+            self.name = ("GRM jagged sequences: 2048 users, lognormal(5,1) lengths capped at 3000, 4 ID features, "
+                         "M=2^24, dim 64 bf16")
+        elif cfg == 4:
+            self.name = ("large table: M=2^26, dim 128 fp32, prefilled to load 0.7, 2^20 IDs Zipf(1.05) over a "
+                         "2^32 key space")
+            self.log2, self.dim, self.row, self.grad = 26, 128, "f32", "f32"
+            self.prefill_ids = lambda: W.large_table_prefill_ids(int(0.7 * (1 << 26)))
+        elif cfg == 5:
+            self.name = ("online churn: M=2^24, dim 64 fp32, 2^23 prefilled keys, 2^18 IDs per step with 10% new, "
+                         "erase of 2^16 keys per step")
+            self.log2, self.dim, self.row, self.grad = 24, 64, "f32", "f32"
+            self.churn = W.ChurnStream(0)
+            self.prefill_ids = self.churn.prefill_ids
+        else:
+            raise ValueError("config must be 1..5")
+        if log2_slots is not None:
+            self.log2 = log2_slots
+        if cfg == 3 and (users != 2048 or self.log2 != 24):
+            self.name = (f"GRM jagged sequences (reduced): {users} users, lognormal(5,1) lengths capped at 3000, "
+                         f"4 ID features, M=2^{self.log2}, dim 64 bf16")
+
+    def batch(self, seed: int):
+        """(batch, erase ids or None) of step `seed`."""
+        if self.cfg == 1:
+            return W.single_table_batch(seed), None
+        if self.cfg == 2:
+            return W.merged_batch(seed), None
+        if self.cfg == 3:
+            return W.jagged_batch(seed, users=self.users), None
+        if self.cfg == 4:
+            return W.large_table_batch(seed), None
+        return self.churn.step(seed)
+
+    def sample_batch(self, seed: int):
+        """A bounded slice of the same workload for the CPU oracle."""
+        if self.cfg == 2:
+            return W.merged_batch(seed, per_table=2048)
+        if self.cfg == 3:
+            return W.jagged_batch(seed, users=256)
+        if self.cfg == 4:
+            return W.large_table_batch(seed, n=1 << 17)
+        if self.cfg == 5:
+            b, _ = self.churn.step(seed)
+            return W.single_feature(b.ids[: 1 << 16])
+        return W.single_table_batch(seed)
+
+    @property
+    def row_bytes(self):
+        return self.dim * (2 if self.row == "bf16" else 4)
+
+    @property
+    def grad_bytes(self):
+        return self.dim * (2 if self.grad == "bf16" else 4)
 
 
 # ---------------------------------------------------------------------------
@@ -74,6 +151,26 @@ def measured_hbm_peak():
         except Exception:
             pass
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def bind_to_gpu_numa_node(dev_index: int) -> str:
+    """Run on the CPUs next to the GPU so pinned host buffers land in its NUMA node."""
+    try:
+        import torch
+        bus = torch.cuda.get_device_properties(dev_index).pci_bus_id.lower()
+        for cand in (bus, "0000" + bus[4:] if len(bus) > 4 else bus):
+            path = f"/sys/bus/pci/devices/{cand}/local_cpulist"
+            if os.path.exists(path):
+                cpus = set()
+                for part in open(path).read().strip().split(","):
+                    a, _, b = part.partition("-")
+                    cpus.update(range(int(a), int(b or a) + 1))
+                if cpus:
+                    os.sched_setaffinity(0, cpus)
+                    return f"cpus {min(cpus)}-{max(cpus)}"
+    except Exception:
+        pass
+    return "unbound"
 
 
 class ClockSampler:
@@ -128,27 +225,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def make_pool(pool: int, rank: int, users: int):
-    """`pool` jagged batches (seeds distinct per rank) plus bf16 grads."""
-    import torch
-    out = []
-    for k in range(pool):
-        seed = 1 + k + 1000 * rank
-        b = W.jagged_batch(seed, users=users)
-        g = torch.from_numpy(W.grads_normal(seed + 500_000, b.n, DIM)).to(torch.bfloat16)
-        keys = (b.table_ids[np.searchsorted(b.feat_offsets, np.arange(b.n), side="right") - 1].astype(np.uint64)
-                << np.uint64(56)) | b.ids.astype(np.uint64)
-        _, cnt = np.unique(keys, return_counts=True)
-        heavy = cnt > 32  # more positions than one team-chunk: reduced by whole warps
-        out.append(dict(batch=b, grads=g, U=int(cnt.size), H=int(heavy.sum()), NH=int(cnt[heavy].sum())))
-    return out
-
-
-def workload_name(args) -> str:
-    if args.users == 2048 and args.log2_slots == LOG2_SLOTS:
-        return WORKLOAD
-    return (f"GRM jagged sequences (reduced): {args.users} users, lognormal(5,1) lengths capped at 3000, "
-            f"4 ID features, M=2^{args.log2_slots}, dim 64 bf16")
+def batch_stats(b):
+    """Unique keys, heavy uniques (more than 32 positions) and their positions, from the batch itself."""
+    f = np.searchsorted(b.feat_offsets, np.arange(b.n), side="right") - 1
+    keys = (b.table_ids[f].astype(np.uint64) << np.uint64(56)) | b.ids.astype(np.uint64)
+    _, cnt = np.unique(keys, return_counts=True)
+    heavy = cnt > 32
+    return int(cnt.size), int(heavy.sum()), int(cnt[heavy].sum())
 
 
 # ---------------------------------------------------------------------------
@@ -167,33 +250,50 @@ def run_ours(args):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if ws > 1 else torch.cuda.current_device())
     torch.cuda.set_device(dev)
+    numa = bind_to_gpu_numa_node(dev.index)
     build_lib.build()
     mt.load_library()
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
 
-    tab = mt.Table(args.log2_slots, DIM, row_dtype=ROW_DTYPE, device=dev)
-    pool = make_pool(args.pool, rank, args.users)
-    B = DIM * 2          # bytes per bf16 row
-    G = DIM * 2          # bytes per bf16 grad row
-    for e in pool:
-        b = e["batch"]
+    wl = Workload(args.config, args.users, args.log2_slots)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
+    tab = mt.Table(wl.log2, wl.dim, row_dtype=wl.row, device=dev)
+    if wl.prefill_ids is not None:  # untimed: the resident key set of a steady state
+        pre = wl.prefill_ids()
+        for s0 in range(0, pre.size, 1 << 22):
+            tab.lookup(torch.from_numpy(pre[s0:s0 + (1 << 22)]).to(dev), gather=False)
+        del pre
+    B, G = wl.row_bytes, wl.grad_bytes
+
+    pool = []
+    for k in range(args.pool):
+        b, er = wl.batch(1 + k + 1000 * rank)
+        U, H, NH = batch_stats(b)
+        g = torch.from_numpy(W.grads_normal(1 + k + 500_000 + 1000 * rank, b.n, wl.dim)).to(tdt[wl.grad])
+        e = dict(batch=b, grads=g, U=U, H=H, NH=NH, erase=None)
         e["ids_d"] = torch.from_numpy(b.ids).to(dev)
-        e["grads_d"] = e["grads"].to(dev)
+        e["grads_d"] = g.to(dev)
         e["res"] = tab.new_result(b.n, gather=True)
+        if er is not None:
+            e["erase"] = torch.from_numpy(er.astype(np.int64)).to(dev)
         e["ids_h"] = torch.from_numpy(b.ids).pin_memory()
-        e["grads_h"] = e["grads"].pin_memory()
+        e["grads_h"] = g.pin_memory()
         e["u_h"] = torch.empty(1, dtype=torch.int64).pin_memory()
+        pool.append(e)
 
     def step(e):
         b = e["batch"]
         tab.lookup(e["ids_d"], b.feat_offsets, b.table_ids, result=e["res"])
         tab.backward_adam(e["res"], e["grads_d"])
+        if e["erase"] is not None:
+            tab.erase(e["erase"], want_found=False)
 
-    # step 0: the cold batch (every key new) -- untimed
-    cold = W.jagged_batch(1000 * rank, users=args.users)
+    # the cold step (a batch on the table as prefilled; for the jagged workload every key is new) -- untimed
+    cold, _ = wl.batch(1000 * rank + 999)
     cold_ids = torch.from_numpy(cold.ids).to(dev)
-    cold_g = torch.from_numpy(W.grads_normal(7, cold.n, DIM)).to(torch.bfloat16).to(dev)
+    cold_g = torch.from_numpy(W.grads_normal(7, cold.n, wl.dim)).to(tdt[wl.grad]).to(dev)
+    live_before = int(tab.stats()["live"])
     torch.cuda.synchronize(dev)
     c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
     c0.record(stream)
@@ -202,8 +302,8 @@ def run_ours(args):
     tab.backward_adam(cres, cold_g)
     c2.record(stream)
     torch.cuda.synchronize(dev)
-    cold_stats = {"ids": cold.n, "new_keys": int(tab.stats()["live"]), "lookup_ms": c0.elapsed_time(c1),
-                  "backward_ms": c1.elapsed_time(c2), "note": "first step on an empty table, includes lazy set-up"}
+    cold_stats = {"ids": cold.n, "new_keys": int(tab.stats()["live"]) - live_before, "lookup_ms": c0.elapsed_time(c1),
+                  "backward_ms": c1.elapsed_time(c2), "note": "first step after set-up, includes lazy set-up"}
     del cres, cold_ids, cold_g
     for j in range(args.warmup):
         step(pool[j % len(pool)])
@@ -255,10 +355,7 @@ def run_ours(args):
     # -------- per-direction and per-kernel device times (separate pass) --------
     fwd_ms = bwd_ms = 0.0
     npass = min(args.steps, 4 * len(pool))
-    pass_ids = 0
-    pass_U = 0
-    pass_H = 0
-    pass_NH = 0
+    pass_ids = pass_U = pass_H = pass_NH = 0
     evs = []
     for j in range(npass):
         e = pool[j % len(pool)]
@@ -268,6 +365,8 @@ def run_ours(args):
         m_.record(stream)
         tab.backward_adam(e["res"], e["grads_d"])
         z.record(stream)
+        if e["erase"] is not None:
+            tab.erase(e["erase"], want_found=False)
         evs.append((a, m_, z))
         pass_ids += e["batch"].n
         pass_U += e["U"]
@@ -285,14 +384,15 @@ def run_ours(args):
     prof = mt.profile_report(reset=True)
     mt.profile_enable(False)
 
-    # algorithmic bytes (steady state; new keys counted from the live-key growth)
-    n_new_per_step = (live1 - live0) / max(1, args.steps)
+    # algorithmic bytes (new keys counted from the live-key growth of the timed steps)
+    n_new_per_step = max(0.0, (live1 - live0) / max(1, args.steps))
     N_avg = pass_ids / npass
     U_avg = pass_U / npass
-    fwd_bytes = 8 * N_avg + 4 * N_avg + U_avg * (8 + 16) + U_avg * B + N_avg * B + n_new_per_step * (16 + B + 8 * DIM)
-    bwd_bytes = N_avg * G + 4 * N_avg + U_avg * (4 + 2 * B + 16 * DIM)
     H_avg, NH_avg = pass_H / npass, pass_NH / npass
-    row_rw = 2 * B + 16 * DIM  # emb, m, v read and written
+    fwd_bytes = (8 * N_avg + 4 * N_avg + U_avg * (8 + 16) + U_avg * B + N_avg * B
+                 + n_new_per_step * (16 + B + 8 * wl.dim))
+    bwd_bytes = N_avg * G + 4 * N_avg + U_avg * (4 + 2 * B + 16 * wl.dim)
+    row_rw = 2 * B + 16 * wl.dim  # emb, m, v read and written
     kernel_bytes = {  # algorithmic bytes per launch of the kernels that move the bulk
         "k_bw_heavy_reduce": NH_avg * (G + 4) + H_avg * row_rw,
         "k_bw_light_reduce": (N_avg - NH_avg) * (G + 4) + (U_avg - H_avg) * (row_rw + 16),
@@ -305,7 +405,7 @@ def run_ours(args):
     achieved = kernel_bytes[dom] / (dom_ms / 1e3) / 1e9
     traffic = None  # DRAM bytes per launch from the committed ncu summary, scaled by the IDs of a launch
     tpath = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
-    if os.path.exists(tpath):
+    if args.config == 3 and os.path.exists(tpath):
         for line in open(tpath):
             f = line.split()
             if len(f) == 2 and f[0] == dom:
@@ -324,7 +424,7 @@ def run_ours(args):
         e["grads_d"].copy_(e["grads_h"], non_blocking=True)
         step(e)
         e["u_h"].copy_(e["res"].num_unique, non_blocking=True)
-        h2d += e["ids_h"].numel() * 8 + e["grads_h"].numel() * 2
+        h2d += e["ids_h"].numel() * 8 + e["grads_h"].numel() * e["grads_h"].element_size()
         d2h += 8
         e2e_ids += e["batch"].n
     ev3.record(stream)
@@ -339,11 +439,12 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": tot_ids / tot_secs, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * tot_secs / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(args), "ids_per_step": N_avg, "unique_per_step": U_avg,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.row, "data": "synthetic",
+        "config": {"workload": wl.name, "ids_per_step": N_avg, "unique_per_step": U_avg,
                    "new_keys_per_step": n_new_per_step, "batch_pool": len(pool), "cuda_graph": bool(args.graph),
-                   "l2": "inputs larger than L2 (ids+grads+out ~0.5 GB per step), no flush",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+                   "l2": ("inputs larger than L2 (ids+grads+out ~0.5 GB per step), no flush" if args.config == 3
+                          else "batch pool cycled; see the workload's sizes"),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "host_binding": numa},
         "fwd_ids_per_s": pass_ids / (fwd_ms / 1e3), "bwd_ids_per_s": pass_ids / (bwd_ms / 1e3),
         "kernel_rooflines": {k: {"GB/s": kernel_bytes[k] / (prof[k][1] / prof[k][0] / 1e3) / 1e9,
                                  "frac": kernel_bytes[k] / (prof[k][1] / prof[k][0] / 1e3) / 1e9 / peak}
@@ -364,7 +465,7 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -377,48 +478,54 @@ def run_ours(args):
 # the oracle on the host cores (reported baseline / reference arm)
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(budget_s: float, users: int = 256):
-    """Oracle lookup+backward IDs/s on a bounded sample of the workload.
-
-    Sample: the first `users` users' worth of tokens per step (same length
-    distribution, same 4 features and table), cold step untimed, then steps
-    until about `budget_s` seconds of oracle time have been spent."""
-    import oracle
-    ref = oracle.Table(LOG2_SLOTS, DIM, row_dtype=oracle.BF16)
-    cold = W.jagged_batch(0, users=users)
-    ref.lookup(cold.ids, cold.feat_offsets, cold.table_ids)
-    gb = W.grads_normal(7, cold.n, DIM)
+def cpu_baseline(wl: Workload, budget_s: float):
+    """Oracle lookup+backward IDs/s on a bounded sample of the workload: a smaller
+    batch of the same distributions per step (for the jagged workload the first
+    256 users), one untimed cold step, then steps until about `budget_s` seconds
+    of oracle time have been spent."""
     import torch
-    gbits = torch.from_numpy(gb).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-    ref.backward_adam(gbits, grad_dtype=oracle.BF16)
+
+    import oracle
+
+    def grads(seed, n):
+        g = W.grads_normal(seed, n, wl.dim)
+        if wl.grad == "bf16":
+            return torch.from_numpy(g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16), oracle.BF16
+        return g, oracle.F32
+
+    ref = oracle.Table(wl.log2, wl.dim, row_dtype=oracle.BF16 if wl.row == "bf16" else oracle.F32)
+    cold = wl.sample_batch(0)
+    ref.lookup(cold.ids, cold.feat_offsets, cold.table_ids)
+    g, gd = grads(7, cold.n)
+    ref.backward_adam(g, grad_dtype=gd)
     ids_done, t_total, steps = 0, 0.0, 0
     k = 1
     while t_total < budget_s and steps < 10_000:
-        b = W.jagged_batch(k, users=users)
-        g = torch.from_numpy(W.grads_normal(k + 500_000, b.n, DIM)).to(torch.bfloat16).view(torch.int16).numpy()
-        g = g.view(np.uint16)
+        b = wl.sample_batch(k)
+        g, gd = grads(k + 500_000, b.n)
         t0 = time.perf_counter()
         ref.lookup(b.ids, b.feat_offsets, b.table_ids)
-        ref.backward_adam(g, grad_dtype=oracle.BF16)
+        ref.backward_adam(g, grad_dtype=gd)
         t_total += time.perf_counter() - t0
         ids_done += b.n
         steps += 1
         k += 1
     return {"value": ids_done / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{steps} steps of the first {users} users (avg {ids_done // max(1, steps)} IDs/step) "
-                      f"after one untimed cold step; single-threaded C++ oracle, {t_total:.1f} s"}
+            "sample": f"{steps} steps of a reduced batch (avg {ids_done // max(1, steps)} IDs/step) of the same "
+                      f"workload after one untimed cold step; single-threaded C++ oracle, {t_total:.1f} s"}
 
 
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    cb = cpu_baseline(args.cpu_seconds)
+    wl = Workload(args.config, args.users, args.log2_slots)
+    cb = cpu_baseline(wl, args.cpu_seconds)
     line = {
         "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD + " (bounded sample: 256 users per step)"},
+        "config": {"workload": wl.name + " (bounded sample per step, see cpu_baseline.sample)"},
         "cpu_baseline": cb,
         "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -431,12 +538,13 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--pool", type=int, default=8, help="distinct pre-generated batches cycled through")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--users", type=int, default=2048, help="users per batch (smaller cases for profiling)")
-    ap.add_argument("--log2-slots", type=int, default=LOG2_SLOTS)
+    ap.add_argument("--users", type=int, default=2048, help="users per jagged batch (smaller cases for profiling)")
+    ap.add_argument("--log2-slots", type=int, default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
