@@ -241,32 +241,63 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
 
 // ---- reduction + Adam -------------------------------------------------------
 
-// s + e = a + b exactly (Knuth's TwoSum).
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+// ---- packed fp32 pairs ---------------------------------------------------------
+// Two adjacent columns travel in one 64-bit register (low half: the even
+// column) and are combined by the paired fp32 instructions (add/sub
+// .rn.f32x2): each half is rounded to nearest on its own, exactly like the
+// scalar __fadd_rn/__fsub_rn, at one instruction per pair.  Only additions
+// and subtractions are paired: with no product in the chain nothing can be
+// fused, so TwoSum stays exact.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pk(float lo, float hi) {
+  f32x2 d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float2 upk(f32x2 a) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a));
+  return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Two bf16 in one word (low half: the even column) widened to fp32 (exact).
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
+
+// s + e = a + b exactly, per half (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(f32x2 a, f32x2 b, f32x2& s, f32x2& e) {
+  s = add2(a, b);
+  const f32x2 bb = sub2(s, a);
+  e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
 }
 
-// Add x and y (already an exact pair sum s + e of two rows) to the running
-// pair: the two rows' TwoSum does not depend on the running pair, so the
-// serial chain per column is one TwoSum per two rows.
-__device__ __forceinline__ void two_sum_add2(float& hi, float& lo, float x, float y) {
-  float s, e, s2, e2;
+// Add x and y (two rows' pairs) to the running pair (hi, lo), which carries
+// the sum with about twice fp32's precision: the two rows' TwoSum does not
+// depend on the running pair, so the serial chain per column is one TwoSum
+// per two rows.
+__device__ __forceinline__ void two_sum_add2(f32x2& hi, f32x2& lo, f32x2 x, f32x2 y) {
+  f32x2 s, e, s2, e2;
   two_sum(x, y, s, e);
   two_sum(hi, s, s2, e2);
   hi = s2;
-  lo = __fadd_rn(lo, __fadd_rn(e2, e));
+  lo = add2(lo, add2(e2, e));
 }
 
-// a + b = s + e exactly (Knuth's TwoSum); the running pair (hi, lo) carries
-// the sum with about twice fp32's precision.
-__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float x) {
-  const float s = __fadd_rn(hi, x);
-  const float bb = __fsub_rn(s, hi);
-  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
+// Add one row's pair x to the running pair (hi, lo).
+__device__ __forceinline__ void two_sum_add(f32x2& hi, f32x2& lo, f32x2 x) {
+  f32x2 s, e;
+  two_sum(hi, x, s, e);
   hi = s;
-  lo = __fadd_rn(lo, e);
+  lo = add2(lo, e);
 }
 
 // Raw gradient words of one lane's VEC columns: VEC fp32 words, or VEC/2
@@ -295,22 +326,30 @@ __device__ __forceinline__ void load_grad_raw(const void* grads, long long pos, 
   }
 }
 
+// Columns 2k and 2k + 1 of a raw gradient share as an fp32 pair.
 template <int GD, int VEC>
-__device__ __forceinline__ float grad_value(const GradRaw<GD, VEC>& g, int j) {
-  if (GD == MT_F32) return __uint_as_float(g.w[j]);
-  const uint32_t w = g.w[j >> 1];
-  return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));  // bf16 -> fp32 is exact
+__device__ __forceinline__ f32x2 grad_pair(const GradRaw<GD, VEC>& g, int k) {
+  if (GD == MT_F32) return pk(__uint_as_float(g.w[2 * k]), __uint_as_float(g.w[2 * k + 1]));
+  return bf16x2_to_f32x2(g.w[k]);
 }
 
 // One Adam step on columns [col, col + VEC) of a row, every operation
 // rounded once: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
-// w -= step_size * m / (sqrt(v) * inv_sqrt_bc2 + eps).  The moments are
-// streamed four columns at a time to keep few registers live.
+// w -= step_size * m / (sqrt(v) * inv_sqrt_bc2 + eps).  Scalar operations
+// only: a paired multiply followed by a paired add may be contracted into
+// one fused multiply-add by the code generator, which changes the rounding.
+// The moments are streamed four columns at a time to keep few registers live.
 template <int RD, int VEC>
-__device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, int col, const float g[VEC],
+__device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, int col, const f32x2 g2[VEC / 2],
                                           float step_size, float inv_sqrt_bc2) {
   char* rec = row_ptr(p.T, row);
-  float w[VEC];
+  float g[VEC], w[VEC];
+#pragma unroll
+  for (int j = 0; j < VEC / 2; ++j) {
+    const float2 t = upk(g2[j]);
+    g[2 * j] = t.x;
+    g[2 * j + 1] = t.y;
+  }
   if (RD == MT_F32) {
     const float4* e = reinterpret_cast<const float4*>(rec) + col / 4;
 #pragma unroll
@@ -359,10 +398,9 @@ __device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, 
   }
 }
 
-
-__device__ __forceinline__ void store_gsum(float* gsum_out, int u, int d, int col, const float* gs, int vec) {
-  float4* o = reinterpret_cast<float4*>(gsum_out + (size_t)u * d + col);
-  for (int r = 0; r < vec / 4; ++r) o[r] = make_float4(gs[4 * r], gs[4 * r + 1], gs[4 * r + 2], gs[4 * r + 3]);
+__device__ __forceinline__ void store_gsum(float* gsum_out, int u, int d, int col, const f32x2* gs, int vec) {
+  ulonglong2* o = reinterpret_cast<ulonglong2*>(gsum_out + (size_t)u * d + col);
+  for (int r = 0; r < vec / 4; ++r) o[r] = make_ulonglong2(gs[2 * r], gs[2 * r + 1]);
 }
 
 constexpr int kMinTeamShift = 2;                              // teams of at least 4 lanes
@@ -417,7 +455,7 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
 // columns, in TwoSum pairs, UNR rows in flight.
 template <int GD, int VEC, int UNR, bool LOOKAHEAD = false>
 __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* pos, int n, int d, int col,
-                                           float hi[VEC], float lo[VEC]) {
+                                           f32x2 hi[VEC / 2], f32x2 lo[VEC / 2]) {
   for (int q0 = 0; q0 < n; q0 += UNR) {
     if (LOOKAHEAD) {  // pull the next UNR rows toward L2 while these are summed
 #pragma unroll
@@ -435,7 +473,7 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
     for (int r = 0; r < UNR; ++r)
       if (q0 + r < n && pos[q0 + r] >= 0) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) two_sum_add(hi[j], lo[j], grad_value<GD, VEC>(g[r], j));
+        for (int j = 0; j < VEC / 2; ++j) two_sum_add(hi[j], lo[j], grad_pair<GD, VEC>(g[r], j));
       }
   }
 }
@@ -454,7 +492,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // these are summed, and no register holds a row in flight.
 template <int GD, int VEC, int HS>
 __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const int* pos, int n, int d, int col,
-                                                 uint4* ring, float hi[VEC], float lo[VEC]) {
+                                                 uint4* ring, f32x2 hi[VEC / 2], f32x2 lo[VEC / 2]) {
   constexpr int W = GradRaw<GD, VEC>::W;
   constexpr int Q = W / 4;  // 16-byte pieces of one lane's share of a row
   const char* gbase = reinterpret_cast<const char*>(p.grads);
@@ -494,7 +532,7 @@ __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const 
       }
       if (ok0 || ok1) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) two_sum_add2(hi[j], lo[j], grad_value<GD, VEC>(g0, j), grad_value<GD, VEC>(g1, j));
+        for (int j = 0; j < VEC / 2; ++j) two_sum_add2(hi[j], lo[j], grad_pair<GD, VEC>(g0, j), grad_pair<GD, VEC>(g1, j));
       }
     }
   }
@@ -561,9 +599,9 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + col0;
       const bool active = col < d;
-      float hi[VEC], lo[VEC];
+      f32x2 hi[VEC / 2], lo[VEC / 2];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
+      for (int j = 0; j < VEC / 2; ++j) hi[j] = lo[j] = 0ull;
       if (c0 == 0) {  // this team's share of the warp-chunk (at most kTeamShare positions)
         for (int q = lt; q < te - tb; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[tb + q]));
         __syncwarp(team_mask);
@@ -574,24 +612,28 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
       }
       for (int o = team; o < 32; o <<= 1) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          const float h2 = __shfl_xor_sync(kFull, hi[j], o);
-          const float l2 = __shfl_xor_sync(kFull, lo[j], o);
+        for (int j = 0; j < VEC / 2; ++j) {
+          const f32x2 h2 = __shfl_xor_sync(kFull, hi[j], o);
+          const f32x2 l2 = __shfl_xor_sync(kFull, lo[j], o);
           two_sum_add(hi[j], lo[j], h2);
-          lo[j] = __fadd_rn(lo[j], l2);
+          lo[j] = add2(lo[j], l2);
         }
       }
       if (tiw == 0 && active) {
         if (hinfo.y == 1) {
-          float gs[VEC];
+          f32x2 gs[VEC / 2];
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
+          for (int j = 0; j < VEC / 2; ++j) gs[j] = add2(hi[j], lo[j]);
           if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
           if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
         } else {
           double* a = p.acc64 + (size_t)h * d + col;
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) atomicAdd(a + j, (double)hi[j] + (double)lo[j]);
+          for (int j = 0; j < VEC / 2; ++j) {
+            const float2 x = upk(hi[j]), y = upk(lo[j]);
+            atomicAdd(a + 2 * j, (double)x.x + (double)y.x);
+            atomicAdd(a + 2 * j + 1, (double)x.y + (double)y.y);
+          }
         }
       }
     }
@@ -606,10 +648,10 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
         for (int c0 = 0; c0 < d; c0 += team * VEC) {
           const int col = c0 + col0;
           if (col >= d) continue;
-          float gs[VEC];
+          f32x2 gs[VEC / 2];
           const double* a = p.acc64 + (size_t)h * d + col;
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) gs[j] = (float)__ldcg(a + j);
+          for (int j = 0; j < VEC / 2; ++j) gs[j] = pk((float)__ldcg(a + 2 * j), (float)__ldcg(a + 2 * j + 1));
           if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
           if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
         }
@@ -692,18 +734,18 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + col0;
       if (col >= d) continue;
-      float hi[VEC], lo[VEC];
+      f32x2 hi[VEC / 2], lo[VEC / 2];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.f;
+      for (int j = 0; j < VEC / 2; ++j) hi[j] = lo[j] = 0ull;
       accumulate<GD, VEC, UNR>(p, my_pos, cnt, d, col, hi, lo);
       if (c0 == 0) {  // the next unique's gradient rows (one 128-byte line per lane-position)
 #pragma unroll
         for (int k = 0; k < kPosRegs; ++k)
           if (npos[k] >= 0) prefetch_l2(reinterpret_cast<const char*>(p.grads) + (size_t)npos[k] * d * gbytes);
       }
-      float gs[VEC];
+      f32x2 gs[VEC / 2];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) gs[j] = __fadd_rn(hi[j], lo[j]);
+      for (int j = 0; j < VEC / 2; ++j) gs[j] = add2(hi[j], lo[j]);
       if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
       if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
     }
