@@ -260,7 +260,7 @@ int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const 
   p.gsum_out = gsum_out;
   p.bsum = reinterpret_cast<int32_t*>(w + L.bsum);
   p.boff = reinterpret_cast<int32_t*>(w + L.boff);
-  p.cursor = reinterpret_cast<int32_t*>(w + L.cursor);
+  p.seg = reinterpret_cast<int2*>(w + L.seg);
   p.chunks = reinterpret_cast<int4*>(w + L.chunks);
   p.heavy_info = reinterpret_cast<int4*>(w + L.heavy_info);
   p.pos_sorted = reinterpret_cast<int32_t*>(w + L.pos_sorted);

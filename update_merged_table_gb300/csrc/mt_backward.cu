@@ -12,7 +12,7 @@
 //  k_bw_blocksum     per block of uniques: sums of positions, of heavy
 //                    warp-chunks and of heavy uniques (more than kChunk
 //                    positions); block 0 advances the table's step counter.
-//  k_bw_offsets      per unique: segment start; per light unique one chunk
+//  k_bw_offsets      per unique: {segment start, count}; per light unique one chunk
 //                    descriptor, per heavy unique its warp-chunk descriptors
 //                    and zeroed fp64 accumulators (each block sums the block
 //                    totals before it itself).
@@ -81,13 +81,19 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
     p.work[0] = 0;
   }
   const long long U = *p.num_unique;
-  const long long u0 = (long long)blockIdx.x * kScanTile;
+  const long long u0 = (long long)blockIdx.x * kScanTile + threadIdx.x;
+  int c[kScanTile / kScanThreads];  // every load in flight before the sums
+#pragma unroll
+  for (int k = 0; k < kScanTile / kScanThreads; ++k) {
+    const long long u = u0 + (long long)k * kScanThreads;
+    c[k] = u < U ? __ldg(&p.counts[u]) : 0;
+  }
   int v[3] = {0, 0, 0};
-  for (long long u = u0 + threadIdx.x; u < U && u < u0 + kScanTile; u += kScanThreads) {
-    const int c = p.counts[u];
-    v[0] += c;
-    v[1] += warp_chunks(c, p.warp_chunk);
-    v[2] += c > kChunk;
+#pragma unroll
+  for (int k = 0; k < kScanTile / kScanThreads; ++k) {
+    v[0] += c[k];
+    v[1] += warp_chunks(c[k], p.warp_chunk);
+    v[2] += c[k] > kChunk;
   }
   int ex[3], tot[3];
   block_scan3<kScanThreads>(v, ex, tot, s_warp);
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
 
 constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_offsets
 
-// Per unique: segment start (cursor).  A light unique gets its team-chunk
+// Per unique: {segment start, count}.  A light unique gets its team-chunk
 // descriptor {start, end, row, u} at HWC + its rank among light uniques (HWC
 // = warp-chunks of all heavy uniques, which come first); a heavy unique gets
 // {u, warp-chunks, segment start, first chunk}, its warp-chunk descriptors,
@@ -134,11 +140,15 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   }
   if ((long long)b * kScanTile >= U) return;  // uniform over the block
   const long long u0 = (long long)b * kScanTile + (long long)threadIdx.x * kUPT;
-  int c[kUPT];
+  int c[kUPT], rows[kUPT];  // every load in flight before the scan and the stores
+#pragma unroll
+  for (int k = 0; k < kUPT; ++k) {
+    c[k] = u0 + k < U ? __ldg(&p.counts[u0 + k]) : 0;
+    rows[k] = u0 + k < U ? __ldg(&p.unique_rows[u0 + k]) : -1;
+  }
   int v[3] = {0, 0, 0};
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
-    c[k] = u0 + k < U ? p.counts[u0 + k] : 0;
     v[0] += c[k];
     v[1] += warp_chunks(c[k], p.warp_chunk);
     v[2] += c[k] > kChunk;
@@ -154,8 +164,8 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   for (int k = 0; k < kUPT; ++k) {
     const long long u = u0 + k;
     if (u >= U) break;
-    p.cursor[u] = seg;
-    const int row = p.unique_rows[u];
+    p.seg[u] = make_int2(seg, c[k]);
+    const int row = rows[k];
     if (c[k] <= kChunk) {
       p.chunks[HWC + (int)(u - hv)] = make_int4(seg, seg + c[k], row, (int)u);
     } else {
@@ -179,7 +189,7 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
 
 // Positions grouped by unique: each tile groups its positions by unique in
 // shared memory, reserves room for each group with one atomic on the
-// unique's cursor, then scatters the positions.
+// unique's segment start, then scatters the positions.
 __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
   __shared__ int32_t s_hkey[kHS];
   __shared__ int32_t s_hcnt[kHS];
@@ -230,7 +240,7 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
   __syncthreads();
   for (int h = tid; h < kHS; h += kThreads) {
     const int u = s_hkey[h];
-    if (u >= 0) s_hcnt[h] = atomicAdd(&p.cursor[u], s_hcnt[h]);  // group count -> group base
+    if (u >= 0) s_hcnt[h] = atomicAdd(&p.seg[u].x, s_hcnt[h]);  // group count -> group base
   }
   __syncthreads();
   for (int lp = tid; lp < cnt; lp += kThreads) {
@@ -415,7 +425,8 @@ __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   bool bad = false;
   for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < p.n; i0 += 4 * stride) {
-    int u[4], r[4], cnt[4], cur[4];  // four positions' loads in flight
+    int u[4], r[4];
+    int2 sg[4];  // four positions' loads in flight
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const long long i = i0 + k * stride;
@@ -425,17 +436,16 @@ __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const bool ok = u[k] >= 0 && u[k] < U;
-      cnt[k] = ok ? __ldg(&p.counts[u[k]]) : 0;
-      cur[k] = ok ? __ldg(&p.cursor[u[k]]) : 0;
+      sg[k] = ok ? __ldg(&p.seg[u[k]]) : make_int2(0, 0);  // {segment start, count}
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       if (u[k] < 0) continue;
-      if (u[k] >= U || r[k] < 0 || r[k] >= cnt[k]) {
+      if (u[k] >= U || r[k] < 0 || r[k] >= sg[k].y) {
         bad = true;
         continue;
       }
-      p.pos_sorted[cur[k] + r[k]] = (int32_t)(i0 + k * stride);
+      p.pos_sorted[sg[k].x + r[k]] = (int32_t)(i0 + k * stride);
     }
   }
   if (bad) latch_error(p.T.hdr, MT_EINVAL);
@@ -446,6 +456,7 @@ __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
 __device__ __forceinline__ int valid_pos(const BackwardParams& p, int v) {
   return (unsigned)v < (unsigned long long)p.n ? v : -1;
 }
+__device__ __forceinline__ bool pos_ok(const BackwardParams& p, int v) { return (unsigned)v < (unsigned long long)p.n; }
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
@@ -487,10 +498,12 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // accumulate() with the gradient rows brought in by asynchronous 16-byte
-// copies into a two-stage ring of HS rows in shared memory (this thread's
-// slots only, so no barrier is needed): the next HS rows are in flight while
-// these are summed, and no register holds a row in flight.
-template <int GD, int VEC, int HS>
+// copies into a ring of NST stages of HS rows in shared memory (this
+// thread's slots only, so no barrier is needed): NST - 1 stages are in
+// flight while one is summed, and no register holds a row in flight.  Every
+// stage commits one copy group (empty past the end), so waiting until at
+// most NST - 1 groups are pending means the stage about to be summed landed.
+template <int GD, int VEC, int HS, int NST>
 __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const int* pos, int n, int d, int col,
                                                  uint4* ring, f32x2 hi[VEC / 2], f32x2 lo[VEC / 2]) {
   constexpr int W = GradRaw<GD, VEC>::W;
@@ -501,7 +514,7 @@ __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const 
 #pragma unroll
     for (int r = 0; r < HS; ++r) {
       const int qq = q0 + r;
-      if (qq < n && pos[qq] >= 0) {
+      if (qq < n && pos_ok(p, pos[qq])) {
         const char* src = gbase + ((size_t)pos[qq] * d + col) * ges;
 #pragma unroll
         for (int q = 0; q < Q; ++q) cp_async16(ring + ((st * HS + r) * Q + q) * 256, src + 16 * q);
@@ -509,19 +522,16 @@ __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const 
     }
     cp_async_commit();
   };
-  issue(0, 0);
+#pragma unroll
+  for (int s0 = 0; s0 < NST - 1; ++s0) issue(s0, s0 * HS);
   int st = 0;
-  for (int q0 = 0; q0 < n; q0 += HS, st ^= 1) {
-    if (q0 + HS < n) {
-      issue(st ^ 1, q0 + HS);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+  for (int q0 = 0; q0 < n; q0 += HS) {
+    issue(st == 0 ? NST - 1 : st - 1, q0 + (NST - 1) * HS);  // the slot summed last round
+    cp_async_wait<NST - 1>();
 #pragma unroll
     for (int r = 0; r < HS; r += 2) {
-      const bool ok0 = q0 + r < n && pos[q0 + r] >= 0;
-      const bool ok1 = r + 1 < HS && q0 + r + 1 < n && pos[q0 + r + 1] >= 0;
+      const bool ok0 = q0 + r < n && pos_ok(p, pos[q0 + r]);
+      const bool ok1 = r + 1 < HS && q0 + r + 1 < n && pos_ok(p, pos[q0 + r + 1]);
       GradRaw<GD, VEC> g0, g1;
 #pragma unroll
       for (int q = 0; q < Q; ++q) {
@@ -535,13 +545,17 @@ __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const 
         for (int j = 0; j < VEC / 2; ++j) two_sum_add2(hi[j], lo[j], grad_pair<GD, VEC>(g0, j), grad_pair<GD, VEC>(g1, j));
       }
     }
+    st = st + 1 == NST ? 0 : st + 1;
   }
+  cp_async_wait<0>();  // nothing of this call stays in flight (the groups past the end are empty)
 }
 
-// Rows per ring stage of the heavy kernel (0: keep rows in registers).
+// Rows per ring stage of the heavy kernel (0: keep rows in registers) and
+// stages per ring: 16-byte pieces per lane and row x rows x stages = 16.
+constexpr int kHeavyStages = 4;
 template <int RD, int GD>
 __host__ __device__ constexpr int heavy_stage_rows() {
-  return (GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W % 4) ? 0 : 6 / (GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W / 4);
+  return (GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W % 4) ? 0 : 4 / (GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W / 4);
 }
 
 // Heavy uniques (more than kChunk positions): each warp takes a warp-chunk;
@@ -557,10 +571,10 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
   constexpr int UNR = 32 / GradRaw<GD, VEC>::W;  // register path: gradient rows in flight per lane
   constexpr int HS = heavy_stage_rows<RD, GD>();
   constexpr int Q = GradRaw<GD, VEC>::W / 4;
-  extern __shared__ __align__(16) uint4 dsmem[];  // [2][HS][Q][256] ring, then positions
+  extern __shared__ __align__(16) uint4 dsmem[];  // [kHeavyStages][HS][Q][256] ring, then positions
   __shared__ float s_scal[2];
   uint4* ring = dsmem + threadIdx.x;
-  int* s_pos = reinterpret_cast<int*>(dsmem + (HS > 0 ? 2 * HS * Q * 256 : 0));
+  int* s_pos = reinterpret_cast<int*>(dsmem + (HS > 0 ? kHeavyStages * HS * Q * 256 : 0));
   if (threadIdx.x == 0) {
     const double t = (double)p.T.hdr->step;
     const double bc1 = 1.0 - pow((double)p.beta1, t);
@@ -607,7 +621,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
         __syncwarp(team_mask);
       }
       if (active) {
-        if (HS > 0) accumulate_async<GD, VEC, (HS > 0 ? HS : 1)>(p, my_pos, te - tb, d, col, ring, hi, lo);
+        if (HS > 0) accumulate_async<GD, VEC, (HS > 0 ? HS : 1), kHeavyStages>(p, my_pos, te - tb, d, col, ring, hi, lo);
         else accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
       }
       for (int o = team; o < 32; o <<= 1) {
@@ -769,7 +783,8 @@ cudaError_t launch_reduce(const BackwardParams& p, cudaStream_t s) {
   const int idx = RD * 2 + GD;
   constexpr int HS = heavy_stage_rows<RD, GD>();
   constexpr int Q = GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W / 4;
-  const size_t heavy_smem = (size_t)(HS > 0 ? 2 * HS * Q * 256 : 0) * 16 + (size_t)(256 >> p.team_shift) * kTeamShare * 4;
+  const size_t heavy_smem =
+      (size_t)(HS > 0 ? kHeavyStages * HS * Q * 256 : 0) * 16 + (size_t)(256 >> p.team_shift) * kTeamShare * 4;
   if (g_heavy_grid[idx] == 0 || g_heavy_smem[idx] != heavy_smem) {
     int dev = 0, sms = 0, per_h = 0, per_l = 0;
     cudaGetDevice(&dev);
@@ -811,7 +826,7 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
   const size_t nn = (size_t)(n > 0 ? n : 1);
   L.bsum = take((size_t)L.nblk * 3 * 4);
   L.boff = take(((size_t)L.nblk + 1) * 3 * 4);
-  L.cursor = take(nn * 4);
+  L.seg = take(nn * 8);
   L.chunks = take(nn * 16);
   L.heavy_info = take((size_t)L.heavy_cap * 16);
   L.pos_sorted = take(nn * 4);

@@ -60,7 +60,7 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s);
 // ---- backward ---------------------------------------------------------------
 
 constexpr int kChunk = 32;          // most positions a light unique has (one team-chunk)
-constexpr int kTeamShare = 128;     // positions per team in a heavy unique's warp-chunk
+constexpr int kTeamShare = 64;      // positions per team in a heavy unique's warp-chunk
 constexpr int kScanTile = 2048;     // uniques per scan block
 constexpr int kScanThreads = 256;
 
@@ -80,7 +80,7 @@ struct BackwardParams {
   // workspace
   int32_t* bsum;        // [nblk * 3] per scan block: sums of counts, heavy chunks, heavy uniques
   int32_t* boff;        // [(nblk + 1) * 3] exclusive offsets (+ totals)
-  int32_t* cursor;      // [n] segment start of each unique, advanced to its end by the fill
+  int2* seg;            // [n] {segment start, count} of each unique; the fill advances the start to the end
   int4* chunks;         // [n] descriptors {start, end, row, u or -(heavy index + 1)}: the warp-chunks of
                         //     heavy uniques (more than kChunk positions) first, then one team-chunk per light unique
   int4* heavy_info;     // [heavy_cap] {u, warp-chunks, segment start, first chunk} of each heavy unique
@@ -95,7 +95,7 @@ struct BackwardParams {
 };
 
 struct BackwardWsLayout {
-  size_t bsum, boff, cursor, chunks, heavy_info, pos_sorted, acc64, arrive, work, total;
+  size_t bsum, boff, seg, chunks, heavy_info, pos_sorted, acc64, arrive, work, total;
   long long heavy_cap;
   int nblk, ntiles;
 };
