@@ -170,20 +170,37 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
       p.chunks[HWC + (int)(u - hv)] = make_int4(seg, seg + c[k], row, (int)u);
     } else {
       const int nw = warp_chunks(c[k], p.warp_chunk);
-      p.heavy_info[hv] = make_int4((int)u, nw, seg, hch);
-      for (int q = 0; q < nw; ++q) {
-        const int start = seg + q * p.warp_chunk;
-        p.chunks[hch + q] = make_int4(start, min(start + p.warp_chunk, seg + c[k]), row, -(hv + 1));
-      }
-      if (nw > 1) {
-        double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)hv * d);
-        for (int q = 0; q < d / 2; ++q) a[q] = make_double2(0.0, 0.0);
-        p.arrive[hv] = 0;
-      }
+      p.heavy_info[hv] = make_int4((int)u, nw, seg, hch);  // its warp-chunks are written by the grouping kernel
       ++hv;
       hch += nw;
     }
     seg += c[k];
+  }
+}
+
+// Warp-chunk descriptors of the heavy uniques, a warp per heavy unique over
+// the whole grid (the hottest IDs are seen first, so their uniques cluster
+// in the first offsets block); a unique with several warp-chunks also gets
+// its fp64 accumulator and arrival count cleared.  Called by every thread of
+// the grouping kernels before they group.
+__device__ __forceinline__ void write_heavy_chunks(const BackwardParams& p) {
+  const int H = p.boff[(size_t)p.nblk * 3 + 2];
+  const int d = (int)p.T.dim;
+  const int lane = threadIdx.x & 31;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nw_grid = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long h = gw; h < H; h += nw_grid) {
+    const int4 hi = __ldg(&p.heavy_info[h]);  // {u, warp-chunks, segment start, first warp-chunk}
+    const int cnt = __ldg(&p.seg[hi.x]).y, row = __ldg(&p.unique_rows[hi.x]);
+    for (int q = lane; q < hi.y; q += 32) {
+      const int start = hi.z + q * p.warp_chunk;
+      p.chunks[hi.w + q] = make_int4(start, min(start + p.warp_chunk, hi.z + cnt), row, -(int)(h + 1));
+    }
+    if (hi.y > 1) {
+      double2* a = reinterpret_cast<double2*>(p.acc64 + (size_t)h * d);
+      for (int q = lane; q < d / 2; q += 32) a[q] = make_double2(0.0, 0.0);
+      if (lane == 0) p.arrive[h] = 0;
+    }
   }
 }
 
@@ -198,6 +215,7 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
   const int tid = threadIdx.x, lane = tid & 31;
   const long long base = (long long)blockIdx.x * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
+  write_heavy_chunks(p);
   const long long U = *p.num_unique;
   for (int h = tid; h < kHS; h += kThreads) {
     s_hkey[h] = -1;
@@ -421,6 +439,7 @@ constexpr int kMaxTeams = 256 >> kMinTeamShift;               // per block
 // index that does not belong to the lookup result (a caller passing some
 // other buffer) is skipped and latches MT_EINVAL instead of writing.
 __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
+  write_heavy_chunks(p);
   const long long U = *p.num_unique;
   const long long stride = (long long)gridDim.x * blockDim.x;
   bool bad = false;
