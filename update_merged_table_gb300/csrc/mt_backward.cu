@@ -512,6 +512,12 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
+// 16-byte asynchronous copy that reads src_bytes (16 or 0) from gmem and
+// fills the rest of the 16 bytes with zeros: with 0, nothing is read.
+__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, int src_bytes) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(src_bytes) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -520,24 +526,26 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // copies into a ring of NST stages of HS rows in shared memory (this
 // thread's slots only, so no barrier is needed): NST - 1 stages are in
 // flight while one is summed, and no register holds a row in flight.  Every
-// stage commits one copy group (empty past the end), so waiting until at
-// most NST - 1 groups are pending means the stage about to be summed landed.
+// stage commits one copy group, so waiting until at most NST - 1 groups are
+// pending means the stage about to be summed landed.
 template <int GD, int VEC, int HS, int NST>
 __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const int* pos, int n, int d, int col,
                                                  uint4* ring, f32x2 hi[VEC / 2], f32x2 lo[VEC / 2]) {
   constexpr int W = GradRaw<GD, VEC>::W;
   constexpr int Q = W / 4;  // 16-byte pieces of one lane's share of a row
-  const char* gbase = reinterpret_cast<const char*>(p.grads);
-  const size_t ges = GD == MT_F32 ? 4 : 2;
+  const size_t rowb = (size_t)d * (GD == MT_F32 ? 4 : 2);
+  const char* cbase = reinterpret_cast<const char*>(p.grads) + (size_t)col * (GD == MT_F32 ? 4 : 2);
+  // a row past the end or at an invalid position lands as zeros (nothing is
+  // read for it), which the exact pair sum adds without change
   auto issue = [&](int st, int q0) {
 #pragma unroll
     for (int r = 0; r < HS; ++r) {
       const int qq = q0 + r;
-      if (qq < n && pos_ok(p, pos[qq])) {
-        const char* src = gbase + ((size_t)pos[qq] * d + col) * ges;
+      const int v = qq < n ? pos[qq] : -1;
+      const bool ok = pos_ok(p, v);
+      const char* src = ok ? cbase + (size_t)v * rowb : cbase;
 #pragma unroll
-        for (int q = 0; q < Q; ++q) cp_async16(ring + ((st * HS + r) * Q + q) * 256, src + 16 * q);
-      }
+      for (int q = 0; q < Q; ++q) cp_async16_zfill(ring + ((st * HS + r) * Q + q) * 256, src + 16 * q, ok ? 16 : 0);
     }
     cp_async_commit();
   };
@@ -549,24 +557,20 @@ __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const 
     cp_async_wait<NST - 1>();
 #pragma unroll
     for (int r = 0; r < HS; r += 2) {
-      const bool ok0 = q0 + r < n && pos_ok(p, pos[q0 + r]);
-      const bool ok1 = r + 1 < HS && q0 + r + 1 < n && pos_ok(p, pos[q0 + r + 1]);
       GradRaw<GD, VEC> g0, g1;
 #pragma unroll
       for (int q = 0; q < Q; ++q) {
-        const uint4 t0 = ok0 ? ring[((st * HS + r) * Q + q) * 256] : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 t1 = ok1 ? ring[((st * HS + r + 1) * Q + q) * 256] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 t0 = ring[((st * HS + r) * Q + q) * 256];
+        const uint4 t1 = r + 1 < HS ? ring[((st * HS + r + 1) * Q + q) * 256] : make_uint4(0u, 0u, 0u, 0u);
         g0.w[4 * q] = t0.x; g0.w[4 * q + 1] = t0.y; g0.w[4 * q + 2] = t0.z; g0.w[4 * q + 3] = t0.w;
         g1.w[4 * q] = t1.x; g1.w[4 * q + 1] = t1.y; g1.w[4 * q + 2] = t1.z; g1.w[4 * q + 3] = t1.w;
       }
-      if (ok0 || ok1) {
 #pragma unroll
-        for (int j = 0; j < VEC / 2; ++j) two_sum_add2(hi[j], lo[j], grad_pair<GD, VEC>(g0, j), grad_pair<GD, VEC>(g1, j));
-      }
+      for (int j = 0; j < VEC / 2; ++j) two_sum_add2(hi[j], lo[j], grad_pair<GD, VEC>(g0, j), grad_pair<GD, VEC>(g1, j));
     }
     st = st + 1 == NST ? 0 : st + 1;
   }
-  cp_async_wait<0>();  // nothing of this call stays in flight (the groups past the end are empty)
+  cp_async_wait<0>();  // nothing of this call stays in flight
 }
 
 // Rows per ring stage of the heavy kernel (0: keep rows in registers) and
