@@ -182,6 +182,7 @@ struct Table {
   float init_scale;
   int64_t num_rows;
   int64_t step = 0;
+  double b1pow = 1.0, b2pow = 1.0;  // beta-power accumulators b1^t, b2^t
   int error = 0;
   std::unordered_map<uint64_t, Row> rows;
   Simulator* sim = nullptr;
@@ -388,11 +389,15 @@ int orc_backward_adam(void* h, const void* grads, int grad_dtype, float lr, floa
   // Kingma & Ba's m_hat / (sqrt(v_hat) + eps) with m_hat = m / (1 - b1^t) and
   // sqrt(v_hat) = sqrt(v) / sqrt(1 - b2^t): the two bias corrections enter as
   // the per-step scalars step_size = lr / (1 - b1^t) and
-  // inv_sqrt_bc2 = 1 / sqrt(1 - b2^t).
+  // inv_sqrt_bc2 = 1 / sqrt(1 - b2^t).  b1^t and b2^t are the article's
+  // beta-power accumulators (section 3.2): one multiply by the step's beta
+  // each step, starting from 1.
   const float omb1 = (float)(1.0 - (double)beta1);
   const float omb2 = (float)(1.0 - (double)beta2);
-  const double bc1 = 1.0 - std::pow((double)beta1, (double)t->step);
-  const double bc2 = 1.0 - std::pow((double)beta2, (double)t->step);
+  t->b1pow *= (double)beta1;
+  t->b2pow *= (double)beta2;
+  const double bc1 = 1.0 - t->b1pow;
+  const double bc2 = 1.0 - t->b2pow;
   const float step_size = (float)((double)lr / bc1);
   const float inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
   for (int64_t u = 0; u < U; ++u) {
