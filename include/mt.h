@@ -209,7 +209,10 @@ size_t mt_backward_workspace_bytes(const mt_table* t, int64_t n);
  * with step_size = lr / (1-b1^t) and inv_sqrt_bc2 = 1 / sqrt(1-b2^t), i.e.
  * Kingma & Ba's m_hat / (sqrt(v_hat) + eps) with the bias corrections folded
  * into per-step scalars (1-b1, 1-b2 and both scalars evaluated in double,
- * then rounded to fp32; every per-element operation rounds once).
+ * then rounded to fp32; every per-element operation rounds once).  b1^t and
+ * b2^t are the table's beta-power accumulators (Meituan TensorFlow article,
+ * section 3.2): starting from 1, each call multiplies them (in double) by
+ * that call's b1 and b2.
  * Rows absent from the batch are not touched.
  *  grads      device [n, d] of grad_dtype (MT_F32 or MT_BF16).
  *  gsum_out   device fp32 [n, d] or NULL: the first U rows receive g_u.

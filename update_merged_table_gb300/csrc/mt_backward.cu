@@ -11,7 +11,8 @@
 // Kernels, in launch order:
 //  k_bw_blocksum     per block of uniques: sums of positions, of heavy
 //                    warp-chunks and of heavy uniques (more than kChunk
-//                    positions); block 0 advances the table's step counter.
+//                    positions); one extra block advances the table's step
+//                    counter and beta powers and computes the Adam scalars.
 //  k_bw_offsets      per unique: {segment start, count}; per light unique one chunk
 //                    descriptor, per heavy unique its warp-chunk descriptors
 //                    and zeroed fp64 accumulators (each block sums the block
@@ -73,12 +74,26 @@ __device__ __forceinline__ void block_scan3(const int v[3], int ex[3], int tot[3
 __device__ __forceinline__ int warp_chunks(int c, int wc) { return c > kChunk ? (c + wc - 1) / wc : 0; }
 
 // Sums over a block of uniques: positions, chunks of heavy (multi-chunk)
-// uniques, heavy uniques.  Block 0 advances the table's step counter.
+// uniques, heavy uniques.  The block after the last one advances the
+// table's step counter and beta-power accumulators and computes the step's
+// Adam scalars.
 __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    p.T.hdr->step += 1;
-    p.work[0] = 0;
+  if (blockIdx.x == p.nblk) {  // the extra block: step counter and this step's Adam scalars
+    if (threadIdx.x == 0) {
+      p.T.hdr->step += 1;
+      p.work[0] = 0;
+      // the beta-power accumulators advance by one multiply each (in
+      // double); then, rounded once to fp32, step_size = lr / (1 - b1^t)
+      // and inv_sqrt_bc2 = 1 / sqrt(1 - b2^t)
+      const double b1t = __dmul_rn(p.T.hdr->b1pow, (double)p.beta1);
+      const double b2t = __dmul_rn(p.T.hdr->b2pow, (double)p.beta2);
+      p.T.hdr->b1pow = b1t;
+      p.T.hdr->b2pow = b2t;
+      p.work[2] = __float_as_int((float)__ddiv_rn((double)p.lr, __dsub_rn(1.0, b1t)));
+      p.work[3] = __float_as_int((float)__ddiv_rn(1.0, __dsqrt_rn(__dsub_rn(1.0, b2t))));
+    }
+    return;
   }
   const long long U = *p.num_unique;
   const long long u0 = (long long)blockIdx.x * kScanTile + threadIdx.x;
@@ -366,7 +381,9 @@ __device__ __forceinline__ f32x2 grad_pair(const GradRaw<GD, VEC>& g, int k) {
 // w -= step_size * m / (sqrt(v) * inv_sqrt_bc2 + eps).  Scalar operations
 // only: a paired multiply followed by a paired add may be contracted into
 // one fused multiply-add by the code generator, which changes the rounding.
-// The moments are streamed four columns at a time to keep few registers live.
+// The moments are streamed four columns at a time to keep few registers
+// live; the record is written back with evict-first stores (it is not read
+// again this step, and it would push prefetched lines out of L2).
 template <int RD, int VEC>
 __device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, int col, const f32x2 g2[VEC / 2],
                                           float step_size, float inv_sqrt_bc2) {
@@ -408,13 +425,13 @@ __device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, 
       const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v[k]), inv_sqrt_bc2), p.eps);
       w[j] = __fsub_rn(w[j], __fmul_rn(step_size, __fdiv_rn(m[k], den)));
     }
-    mp[q] = make_float4(m[0], m[1], m[2], m[3]);
-    vp[q] = make_float4(v[0], v[1], v[2], v[3]);
+    __stcs(mp + q, make_float4(m[0], m[1], m[2], m[3]));  // written once per step: evict first
+    __stcs(vp + q, make_float4(v[0], v[1], v[2], v[3]));
   }
   if (RD == MT_F32) {
     float4* e = reinterpret_cast<float4*>(rec) + col / 4;
 #pragma unroll
-    for (int q = 0; q < VEC / 4; ++q) e[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    for (int q = 0; q < VEC / 4; ++q) __stcs(e + q, make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
   } else {
     uint32_t ww[4];
 #pragma unroll
@@ -422,7 +439,7 @@ __device__ __forceinline__ void adam_cols(const BackwardParams& p, int32_t row, 
       __nv_bfloat162 b2 = __floats2bfloat162_rn(w[2 * q], w[2 * q + 1]);
       ww[q] = *reinterpret_cast<uint32_t*>(&b2);
     }
-    *(reinterpret_cast<uint4*>(rec) + col / 8) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+    __stcs(reinterpret_cast<uint4*>(rec) + col / 8, make_uint4(ww[0], ww[1], ww[2], ww[3]));
   }
 }
 
@@ -595,18 +612,10 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
   constexpr int HS = heavy_stage_rows<RD, GD>();
   constexpr int Q = GradRaw<GD, VEC>::W / 4;
   extern __shared__ __align__(16) uint4 dsmem[];  // [kHeavyStages][HS][Q][256] ring, then positions
-  __shared__ float s_scal[2];
   uint4* ring = dsmem + threadIdx.x;
   int* s_pos = reinterpret_cast<int*>(dsmem + (HS > 0 ? kHeavyStages * HS * Q * 256 : 0));
-  if (threadIdx.x == 0) {
-    const double t = (double)p.T.hdr->step;
-    const double bc1 = 1.0 - pow((double)p.beta1, t);
-    const double bc2 = 1.0 - pow((double)p.beta2, t);
-    s_scal[0] = (float)((double)p.lr / bc1);
-    s_scal[1] = (float)(1.0 / sqrt(bc2));
-  }
-  __syncthreads();
-  const float step_size = s_scal[0], inv_sqrt_bc2 = s_scal[1];
+  const float step_size = __int_as_float(__ldg(&p.work[2]));  // set by k_bw_blocksum
+  const float inv_sqrt_bc2 = __int_as_float(__ldg(&p.work[3]));
 
   const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
@@ -706,17 +715,9 @@ template <int RD, int GD>
 __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams p) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;
   constexpr int UNR = 16 / GradRaw<GD, VEC>::W;  // gradient rows in flight per lane (16 raw words)
-  __shared__ float s_scal[2];
   __shared__ int s_pos[kMaxTeams * kChunk];
-  if (threadIdx.x == 0) {
-    const double t = (double)p.T.hdr->step;
-    const double bc1 = 1.0 - pow((double)p.beta1, t);
-    const double bc2 = 1.0 - pow((double)p.beta2, t);
-    s_scal[0] = (float)((double)p.lr / bc1);
-    s_scal[1] = (float)(1.0 / sqrt(bc2));
-  }
-  __syncthreads();
-  const float step_size = s_scal[0], inv_sqrt_bc2 = s_scal[1];
+  const float step_size = __int_as_float(__ldg(&p.work[2]));  // set by k_bw_blocksum
+  const float inv_sqrt_bc2 = __int_as_float(__ldg(&p.work[3]));
 
   const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
@@ -863,7 +864,7 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
 cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
   {
     MT_LAUNCH("k_bw_blocksum", s);
-    k_bw_blocksum<<<p.nblk, kScanThreads, 0, s>>>(p);
+    k_bw_blocksum<<<p.nblk + 1, kScanThreads, 0, s>>>(p);  // + the block that sets up the step
   }
   {
     MT_LAUNCH("k_bw_offsets", s);

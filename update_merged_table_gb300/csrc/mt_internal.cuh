@@ -37,7 +37,8 @@ struct __align__(256) Header {
   long long free_top;      // rows on the free stack
   long long step;          // Adam steps taken
   long long export_count;  // scratch for mt_export
-  long long pad1[4];
+  double b1pow, b2pow;     // Adam's beta-power accumulators: b1^t and b2^t, one multiply per step
+  long long pad1[2];
   // mt_stats accumulators
   unsigned long long live, tombs, disp;
   unsigned long long hist[MT_HIST_BINS];

@@ -87,7 +87,7 @@ struct BackwardParams {
   int32_t* pos_sorted;  // [n] positions grouped by unique
   double* acc64;        // [heavy_cap * d] cross-chunk sums of heavy uniques
   int32_t* arrive;      // [heavy_cap] chunks finished per heavy unique
-  int32_t* work;        // [4] work counters (heavy warp-chunks handed out), zeroed per call
+  int32_t* work;        // [4] heavy warp-chunks handed out (zeroed per call), -, step_size and inv_sqrt_bc2 (fp32 bits)
   int nblk;
   int ntiles;
   int team_shift;       // log2 lanes per team (one team covers VEC columns per lane)

@@ -18,6 +18,8 @@ __global__ void k_table_init(const TableDev T) {
     T.hdr->error = 0;
     T.hdr->free_top = R;
     T.hdr->step = 0;
+    T.hdr->b1pow = 1.0;
+    T.hdr->b2pow = 1.0;
   }
 }
 
