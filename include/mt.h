@@ -46,7 +46,8 @@ enum {
   MT_EFULL = -3,    /* device: probe limit reached or row pool exhausted */
   MT_EKEY = -4,     /* device: an ID outside [0, 2^56) */
   MT_ECUDA = -5,    /* a CUDA runtime call failed */
-  MT_ETOOBIG = -6   /* batch larger than a fixed-size entry point allows (mt_lookup_static) */
+  MT_ETOOBIG = -6,  /* batch larger than a fixed-size entry point allows (mt_lookup_static) */
+  MT_ETIMEOUT = -7  /* device: a bounded wait inside a kernel gave up; that call's results are invalid */
 };
 
 /* Element types of rows and gradients. */
@@ -186,7 +187,7 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
- *  - Every GPU that loads the library holds the array (3 MiB) until exit.
+ *  - Every GPU that loads the library holds the array (4 MiB) until exit.
  *  - All calls share the array: calls whose work overlaps on the GPU (other
  *    streams or host threads) race on it.  The array keeps the last call's
  *    contents; each call clears what it needs cleared.

@@ -23,7 +23,7 @@ import numpy as np
 __all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "KEY_EMPTY", "KEY_TOMBSTONE",
            "ABI_FUNCTIONS", "profile_enable", "profile_report", "kernel_launches"]
 
-MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA, MT_ETOOBIG = 0, -1, -2, -3, -4, -5, -6
+MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA, MT_ETOOBIG, MT_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
 LOOKUP_STATIC_MAX_IDS = 65536
 MT_F32, MT_BF16 = 0, 1
 KEY_EMPTY = (1 << 64) - 1

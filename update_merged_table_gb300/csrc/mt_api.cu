@@ -97,6 +97,7 @@ const char* mt_strerror(int code) {
     case MT_EKEY: return "ID outside [0, 2^56)";
     case MT_ECUDA: return "CUDA runtime error";
     case MT_ETOOBIG: return "batch larger than the fixed-size workspace allows";
+    case MT_ETIMEOUT: return "a bounded wait inside a kernel gave up";
     default: return "unknown status";
   }
 }
@@ -211,10 +212,11 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
     p.sc_key = reinterpret_cast<unsigned long long*>(w + L.sc_key);
     p.sc_minpos = reinterpret_cast<uint32_t*>(w + L.sc_minpos);
     p.sc_uidx = reinterpret_cast<int32_t*>(w + L.sc_uidx);
+    p.sc_row = reinterpret_cast<int32_t*>(w + L.sc_row);
     p.scratch_mask = L.scratch_slots - 1;
     p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
-    p.tile_owners = reinterpret_cast<int32_t*>(w + L.tile_owners);
-    p.tile_offset = reinterpret_cast<int32_t*>(w + L.tile_offset);
+    p.tile_status = reinterpret_cast<unsigned long long*>(w + L.tile_status);
+    p.ticket = reinterpret_cast<int32_t*>(w + L.ticket);
     p.lfirst = reinterpret_cast<uint32_t*>(w + L.lfirst);
     p.lsslot = reinterpret_cast<uint32_t*>(w + L.lsslot);
     p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);

@@ -15,7 +15,6 @@ constexpr int kThreadsA = 512;           // threads per dedup CTA (k_dedup_claim
 constexpr int kPPTA = kTile / kThreadsA; // positions per dedup thread
 constexpr int kHS = 2 * kTile;           // shared-memory hash slots (backward fill)
 constexpr int kHSA = 3 * kTile / 2;      // shared-memory hash slots of stage 1 (load <= 2/3)
-constexpr int kMaxInBlockPrefix = 8192;  // tiles up to which each CTA sums its own tile offset
 constexpr uint16_t kNoIdx = 0xFFFF;
 
 struct LookupParams {
@@ -39,10 +38,11 @@ struct LookupParams {
   unsigned long long* sc_key;
   uint32_t* sc_minpos;
   int32_t* sc_uidx;
+  int32_t* sc_row;        // table row of the key, written by its claimer (-1: absent)
   unsigned long long scratch_mask;
   int32_t* tile_L;        // [ntiles] local uniques per tile
-  int32_t* tile_owners;   // [ntiles] global-first keys per tile
-  int32_t* tile_offset;   // [ntiles + 1] exclusive scan of tile_owners
+  unsigned long long* tile_status;  // [ntiles] owner-count scan: flag << 32 | count (cleared by k_dedup_claim)
+  int32_t* ticket;        // tiles handed to k_assign_resolve blocks in start order
   uint32_t* lfirst;       // [ntiles * kTile] first global position of local unique l
   uint32_t* lsslot;       // [ntiles * kTile] its scratch slot
   uint16_t* lidx;         // [ntiles * kTile] local unique index of each position
@@ -50,7 +50,7 @@ struct LookupParams {
 };
 
 struct LookupWsLayout {
-  size_t sc_key, sc_minpos, sc_uidx, tile_L, tile_owners, tile_offset, lfirst, lsslot, lidx, total;
+  size_t sc_key, sc_minpos, sc_uidx, sc_row, tile_L, tile_status, ticket, lfirst, lsslot, lidx, total;
   unsigned long long scratch_slots;
   int ntiles;
 };
@@ -113,12 +113,6 @@ cudaError_t launch_export(const TableDev& T, unsigned long long* keys, int32_t* 
                           cudaStream_t s);
 cudaError_t launch_read_rows(const TableDev& T, const int32_t* rows, long long n, float* emb, float* m, float* v,
                              cudaStream_t s);
-
-// Single-block exclusive scan of `count` int32 triples/ints, used for the
-// tile-offset and scan-block-offset passes.  out[count] receives the total.
-// With total_to != nullptr the total is also stored there as int64.
-cudaError_t launch_scan_small(const int32_t* in, int32_t* out, int count, int width, long long* total_to,
-                              cudaStream_t s);
 
 // Counts every kernel launch of the library and, while profiling is on,
 // brackets it with CUDA events on its stream (mt_profile.cu).

@@ -13,14 +13,16 @@
 //                    shared-memory hash (CAS insert, atomicMin of the first
 //                    position); stage 2: each tile-local unique claims its
 //                    key in a global scratch hash and lowers the key's first
-//                    position there (atomicMin).
-//  k_count_owners    a tile owns a key when its first position is the key's
-//                    global first position; count owners per tile.
-//  k_scan_small      tile offsets = exclusive scan of owner counts; U.
-//  k_assign_resolve  owners take unique indices in first-occurrence order,
-//                    publish them in the scratch hash, find or insert their
-//                    key in the table (odd-step probing, tombstone reuse,
-//                    warp-aggregated row pops) and initialise fresh rows.
+//                    position there (atomicMin); the one thread whose CAS
+//                    put the key there finds or inserts it in the table
+//                    (odd-step probing, tombstone reuse, warp-aggregated
+//                    row pops), publishes the row in the scratch hash and
+//                    its block initialises the fresh rows.
+//  k_assign_resolve  a tile owns a key when its first position is the key's
+//                    global first position; owners take unique indices in
+//                    first-occurrence order (tile offsets by a decoupled
+//                    look-back over the tiles' owner counts) and publish
+//                    them in the scratch hash; key and row come from there.
 //  k_expand          per tile-local unique: its unique index and counts;
 //                    per position: the inverse index.
 //  k_gather          the 16-byte vectorised row gather, grid-stride over
@@ -78,7 +80,7 @@ __device__ __forceinline__ int block_sum(int v, int* s_warp) {
 
 constexpr size_t kSmemA = kHSA * 8 + kHSA * 4 + kTile * 4 + kTile * 2 + (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
 
-__global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p) {
+__global__ void __launch_bounds__(kThreadsA, 3) k_dedup_claim(const LookupParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHSA] stage-1 hash keys
   uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHSA);             // [kHSA] first local position, then local index
@@ -88,6 +90,7 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
   unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
   __shared__ int s_warp[kThreadsA / 32];
   __shared__ int s_frange[2];  // features of the tile's first and last position
+  __shared__ int s_nnew;       // fresh rows listed by stage 2
 
   const int tile = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -100,6 +103,11 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
   }
   for (int i = tid; i <= p.F; i += kThreadsA) s_off[i] = p.feat_off[i];
   for (int i = tid; i < p.F; i += kThreadsA) s_tid[i] = p.table_ids[i];
+  if (tid == 0) {
+    s_nnew = 0;
+    p.tile_status[tile] = 0ull;  // no owner count published yet (read by k_assign_resolve)
+    if (tile == 0) *p.ticket = 0;
+  }
   __syncthreads();
   if (tid < 2) {  // feature of position base (tid 0) and base + cnt - 1 (tid 1): last f with off[f] <= i
     const long long i = base + (tid == 0 ? 0 : cnt - 1);
@@ -189,113 +197,52 @@ __global__ void __launch_bounds__(kThreadsA) k_dedup_claim(const LookupParams p)
     lidx[lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
   }
 
-  // ---- stage 2: claim every local unique in the global scratch hash ----
+  // ---- stage 2: claim every local unique in the global scratch hash; the
+  // thread whose CAS puts a key there is the only one in the grid to see it
+  // EMPTY, and it resolves the key in the table right away (find, or insert
+  // with tombstone reuse and a warp-aggregated row pop) and publishes the
+  // row in the scratch hash ----
+  __syncthreads();  // s_min and s_pslot are free from here: fresh rows are listed there
+  int32_t* s_newrow = reinterpret_cast<int32_t*>(s_min);  // [kHSA >= kTile] rows to initialise
+  uint16_t* s_newli = s_pslot;                           // [kTile] their local uniques
   const size_t lb = (size_t)tile * kTile;
-  for (int li = tid; li < L; li += kThreadsA) {
-    const uint32_t it = s_item[li];
-    const unsigned long long key = s_key[it >> 16];
-    const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
-    unsigned long long h = stage2_hash(key) & p.scratch_mask;
-    for (unsigned long long probe = 0; probe <= p.scratch_mask; ++probe) {
-      unsigned long long cur = load_key_relaxed(&p.sc_key[h]);
-      if (cur == kEmpty) {
-        cur = atomicCAS(&p.sc_key[h], kEmpty, key);
-        if (cur == kEmpty) cur = key;
-      }
-      if (cur == key) break;
-      h = (h + 1) & p.scratch_mask;
-    }
-    atomicMin(&p.sc_minpos[h], gpos);
-    p.lfirst[lb + li] = gpos;
-    p.lsslot[lb + li] = (uint32_t)h;
-  }
-  if (tid == 0) p.tile_L[tile] = L;
-}
-
-__global__ void __launch_bounds__(kThreads) k_count_owners(const LookupParams p) {
-  __shared__ int s_warp[kThreads / 32];
-  const int tile = blockIdx.x;
-  const int L = p.tile_L[tile];
-  const size_t lb = (size_t)tile * kTile;
-  int c = 0;
-  for (int l = threadIdx.x; l < L; l += kThreads) c += __ldcg(&p.sc_minpos[p.lsslot[lb + l]]) == p.lfirst[lb + l];
-  const int tot = block_sum<kThreads>(c, s_warp);
-  if (threadIdx.x == 0) p.tile_owners[tile] = tot;
-}
-
-__global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams p) {
-  __shared__ int s_warp[kThreads / 32];
-  __shared__ uint32_t s_oslot[kTile];  // scratch slot of owner j
-  __shared__ int32_t s_orow[kTile];    // table row of owner j
-  __shared__ int32_t s_new[kTile];     // owners that inserted a fresh row
-  __shared__ unsigned long long s_okey[kTile];  // key of owner j
-  __shared__ int s_nnew;
-
-  const int tile = blockIdx.x, tid = threadIdx.x;
-  const int L = p.tile_L[tile];
-  const size_t lb = (size_t)tile * kTile;
-  int off;
-  if (p.ntiles <= kMaxInBlockPrefix) {  // sum the owner counts of the earlier tiles (L2 reads, no scan launch)
-    int sum = 0;
-    for (int t = tid; t < tile; t += kThreads) sum += __ldg(&p.tile_owners[t]);
-    off = block_sum<kThreads>(sum, s_warp);
-  } else {
-    off = p.tile_offset[tile];
-  }
-  if (tid == 0) s_nnew = 0;
-
-  // owners, in local (first-occurrence) order
-  uint32_t flags = 0;
-  uint32_t sl[kPPT];
-  unsigned long long key[kPPT];
-  int c = 0;
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    const int l = tid * kPPT + k;
-    sl[k] = 0;
-    key[k] = 0;
-    if (l < L) {
-      sl[k] = p.lsslot[lb + l];
-      if (__ldcg(&p.sc_minpos[sl[k]]) == p.lfirst[lb + l]) {  // this tile holds the key's first position
-        key[k] = __ldcg(&p.sc_key[sl[k]]);
-        flags |= 1u << k;
-        ++c;
-      }
-    }
-  }
-  int O;
-  int j = block_exclusive_scan<kThreads>(c, s_warp, &O);
-  if (tid == 0 && tile == p.ntiles - 1 && p.ntiles <= kMaxInBlockPrefix) *p.num_unique = off + O;
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    if (flags & (1u << k)) {
-      const int u = off + j;
-      p.sc_uidx[sl[k]] = u;
-      p.unique_keys[u] = key[k];
-      p.counts[u] = 0;
-      s_oslot[j] = sl[k];
-      s_okey[j] = key[k];
-      ++j;
-    }
-  }
-  __syncthreads();
-
-  // find or insert each owned key in the table
   const uint32_t step = (uint32_t)p.T.hdr->step;
-  for (int j0 = 0; j0 < O; j0 += kThreads) {
-    const int jj = j0 + tid;
-    const bool act = jj < O;
+  for (int li0 = 0; li0 < L; li0 += kThreadsA) {  // warp-uniform trip count (row pops are warp-wide)
+    const int li = li0 + tid;
+    const bool act = li < L;
+    unsigned long long key = 0, h = 0;
+    bool won = false;
+    if (act) {
+      const uint32_t it = s_item[li];
+      key = s_key[it >> 16];
+      const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
+      h = stage2_hash(key) & p.scratch_mask;
+      for (unsigned long long probe = 0; probe <= p.scratch_mask; ++probe) {
+        unsigned long long cur = load_key_relaxed(&p.sc_key[h]);
+        if (cur == kEmpty) {
+          cur = atomicCAS(&p.sc_key[h], kEmpty, key);
+          if (cur == kEmpty) {
+            won = true;
+            cur = key;
+          }
+        }
+        if (cur == key) break;
+        h = (h + 1) & p.scratch_mask;
+      }
+      atomicMin(&p.sc_minpos[h], gpos);
+      p.lfirst[lb + li] = gpos;
+      p.lsslot[lb + li] = (uint32_t)h;
+    }
     int32_t row = -1;
     bool claimed = false;
     unsigned long long cs = 0;
-    if (act) {
-      const unsigned long long key = s_okey[jj];
+    if (won) {
       long long t_end, t_tomb;
-      const long long s = find_slot(p.T, key, &t_end, &t_tomb, &row);
-      if (s < 0 && p.insert_missing) {
-        // the key is absent and no other thread inserts it (it is unique in
-        // the batch): take the first tombstone of its chain, else the EMPTY
-        // slot that ended the chain, else the next free slot after them
+      const long long sidx = find_slot(p.T, key, &t_end, &t_tomb, &row);
+      if (sidx < 0 && p.insert_missing) {
+        // absent, and no other thread inserts it (it won the scratch hash):
+        // take the first tombstone of its chain, else the EMPTY slot that
+        // ended the chain, else the next free slot after them
         long long t = t_tomb >= 0 ? t_tomb : t_end;
         unsigned long long slot = (home_slot(p.T, key) + (unsigned long long)t * p.T.S) & p.T.mask;
         for (; t < (long long)p.T.max_probes; ++t) {
@@ -319,14 +266,14 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
       } else {
         p.T.slots[cs].row = row;
         p.T.slots[cs].meta = step;
-        s_new[atomicAdd(&s_nnew, 1)] = jj;
+        const int q = atomicAdd(&s_nnew, 1);
+        s_newrow[q] = row;
+        s_newli[q] = (uint16_t)li;
       }
     }
-    if (act) {
-      p.unique_rows[off + jj] = row;
-      s_orow[jj] = row;
-    }
+    if (won) p.sc_row[h] = row;
   }
+  if (tid == 0) p.tile_L[tile] = L;
   __syncthreads();
 
   // initialise fresh rows, one team of lanes per row
@@ -334,10 +281,119 @@ __global__ void __launch_bounds__(kThreads) k_assign_resolve(const LookupParams 
   const uint32_t vecs = p.T.row_dtype == MT_F32 ? p.T.dim / 4 : p.T.dim / 8;
   int team = 1;
   while (team < 32 && team < (int)vecs) team <<= 1;
-  const int nteams = kThreads / team, my_team = tid / team, lt = tid % team;
-  for (int q = my_team; q < nnew; q += nteams) {
-    const int jj = s_new[q];
-    init_row_coop(p.T, s_orow[jj], s_okey[jj], lt, team);
+  const int nteams = kThreadsA / team, my_team = tid / team, lt = tid % team;
+  for (int q = my_team; q < nnew; q += nteams)
+    init_row_coop(p.T, s_newrow[q], s_key[s_item[s_newli[q]] >> 16], lt, team);
+}
+
+// Tile status words of the owner-count scan: flag in the high half
+// (kStatAgg: the tile's own owner count; kStatIncl: owners of this tile and
+// all before it), value in the low half.
+constexpr unsigned long long kStatAgg = 1ull << 32, kStatIncl = 2ull << 32;
+constexpr int kLookbackTries = 1 << 22;
+
+__device__ __forceinline__ void store_status(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long load_status(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Owners take unique indices in first-occurrence order: a tile's owners are
+// the tile-local uniques whose first position is the key's global first
+// position.  Tiles are taken in start order (a ticket), so every tile
+// before a block's tile has started; the block publishes its owner count,
+// then its first warp adds up the counts of the tiles before it from their
+// status words (a decoupled look-back: a tile that already knows its
+// inclusive count ends the walk).  A wait that runs out of polls latches
+// MT_ETIMEOUT and leaves every index in bounds.  Key and row of each owner
+// come from the scratch hash, where its claimer put them.
+__global__ void __launch_bounds__(kThreads, 6) k_assign_resolve(const LookupParams p) {
+  __shared__ int s_warp[kThreads / 32];
+  __shared__ int s_tile;
+  __shared__ long long s_off;
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) s_tile = atomicAdd(p.ticket, 1);
+  __syncthreads();
+  const int tile = s_tile;
+  const int L = p.tile_L[tile];
+  const size_t lb = (size_t)tile * kTile;
+
+  uint32_t sl[kPPT], lf[kPPT], mp[kPPT];  // each round of loads all in flight at once
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int l = tid * kPPT + k;
+    sl[k] = l < L ? __ldg(&p.lsslot[lb + l]) : 0u;
+    lf[k] = l < L ? __ldg(&p.lfirst[lb + l]) : 0u;
+  }
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) mp[k] = tid * kPPT + k < L ? __ldcg(&p.sc_minpos[sl[k]]) : 1u;
+  uint32_t flags = 0;
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    if (mp[k] == lf[k]) {  // this tile holds the key's first position
+      flags |= 1u << k;
+      ++c;
+    }
+  }
+  int O;
+  int j = block_exclusive_scan<kThreads>(c, s_warp, &O);
+  unsigned long long* st = p.tile_status;
+  if (tid < 32) {
+    if (lane == 0) store_status(st + tile, (tile == 0 ? kStatIncl : kStatAgg) | (unsigned long long)O);
+    long long excl = 0;
+    bool ok = true;
+    for (int q = tile - 1, tries = 0; q >= 0;) {
+      const int pq = q - lane;
+      const unsigned long long v = pq >= 0 ? load_status(st + pq) : kStatIncl;  // before tile 0: inclusive 0
+      const unsigned long long flag = v & ~0xFFFFFFFFull;
+      if (__ballot_sync(kFull, flag != 0) != kFull) {  // a tile in this window has not published yet
+        if (++tries >= kLookbackTries) {
+          ok = false;
+          break;
+        }
+        continue;
+      }
+      const unsigned incl = __ballot_sync(kFull, flag == kStatIncl);
+      const int stop = incl ? __ffs(incl) - 1 : 31;
+      long long x = lane <= stop ? (long long)(v & 0xFFFFFFFFull) : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+      excl += x;
+      if (incl) break;
+      q -= 32;
+    }
+    if (!ok) excl = 0;  // in bounds (every index stays below this tile's owner count); the call reports the error
+    if (lane == 0) {
+      if (!ok) latch_error(p.T.hdr, MT_ETIMEOUT);
+      if (tile > 0) store_status(st + tile, kStatIncl | (unsigned long long)(excl + O));
+      s_off = excl;
+    }
+  }
+  __syncthreads();
+  const long long off = s_off;
+  if (tid == 0 && tile == p.ntiles - 1) *p.num_unique = off + O;
+  unsigned long long key[kPPT];
+  int32_t row[kPPT];
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    key[k] = (flags >> k) & 1u ? __ldcg(&p.sc_key[sl[k]]) : 0ull;
+    row[k] = (flags >> k) & 1u ? __ldcg(&p.sc_row[sl[k]]) : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    if (flags & (1u << k)) {
+      const int u = (int)(off + j);
+      p.sc_uidx[sl[k]] = u;
+      p.unique_keys[u] = key[k];
+      p.unique_rows[u] = row[k];
+      p.counts[u] = 0;
+      ++j;
+    }
   }
 }
 
@@ -442,28 +498,6 @@ __global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
   }
 }
 
-__global__ void __launch_bounds__(1024) k_scan_small(const int32_t* in, int32_t* out, int count, int width,
-                                                      long long* total_to) {
-  __shared__ int s_warp[32];
-  __shared__ int s_carry[4];
-  if (threadIdx.x < 4) s_carry[threadIdx.x] = 0;
-  __syncthreads();
-  for (int w = 0; w < width; ++w) {
-    for (int b = 0; b < count; b += 1024) {
-      const int i = b + (int)threadIdx.x;
-      const int v = i < count ? in[(size_t)i * width + w] : 0;
-      int tot;
-      const int ex = block_exclusive_scan<1024>(v, s_warp, &tot);
-      if (i < count) out[(size_t)i * width + w] = s_carry[w] + ex;
-      __syncthreads();
-      if (threadIdx.x == 0) s_carry[w] += tot;
-      __syncthreads();
-    }
-  }
-  if ((int)threadIdx.x < width) out[(size_t)count * width + threadIdx.x] = s_carry[threadIdx.x];
-  if (total_to != nullptr && threadIdx.x == 0) *total_to = s_carry[0];
-}
-
 }  // namespace
 
 LookupWsLayout lookup_ws_layout(long long n) {
@@ -482,23 +516,15 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.sc_key = take(ss * 8);
   L.sc_minpos = take(ss * 4);
   L.sc_uidx = take(ss * 4);
+  L.sc_row = take(ss * 4);
   L.tile_L = take((size_t)L.ntiles * 4);
-  L.tile_owners = take((size_t)L.ntiles * 4);
-  L.tile_offset = take(((size_t)L.ntiles + 1) * 4);
+  L.tile_status = take((size_t)L.ntiles * 8);
+  L.ticket = take(16);
   L.lfirst = take(cap * 4);
   L.lsslot = take(cap * 4);
   L.lidx = take(cap * 2);
   L.total = off;
   return L;
-}
-
-cudaError_t launch_scan_small(const int32_t* in, int32_t* out, int count, int width, long long* total_to,
-                              cudaStream_t s) {
-  {
-    MT_LAUNCH("k_scan_small", s);
-    k_scan_small<<<1, 1024, 0, s>>>(in, out, count, width, total_to);
-  }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
@@ -517,14 +543,6 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
   {
     MT_LAUNCH("k_dedup_claim", s);
     k_dedup_claim<<<p.ntiles, kThreadsA, kSmemA, s>>>(p);
-  }
-  {
-    MT_LAUNCH("k_count_owners", s);
-    k_count_owners<<<p.ntiles, kThreads, 0, s>>>(p);
-  }
-  if (p.ntiles > kMaxInBlockPrefix) {
-    e = launch_scan_small(p.tile_owners, p.tile_offset, p.ntiles, 1, p.num_unique, s);
-    if (e != cudaSuccess) return e;
   }
   {
     MT_LAUNCH("k_assign_resolve", s);

@@ -24,7 +24,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = 3u << 20;  // 3 MiB: the lookup workspace for MT_LOOKUP_STATIC_MAX_IDS IDs
+constexpr size_t kStaticScratchBytes = 4u << 20;  // 4 MiB: the lookup workspace for MT_LOOKUP_STATIC_MAX_IDS IDs
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_lookup_scratch[kStaticScratchBytes];
