@@ -459,19 +459,23 @@ __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
 
 // out[i] = row of unique inverse[i] (zeros for an invalid ID or an absent
 // key): 16-byte items (position, vector), consecutive threads on consecutive
-// items, four independent items in flight per thread, grid-stride over the
-// whole batch so every SM stays busy to the end.
+// items; each round a block covers kGatherILP * blockDim contiguous items
+// (one independent item in flight per thread and step of blockDim), and the
+// blocks stride over the whole batch so every SM stays busy to the end.
+constexpr int kGatherILP = 2;
 __global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
   const int vec16 = (int)(p.T.emb_bytes / 16);
   const int vshift = (vec16 & (vec16 - 1)) == 0 ? __ffs(vec16) - 1 : -1;
   const long long total = p.n * vec16;
-  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long span = (long long)kGatherILP * blockDim.x;  // items a block covers per round, contiguous
   uint4* out = reinterpret_cast<uint4*>(p.out_rows);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
-    int32_t row[4];
+  for (long long b0 = (long long)blockIdx.x * span; b0 < total; b0 += (long long)gridDim.x * span) {
+    const long long i0 = b0 + threadIdx.x;
+    const long long stride = blockDim.x;
+    int32_t row[kGatherILP];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kGatherILP; ++k) {
       const long long it = i0 + k * stride;
       row[k] = -1;
       if (it < total) {
@@ -480,9 +484,9 @@ __global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
         if (u >= 0) row[k] = __ldg(&p.unique_rows[u]);
       }
     }
-    uint4 v[4];
+    uint4 v[kGatherILP];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kGatherILP; ++k) {
       const long long it = i0 + k * stride;
       v[k] = zero;
       if (it < total && row[k] >= 0) {
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kGatherILP; ++k) {
       const long long it = i0 + k * stride;
       if (it < total) __stcs(out + it, v[k]);
     }
