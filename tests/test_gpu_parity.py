@@ -381,6 +381,31 @@ def test_backward_without_ranks_matches_with_ranks():
     assert np.array_equal(out[0][0], out[1][0]) and np.array_equal(out[0][1], out[1][1])
 
 
+def test_many_tiles_first_occurrence_order():
+    """One lookup of 20M IDs (~10k tiles of 2048 positions): unique keys in
+    first-occurrence order, inverse and counts, exactly as numpy's unique
+    defines them.  The owners' tile offsets come from a look-back that walks
+    thousands of earlier tiles."""
+    rng = np.random.default_rng(21)
+    n = 20_000_000
+    ids = W.bijection32(W.zipf_ranks(rng, n, 1.05, 1 << 24))
+    b = W.single_feature(ids, table_id=3)
+    tab = mt.Table(24, 4)
+    res = tab.new_result(n, gather=False, ranks=False)
+    tab.lookup(to_dev(b.ids), b.feat_offsets, b.table_ids, gather=False, result=res)
+    keys = (np.uint64(3) << np.uint64(56)) | ids.astype(np.uint64)
+    uniq, first, inv, cnt = np.unique(keys, return_index=True, return_inverse=True, return_counts=True)
+    order = np.argsort(first, kind="stable")     # unique keys by first position
+    rank = np.empty_like(order)
+    rank[order] = np.arange(order.size)
+    U = res.U
+    assert U == uniq.size
+    assert np.array_equal(res.unique_keys[:U].cpu().numpy().view(np.uint64), uniq[order])
+    assert np.array_equal(res.inverse[:n].cpu().numpy(), rank[inv].astype(np.int32))
+    assert np.array_equal(res.counts[:U].cpu().numpy(), cnt[order].astype(np.int32))
+    assert tab.error() == 0
+
+
 def test_full_size_large_table():
     """M = 2^26 slots, dim 128 fp32, prefilled with 0.7 M keys (46,976,204); a 2^20-ID batch Zipf(1.05)
     over a 2^32 key space: unique/inverse/counts bit-exact, sampled gathered rows bit-exact (untouched
