@@ -539,10 +539,11 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // keys EMPTY and first positions "none": sc_key and sc_minpos are adjacent
-  cudaError_t e = cudaMemsetAsync(p.sc_key, 0xFF, (p.scratch_mask + 1) * 8, s);
-  if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(p.sc_minpos, 0xFF, (p.scratch_mask + 1) * 4, s);
+  // keys EMPTY and first positions "none", in one memset: the layout puts
+  // sc_minpos right after sc_key (8-byte keys keep it 256-byte aligned)
+  const size_t clear = (size_t)(reinterpret_cast<const char*>(p.sc_minpos) - reinterpret_cast<const char*>(p.sc_key)) +
+                       (p.scratch_mask + 1) * 4;
+  cudaError_t e = cudaMemsetAsync(p.sc_key, 0xFF, clear, s);
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_dedup_claim", s);
