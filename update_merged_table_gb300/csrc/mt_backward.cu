@@ -455,27 +455,29 @@ constexpr int kMaxTeams = 256 >> kMinTeamShift;               // per block
 // scatter, pos_sorted[segment start + rank] = position.  A rank or unique
 // index that does not belong to the lookup result (a caller passing some
 // other buffer) is skipped and latches MT_EINVAL instead of writing.
+constexpr int kScatterILP = 4;  // positions in flight per thread
+
 __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
   write_heavy_chunks(p);
   const long long U = *p.num_unique;
   const long long stride = (long long)gridDim.x * blockDim.x;
   bool bad = false;
-  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < p.n; i0 += 4 * stride) {
-    int u[4], r[4];
-    int2 sg[4];  // four positions' loads in flight
+  for (long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < p.n; i0 += kScatterILP * stride) {
+    int u[kScatterILP], r[kScatterILP];
+    int2 sg[kScatterILP];  // kScatterILP positions' loads in flight
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kScatterILP; ++k) {
       const long long i = i0 + k * stride;
       u[k] = i < p.n ? __ldg(&p.inverse[i]) : -1;
       r[k] = i < p.n ? __ldg(&p.ranks[i]) : -1;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kScatterILP; ++k) {
       const bool ok = u[k] >= 0 && u[k] < U;
       sg[k] = ok ? __ldg(&p.seg[u[k]]) : make_int2(0, 0);  // {segment start, count}
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kScatterILP; ++k) {
       if (u[k] < 0) continue;
       if (u[k] >= U || r[k] < 0 || r[k] >= sg[k].y) {
         bad = true;
