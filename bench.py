@@ -531,56 +531,82 @@ def run_ours(args):
 # the oracle on the host cores (reported baseline / reference arm)
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(wl: Workload, budget_s: float):
-    """Oracle lookup+backward IDs/s on a bounded sample of the workload: a smaller
-    batch of the same distributions per step (for the jagged workload the first
-    256 users), one untimed cold step, then steps until about `budget_s` seconds
-    of oracle time have been spent."""
-    import torch
+class OracleSteps:
+    """The oracle (single-threaded C++) on bounded samples of the workload: a
+    smaller batch of the same distributions per step (for the jagged workload
+    the first 256 users), starting with one untimed cold step."""
 
-    import oracle
+    def __init__(self, wl: Workload):
+        import oracle
+        self.oracle = oracle
+        self.wl = wl
+        self.ref = oracle.Table(wl.log2, wl.dim, row_dtype=oracle.BF16 if wl.row == "bf16" else oracle.F32)
+        self.k = 0
+        self.step()  # cold step
 
-    def grads(seed, n):
-        g = W.grads_normal(seed, n, wl.dim)
-        if wl.grad == "bf16":
-            return torch.from_numpy(g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16), oracle.BF16
-        return g, oracle.F32
+    def _grads(self, seed, n):
+        import torch
+        g = W.grads_normal(seed, n, self.wl.dim)
+        if self.wl.grad == "bf16":
+            return torch.from_numpy(g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16), self.oracle.BF16
+        return g, self.oracle.F32
 
-    ref = oracle.Table(wl.log2, wl.dim, row_dtype=oracle.BF16 if wl.row == "bf16" else oracle.F32)
-    cold = wl.sample_batch(0)
-    ref.lookup(cold.ids, cold.feat_offsets, cold.table_ids)
-    g, gd = grads(7, cold.n)
-    ref.backward_adam(g, grad_dtype=gd)
-    ids_done, t_total, steps = 0, 0.0, 0
-    k = 1
-    while t_total < budget_s and steps < 10_000:
-        b = wl.sample_batch(k)
-        g, gd = grads(k + 500_000, b.n)
+    def step(self):
+        """One lookup + backward on the next sample batch; returns (IDs, seconds of oracle time)."""
+        b = self.wl.sample_batch(self.k)
+        g, gd = self._grads(self.k + 500_000, b.n)
         t0 = time.perf_counter()
-        ref.lookup(b.ids, b.feat_offsets, b.table_ids)
-        ref.backward_adam(g, grad_dtype=gd)
-        t_total += time.perf_counter() - t0
-        ids_done += b.n
+        self.ref.lookup(b.ids, b.feat_offsets, b.table_ids)
+        self.ref.backward_adam(g, grad_dtype=gd)
+        dt = time.perf_counter() - t0
+        self.k += 1
+        return b.n, dt
+
+
+def cpu_baseline(wl: Workload, budget_s: float):
+    """Oracle lookup+backward IDs/s: steps on bounded samples until about
+    `budget_s` seconds of oracle time have been spent."""
+    runner = OracleSteps(wl)
+    ids_done, t_total, steps = 0, 0.0, 0
+    while t_total < budget_s and steps < 10_000:
+        n, dt = runner.step()
+        ids_done += n
+        t_total += dt
         steps += 1
-        k += 1
     return {"value": ids_done / t_total, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{steps} steps of a reduced batch (avg {ids_done // max(1, steps)} IDs/step) of the same "
                       f"workload after one untimed cold step; single-threaded C++ oracle, {t_total:.1f} s"}
 
 
 def run_reference(args):
+    """The reference arm: the oracle as it stands, W untimed warm-up steps and
+    then K timed steps, each a bounded sample of the workload (a time cap
+    ends the timed steps early if K of them would take too long; the line
+    says how many ran)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     wl = Workload(args.config, args.users, args.log2_slots)
-    cb = cpu_baseline(wl, args.cpu_seconds)
+    runner = OracleSteps(wl)
+    for _ in range(args.warmup):
+        runner.step()
+    ids_done, t_total, steps = 0, 0.0, 0
+    while steps < args.steps and t_total < args.ref_seconds:
+        n, dt = runner.step()
+        ids_done += n
+        t_total += dt
+        steps += 1
+    value = ids_done / t_total
+    sample = (f"{steps} timed steps (of {args.steps} asked; cap {args.ref_seconds:.0f} s) of a reduced batch "
+              f"(avg {ids_done // max(1, steps)} IDs/step) of the same workload after one cold and {args.warmup} "
+              f"warm-up steps; single-threaded C++ oracle, {t_total:.1f} s")
     line = {
-        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_total / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name + " (bounded sample per step, see cpu_baseline.sample)"},
-        "cpu_baseline": cb,
-        "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -595,6 +621,8 @@ def main():
     ap.add_argument("--pool", type=int, default=8, help="distinct pre-generated batches cycled through")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="--impl reference: cap on the timed oracle seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--users", type=int, default=2048, help="users per jagged batch (smaller cases for profiling)")
     ap.add_argument("--log2-slots", type=int, default=None)
