@@ -69,6 +69,27 @@ def test_static_lookup_matches_lookup_on_two_calls():
     assert tab.error() == 0 and ref.error() == 0
 
 
+def test_static_lookup_takes_the_largest_batch():
+    """Exactly MT_LOOKUP_STATIC_MAX_IDS IDs fit the static workspace; same result as mt_lookup."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    n = mt.LOOKUP_STATIC_MAX_IDS
+    ids = W.bijection32(W.zipf_ranks(np.random.default_rng(5), n, 1.1, 1 << 20))
+    b = W.single_feature(ids)
+    ref = mt.Table(18, 8, device=dev)
+    tab = mt.Table(18, 8, device=dev)
+    d_ids = torch.from_numpy(b.ids).to(dev)
+    want = ref.lookup(d_ids, b.feat_offsets, b.table_ids)
+    got = tab.new_result(n)
+    assert _lookup_static(tab, d_ids, b, got) == mt.MT_OK
+    torch.cuda.synchronize()
+    U = want.U
+    assert got.U == U
+    assert torch.equal(got.unique_keys[:U], want.unique_keys[:U])
+    assert torch.equal(got.inverse[:n], want.inverse[:n])
+    assert torch.equal(got.rows, want.rows)
+    assert tab.error() == 0
+
+
 def test_static_lookup_refuses_oversized_batch():
     dev = torch.device("cuda", torch.cuda.current_device())
     tab = mt.Table(10, 8, device=dev)
