@@ -25,6 +25,8 @@
 //                    last warp-chunk of a unique applies Adam.
 //  k_bw_light_reduce light uniques: a team of lanes per unique, software
 //                    pipelined across the team's uniques; Adam fused.
+#include <atomic>
+
 #include "mt_kernels.cuh"
 
 namespace mt {
@@ -800,37 +802,48 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
   }
 }
 
-int g_heavy_grid[4] = {0, 0, 0, 0};
-size_t g_heavy_smem[4] = {0, 0, 0, 0};
-int g_light_grid[4] = {0, 0, 0, 0};
+// Per device, per (row dtype, grad dtype) and per team size: grid sizes of
+// the two reduce kernels; 0 = not set up yet.  The heavy kernel's
+// shared-memory limit is raised once per device to its largest size (the
+// smallest team), so any table's launch fits.
+constexpr int kTeamShifts = 6 - kMinTeamShift;  // team of 4 .. 32 lanes
+std::atomic<int> g_heavy_grid[kMaxDevices][4][kTeamShifts];
+std::atomic<int> g_light_grid[kMaxDevices][4][kTeamShifts];
+
+template <int RD, int GD>
+size_t heavy_smem_bytes(int team_shift) {
+  constexpr int HS = heavy_stage_rows<RD, GD>();
+  constexpr int Q = GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W / 4;
+  return (size_t)(HS > 0 ? kHeavyStages * HS * Q * 256 : 0) * 16 + (size_t)(256 >> team_shift) * kTeamShare * 4;
+}
 
 template <int RD, int GD>
 cudaError_t launch_reduce(const BackwardParams& p, cudaStream_t s) {
   const int idx = RD * 2 + GD;
-  constexpr int HS = heavy_stage_rows<RD, GD>();
-  constexpr int Q = GradRaw<GD, (RD == MT_F32 ? 4 : 8)>::W / 4;
-  const size_t heavy_smem =
-      (size_t)(HS > 0 ? kHeavyStages * HS * Q * 256 : 0) * 16 + (size_t)(256 >> p.team_shift) * kTeamShare * 4;
-  if (g_heavy_grid[idx] == 0 || g_heavy_smem[idx] != heavy_smem) {
-    int dev = 0, sms = 0, per_h = 0, per_l = 0;
-    cudaGetDevice(&dev);
+  const int dev = current_device();
+  if (dev < 0 || p.team_shift < kMinTeamShift || p.team_shift > 5) return cudaErrorInvalidValue;
+  const int ts = p.team_shift - kMinTeamShift;
+  const size_t heavy_smem = heavy_smem_bytes<RD, GD>(p.team_shift);
+  if (g_heavy_grid[dev][idx][ts].load(std::memory_order_relaxed) == 0) {
+    int sms = 0, per_h = 0, per_l = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaError_t e = cudaFuncSetAttribute(k_bw_heavy_reduce<RD, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)heavy_smem);
+                                         (int)heavy_smem_bytes<RD, GD>(kMinTeamShift));
     if (e != cudaSuccess) return e;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_h, k_bw_heavy_reduce<RD, GD>, 256, heavy_smem);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_l, k_bw_light_reduce<RD, GD>, 256, 0);
-    g_heavy_grid[idx] = sms * (per_h > 0 ? per_h : 1);
-    g_light_grid[idx] = sms * (per_l > 0 ? per_l : 1);
-    g_heavy_smem[idx] = heavy_smem;
+    g_light_grid[dev][idx][ts].store(sms * (per_l > 0 ? per_l : 1), std::memory_order_relaxed);
+    g_heavy_grid[dev][idx][ts].store(sms * (per_h > 0 ? per_h : 1), std::memory_order_relaxed);
   }
+  const int heavy_grid = g_heavy_grid[dev][idx][ts].load(std::memory_order_relaxed);
+  const int light_grid = g_light_grid[dev][idx][ts].load(std::memory_order_relaxed);
   {
     MT_LAUNCH("k_bw_heavy_reduce", s);
-    k_bw_heavy_reduce<RD, GD><<<g_heavy_grid[idx], 256, heavy_smem, s>>>(p);
+    k_bw_heavy_reduce<RD, GD><<<heavy_grid, 256, heavy_smem, s>>>(p);
   }
   {
     MT_LAUNCH("k_bw_light_reduce", s);
-    k_bw_light_reduce<RD, GD><<<g_light_grid[idx], 256, 0, s>>>(p);
+    k_bw_light_reduce<RD, GD><<<light_grid, 256, 0, s>>>(p);
   }
   return cudaGetLastError();
 }

@@ -136,4 +136,14 @@ class LaunchScope {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launch settings (grid sizes, shared-memory attributes) are cached per
+// device: a process may drive tables on several GPUs.  Entries are written
+// with idempotent values, so concurrent first calls only repeat the work.
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
 }  // namespace mt

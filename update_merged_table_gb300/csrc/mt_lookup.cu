@@ -27,6 +27,8 @@
 //                    per position: the inverse index.
 //  k_gather          the 16-byte vectorised row gather, grid-stride over
 //                    the batch with four independent items per thread.
+#include <atomic>
+
 #include "mt_kernels.cuh"
 
 namespace mt {
@@ -533,11 +535,16 @@ LookupWsLayout lookup_ws_layout(long long n) {
 
 cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
   if (p.n == 0) return cudaMemsetAsync(p.num_unique, 0, sizeof(long long), s);
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<int> gather_grid[kMaxDevices];  // 0: not set up on that device yet
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (gather_grid[dev].load(std::memory_order_relaxed) == 0) {
     cudaError_t e = cudaFuncSetAttribute(k_dedup_claim, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    int sms = 0, per = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_gather, 256, 0);
+    gather_grid[dev].store(sms * (per > 0 ? per : 1), std::memory_order_relaxed);
   }
   // keys EMPTY and first positions "none", in one memset: the layout puts
   // sc_minpos right after sc_key (8-byte keys keep it 256-byte aligned)
@@ -558,16 +565,8 @@ cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
     k_expand<<<p.ntiles, kThreads, 0, s>>>(p);
   }
   if (p.out_rows != nullptr) {
-    static int grid = 0;
-    if (grid == 0) {
-      int dev = 0, sms = 0, per = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_gather, 256, 0);
-      grid = sms * (per > 0 ? per : 1);
-    }
     MT_LAUNCH("k_gather", s);
-    k_gather<<<grid, 256, 0, s>>>(p);
+    k_gather<<<gather_grid[dev].load(std::memory_order_relaxed), 256, 0, s>>>(p);
   }
   return cudaGetLastError();
 }

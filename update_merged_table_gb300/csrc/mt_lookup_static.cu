@@ -25,17 +25,16 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = 4u << 20;  // 4 MiB: the lookup workspace for MT_LOOKUP_STATIC_MAX_IDS IDs
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_lookup_scratch[kStaticScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ptr[mt::kMaxDevices] = {};
 
 // Device address of the scratch array on the current device, or nullptr.
 void* scratch_on_current_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= mt::kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* ptr = nullptr;
