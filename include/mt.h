@@ -59,6 +59,13 @@ enum { MT_F32 = 0, MT_BF16 = 1 };
 #define MT_KEY_EMPTY 0xFFFFFFFFFFFFFFFFull
 #define MT_KEY_TOMBSTONE 0xFFFFFFFFFFFFFFFEull
 #define MT_MAX_FEATURES 256
+
+/* Testing only: on a table created with this flag, the first tile of every
+ * lookup never publishes its owner count, so the other tiles' bounded waits
+ * in the owner-count scan run out (after ~2^22 polls, a few seconds): the
+ * lookup latches MT_ETIMEOUT and leaves every index in bounds, and the CUDA
+ * context stays usable.  It exercises the timeout path without a GPU fault. */
+#define MT_FLAG_TEST_STALL_SCAN 0x80000000u
 #define MT_MAX_DIM 1024
 #define MT_HIST_BINS 64
 
@@ -90,7 +97,7 @@ typedef struct {
   uint64_t hash_seed;
   uint64_t init_seed;
   float init_scale;
-  uint32_t flags; /* reserved, must be 0 */
+  uint32_t flags; /* 0, or MT_FLAG_TEST_STALL_SCAN (testing only) */
   int64_t num_rows;
 } mt_config;
 

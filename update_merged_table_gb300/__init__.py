@@ -24,6 +24,7 @@ __all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF1
            "ABI_FUNCTIONS", "profile_enable", "profile_report", "kernel_launches"]
 
 MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA, MT_ETOOBIG, MT_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
+MT_FLAG_TEST_STALL_SCAN = 0x80000000  # testing only (see include/mt.h)
 LOOKUP_STATIC_MAX_IDS = 65536
 MT_F32, MT_BF16 = 0, 1
 KEY_EMPTY = (1 << 64) - 1
@@ -197,14 +198,14 @@ class Table:
 
     def __init__(self, log2_slots: int, dim: int, row_dtype: str = "f32", probe_step: int = 1, hash_seed: int = 0,
                  init_seed: int = 0, init_scale: float = 0.0, max_probes: int = 0, num_rows: int = 0,
-                 device=None, stream=None):
+                 device=None, stream=None, flags: int = 0):
         torch = _torch()
         self.lib = load_library()
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         dt = {"f32": MT_F32, "bf16": MT_BF16}[row_dtype]
         self.row_dtype = row_dtype
         self.torch_row_dtype = torch.float32 if dt == MT_F32 else torch.bfloat16
-        self.cfg = _Config(log2_slots, dim, dt, max_probes, probe_step, hash_seed, init_seed, init_scale, 0,
+        self.cfg = _Config(log2_slots, dim, dt, max_probes, probe_step, hash_seed, init_seed, init_scale, flags,
                            num_rows)
         nbytes = self.lib.mt_table_bytes(ctypes.byref(self.cfg))
         if nbytes == 0:

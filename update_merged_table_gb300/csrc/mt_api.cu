@@ -25,7 +25,7 @@ int normalise(const mt_config* in, mt_config* out) {
   if (in == nullptr) return MT_EINVAL;
   mt_config c = *in;
   if (c.log2_slots < 1 || c.log2_slots > 31) return MT_EINVAL;
-  if (c.flags != 0) return MT_EINVAL;
+  if ((c.flags & ~MT_FLAG_TEST_STALL_SCAN) != 0) return MT_EINVAL;
   if (c.row_dtype != MT_F32 && c.row_dtype != MT_BF16) return MT_EINVAL;
   const uint32_t vec = c.row_dtype == MT_F32 ? 4 : 8;
   if (c.dim < 4 || c.dim > MT_MAX_DIM || c.dim % vec != 0) return MT_EINVAL;
@@ -135,6 +135,7 @@ int mt_table_create(const mt_config* cfg, void* dev_mem, size_t bytes, mt_stream
   T.Sinv = inverse_mod_2_64(c.probe_step) & (M - 1);
   T.log2_slots = c.log2_slots;
   T.max_probes = c.max_probes;
+  T.flags = c.flags;
   T.dim = c.dim;
   T.rec_bytes = L.rec_bytes;
   T.emb_bytes = L.emb_bytes;

@@ -346,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 6) k_assign_resolve(const LookupPara
   int j = block_exclusive_scan<kThreads>(c, s_warp, &O);
   unsigned long long* st = p.tile_status;
   if (tid < 32) {
-    if (lane == 0) store_status(st + tile, (tile == 0 ? kStatIncl : kStatAgg) | (unsigned long long)O);
+    const bool stall = tile == 0 && (p.T.flags & MT_FLAG_TEST_STALL_SCAN);  // testing only: never publish
+    if (lane == 0 && !stall) store_status(st + tile, (tile == 0 ? kStatIncl : kStatAgg) | (unsigned long long)O);
     long long excl = 0;
     bool ok = true;
     for (int q = tile - 1, tries = 0; q >= 0;) {
