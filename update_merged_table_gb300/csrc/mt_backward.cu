@@ -504,18 +504,10 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
 
 // Sum of the gradient rows at positions pos[0 .. n) for one lane's VEC
 // columns, in TwoSum pairs, UNR rows in flight.
-template <int GD, int VEC, int UNR, bool LOOKAHEAD = false>
+template <int GD, int VEC, int UNR>
 __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* pos, int n, int d, int col,
                                            f32x2 hi[VEC / 2], f32x2 lo[VEC / 2]) {
   for (int q0 = 0; q0 < n; q0 += UNR) {
-    if (LOOKAHEAD) {  // pull the next UNR rows toward L2 while these are summed
-#pragma unroll
-      for (int r = 0; r < UNR; ++r) {
-        const int q = q0 + UNR + r;
-        if (q < n && pos[q] >= 0)
-          prefetch_l2(reinterpret_cast<const char*>(p.grads) + ((size_t)pos[q] * d + col) * (GD == MT_F32 ? 4 : 2));
-      }
-    }
     GradRaw<GD, VEC> g[UNR];
 #pragma unroll
     for (int r = 0; r < UNR; ++r)
@@ -529,10 +521,6 @@ __device__ __forceinline__ void accumulate(const BackwardParams& p, const int* p
   }
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
 // 16-byte asynchronous copy that reads src_bytes (16 or 0) from gmem and
 // fills the rest of the 16 bytes with zeros: with 0, nothing is read.
 __device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, int src_bytes) {
