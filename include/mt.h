@@ -245,6 +245,22 @@ int mt_erase(mt_table* t, const uint64_t* keys, int64_t n, uint8_t* found, void*
 
 /* ---- inspection ------------------------------------------------------------ */
 
+/* Workspace bytes mt_compact needs: one slot array of the table (M x 16 B)
+ * plus 256 bytes. */
+size_t mt_compact_workspace_bytes(const mt_table* t);
+
+/* Tombstone compaction of the key store (the key store can be rebuilt on its
+ * own: MTGR section 5, Embedding Management).  Every live key is inserted
+ * again, with its row and insertion step, along its probe sequence
+ * h_t = (h0 + t*S) mod M into a fresh slot array in ws, which then replaces
+ * the table's slots.  Tombstones disappear and chains shorten; rows, the
+ * free list, the step counter and every key's row stay as they were.  If a
+ * key would need more than max_probes probes in the new order (possible
+ * only with a small max_probes), the table is left unchanged and MT_EFULL is
+ * latched.  Stream-ordered; no other call may run on the table meanwhile.
+ *  ws   device, >= mt_compact_workspace_bytes(t), 256-byte aligned. */
+int mt_compact(mt_table* t, void* ws, size_t ws_bytes, mt_stream stream);
+
 /* Scan the key store: live keys, tombstones, and each live key's probe index
  * t = (slot - h0) * S^-1 mod M (S is odd, so S^-1 mod 2^n exists; MTGenRec
  * Theorem 1).  Synchronises `stream`. */

@@ -330,6 +330,43 @@ def test_erase_duplicates_and_reinsert():
     assert st["live"] == 39 and st["tombstones"] <= 2
 
 
+@pytest.mark.parametrize("probe_step", [1, 3])
+def test_compact_drops_tombstones_and_keeps_rows(probe_step):
+    """mt_compact after heavy erasing: no tombstones, the same live keys on
+    the same rows (lookups gather identical rows), and the table keeps
+    training in step with the oracle."""
+    rng = np.random.default_rng(9)
+    tab = mt.Table(14, 8, probe_step=probe_step, init_seed=4)  # room for every key of the test
+    ref = oracle.Table(14, 8, probe_step=probe_step, init_seed=4)
+    ids = rng.choice(1 << 20, 2500, replace=False).astype(np.int64)
+    res = tab.lookup(to_dev(ids))
+    ref.lookup(ids)
+    g = W.grads_normal(3, ids.size, 8)
+    tab.backward_adam(res, to_dev(g))
+    ref.backward_adam(g)
+    er = ids[::2].copy()
+    tab.erase(to_dev(er))
+    ref.erase(er.astype(np.uint64))
+    more = rng.choice(1 << 20, 800).astype(np.int64)  # inserts after the erases reuse some tombstones
+    tab.lookup(to_dev(more))
+    ref.lookup(more)
+    st0 = tab.stats()
+    assert st0["tombstones"] > 0
+    before = tab.lookup(to_dev(ids), insert_missing=False)
+    U = before.U
+    rows_before, urows_before = before.rows.clone(), before.unique_rows[:U].clone()
+    tab.compact()
+    st1 = tab.stats()
+    assert tab.error() == 0
+    assert st1["tombstones"] == 0 and st1["live"] == st0["live"] == ref.live
+    assert st1["rows_free"] == st0["rows_free"] and st1["step"] == st0["step"]
+    after = tab.lookup(to_dev(ids), insert_missing=False)
+    assert after.U == U
+    assert torch.equal(after.unique_rows[:U], urows_before)
+    assert torch.equal(after.rows, rows_before)
+    run_steps(tab, ref, [W.single_feature(rng.choice(1 << 20, 3000).astype(np.int64))], seed0=50)
+
+
 def test_step_counter_and_lazy_rows():
     tab = mt.Table(10, 8)
     ref = oracle.Table(10, 8)

@@ -82,6 +82,8 @@ ABI_FUNCTIONS = {
     "mt_backward_adam": (_I32, [_P, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "mt_erase_workspace_bytes": (_SZ, [_I64]),
     "mt_erase": (_I32, [_P, _P, _I64, _P, _P, _SZ, _P]),
+    "mt_compact_workspace_bytes": (_SZ, [_P]),
+    "mt_compact": (_I32, [_P, _P, _SZ, _P]),
     "mt_stats": (_I32, [_P, _P, _P]),
     "mt_export": (_I32, [_P, _P, _P, _I64, _P, _P]),
     "mt_read_rows": (_I32, [_P, _P, _I64, _P, _P, _P, _P]),
@@ -310,6 +312,11 @@ class Table:
                                          ctypes.byref(hp), _ptr(gsum), ws.data_ptr(), ws.numel(), _stream(stream)),
                "mt_backward_adam")
         return gsum
+
+    def compact(self, stream=None):
+        """Rebuild the key store without tombstones (rows and keys unchanged)."""
+        ws = self._workspace("compact", self.lib.mt_compact_workspace_bytes(self.h))
+        _check(self.lib.mt_compact(self.h, ws.data_ptr(), ws.numel(), _stream(stream)), "mt_compact")
 
     def erase(self, keys, want_found: bool = True, stream=None):
         """Delete merged keys (int64 CUDA tensor holding the uint64 bit patterns)."""

@@ -293,6 +293,17 @@ int mt_erase(mt_table* t, const uint64_t* keys, int64_t n, uint8_t* found, void*
                                       static_cast<int32_t*>(ws), as_stream(stream)));
 }
 
+size_t mt_compact_workspace_bytes(const mt_table* t) {
+  if (t == nullptr) return 0;
+  return align_up((size_t)(t->dev.mask + 1) * 16 + 256, 256);
+}
+
+int mt_compact(mt_table* t, void* ws, size_t ws_bytes, mt_stream stream) {
+  if (t == nullptr) return MT_EINVAL;
+  if (ws == nullptr || ws_bytes < mt_compact_workspace_bytes(t) || !aligned(ws, 256)) return MT_ENOSPACE;
+  return cuda_status(mt::launch_compact(t->dev, ws, as_stream(stream)));
+}
+
 int mt_stats(mt_table* t, mt_stats_out* out, mt_stream stream) {
   if (t == nullptr || out == nullptr) return MT_EINVAL;
   cudaStream_t s = as_stream(stream);

@@ -60,6 +60,46 @@ __global__ void k_erase_apply(const TableDev T, const unsigned long long* keys, 
   }
 }
 
+// Compaction pass 1: every live key of the table is inserted again, with
+// its row and meta, into the fresh slot array `fresh` (all EMPTY), along the
+// same probe sequence; keys are distinct, so a CAS only ever loses to
+// another key.  A key that finds no EMPTY slot within max_probes sets *fail.
+__global__ void k_compact_rebuild(const TableDev T, Slot* fresh, int* fail) {
+  const unsigned long long M = T.mask + 1;
+  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
+       s += (unsigned long long)gridDim.x * blockDim.x) {
+    const Slot old = T.slots[s];
+    if (old.key == kEmpty || old.key == kTomb) continue;
+    unsigned long long h = home_slot(T, old.key);
+    bool placed = false;
+    for (uint32_t t = 0; t < T.max_probes; ++t) {
+      if (atomicCAS(&fresh[h].key, kEmpty, old.key) == kEmpty) {
+        fresh[h].row = old.row;
+        fresh[h].meta = old.meta;
+        placed = true;
+        break;
+      }
+      h = (h + T.S) & T.mask;
+    }
+    if (!placed) atomicExch(fail, 1);
+  }
+}
+
+// Compaction pass 2: the fresh slots replace the table's, unless a key did
+// not fit (then the table stays as it was and MT_EFULL is latched).
+__global__ void k_compact_commit(const TableDev T, const Slot* fresh, const int* fail) {
+  if (*fail) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) latch_error(T.hdr, MT_EFULL);
+    return;
+  }
+  const unsigned long long M = T.mask + 1;
+  const uint4* src = reinterpret_cast<const uint4*>(fresh);
+  uint4* dst = reinterpret_cast<uint4*>(T.slots);
+  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
+       s += (unsigned long long)gridDim.x * blockDim.x)
+    dst[s] = src[s];
+}
+
 __global__ void __launch_bounds__(256) k_stats(const TableDev T) {
   __shared__ unsigned long long s_hist[MT_HIST_BINS];
   __shared__ unsigned long long s_live, s_tomb, s_disp;
@@ -176,6 +216,25 @@ cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long
   {
     MT_LAUNCH("k_erase_apply", s);
     k_erase_apply<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot, found);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact(const TableDev& T, void* ws, cudaStream_t s) {
+  const unsigned long long M = T.mask + 1;
+  Slot* fresh = static_cast<Slot*>(ws);
+  int* fail = reinterpret_cast<int*>(static_cast<char*>(ws) + M * sizeof(Slot));
+  cudaError_t e = cudaMemsetAsync(fresh, 0xFF, M * sizeof(Slot), s);  // keys EMPTY
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(fail, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  {
+    MT_LAUNCH("k_compact_rebuild", s);
+    k_compact_rebuild<<<grid_for((long long)M, 256), 256, 0, s>>>(T, fresh, fail);
+  }
+  {
+    MT_LAUNCH("k_compact_commit", s);
+    k_compact_commit<<<grid_for((long long)M, 256), 256, 0, s>>>(T, fresh, fail);
   }
   return cudaGetLastError();
 }
