@@ -276,6 +276,28 @@ int mt_export(mt_table* t, uint64_t* keys, int32_t* rows, int64_t capacity, int6
 int mt_read_rows(const mt_table* t, const int32_t* rows, int64_t n, float* emb, float* m, float* v,
                  mt_stream stream);
 
+/* Workspace bytes mt_import needs for n keys. */
+size_t mt_import_workspace_bytes(int64_t n);
+
+/* Checkpoint restore (with mt_export, mt_read_rows and the Adam state
+ * below): for each of n merged keys, find the key or insert it as a lookup
+ * would (first tombstone-or-EMPTY slot of its chain, a row from the free
+ * list), then write its row: embedding emb[i] (fp32; stored with
+ * round-to-nearest-even when the rows are bf16), moments m[i] and v[i].
+ *  keys        device uint64 [n] merged keys; they must be distinct (with
+ *              duplicates the table's contents are unspecified, but every
+ *              access stays in bounds).  A sentinel key latches MT_EKEY.
+ *  emb, m, v   device fp32 [n, d].
+ *  ws          device, >= mt_import_workspace_bytes(n), 256-byte aligned.
+ * A full chain or an empty row pool latches MT_EFULL for that key. */
+int mt_import(mt_table* t, const uint64_t* keys, int64_t n, const float* emb, const float* m, const float* v,
+              void* ws, size_t ws_bytes, mt_stream stream);
+
+/* The table's Adam state: steps taken and the beta-power accumulators
+ * b1^t and b2^t (see mt_backward_adam).  Both synchronise `stream`. */
+int mt_get_adam_state(mt_table* t, int64_t* step, double* b1pow, double* b2pow, mt_stream stream);
+int mt_set_adam_state(mt_table* t, int64_t step, double b1pow, double b2pow, mt_stream stream);
+
 /* The first latched device error (0 if none) into *device_error (host);
  * clears it when `clear` is non-zero.  Synchronises `stream`. */
 int mt_get_error(mt_table* t, int32_t* device_error, int clear, mt_stream stream);

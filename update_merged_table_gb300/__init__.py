@@ -87,6 +87,10 @@ ABI_FUNCTIONS = {
     "mt_stats": (_I32, [_P, _P, _P]),
     "mt_export": (_I32, [_P, _P, _P, _I64, _P, _P]),
     "mt_read_rows": (_I32, [_P, _P, _I64, _P, _P, _P, _P]),
+    "mt_import_workspace_bytes": (_SZ, [_I64]),
+    "mt_import": (_I32, [_P, _P, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "mt_get_adam_state": (_I32, [_P, _P, _P, _P, _P]),
+    "mt_set_adam_state": (_I32, [_P, _I64, ctypes.c_double, ctypes.c_double, _P]),
     "mt_get_error": (_I32, [_P, _P, _I32, _P]),
     "mt_step": (_I64, [_P]),
     "mt_profile_enable": (_I32, [_I32]),
@@ -359,6 +363,33 @@ class Table:
         _check(self.lib.mt_read_rows(self.h, rows.data_ptr() if n else None, n, emb.data_ptr(), m.data_ptr(),
                                      v.data_ptr(), _stream(stream)), "mt_read_rows")
         return emb[:n], m[:n], v[:n]
+
+    def import_rows(self, keys, emb, m, v, stream=None):
+        """Checkpoint restore: find or insert each merged key (int64 CUDA tensor of the
+        uint64 bit patterns, distinct) and write its row from fp32 [n, dim] emb, m, v."""
+        torch = _torch()
+        n = keys.numel()
+        if keys.dtype != torch.int64 or not keys.is_cuda or not keys.is_contiguous():
+            raise TypeError("keys must be a contiguous int64 CUDA tensor")
+        for x in (emb, m, v):
+            if x.shape != (n, self.dim) or x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+                raise ValueError("emb, m, v must be contiguous fp32 CUDA tensors [n, dim]")
+        if n and torch.unique(keys).numel() != n:
+            raise ValueError("keys must be distinct")
+        ws = self._workspace("import", self.lib.mt_import_workspace_bytes(n))
+        _check(self.lib.mt_import(self.h, keys.data_ptr() if n else None, n, emb.data_ptr() if n else None,
+                                  m.data_ptr() if n else None, v.data_ptr() if n else None, ws.data_ptr(),
+                                  ws.numel(), _stream(stream)), "mt_import")
+
+    def adam_state(self, stream=None):
+        """(steps taken, beta1^t, beta2^t) of the table's Adam accumulators."""
+        st, b1, b2 = ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+        _check(self.lib.mt_get_adam_state(self.h, ctypes.byref(st), ctypes.byref(b1), ctypes.byref(b2),
+                                          _stream(stream)), "mt_get_adam_state")
+        return int(st.value), float(b1.value), float(b2.value)
+
+    def set_adam_state(self, step: int, b1pow: float, b2pow: float, stream=None):
+        _check(self.lib.mt_set_adam_state(self.h, step, b1pow, b2pow, _stream(stream)), "mt_set_adam_state")
 
     def error(self, clear: bool = False, stream=None) -> int:
         e = ctypes.c_int32()

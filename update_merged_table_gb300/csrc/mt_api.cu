@@ -345,6 +345,48 @@ int mt_read_rows(const mt_table* t, const int32_t* rows, int64_t n, float* emb, 
   return cuda_status(mt::launch_read_rows(t->dev, rows, n, emb, m, v, as_stream(stream)));
 }
 
+size_t mt_import_workspace_bytes(int64_t n) {
+  if (n < 0) return 0;
+  return align_up((size_t)(n > 0 ? n : 1) * 4, 256);
+}
+
+int mt_import(mt_table* t, const uint64_t* keys, int64_t n, const float* emb, const float* m, const float* v,
+              void* ws, size_t ws_bytes, mt_stream stream) {
+  if (t == nullptr || n < 0) return MT_EINVAL;
+  if (n > 0 && (keys == nullptr || emb == nullptr || m == nullptr || v == nullptr || !aligned(keys, 8)))
+    return MT_EINVAL;
+  if (n > 0 && (ws == nullptr || ws_bytes < mt_import_workspace_bytes(n) || !aligned(ws, 256))) return MT_ENOSPACE;
+  return cuda_status(mt::launch_import(t->dev, reinterpret_cast<const unsigned long long*>(keys), n, emb, m, v,
+                                       static_cast<int32_t*>(ws), as_stream(stream)));
+}
+
+int mt_get_adam_state(mt_table* t, int64_t* step, double* b1pow, double* b2pow, mt_stream stream) {
+  if (t == nullptr || step == nullptr || b1pow == nullptr || b2pow == nullptr) return MT_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  long long st = 0;
+  double p[2] = {0.0, 0.0};
+  if (cudaMemcpyAsync(&st, &t->dev.hdr->step, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MT_ECUDA;
+  if (cudaMemcpyAsync(p, &t->dev.hdr->b1pow, sizeof(p), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MT_ECUDA;
+  *step = st;
+  *b1pow = p[0];
+  *b2pow = p[1];
+  return MT_OK;
+}
+
+int mt_set_adam_state(mt_table* t, int64_t step, double b1pow, double b2pow, mt_stream stream) {
+  if (t == nullptr || step < 0 || !(b1pow >= 0.0 && b1pow <= 1.0) || !(b2pow >= 0.0 && b2pow <= 1.0))
+    return MT_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  const long long st = step;
+  const double p[2] = {b1pow, b2pow};
+  if (cudaMemcpyAsync(&t->dev.hdr->step, &st, sizeof(st), cudaMemcpyHostToDevice, s) != cudaSuccess) return MT_ECUDA;
+  if (cudaMemcpyAsync(&t->dev.hdr->b1pow, p, sizeof(p), cudaMemcpyHostToDevice, s) != cudaSuccess) return MT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MT_ECUDA;  // the host values above go out of scope
+  t->step = step;
+  return MT_OK;
+}
+
 int mt_get_error(mt_table* t, int32_t* device_error, int clear, mt_stream stream) {
   if (t == nullptr || device_error == nullptr) return MT_EINVAL;
   cudaStream_t s = as_stream(stream);

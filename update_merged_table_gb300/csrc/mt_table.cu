@@ -100,6 +100,71 @@ __global__ void k_compact_commit(const TableDev T, const Slot* fresh, const int*
     dst[s] = src[s];
 }
 
+// Import pass 1: find each key, or insert it like a lookup does (first
+// tombstone-or-EMPTY slot of its chain; warp-aggregated row pops); its row
+// goes to rows_out[i] (-1 when it could not be placed).
+__global__ void k_import_resolve(const TableDev T, const unsigned long long* keys, long long n, int32_t* rows_out) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long n_round = (n + 31) / 32 * 32;
+  const uint32_t step = (uint32_t)T.hdr->step;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_round; i += stride) {
+    const bool in = i < n;
+    const unsigned long long key = in ? keys[i] : kEmpty;
+    int32_t row = -1;
+    bool claimed = false;
+    unsigned long long cs = 0;
+    if (in && (key >> 56) == 0xFFull) latch_error(T.hdr, MT_EKEY);  // table id 255 holds the sentinels
+    if (in && (key >> 56) != 0xFFull) {
+      long long t_end, t_tomb;
+      const long long sidx = find_slot(T, key, &t_end, &t_tomb, &row);
+      if (sidx < 0) {
+        long long t = t_tomb >= 0 ? t_tomb : t_end;
+        unsigned long long slot = (home_slot(T, key) + (unsigned long long)t * T.S) & T.mask;
+        for (; t < (long long)T.max_probes; ++t) {
+          const unsigned long long k = load_key_relaxed(&T.slots[slot].key);
+          if ((k == kEmpty || k == kTomb) && atomicCAS(&T.slots[slot].key, k, key) == k) {
+            claimed = true;
+            cs = slot;
+            break;
+          }
+          slot = (slot + T.S) & T.mask;
+        }
+        if (!claimed) latch_error(T.hdr, MT_EFULL);
+      }
+    }
+    const unsigned need = __ballot_sync(kFull, claimed);
+    if (claimed) {
+      row = pop_row_warp(T, need);
+      if (row < 0) {
+        atomicExch(&T.slots[cs].key, kTomb);  // give the slot back; the chain stays intact
+        latch_error(T.hdr, MT_EFULL);
+      } else {
+        T.slots[cs].row = row;
+        T.slots[cs].meta = step;
+      }
+    }
+    if (in) rows_out[i] = row;
+  }
+}
+
+// Import pass 2: the given embedding and moments into each placed row.
+__global__ void k_import_write(const TableDev T, const int32_t* rows, long long n, const float* emb, const float* m,
+                               const float* v) {
+  const long long d = T.dim;
+  const long long total = n * d;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const long long i = it / d, j = it - i * d;
+    const int32_t r = rows[i];
+    if (r < 0 || r >= T.num_rows) continue;
+    char* rec = row_ptr(T, r);
+    if (T.row_dtype == MT_F32) reinterpret_cast<float*>(rec)[j] = emb[it];
+    else reinterpret_cast<__nv_bfloat16*>(rec)[j] = __float2bfloat16_rn(emb[it]);
+    reinterpret_cast<float*>(rec + T.emb_bytes)[j] = m[it];
+    reinterpret_cast<float*>(rec + T.emb_bytes + T.mv_bytes)[j] = v[it];
+  }
+}
+
 __global__ void __launch_bounds__(256) k_stats(const TableDev T) {
   __shared__ unsigned long long s_hist[MT_HIST_BINS];
   __shared__ unsigned long long s_live, s_tomb, s_disp;
@@ -256,6 +321,20 @@ cudaError_t launch_export(const TableDev& T, unsigned long long* keys, int32_t* 
   {
     MT_LAUNCH("k_export", s);
     k_export<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T, keys, rows, capacity);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_import(const TableDev& T, const unsigned long long* keys, long long n, const float* emb,
+                          const float* m, const float* v, int32_t* ws_rows, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  {
+    MT_LAUNCH("k_import_resolve", s);
+    k_import_resolve<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_rows);
+  }
+  {
+    MT_LAUNCH("k_import_write", s);
+    k_import_write<<<grid_for(n * T.dim, 256), 256, 0, s>>>(T, ws_rows, n, emb, m, v);
   }
   return cudaGetLastError();
 }
