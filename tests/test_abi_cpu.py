@@ -104,6 +104,13 @@ def test_null_handles_rejected(lib):
     assert lib.mt_step(None) == -1
     assert lib.mt_lookup_workspace_bytes(None, 10) == 0
     assert lib.mt_erase_workspace_bytes(1000) >= 4000
+    assert lib.mt_compact(None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_compact_workspace_bytes(None) == 0
+    assert lib.mt_import(None, None, 0, None, None, None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_import_workspace_bytes(1000) >= 4000 and lib.mt_import_workspace_bytes(-1) == 0
+    st, b1, b2 = ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+    assert lib.mt_get_adam_state(None, ctypes.byref(st), ctypes.byref(b1), ctypes.byref(b2), None) == mt.MT_EINVAL
+    assert lib.mt_set_adam_state(None, 0, 1.0, 1.0, None) == mt.MT_EINVAL
 
 
 def test_product_path_has_no_oracle_or_fallback():
