@@ -245,6 +245,20 @@ int mt_erase(mt_table* t, const uint64_t* keys, int64_t n, uint8_t* found, void*
 
 /* ---- inspection ------------------------------------------------------------ */
 
+/* Capacity expansion: move the table into a new arena `dev_mem` laid out
+ * for `new_cfg` (from mt_table_bytes(new_cfg)), which may have more slots
+ * (log2_slots) and more rows (num_rows) but must otherwise equal the
+ * table's configuration (dim, row dtype, probe step, seeds, init scale,
+ * flags; max_probes 0 means the new M).  The header, the Adam state and
+ * every row are copied (row indices do not change), the new rows join the
+ * free list, and every live key is inserted again along its probe sequence
+ * in the larger slot array (the key store is rebuilt on its own: MTGR
+ * section 5, Embedding Management).  Synchronises `stream`.  On success
+ * the handle uses the new arena and the caller may free the old one; if a
+ * key does not fit within the new max_probes, MT_EFULL is returned and the
+ * handle keeps the old arena, unchanged. */
+int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* dev_mem, size_t bytes, mt_stream stream);
+
 /* Workspace bytes mt_compact needs: one slot array of the table (M x 16 B)
  * plus 256 bytes. */
 size_t mt_compact_workspace_bytes(const mt_table* t);

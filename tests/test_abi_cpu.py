@@ -105,6 +105,7 @@ def test_null_handles_rejected(lib):
     assert lib.mt_lookup_workspace_bytes(None, 10) == 0
     assert lib.mt_erase_workspace_bytes(1000) >= 4000
     assert lib.mt_compact(None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_table_grow(None, None, None, 0, None) == mt.MT_EINVAL
     assert lib.mt_compact_workspace_bytes(None) == 0
     assert lib.mt_import(None, None, 0, None, None, None, None, 0, None) == mt.MT_EINVAL
     assert lib.mt_import_workspace_bytes(1000) >= 4000 and lib.mt_import_workspace_bytes(-1) == 0

@@ -403,6 +403,30 @@ def test_checkpoint_restore_continues_bit_identically(row_dtype):
     assert tab.error() == 0 and tab2.error() == 0
 
 
+def test_grow_keeps_keys_rows_and_training():
+    """Capacity expansion (2^10 to 2^12 slots, 1024 to 4096 rows) mid-training:
+    the same keys on the same rows, the Adam state kept, room for new keys,
+    and training continues in step with the oracle."""
+    rng = np.random.default_rng(13)
+    tab = mt.Table(10, 8, probe_step=3, init_seed=5)
+    ref = oracle.Table(12, 8, probe_step=3, init_seed=5)  # its capacity never binds in this test
+    ids = rng.choice(1 << 20, 600, replace=False).astype(np.int64)
+    run_steps(tab, ref, [W.single_feature(ids)], seed0=60)
+    before = tab.lookup(to_dev(ids), insert_missing=False)
+    U = before.U
+    rows_before, urows_before = before.rows.clone(), before.unique_rows[:U].clone()
+    st0, state0 = tab.stats(), tab.adam_state()
+    tab.grow(12)
+    st1 = tab.stats()
+    assert tab.error() == 0 and tab.adam_state() == state0
+    assert st1["capacity"] == 4096 and st1["live"] == st0["live"] == 600 and st1["tombstones"] == 0
+    assert st1["rows_free"] == 4096 - 600
+    after = tab.lookup(to_dev(ids), insert_missing=False)
+    assert after.U == U and torch.equal(after.unique_rows[:U], urows_before) and torch.equal(after.rows, rows_before)
+    more = np.concatenate([ids[:300], rng.choice(1 << 20, 2000).astype(np.int64)])
+    run_steps(tab, ref, [W.single_feature(more)], seed0=61)  # 2600 keys: more than the old table held
+
+
 def test_step_counter_and_lazy_rows():
     tab = mt.Table(10, 8)
     ref = oracle.Table(10, 8)

@@ -75,6 +75,7 @@ ABI_FUNCTIONS = {
     "mt_table_create": (_I32, [_P, _P, _SZ, _P, _P]),
     "mt_table_destroy": (_I32, [_P]),
     "mt_table_config": (_I32, [_P, _P]),
+    "mt_table_grow": (_I32, [_P, _P, _P, _SZ, _P]),
     "mt_lookup_workspace_bytes": (_SZ, [_P, _I64]),
     "mt_lookup": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "mt_lookup_static": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P]),
@@ -316,6 +317,24 @@ class Table:
                                          ctypes.byref(hp), _ptr(gsum), ws.data_ptr(), ws.numel(), _stream(stream)),
                "mt_backward_adam")
         return gsum
+
+    def grow(self, log2_slots: int, num_rows: int = 0, stream=None):
+        """Capacity expansion into a new arena with 2^log2_slots slots and num_rows rows
+        (0 = one per slot); keys, rows and the Adam state carry over."""
+        torch = _torch()
+        c = _Config(log2_slots, self.cfg.dim, self.cfg.row_dtype, 0, self.cfg.probe_step, self.cfg.hash_seed,
+                    self.cfg.init_seed, self.cfg.init_scale, self.cfg.flags, num_rows)
+        nbytes = self.lib.mt_table_bytes(ctypes.byref(c))
+        if nbytes == 0:
+            raise MTError(MT_EINVAL, "mt_table_bytes")
+        arena = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        _check(self.lib.mt_table_grow(self.h, ctypes.byref(c), arena.data_ptr(), nbytes, _stream(stream)),
+               "mt_table_grow")
+        self.arena = arena  # the old arena is released with the last reference to it
+        out = _Config()
+        _check(self.lib.mt_table_config(self.h, ctypes.byref(out)), "mt_table_config")
+        self.cfg = out
+        self.log2_slots = log2_slots
 
     def compact(self, stream=None):
         """Rebuild the key store without tombstones (rows and keys unchanged)."""

@@ -65,6 +65,35 @@ ArenaLayout arena_layout(const mt_config& c) {
   return L;
 }
 
+uint64_t inverse_mod_2_64(uint64_t S);
+
+// The kernels' view of a table laid out by L in the arena at dev_mem.
+mt::TableDev device_view(const mt_config& c, const ArenaLayout& L, void* dev_mem) {
+  mt::TableDev T{};
+  char* base = static_cast<char*>(dev_mem);
+  T.hdr = reinterpret_cast<mt::Header*>(base + L.hdr);
+  T.slots = reinterpret_cast<mt::Slot*>(base + L.slots);
+  T.free_stack = reinterpret_cast<int32_t*>(base + L.stack);
+  T.rows = base + L.rows;
+  const uint64_t M = 1ull << c.log2_slots;
+  T.mask = M - 1;
+  T.S = c.probe_step;
+  T.hash_seed = c.hash_seed;
+  T.init_seed = c.init_seed;
+  T.Sinv = inverse_mod_2_64(c.probe_step) & (M - 1);
+  T.log2_slots = c.log2_slots;
+  T.max_probes = c.max_probes;
+  T.flags = c.flags;
+  T.dim = c.dim;
+  T.rec_bytes = L.rec_bytes;
+  T.emb_bytes = L.emb_bytes;
+  T.mv_bytes = L.mv_bytes;
+  T.row_dtype = (int)c.row_dtype;
+  T.init_scale = c.init_scale;
+  T.num_rows = c.num_rows;
+  return T;
+}
+
 // S^-1 mod 2^64 by Newton's iteration x <- x(2 - Sx); exact for odd S.
 uint64_t inverse_mod_2_64(uint64_t S) {
   uint64_t x = S;  // correct to 3 bits for odd S
@@ -121,34 +150,39 @@ int mt_table_create(const mt_config* cfg, void* dev_mem, size_t bytes, mt_stream
   t->cfg = c;
   t->arena_bytes = L.total;
   t->step = 0;
-  char* base = static_cast<char*>(dev_mem);
   mt::TableDev& T = t->dev;
-  T.hdr = reinterpret_cast<mt::Header*>(base + L.hdr);
-  T.slots = reinterpret_cast<mt::Slot*>(base + L.slots);
-  T.free_stack = reinterpret_cast<int32_t*>(base + L.stack);
-  T.rows = base + L.rows;
-  const uint64_t M = 1ull << c.log2_slots;
-  T.mask = M - 1;
-  T.S = c.probe_step;
-  T.hash_seed = c.hash_seed;
-  T.init_seed = c.init_seed;
-  T.Sinv = inverse_mod_2_64(c.probe_step) & (M - 1);
-  T.log2_slots = c.log2_slots;
-  T.max_probes = c.max_probes;
-  T.flags = c.flags;
-  T.dim = c.dim;
-  T.rec_bytes = L.rec_bytes;
-  T.emb_bytes = L.emb_bytes;
-  T.mv_bytes = L.mv_bytes;
-  T.row_dtype = (int)c.row_dtype;
-  T.init_scale = c.init_scale;
-  T.num_rows = c.num_rows;
+  T = device_view(c, L, dev_mem);
   const cudaError_t e = mt::launch_table_init(T, as_stream(stream));
   if (e != cudaSuccess) {
     delete t;
     return MT_ECUDA;
   }
   *out = t;
+  return MT_OK;
+}
+
+int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* dev_mem, size_t bytes, mt_stream stream) {
+  if (t == nullptr) return MT_EINVAL;
+  mt_config c;
+  const int rc = normalise(new_cfg, &c);
+  if (rc != MT_OK) return rc;
+  const mt_config& o = t->cfg;
+  if (c.log2_slots < o.log2_slots || c.num_rows < o.num_rows || c.dim != o.dim || c.row_dtype != o.row_dtype ||
+      c.hash_seed != o.hash_seed || c.init_seed != o.init_seed || c.init_scale != o.init_scale ||
+      c.flags != o.flags || (c.probe_step & ((1ull << o.log2_slots) - 1)) != o.probe_step)
+    return MT_EINVAL;
+  const ArenaLayout L = arena_layout(c);
+  if (dev_mem == nullptr || bytes < L.total || !aligned(dev_mem, 256)) return MT_ENOSPACE;
+  const mt::TableDev T2 = device_view(c, L, dev_mem);
+  cudaStream_t s = as_stream(stream);
+  if (mt::launch_grow(t->dev, T2, s) != cudaSuccess) return MT_ECUDA;
+  int32_t fail = 0;
+  if (cudaMemcpyAsync(&fail, &T2.hdr->pad0, sizeof(fail), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MT_ECUDA;
+  if (fail) return MT_EFULL;
+  t->cfg = c;
+  t->dev = T2;
+  t->arena_bytes = L.total;
   return MT_OK;
 }
 

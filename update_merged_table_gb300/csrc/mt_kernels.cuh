@@ -111,6 +111,7 @@ cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long
 cudaError_t launch_compact(const TableDev& T, void* ws, cudaStream_t s);
 cudaError_t launch_import(const TableDev& T, const unsigned long long* keys, long long n, const float* emb,
                           const float* m, const float* v, int32_t* ws_rows, cudaStream_t s);
+cudaError_t launch_grow(const TableDev& T, const TableDev& T2, cudaStream_t s);
 cudaError_t launch_stats(const TableDev& T, cudaStream_t s);
 cudaError_t launch_export(const TableDev& T, unsigned long long* keys, int32_t* rows, long long capacity,
                           cudaStream_t s);

@@ -165,6 +165,43 @@ __global__ void k_import_write(const TableDev T, const int32_t* rows, long long 
   }
 }
 
+// Capacity expansion, pass 1: the new rows (old R .. new R - 1) join the
+// free list above the old free entries, and the free count grows with them.
+__global__ void k_grow_rows(const TableDev T2, long long old_rows) {
+  const long long added = T2.num_rows - old_rows;
+  const long long top = T2.hdr->free_top;  // copied from the old header
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < added;
+       i += (long long)gridDim.x * blockDim.x)
+    T2.free_stack[top + i] = (int32_t)(old_rows + i);
+}
+__global__ void k_grow_top(const TableDev T2, long long old_rows) {
+  T2.hdr->free_top += T2.num_rows - old_rows;
+  T2.hdr->pad0 = 0;  // the rebuild's "a key did not fit" flag
+}
+
+// Capacity expansion, pass 2: every live key of the old slots is inserted
+// into the new (all EMPTY) slots along its probe sequence in the new table.
+__global__ void k_grow_rebuild(const TableDev T, const TableDev T2) {
+  const unsigned long long M = T.mask + 1;
+  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
+       s += (unsigned long long)gridDim.x * blockDim.x) {
+    const Slot old = T.slots[s];
+    if (old.key == kEmpty || old.key == kTomb) continue;
+    unsigned long long h = home_slot(T2, old.key);
+    bool placed = false;
+    for (uint32_t t = 0; t < T2.max_probes; ++t) {
+      if (atomicCAS(&T2.slots[h].key, kEmpty, old.key) == kEmpty) {
+        T2.slots[h].row = old.row;
+        T2.slots[h].meta = old.meta;
+        placed = true;
+        break;
+      }
+      h = (h + T2.S) & T2.mask;
+    }
+    if (!placed) atomicExch(&T2.hdr->pad0, 1);
+  }
+}
+
 __global__ void __launch_bounds__(256) k_stats(const TableDev T) {
   __shared__ unsigned long long s_hist[MT_HIST_BINS];
   __shared__ unsigned long long s_live, s_tomb, s_disp;
@@ -335,6 +372,27 @@ cudaError_t launch_import(const TableDev& T, const unsigned long long* keys, lon
   {
     MT_LAUNCH("k_import_write", s);
     k_import_write<<<grid_for(n * T.dim, 256), 256, 0, s>>>(T, ws_rows, n, emb, m, v);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grow(const TableDev& T, const TableDev& T2, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(T2.hdr, T.hdr, kHeaderBytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(T2.free_stack, T.free_stack, (size_t)T.num_rows * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(T2.rows, T.rows, (size_t)T.num_rows * T.rec_bytes, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(T2.slots, 0xFF, (size_t)(T2.mask + 1) * sizeof(Slot), s);  // keys EMPTY
+  if (e != cudaSuccess) return e;
+  if (T2.num_rows > T.num_rows) {
+    MT_LAUNCH("k_grow_rows", s);
+    k_grow_rows<<<grid_for(T2.num_rows - T.num_rows, 256), 256, 0, s>>>(T2, T.num_rows);
+  }
+  {
+    MT_LAUNCH("k_grow_top", s);
+    k_grow_top<<<1, 1, 0, s>>>(T2, T.num_rows);
+  }
+  {
+    MT_LAUNCH("k_grow_rebuild", s);
+    k_grow_rebuild<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T, T2);
   }
   return cudaGetLastError();
 }
