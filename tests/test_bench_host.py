@@ -1,0 +1,52 @@
+"""The benchmark's host-side pieces on CPU: every workload builds batches of
+the sizes it states, its bounded oracle sample is smaller than the timed
+batch, and the batch statistics behind the algorithmic bytes (uniques, heavy
+uniques and their positions) match a plain count."""
+import collections
+
+import numpy as np
+import pytest
+
+import bench
+
+
+def plain_stats(b):
+    f = np.searchsorted(b.feat_offsets, np.arange(b.n), side="right") - 1
+    keys = [(int(b.table_ids[f[i]]) << 56) | int(b.ids[i]) for i in range(b.n)]
+    cnt = collections.Counter(keys)
+    heavy = [c for c in cnt.values() if c > 32]
+    return len(cnt), len(heavy), sum(heavy)
+
+
+@pytest.mark.parametrize("cfg, n", [(1, 4096), (2, 65536), (4, 1 << 20)])
+def test_workload_batch_sizes(cfg, n):
+    wl = bench.Workload(cfg)
+    b, er = wl.batch(1)
+    assert b.n == n and er is None
+    assert b.feat_offsets[0] == 0 and b.feat_offsets[-1] == b.n and np.all(np.diff(b.feat_offsets) >= 0)
+    s = wl.sample_batch(1)
+    assert 0 < s.n <= b.n
+
+
+def test_jagged_workload_and_reduced_name():
+    wl = bench.Workload(3, users=64, log2_slots=18)
+    b, er = wl.batch(2)
+    assert er is None and b.table_ids.tolist() == [0, 1, 2, 3]
+    assert b.n == b.feat_offsets[-1] and b.n % 4 == 0  # four features per token
+    assert "reduced" in wl.name and wl.log2 == 18 and wl.row == "bf16" and wl.grad == "bf16"
+
+
+def test_batch_stats_match_a_plain_count():
+    wl = bench.Workload(2)
+    b, _ = wl.batch(3)
+    assert bench.batch_stats(b) == plain_stats(b)
+    wl3 = bench.Workload(3, users=48)
+    b3, _ = wl3.batch(0)
+    assert bench.batch_stats(b3) == plain_stats(b3)
+
+
+def test_row_and_grad_bytes():
+    wl = bench.Workload(3)
+    assert wl.row_bytes == 128 and wl.grad_bytes == 128
+    wl4 = bench.Workload(4)
+    assert wl4.row_bytes == 512 and wl4.grad_bytes == 512
