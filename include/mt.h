@@ -3,10 +3,11 @@
  * The hot path of a dynamic hash embedding table as described in "MTGenRec:
  * An Efficient Distributed Training System for Generative Recommendation
  * Models in Meituan" (TL;DR and abstract: dynamic hash tables replacing
- * static ones for real-time insertion and deletion, automated table merging,
- * two-stage ID deduplication) and in "MTGR: Industrial-Scale Generative
+ * static ones so keys can be inserted and deleted while training runs, feature
+ * tables merged into one, ID deduplication in two stages) and in "MTGR: Industrial-Scale Generative
  * Recommendation Framework in Meituan" (section 5, Embedding Management: keys
- * map to embedding vectors plus metadata; Embedding Lookup: IDs stay unique).
+ * lead to embeddings plus bookkeeping data; Embedding Lookup: no duplicate IDs
+ * on either side of an exchange).
  *
  * Conventions that hold for every call:
  *  - Plain C types only.  `mt_stream` is a cudaStream_t passed as void*
@@ -54,7 +55,7 @@ enum {
 enum { MT_F32 = 0, MT_BF16 = 1 };
 
 /* Merged key = (table_id << 56) | id with table_id in [0, 254] and id in
- * [0, 2^56) ("automated table merging", MTGenRec TL;DR).  Table id 255 is
+ * [0, 2^56) (feature tables merged into one table, MTGenRec TL;DR).  Table id 255 is
  * reserved for the two slot sentinels. */
 #define MT_KEY_EMPTY 0xFFFFFFFFFFFFFFFFull
 #define MT_KEY_TOMBSTONE 0xFFFFFFFFFFFFFFFEull
@@ -233,7 +234,7 @@ int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const 
 /* Workspace bytes mt_erase needs for n keys. */
 size_t mt_erase_workspace_bytes(int64_t n);
 
-/* Delete n merged keys ("real-time deletions", MTGenRec abstract): a live
+/* Delete n merged keys (keys deleted while training runs, MTGenRec abstract): a live
  * key's slot becomes MT_KEY_TOMBSTONE, which later probes pass over and
  * later inserts may reuse, and its row returns to the free list.  A key
  * inserted again later starts from its initial row with m = v = 0.
@@ -282,7 +283,7 @@ int mt_stats(mt_table* t, mt_stats_out* out, mt_stream stream);
 
 /* Copy up to `capacity` live (key, row) pairs into device buffers keys/rows
  * (in no particular order) and the number of live keys into *count (host).
- * Synchronises `stream`.  ("compact key scanning", MTGR section 5.) */
+ * Synchronises `stream`.  (export by a scan of the key store, MTGR section 5.) */
 int mt_export(mt_table* t, uint64_t* keys, int32_t* rows, int64_t capacity, int64_t* count, mt_stream stream);
 
 /* Read n rows (device int32 row indices; -1 gives zeros) as fp32 into device

@@ -7,17 +7,17 @@
 // double accumulation in position order and Adam is a serial fp32 loop.
 //
 // What each part follows:
-//  * Merged keys -- "automated table merging" (MTGenRec, TL;DR and abstract):
+//  * Merged keys -- feature tables merged into one (MTGenRec, TL;DR and abstract):
 //    several feature tables share one hash table.  A key is
 //    (table_id << 56) | id with table_id in [0, 254]; table_id 255 holds the
 //    two sentinels (EMPTY = 2^64-1, TOMBSTONE = 2^64-2).
-//  * Unique + inverse -- "two-stage ID deduplication" (MTGenRec, TL;DR) and
-//    "IDs remain unique before and after communication" (MTGR, section 5,
-//    Embedding Lookup).  The unique list is in first-occurrence order, the
+//  * Unique + inverse -- ID deduplication in two stages (MTGenRec, TL;DR);
+//    the IDs a lookup exchanges hold no duplicates on either side of the
+//    exchange (MTGR, section 5, Embedding Lookup).  The unique list is in first-occurrence order, the
 //    semantics of the Unique operator (Meituan TensorFlow article, section 3.6).
-//  * Dynamic table with real-time insertion and deletion (MTGenRec, abstract;
-//    MTGR section 5, Embedding Management: keys map to embedding vectors and
-//    metadata).
+//  * Dynamic table whose keys are inserted and deleted while training runs
+//    (MTGenRec, abstract; MTGR section 5, Embedding Management: each key
+//    leads to its embedding and to bookkeeping data).
 //  * Probe sequence h_t = (h0 + t*S) mod M, M = 2^n, S odd (MTGenRec,
 //    Theorem 1) -- used only by the shadow open-addressing simulator that
 //    produces occupancy statistics; the table itself is an unordered_map.

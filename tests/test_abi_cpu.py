@@ -114,6 +114,19 @@ def test_null_handles_rejected(lib):
     assert lib.mt_set_adam_state(None, 0, 1.0, 1.0, None) == mt.MT_EINVAL
 
 
+def test_set_adam_state_rejects_inconsistent_state(lib):
+    """Arguments are checked before the handle is used: a zeroed stand-in handle (never a real table
+    here) shows which combinations pass validation (they then fail at the CUDA call: no GPU)."""
+    fake = ctypes.create_string_buffer(4096)
+    h = ctypes.cast(fake, ctypes.c_void_p)
+    for step, b1, b2 in [(0, 0.9, 1.0), (0, 1.0, 0.999), (3, 1.0, 0.5), (3, 0.5, 1.0), (-1, 1.0, 1.0),
+                         (2, float("nan"), 0.5), (2, 0.5, 1.5), (2, -0.1, 0.5)]:
+        assert lib.mt_set_adam_state(h, step, b1, b2, None) == mt.MT_EINVAL, (step, b1, b2)
+    for step, b1, b2 in [(0, 1.0, 1.0), (3, 0.729, 0.997002999), (5, 0.0, 0.0)]:
+        rc = lib.mt_set_adam_state(h, step, b1, b2, None)
+        assert rc != mt.MT_EINVAL, (step, b1, b2)
+
+
 def test_product_path_has_no_oracle_or_fallback():
     """The package never imports the oracle and has no CPU path."""
     pkg = os.path.join(ROOT, "update_merged_table_gb300")

@@ -16,7 +16,7 @@ from update_merged_table_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-RTOL, ATOL = 1e-5, 1e-6
+from numerics import ATOL, RTOL, assert_rows_close  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -33,23 +33,6 @@ def dev():
 
 def to_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
-
-
-def bf16_bits_of(x: np.ndarray) -> np.ndarray:
-    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
-
-
-def assert_rows_close(got: np.ndarray, want: np.ndarray, row_dtype: str):
-    if row_dtype == "bf16":
-        # both sides hold bf16 values; allow one unit in the last place
-        gb = bf16_bits_of(got).astype(np.int32)
-        wb = bf16_bits_of(want).astype(np.int32)
-        same_sign = np.sign(got) == np.sign(want)
-        diff = np.where(same_sign, np.abs(gb - wb), np.abs(got - want) > 0)
-        bad = (diff > 1) & ~((np.abs(got) < 1e-30) & (np.abs(want) < 1e-30))
-        assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], want[bad][:5])
-    else:
-        np.testing.assert_allclose(got, want, rtol=RTOL, atol=ATOL)
 
 
 def compare_lookup(res, r, gather=True):
@@ -455,19 +438,33 @@ def test_integer_grads_sum_exactly():
 # full size, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
 
-def test_full_size_jagged_two_steps():
-    """2048 users, lognormal(5, 1) lengths capped at 3000, 4 features, M = 2^24, dim 64 bf16."""
+def test_full_size_jagged_fresh_steps():
+    """2048 users, lognormal(5, 1) lengths capped at 3000, 4 features, M = 2^24, dim 64 bf16: the cold step 0
+    and five fresh-seed steps (each a new batch of users, so every step inserts keys), all compared in full."""
     tab = mt.Table(24, 64, row_dtype="bf16")
     ref = oracle.Table(24, 64, row_dtype=oracle.BF16)
-    batches = [W.jagged_batch(s, lengths_seed=0) for s in range(2)]
+    batches = [W.jagged_batch(s) for s in range(6)]
     run_steps(tab, ref, batches, row_dtype="bf16", grad_dtype="bf16")
+    assert tab.stats()["live"] == ref.live
 
 
 def test_full_size_merged():
-    """8 tables, 65536 IDs, M = 2^22, dim 32 fp32, 3 steps."""
+    """8 tables, 65536 IDs, M = 2^22, dim 32 fp32: all 100 steps, lookups compared every step and
+    gradient sums and Adam rows every tenth step."""
     tab = mt.Table(22, 32)
     ref = oracle.Table(22, 32)
-    run_steps(tab, ref, [W.merged_batch(s) for s in range(3)])
+    for k in range(100):
+        b = W.merged_batch(k)
+        res = tab.lookup(to_dev(b.ids), b.feat_offsets, b.table_ids)
+        r = ref.lookup(b.ids, b.feat_offsets, b.table_ids, gather=(k % 10 == 0))
+        compare_lookup(res, r, gather=(k % 10 == 0))
+        gd, gh, gdt = grads_for(300 + k, b.n, 32, "f32")
+        check = k % 10 == 0 or k == 99
+        gsum = tab.backward_adam(res, gd, want_gsum=check)
+        ref_gsum = ref.backward_adam(gh, grad_dtype=gdt, want_gsum=check)
+        if check:
+            compare_after_adam(tab, res, ref, r, "f32", gsum, ref_gsum)
+    assert tab.error() == 0 and ref.error == 0 and tab.step == ref.step == 100
 
 
 def test_ranks_are_a_permutation_per_key():
@@ -566,6 +563,7 @@ def test_full_size_large_table():
     assert pr.all()
     np.testing.assert_allclose(emb.cpu().numpy(), e2, rtol=RTOL, atol=ATOL)
     np.testing.assert_allclose(m.cpu().numpy(), m2, rtol=RTOL, atol=ATOL)
+    np.testing.assert_allclose(v.cpu().numpy(), v2, rtol=RTOL, atol=1e-9)
     assert tab.error() == 0
 
 
@@ -610,5 +608,6 @@ def test_full_size_online_churn():
             e2, m2, v2, pr = ref.get_rows(keys_now)
             assert np.array_equal(rows_now.cpu().numpy() >= 0, pr)
             np.testing.assert_allclose(emb.cpu().numpy()[pr], e2[pr], rtol=RTOL, atol=ATOL)
+            np.testing.assert_allclose(m.cpu().numpy()[pr], m2[pr], rtol=RTOL, atol=ATOL)
             np.testing.assert_allclose(v.cpu().numpy()[pr], v2[pr], rtol=RTOL, atol=1e-9)
     assert tab.error() == 0 and ref.error == 0

@@ -82,6 +82,23 @@ def test_churn_stream_fresh_ids():
     assert e1.max() < cs.next_fresh
 
 
+def test_churn_erases_only_live_ids():
+    """The erase set of each step is distinct and drawn from the IDs live after that step's lookup:
+    the prefill, plus every ID handed out, minus every ID erased and not handed out again."""
+    hot = 1 << 12
+    cs = W.ChurnStream(1, hot=hot, n=1 << 10, erase=1 << 9)
+    live = set(range(hot))
+    for k in range(6):
+        b, er = cs.step(k)
+        live.update(b.ids.tolist())
+        assert er.size == 1 << 9 and np.unique(er).size == er.size
+        assert all(int(x) in live for x in er)
+        live.difference_update(er.tolist())
+        assert set(cs.live_ids().tolist()) == live
+    with pytest.raises(ValueError):
+        cs.step(9)  # steps are taken in order
+
+
 def test_batches_are_deterministic():
     a = W.merged_batch(3, per_table=256)
     b = W.merged_batch(3, per_table=256)

@@ -8,8 +8,8 @@ fallback: without the built library every call raises.
 
 The path follows "MTGenRec: An Efficient Distributed Training System for
 Generative Recommendation Models in Meituan" (TL;DR and abstract: dynamic
-hash embedding tables with real-time insertion and deletion, automated table
-merging, two-stage ID deduplication; Theorem 1: probing h_t = (h0 + t*S) mod
+hash embedding tables whose keys are inserted and deleted while training
+runs, feature tables merged into one table, ID deduplication in two stages; Theorem 1: probing h_t = (h0 + t*S) mod
 2^n with odd S) and "MTGR" section 5 (Embedding Management, Embedding Lookup).
 """
 from __future__ import annotations

@@ -173,6 +173,11 @@ int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* dev_mem, size_t b
     return MT_EINVAL;
   const ArenaLayout L = arena_layout(c);
   if (dev_mem == nullptr || bytes < L.total || !aligned(dev_mem, 256)) return MT_ENOSPACE;
+  {  // the new arena must not overlap the old one: the rebuild reads the old slots while it writes the new
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(dev_mem), a1 = a0 + L.total;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(t->dev.hdr), b1 = b0 + t->arena_bytes;
+    if (a0 < b1 && b0 < a1) return MT_EINVAL;
+  }
   const mt::TableDev T2 = device_view(c, L, dev_mem);
   cudaStream_t s = as_stream(stream);
   if (mt::launch_grow(t->dev, T2, s) != cudaSuccess) return MT_ECUDA;
@@ -409,8 +414,12 @@ int mt_get_adam_state(mt_table* t, int64_t* step, double* b1pow, double* b2pow, 
 }
 
 int mt_set_adam_state(mt_table* t, int64_t step, double b1pow, double b2pow, mt_stream stream) {
-  if (t == nullptr || step < 0 || !(b1pow >= 0.0 && b1pow <= 1.0) || !(b2pow >= 0.0 && b2pow <= 1.0))
-    return MT_EINVAL;
+  // The state must be one that backward calls could have produced: before the first step both
+  // powers are exactly 1; after it both lie in [0, 1), so every bias correction 1 - b^t is positive.
+  if (step < 0) return MT_EINVAL;
+  if (step == 0 && !(b1pow == 1.0 && b2pow == 1.0)) return MT_EINVAL;
+  if (step > 0 && !(b1pow >= 0.0 && b1pow < 1.0 && b2pow >= 0.0 && b2pow < 1.0)) return MT_EINVAL;
+  if (t == nullptr) return MT_EINVAL;
   cudaStream_t s = as_stream(stream);
   const long long st = step;
   const double p[2] = {b1pow, b2pow};

@@ -5,8 +5,8 @@
 // A row record is [emb: d x row dtype][m: d x fp32][v: d x fp32], each part a
 // multiple of 16 bytes, so every part of a row is reached with 16-byte vector
 // accesses.  A slot {key, row, meta} maps a merged key to its row and keeps
-// the table step at which it was inserted ("keys map to embedding vectors and
-// metadata", MTGR section 5, Embedding Management); the key store is separate
+// the table step at which it was inserted (MTGR section 5, Embedding
+// Management: each key leads to its embedding and to bookkeeping data); the key store is separate
 // from the rows, so it can be rebuilt without moving any embedding.
 #pragma once
 

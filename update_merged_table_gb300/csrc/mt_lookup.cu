@@ -1,10 +1,10 @@
 // Forward path of the merged dynamic embedding table: merged-key encoding,
-// two-stage ID deduplication, find/insert with odd-step probing, and the
+// ID deduplication in two stages, find/insert with odd-step probing, and the
 // embedding gather.
 //
-// Pages: "MTGenRec" TL;DR and abstract (hash-based dynamic embedding table,
-// automated table merging, two-stage ID deduplication for faster lookup,
-// real-time insertions); Theorem 1 (probe sequence h_t = (h0 + t*S) mod 2^n
+// Pages: "MTGenRec" TL;DR and abstract (a dynamic embedding table built on
+// hashing, feature tables merged into one, deduplication of IDs in two
+// stages to speed up lookups, keys inserted while training runs); Theorem 1 (probe sequence h_t = (h0 + t*S) mod 2^n
 // with S odd covers the table); "MTGR" section 5, Embedding Lookup (IDs stay
 // unique).
 //

@@ -1,9 +1,9 @@
 // Table maintenance kernels: arena initialisation, key deletion with
 // tombstones, the occupancy scan, live-key export and row read-back.
 //
-// Pages: "MTGenRec" abstract (real-time insertions and deletions in dynamic
+// Pages: "MTGenRec" abstract (dynamic hash tables whose keys are inserted and deleted while training runs, in
 // hash tables) and Theorem 1 (probe sequence h_t = (h0 + t*S) mod 2^n, S odd);
-// "MTGR" section 5, Embedding Management (compact key scanning).
+// "MTGR" section 5, Embedding Management (exporting keys by scanning the key store).
 #include "mt_kernels.cuh"
 
 namespace mt {

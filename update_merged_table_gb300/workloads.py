@@ -7,8 +7,8 @@ fed from here, so the two always see the same bytes.
 
 The workloads follow the sparse-embedding workloads described in
 "MTGenRec: An Efficient Distributed Training System for Generative
-Recommendation Models in Meituan" (dynamic hash embedding table, automated table
-merging, two-stage ID deduplication) and the jagged user sequences of "MTGR:
+Recommendation Models in Meituan" (dynamic hash embedding table, feature tables
+merged into one, ID deduplication in two stages) and the jagged user sequences of "MTGR:
 Industrial-Scale Generative Recommendation Framework in Meituan" (section 5,
 "Load Balance").  The pages measure on production data that is not available,
 so every batch here is synthetic:
@@ -230,9 +230,12 @@ def large_table_prefill_ids(count: int) -> np.ndarray:
 class ChurnStream:
     """Per step: n IDs, `new_frac` of them never seen before, plus an erase set.
 
-    The hot universe is IDs [0, hot); fresh IDs count up from `hot`.  The erase
-    set is drawn uniformly from every ID that has been handed out so far (some
-    may already be erased; erasing them again reports not-found).
+    The hot universe is IDs [0, hot); fresh IDs count up from `hot`.  The
+    stream assumes its prefill_ids() were inserted before step 0 and that
+    every ID of a step is inserted by that step's lookup, so it knows which
+    IDs are live: the erase set of a step is drawn uniformly, without
+    replacement, from the IDs live after that step's lookup, and those IDs are
+    live no longer.  Steps must be taken in order 0, 1, 2, ...
     """
 
     def __init__(self, seed: int, hot: int = 1 << 23, n: int = 1 << 18, new_frac: float = 0.1,
@@ -240,11 +243,16 @@ class ChurnStream:
         self.seed, self.hot, self.n, self.new_frac, self.erase, self.s = seed, hot, n, new_frac, erase, s
         self.next_fresh = hot
         self._zipf = ZipfSampler(s, hot)
+        self._live = np.ones(hot, dtype=bool)
+        self._next_step = 0
 
     def prefill_ids(self) -> np.ndarray:
         return np.arange(self.hot, dtype=np.int64)
 
     def step(self, k: int) -> tuple[Batch, np.ndarray]:
+        if k != self._next_step:
+            raise ValueError(f"churn steps must be taken in order: expected step {self._next_step}, got {k}")
+        self._next_step += 1
         rng = np.random.default_rng([self.seed, 0xC4, k])
         n_new = int(round(self.n * self.new_frac))
         hot_ids = self._zipf.sample(rng, self.n - n_new) - 1
@@ -252,5 +260,16 @@ class ChurnStream:
         self.next_fresh += n_new
         ids = np.concatenate([hot_ids, fresh])
         ids = ids[rng.permutation(ids.size)]
-        erase_ids = rng.integers(0, self.next_fresh, size=self.erase, dtype=np.int64)
+        if self._live.size < self.next_fresh:
+            grown = np.zeros(max(self.next_fresh, 2 * self._live.size), dtype=bool)
+            grown[: self._live.size] = self._live
+            self._live = grown
+        self._live[ids] = True
+        live_ids = np.flatnonzero(self._live[: self.next_fresh])
+        erase_ids = rng.choice(live_ids, size=min(self.erase, live_ids.size), replace=False).astype(np.int64)
+        self._live[erase_ids] = False
         return single_feature(ids), erase_ids
+
+    def live_ids(self) -> np.ndarray:
+        """The IDs live after the last step taken (prefill, then every step's inserts and erases)."""
+        return np.flatnonzero(self._live[: self.next_fresh]).astype(np.int64)
