@@ -6,10 +6,12 @@ erase of that step's deletions for the online-churn workload.  The default
 workload (``--config 3``) is the GRM jagged-sequence batch: 2048 users with
 lognormal(5, 1) sequence lengths capped at 3000, 4 ID features per token
 (Zipf(1.1) over 1e6 IDs each, merged by table id), M = 2^24 slots, dim 64
-bf16 rows, fp32 Adam state, bf16 grads.  Synthetic, seeded inputs; every
-step's inputs and outputs exceed the 126 MB L2, so no flush is needed between
-steps.  ``--config 1, 2, 4, 5`` time the single-table, merged-tables,
-large-table and online-churn workloads the same way.
+bf16 rows, fp32 Adam state, bf16 grads.  A run is the cold step 0, warm-up
+steps on it, then K timed steps on fresh seeds 1..K, so every timed step
+inserts the keys it brings that the table has not seen.  Synthetic, seeded
+inputs; every step's inputs and outputs exceed the 126 MB L2, so no flush is
+needed between steps.  ``--config 1, 2, 4, 5`` time the single-table,
+merged-tables, large-table and online-churn workloads the same way.
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle on a bounded
 sample of the same workload instead.
@@ -40,8 +42,16 @@ FALLBACK_HBM_GBS = 6800.0
 # workloads
 # ---------------------------------------------------------------------------
 
+FRESH_CAP = 64  # distinct fresh-seed steps held on the device; longer runs cycle through them
+
+
 class Workload:
-    """Table shape, batch generator and (for the oracle sample) a smaller batch generator."""
+    """Table shape and the step sequence of one workload.
+
+    A run is a cold step 0 (seed 0: on an empty or prefilled table it inserts
+    its keys), warm-up steps, and timed steps 1, 2, ... on fresh seeds, so the
+    timed steps insert whatever keys they bring that the table has not seen.
+    """
 
     def __init__(self, cfg: int, users: int = 2048, log2_slots: int | None = None):
         self.cfg = cfg
@@ -66,10 +76,12 @@ class Workload:
             self.prefill_ids = lambda: W.large_table_prefill_ids(int(0.7 * (1 << 26)))
         elif cfg == 5:
             self.name = ("online churn: M=2^24, dim 64 fp32, 2^23 prefilled keys, 2^18 IDs per step with 10% new, "
-                         "erase of 2^16 keys per step")
+                         "erase of 2^16 live keys per step")
             self.log2, self.dim, self.row, self.grad = 24, 64, "f32", "f32"
             self.churn = W.ChurnStream(0)
             self.prefill_ids = self.churn.prefill_ids
+            self._sample_churn = W.ChurnStream(0)
+            self._sample_next = 0
         else:
             raise ValueError("config must be 1..5")
         if log2_slots is not None:
@@ -79,7 +91,7 @@ class Workload:
                          f"4 ID features, M=2^{self.log2}, dim 64 bf16")
 
     def batch(self, seed: int):
-        """(batch, erase ids or None) of step `seed`."""
+        """(batch, None) of seed `seed` (configs 1-4; the churn stream is sequential, see `steps`)."""
         if self.cfg == 1:
             return W.single_table_batch(seed), None
         if self.cfg == 2:
@@ -88,20 +100,28 @@ class Workload:
             return W.jagged_batch(seed, users=self.users), None
         if self.cfg == 4:
             return W.large_table_batch(seed), None
-        return self.churn.step(seed)
+        raise ValueError("the churn workload draws its steps in order: use steps()")
 
-    def sample_batch(self, seed: int):
-        """A bounded slice of the same workload for the CPU oracle."""
-        if self.cfg == 2:
-            return W.merged_batch(seed, per_table=2048)
-        if self.cfg == 3:
-            return W.jagged_batch(seed, users=256)
-        if self.cfg == 4:
-            return W.large_table_batch(seed, n=1 << 17)
+    def steps(self, first: int, count: int):
+        """(batch, erase ids or None) of steps first .. first+count-1.  For the churn workload
+        the stream is sequential, so successive calls must continue where the last one ended."""
         if self.cfg == 5:
-            b, _ = self.churn.step(seed)
+            return [self.churn.step(k) for k in range(first, first + count)]
+        return [self.batch(k) for k in range(first, first + count)]
+
+    def sample_batch(self, k: int):
+        """A bounded slice of step k of the same workload for the CPU oracle (k = 0, 1, 2, ...)."""
+        if self.cfg == 2:
+            return W.merged_batch(k, per_table=2048)
+        if self.cfg == 3:
+            return W.jagged_batch(k, users=256)
+        if self.cfg == 4:
+            return W.large_table_batch(k, n=1 << 17)
+        if self.cfg == 5:
+            b, _ = self._sample_churn.step(self._sample_next)
+            self._sample_next += 1
             return W.single_feature(b.ids[: 1 << 16])
-        return W.single_table_batch(seed)
+        return W.single_table_batch(k)
 
     @property
     def row_bytes(self):
@@ -153,24 +173,105 @@ def measured_hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _parse_cpulist(text: str) -> set:
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        cpus.update(range(int(a), int(b or a) + 1))
+    return cpus
+
+
+def numa_cpus_for_gpu(pci_bus_id: str, sysfs: str = "/sys") -> tuple[set, str]:
+    """CPUs to run on for the GPU at `pci_bus_id`, and how they were chosen.
+
+    In order: the device's own local_cpulist; the CPUs of its numa_node; and,
+    when that node has no CPUs (a GPU-memory node) or none is given, the
+    CPU-bearing node nearest to it by the node distance table (else node 0).
+    """
+    bus = pci_bus_id.lower()
+    dom, _, rest = bus.partition(":")
+    cands = [bus, dom[-4:].zfill(4) + ":" + rest, dom.zfill(8) + ":" + rest]  # sysfs uses a 4-digit domain
+    nodes_dir = os.path.join(sysfs, "devices", "system", "node")
+
+    def node_cpus(n: int) -> set:
+        p = os.path.join(nodes_dir, f"node{n}", "cpulist")
+        return _parse_cpulist(open(p).read()) if os.path.exists(p) else set()
+
+    for cand in cands:
+        dev_dir = os.path.join(sysfs, "bus", "pci", "devices", cand)
+        p = os.path.join(dev_dir, "local_cpulist")
+        if os.path.exists(p):
+            cpus = _parse_cpulist(open(p).read())
+            if cpus:
+                return cpus, "local_cpulist"
+        p = os.path.join(dev_dir, "numa_node")
+        if os.path.exists(p):
+            node = int(open(p).read().strip())
+            if node >= 0:
+                cpus = node_cpus(node)
+                if cpus:
+                    return cpus, f"numa_node {node}"
+                dpath = os.path.join(nodes_dir, f"node{node}", "distance")
+                if os.path.exists(dpath):
+                    dist = [int(x) for x in open(dpath).read().split()]
+                    order = sorted(range(len(dist)), key=lambda k: dist[k])
+                    for k in order:
+                        cpus = node_cpus(k)
+                        if cpus:
+                            return cpus, f"node {k}, nearest CPU node to GPU node {node}"
+    cpus = node_cpus(0)
+    return cpus, "node 0 (no NUMA information for the GPU)" if cpus else "unbound"
+
+
 def bind_to_gpu_numa_node(dev_index: int) -> str:
     """Run on the CPUs next to the GPU so pinned host buffers land in its NUMA node."""
     try:
         import torch
-        bus = torch.cuda.get_device_properties(dev_index).pci_bus_id.lower()
-        for cand in (bus, "0000" + bus[4:] if len(bus) > 4 else bus):
-            path = f"/sys/bus/pci/devices/{cand}/local_cpulist"
-            if os.path.exists(path):
-                cpus = set()
-                for part in open(path).read().strip().split(","):
-                    a, _, b = part.partition("-")
-                    cpus.update(range(int(a), int(b or a) + 1))
-                if cpus:
-                    os.sched_setaffinity(0, cpus)
-                    return f"cpus {min(cpus)}-{max(cpus)}"
-    except Exception:
-        pass
+        bus = torch.cuda.get_device_properties(dev_index).pci_bus_id
+        cpus, how = numa_cpus_for_gpu(bus)
+        avail = os.sched_getaffinity(0)
+        cpus &= avail
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+            return f"cpus {min(cpus)}-{max(cpus)} ({len(cpus)}; {how})"
+    except Exception as e:  # pragma: no cover
+        return f"unbound ({type(e).__name__})"
     return "unbound"
+
+
+def source_digest() -> str:
+    """Digest of the CUDA sources: kernel counters taken from another build do not apply."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "update_merged_table_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "mt.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """(DRAM bytes per ID of `kernel`, capture note) from the committed ncu summary, or
+    (None, reason) when there is none or it was taken on other kernel sources."""
+    tpath = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
+    if not os.path.exists(tpath):
+        return None, "no committed ncu summary"
+    digest, per_id = None, {}
+    for line in open(tpath):
+        f = line.split()
+        if len(f) == 2 and f[0] == "source_digest":
+            digest = f[1]
+        elif len(f) == 2 and not line.startswith("#"):
+            per_id[f[0]] = float(f[1])
+    if digest != source_digest():
+        return None, "the committed ncu counters were taken on other kernel sources"
+    if kernel not in per_id:
+        return None, f"no counters for {kernel}"
+    return per_id[kernel], "profiles/kernel_traffic.txt"
 
 
 class ClockSampler:
@@ -238,6 +339,125 @@ def batch_stats(b):
 # our implementation
 # ---------------------------------------------------------------------------
 
+def _device_grads(torch, dev, dtype, seed: int, n: int, dim: int):
+    """N(0, 1) gradients [n, dim] drawn on the device from a seeded generator."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(500_000 + seed)
+    return torch.randn((max(n, 1), dim), generator=g, device=dev, dtype=torch.float32)[:n].to(dtype)
+
+
+def _prefill(torch, tab, wl, dev):
+    if wl.prefill_ids is not None:  # untimed: the resident key set of a steady state
+        pre = wl.prefill_ids()
+        for s0 in range(0, pre.size, 1 << 22):
+            tab.lookup(torch.from_numpy(pre[s0:s0 + (1 << 22)]).to(dev), gather=False)
+
+
+def e2e_run(args, dev, stream, tdt):
+    """The same step sequence through the public API with HOST buffers, on a table of its own: a cold
+    step, warm-up steps, then K fresh steps, each copying its IDs and gradients from pinned host memory
+    (step j + 1's copies on a copy stream while step j computes) and reading its unique count back."""
+    import torch
+    import update_merged_table_gb300 as mt
+    wl = Workload(args.config, args.users, args.log2_slots)
+    tab = mt.Table(wl.log2, wl.dim, row_dtype=wl.row, device=dev)
+    _prefill(torch, tab, wl, dev)
+    ke = min(args.steps, FRESH_CAP)
+    seq = wl.steps(0, 1 + ke)
+    (cold, _), steps = seq[0], seq[1:]
+    cold_ids = torch.from_numpy(cold.ids).to(dev)
+    cold_g = _device_grads(torch, dev, tdt[wl.grad], 0, cold.n, wl.dim)
+    for _ in range(1 + args.warmup):
+        r = tab.lookup(cold_ids, cold.feat_offsets, cold.table_ids)
+        tab.backward_adam(r, cold_g)
+    del r, cold_ids, cold_g
+    nmax = max(b.n for b, _ in steps)
+    host = []
+    for j, (b, er) in enumerate(steps):
+        ids_h = torch.from_numpy(b.ids).pin_memory()
+        g_h = torch.empty((b.n, wl.dim), dtype=tdt[wl.grad], pin_memory=True)
+        g_h.copy_(_device_grads(torch, dev, tdt[wl.grad], 1 + j, b.n, wl.dim))
+        er_h = torch.from_numpy(er.astype(np.int64)).pin_memory() if er is not None else None
+        host.append((b, ids_h, g_h, er_h))
+    slots = []
+    for _ in range(2):
+        big = tab.new_result(nmax, gather=True)
+        slots.append(dict(ids=torch.empty(nmax, dtype=torch.int64, device=dev),
+                          grads=torch.empty((nmax, wl.dim), dtype=tdt[wl.grad], device=dev),
+                          erase=torch.empty(max(1, max((h[3].numel() for h in host if h[3] is not None),
+                                                       default=1)), dtype=torch.int64, device=dev),
+                          big=big, u_h=torch.empty(1, dtype=torch.int64).pin_memory()))
+    copy_stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize(dev)
+    # the link alone: one step's copies, timed on the copy stream
+    la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0, ids0, g0, _ = host[0]
+    with torch.cuda.stream(copy_stream):
+        la.record(copy_stream)
+        slots[0]["ids"][:b0.n].copy_(ids0, non_blocking=True)
+        slots[0]["grads"][:b0.n].copy_(g0, non_blocking=True)
+        lb.record(copy_stream)
+    torch.cuda.synchronize(dev)
+    link_gbs = (ids0.numel() * 8 + g0.numel() * g0.element_size()) / (la.elapsed_time(lb) / 1e3) / 1e9
+
+    used = [None, None]
+    landed = [None, None]
+
+    def issue_copy(j):
+        k = j % 2
+        b, ids_h, g_h, er_h = host[j]
+        with torch.cuda.stream(copy_stream):
+            if used[k] is not None:
+                copy_stream.wait_event(used[k])
+            slots[k]["ids"][:b.n].copy_(ids_h, non_blocking=True)
+            slots[k]["grads"][:b.n].copy_(g_h, non_blocking=True)
+            if er_h is not None:
+                slots[k]["erase"][:er_h.numel()].copy_(er_h, non_blocking=True)
+            landed[k] = torch.cuda.Event()
+            landed[k].record(copy_stream)
+
+    h2d = d2h = ids_done = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_event(e0)
+    issue_copy(0)
+    for j in range(ke):
+        if j + 1 < ke:
+            issue_copy(j + 1)
+        k = j % 2
+        b, ids_h, g_h, er_h = host[j]
+        stream.wait_event(landed[k])
+        s = slots[k]
+        big = s["big"]
+        res = mt.LookupResult(big.unique_keys[:b.n], big.inverse[:b.n], big.counts[:b.n], big.unique_rows[:b.n],
+                              big.num_unique, big.rows[:b.n], b.n, big.ranks[:b.n])
+        tab.lookup(s["ids"][:b.n], b.feat_offsets, b.table_ids, result=res)
+        tab.backward_adam(res, s["grads"][:b.n])
+        if er_h is not None:
+            tab.erase(s["erase"][:er_h.numel()], want_found=False)
+        s["u_h"].copy_(res.num_unique, non_blocking=True)
+        used[k] = torch.cuda.Event()
+        used[k].record(stream)
+        h2d += ids_h.numel() * 8 + g_h.numel() * g_h.element_size() + (er_h.numel() * 8 if er_h is not None else 0)
+        d2h += 8
+        ids_done += b.n
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    secs = e0.elapsed_time(e1) / 1e3
+    if tab.error() != 0:
+        raise RuntimeError(f"device error {tab.error()} in the end-to-end run")
+    tot, mx = aggregate(float(ids_done), secs)
+    out = {"value": tot / mx, "unit": UNIT, "h2d_bytes_per_step": h2d // ke, "d2h_bytes_per_step": d2h // ke,
+           "steps": ke, "h2d_GB/s_effective": h2d / secs / 1e9, "h2d_GB/s_link": link_gbs,
+           "what": "mt_lookup + mt_backward_adam through the Python binding, inputs copied from pinned host "
+                   "memory inside the timed region; the unique count read back each step; a table of its own "
+                   "running the same cold, warm-up and fresh steps"}
+    del tab, host, slots
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import update_merged_table_gb300 as mt
@@ -255,44 +475,47 @@ def run_ours(args):
     mt.load_library()
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+    # -------- end to end through the public API with host buffers (its own table, before any capture) ----
+    e2e = e2e_run(args, dev, stream, tdt) if args.e2e else None
 
     wl = Workload(args.config, args.users, args.log2_slots)
-    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
     tab = mt.Table(wl.log2, wl.dim, row_dtype=wl.row, device=dev)
-    if wl.prefill_ids is not None:  # untimed: the resident key set of a steady state
-        pre = wl.prefill_ids()
-        for s0 in range(0, pre.size, 1 << 22):
-            tab.lookup(torch.from_numpy(pre[s0:s0 + (1 << 22)]).to(dev), gather=False)
-        del pre
+    _prefill(torch, tab, wl, dev)
     B, G = wl.row_bytes, wl.grad_bytes
+    K = args.steps
+    kf = min(K, FRESH_CAP)
+    nprof = min(K, 8)
+    seq = wl.steps(0, 1 + kf + nprof)  # cold step 0, the timed fresh steps, then the profiling steps
+    (cold, _), timed, prof_steps = seq[0], seq[1:1 + kf], seq[1 + kf:]
 
-    pool = []
-    for k in range(args.pool):
-        b, er = wl.batch(1 + k + 1000 * rank)
+    def entry(j, b, er):
         U, H, NH = batch_stats(b)
-        g = torch.from_numpy(W.grads_normal(1 + k + 500_000 + 1000 * rank, b.n, wl.dim)).to(tdt[wl.grad])
-        e = dict(batch=b, grads=g, U=U, H=H, NH=NH, erase=None)
+        e = dict(batch=b, U=U, H=H, NH=NH, erase=None, n_erase=0)
         e["ids_d"] = torch.from_numpy(b.ids).to(dev)
-        e["grads_d"] = g.to(dev)
+        e["grads_d"] = _device_grads(torch, dev, tdt[wl.grad], j, b.n, wl.dim)
         e["res"] = tab.new_result(b.n, gather=True)
         if er is not None:
             e["erase"] = torch.from_numpy(er.astype(np.int64)).to(dev)
-        e["ids_h"] = torch.from_numpy(b.ids).pin_memory()
-        e["grads_h"] = g.pin_memory()
-        e["u_h"] = torch.empty(1, dtype=torch.int64).pin_memory()
-        pool.append(e)
+            e["n_erase"] = er.size
+        return e
 
-    def step(e):
+    pool = [entry(1 + j, b, er) for j, (b, er) in enumerate(timed)]
+    prof_pool = [entry(1 + kf + j, b, er) for j, (b, er) in enumerate(prof_steps)]
+
+    def fwd_call(e):
         b = e["batch"]
         tab.lookup(e["ids_d"], b.feat_offsets, b.table_ids, result=e["res"])
+
+    def bwd_call(e):
         tab.backward_adam(e["res"], e["grads_d"])
         if e["erase"] is not None:
             tab.erase(e["erase"], want_found=False)
 
-    # the cold step (a batch on the table as prefilled; for the jagged workload every key is new) -- untimed
-    cold, _ = wl.batch(1000 * rank + 999)
+    # the cold step (seed 0; on an empty table every key is new) -- timed on its own, untimed in the run
     cold_ids = torch.from_numpy(cold.ids).to(dev)
-    cold_g = torch.from_numpy(W.grads_normal(7, cold.n, wl.dim)).to(tdt[wl.grad]).to(dev)
+    cold_g = _device_grads(torch, dev, tdt[wl.grad], 0, cold.n, wl.dim)
     live_before = int(tab.stats()["live"])
     torch.cuda.synchronize(dev)
     c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -303,84 +526,47 @@ def run_ours(args):
     c2.record(stream)
     torch.cuda.synchronize(dev)
     cold_stats = {"ids": cold.n, "new_keys": int(tab.stats()["live"]) - live_before, "lookup_ms": c0.elapsed_time(c1),
-                  "backward_ms": c1.elapsed_time(c2), "note": "first step after set-up, includes lazy set-up"}
+                  "backward_ms": c1.elapsed_time(c2), "note": "step 0, the first call: includes lazy set-up"}
+    # warm-up: the cold batch again (its keys are resident now; no erase)
+    for _ in range(args.warmup):
+        cres = tab.lookup(cold_ids, cold.feat_offsets, cold.table_ids, result=cres)
+        tab.backward_adam(cres, cold_g)
+    torch.cuda.synchronize(dev)
     del cres, cold_ids, cold_g
-    for j in range(args.warmup):
-        step(pool[j % len(pool)])
-    torch.cuda.synchronize(dev)
-
-    # -------- end to end through the public API with host buffers --------
-    # (measured before any graph is captured: the eager API is what a caller
-    # feeding host buffers uses)
-    # Every step copies its IDs and gradients from pinned host memory and reads
-    # its unique count back; the copies of step j + 1 run on a copy stream
-    # while step j computes (the pool entry's device buffers are rewritten only
-    # after the step that last used them has finished).
-    e2e_steps = min(args.steps, 4 * len(pool))
-    h2d = d2h = 0
-    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ids = 0
-    copy_stream = torch.cuda.Stream(device=dev)
-    P = len(pool)
-    used = [None] * P    # event after the step that last used entry k's device buffers
-    landed = [None] * P  # event after entry k's inputs reached the device
-
-    def issue_copy(j):
-        k = j % P
-        e = pool[k]
-        with torch.cuda.stream(copy_stream):
-            if used[k] is not None:
-                copy_stream.wait_event(used[k])
-            e["ids_d"].copy_(e["ids_h"], non_blocking=True)
-            e["grads_d"].copy_(e["grads_h"], non_blocking=True)
-            landed[k] = torch.cuda.Event()
-            landed[k].record(copy_stream)
-
-    torch.cuda.synchronize(dev)
-    ev2.record(stream)
-    copy_stream.wait_event(ev2)
-    issue_copy(0)
-    for j in range(e2e_steps):
-        if j + 1 < e2e_steps:
-            issue_copy(j + 1)
-        k = j % P
-        e = pool[k]
-        stream.wait_event(landed[k])
-        step(e)
-        e["u_h"].copy_(e["res"].num_unique, non_blocking=True)
-        used[k] = torch.cuda.Event()
-        used[k].record(stream)
-        h2d += e["ids_h"].numel() * 8 + e["grads_h"].numel() * e["grads_h"].element_size()
-        d2h += 8
-        e2e_ids += e["batch"].n
-    ev3.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_secs = ev2.elapsed_time(ev3) / 1e3
-    e2e_tot, e2e_max = aggregate(float(e2e_ids), e2e_secs)
 
     graphs = None
     launches_per_step = None
     if args.graph:
         graphs = []
-        c0 = mt.kernel_launches()
+        l0 = mt.kernel_launches()
         for e in pool:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                step(e)
-            graphs.append(g)
+            gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gf, stream=stream):
+                fwd_call(e)
+            with torch.cuda.graph(gb, stream=stream):
+                bwd_call(e)
+            graphs.append((gf, gb))
         torch.cuda.synchronize(dev)
-        launches_per_step = (mt.kernel_launches() - c0) / len(pool)
+        launches_per_step = (mt.kernel_launches() - l0) / len(pool)
 
-        def run(j):
-            graphs[j % len(pool)].replay()
-    else:
-        def run(j):
-            step(pool[j % len(pool)])
+    def run_fwd(j):
+        if graphs is not None:
+            graphs[j % kf][0].replay()
+        else:
+            fwd_call(pool[j % kf])
 
-    # -------- timed region: K steps, inputs resident in HBM --------
-    live0 = tab.stats()["live"]
-    n_ids = sum(pool[j % len(pool)]["batch"].n for j in range(args.steps))
+    def run_bwd(j):
+        if graphs is not None:
+            graphs[j % kf][1].replay()
+        else:
+            bwd_call(pool[j % kf])
+
+    # -------- timed region: K steps on fresh batches, inputs resident in HBM --------
+    st0 = tab.stats()
+    n_ids = sum(pool[j % kf]["batch"].n for j in range(K))
     launches0 = mt.kernel_launches()
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         import torch.distributed as dist
@@ -388,103 +574,66 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index) as clk:
         ev0.record(stream)
-        for j in range(args.steps):
-            run(j)
+        for j in range(K):
+            ev_a[j].record(stream)
+            run_fwd(j)
+            ev_m[j].record(stream)
+            run_bwd(j)
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
     secs = ev0.elapsed_time(ev1) / 1e3
+    fwd_ms = sum(ev_a[j].elapsed_time(ev_m[j]) for j in range(K))
+    bwd_ms = sum(ev_m[j].elapsed_time(ev_a[j + 1] if j + 1 < K else ev1) for j in range(K))
     launches = mt.kernel_launches() - launches0
     if launches_per_step is not None:  # graph replays launch the captured kernels
-        launches = int(round(launches_per_step * args.steps))
-    live1 = tab.stats()["live"]
+        launches = int(round(launches_per_step * K))
+    st1 = tab.stats()
+    erased = sum(pool[j % kf]["n_erase"] for j in range(K))  # every erase key of the stream is live
+    n_new_per_step = max(0.0, (st1["live"] - st0["live"] + erased) / K)
     tot_ids, tot_secs = aggregate(float(n_ids), secs)
 
-    # -------- per-direction and per-kernel device times (separate pass) --------
-    # The lookup and the backward are timed the way the step runs: as CUDA
-    # graph replays when the step is replayed from a graph, else eagerly.
-    def fwd_call(e):
-        tab.lookup(e["ids_d"], e["batch"].feat_offsets, e["batch"].table_ids, result=e["res"])
-
-    def bwd_call(e):
-        tab.backward_adam(e["res"], e["grads_d"])
-
-    if args.graph:
-        dir_graphs = []
-        for e in pool:
-            gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gf, stream=stream):
-                fwd_call(e)
-            with torch.cuda.graph(gb, stream=stream):
-                bwd_call(e)
-            dir_graphs.append((gf, gb))
-        torch.cuda.synchronize(dev)
-    fwd_ms = bwd_ms = 0.0
-    npass = min(args.steps, 4 * len(pool))
-    pass_ids = pass_U = pass_H = pass_NH = 0
-    evs = []
-    for j in range(npass):
-        e = pool[j % len(pool)]
-        a, m_, z = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        a.record(stream)
-        if args.graph:
-            dir_graphs[j % len(pool)][0].replay()
-        else:
-            fwd_call(e)
-        m_.record(stream)
-        if args.graph:
-            dir_graphs[j % len(pool)][1].replay()
-        else:
-            bwd_call(e)
-        z.record(stream)
-        if e["erase"] is not None:
-            tab.erase(e["erase"], want_found=False)
-        evs.append((a, m_, z))
-        pass_ids += e["batch"].n
-        pass_U += e["U"]
-        pass_H += e["H"]
-        pass_NH += e["NH"]
-    torch.cuda.synchronize(dev)
-    for a, m_, z in evs:
-        fwd_ms += a.elapsed_time(m_)
-        bwd_ms += m_.elapsed_time(z)
+    # -------- per-kernel device times: an eager pass over further fresh steps --------
     mt.profile_enable(True)
     mt.profile_report(reset=True)
-    for j in range(npass):
-        step(pool[j % len(pool)])
+    pst0 = tab.stats()
+    for e in prof_pool:
+        fwd_call(e)
+        bwd_call(e)
     torch.cuda.synchronize(dev)
     prof = mt.profile_report(reset=True)
     mt.profile_enable(False)
+    pst1 = tab.stats()
+    p_erased = sum(e["n_erase"] for e in prof_pool)
+    p_new = max(0.0, (pst1["live"] - pst0["live"] + p_erased) / len(prof_pool))
 
-    # algorithmic bytes (new keys counted from the live-key growth of the timed steps)
-    n_new_per_step = max(0.0, (live1 - live0) / max(1, args.steps))
-    N_avg = pass_ids / npass
-    U_avg = pass_U / npass
-    H_avg, NH_avg = pass_H / npass, pass_NH / npass
+    # algorithmic bytes per step (the timed steps' own batches; new keys from the table's growth)
+    def mean(key, entries):
+        return sum(e[key] for e in entries) / len(entries)
+
+    N_avg = sum(pool[j % kf]["batch"].n for j in range(K)) / K
+    U_avg = sum(pool[j % kf]["U"] for j in range(K)) / K
     fwd_bytes = (8 * N_avg + 4 * N_avg + U_avg * (8 + 16) + U_avg * B + N_avg * B
                  + n_new_per_step * (16 + B + 8 * wl.dim))
     bwd_bytes = N_avg * G + 4 * N_avg + U_avg * (4 + 2 * B + 16 * wl.dim)
     row_rw = 2 * B + 16 * wl.dim  # emb, m, v read and written
+    pN = sum(e["batch"].n for e in prof_pool) / len(prof_pool)
+    pU, pH, pNH = mean("U", prof_pool), mean("H", prof_pool), mean("NH", prof_pool)
     kernel_bytes = {  # algorithmic bytes per launch of the kernels that move the bulk
-        "k_bw_heavy_reduce": NH_avg * (G + 4) + H_avg * row_rw,
-        "k_bw_light_reduce": (N_avg - NH_avg) * (G + 4) + (U_avg - H_avg) * (row_rw + 16),
-        "k_gather": N_avg * B + U_avg * B + 4 * N_avg,
+        "k_bw_heavy_reduce": pNH * (G + 4) + pH * row_rw,
+        "k_bw_light_reduce": (pN - pNH) * (G + 4) + (pU - pH) * (row_rw + 16),
+        "k_gather": pN * B + pU * B + 4 * pN,
     }
     peak, peak_kind = measured_hbm_peak()
     tot_k = sum(v[1] for v in prof.values()) or 1.0
     dom = max((k for k in prof if k in kernel_bytes), key=lambda k: prof[k][1])
     dom_ms = prof[dom][1] / prof[dom][0]
     achieved = kernel_bytes[dom] / (dom_ms / 1e3) / 1e9
-    traffic = None  # DRAM bytes per launch from the committed ncu summary, scaled by the IDs of a launch
-    tpath = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
-    if args.config == 3 and os.path.exists(tpath):
-        for line in open(tpath):
-            f = line.split()
-            if len(f) == 2 and f[0] == dom:
-                traffic = float(f[1]) * N_avg
+    per_id, traffic_note = committed_traffic(dom) if args.config == 3 else (None, "counters cover the jagged workload")
+    traffic = per_id * pN if per_id is not None else None
 
-    # -------- tombstone compaction of the key store (one call, untimed in the step) --------
+    # -------- tombstone compaction of the key store (one call, outside the step) --------
     comp = None
     if ws == 1:
         st_before = tab.stats()
@@ -499,45 +648,51 @@ def run_ours(args):
         M = 1 << wl.log2
         comp = {"ms": c_ms, "slots": M, "live": int(st_before["live"]),
                 "algorithmic_GB/s": 32.0 * M / (c_ms / 1e3) / 1e9,  # read every old slot, write every new one
-                "moved_GB/s": 80.0 * M / (c_ms / 1e3) / 1e9,  # + clear the fresh array, copy it back
                 "note": "mt_compact: live keys re-inserted into a fresh slot array that replaces the table's"}
 
     err = tab.error()
     if err != 0:
         raise RuntimeError(f"device error {err} during the benchmark")
 
+    fwd_s, bwd_s = fwd_ms / K / 1e3, bwd_ms / K / 1e3
     line = {
-        "metric": METRIC, "value": tot_ids / tot_secs, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * tot_secs / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": tot_ids / tot_secs, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": 1e3 * tot_secs / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.row, "data": "synthetic",
         "config": {"workload": wl.name, "ids_per_step": N_avg, "unique_per_step": U_avg,
-                   "new_keys_per_step": n_new_per_step, "batch_pool": len(pool), "cuda_graph": bool(args.graph),
+                   "new_keys_per_step": n_new_per_step, "fresh_steps": kf,
+                   "steps_cycle_fresh_batches": K > kf,
+                   "step_sequence": (f"cold step 0 (seed 0) untimed, {args.warmup} warm-up steps on it, then timed "
+                                     f"steps 1..{K} on fresh seeds" + (f" (cycling {kf} batches)" if K > kf else "")),
+                   "cuda_graph": bool(args.graph),
                    "l2": ("inputs larger than L2 (ids+grads+out ~0.5 GB per step), no flush" if args.config == 3
-                          else "batch pool cycled; see the workload's sizes"),
+                          else "fresh batches every step; see the workload's sizes"),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "host_binding": numa,
-                   "direction_timing": "graph replays" if args.graph else "eager"},
-        "fwd_ids_per_s": pass_ids / (fwd_ms / 1e3), "bwd_ids_per_s": pass_ids / (bwd_ms / 1e3),
+                   "direction_timing": "CUDA events between the lookup and backward graph replays of each step"},
+        "fwd_ids_per_s": N_avg / fwd_s, "bwd_ids_per_s": N_avg / bwd_s,
+        "roofline_fwd": {"bytes_per_step": fwd_bytes, "ms_per_step": fwd_s * 1e3, "achieved": fwd_bytes / fwd_s / 1e9,
+                         "peak": peak, "unit": "GB/s", "frac": fwd_bytes / fwd_s / 1e9 / peak},
+        "roofline_bwd": {"bytes_per_step": bwd_bytes, "ms_per_step": bwd_s * 1e3, "achieved": bwd_bytes / bwd_s / 1e9,
+                         "peak": peak, "unit": "GB/s", "frac": bwd_bytes / bwd_s / 1e9 / peak},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
+                     "traffic_source": traffic_note,
+                     "algorithmic_bytes_per_launch": kernel_bytes[dom], "avg_launch_ms": dom_ms,
+                     "time_share": prof[dom][1] / tot_k},
         "kernel_rooflines": {k: {"GB/s": kernel_bytes[k] / (prof[k][1] / prof[k][0] / 1e3) / 1e9,
                                  "frac": kernel_bytes[k] / (prof[k][1] / prof[k][0] / 1e3) / 1e9 / peak}
                              for k in kernel_bytes if k in prof},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": kernel_bytes[dom], "avg_launch_ms": dom_ms,
-                     "time_share": prof[dom][1] / tot_k},
-        "roofline_fwd": {"bytes_per_step": fwd_bytes, "achieved": fwd_bytes / (fwd_ms / npass / 1e3) / 1e9,
-                         "frac": fwd_bytes / (fwd_ms / npass / 1e3) / 1e9 / peak},
-        "roofline_bwd": {"bytes_per_step": bwd_bytes, "achieved": bwd_bytes / (bwd_ms / npass / 1e3) / 1e9,
-                         "frac": bwd_bytes / (bwd_ms / npass / 1e3) / 1e9 / peak},
         "kernels": {k: {"launches": v[0], "avg_us": 1e3 * v[1] / v[0], "share": v[1] / tot_k} for k, v in prof.items()},
+        "kernel_pass": f"eager, CUDA events around each launch, {len(prof_pool)} further fresh steps "
+                       f"({p_new:.0f} new keys per step)",
         "cold_step": cold_stats,
         "compaction": comp,
-        "e2e": {"value": e2e_tot / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d // e2e_steps,
-                "d2h_bytes_per_step": d2h // e2e_steps},
+        "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(Workload(args.config, args.users, args.log2_slots), args.cpu_seconds)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -633,11 +788,11 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--pool", type=int, default=8, help="distinct pre-generated batches cycled through")
+    ap.add_argument("--e2e", type=int, default=1, help="also time the step through host buffers (its own table)")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=150.0,

@@ -50,3 +50,51 @@ def test_row_and_grad_bytes():
     assert wl.row_bytes == 128 and wl.grad_bytes == 128
     wl4 = bench.Workload(4)
     assert wl4.row_bytes == 512 and wl4.grad_bytes == 512
+
+
+def test_churn_steps_are_sequential():
+    wl = bench.Workload(5)
+    wl.churn = bench.W.ChurnStream(0, hot=1 << 12, n=1 << 10, erase=1 << 8)
+    a = wl.steps(0, 2)
+    b = wl.steps(2, 1)
+    assert len(a) == 2 and len(b) == 1 and all(er is not None and er.size == 1 << 8 for _, er in a + b)
+    with pytest.raises(ValueError):
+        wl.steps(7, 1)
+    with pytest.raises(ValueError):
+        wl.batch(1)
+
+
+def _fake_sysfs(tmp_path, bus, local=None, node=None, nodes=None, distance=None):
+    d = tmp_path / "bus" / "pci" / "devices" / bus
+    d.mkdir(parents=True)
+    if local is not None:
+        (d / "local_cpulist").write_text(local + "\n")
+    if node is not None:
+        (d / "numa_node").write_text(f"{node}\n")
+    for k, cpus in (nodes or {}).items():
+        nd = tmp_path / "devices" / "system" / "node" / f"node{k}"
+        nd.mkdir(parents=True)
+        (nd / "cpulist").write_text(cpus + "\n")
+        if distance and k in distance:
+            (nd / "distance").write_text(" ".join(map(str, distance[k])) + "\n")
+    return str(tmp_path)
+
+
+def test_numa_binding_prefers_local_cpulist(tmp_path):
+    root = _fake_sysfs(tmp_path, "0000:01:00.0", local="0-3,8")
+    cpus, how = bench.numa_cpus_for_gpu("00000000:01:00.0", root)
+    assert cpus == {0, 1, 2, 3, 8} and how == "local_cpulist"
+
+
+def test_numa_binding_from_numa_node(tmp_path):
+    root = _fake_sysfs(tmp_path, "0009:01:00.0", node=1, nodes={0: "0-71", 1: "72-143"})
+    cpus, how = bench.numa_cpus_for_gpu("0009:01:00.0", root)
+    assert cpus == set(range(72, 144)) and how == "numa_node 1"
+
+
+def test_numa_binding_gpu_memory_node_takes_nearest_cpu_node(tmp_path):
+    # the GPU's node holds memory only (no CPUs): the CPU node at the smallest distance is chosen
+    root = _fake_sysfs(tmp_path, "0009:01:00.0", node=4, nodes={0: "0-71", 1: "72-143", 4: ""},
+                       distance={4: [80, 40, 80, 80, 10]})
+    cpus, how = bench.numa_cpus_for_gpu("0009:01:00.0", root)
+    assert cpus == set(range(72, 144)) and "nearest" in how
