@@ -37,7 +37,7 @@
 extern "C" {
 #endif
 
-#define MT_ABI_VERSION 1
+#define MT_ABI_VERSION 2
 
 /* Status codes. */
 enum {
@@ -47,8 +47,7 @@ enum {
   MT_EFULL = -3,    /* device: probe limit reached or row pool exhausted */
   MT_EKEY = -4,     /* device: an ID outside [0, 2^56) */
   MT_ECUDA = -5,    /* a CUDA runtime call failed */
-  MT_ETOOBIG = -6,  /* batch larger than a fixed-size entry point allows (mt_lookup_static) */
-  MT_ETIMEOUT = -7  /* device: a bounded wait inside a kernel gave up; that call's results are invalid */
+  MT_ETOOBIG = -6   /* batch larger than a fixed-size entry point allows (mt_lookup_static) */
 };
 
 /* Element types of rows and gradients. */
@@ -61,12 +60,6 @@ enum { MT_F32 = 0, MT_BF16 = 1 };
 #define MT_KEY_TOMBSTONE 0xFFFFFFFFFFFFFFFEull
 #define MT_MAX_FEATURES 256
 
-/* Testing only: on a table created with this flag, the first tile of every
- * lookup never publishes its owner count, so the other tiles' bounded waits
- * in the owner-count scan run out (after ~2^22 polls, a few seconds): the
- * lookup latches MT_ETIMEOUT and leaves every index in bounds, and the CUDA
- * context stays usable.  It exercises the timeout path without a GPU fault. */
-#define MT_FLAG_TEST_STALL_SCAN 0x80000000u
 #define MT_MAX_DIM 1024
 #define MT_HIST_BINS 64
 
@@ -98,7 +91,7 @@ typedef struct {
   uint64_t hash_seed;
   uint64_t init_seed;
   float init_scale;
-  uint32_t flags; /* 0, or MT_FLAG_TEST_STALL_SCAN (testing only) */
+  uint32_t flags; /* must be 0 (reserved) */
   int64_t num_rows;
 } mt_config;
 

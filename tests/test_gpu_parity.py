@@ -272,27 +272,6 @@ def test_probe_limit_latches_full_without_hang():
     assert np.array_equal(again.unique_rows[:64].cpu().numpy()[placed], rows[placed])
 
 
-def test_scan_wait_runs_out_and_reports_timeout():
-    """A table created with MT_FLAG_TEST_STALL_SCAN: the first tile never
-    publishes its owner count, so the other tiles' bounded waits run out.  The
-    lookup latches MT_ETIMEOUT and keeps every index in bounds, and the
-    device stays usable (a flag that nothing sets; no fault, no hang)."""
-    n = 4 * 2048
-    ids = np.arange(n, dtype=np.int64) % 3000
-    b = W.single_feature(ids)
-    tab = mt.Table(14, 4, flags=mt.MT_FLAG_TEST_STALL_SCAN)
-    res = tab.lookup(to_dev(b.ids))
-    torch.cuda.synchronize()
-    assert tab.error() == mt.MT_ETIMEOUT
-    assert 0 <= res.U <= n
-    inv = res.inverse[:n].cpu().numpy()
-    assert inv.min() >= -1 and inv.max() < n
-    tab2 = mt.Table(14, 4)  # the context still works, and gives the exact result
-    res2 = tab2.lookup(to_dev(b.ids))
-    assert res2.U == 3000 and tab2.error() == 0
-    assert np.array_equal(res2.inverse[:n].cpu().numpy(), ids.astype(np.int32))
-
-
 def test_erase_duplicates_and_reinsert():
     tab = mt.Table(10, 16, init_seed=3)
     ref = oracle.Table(10, 16, init_seed=3)

@@ -23,8 +23,8 @@ import numpy as np
 __all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "KEY_EMPTY", "KEY_TOMBSTONE",
            "ABI_FUNCTIONS", "profile_enable", "profile_report", "kernel_launches"]
 
-MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA, MT_ETOOBIG, MT_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
-MT_FLAG_TEST_STALL_SCAN = 0x80000000  # testing only (see include/mt.h)
+MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA, MT_ETOOBIG = 0, -1, -2, -3, -4, -5, -6
+ABI_VERSION = 2
 LOOKUP_STATIC_MAX_IDS = 65536
 MT_F32, MT_BF16 = 0, 1
 KEY_EMPTY = (1 << 64) - 1
@@ -139,7 +139,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         fn = getattr(L, name)
         fn.restype = res
         fn.argtypes = args
-    if L.mt_abi_version() != 1:
+    if L.mt_abi_version() != ABI_VERSION:
         raise RuntimeError("libmt.so ABI version mismatch")
     if path is None:
         _lib = L

@@ -25,7 +25,7 @@ int normalise(const mt_config* in, mt_config* out) {
   if (in == nullptr) return MT_EINVAL;
   mt_config c = *in;
   if (c.log2_slots < 1 || c.log2_slots > 31) return MT_EINVAL;
-  if ((c.flags & ~MT_FLAG_TEST_STALL_SCAN) != 0) return MT_EINVAL;
+  if (c.flags != 0) return MT_EINVAL;
   if (c.row_dtype != MT_F32 && c.row_dtype != MT_BF16) return MT_EINVAL;
   const uint32_t vec = c.row_dtype == MT_F32 ? 4 : 8;
   if (c.dim < 4 || c.dim > MT_MAX_DIM || c.dim % vec != 0) return MT_EINVAL;
@@ -126,7 +126,6 @@ const char* mt_strerror(int code) {
     case MT_EKEY: return "ID outside [0, 2^56)";
     case MT_ECUDA: return "CUDA runtime error";
     case MT_ETOOBIG: return "batch larger than the fixed-size workspace allows";
-    case MT_ETIMEOUT: return "a bounded wait inside a kernel gave up";
     default: return "unknown status";
   }
 }
@@ -249,16 +248,17 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
   p.num_unique = reinterpret_cast<long long*>(res->num_unique);
   p.ranks = res->ranks;
   if (n > 0) {
-    p.sc_key = reinterpret_cast<unsigned long long*>(w + L.sc_key);
-    p.sc_minpos = reinterpret_cast<uint32_t*>(w + L.sc_minpos);
-    p.sc_uidx = reinterpret_cast<int32_t*>(w + L.sc_uidx);
+    p.sc = reinterpret_cast<mt::ScSlot*>(w + L.sc);
+    p.ss = L.ss;
+    p.ulist_n = reinterpret_cast<uint32_t*>(w + L.ulist_n);
+    p.ulist = reinterpret_cast<int32_t*>(w + L.ulist);
     p.sc_row = reinterpret_cast<int32_t*>(w + L.sc_row);
-    p.scratch_mask = L.scratch_slots - 1;
     p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
-    p.tile_status = reinterpret_cast<unsigned long long*>(w + L.tile_status);
-    p.ticket = reinterpret_cast<int32_t*>(w + L.ticket);
-    p.lfirst = reinterpret_cast<uint32_t*>(w + L.lfirst);
-    p.lsslot = reinterpret_cast<uint32_t*>(w + L.lsslot);
+    p.tile_O = reinterpret_cast<int32_t*>(w + L.tile_O);
+    p.tile_pre = reinterpret_cast<int32_t*>(w + L.tile_pre);
+    p.done = reinterpret_cast<uint32_t*>(w + L.done);
+    p.first_slot = reinterpret_cast<int32_t*>(w + L.first_slot);
+    p.lsslot = reinterpret_cast<int32_t*>(w + L.lsslot);
     p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
     p.ntiles = L.ntiles;
   }

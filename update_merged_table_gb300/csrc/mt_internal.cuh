@@ -63,7 +63,7 @@ struct TableDev {
   uint32_t rec_bytes;            // bytes per row record
   uint32_t emb_bytes;            // d x row element bytes
   uint32_t mv_bytes;             // d x 4
-  uint32_t flags;                // mt_config flags (MT_FLAG_TEST_STALL_SCAN)
+  uint32_t flags;                // mt_config flags (reserved, 0)
   int row_dtype;
   float init_scale;
   long long num_rows;

@@ -9,13 +9,26 @@ namespace mt {
 // ---- forward ----------------------------------------------------------------
 
 constexpr int kTile = 2048;              // positions per lookup tile (one CTA)
-constexpr int kThreads = 256;            // threads per lookup CTA
+constexpr int kThreads = 256;            // threads per lookup CTA (number, expand)
 constexpr int kPPT = kTile / kThreads;   // positions per thread
-constexpr int kThreadsA = 512;           // threads per dedup CTA (k_dedup_claim)
-constexpr int kPPTA = kTile / kThreadsA; // positions per dedup thread
+constexpr int kThreadsA = 512;           // threads per claim CTA (k_claim)
+constexpr int kPPTA = kTile / kThreadsA; // positions per claim thread
 constexpr int kHS = 2 * kTile;           // shared-memory hash slots (backward fill)
 constexpr int kHSA = 3 * kTile / 2;      // shared-memory hash slots of stage 1 (load <= 2/3)
+constexpr int kThreadsR = 256;           // threads per resolve CTA (k_resolve)
 constexpr uint16_t kNoIdx = 0xFFFF;
+
+// One slot of the stage-2 scratch hash.  The lookup clears the slots to all
+// ones, so a fresh slot holds key EMPTY, first = "none" and cnt = 2^32 - 1,
+// i.e. cnt stores (positions - 1): an atomicAdd of c returns (positions
+// added before) - 1.  After numbering, `first` is overwritten with the key's
+// unique index.
+struct __align__(16) ScSlot {
+  unsigned long long key;
+  uint32_t first;  // smallest position holding the key (atomicMin), then its unique index
+  uint32_t cnt;    // positions holding the key, minus one
+};
+static_assert(sizeof(ScSlot) == 16, "scratch slot is 16 bytes");
 
 struct LookupParams {
   TableDev T;
@@ -32,26 +45,27 @@ struct LookupParams {
   int32_t* unique_rows;
   long long* num_unique;
   int32_t* ranks;         // nullable
-  // workspace
-  // stage-2 global scratch hash, one array per field (keys and first
-  // positions start all-ones; unique indices are written before they are read)
-  unsigned long long* sc_key;
-  uint32_t* sc_minpos;
-  int32_t* sc_uidx;
-  int32_t* sc_row;        // table row of the key, written by its claimer (-1: absent)
-  unsigned long long scratch_mask;
-  int32_t* tile_L;        // [ntiles] local uniques per tile
-  unsigned long long* tile_status;  // [ntiles] owner-count scan: flag << 32 | count (cleared by k_dedup_claim)
-  int32_t* ticket;        // tiles handed to k_assign_resolve blocks in start order
-  uint32_t* lfirst;       // [ntiles * kTile] first global position of local unique l
-  uint32_t* lsslot;       // [ntiles * kTile] its scratch slot
-  uint16_t* lidx;         // [ntiles * kTile] local unique index of each position
+  // workspace (the scratch slots and the distinct-key counter are cleared to all ones per call)
+  ScSlot* sc;             // [ss] stage-2 scratch hash
+  unsigned long long ss;  // scratch slots (>= n + 1; not a power of two)
+  uint32_t* ulist_n;      // distinct keys listed so far, minus one
+  int32_t* ulist;         // [n] scratch slot of each distinct key, in claim order
+  int32_t* sc_row;        // [ss] table row of the key in a slot (-1: none)
+  int32_t* tile_L;        // [ntiles] tile-local uniques per tile
+  int32_t* tile_O;        // [ntiles] distinct keys whose first position lies in the tile (zeroed by k_claim)
+  int32_t* tile_pre;      // [ntiles + 1] exclusive prefix of tile_O (written by the last k_resolve block)
+  uint32_t* done;         // k_resolve blocks finished (zeroed by k_claim)
+  int32_t* first_slot;    // [ntiles * kTile] scratch slot of the key first seen at each position, else -1
+  int32_t* lsslot;        // [ntiles * kTile] scratch slot of each tile-local unique
+  uint16_t* lidx;         // [ntiles * kTile] tile-local unique of each position
   int ntiles;
+  int resolve_grid;
 };
 
 struct LookupWsLayout {
-  size_t sc_key, sc_minpos, sc_uidx, sc_row, tile_L, tile_status, ticket, lfirst, lsslot, lidx, total;
-  unsigned long long scratch_slots;
+  size_t sc, ulist_n, ulist, sc_row, tile_L, tile_O, tile_pre, done, first_slot, lsslot, lidx, total;
+  size_t clear_bytes;  // bytes from the start of the workspace cleared to all ones per call
+  unsigned long long ss;
   int ntiles;
 };
 LookupWsLayout lookup_ws_layout(long long n);

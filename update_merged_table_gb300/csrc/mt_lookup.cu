@@ -4,29 +4,35 @@
 //
 // Pages: "MTGenRec" TL;DR and abstract (a dynamic embedding table built on
 // hashing, feature tables merged into one, deduplication of IDs in two
-// stages to speed up lookups, keys inserted while training runs); Theorem 1 (probe sequence h_t = (h0 + t*S) mod 2^n
-// with S odd covers the table); "MTGR" section 5, Embedding Lookup (IDs stay
-// unique).
+// stages to speed up lookups, keys inserted while training runs); Theorem 1
+// (probe sequence h_t = (h0 + t*S) mod 2^n with S odd covers the table);
+// "MTGR" section 5, Embedding Lookup (no duplicate IDs on either side of an
+// exchange).
 //
-// Kernels, in launch order (one CTA per tile of kTile consecutive positions):
-//  k_dedup_claim     encode keys; stage 1: dedup inside the tile with a
-//                    shared-memory hash (CAS insert, atomicMin of the first
-//                    position); stage 2: each tile-local unique claims its
-//                    key in a global scratch hash and lowers the key's first
-//                    position there (atomicMin); the one thread whose CAS
-//                    put the key there finds or inserts it in the table
-//                    (odd-step probing, tombstone reuse, warp-aggregated
-//                    row pops), publishes the row in the scratch hash and
-//                    its block initialises the fresh rows.
-//  k_assign_resolve  a tile owns a key when its first position is the key's
-//                    global first position; owners take unique indices in
-//                    first-occurrence order (tile offsets by a decoupled
-//                    look-back over the tiles' owner counts) and publish
-//                    them in the scratch hash; key and row come from there.
-//  k_expand          per tile-local unique: its unique index and counts;
-//                    per position: the inverse index.
-//  k_gather          the 16-byte vectorised row gather, grid-stride over
-//                    the batch with four independent items per thread.
+// The unique keys come out in first-occurrence order.  Kernels, in launch
+// order (after one memset that clears the stage-2 scratch hash):
+//  k_claim    per tile of kTile positions: encode keys; stage 1: dedup inside
+//             the tile with a shared-memory hash (first position, count and
+//             each position's rank among its key's positions); stage 2: each
+//             tile-local unique claims its key in the global scratch hash,
+//             lowers the key's first position there (atomicMin) and adds its
+//             count (the returned total is the rank base of the tile's
+//             positions, so the ranks are written here).  The one thread whose
+//             CAS put a key into the scratch hash appends the slot to the list
+//             of distinct keys.
+//  k_resolve  one thread per distinct key, over the whole GPU: find the key in
+//             the table (odd-step probing) or insert it (first tombstone or
+//             EMPTY slot of its chain, rows popped once per block, fresh rows
+//             initialised by teams of lanes); note the key at its first
+//             position and count it in the tile that holds that position.
+//             The last block to finish turns the per-tile counts into tile
+//             offsets.
+//  k_number   per tile: the keys first seen in the tile take unique indices
+//             tile offset + their order inside the tile, i.e. first-occurrence
+//             order, and write the unique keys, rows and counts.
+//  k_expand   per tile: inverse index of every position.
+//  k_gather   the 16-byte vectorised row gather over the whole batch.
+// No kernel waits on another block.
 #include <atomic>
 
 #include "mt_kernels.cuh"
@@ -40,8 +46,9 @@ __device__ __forceinline__ uint32_t stage1_hash(unsigned long long key) {
   return (uint32_t)(((mix64(key ^ 0x2545F4914F6CDD1Dull) >> 32) * (unsigned long long)kHSA) >> 32);
 }
 
-__device__ __forceinline__ unsigned long long stage2_hash(unsigned long long key) {
-  return mix64(key ^ 0x9FB21C651E98DF25ull);
+// Home slot in the stage-2 scratch hash of ss slots (ss < 2^32).
+__device__ __forceinline__ unsigned long long stage2_home(unsigned long long key, unsigned long long ss) {
+  return ((mix64(key ^ 0x9FB21C651E98DF25ull) >> 32) * ss) >> 32;
 }
 
 // Exclusive scan of one int per thread over a block of NT threads; *total
@@ -73,26 +80,21 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return r;
 }
 
-template <int NT>
-__device__ __forceinline__ int block_sum(int v, int* s_warp) {
-  int t;
-  block_exclusive_scan<NT>(v, s_warp, &t);
-  return t;
-}
+constexpr size_t kSmemA = kHSA * 8 + kHSA * 4 + kHSA * 4 + kTile * 4 + kTile * 2 + kTile * 2 +
+                          (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
 
-constexpr size_t kSmemA = kHSA * 8 + kHSA * 4 + kTile * 4 + kTile * 2 + (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
-
-__global__ void __launch_bounds__(kThreadsA, 3) k_dedup_claim(const LookupParams p) {
+__global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHSA] stage-1 hash keys
   uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHSA);             // [kHSA] first local position, then local index
-  uint32_t* s_item = s_min + kHSA;                                         // [kTile] (hash slot << 16) | first position of local unique l
+  uint32_t* s_cnt = s_min + kHSA;                                          // [kHSA] positions per key, then rank base
+  uint32_t* s_item = s_cnt + kHSA;                                         // [kTile] (hash slot << 16) | first position of local unique l
   uint16_t* s_pslot = reinterpret_cast<uint16_t*>(s_item + kTile);         // [kTile] hash slot of each position
-  long long* s_off = reinterpret_cast<long long*>(s_pslot + kTile);        // [F + 1]
+  uint16_t* s_lrank = s_pslot + kTile;                                     // [kTile] rank of each position inside the tile
+  long long* s_off = reinterpret_cast<long long*>(s_lrank + kTile);        // [F + 1]
   unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
   __shared__ int s_warp[kThreadsA / 32];
   __shared__ int s_frange[2];  // features of the tile's first and last position
-  __shared__ int s_nnew;       // fresh rows listed by stage 2
 
   const int tile = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -102,13 +104,13 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_dedup_claim(const LookupParams
   for (int i = tid; i < kHSA; i += kThreadsA) {
     s_key[i] = kEmpty;
     s_min[i] = 0xFFFFFFFFu;
+    s_cnt[i] = 0u;
   }
   for (int i = tid; i <= p.F; i += kThreadsA) s_off[i] = p.feat_off[i];
   for (int i = tid; i < p.F; i += kThreadsA) s_tid[i] = p.table_ids[i];
   if (tid == 0) {
-    s_nnew = 0;
-    p.tile_status[tile] = 0ull;  // no owner count published yet (read by k_assign_resolve)
-    if (tile == 0) *p.ticket = 0;
+    p.tile_O[tile] = 0;  // counted by k_resolve
+    if (tile == 0) *p.done = 0u;
   }
   __syncthreads();
   if (tid < 2) {  // feature of position base (tid 0) and base + cnt - 1 (tid 1): last f with off[f] <= i
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_dedup_claim(const LookupParams
   __syncthreads();
   const int f_first = s_frange[0], f_last = s_frange[1];
 
-  // ---- encode + stage 1 (tile-local dedup) ----
+  // ---- encode + stage 1 (tile-local dedup: first position, count, rank) ----
   bool bad = false;
   long long idv[kPPTA];  // every ID load in flight before the shared-memory work
 #pragma unroll
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_dedup_claim(const LookupParams
         h = h + 1 == (uint32_t)kHSA ? 0u : h + 1;
       }
       atomicMin(&s_min[h], (uint32_t)lp);
+      s_lrank[lp] = (uint16_t)atomicAdd(&s_cnt[h], 1u);
       s_pslot[lp] = (uint16_t)h;
     } else if (in) {
       s_pslot[lp] = kNoIdx;
@@ -193,278 +196,283 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_dedup_claim(const LookupParams
   }
   __syncthreads();
 
-  uint16_t* lidx = p.lidx + base;
   for (int lp = tid; lp < cnt; lp += kThreadsA) {
     const uint16_t sl = s_pslot[lp];
-    lidx[lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
+    p.lidx[base + lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
+    p.first_slot[base + lp] = -1;  // k_resolve notes each key at its first position
   }
 
-  // ---- stage 2: claim every local unique in the global scratch hash; the
-  // thread whose CAS puts a key there is the only one in the grid to see it
-  // EMPTY, and it resolves the key in the table right away (find, or insert
-  // with tombstone reuse and a warp-aggregated row pop) and publishes the
-  // row in the scratch hash ----
-  __syncthreads();  // s_min and s_pslot are free from here: fresh rows are listed there
-  int32_t* s_newrow = reinterpret_cast<int32_t*>(s_min);  // [kHSA >= kTile] rows to initialise
-  uint16_t* s_newli = s_pslot;                           // [kTile] their local uniques
+  // ---- stage 2: every local unique claims its key in the global scratch hash,
+  // lowers the key's first position and adds its count there.  The thread
+  // whose CAS put the key into the scratch hash is the only one in the grid to
+  // see it EMPTY; it lists the slot as a distinct key. ----
   const size_t lb = (size_t)tile * kTile;
-  const uint32_t step = (uint32_t)p.T.hdr->step;
-  for (int li0 = 0; li0 < L; li0 += kThreadsA) {  // warp-uniform trip count (row pops are warp-wide)
+  for (int li0 = 0; li0 < L; li0 += kThreadsA) {  // warp-uniform trip count (the list append is warp-wide)
     const int li = li0 + tid;
     const bool act = li < L;
-    unsigned long long key = 0, h = 0;
+    unsigned long long h = 0;
     bool won = false;
     if (act) {
       const uint32_t it = s_item[li];
-      key = s_key[it >> 16];
+      const uint32_t sl = it >> 16;
+      const unsigned long long key = s_key[sl];
       const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
-      h = stage2_hash(key) & p.scratch_mask;
-      for (unsigned long long probe = 0; probe <= p.scratch_mask; ++probe) {
-        unsigned long long cur = load_key_relaxed(&p.sc_key[h]);
+      h = stage2_home(key, p.ss);
+      for (unsigned long long probe = 0; probe < p.ss; ++probe) {
+        unsigned long long cur = load_key_relaxed(&p.sc[h].key);
         if (cur == kEmpty) {
-          cur = atomicCAS(&p.sc_key[h], kEmpty, key);
+          cur = atomicCAS(&p.sc[h].key, kEmpty, key);
           if (cur == kEmpty) {
             won = true;
             cur = key;
           }
         }
         if (cur == key) break;
-        h = (h + 1) & p.scratch_mask;
+        h = h + 1 == p.ss ? 0ull : h + 1;
       }
-      atomicMin(&p.sc_minpos[h], gpos);
-      p.lfirst[lb + li] = gpos;
-      p.lsslot[lb + li] = (uint32_t)h;
+      atomicMin(&p.sc[h].first, gpos);
+      const uint32_t before = atomicAdd(&p.sc[h].cnt, s_cnt[sl]) + 1u;  // the slot starts at "count - 1" = 2^32 - 1
+      s_cnt[sl] = before;  // rank base of this tile's positions of the key
+      p.lsslot[lb + li] = (int32_t)h;
     }
-    int32_t row = -1;
-    bool claimed = false;
-    unsigned long long cs = 0;
-    if (won) {
-      long long t_end, t_tomb;
-      const long long sidx = find_slot(p.T, key, &t_end, &t_tomb, &row);
-      if (sidx < 0 && p.insert_missing) {
-        // absent, and no other thread inserts it (it won the scratch hash):
-        // take the first tombstone of its chain, else the EMPTY slot that
-        // ended the chain, else the next free slot after them
-        long long t = t_tomb >= 0 ? t_tomb : t_end;
-        unsigned long long slot = (home_slot(p.T, key) + (unsigned long long)t * p.T.S) & p.T.mask;
-        for (; t < (long long)p.T.max_probes; ++t) {
-          const unsigned long long k = load_key_relaxed(&p.T.slots[slot].key);
-          if ((k == kEmpty || k == kTomb) && atomicCAS(&p.T.slots[slot].key, k, key) == k) {
-            claimed = true;
-            cs = slot;
-            break;
-          }
-          slot = (slot + p.T.S) & p.T.mask;
-        }
-        if (!claimed) latch_error(p.T.hdr, MT_EFULL);
-      }
+    const unsigned wm = __ballot_sync(kFull, won);
+    if (wm) {
+      const int leader = __ffs(wm) - 1;
+      uint32_t first = 0;
+      if (lane == leader) first = atomicAdd(p.ulist_n, (uint32_t)__popc(wm)) + 1u;  // counter starts at 2^32 - 1
+      first = __shfl_sync(kFull, first, leader);
+      if (won) p.ulist[first + __popc(wm & ((1u << lane) - 1u))] = (int32_t)h;
     }
-    const unsigned need = __ballot_sync(kFull, claimed);
-    if (claimed) {
-      row = pop_row_warp(p.T, need);
-      if (row < 0) {
-        atomicExch(&p.T.slots[cs].key, kTomb);  // give the slot back; the chain stays intact
-        latch_error(p.T.hdr, MT_EFULL);
-      } else {
-        p.T.slots[cs].row = row;
-        p.T.slots[cs].meta = step;
-        const int q = atomicAdd(&s_nnew, 1);
-        s_newrow[q] = row;
-        s_newli[q] = (uint16_t)li;
-      }
-    }
-    if (won) p.sc_row[h] = row;
   }
   if (tid == 0) p.tile_L[tile] = L;
   __syncthreads();
 
-  // initialise fresh rows, one team of lanes per row
-  const int nnew = s_nnew;
+  if (p.ranks != nullptr) {
+    for (int lp = tid; lp < cnt; lp += kThreadsA) {
+      const uint16_t sl = s_pslot[lp];
+      p.ranks[base + lp] = sl == kNoIdx ? -1 : (int32_t)(s_cnt[sl] + s_lrank[lp]);
+    }
+  }
+}
+
+// One thread per distinct key, grid-stride over the list k_claim built.
+// Rows for inserted keys are popped from the free stack with one atomic per
+// block and iteration; a block's fresh rows are then initialised by teams of
+// lanes.  Every key is noted at its first position (first_slot) and counted
+// in the tile holding that position (tile_O).  The last block to finish
+// (counted on `done` after a fence) writes the exclusive prefix of tile_O and
+// the number of unique keys.
+__global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
+  __shared__ int s_need, s_nnew, s_avail;
+  __shared__ long long s_rowbase;
+  __shared__ int32_t s_newrow[kThreadsR];
+  __shared__ unsigned long long s_newkey[kThreadsR];
+  __shared__ int s_warp[kThreadsR / 32];
+  __shared__ bool s_last;
+
+  const int tid = threadIdx.x;
+  const uint32_t U = *p.ulist_n + 1u;  // the counter starts at 2^32 - 1
+  const uint32_t step = (uint32_t)p.T.hdr->step;
   const uint32_t vecs = p.T.row_dtype == MT_F32 ? p.T.dim / 4 : p.T.dim / 8;
   int team = 1;
   while (team < 32 && team < (int)vecs) team <<= 1;
-  const int nteams = kThreadsA / team, my_team = tid / team, lt = tid % team;
-  for (int q = my_team; q < nnew; q += nteams)
-    init_row_coop(p.T, s_newrow[q], s_key[s_item[s_newli[q]] >> 16], lt, team);
-}
+  const int nteams = kThreadsR / team, my_team = tid / team, lt = tid % team;
 
-// Tile status words of the owner-count scan: flag in the high half
-// (kStatAgg: the tile's own owner count; kStatIncl: owners of this tile and
-// all before it), value in the low half.
-constexpr unsigned long long kStatAgg = 1ull << 32, kStatIncl = 2ull << 32;
-constexpr int kLookbackTries = 1 << 22;
-
-__device__ __forceinline__ void store_status(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long load_status(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Owners take unique indices in first-occurrence order: a tile's owners are
-// the tile-local uniques whose first position is the key's global first
-// position.  Tiles are taken in start order (a ticket), so every tile
-// before a block's tile has started; the block publishes its owner count,
-// then its first warp adds up the counts of the tiles before it from their
-// status words (a decoupled look-back: a tile that already knows its
-// inclusive count ends the walk).  A wait that runs out of polls latches
-// MT_ETIMEOUT and leaves every index in bounds.  Key and row of each owner
-// come from the scratch hash, where its claimer put them.
-__global__ void __launch_bounds__(kThreads, 6) k_assign_resolve(const LookupParams p) {
-  __shared__ int s_warp[kThreads / 32];
-  __shared__ int s_tile;
-  __shared__ long long s_off;
-
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (tid == 0) s_tile = atomicAdd(p.ticket, 1);
-  __syncthreads();
-  const int tile = s_tile;
-  const int L = p.tile_L[tile];
-  const size_t lb = (size_t)tile * kTile;
-
-  uint32_t sl[kPPT], lf[kPPT], mp[kPPT];  // each round of loads all in flight at once
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    const int l = tid * kPPT + k;
-    sl[k] = l < L ? __ldg(&p.lsslot[lb + l]) : 0u;
-    lf[k] = l < L ? __ldg(&p.lfirst[lb + l]) : 0u;
-  }
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) mp[k] = tid * kPPT + k < L ? __ldcg(&p.sc_minpos[sl[k]]) : 1u;
-  uint32_t flags = 0;
-  int c = 0;
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    if (mp[k] == lf[k]) {  // this tile holds the key's first position
-      flags |= 1u << k;
-      ++c;
+  for (uint32_t b0 = blockIdx.x * kThreadsR; b0 < U; b0 += gridDim.x * kThreadsR) {  // block-uniform trip count
+    const uint32_t idx = b0 + tid;
+    const bool act = idx < U;
+    if (tid == 0) {
+      s_need = 0;
+      s_nnew = 0;
     }
-  }
-  int O;
-  int j = block_exclusive_scan<kThreads>(c, s_warp, &O);
-  unsigned long long* st = p.tile_status;
-  if (tid < 32) {
-    const bool stall = tile == 0 && (p.T.flags & MT_FLAG_TEST_STALL_SCAN);  // testing only: never publish
-    if (lane == 0 && !stall) store_status(st + tile, (tile == 0 ? kStatIncl : kStatAgg) | (unsigned long long)O);
-    long long excl = 0;
-    bool ok = true;
-    for (int q = tile - 1, tries = 0; q >= 0;) {
-      const int pq = q - lane;
-      const unsigned long long v = pq >= 0 ? load_status(st + pq) : kStatIncl;  // before tile 0: inclusive 0
-      const unsigned long long flag = v & ~0xFFFFFFFFull;
-      if (__ballot_sync(kFull, flag != 0) != kFull) {  // a tile in this window has not published yet
-        if (++tries >= kLookbackTries) {
-          ok = false;
-          break;
+    __syncthreads();
+    int32_t slot = 0, row = -1;
+    unsigned long long key = 0, cs = 0;
+    uint32_t gfirst = 0;
+    bool claimed = false;
+    if (act) {
+      slot = __ldcg(&p.ulist[idx]);
+      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[slot]));
+      key = sv.x;
+      gfirst = (uint32_t)(sv.y & 0xFFFFFFFFull);
+      long long t_end, t_tomb;
+      const long long sidx = find_slot(p.T, key, &t_end, &t_tomb, &row);
+      if (sidx < 0 && p.insert_missing) {
+        // absent, and no other thread inserts it (its key is listed once):
+        // take the first tombstone of its chain, else the EMPTY slot that
+        // ended the chain, else the next free slot after them
+        long long t = t_tomb >= 0 ? t_tomb : t_end;
+        unsigned long long s = (home_slot(p.T, key) + (unsigned long long)t * p.T.S) & p.T.mask;
+        for (; t < (long long)p.T.max_probes; ++t) {
+          const unsigned long long k = load_key_relaxed(&p.T.slots[s].key);
+          if ((k == kEmpty || k == kTomb) && atomicCAS(&p.T.slots[s].key, k, key) == k) {
+            claimed = true;
+            cs = s;
+            break;
+          }
+          s = (s + p.T.S) & p.T.mask;
         }
-        continue;
+        if (!claimed) latch_error(p.T.hdr, MT_EFULL);
       }
-      const unsigned incl = __ballot_sync(kFull, flag == kStatIncl);
-      const int stop = incl ? __ffs(incl) - 1 : 31;
-      long long x = lane <= stop ? (long long)(v & 0xFFFFFFFFull) : 0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-      excl += x;
-      if (incl) break;
-      q -= 32;
     }
-    if (!ok) excl = 0;  // in bounds (every index stays below this tile's owner count); the call reports the error
-    if (lane == 0) {
-      if (!ok) latch_error(p.T.hdr, MT_ETIMEOUT);
-      if (tile > 0) store_status(st + tile, kStatIncl | (unsigned long long)(excl + O));
-      s_off = excl;
+    const int q = claimed ? atomicAdd(&s_need, 1) : -1;
+    __syncthreads();
+    if (tid == 0 && s_need > 0) {  // one pop for the block: rows on the stack are free_stack[0 .. free_top)
+      const long long k = s_need;
+      const long long old = (long long)atomicAdd((unsigned long long*)&p.T.hdr->free_top, (unsigned long long)(-k));
+      const long long avail = old < 0 ? 0 : (old < k ? old : k);
+      if (avail < k) atomicAdd((unsigned long long*)&p.T.hdr->free_top, (unsigned long long)(k - avail));
+      s_rowbase = old;
+      s_avail = (int)avail;
     }
+    __syncthreads();
+    if (claimed) {
+      if (q < s_avail) {
+        row = p.T.free_stack[s_rowbase - 1 - q];
+        p.T.slots[cs].row = row;
+        p.T.slots[cs].meta = step;
+        const int w = atomicAdd(&s_nnew, 1);
+        s_newrow[w] = row;
+        s_newkey[w] = key;
+      } else {
+        atomicExch(&p.T.slots[cs].key, kTomb);  // give the slot back; the chain stays intact
+        latch_error(p.T.hdr, MT_EFULL);
+      }
+    }
+    if (act) {
+      p.sc_row[slot] = row;
+      p.first_slot[gfirst] = slot;
+      atomicAdd(&p.tile_O[gfirst / kTile], 1);
+    }
+    __syncthreads();
+    const int nnew = s_nnew;
+    for (int w = my_team; w < nnew; w += nteams) init_row_coop(p.T, s_newrow[w], s_newkey[w], lt, team);
+    __syncthreads();
   }
+
+  // the last block to finish: tile offsets of the first-occurrence numbering
+  __threadfence();
   __syncthreads();
-  const long long off = s_off;
-  if (tid == 0 && tile == p.ntiles - 1) *p.num_unique = off + O;
-  unsigned long long key[kPPT];
-  int32_t row[kPPT];
+  if (tid == 0) s_last = atomicAdd(p.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  long long carry = 0;
+  for (int c0 = 0; c0 < p.ntiles; c0 += kThreadsR * 4) {
+    int v[4], sum = 0;
 #pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    key[k] = (flags >> k) & 1u ? __ldcg(&p.sc_key[sl[k]]) : 0ull;
-    row[k] = (flags >> k) & 1u ? __ldcg(&p.sc_row[sl[k]]) : -1;
-  }
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
-    if (flags & (1u << k)) {
-      const int u = (int)(off + j);
-      p.sc_uidx[sl[k]] = u;
-      p.unique_keys[u] = key[k];
-      p.unique_rows[u] = row[k];
-      p.counts[u] = 0;
-      ++j;
+    for (int k = 0; k < 4; ++k) {
+      const int t = c0 + tid * 4 + k;
+      v[k] = t < p.ntiles ? __ldcg(&p.tile_O[t]) : 0;
+      sum += v[k];
     }
+    int tot;
+    int run = (int)carry + block_exclusive_scan<kThreadsR>(sum, s_warp, &tot);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = c0 + tid * 4 + k;
+      if (t < p.ntiles) p.tile_pre[t] = run;
+      run += v[k];
+    }
+    carry += tot;
+  }
+  if (tid == 0) {
+    p.tile_pre[p.ntiles] = (int32_t)carry;
+    *p.num_unique = (long long)U;
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
-  __shared__ int32_t s_lcnt[kTile];   // positions of local unique l in this tile, then its rank base
-  __shared__ int32_t s_u[kTile];      // unique index of local unique l
-  __shared__ uint16_t s_pl[kTile];    // local unique of each position
-  __shared__ uint16_t s_lrank[kTile]; // rank of each position among its local unique's positions
-
-  const int tile = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+// The keys first seen in a tile take the unique indices tile offset + their
+// order inside the tile: first-occurrence order over the whole batch.
+__global__ void __launch_bounds__(kThreads, 6) k_number(const LookupParams p) {
+  __shared__ int s_warp[kThreads / 32];
+  const int tile = blockIdx.x, tid = threadIdx.x;
   const long long base = (long long)tile * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
-  const int L = p.tile_L[tile];
-  const size_t lb = (size_t)tile * kTile;
+  const int pre = __ldg(&p.tile_pre[tile]);
 
-  for (int l = tid; l < L; l += kThreads) s_lcnt[l] = 0;
+  int32_t v[kPPT];  // positions tid*kPPT .. tid*kPPT + kPPT - 1, in order
+  if ((tid + 1) * kPPT <= cnt) {
+    const int4* src = reinterpret_cast<const int4*>(p.first_slot + base + tid * kPPT);
+#pragma unroll
+    for (int k = 0; k < kPPT / 4; ++k) {
+      const int4 w = __ldcg(src + k);
+      v[4 * k] = w.x;
+      v[4 * k + 1] = w.y;
+      v[4 * k + 2] = w.z;
+      v[4 * k + 3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+      const int lp = tid * kPPT + k;
+      v[k] = lp < cnt ? __ldcg(&p.first_slot[base + lp]) : -1;
+    }
+  }
+  int c = 0;
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) c += v[k] >= 0;
+  int tot;
+  int r = block_exclusive_scan<kThreads>(c, s_warp, &tot);
+  ulonglong2 sv[kPPT];
+  int32_t row[kPPT];
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {  // every owner's loads in flight at once
+    if (v[k] >= 0) {
+      sv[k] = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[v[k]]));
+      row[k] = __ldcg(&p.sc_row[v[k]]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    if (v[k] >= 0) {
+      const int u = pre + r++;
+      p.unique_keys[u] = sv[k].x;
+      p.unique_rows[u] = row[k];
+      p.counts[u] = (int32_t)((uint32_t)(sv[k].y >> 32) + 1u);
+      p.sc[v[k]].first = (uint32_t)u;  // from here on the slot holds the key's unique index
+    }
+  }
+}
+
+// inverse[i] = unique index of position i (-1 for an invalid ID).
+__global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
+  __shared__ int32_t s_u[kTile];  // unique index of each tile-local unique
+  const int tile = blockIdx.x, tid = threadIdx.x;
+  const long long base = (long long)tile * kTile;
+  const int cnt = (int)min((long long)kTile, p.n - base);
+  const int L = __ldg(&p.tile_L[tile]);
+  const size_t lb = (size_t)tile * kTile;
+  int32_t sl[kPPT];
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int l = k * kThreads + tid;
+    sl[k] = l < L ? __ldg(&p.lsslot[lb + l]) : -1;
+  }
+#pragma unroll
+  for (int k = 0; k < kPPT; ++k) {
+    const int l = k * kThreads + tid;
+    if (l < L) s_u[l] = (int32_t)__ldcg(&p.sc[sl[k]].first);
+  }
   __syncthreads();
-  uint32_t liv[kPPT];  // every local-index load in flight before the warp-synchronous work
+  uint16_t li[kPPT];
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int lp = k * kThreads + tid;
-    liv[k] = lp < cnt ? __ldg(&p.lidx[base + lp]) : kNoIdx;
+    li[k] = lp < cnt ? __ldg(&p.lidx[base + lp]) : kNoIdx;
   }
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int lp = k * kThreads + tid;
-    const bool in = lp < cnt;
-    const uint32_t li = liv[k];
-    if (in) s_pl[lp] = (uint16_t)li;
-    if (in && li != kNoIdx) s_lrank[lp] = (uint16_t)atomicAdd(&s_lcnt[li], 1);
-  }
-  __syncthreads();
-  // one atomic per (tile, unique): the old count is where this tile's
-  // positions start among all positions of the unique
-  for (int l0 = tid; l0 < L; l0 += 4 * kThreads) {  // four independent atomics in flight per thread
-    int32_t u[4], old[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int l = l0 + k * kThreads;
-      u[k] = l < L ? __ldcg(&p.sc_uidx[__ldg(&p.lsslot[lb + l])]) : 0;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int l = l0 + k * kThreads;
-      if (l < L) old[k] = atomicAdd(&p.counts[u[k]], s_lcnt[l]);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int l = l0 + k * kThreads;
-      if (l < L) {
-        s_u[l] = u[k];
-        s_lcnt[l] = old[k];
-      }
-    }
-  }
-  __syncthreads();
-  for (int lp = tid; lp < cnt; lp += kThreads) {
-    const uint16_t li = s_pl[lp];
-    p.inverse[base + lp] = li == kNoIdx ? -1 : s_u[li];
-    if (p.ranks != nullptr) p.ranks[base + lp] = li == kNoIdx ? -1 : s_lcnt[li] + s_lrank[lp];
+    if (lp < cnt) p.inverse[base + lp] = li[k] == kNoIdx ? -1 : s_u[li[k]];
   }
 }
 
 // out[i] = row of unique inverse[i] (zeros for an invalid ID or an absent
 // key): 16-byte items (position, vector), consecutive threads on consecutive
 // items; each round a block covers kGatherILP * blockDim contiguous items
-// (one independent item in flight per thread and step of blockDim), and the
-// blocks stride over the whole batch so every SM stays busy to the end.
+// (kGatherILP independent items in flight per thread), and the blocks stride
+// over the whole batch so every SM stays busy to the end.
 constexpr int kGatherILP = 2;
 __global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
   const int vec16 = (int)(p.T.emb_bytes / 16);
@@ -510,9 +518,9 @@ __global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
 LookupWsLayout lookup_ws_layout(long long n) {
   LookupWsLayout L{};
   L.ntiles = (int)((n + kTile - 1) / kTile);
-  unsigned long long ss = 1024;
-  while (ss < 2ull * (unsigned long long)n) ss <<= 1;
-  L.scratch_slots = ss;
+  // every distinct key needs a slot and every probe chain an EMPTY end: more
+  // slots than IDs; a quarter more keeps chains short even if all IDs differ
+  L.ss = align_up((size_t)n + (size_t)n / 4 + 1024, 1024);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -520,46 +528,57 @@ LookupWsLayout lookup_ws_layout(long long n) {
     return o;
   };
   const size_t cap = (size_t)L.ntiles * kTile;
-  L.sc_key = take(ss * 8);
-  L.sc_minpos = take(ss * 4);
-  L.sc_uidx = take(ss * 4);
-  L.sc_row = take(ss * 4);
+  L.sc = take(L.ss * sizeof(ScSlot));
+  L.ulist_n = off;                      // right after the slots: cleared by the same memset
+  L.clear_bytes = L.ss * sizeof(ScSlot) + 16;
+  take(16);
+  L.ulist = take((size_t)(n > 0 ? n : 1) * 4);
+  L.sc_row = take(L.ss * 4);
   L.tile_L = take((size_t)L.ntiles * 4);
-  L.tile_status = take((size_t)L.ntiles * 8);
-  L.ticket = take(16);
-  L.lfirst = take(cap * 4);
+  L.tile_O = take((size_t)L.ntiles * 4);
+  L.tile_pre = take((size_t)(L.ntiles + 1) * 4);
+  L.done = take(16);
+  L.first_slot = take(cap * 4);
   L.lsslot = take(cap * 4);
   L.lidx = take(cap * 2);
   L.total = off;
   return L;
 }
 
-cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s) {
-  if (p.n == 0) return cudaMemsetAsync(p.num_unique, 0, sizeof(long long), s);
-  static std::atomic<int> gather_grid[kMaxDevices];  // 0: not set up on that device yet
+cudaError_t launch_lookup(const LookupParams& p_in, cudaStream_t s) {
+  if (p_in.n == 0) return cudaMemsetAsync(p_in.num_unique, 0, sizeof(long long), s);
+  static std::atomic<int> gather_grid[kMaxDevices];   // 0: not set up on that device yet
+  static std::atomic<int> resolve_slots[kMaxDevices];
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
   if (gather_grid[dev].load(std::memory_order_relaxed) == 0) {
-    cudaError_t e = cudaFuncSetAttribute(k_dedup_claim, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
+    cudaError_t e = cudaFuncSetAttribute(k_claim, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
     if (e != cudaSuccess) return e;
-    int sms = 0, per = 0;
+    int sms = 0, per = 0, rper = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_gather, 256, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rper, k_resolve, kThreadsR, 0);
+    resolve_slots[dev].store(sms * (rper > 0 ? rper : 1), std::memory_order_relaxed);
     gather_grid[dev].store(sms * (per > 0 ? per : 1), std::memory_order_relaxed);
   }
-  // keys EMPTY and first positions "none", in one memset: the layout puts
-  // sc_minpos right after sc_key (8-byte keys keep it 256-byte aligned)
-  const size_t clear = (size_t)(reinterpret_cast<const char*>(p.sc_minpos) - reinterpret_cast<const char*>(p.sc_key)) +
-                       (p.scratch_mask + 1) * 4;
-  cudaError_t e = cudaMemsetAsync(p.sc_key, 0xFF, clear, s);
+  LookupParams p = p_in;
+  const long long want = (p.n + kThreadsR - 1) / kThreadsR;  // blocks if every ID were distinct
+  const int slots = resolve_slots[dev].load(std::memory_order_relaxed);
+  p.resolve_grid = (int)(want < slots ? want : slots);
+  // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1) and the distinct-key counter: all ones
+  cudaError_t e = cudaMemsetAsync(p.sc, 0xFF, (size_t)p.ss * sizeof(ScSlot) + 16, s);
   if (e != cudaSuccess) return e;
   {
-    MT_LAUNCH("k_dedup_claim", s);
-    k_dedup_claim<<<p.ntiles, kThreadsA, kSmemA, s>>>(p);
+    MT_LAUNCH("k_claim", s);
+    k_claim<<<p.ntiles, kThreadsA, kSmemA, s>>>(p);
   }
   {
-    MT_LAUNCH("k_assign_resolve", s);
-    k_assign_resolve<<<p.ntiles, kThreads, 0, s>>>(p);
+    MT_LAUNCH("k_resolve", s);
+    k_resolve<<<p.resolve_grid, kThreadsR, 0, s>>>(p);
+  }
+  {
+    MT_LAUNCH("k_number", s);
+    k_number<<<p.ntiles, kThreads, 0, s>>>(p);
   }
   {
     MT_LAUNCH("k_expand", s);
