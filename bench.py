@@ -458,6 +458,81 @@ def e2e_run(args, dev, stream, tdt):
     return out
 
 
+def jagged_bag_offsets(b) -> np.ndarray:
+    """Bags of a feature-major jagged batch: feature f of user u covers positions f*T + [uo[u], uo[u+1])."""
+    T = int(b.user_offsets[-1])
+    F = b.feat_offsets.size - 1
+    return np.concatenate([f * T + b.user_offsets[:-1] for f in range(F)] + [[F * T]]).astype(np.int64)
+
+
+def pooled_run(args, tab, wl, dev, stream, first_seed: int):
+    """Mean-pooled jagged bags: each step is a lookup without the per-position gather, the pooled forward
+    (mt_pool_forward) and the pooled backward + Adam (mt_backward_adam_pooled), on fresh batches, replayed as
+    CUDA graphs with events between the two halves."""
+    import torch
+    steps = min(args.steps, 8)
+    seq = wl.steps(first_seed, steps)
+    entries = []
+    for j, (b, _) in enumerate(seq):
+        U, _, _ = batch_stats(b)
+        bo = jagged_bag_offsets(b)
+        Bg = bo.size - 1
+        e = dict(batch=b, U=U, Bg=Bg, ids=torch.from_numpy(b.ids).to(dev), bo=torch.from_numpy(bo).to(dev),
+                 res=tab.new_result(b.n, gather=False),
+                 dp=_device_grads(torch, dev, torch.float32, 700_000 + first_seed + j, Bg, wl.dim))
+        e["out"] = torch.empty((Bg, wl.dim), dtype=torch.float32, device=dev)
+        entries.append(e)
+
+    def fwd(e):
+        b = e["batch"]
+        tab.lookup(e["ids"], b.feat_offsets, b.table_ids, gather=False, result=e["res"])
+        tab.pool_forward(e["res"], e["bo"], mode="mean", out=e["out"])
+
+    def bwd(e):
+        tab.backward_adam_pooled(e["res"], e["bo"], e["dp"], mode="mean")
+
+    # workspaces sized before capture (a capture must not allocate them)
+    tab.reserve_workspaces(max(e["batch"].n for e in entries), max(e["Bg"] for e in entries))
+    torch.cuda.synchronize(dev)
+    graphs = []
+    for e in entries:
+        gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf, stream=stream):
+            fwd(e)
+        with torch.cuda.graph(gb, stream=stream):
+            bwd(e)
+        graphs.append((gf, gb))
+    st0 = tab.stats()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in entries]
+    for (gf, gb), (a, m_, z) in zip(graphs, ev):
+        a.record(stream)
+        gf.replay()
+        m_.record(stream)
+        gb.replay()
+        z.record(stream)
+    torch.cuda.synchronize(dev)
+    fwd_s = sum(a.elapsed_time(m_) for a, m_, _ in ev) / 1e3 / steps
+    bwd_s = sum(m_.elapsed_time(z) for _, m_, z in ev) / 1e3 / steps
+    new_keys = max(0.0, (tab.stats()["live"] - st0["live"]) / steps)
+    N = sum(e["batch"].n for e in entries) / steps
+    U = sum(e["U"] for e in entries) / steps
+    Bg = sum(e["Bg"] for e in entries) / steps
+    B, d = wl.row_bytes, wl.dim
+    fwd_bytes = 12 * N + 24 * U + new_keys * (16 + B + 8 * d) + 4 * N + U * B + 8 * (Bg + 1) + 4 * d * Bg
+    bwd_bytes = 4 * N + 4 * d * Bg + U * (4 + 2 * B + 16 * d)
+    peak, _ = measured_hbm_peak()
+    return {"mode": "mean", "steps": steps, "bags_per_step": Bg, "ids_per_step": N, "new_keys_per_step": new_keys,
+            "fwd_ids_per_s": N / fwd_s, "bwd_ids_per_s": N / bwd_s,
+            "roofline_fwd": {"bytes_per_step": fwd_bytes, "ms_per_step": fwd_s * 1e3,
+                             "achieved": fwd_bytes / fwd_s / 1e9, "frac": fwd_bytes / fwd_s / 1e9 / peak},
+            "roofline_bwd": {"bytes_per_step": bwd_bytes, "ms_per_step": bwd_s * 1e3,
+                             "achieved": bwd_bytes / bwd_s / 1e9, "frac": bwd_bytes / bwd_s / 1e9 / peak},
+            "what": "lookup without the per-position gather + mean pooling of each (user, feature) bag; backward "
+                    "of the pooling folded into the per-unique reduction + Adam (no per-position gradient rows)"}
+
+
 def run_ours(args):
     import torch
     import update_merged_table_gb300 as mt
@@ -633,6 +708,9 @@ def run_ours(args):
     per_id, traffic_note = committed_traffic(dom) if args.config == 3 else (None, "counters cover the jagged workload")
     traffic = per_id * pN if per_id is not None else None
 
+    # -------- pooled jagged bags (sum/mean of each user's rows per feature) on further fresh steps --------
+    pooled = pooled_run(args, tab, wl, dev, stream, 1 + kf + nprof) if (args.config == 3 and args.pooled) else None
+
     # -------- tombstone compaction of the key store (one call, outside the step) --------
     comp = None
     if ws == 1:
@@ -686,6 +764,7 @@ def run_ours(args):
         "kernel_pass": f"eager, CUDA events around each launch, {len(prof_pool)} further fresh steps "
                        f"({p_new:.0f} new keys per step)",
         "cold_step": cold_stats,
+        "pooled": pooled,
         "compaction": comp,
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -793,6 +872,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--e2e", type=int, default=1, help="also time the step through host buffers (its own table)")
+    ap.add_argument("--pooled", type=int, default=1, help="also time the pooled jagged-bag step (jagged workload)")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=150.0,

@@ -222,6 +222,48 @@ size_t mt_backward_workspace_bytes(const mt_table* t, int64_t n);
 int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const void* grads, int grad_dtype,
                      const mt_adam* hp, float* gsum_out, void* ws, size_t ws_bytes, mt_stream stream);
 
+/* ---- pooled bags of a jagged batch ------------------------------------------ */
+
+/* A bag is a run of consecutive positions [bag_offsets[b], bag_offsets[b+1])
+ * of a lookup batch; in a jagged sequence batch one bag holds one user's
+ * tokens of one feature (MTGR section 5, Load Balance: user sequences of very
+ * different lengths).  Pooling replaces the bag's rows by their sum or mean. */
+#define MT_POOL_SUM 0
+#define MT_POOL_MEAN 1
+
+/* Workspace bytes mt_pool_forward needs for num_bags bags (an fp64 [num_bags, d] accumulator). */
+size_t mt_pool_workspace_bytes(const mt_table* t, int64_t num_bags);
+
+/* Pooled embeddings of the lookup `res` (same n, as the table holds the rows
+ * now): out[b] = sum of the rows of the keys at the bag's positions (zero
+ * rows for invalid IDs and absent keys), divided by the bag's length for
+ * MT_POOL_MEAN; accumulated as exact fp32 pairs and fp64, rounded once to
+ * fp32.  Empty bags give zeros.
+ *  bag_offsets  device int64 [num_bags + 1], non-decreasing within [0, n];
+ *               positions outside [bag_offsets[0], bag_offsets[num_bags])
+ *               are in no bag.  Offsets that break this latch MT_EINVAL on
+ *               the device (those bags read as zeros; every access stays in
+ *               bounds).
+ *  out          device fp32 [num_bags, d].
+ *  ws           device workspace of mt_pool_workspace_bytes(t, num_bags) bytes. */
+int mt_pool_forward(mt_table* t, const mt_lookup_result* res, int64_t n, const int64_t* bag_offsets,
+                    int64_t num_bags, int mode, float* out, void* ws, size_t ws_bytes, mt_stream stream);
+
+/* Workspace bytes mt_backward_adam_pooled needs. */
+size_t mt_backward_pooled_workspace_bytes(const mt_table* t, int64_t n, int64_t num_bags);
+
+/* Backward of mt_pool_forward followed by mt_backward_adam, with no
+ * per-position gradient rows: every position of bag b takes the gradient
+ * dpooled[b] (MT_POOL_SUM) or dpooled[b] * s_b rounded once to fp32 with
+ * s_b = fp32(1 / len_b) (MT_POOL_MEAN); positions in no bag take zero.  Then
+ * exactly the per-unique sum and Adam step of mt_backward_adam (the table's
+ * step counter advances once).
+ *  dpooled   device fp32 [num_bags, d].
+ *  ws        device workspace of mt_backward_pooled_workspace_bytes bytes. */
+int mt_backward_adam_pooled(mt_table* t, const mt_lookup_result* res, int64_t n, const int64_t* bag_offsets,
+                            int64_t num_bags, int mode, const float* dpooled, const mt_adam* hp, float* gsum_out,
+                            void* ws, size_t ws_bytes, mt_stream stream);
+
 /* ---- deletion ------------------------------------------------------------ */
 
 /* Workspace bytes mt_erase needs for n keys. */

@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
             "orc_sim_placed": (I64, [P, U64]),
             "orc_sim_sequence": (None, [P, U64, U64, P]),
             "orc_sim_raw_occupancy": (I64, [P, P]),
+            "orc_pool_forward": (I32, [P, P, I64, I32, P]),
+            "orc_backward_adam_pooled": (I32, [P, P, I64, I32, P, F, F, F, F, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -205,6 +207,28 @@ class Table:
         rc = lib().orc_backward_adam(self.h, _p(g), grad_dtype, lr, beta1, beta2, eps, _p(gsum))
         if rc != 0:
             raise RuntimeError(f"oracle backward failed: {rc}")
+        return gsum
+
+    def pool_forward(self, bag_offsets, mode: int = 0):
+        """Pooled rows [B, dim] fp32 of the last lookup: per bag of positions [bo[b], bo[b+1]) the sum
+        (mode 0) or mean (mode 1) of the rows, in double, rounded once."""
+        bo = _c(bag_offsets, np.int64)
+        B = bo.size - 1
+        out = np.zeros((max(B, 0), self.dim), np.float32)
+        if lib().orc_pool_forward(self.h, _p(bo), B, mode, _p(out)) != 0:
+            raise ValueError("bag offsets must be non-decreasing within [0, n]")
+        return out
+
+    def backward_adam_pooled(self, bag_offsets, dpooled, mode: int = 0, lr=1e-3, beta1=0.9, beta2=0.999,
+                             eps=1e-8, want_gsum=False):
+        """Backward of pool_forward followed by the table's backward + Adam; dpooled: fp32 [B, dim]."""
+        bo = _c(bag_offsets, np.int64)
+        dp = _c(dpooled, np.float32)
+        gsum = np.zeros((self._U, self.dim), np.float32) if want_gsum else None
+        rc = lib().orc_backward_adam_pooled(self.h, _p(bo), bo.size - 1, mode, _p(dp), lr, beta1, beta2, eps,
+                                            _p(gsum))
+        if rc != 0:
+            raise ValueError("bag offsets must be non-decreasing within [0, n]")
         return gsum
 
     def insert_keys(self, keys) -> int:

@@ -420,6 +420,67 @@ int orc_backward_adam(void* h, const void* grads, int grad_dtype, float lr, floa
   return ORC_OK;
 }
 
+// ---- pooled embeddings of jagged bags ---------------------------------------
+// A bag is a run of consecutive positions [bag_offsets[b], bag_offsets[b+1]):
+// in the jagged batches of MTGR (section 5, Load Balance: user sequences of
+// very different lengths) one bag is one user's tokens of one feature.  The
+// bag's pooled embedding is the sum (mode 0) or the mean (mode 1) of the rows
+// of its positions.  Positions outside every bag are in no output.
+
+// out[b] = sum over the bag's positions of the (stored) row of the position's
+// key after the last lookup, accumulated in double in position order; mode 1
+// divides the double sum by the bag's length; each value rounded once to
+// fp32.  Invalid positions and absent keys add zero rows.  Empty bags give
+// zeros.  Returns ORC_EINVAL (and writes nothing) for offsets that decrease
+// or leave [0, n].
+int orc_pool_forward(void* h, const int64_t* bag_offsets, int64_t B, int mode, float* out) {
+  Table* t = (Table*)h;
+  const int64_t n = (int64_t)t->last_inverse.size();
+  const uint32_t d = t->dim;
+  for (int64_t b = 0; b < B; ++b)
+    if (bag_offsets[b] < 0 || bag_offsets[b] > bag_offsets[b + 1] || bag_offsets[b + 1] > n) return ORC_EINVAL;
+  std::vector<double> acc(d);
+  for (int64_t b = 0; b < B; ++b) {
+    std::fill(acc.begin(), acc.end(), 0.0);
+    for (int64_t i = bag_offsets[b]; i < bag_offsets[b + 1]; ++i) {
+      const int32_t u = t->last_inverse[i];
+      if (u < 0) continue;
+      auto it = t->rows.find(t->last_uniq[u]);
+      if (it == t->rows.end()) continue;
+      for (uint32_t j = 0; j < d; ++j) acc[j] += (double)t->emb_at(t->last_uniq[u], it->second, j);
+    }
+    const int64_t len = bag_offsets[b + 1] - bag_offsets[b];
+    for (uint32_t j = 0; j < d; ++j)
+      out[(size_t)b * d + j] = (float)(mode == 1 && len > 0 ? acc[j] / (double)len : acc[j]);
+  }
+  return ORC_OK;
+}
+
+// The backward of pooling followed by the table's backward: every position
+// of bag b receives the bag's gradient dpooled[b] (mode 0) or, for the mean,
+// dpooled[b] * s_b rounded once to fp32, with s_b = 1 / len_b rounded once to
+// fp32 (mode 1); positions outside every bag receive zero.  Then exactly
+// orc_backward_adam on those per-position gradients.
+int orc_backward_adam_pooled(void* h, const int64_t* bag_offsets, int64_t B, int mode, const float* dpooled,
+                             float lr, float beta1, float beta2, float eps, float* gsum_out) {
+  Table* t = (Table*)h;
+  const int64_t n = (int64_t)t->last_inverse.size();
+  const uint32_t d = t->dim;
+  for (int64_t b = 0; b < B; ++b)
+    if (bag_offsets[b] < 0 || bag_offsets[b] > bag_offsets[b + 1] || bag_offsets[b + 1] > n) return ORC_EINVAL;
+  std::vector<float> grads((size_t)n * d, 0.0f);
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t len = bag_offsets[b + 1] - bag_offsets[b];
+    const float s = (float)(1.0 / (double)(len > 0 ? len : 1));
+    for (int64_t i = bag_offsets[b]; i < bag_offsets[b + 1]; ++i)
+      for (uint32_t j = 0; j < d; ++j) {
+        const float g = dpooled[(size_t)b * d + j];
+        grads[(size_t)i * d + j] = mode == 1 ? g * s : g;
+      }
+  }
+  return orc_backward_adam(h, grads.data(), ORC_F32, lr, beta1, beta2, eps, gsum_out);
+}
+
 // Erase a batch of merged keys.  found[i] = 1 when keys[i] was present before
 // the call (every duplicate of a present key reports 1).  A later re-insert
 // of an erased key starts again from init(key) with m = v = 0.

@@ -421,3 +421,116 @@ def test_tombstone_reuse_and_chain():
     assert sim.placed(d) == 1        # reuses it
     occ, _ = sim.occupancy()
     assert (occ == 2).sum() == 0
+
+
+# ---------------------------------------------------------------------------
+# Adam: the folded form against the textbook form over many steps
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("row_dtype", [oracle.F32, oracle.BF16])
+def test_adam_folded_form_matches_textbook_form(row_dtype):
+    """The oracle applies w -= step_size * m / (sqrt(v) * inv_sqrt_bc2 + eps) with the bias corrections folded
+    into per-step scalars and beta powers kept as running products.  Kingma & Ba's textbook form,
+    m_hat = m / (1 - b1^t), v_hat = v / (1 - b2^t), w -= lr * m_hat / (sqrt(v_hat) + eps), written here in
+    float32 numpy with pow() for the beta powers, must agree over 30 steps: fp32 rows to 1e-5 relative,
+    bf16 rows (stored rounded each step, as the table does) to one bf16 ulp."""
+    from numerics import bf16_ulp_distance
+    rng = np.random.default_rng(12)
+    dim, keys = 16, np.arange(20, dtype=np.int64)
+    t = oracle.Table(8, dim, row_dtype=row_dtype)
+    t.lookup(keys)
+    w = np.stack([t.get_row(int(k))[0] for k in keys]).astype(np.float32)
+    m = np.zeros_like(w)
+    v = np.zeros_like(w)
+    lr, b1, b2, eps = np.float32(1e-3), np.float32(0.9), np.float32(0.999), np.float32(1e-8)
+    for step in range(1, 31):
+        t.lookup(keys)
+        g = rng.standard_normal((keys.size, dim)).astype(np.float32)
+        t.backward_adam(g)
+        m = b1 * m + (np.float32(1) - b1) * g
+        v = b2 * v + (np.float32(1) - b2) * g * g
+        m_hat = m / np.float32(1.0 - 0.9 ** step)
+        v_hat = v / np.float32(1.0 - 0.999 ** step)
+        w = w - lr * m_hat / (np.sqrt(v_hat) + eps)
+        if row_dtype == oracle.BF16:
+            w = torch.from_numpy(w).to(torch.bfloat16).float().numpy()
+    got = np.stack([t.get_row(int(k))[0] for k in keys])
+    if row_dtype == oracle.BF16:
+        assert bf16_ulp_distance(got, w).max() <= 1
+    else:
+        np.testing.assert_allclose(got, w, rtol=1e-5, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Pooled bags
+# ---------------------------------------------------------------------------
+
+def _pool_case(seed, dim=8, n=3000, vocab=400):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, vocab, size=n)
+    cuts = np.sort(rng.choice(np.arange(1, n), size=40, replace=False))
+    bo = np.concatenate([[0], cuts, [n]]).astype(np.int64)
+    bo = np.insert(bo, 5, bo[5])  # an empty bag
+    t = oracle.Table(12, dim)
+    r = t.lookup(ids)
+    return t, r, bo, rng
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_pool_forward_matches_numpy_segment_sum(mode):
+    """Sum (mode 0) and mean (mode 1) of each bag's gathered rows, against numpy's reduceat in float64."""
+    t, r, bo, _ = _pool_case(3)  # bags cover every position, one of them is empty
+    got = t.pool_forward(bo, mode)
+    lens = np.diff(bo)
+    full = lens > 0
+    seg = np.add.reduceat(r["rows"].astype(np.float64), bo[:-1][full], axis=0)  # contiguous bags up to n
+    if mode == 1:
+        seg = seg / lens[full][:, None]
+    assert np.array_equal(got[full], seg.astype(np.float32))
+    assert not got[~full].any()
+
+
+def test_pool_forward_partial_cover_and_bad_offsets():
+    t, r, _, _ = _pool_case(4)
+    bo = np.array([100, 100, 300, 301], np.int64)  # positions before 100 and from 301 on are in no bag
+    got = t.pool_forward(bo)
+    assert not got[0].any()
+    assert np.array_equal(got[1], r["rows"][100:300].astype(np.float64).sum(0).astype(np.float32))
+    assert np.array_equal(got[2], r["rows"][300])
+    with pytest.raises(ValueError):
+        t.pool_forward(np.array([0, 20, 10], np.int64))
+    with pytest.raises(ValueError):
+        t.pool_forward(np.array([0, 5000], np.int64))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_pool_backward_equals_expanded_backward(mode):
+    """The pooled backward equals the plain backward fed the bag gradient at every position of the bag (times
+    fp32(1/len) for the mean); its gradient sums equal torch's index_add_ of those expanded rows."""
+    t1, r, bo, rng = _pool_case(5, dim=8)
+    t2, _, _, _ = _pool_case(5, dim=8)
+    B = bo.size - 1
+    dp = rng.standard_normal((B, 8)).astype(np.float32)
+    gs1 = t1.backward_adam_pooled(bo, dp, mode=mode, want_gsum=True)
+    lens = np.diff(bo)
+    scale = np.where(lens > 0, np.float32(1) / np.maximum(lens, 1).astype(np.float32), np.float32(1))
+    per_bag = dp * scale[:, None] if mode == 1 else dp
+    expanded = np.repeat(per_bag.astype(np.float32), lens, axis=0)
+    gs2 = t2.backward_adam(expanded, want_gsum=True)
+    assert np.array_equal(gs1, gs2)
+    ref = torch.zeros(r["U"], 8, dtype=torch.float64)
+    ref.index_add_(0, torch.from_numpy(r["inverse"].astype(np.int64)), torch.from_numpy(expanded).double())
+    assert np.array_equal(gs1, ref.float().numpy())
+    for k in r["unique"][:50]:
+        a, b_ = t1.get_row(int(k)), t2.get_row(int(k))
+        assert all(np.array_equal(x, y) for x, y in zip(a, b_))
+
+
+def test_reciprocal_of_bag_length_is_correctly_rounded():
+    """The mean's scale fp32(1/len), taken from the double quotient, equals IEEE's correctly rounded fp32
+    division 1/len for every length up to 10^5 (no double-rounding case), so the CUDA side may use the
+    correctly rounded fp32 reciprocal."""
+    lens = np.arange(1, 100_001, dtype=np.float64)
+    via_double = (1.0 / lens).astype(np.float32)
+    direct = np.float32(1) / lens.astype(np.float32)
+    assert np.array_equal(via_double, direct)

@@ -20,13 +20,15 @@ import os
 
 import numpy as np
 
-__all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "KEY_EMPTY", "KEY_TOMBSTONE",
+__all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "POOL_SUM", "POOL_MEAN",
+           "KEY_EMPTY", "KEY_TOMBSTONE",
            "ABI_FUNCTIONS", "profile_enable", "profile_report", "kernel_launches"]
 
 MT_OK, MT_EINVAL, MT_ENOSPACE, MT_EFULL, MT_EKEY, MT_ECUDA, MT_ETOOBIG = 0, -1, -2, -3, -4, -5, -6
 ABI_VERSION = 2
 LOOKUP_STATIC_MAX_IDS = 65536
 MT_F32, MT_BF16 = 0, 1
+POOL_SUM, POOL_MEAN = 0, 1
 KEY_EMPTY = (1 << 64) - 1
 KEY_TOMBSTONE = (1 << 64) - 2
 HIST_BINS = 64
@@ -80,6 +82,10 @@ ABI_FUNCTIONS = {
     "mt_lookup": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "mt_lookup_static": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P]),
     "mt_backward_workspace_bytes": (_SZ, [_P, _I64]),
+    "mt_pool_workspace_bytes": (_SZ, [_P, _I64]),
+    "mt_pool_forward": (_I32, [_P, _P, _I64, _P, _I64, _I32, _P, _P, _SZ, _P]),
+    "mt_backward_pooled_workspace_bytes": (_SZ, [_P, _I64, _I64]),
+    "mt_backward_adam_pooled": (_I32, [_P, _P, _I64, _P, _I64, _I32, _P, _P, _P, _P, _SZ, _P]),
     "mt_backward_adam": (_I32, [_P, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
     "mt_erase_workspace_bytes": (_SZ, [_I64]),
     "mt_erase": (_I32, [_P, _P, _I64, _P, _P, _SZ, _P]),
@@ -317,6 +323,62 @@ class Table:
                                          ctypes.byref(hp), _ptr(gsum), ws.data_ptr(), ws.numel(), _stream(stream)),
                "mt_backward_adam")
         return gsum
+
+    def pool_forward(self, res: LookupResult, bag_offsets, mode: str = "sum", out=None, stream=None):
+        """Pooled rows fp32 [B, dim] of the lookup `res`: per bag of positions
+        [bag_offsets[b], bag_offsets[b+1]) the sum or the mean of its rows.
+        bag_offsets: int64 CUDA tensor [B + 1]."""
+        torch = _torch()
+        bo = self._bag_offsets(bag_offsets)
+        B = bo.numel() - 1
+        m = {"sum": POOL_SUM, "mean": POOL_MEAN}[mode]
+        if out is None:
+            out = torch.empty((max(B, 1), self.dim), dtype=torch.float32, device=self.device)
+        ws = self._workspace("pool", self.lib.mt_pool_workspace_bytes(self.h, B))
+        st = res.as_struct()
+        _check(self.lib.mt_pool_forward(self.h, ctypes.byref(st), res.n, bo.data_ptr(), B, m, out.data_ptr(),
+                                        ws.data_ptr(), ws.numel(), _stream(stream)), "mt_pool_forward")
+        return out[:B]
+
+    def backward_adam_pooled(self, res: LookupResult, bag_offsets, dpooled, mode: str = "sum", lr: float = 1e-3,
+                             beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8, want_gsum: bool = False,
+                             stream=None):
+        """Backward of pool_forward (bag gradients dpooled fp32 [B, dim]) and one sparse Adam step."""
+        torch = _torch()
+        bo = self._bag_offsets(bag_offsets)
+        B = bo.numel() - 1
+        m = {"sum": POOL_SUM, "mean": POOL_MEAN}[mode]
+        if dpooled.shape != (B, self.dim) or dpooled.dtype != torch.float32 or not dpooled.is_cuda \
+                or not dpooled.is_contiguous():
+            raise ValueError("dpooled must be a contiguous fp32 CUDA tensor [B, dim]")
+        n = res.n
+        gsum = torch.empty((max(n, 1), self.dim), dtype=torch.float32, device=self.device) if want_gsum else None
+        hp = _Adam(lr, beta1, beta2, eps)
+        ws = self._workspace("backward_pooled", self.lib.mt_backward_pooled_workspace_bytes(self.h, n, B))
+        st = res.as_struct()
+        _check(self.lib.mt_backward_adam_pooled(self.h, ctypes.byref(st), n, bo.data_ptr(), B, m,
+                                                dpooled.data_ptr() if B else None, ctypes.byref(hp), _ptr(gsum),
+                                                ws.data_ptr(), ws.numel(), _stream(stream)),
+               "mt_backward_adam_pooled")
+        return gsum
+
+    def reserve_workspaces(self, n: int, num_bags: int = 0):
+        """Allocate every workspace a batch of n IDs (and num_bags pooled bags) needs, so that later calls
+        (for instance under CUDA graph capture) allocate nothing."""
+        self._workspace("lookup", self.lib.mt_lookup_workspace_bytes(self.h, n))
+        self._workspace("backward", self.lib.mt_backward_workspace_bytes(self.h, n))
+        if num_bags:
+            self._workspace("pool", self.lib.mt_pool_workspace_bytes(self.h, num_bags))
+            self._workspace("backward_pooled", self.lib.mt_backward_pooled_workspace_bytes(self.h, n, num_bags))
+
+    def _bag_offsets(self, bag_offsets):
+        torch = _torch()
+        if not torch.is_tensor(bag_offsets):
+            bag_offsets = torch.as_tensor(np.ascontiguousarray(bag_offsets, dtype=np.int64)).to(self.device)
+        if bag_offsets.dtype != torch.int64 or not bag_offsets.is_cuda or not bag_offsets.is_contiguous() \
+                or bag_offsets.dim() != 1 or bag_offsets.numel() < 1:
+            raise TypeError("bag_offsets must be a contiguous 1-D int64 CUDA tensor [B + 1]")
+        return bag_offsets
 
     def grow(self, log2_slots: int, num_rows: int = 0, stream=None):
         """Capacity expansion into a new arena with 2^log2_slots slots and num_rows rows

@@ -1,11 +1,26 @@
 // The C ABI (include/mt.h): argument validation, arena and workspace
 // carving, kernel launches.  No device memory is allocated here.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <new>
 
 #include "mt_kernels.cuh"
+
+namespace mt {
+int sm_count() {
+  static std::atomic<int> sms[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  int v = sms[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 1;
+    sms[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+}  // namespace mt
 
 struct mt_table {
   mt_config cfg;
@@ -109,6 +124,78 @@ bool valid_result(const mt_lookup_result* r) {
   return r != nullptr && r->unique_keys && r->inverse && r->counts && r->unique_rows && r->num_unique &&
          aligned(r->unique_keys, 16) && aligned(r->inverse, 16) && aligned(r->counts, 16) &&
          aligned(r->unique_rows, 16) && aligned(r->num_unique, 8) && aligned(r->ranks, 16);
+}
+
+int check_backward(const mt_table* t, const mt_lookup_result* res, int grad_dtype, const mt_adam* hp,
+                   const float* gsum_out) {
+  if (!valid_result(res) || hp == nullptr) return MT_EINVAL;
+  if (grad_dtype != MT_F32 && grad_dtype != MT_BF16) return MT_EINVAL;
+  if (gsum_out != nullptr && !aligned(gsum_out, 16)) return MT_EINVAL;
+  if (!(hp->lr >= 0.0f) || !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) ||
+      !(hp->eps > 0.0f))
+    return MT_EINVAL;
+  return MT_OK;
+}
+
+// One backward + Adam step; gradient row r of `grads` feeds every position
+// mapped to it (pos_map, or the position itself when pos_map is NULL).
+int run_backward(mt_table* t, const mt_lookup_result* res, int64_t n, const void* grads, int grad_dtype,
+                 const int32_t* pos_map, int64_t grad_rows, const mt_adam* hp, float* gsum_out, void* ws,
+                 const mt::BackwardWsLayout& L, cudaStream_t stream) {
+  char* w = static_cast<char*>(ws);
+  mt::BackwardParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.T = t->dev;
+  p.n = n;
+  p.pos_map = pos_map;
+  p.grad_rows = grad_rows;
+  p.inverse = res->inverse;
+  p.ranks = res->ranks;
+  p.counts = res->counts;
+  p.unique_rows = res->unique_rows;
+  p.num_unique = reinterpret_cast<const long long*>(res->num_unique);
+  p.grads = grads;
+  p.grad_dtype = grad_dtype;
+  p.lr = hp->lr;
+  p.beta1 = hp->beta1;
+  p.beta2 = hp->beta2;
+  p.eps = hp->eps;
+  p.one_minus_b1 = (float)(1.0 - (double)hp->beta1);
+  p.one_minus_b2 = (float)(1.0 - (double)hp->beta2);
+  p.gsum_out = gsum_out;
+  p.bsum = reinterpret_cast<int32_t*>(w + L.bsum);
+  p.boff = reinterpret_cast<int32_t*>(w + L.boff);
+  p.seg = reinterpret_cast<int2*>(w + L.seg);
+  p.chunks = reinterpret_cast<int4*>(w + L.chunks);
+  p.heavy_info = reinterpret_cast<int4*>(w + L.heavy_info);
+  p.pos_sorted = reinterpret_cast<int32_t*>(w + L.pos_sorted);
+  p.acc64 = reinterpret_cast<double*>(w + L.acc64);
+  p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
+  p.work = reinterpret_cast<int32_t*>(w + L.work);
+  p.nblk = L.nblk;
+  p.ntiles = L.ntiles;
+  p.team_shift = mt::backward_team_shift(t->cfg.dim, (int)t->cfg.row_dtype);
+  p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
+  const int rc = cuda_status(mt::launch_backward(p, stream));
+  if (rc == MT_OK) t->step += 1;
+  return rc;
+}
+
+// Workspace of the pooled backward: the backward's own, the bag of every
+// position, and (for the mean) the scaled bag gradients.
+struct PooledLayout {
+  mt::BackwardWsLayout bw;
+  size_t backward, pos_bag, scaled, total;
+};
+
+PooledLayout pooled_layout(const mt_table* t, int64_t n, int64_t num_bags) {
+  PooledLayout L{};
+  L.bw = mt::backward_ws_layout(n, t->cfg.dim);
+  L.backward = 0;
+  L.pos_bag = align_up(L.bw.total, 256);
+  L.scaled = align_up(L.pos_bag + (size_t)(n > 0 ? n : 1) * 4, 256);
+  L.total = align_up(L.scaled + (size_t)(num_bags > 0 ? num_bags : 1) * t->cfg.dim * 4, 256);
+  return L;
 }
 
 }  // namespace
@@ -272,50 +359,77 @@ size_t mt_backward_workspace_bytes(const mt_table* t, int64_t n) {
 
 int mt_backward_adam(mt_table* t, const mt_lookup_result* res, int64_t n, const void* grads, int grad_dtype,
                      const mt_adam* hp, float* gsum_out, void* ws, size_t ws_bytes, mt_stream stream) {
-  if (t == nullptr || n < 0 || n > 0x7FFFFFFF || !valid_result(res) || hp == nullptr) return MT_EINVAL;
-  if (grad_dtype != MT_F32 && grad_dtype != MT_BF16) return MT_EINVAL;
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF) return MT_EINVAL;
   if (n > 0 && (grads == nullptr || !aligned(grads, 16))) return MT_EINVAL;
-  if (gsum_out != nullptr && !aligned(gsum_out, 16)) return MT_EINVAL;
-  if (!(hp->lr >= 0.0f) || !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) ||
-      !(hp->eps > 0.0f))
-    return MT_EINVAL;
+  const int rc = check_backward(t, res, grad_dtype, hp, gsum_out);
+  if (rc != MT_OK) return rc;
   const mt::BackwardWsLayout L = mt::backward_ws_layout(n, t->cfg.dim);
   if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return MT_ENOSPACE;
-  char* w = static_cast<char*>(ws);
-  mt::BackwardParams p;
+  return run_backward(t, res, n, grads, grad_dtype, nullptr, n, hp, gsum_out, ws, L, as_stream(stream));
+}
+
+size_t mt_pool_workspace_bytes(const mt_table* t, int64_t num_bags) {
+  if (t == nullptr || num_bags < 0 || num_bags > 0x7FFFFFFF) return 0;
+  return align_up((size_t)(num_bags > 0 ? num_bags : 1) * t->cfg.dim * sizeof(double), 256);
+}
+
+int mt_pool_forward(mt_table* t, const mt_lookup_result* res, int64_t n, const int64_t* bag_offsets,
+                    int64_t num_bags, int mode, float* out, void* ws, size_t ws_bytes, mt_stream stream) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF || num_bags < 0 || num_bags > 0x7FFFFFFF || !valid_result(res))
+    return MT_EINVAL;
+  if (mode != MT_POOL_SUM && mode != MT_POOL_MEAN) return MT_EINVAL;
+  if (num_bags > 0 && (bag_offsets == nullptr || !aligned(bag_offsets, 8) || out == nullptr || !aligned(out, 16)))
+    return MT_EINVAL;
+  if (num_bags == 0) return MT_OK;
+  if (ws == nullptr || ws_bytes < mt_pool_workspace_bytes(t, num_bags) || !aligned(ws, 256)) return MT_ENOSPACE;
+  mt::PoolParams p;
   std::memset(&p, 0, sizeof(p));
   p.T = t->dev;
   p.n = n;
   p.inverse = res->inverse;
-  p.ranks = res->ranks;
-  p.counts = res->counts;
   p.unique_rows = res->unique_rows;
   p.num_unique = reinterpret_cast<const long long*>(res->num_unique);
-  p.grads = grads;
-  p.grad_dtype = grad_dtype;
-  p.lr = hp->lr;
-  p.beta1 = hp->beta1;
-  p.beta2 = hp->beta2;
-  p.eps = hp->eps;
-  p.one_minus_b1 = (float)(1.0 - (double)hp->beta1);
-  p.one_minus_b2 = (float)(1.0 - (double)hp->beta2);
-  p.gsum_out = gsum_out;
-  p.bsum = reinterpret_cast<int32_t*>(w + L.bsum);
-  p.boff = reinterpret_cast<int32_t*>(w + L.boff);
-  p.seg = reinterpret_cast<int2*>(w + L.seg);
-  p.chunks = reinterpret_cast<int4*>(w + L.chunks);
-  p.heavy_info = reinterpret_cast<int4*>(w + L.heavy_info);
-  p.pos_sorted = reinterpret_cast<int32_t*>(w + L.pos_sorted);
-  p.acc64 = reinterpret_cast<double*>(w + L.acc64);
-  p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
-  p.work = reinterpret_cast<int32_t*>(w + L.work);
-  p.nblk = L.nblk;
-  p.ntiles = L.ntiles;
+  p.bag_offsets = reinterpret_cast<const long long*>(bag_offsets);
+  p.num_bags = num_bags;
+  p.mode = mode;
   p.team_shift = mt::backward_team_shift(t->cfg.dim, (int)t->cfg.row_dtype);
-  p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
-  const int rc = cuda_status(mt::launch_backward(p, as_stream(stream)));
-  if (rc == MT_OK) t->step += 1;
-  return rc;
+  p.out = out;
+  p.acc = static_cast<double*>(ws);
+  return cuda_status(mt::launch_pool(p, as_stream(stream)));
+}
+
+size_t mt_backward_pooled_workspace_bytes(const mt_table* t, int64_t n, int64_t num_bags) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF || num_bags < 0 || num_bags > 0x7FFFFFFF) return 0;
+  return pooled_layout(t, n, num_bags).total;
+}
+
+int mt_backward_adam_pooled(mt_table* t, const mt_lookup_result* res, int64_t n, const int64_t* bag_offsets,
+                            int64_t num_bags, int mode, const float* dpooled, const mt_adam* hp, float* gsum_out,
+                            void* ws, size_t ws_bytes, mt_stream stream) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF || num_bags < 0 || num_bags > 0x7FFFFFFF) return MT_EINVAL;
+  if (mode != MT_POOL_SUM && mode != MT_POOL_MEAN) return MT_EINVAL;
+  if (num_bags > 0 && (bag_offsets == nullptr || !aligned(bag_offsets, 8) || dpooled == nullptr ||
+                       !aligned(dpooled, 16)))
+    return MT_EINVAL;
+  const int rc = check_backward(t, res, MT_F32, hp, gsum_out);
+  if (rc != MT_OK) return rc;
+  const PooledLayout PL = pooled_layout(t, n, num_bags);
+  if (ws == nullptr || ws_bytes < PL.total || !aligned(ws, 256)) return MT_ENOSPACE;
+  char* w = static_cast<char*>(ws);
+  cudaStream_t s = as_stream(stream);
+  int32_t* pos_bag = reinterpret_cast<int32_t*>(w + PL.pos_bag);
+  if (mt::launch_pos_bag(reinterpret_cast<const long long*>(bag_offsets), num_bags, n, pos_bag, t->dev.hdr, s) !=
+      cudaSuccess)
+    return MT_ECUDA;
+  const float* g = dpooled;
+  if (mode == MT_POOL_MEAN && num_bags > 0) {
+    float* scaled = reinterpret_cast<float*>(w + PL.scaled);
+    if (mt::launch_pool_scale(reinterpret_cast<const long long*>(bag_offsets), num_bags, (int)t->cfg.dim, dpooled,
+                              scaled, s) != cudaSuccess)
+      return MT_ECUDA;
+    g = scaled;
+  }
+  return run_backward(t, res, n, g, MT_F32, pos_bag, num_bags, hp, gsum_out, w + PL.backward, PL.bw, s);
 }
 
 size_t mt_erase_workspace_bytes(int64_t n) {

@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
   __syncthreads();
   for (int lp = tid; lp < cnt; lp += kThreads) {
     const uint16_t sl = s_slot[lp];
-    if (sl != kNoIdx) p.pos_sorted[s_hcnt[sl] + s_rank[lp]] = (int32_t)(base + lp);
+    if (sl != kNoIdx)
+      p.pos_sorted[s_hcnt[sl] + s_rank[lp]] = p.pos_map ? __ldg(&p.pos_map[base + lp]) : (int32_t)(base + lp);
   }
 }
 
@@ -485,18 +486,21 @@ __global__ void __launch_bounds__(256) k_bw_scatter(const BackwardParams p) {
         bad = true;
         continue;
       }
-      p.pos_sorted[sg[k].x + r[k]] = (int32_t)(i0 + k * stride);
+      const long long i = i0 + k * stride;
+      p.pos_sorted[sg[k].x + r[k]] = p.pos_map ? __ldg(&p.pos_map[i]) : (int32_t)i;
     }
   }
   if (bad) latch_error(p.T.hdr, MT_EINVAL);
 }
 
-// A grouped position, or -1 when it lies outside the batch (only possible
-// after the grouping kernels skipped inconsistent result buffers).
+// A grouped gradient row, or -1 when it lies outside the gradient rows (a
+// position in no bag, or inconsistent result buffers the grouping skipped).
 __device__ __forceinline__ int valid_pos(const BackwardParams& p, int v) {
-  return (unsigned)v < (unsigned long long)p.n ? v : -1;
+  return (unsigned)v < (unsigned long long)p.grad_rows ? v : -1;
 }
-__device__ __forceinline__ bool pos_ok(const BackwardParams& p, int v) { return (unsigned)v < (unsigned long long)p.n; }
+__device__ __forceinline__ bool pos_ok(const BackwardParams& p, int v) {
+  return (unsigned)v < (unsigned long long)p.grad_rows;
+}
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
@@ -875,8 +879,7 @@ cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
   }
   if (p.ntiles > 0 && p.ranks != nullptr) {
     MT_LAUNCH("k_bw_scatter", s);
-    const long long blocks = (p.n + 255) / 256;
-    k_bw_scatter<<<(int)(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, s>>>(p);
+    k_bw_scatter<<<grid_for(p.n, 256, 16), 256, 0, s>>>(p);
   } else if (p.ntiles > 0) {
     MT_LAUNCH("k_bw_fill", s);
     k_bw_fill<<<p.ntiles, kThreads, 0, s>>>(p);

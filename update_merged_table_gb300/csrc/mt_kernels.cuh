@@ -81,6 +81,8 @@ constexpr int kScanThreads = 256;
 struct BackwardParams {
   TableDev T;
   long long n;
+  const int32_t* pos_map;  // nullable: gradient row of each position (-1: none); NULL means row = position
+  long long grad_rows;     // rows of `grads` (n, or the number of bags)
   const int32_t* inverse;
   const int32_t* ranks;  // nullable: rank of each position among its unique's positions
   const int32_t* counts;
@@ -116,6 +118,27 @@ struct BackwardWsLayout {
 BackwardWsLayout backward_ws_layout(long long n, uint32_t dim);
 int backward_team_shift(uint32_t dim, int row_dtype);
 cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s);
+
+// ---- pooled bags ---------------------------------------------------------------
+
+struct PoolParams {
+  TableDev T;
+  long long n;
+  const int32_t* inverse;
+  const int32_t* unique_rows;
+  const long long* num_unique;
+  const long long* bag_offsets;  // [num_bags + 1] device
+  long long num_bags;
+  int mode;                      // MT_POOL_SUM or MT_POOL_MEAN
+  int team_shift;                // log2 lanes per team (VEC columns per lane)
+  float* out;                    // [num_bags, d]
+  double* acc;                   // [num_bags, d] workspace: sums of bags split over chunks
+};
+cudaError_t launch_pool(const PoolParams& p, cudaStream_t s);
+cudaError_t launch_pos_bag(const long long* bo, long long B, long long n, int32_t* pos_bag, Header* hdr,
+                           cudaStream_t s);
+cudaError_t launch_pool_scale(const long long* bo, long long B, int d, const float* dpooled, float* dscaled,
+                              cudaStream_t s);
 
 // ---- table maintenance --------------------------------------------------------
 
@@ -162,6 +185,19 @@ inline int current_device() {
   int d = -1;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
   return d;
+}
+
+// Streaming multiprocessors of the current device (queried once per device).
+int sm_count();
+
+// Blocks of `threads` for `work` items, capped at `per_sm` blocks per SM
+// (grid-stride kernels loop over the rest).
+inline int grid_for(long long work, int threads, int per_sm) {
+  long long g = (work + threads - 1) / threads;
+  const long long cap = (long long)sm_count() * per_sm;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
 }
 
 }  // namespace mt

@@ -1,0 +1,261 @@
+// Pooled embeddings of jagged bags and the pooled backward.
+//
+// A bag is a run of consecutive positions [bag_offsets[b], bag_offsets[b+1])
+// of a lookup batch: in the jagged sequence batches of "MTGR" section 5 (Load
+// Balance: user behaviour sequences of very different lengths) one bag is one
+// user's tokens of one feature.  The bag's pooled embedding is the sum (or the
+// mean) of the rows of its positions' keys.  The backward hands every
+// position its bag's gradient (times 1/len for the mean) and feeds the table's
+// per-unique reduction and Adam directly: no per-position gradient rows are
+// ever written.
+//
+// Kernels:
+//  k_pool         positions in chunks of kPoolChunk, a team of lanes per
+//                 chunk (VEC columns per lane), rows summed as exact fp32
+//                 pairs (TwoSum); a bag that lies inside one chunk is written
+//                 at once, the pieces of a longer bag meet in an fp64
+//                 accumulator.
+//  k_pool_finish  bags split over chunks (and empty bags): rounded from the
+//                 fp64 accumulator.
+//  k_pos_bag      backward: the bag of every position (-1: in no bag).
+//  k_pool_scale   backward of the mean: each bag's gradient times
+//                 fp32(1/len), rounded once.
+#include "mt_kernels.cuh"
+
+namespace mt {
+
+namespace {
+
+constexpr int kPoolChunk = 64;        // positions per chunk (one team)
+constexpr int kPoolMinTeamShift = 2;  // teams of at least 4 lanes
+
+// s + e = a + b exactly (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum1(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// The bag holding position i: the last b with bo[b] <= i (-1 when i lies
+// before every bag; b may be >= B when it lies after all of them).
+__device__ __forceinline__ long long bag_of(const long long* bo, long long B, long long i) {
+  long long lo = -1, hi = B + 1;  // bo[lo] <= i < bo[hi] with bo[-1] = -inf, bo[B+1] = +inf
+  while (hi - lo > 1) {
+    const long long mid = (lo + hi) >> 1;
+    if (__ldg(&bo[mid]) <= i) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Round a bag's sum (or mean) from double to fp32 into out[b, col .. col + VEC).
+template <int VEC>
+__device__ __forceinline__ void store_pooled(const PoolParams& p, long long b, int col, const double* s, long long len) {
+  float o[VEC];
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) o[j] = (float)(p.mode == MT_POOL_MEAN && len > 0 ? s[j] / (double)len : s[j]);
+  float4* dst = reinterpret_cast<float4*>(p.out + (size_t)b * p.T.dim + col);
+#pragma unroll
+  for (int q = 0; q < VEC / 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+}
+
+// VEC columns of a stored row as fp32 (bf16 widens exactly).
+template <int RD, int VEC>
+__device__ __forceinline__ void load_row_cols(const TableDev& T, int32_t row, int col, float v[VEC]) {
+  const char* rec = row_ptr(T, row);
+  if (RD == MT_F32) {
+    const float4 t = __ldg(reinterpret_cast<const float4*>(rec) + col / 4);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+    const uint4 t = __ldg(reinterpret_cast<const uint4*>(rec) + col / 8);
+    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[2 * q] = __uint_as_float(w[q] << 16);
+      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int RD>
+__global__ void __launch_bounds__(256) k_pool(const PoolParams p) {
+  constexpr int VEC = RD == MT_F32 ? 4 : 8;
+  constexpr int UNR = 32 / VEC;  // rows in flight per lane
+  __shared__ int32_t s_row[(256 >> kPoolMinTeamShift) * kPoolChunk];  // per team: the rows of its chunk
+  const int team_shift = p.team_shift;
+  const int team = 1 << team_shift;
+  const int lane = threadIdx.x & 31;
+  const int lt = lane & (team - 1);
+  const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << (lane & ~(team - 1)));
+  int32_t* my_row = s_row + (threadIdx.x >> team_shift) * kPoolChunk;
+  const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
+  const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
+  const long long nchunks = (p.n + kPoolChunk - 1) / kPoolChunk;
+  const long long U = *p.num_unique;
+  const int d = (int)p.T.dim;
+
+  for (long long c = gteam; c < nchunks; c += nteam) {  // uniform per team
+    const long long p0 = c * kPoolChunk, p1 = min(p0 + kPoolChunk, p.n);
+    // the chunk's rows (-1: nothing to add)
+    for (int q = lt; q < p1 - p0; q += team) {
+      const int32_t u = __ldg(&p.inverse[p0 + q]);
+      my_row[q] = (u >= 0 && u < U) ? __ldg(&p.unique_rows[u]) : -1;
+    }
+    __syncwarp(team_mask);
+    const long long b_first = bag_of(p.bag_offsets, p.num_bags, p0);
+    for (int c0 = 0; c0 < d; c0 += team * VEC) {
+      const int col = c0 + lt * VEC;
+      const bool active = col < d;
+      long long b = b_first < 0 ? 0 : b_first;
+      long long b_end = b < p.num_bags ? __ldg(&p.bag_offsets[b + 1]) : p1;
+      float hi[VEC], lo[VEC];
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.0f;
+      // a bag's sum leaves the running pair: written out when the whole bag lies in this chunk, else added
+      // to the bag's fp64 accumulator
+      auto flush = [&](long long bb, long long bend) {
+        if (bb < 0 || bb >= p.num_bags || !active) return;
+        const long long bstart = __ldg(&p.bag_offsets[bb]);
+        double s[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) s[j] = (double)hi[j] + (double)lo[j];
+        if (bstart >= p0 && bend <= p1 && bend > bstart) {
+          store_pooled<VEC>(p, bb, col, s, bend - bstart);
+        } else {
+          double* a = p.acc + (size_t)bb * d + col;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) atomicAdd(a + j, s[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.0f;
+      };
+      for (long long i0 = p0; i0 < p1; i0 += UNR) {
+        float v[UNR][VEC];
+#pragma unroll
+        for (int r = 0; r < UNR; ++r) {
+          const long long i = i0 + r;
+          const int32_t row = i < p1 ? my_row[i - p0] : -1;
+          if (active && row >= 0) load_row_cols<RD, VEC>(p.T, row, col, v[r]);
+          else {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) v[r][j] = 0.0f;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < UNR; ++r) {
+          const long long i = i0 + r;
+          if (i >= p1) break;
+          while (b < p.num_bags && i >= b_end) {  // position i starts a later bag
+            flush(b, b_end);
+            ++b;
+            b_end = b < p.num_bags ? __ldg(&p.bag_offsets[b + 1]) : p1;
+          }
+          if (b >= p.num_bags || (b_first < 0 && i < __ldg(&p.bag_offsets[0]))) continue;  // in no bag
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            float s, e;
+            two_sum1(hi[j], v[r][j], s, e);
+            hi[j] = s;
+            lo[j] = __fadd_rn(lo[j], e);
+          }
+        }
+      }
+      if (b < p.num_bags) flush(b, b_end);
+    }
+    __syncwarp(team_mask);  // my_row is refilled by the next chunk
+  }
+}
+
+// Bags that k_pool could not write at once: a bag split over chunks takes
+// its fp64 accumulator, an empty bag zeros.  Offsets that decrease or leave
+// [0, n] latch MT_EINVAL (the bag is then written as zeros).
+__global__ void __launch_bounds__(256) k_pool_finish(const PoolParams p) {
+  const int d = (int)p.T.dim;
+  const long long total = p.num_bags * d;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const long long b = it / d;
+    const int j = (int)(it - b * d);
+    const long long s = __ldg(&p.bag_offsets[b]), e = __ldg(&p.bag_offsets[b + 1]);
+    const bool bad = s < 0 || e < s || e > p.n;
+    if (bad && j == 0) latch_error(p.T.hdr, MT_EINVAL);
+    const bool one_chunk = !bad && e > s && s / kPoolChunk == (e - 1) / kPoolChunk;
+    if (one_chunk) continue;  // written by k_pool
+    float o = 0.0f;
+    if (!bad && e > s) {
+      const double a = __ldcg(&p.acc[(size_t)b * d + j]);
+      o = (float)(p.mode == MT_POOL_MEAN ? a / (double)(e - s) : a);
+    }
+    p.out[(size_t)b * d + j] = o;
+  }
+}
+
+// The bag of every position: a warp per bag writes its positions (the
+// positions were set to -1 beforehand).  Offsets that decrease or leave
+// [0, n] latch MT_EINVAL; the writes stay inside [0, n).
+__global__ void __launch_bounds__(256) k_pos_bag(const long long* bo, long long B, long long n, int32_t* pos_bag,
+                                                 Header* hdr) {
+  const int lane = threadIdx.x & 31;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long b = gw; b < B; b += nw) {
+    long long s = __ldg(&bo[b]), e = __ldg(&bo[b + 1]);
+    if ((s < 0 || e < s || e > n) && lane == 0) latch_error(hdr, MT_EINVAL);
+    s = s < 0 ? 0 : (s > n ? n : s);
+    e = e < s ? s : (e > n ? n : e);
+    for (long long i = s + lane; i < e; i += 32) pos_bag[i] = (int32_t)b;
+  }
+}
+
+// dscaled[b] = dpooled[b] * fp32(1/len_b), one rounding per product (the
+// gradient every position of a mean-pooled bag receives).
+__global__ void __launch_bounds__(256) k_pool_scale(const long long* bo, long long B, int d, const float* dpooled,
+                                                    float* dscaled) {
+  const long long total = B * d;
+  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (long long)gridDim.x * blockDim.x) {
+    const long long b = it / d;
+    const long long len = __ldg(&bo[b + 1]) - __ldg(&bo[b]);
+    const float s = len > 0 ? __frcp_rn((float)len) : 1.0f;
+    dscaled[it] = __fmul_rn(__ldg(&dpooled[it]), s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pool(const PoolParams& p, cudaStream_t s) {
+  if (p.num_bags == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(p.acc, 0, (size_t)p.num_bags * p.T.dim * sizeof(double), s);
+  if (e != cudaSuccess) return e;
+  if (p.n > 0) {
+    const long long chunks = (p.n + kPoolChunk - 1) / kPoolChunk;
+    const long long teams_per_block = 256 >> p.team_shift;
+    MT_LAUNCH("k_pool", s);
+    const int grid = grid_for(chunks * (256 / teams_per_block), 256, 16);
+    if (p.T.row_dtype == MT_F32) k_pool<MT_F32><<<grid, 256, 0, s>>>(p);
+    else k_pool<MT_BF16><<<grid, 256, 0, s>>>(p);
+  }
+  {
+    MT_LAUNCH("k_pool_finish", s);
+    k_pool_finish<<<grid_for(p.num_bags * p.T.dim, 256, 16), 256, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pos_bag(const long long* bo, long long B, long long n, int32_t* pos_bag, Header* hdr,
+                           cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(pos_bag, 0xFF, (size_t)(n > 0 ? n : 1) * 4, s);
+  if (e != cudaSuccess || B == 0) return e;
+  MT_LAUNCH("k_pos_bag", s);
+  k_pos_bag<<<grid_for(B * 32, 256, 16), 256, 0, s>>>(bo, B, n, pos_bag, hdr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pool_scale(const long long* bo, long long B, int d, const float* dpooled, float* dscaled,
+                              cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+  MT_LAUNCH("k_pool_scale", s);
+  k_pool_scale<<<grid_for(B * d, 256, 16), 256, 0, s>>>(bo, B, d, dpooled, dscaled);
+  return cudaGetLastError();
+}
+
+}  // namespace mt

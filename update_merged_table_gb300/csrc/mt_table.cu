@@ -287,13 +287,6 @@ __global__ void k_read_rows(const TableDev T, const int32_t* rows, long long n, 
   }
 }
 
-int grid_for(long long work, int threads) {
-  long long g = (work + threads - 1) / threads;
-  if (g < 1) g = 1;
-  if (g > 152 * 32) g = 152 * 32;
-  return (int)g;
-}
-
 }  // namespace
 
 cudaError_t launch_table_init(const TableDev& T, cudaStream_t s) {
@@ -303,7 +296,7 @@ cudaError_t launch_table_init(const TableDev& T, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_table_init", s);
-    k_table_init<<<grid_for(T.num_rows, 256), 256, 0, s>>>(T);
+    k_table_init<<<grid_for(T.num_rows, 256, 32), 256, 0, s>>>(T);
   }
   return cudaGetLastError();
 }
@@ -313,11 +306,11 @@ cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long
   if (n == 0) return cudaSuccess;
   {
     MT_LAUNCH("k_erase_find", s);
-    k_erase_find<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot);
+    k_erase_find<<<grid_for(n, 256, 32), 256, 0, s>>>(T, keys, n, ws_slot);
   }
   {
     MT_LAUNCH("k_erase_apply", s);
-    k_erase_apply<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_slot, found);
+    k_erase_apply<<<grid_for(n, 256, 32), 256, 0, s>>>(T, keys, n, ws_slot, found);
   }
   return cudaGetLastError();
 }
@@ -332,11 +325,11 @@ cudaError_t launch_compact(const TableDev& T, void* ws, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_compact_rebuild", s);
-    k_compact_rebuild<<<grid_for((long long)M, 256), 256, 0, s>>>(T, fresh, fail);
+    k_compact_rebuild<<<grid_for((long long)M, 256, 32), 256, 0, s>>>(T, fresh, fail);
   }
   {
     MT_LAUNCH("k_compact_commit", s);
-    k_compact_commit<<<grid_for((long long)M, 256), 256, 0, s>>>(T, fresh, fail);
+    k_compact_commit<<<grid_for((long long)M, 256, 32), 256, 0, s>>>(T, fresh, fail);
   }
   return cudaGetLastError();
 }
@@ -346,7 +339,7 @@ cudaError_t launch_stats(const TableDev& T, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_stats", s);
-    k_stats<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T);
+    k_stats<<<grid_for((long long)(T.mask + 1), 256, 32), 256, 0, s>>>(T);
   }
   return cudaGetLastError();
 }
@@ -357,7 +350,7 @@ cudaError_t launch_export(const TableDev& T, unsigned long long* keys, int32_t* 
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_export", s);
-    k_export<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T, keys, rows, capacity);
+    k_export<<<grid_for((long long)(T.mask + 1), 256, 32), 256, 0, s>>>(T, keys, rows, capacity);
   }
   return cudaGetLastError();
 }
@@ -367,11 +360,11 @@ cudaError_t launch_import(const TableDev& T, const unsigned long long* keys, lon
   if (n == 0) return cudaSuccess;
   {
     MT_LAUNCH("k_import_resolve", s);
-    k_import_resolve<<<grid_for(n, 256), 256, 0, s>>>(T, keys, n, ws_rows);
+    k_import_resolve<<<grid_for(n, 256, 32), 256, 0, s>>>(T, keys, n, ws_rows);
   }
   {
     MT_LAUNCH("k_import_write", s);
-    k_import_write<<<grid_for(n * T.dim, 256), 256, 0, s>>>(T, ws_rows, n, emb, m, v);
+    k_import_write<<<grid_for(n * T.dim, 256, 32), 256, 0, s>>>(T, ws_rows, n, emb, m, v);
   }
   return cudaGetLastError();
 }
@@ -384,7 +377,7 @@ cudaError_t launch_grow(const TableDev& T, const TableDev& T2, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (T2.num_rows > T.num_rows) {
     MT_LAUNCH("k_grow_rows", s);
-    k_grow_rows<<<grid_for(T2.num_rows - T.num_rows, 256), 256, 0, s>>>(T2, T.num_rows);
+    k_grow_rows<<<grid_for(T2.num_rows - T.num_rows, 256, 32), 256, 0, s>>>(T2, T.num_rows);
   }
   {
     MT_LAUNCH("k_grow_top", s);
@@ -392,7 +385,7 @@ cudaError_t launch_grow(const TableDev& T, const TableDev& T2, cudaStream_t s) {
   }
   {
     MT_LAUNCH("k_grow_rebuild", s);
-    k_grow_rebuild<<<grid_for((long long)(T.mask + 1), 256), 256, 0, s>>>(T, T2);
+    k_grow_rebuild<<<grid_for((long long)(T.mask + 1), 256, 32), 256, 0, s>>>(T, T2);
   }
   return cudaGetLastError();
 }
@@ -402,7 +395,7 @@ cudaError_t launch_read_rows(const TableDev& T, const int32_t* rows, long long n
   if (n == 0) return cudaSuccess;
   {
     MT_LAUNCH("k_read_rows", s);
-    k_read_rows<<<grid_for(n * T.dim, 256), 256, 0, s>>>(T, rows, n, emb, m, v);
+    k_read_rows<<<grid_for(n * T.dim, 256, 32), 256, 0, s>>>(T, rows, n, emb, m, v);
   }
   return cudaGetLastError();
 }
