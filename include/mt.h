@@ -132,17 +132,38 @@ typedef struct {
 
 /* ---- table ------------------------------------------------------------- */
 
-/* Device bytes the table arena needs: a header, M 16-byte slots {key, row,
- * insert step}, the row free list (R int32) and R row records
- * [emb d x row dtype | m d x fp32 | v d x fp32], each padded to 16 bytes.
- * Returns 0 for an invalid configuration. */
+/* A table lives in caller-owned device memory in two kinds of parts: one key
+ * store (a header, M 16-byte slots {key, row, insert step} and the row free
+ * list, R int32) and up to MT_MAX_ROW_SEGMENTS row segments holding the row
+ * records [emb d x row dtype | m d x fp32 | v d x fp32], each part padded to
+ * 16 bytes.  Keys lead to rows through the key store only (MTGR section 5,
+ * Embedding Management), so growing the table or compacting its key store
+ * rebuilds the key store and never moves a row. */
+#define MT_MAX_ROW_SEGMENTS 8
+
+/* Bytes of a single arena holding the key store followed by all R rows (the
+ * layout mt_table_create uses).  Returns 0 for an invalid configuration. */
 size_t mt_table_bytes(const mt_config* cfg);
+
+/* Bytes of the key store alone for `cfg` (header, M slots, free list of
+ * cfg->num_rows entries).  Returns 0 for an invalid configuration. */
+size_t mt_keystore_bytes(const mt_config* cfg);
+
+/* Bytes of a row segment of `rows` records for `cfg`'s dim and row dtype. */
+size_t mt_rows_bytes(const mt_config* cfg, int64_t rows);
 
 /* Build a table in caller-owned device memory `dev_mem` (>= mt_table_bytes
  * bytes, 256-byte aligned; owned by the caller and used by the table until
- * it is destroyed).  Marks every slot EMPTY and every row free, enqueued on
- * `stream`.  *out receives a host handle. */
+ * it is destroyed): the key store first, then one row segment of all R rows.
+ * Marks every slot EMPTY and every row free, enqueued on `stream`.  *out
+ * receives a host handle. */
 int mt_table_create(const mt_config* cfg, void* dev_mem, size_t bytes, mt_stream stream, mt_table** out);
+
+/* The same with the key store and the rows in separate caller-owned buffers:
+ * `keystore` (>= mt_keystore_bytes) and `rows` (>= mt_rows_bytes(cfg, R)),
+ * both 256-byte aligned and not overlapping. */
+int mt_table_create_split(const mt_config* cfg, void* keystore, size_t keystore_bytes, void* rows,
+                          size_t rows_bytes, mt_stream stream, mt_table** out);
 
 /* Free the host handle (not the arena). */
 int mt_table_destroy(mt_table* t);
@@ -281,35 +302,45 @@ int mt_erase(mt_table* t, const uint64_t* keys, int64_t n, uint8_t* found, void*
 
 /* ---- inspection ------------------------------------------------------------ */
 
-/* Capacity expansion: move the table into a new arena `dev_mem` laid out
- * for `new_cfg` (from mt_table_bytes(new_cfg)), which may have more slots
- * (log2_slots) and more rows (num_rows) but must otherwise equal the
- * table's configuration (dim, row dtype, probe step, seeds, init scale,
- * flags; max_probes 0 means the new M).  The header, the Adam state and
- * every row are copied (row indices do not change), the new rows join the
- * free list, and every live key is inserted again along its probe sequence
- * in the larger slot array (the key store is rebuilt on its own: MTGR
- * section 5, Embedding Management).  Synchronises `stream`.  On success
- * the handle uses the new arena and the caller may free the old one; if a
- * key does not fit within the new max_probes, MT_EFULL is returned and the
- * handle keeps the old arena, unchanged. */
-int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* dev_mem, size_t bytes, mt_stream stream);
+/* Capacity expansion (MTGR section 5, Embedding Management: the key store is
+ * replicated, the embeddings are not).  new_cfg may have more slots
+ * (log2_slots) and more rows (num_rows) but must otherwise equal the table's
+ * configuration (dim, row dtype, probe step, seeds, init scale, flags;
+ * max_probes 0 means the new M).  A new key store is built in `keystore`
+ * (>= mt_keystore_bytes(new_cfg), 256-byte aligned, overlapping none of the
+ * table's memory): the header and the Adam state are copied, the free list
+ * is copied and extended by the new rows, and every live key is inserted
+ * again along its probe sequence in the larger slot array.  The new rows
+ * (new_cfg->num_rows - R of them) form a new row segment in `rows`
+ * (>= mt_rows_bytes(new_cfg, new R - R) bytes; NULL when no rows are added);
+ * existing rows stay where they are, with the same row indices.  At most
+ * MT_MAX_ROW_SEGMENTS segments (else MT_EINVAL).  Synchronises `stream`.  On
+ * success the table uses the new key store, and the old one (which the caller
+ * may free, unless it shares an allocation with rows) is no longer read.  If
+ * a key does not fit within the new max_probes, MT_EFULL is returned and the
+ * table keeps its old key store, unchanged.  CUDA graphs captured before the
+ * call must be captured again. */
+int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* keystore, size_t keystore_bytes, void* rows,
+                  size_t rows_bytes, mt_stream stream);
 
-/* Workspace bytes mt_compact needs: one slot array of the table (M x 16 B)
- * plus 256 bytes. */
+/* Bytes of the slot array mt_compact needs: M x 16. */
 size_t mt_compact_workspace_bytes(const mt_table* t);
 
-/* Tombstone compaction of the key store (the key store can be rebuilt on its
- * own: MTGR section 5, Embedding Management).  Every live key is inserted
- * again, with its row and insertion step, along its probe sequence
- * h_t = (h0 + t*S) mod M into a fresh slot array in ws, which then replaces
- * the table's slots.  Tombstones disappear and chains shorten; rows, the
- * free list, the step counter and every key's row stay as they were.  If a
- * key would need more than max_probes probes in the new order (possible
- * only with a small max_probes), the table is left unchanged and MT_EFULL is
- * latched.  Stream-ordered; no other call may run on the table meanwhile.
- *  ws   device, >= mt_compact_workspace_bytes(t), 256-byte aligned. */
-int mt_compact(mt_table* t, void* ws, size_t ws_bytes, mt_stream stream);
+/* Tombstone compaction of the key store.  Every live key is inserted again,
+ * with its row and insertion step, along its probe sequence
+ * h_t = (h0 + t*S) mod M into the fresh slot array `ws` (>=
+ * mt_compact_workspace_bytes, 256-byte aligned, not the table's slots),
+ * which then becomes the table's slot array: no slots are copied back.
+ * Tombstones disappear and chains shorten; rows, the free list, the step
+ * counter and every key's row stay as they were.  On success *released
+ * receives the slot array the table used before: that memory belongs to the
+ * caller again (it lies in the caller's key store, or in an earlier `ws`)
+ * and may serve as the next call's `ws`; `ws` must stay allocated while the
+ * table uses it.  If a key would need more than max_probes probes in the new
+ * order (possible only with a small max_probes), MT_EFULL is returned and the
+ * table is unchanged (*released = NULL).  Synchronises `stream`.  CUDA graphs
+ * captured before the call must be captured again. */
+int mt_compact(mt_table* t, void* ws, size_t ws_bytes, void** released, mt_stream stream);
 
 /* Scan the key store: live keys, tombstones, and each live key's probe index
  * t = (slot - h0) * S^-1 mod M (S is odd, so S^-1 mod 2^n exists; MTGenRec

@@ -85,6 +85,30 @@ def test_odd_steps_accepted(lib):
         assert lib.mt_table_bytes(ctypes.byref(_cfg(probe_step=S))) > 0
 
 
+def test_keystore_and_rows_bytes(lib):
+    c = _cfg(log2_slots=10, dim=16)
+    ks = lib.mt_keystore_bytes(ctypes.byref(c))
+    assert ks == 1024 + 1024 * 16 + 1024 * 4  # header, slots, free list
+    assert lib.mt_rows_bytes(ctypes.byref(c), 1000) == 1000 * 16 * 4 * 3
+    assert lib.mt_rows_bytes(ctypes.byref(c), 3) == 768  # 3 x 192 B, padded to 256
+    assert lib.mt_table_bytes(ctypes.byref(c)) == ks + lib.mt_rows_bytes(ctypes.byref(c), 1024)
+    assert lib.mt_rows_bytes(ctypes.byref(c), -1) == 0
+
+
+def test_create_split_checks_buffers(lib):
+    c = _cfg(log2_slots=10, dim=16)
+    h = ctypes.c_void_p()
+    ks = lib.mt_keystore_bytes(ctypes.byref(c))
+    rb = lib.mt_rows_bytes(ctypes.byref(c), 1024)
+    assert lib.mt_table_create_split(ctypes.byref(c), None, ks, 1 << 20, rb, None, ctypes.byref(h)) == mt.MT_ENOSPACE
+    assert lib.mt_table_create_split(ctypes.byref(c), 1 << 20, ks - 1, 1 << 30, rb, None,
+                                     ctypes.byref(h)) == mt.MT_ENOSPACE
+    # the key store and the rows must not overlap (checked before any device call)
+    assert lib.mt_table_create_split(ctypes.byref(c), 1 << 20, ks, (1 << 20) + 256, rb, None,
+                                     ctypes.byref(h)) == mt.MT_EINVAL
+    assert not h.value
+
+
 def test_create_needs_space(lib):
     c = _cfg()
     h = ctypes.c_void_p()
@@ -103,8 +127,8 @@ def test_null_handles_rejected(lib):
     assert lib.mt_step(None) == -1
     assert lib.mt_lookup_workspace_bytes(None, 10) == 0
     assert lib.mt_erase_workspace_bytes(1000) >= 4000
-    assert lib.mt_compact(None, None, 0, None) == mt.MT_EINVAL
-    assert lib.mt_table_grow(None, None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_compact(None, None, 0, None, None) == mt.MT_EINVAL
+    assert lib.mt_table_grow(None, None, None, 0, None, 0, None) == mt.MT_EINVAL
     assert lib.mt_compact_workspace_bytes(None) == 0
     assert lib.mt_import(None, None, 0, None, None, None, None, 0, None) == mt.MT_EINVAL
     assert lib.mt_import_workspace_bytes(1000) >= 4000 and lib.mt_import_workspace_bytes(-1) == 0

@@ -6,6 +6,8 @@ slot placement is not compared).  Within tolerance: gradient sums and
 Adam-updated rows (fp32 rows 1e-5 relative + 1e-6 absolute; bf16 rows within
 one bf16 ulp), as the table's specification fixes.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -327,6 +329,14 @@ def test_compact_drops_tombstones_and_keeps_rows(probe_step):
     assert torch.equal(after.unique_rows[:U], urows_before)
     assert torch.equal(after.rows, rows_before)
     run_steps(tab, ref, [W.single_feature(rng.choice(1 << 20, 3000).astype(np.int64))], seed0=50)
+    # the slot array now lives in the first spare; a second compaction goes back into the key store's
+    tab.erase(to_dev(ids[1::2].copy()))
+    ref.erase(ids[1::2].astype(np.uint64))
+    first_home = tab._slots_buf.data_ptr()
+    tab.compact()
+    assert tab._slots_buf.data_ptr() != first_home and tab.stats()["tombstones"] == 0
+    assert tab.stats()["live"] == ref.live
+    run_steps(tab, ref, [W.single_feature(rng.choice(1 << 20, 3000).astype(np.int64))], seed0=51)
 
 
 @pytest.mark.parametrize("row_dtype", ["f32", "bf16"])
@@ -371,14 +381,17 @@ def test_grow_keeps_keys_rows_and_training():
     and training continues in step with the oracle."""
     rng = np.random.default_rng(13)
     tab = mt.Table(10, 8, probe_step=3, init_seed=5)
-    ref = oracle.Table(12, 8, probe_step=3, init_seed=5)  # its capacity never binds in this test
+    ref = oracle.Table(13, 8, probe_step=3, init_seed=5)  # its capacity never binds in this test
     ids = rng.choice(1 << 20, 600, replace=False).astype(np.int64)
     run_steps(tab, ref, [W.single_feature(ids)], seed0=60)
     before = tab.lookup(to_dev(ids), insert_missing=False)
     U = before.U
     rows_before, urows_before = before.rows.clone(), before.unique_rows[:U].clone()
     st0, state0 = tab.stats(), tab.adam_state()
+    ks_old = tab.lib.mt_keystore_bytes(ctypes.byref(tab.cfg))
+    rows_before_grow = tab.arena[ks_old:].clone()  # the first row segment lives after the key store
     tab.grow(12)
+    assert torch.equal(tab.arena[ks_old:], rows_before_grow)  # no row was moved or rewritten
     st1 = tab.stats()
     assert tab.error() == 0 and tab.adam_state() == state0
     assert st1["capacity"] == 4096 and st1["live"] == st0["live"] == 600 and st1["tombstones"] == 0
@@ -387,6 +400,13 @@ def test_grow_keeps_keys_rows_and_training():
     assert after.U == U and torch.equal(after.unique_rows[:U], urows_before) and torch.equal(after.rows, rows_before)
     more = np.concatenate([ids[:300], rng.choice(1 << 20, 2000).astype(np.int64)])
     run_steps(tab, ref, [W.single_feature(more)], seed0=61)  # 2600 keys: more than the old table held
+    assert not torch.equal(tab.arena[ks_old:], rows_before_grow)  # the old keys' rows trained in place
+    # a second expansion adds a second new row segment; a compaction then moves the slot array
+    tab.grow(13, num_rows=6000)
+    assert tab.stats()["rows_free"] == 6000 - ref.live and len(tab._row_bufs) == 3
+    tab.compact()
+    run_steps(tab, ref, [W.single_feature(rng.choice(1 << 20, 1500).astype(np.int64))], seed0=62)
+    assert tab.error() == 0 and tab.stats()["live"] == ref.live
 
 
 def test_step_counter_and_lazy_rows():

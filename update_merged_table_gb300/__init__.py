@@ -77,7 +77,10 @@ ABI_FUNCTIONS = {
     "mt_table_create": (_I32, [_P, _P, _SZ, _P, _P]),
     "mt_table_destroy": (_I32, [_P]),
     "mt_table_config": (_I32, [_P, _P]),
-    "mt_table_grow": (_I32, [_P, _P, _P, _SZ, _P]),
+    "mt_table_grow": (_I32, [_P, _P, _P, _SZ, _P, _SZ, _P]),
+    "mt_keystore_bytes": (_SZ, [_P]),
+    "mt_rows_bytes": (_SZ, [_P, _I64]),
+    "mt_table_create_split": (_I32, [_P, _P, _SZ, _P, _SZ, _P, _P]),
     "mt_lookup_workspace_bytes": (_SZ, [_P, _I64]),
     "mt_lookup": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "mt_lookup_static": (_I32, [_P, _P, _I64, _P, _P, _I32, _I32, _P, _P, _P]),
@@ -90,7 +93,7 @@ ABI_FUNCTIONS = {
     "mt_erase_workspace_bytes": (_SZ, [_I64]),
     "mt_erase": (_I32, [_P, _P, _I64, _P, _P, _SZ, _P]),
     "mt_compact_workspace_bytes": (_SZ, [_P]),
-    "mt_compact": (_I32, [_P, _P, _SZ, _P]),
+    "mt_compact": (_I32, [_P, _P, _SZ, _P, _P]),
     "mt_stats": (_I32, [_P, _P, _P]),
     "mt_export": (_I32, [_P, _P, _P, _I64, _P, _P]),
     "mt_read_rows": (_I32, [_P, _P, _I64, _P, _P, _P, _P]),
@@ -228,6 +231,12 @@ class Table:
         with torch.cuda.device(self.device):
             _check(self.lib.mt_table_create(ctypes.byref(self.cfg), self.arena.data_ptr(), nbytes, _stream(stream),
                                             ctypes.byref(self.h)), "mt_table_create")
+        # device memory the table uses: row segments (the arena holds the first), the key store, the slot
+        # array when compaction moved it out of the key store, and a spare slot array for the next compaction
+        self._row_bufs = [self.arena]
+        self._keystore = self.arena
+        self._slots_buf = None
+        self._spare = None
         out = _Config()
         _check(self.lib.mt_table_config(self.h, ctypes.byref(out)), "mt_table_config")
         self.cfg = out
@@ -381,27 +390,52 @@ class Table:
         return bag_offsets
 
     def grow(self, log2_slots: int, num_rows: int = 0, stream=None):
-        """Capacity expansion into a new arena with 2^log2_slots slots and num_rows rows
-        (0 = one per slot); keys, rows and the Adam state carry over."""
+        """Capacity expansion to 2^log2_slots slots and num_rows rows (0 = one per slot): a new key store
+        is built and the added rows come as a new row segment; no row moves."""
         torch = _torch()
         c = _Config(log2_slots, self.cfg.dim, self.cfg.row_dtype, 0, self.cfg.probe_step, self.cfg.hash_seed,
                     self.cfg.init_seed, self.cfg.init_scale, self.cfg.flags, num_rows)
-        nbytes = self.lib.mt_table_bytes(ctypes.byref(c))
-        if nbytes == 0:
-            raise MTError(MT_EINVAL, "mt_table_bytes")
-        arena = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
-        _check(self.lib.mt_table_grow(self.h, ctypes.byref(c), arena.data_ptr(), nbytes, _stream(stream)),
-               "mt_table_grow")
-        self.arena = arena  # the old arena is released with the last reference to it
+        ks_bytes = self.lib.mt_keystore_bytes(ctypes.byref(c))
+        if ks_bytes == 0:
+            raise MTError(MT_EINVAL, "mt_keystore_bytes")
+        new_rows = (num_rows or (1 << log2_slots)) - self.cfg.num_rows
+        ks = torch.empty(ks_bytes, dtype=torch.uint8, device=self.device)
+        rows = None
+        if new_rows > 0:
+            rows = torch.empty(self.lib.mt_rows_bytes(ctypes.byref(c), new_rows), dtype=torch.uint8,
+                               device=self.device)
+        _check(self.lib.mt_table_grow(self.h, ctypes.byref(c), ks.data_ptr(), ks_bytes,
+                                      rows.data_ptr() if rows is not None else None,
+                                      rows.numel() if rows is not None else 0, _stream(stream)), "mt_table_grow")
+        self._keystore = ks  # the old key store is released with its last reference (the arena stays: rows)
+        self._slots_buf = None
+        self._spare = None
+        if rows is not None:
+            self._row_bufs.append(rows)
         out = _Config()
         _check(self.lib.mt_table_config(self.h, ctypes.byref(out)), "mt_table_config")
         self.cfg = out
         self.log2_slots = log2_slots
 
     def compact(self, stream=None):
-        """Rebuild the key store without tombstones (rows and keys unchanged)."""
-        ws = self._workspace("compact", self.lib.mt_compact_workspace_bytes(self.h))
-        _check(self.lib.mt_compact(self.h, ws.data_ptr(), ws.numel(), _stream(stream)), "mt_compact")
+        """Rebuild the key store's slots without tombstones into a spare slot array, which becomes the
+        table's (rows and keys unchanged); the slot array used before becomes the next spare."""
+        torch = _torch()
+        need = self.lib.mt_compact_workspace_bytes(self.h)
+        spare = self._spare
+        if spare is None or spare.numel() < need:
+            spare = torch.empty(need, dtype=torch.uint8, device=self.device)
+        released = ctypes.c_void_p()
+        _check(self.lib.mt_compact(self.h, spare.data_ptr(), spare.numel(), ctypes.byref(released),
+                                   _stream(stream)), "mt_compact")
+        old = released.value
+        holder = None
+        for buf in (self._slots_buf, self._keystore):
+            if buf is not None and buf.data_ptr() <= old < buf.data_ptr() + buf.numel():
+                holder = buf[old - buf.data_ptr(): old - buf.data_ptr() + need]
+                break
+        self._slots_buf = spare
+        self._spare = holder
 
     def erase(self, keys, want_found: bool = True, stream=None):
         """Delete merged keys (int64 CUDA tensor holding the uint64 bit patterns)."""

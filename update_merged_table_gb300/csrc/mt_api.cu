@@ -25,8 +25,9 @@ int sm_count() {
 struct mt_table {
   mt_config cfg;
   mt::TableDev dev;
-  size_t arena_bytes;
-  long long step;  // host-side count of backward calls
+  char* ks_base;     // the key store in use (header at its start)
+  size_t ks_bytes;
+  long long step;    // host-side count of backward calls
 };
 
 namespace {
@@ -56,13 +57,14 @@ int normalise(const mt_config* in, mt_config* out) {
   return MT_OK;
 }
 
-struct ArenaLayout {
-  size_t hdr, slots, stack, rows, total;
+// Key store: [header 1 KiB][M slots x 16 B][free list: R x int32], each part 256-byte aligned.
+struct KeystoreLayout {
+  size_t hdr, slots, stack, total;
   uint32_t rec_bytes, emb_bytes, mv_bytes;
 };
 
-ArenaLayout arena_layout(const mt_config& c) {
-  ArenaLayout L{};
+KeystoreLayout keystore_layout(const mt_config& c) {
+  KeystoreLayout L{};
   const uint64_t M = 1ull << c.log2_slots;
   L.emb_bytes = c.dim * (c.row_dtype == MT_F32 ? 4u : 2u);
   L.mv_bytes = c.dim * 4u;
@@ -74,22 +76,28 @@ ArenaLayout arena_layout(const mt_config& c) {
   off = align_up(off + (size_t)M * sizeof(mt::Slot), 256);
   L.stack = off;
   off = align_up(off + (size_t)c.num_rows * 4, 256);
-  L.rows = off;
-  off = align_up(off + (size_t)c.num_rows * L.rec_bytes, 256);
   L.total = off;
   return L;
 }
 
+size_t rows_bytes_of(const mt_config& c, long long rows) {
+  const KeystoreLayout L = keystore_layout(c);
+  return align_up((size_t)rows * L.rec_bytes, 256);
+}
+
 uint64_t inverse_mod_2_64(uint64_t S);
 
-// The kernels' view of a table laid out by L in the arena at dev_mem.
-mt::TableDev device_view(const mt_config& c, const ArenaLayout& L, void* dev_mem) {
+// The kernels' view of a table whose key store is at `ks` and whose only row segment is `rows`.
+mt::TableDev device_view(const mt_config& c, void* ks, void* rows) {
+  const KeystoreLayout L = keystore_layout(c);
   mt::TableDev T{};
-  char* base = static_cast<char*>(dev_mem);
+  char* base = static_cast<char*>(ks);
   T.hdr = reinterpret_cast<mt::Header*>(base + L.hdr);
   T.slots = reinterpret_cast<mt::Slot*>(base + L.slots);
   T.free_stack = reinterpret_cast<int32_t*>(base + L.stack);
-  T.rows = base + L.rows;
+  T.seg_base[0] = static_cast<char*>(rows);
+  T.seg_first[0] = 0;
+  T.nseg = 1;
   const uint64_t M = 1ull << c.log2_slots;
   T.mask = M - 1;
   T.S = c.probe_step;
@@ -107,6 +115,38 @@ mt::TableDev device_view(const mt_config& c, const ArenaLayout& L, void* dev_mem
   T.init_scale = c.init_scale;
   T.num_rows = c.num_rows;
   return T;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Does [p, p + n) overlap any memory the table uses (key store, slots, row segments)?
+bool overlaps_table(const mt_table* t, const void* p, size_t n) {
+  if (overlap(p, n, t->ks_base, t->ks_bytes)) return true;
+  if (overlap(p, n, t->dev.slots, (size_t)(t->dev.mask + 1) * sizeof(mt::Slot))) return true;
+  for (int s = 0; s < t->dev.nseg; ++s) {
+    const long long end = s + 1 < t->dev.nseg ? t->dev.seg_first[s + 1] : t->dev.num_rows;
+    if (overlap(p, n, t->dev.seg_base[s], (size_t)(end - t->dev.seg_first[s]) * t->dev.rec_bytes)) return true;
+  }
+  return false;
+}
+
+int create_table(const mt_config& c, void* ks, void* rows, cudaStream_t stream, mt_table** out) {
+  mt_table* t = new (std::nothrow) mt_table();
+  if (t == nullptr) return MT_ECUDA;
+  t->cfg = c;
+  t->ks_base = static_cast<char*>(ks);
+  t->ks_bytes = keystore_layout(c).total;
+  t->step = 0;
+  t->dev = device_view(c, ks, rows);
+  if (mt::launch_table_init(t->dev, stream) != cudaSuccess) {
+    delete t;
+    return MT_ECUDA;
+  }
+  *out = t;
+  return MT_OK;
 }
 
 // S^-1 mod 2^64 by Newton's iteration x <- x(2 - Sx); exact for odd S.
@@ -220,7 +260,19 @@ const char* mt_strerror(int code) {
 size_t mt_table_bytes(const mt_config* cfg) {
   mt_config c;
   if (normalise(cfg, &c) != MT_OK) return 0;
-  return arena_layout(c).total;
+  return keystore_layout(c).total + rows_bytes_of(c, c.num_rows);
+}
+
+size_t mt_keystore_bytes(const mt_config* cfg) {
+  mt_config c;
+  if (normalise(cfg, &c) != MT_OK) return 0;
+  return keystore_layout(c).total;
+}
+
+size_t mt_rows_bytes(const mt_config* cfg, int64_t rows) {
+  mt_config c;
+  if (normalise(cfg, &c) != MT_OK || rows < 0 || rows > 0x7FFFFFFF) return 0;
+  return rows_bytes_of(c, rows);
 }
 
 int mt_table_create(const mt_config* cfg, void* dev_mem, size_t bytes, mt_stream stream, mt_table** out) {
@@ -229,25 +281,27 @@ int mt_table_create(const mt_config* cfg, void* dev_mem, size_t bytes, mt_stream
   mt_config c;
   const int rc = normalise(cfg, &c);
   if (rc != MT_OK) return rc;
-  const ArenaLayout L = arena_layout(c);
-  if (dev_mem == nullptr || bytes < L.total || !aligned(dev_mem, 256)) return MT_ENOSPACE;
-  mt_table* t = new (std::nothrow) mt_table();
-  if (t == nullptr) return MT_ECUDA;
-  t->cfg = c;
-  t->arena_bytes = L.total;
-  t->step = 0;
-  mt::TableDev& T = t->dev;
-  T = device_view(c, L, dev_mem);
-  const cudaError_t e = mt::launch_table_init(T, as_stream(stream));
-  if (e != cudaSuccess) {
-    delete t;
-    return MT_ECUDA;
-  }
-  *out = t;
-  return MT_OK;
+  const size_t ks = keystore_layout(c).total;
+  if (dev_mem == nullptr || bytes < ks + rows_bytes_of(c, c.num_rows) || !aligned(dev_mem, 256)) return MT_ENOSPACE;
+  return create_table(c, dev_mem, static_cast<char*>(dev_mem) + ks, as_stream(stream), out);
 }
 
-int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* dev_mem, size_t bytes, mt_stream stream) {
+int mt_table_create_split(const mt_config* cfg, void* keystore, size_t keystore_bytes, void* rows,
+                          size_t rows_bytes, mt_stream stream, mt_table** out) {
+  if (out == nullptr) return MT_EINVAL;
+  *out = nullptr;
+  mt_config c;
+  const int rc = normalise(cfg, &c);
+  if (rc != MT_OK) return rc;
+  const size_t ks = keystore_layout(c).total, rb = rows_bytes_of(c, c.num_rows);
+  if (keystore == nullptr || keystore_bytes < ks || !aligned(keystore, 256)) return MT_ENOSPACE;
+  if (rows == nullptr || rows_bytes < rb || !aligned(rows, 256)) return MT_ENOSPACE;
+  if (overlap(keystore, ks, rows, rb)) return MT_EINVAL;
+  return create_table(c, keystore, rows, as_stream(stream), out);
+}
+
+int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* keystore, size_t keystore_bytes, void* rows,
+                  size_t rows_bytes, mt_stream stream) {
   if (t == nullptr) return MT_EINVAL;
   mt_config c;
   const int rc = normalise(new_cfg, &c);
@@ -257,14 +311,25 @@ int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* dev_mem, size_t b
       c.hash_seed != o.hash_seed || c.init_seed != o.init_seed || c.init_scale != o.init_scale ||
       c.flags != o.flags || (c.probe_step & ((1ull << o.log2_slots) - 1)) != o.probe_step)
     return MT_EINVAL;
-  const ArenaLayout L = arena_layout(c);
-  if (dev_mem == nullptr || bytes < L.total || !aligned(dev_mem, 256)) return MT_ENOSPACE;
-  {  // the new arena must not overlap the old one: the rebuild reads the old slots while it writes the new
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(dev_mem), a1 = a0 + L.total;
-    const uintptr_t b0 = reinterpret_cast<uintptr_t>(t->dev.hdr), b1 = b0 + t->arena_bytes;
-    if (a0 < b1 && b0 < a1) return MT_EINVAL;
+  const long long added = c.num_rows - o.num_rows;
+  if (added > 0 && t->dev.nseg >= mt::kMaxRowSegments) return MT_EINVAL;
+  const size_t ks = keystore_layout(c).total, rb = rows_bytes_of(c, added);
+  if (keystore == nullptr || keystore_bytes < ks || !aligned(keystore, 256)) return MT_ENOSPACE;
+  if (added > 0 && (rows == nullptr || rows_bytes < rb || !aligned(rows, 256))) return MT_ENOSPACE;
+  // the rebuild reads the old key store while it writes the new one, and no row may be overwritten
+  if (overlaps_table(t, keystore, ks) || (added > 0 && (overlaps_table(t, rows, rb) || overlap(keystore, ks, rows, rb))))
+    return MT_EINVAL;
+  mt::TableDev T2 = device_view(c, keystore, t->dev.seg_base[0]);
+  T2.nseg = t->dev.nseg;
+  for (int s = 0; s < t->dev.nseg; ++s) {
+    T2.seg_base[s] = t->dev.seg_base[s];
+    T2.seg_first[s] = t->dev.seg_first[s];
   }
-  const mt::TableDev T2 = device_view(c, L, dev_mem);
+  if (added > 0) {
+    T2.seg_base[T2.nseg] = static_cast<char*>(rows);
+    T2.seg_first[T2.nseg] = o.num_rows;
+    T2.nseg += 1;
+  }
   cudaStream_t s = as_stream(stream);
   if (mt::launch_grow(t->dev, T2, s) != cudaSuccess) return MT_ECUDA;
   int32_t fail = 0;
@@ -273,7 +338,8 @@ int mt_table_grow(mt_table* t, const mt_config* new_cfg, void* dev_mem, size_t b
   if (fail) return MT_EFULL;
   t->cfg = c;
   t->dev = T2;
-  t->arena_bytes = L.total;
+  t->ks_base = static_cast<char*>(keystore);
+  t->ks_bytes = ks;
   return MT_OK;
 }
 
@@ -348,6 +414,7 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
     p.lsslot = reinterpret_cast<int32_t*>(w + L.lsslot);
     p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
     p.ntiles = L.ntiles;
+    p.clear_bytes = L.clear_bytes;
   }
   return cuda_status(mt::launch_lookup(p, as_stream(stream)));
 }
@@ -448,13 +515,33 @@ int mt_erase(mt_table* t, const uint64_t* keys, int64_t n, uint8_t* found, void*
 
 size_t mt_compact_workspace_bytes(const mt_table* t) {
   if (t == nullptr) return 0;
-  return align_up((size_t)(t->dev.mask + 1) * 16 + 256, 256);
+  return (size_t)(t->dev.mask + 1) * sizeof(mt::Slot);
 }
 
-int mt_compact(mt_table* t, void* ws, size_t ws_bytes, mt_stream stream) {
-  if (t == nullptr) return MT_EINVAL;
-  if (ws == nullptr || ws_bytes < mt_compact_workspace_bytes(t) || !aligned(ws, 256)) return MT_ENOSPACE;
-  return cuda_status(mt::launch_compact(t->dev, ws, as_stream(stream)));
+int mt_compact(mt_table* t, void* ws, size_t ws_bytes, void** released, mt_stream stream) {
+  if (t == nullptr || released == nullptr) return MT_EINVAL;
+  *released = nullptr;
+  const size_t need = mt_compact_workspace_bytes(t);
+  if (ws == nullptr || ws_bytes < need || !aligned(ws, 256)) return MT_ENOSPACE;
+  if (overlap(ws, need, t->dev.slots, need)) return MT_EINVAL;
+  for (int s = 0; s < t->dev.nseg; ++s) {
+    const long long end = s + 1 < t->dev.nseg ? t->dev.seg_first[s + 1] : t->dev.num_rows;
+    if (overlap(ws, need, t->dev.seg_base[s], (size_t)(end - t->dev.seg_first[s]) * t->dev.rec_bytes)) return MT_EINVAL;
+  }
+  if (overlap(ws, need, t->dev.hdr, mt::kHeaderBytes) ||
+      overlap(ws, need, t->dev.free_stack, (size_t)t->dev.num_rows * 4))
+    return MT_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  mt::Slot* fresh = static_cast<mt::Slot*>(ws);
+  if (mt::launch_compact(t->dev, fresh, s) != cudaSuccess) return MT_ECUDA;
+  int32_t fail = 0;
+  if (cudaMemcpyAsync(&fail, &t->dev.hdr->pad0, sizeof(fail), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MT_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MT_ECUDA;
+  if (fail) return MT_EFULL;
+  *released = t->dev.slots;
+  t->dev.slots = fresh;
+  return MT_OK;
 }
 
 int mt_stats(mt_table* t, mt_stats_out* out, mt_stream stream) {

@@ -1,13 +1,16 @@
 // Internal declarations of the CUDA path of the merged dynamic embedding table.
 //
-// Layout of the table arena (all in one caller-owned device allocation):
-//   [Header 1 KiB][slots: M x Slot (16 B)][free stack: R x int32][rows: R x record]
+// A table is a key store and one or more row segments, each in caller-owned
+// device memory:
+//   key store:    [Header 1 KiB][slots: M x Slot (16 B)][free stack: R x int32]
+//   row segment:  [records of rows first .. first + count - 1]
 // A row record is [emb: d x row dtype][m: d x fp32][v: d x fp32], each part a
 // multiple of 16 bytes, so every part of a row is reached with 16-byte vector
 // accesses.  A slot {key, row, meta} maps a merged key to its row and keeps
 // the table step at which it was inserted (MTGR section 5, Embedding
-// Management: each key leads to its embedding and to bookkeeping data); the key store is separate
-// from the rows, so it can be rebuilt without moving any embedding.
+// Management: each key leads to its embedding and to bookkeeping data).  The
+// key store is separate from the rows, so capacity expansion and compaction
+// rebuild it without moving any embedding; new rows arrive as a new segment.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -46,12 +49,16 @@ struct __align__(256) Header {
 constexpr size_t kHeaderBytes = 1024;
 static_assert(sizeof(Header) <= kHeaderBytes, "header fits");
 
+constexpr int kMaxRowSegments = MT_MAX_ROW_SEGMENTS;
+
 // Everything a kernel needs to reach the table (passed by value).
 struct TableDev {
   Header* hdr;
   Slot* slots;
   int32_t* free_stack;
-  char* rows;
+  char* seg_base[kMaxRowSegments];       // row segment s holds rows seg_first[s] .. seg_first[s+1] - 1
+  long long seg_first[kMaxRowSegments];  // seg_first[0] = 0
+  int nseg;
   unsigned long long mask;       // M - 1
   unsigned long long S;          // odd probe step, reduced mod M
   unsigned long long hash_seed;
@@ -93,8 +100,20 @@ __device__ __forceinline__ unsigned long long load_key_relaxed(const unsigned lo
   return v;
 }
 
+// The record of a row: its segment is found with constant indices only (the
+// table view lives in kernel parameter space, which dynamic indexing would
+// copy to local memory).
 __device__ __forceinline__ char* row_ptr(const TableDev& T, int32_t row) {
-  return T.rows + (size_t)row * T.rec_bytes;
+  char* base = T.seg_base[0];
+  long long first = 0;
+#pragma unroll
+  for (int s = 1; s < kMaxRowSegments; ++s) {
+    if (s < T.nseg && row >= T.seg_first[s]) {
+      base = T.seg_base[s];
+      first = T.seg_first[s];
+    }
+  }
+  return base + (size_t)(row - first) * T.rec_bytes;
 }
 
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two

@@ -52,7 +52,7 @@ struct LookupParams {
   int32_t* ulist;         // [n] scratch slot of each distinct key, in claim order
   int32_t* sc_row;        // [ss] table row of the key in a slot (-1: none)
   int32_t* tile_L;        // [ntiles] tile-local uniques per tile
-  int32_t* tile_O;        // [ntiles] distinct keys whose first position lies in the tile (zeroed by k_claim)
+  int32_t* tile_O;        // [ntiles] keys whose first position lies in the tile, minus one (cleared to -1)
   int32_t* tile_pre;      // [ntiles + 1] exclusive prefix of tile_O (written by the last k_resolve block)
   uint32_t* done;         // k_resolve blocks finished (zeroed by k_claim)
   int32_t* first_slot;    // [ntiles * kTile] scratch slot of the key first seen at each position, else -1
@@ -60,6 +60,7 @@ struct LookupParams {
   uint16_t* lidx;         // [ntiles * kTile] tile-local unique of each position
   int ntiles;
   int resolve_grid;
+  size_t clear_bytes;     // bytes from sc on cleared to all ones per call (slots, counter, tile counts)
 };
 
 struct LookupWsLayout {
@@ -145,7 +146,7 @@ cudaError_t launch_pool_scale(const long long* bo, long long B, int d, const flo
 cudaError_t launch_table_init(const TableDev& T, cudaStream_t s);
 cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long long n, unsigned char* found,
                          int32_t* ws_slot, cudaStream_t s);
-cudaError_t launch_compact(const TableDev& T, void* ws, cudaStream_t s);
+cudaError_t launch_compact(const TableDev& T, Slot* fresh, cudaStream_t s);
 cudaError_t launch_import(const TableDev& T, const unsigned long long* keys, long long n, const float* emb,
                           const float* m, const float* v, int32_t* ws_rows, cudaStream_t s);
 cudaError_t launch_grow(const TableDev& T, const TableDev& T2, cudaStream_t s);

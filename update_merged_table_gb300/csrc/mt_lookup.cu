@@ -18,15 +18,16 @@
 //             lowers the key's first position there (atomicMin) and adds its
 //             count (the returned total is the rank base of the tile's
 //             positions, so the ranks are written here).  The one thread whose
-//             CAS put a key into the scratch hash appends the slot to the list
-//             of distinct keys.
+//             CAS put a key into the scratch hash lists the slot as a distinct
+//             key (one global atomic per block); the tile holding a key's
+//             first position so far counts the key, and takes the count over
+//             from the tile it lowers the first position of.
 //  k_resolve  one thread per distinct key, over the whole GPU: find the key in
 //             the table (odd-step probing) or insert it (first tombstone or
 //             EMPTY slot of its chain, rows popped once per block, fresh rows
 //             initialised by teams of lanes); note the key at its first
-//             position and count it in the tile that holds that position.
-//             The last block to finish turns the per-tile counts into tile
-//             offsets.
+//             position.  The last block to finish turns the per-tile counts
+//             of first positions into tile offsets.
 //  k_number   per tile: the keys first seen in the tile take unique indices
 //             tile offset + their order inside the tile, i.e. first-occurrence
 //             order, and write the unique keys, rows and counts.
@@ -95,6 +96,9 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
   __shared__ int s_warp[kThreadsA / 32];
   __shared__ int s_frange[2];  // features of the tile's first and last position
+  __shared__ int s_nwin;       // distinct keys this block put into the scratch hash
+  __shared__ int s_take;       // keys whose first position so far lies in this tile
+  __shared__ int s_wbase;      // where the block's distinct keys go in the list
 
   const int tile = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -108,10 +112,7 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   }
   for (int i = tid; i <= p.F; i += kThreadsA) s_off[i] = p.feat_off[i];
   for (int i = tid; i < p.F; i += kThreadsA) s_tid[i] = p.table_ids[i];
-  if (tid == 0) {
-    p.tile_O[tile] = 0;  // counted by k_resolve
-    if (tile == 0) *p.done = 0u;
-  }
+  if (tid == 0 && tile == 0) *p.done = 0u;
   __syncthreads();
   if (tid < 2) {  // feature of position base (tid 0) and base + cnt - 1 (tid 1): last f with off[f] <= i
     const long long i = base + (tid == 0 ? 0 : cnt - 1);
@@ -205,47 +206,51 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   // ---- stage 2: every local unique claims its key in the global scratch hash,
   // lowers the key's first position and adds its count there.  The thread
   // whose CAS put the key into the scratch hash is the only one in the grid to
-  // see it EMPTY; it lists the slot as a distinct key. ----
+  // see it EMPTY; it lists the slot as a distinct key (the block's list goes
+  // out with one global atomic).  The tile that holds a key's first position
+  // so far counts the key; a tile that lowers the first position below
+  // another tile's takes the count over from it. ----
+  __syncthreads();  // s_min (local indices) is free from here: the block's new distinct keys are listed there
+  int32_t* s_win = reinterpret_cast<int32_t*>(s_min);  // [kHSA >= kTile]
+  if (tid == 0) {
+    s_nwin = 0;
+    s_take = 0;
+  }
+  __syncthreads();
   const size_t lb = (size_t)tile * kTile;
-  for (int li0 = 0; li0 < L; li0 += kThreadsA) {  // warp-uniform trip count (the list append is warp-wide)
-    const int li = li0 + tid;
-    const bool act = li < L;
-    unsigned long long h = 0;
+  for (int li = tid; li < L; li += kThreadsA) {
+    const uint32_t it = s_item[li];
+    const uint32_t sl = it >> 16;
+    const unsigned long long key = s_key[sl];
+    const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
+    unsigned long long h = stage2_home(key, p.ss);
     bool won = false;
-    if (act) {
-      const uint32_t it = s_item[li];
-      const uint32_t sl = it >> 16;
-      const unsigned long long key = s_key[sl];
-      const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
-      h = stage2_home(key, p.ss);
-      for (unsigned long long probe = 0; probe < p.ss; ++probe) {
-        unsigned long long cur = load_key_relaxed(&p.sc[h].key);
-        if (cur == kEmpty) {
-          cur = atomicCAS(&p.sc[h].key, kEmpty, key);
-          if (cur == kEmpty) {
-            won = true;
-            cur = key;
-          }
-        }
-        if (cur == key) break;
-        h = h + 1 == p.ss ? 0ull : h + 1;
+    for (unsigned long long probe = 0; probe < p.ss; ++probe) {
+      const unsigned long long cur = atomicCAS(&p.sc[h].key, kEmpty, key);
+      if (cur == kEmpty || cur == key) {
+        won = cur == kEmpty;
+        break;
       }
-      atomicMin(&p.sc[h].first, gpos);
-      const uint32_t before = atomicAdd(&p.sc[h].cnt, s_cnt[sl]) + 1u;  // the slot starts at "count - 1" = 2^32 - 1
-      s_cnt[sl] = before;  // rank base of this tile's positions of the key
-      p.lsslot[lb + li] = (int32_t)h;
+      h = h + 1 == p.ss ? 0ull : h + 1;
     }
-    const unsigned wm = __ballot_sync(kFull, won);
-    if (wm) {
-      const int leader = __ffs(wm) - 1;
-      uint32_t first = 0;
-      if (lane == leader) first = atomicAdd(p.ulist_n, (uint32_t)__popc(wm)) + 1u;  // counter starts at 2^32 - 1
-      first = __shfl_sync(kFull, first, leader);
-      if (won) p.ulist[first + __popc(wm & ((1u << lane) - 1u))] = (int32_t)h;
+    const uint32_t prev_first = atomicMin(&p.sc[h].first, gpos);
+    const uint32_t before = atomicAdd(&p.sc[h].cnt, s_cnt[sl]) + 1u;  // the slot starts at "count - 1" = 2^32 - 1
+    s_cnt[sl] = before;  // rank base of this tile's positions of the key
+    p.lsslot[lb + li] = (int32_t)h;
+    if (gpos < prev_first) {
+      atomicAdd(&s_take, 1);
+      if (prev_first != 0xFFFFFFFFu) atomicAdd(&p.tile_O[prev_first / kTile], -1);
     }
+    if (won) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h;
   }
   if (tid == 0) p.tile_L[tile] = L;
   __syncthreads();
+  if (tid == 0) {
+    s_wbase = s_nwin ? (int)(atomicAdd(p.ulist_n, (uint32_t)s_nwin) + 1u) : 0;  // the counter starts at 2^32 - 1
+    if (s_take) atomicAdd(&p.tile_O[tile], s_take);
+  }
+  __syncthreads();
+  for (int w = tid; w < s_nwin; w += kThreadsA) p.ulist[s_wbase + w] = s_win[w];
 
   if (p.ranks != nullptr) {
     for (int lp = tid; lp < cnt; lp += kThreadsA) {
@@ -342,7 +347,6 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
     if (act) {
       p.sc_row[slot] = row;
       p.first_slot[gfirst] = slot;
-      atomicAdd(&p.tile_O[gfirst / kTile], 1);
     }
     __syncthreads();
     const int nnew = s_nnew;
@@ -363,7 +367,7 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int t = c0 + tid * 4 + k;
-      v[k] = t < p.ntiles ? __ldcg(&p.tile_O[t]) : 0;
+      v[k] = t < p.ntiles ? __ldcg(&p.tile_O[t]) + 1 : 0;  // the counts start at -1
       sum += v[k];
     }
     int tot;
@@ -414,22 +418,15 @@ __global__ void __launch_bounds__(kThreads, 6) k_number(const LookupParams p) {
   for (int k = 0; k < kPPT; ++k) c += v[k] >= 0;
   int tot;
   int r = block_exclusive_scan<kThreads>(c, s_warp, &tot);
-  ulonglong2 sv[kPPT];
-  int32_t row[kPPT];
 #pragma unroll
-  for (int k = 0; k < kPPT; ++k) {  // every owner's loads in flight at once
-    if (v[k] >= 0) {
-      sv[k] = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[v[k]]));
-      row[k] = __ldcg(&p.sc_row[v[k]]);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) {
+  for (int k = 0; k < kPPT; ++k) {  // about one key in six is first seen here: their loads run one by one
     if (v[k] >= 0) {
       const int u = pre + r++;
-      p.unique_keys[u] = sv[k].x;
-      p.unique_rows[u] = row[k];
-      p.counts[u] = (int32_t)((uint32_t)(sv[k].y >> 32) + 1u);
+      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[v[k]]));
+      const int32_t row = __ldcg(&p.sc_row[v[k]]);
+      p.unique_keys[u] = sv.x;
+      p.unique_rows[u] = row;
+      p.counts[u] = (int32_t)((uint32_t)(sv.y >> 32) + 1u);
       p.sc[v[k]].first = (uint32_t)u;  // from here on the slot holds the key's unique index
     }
   }
@@ -529,13 +526,14 @@ LookupWsLayout lookup_ws_layout(long long n) {
   };
   const size_t cap = (size_t)L.ntiles * kTile;
   L.sc = take(L.ss * sizeof(ScSlot));
-  L.ulist_n = off;                      // right after the slots: cleared by the same memset
-  L.clear_bytes = L.ss * sizeof(ScSlot) + 16;
-  take(16);
+  L.ulist_n = off;  // right after the slots, then the tile counts: one memset clears all three
+  off += 16;
+  L.tile_O = off;
+  L.clear_bytes = off + (size_t)L.ntiles * 4;
+  take((size_t)L.ntiles * 4);
   L.ulist = take((size_t)(n > 0 ? n : 1) * 4);
   L.sc_row = take(L.ss * 4);
   L.tile_L = take((size_t)L.ntiles * 4);
-  L.tile_O = take((size_t)L.ntiles * 4);
   L.tile_pre = take((size_t)(L.ntiles + 1) * 4);
   L.done = take(16);
   L.first_slot = take(cap * 4);
@@ -565,8 +563,9 @@ cudaError_t launch_lookup(const LookupParams& p_in, cudaStream_t s) {
   const long long want = (p.n + kThreadsR - 1) / kThreadsR;  // blocks if every ID were distinct
   const int slots = resolve_slots[dev].load(std::memory_order_relaxed);
   p.resolve_grid = (int)(want < slots ? want : slots);
-  // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1) and the distinct-key counter: all ones
-  cudaError_t e = cudaMemsetAsync(p.sc, 0xFF, (size_t)p.ss * sizeof(ScSlot) + 16, s);
+  // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1), the distinct-key counter and the tile counts
+  // (both minus one): all ones
+  cudaError_t e = cudaMemsetAsync(p.sc, 0xFF, p.clear_bytes, s);
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_claim", s);

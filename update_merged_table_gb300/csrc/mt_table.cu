@@ -60,11 +60,12 @@ __global__ void k_erase_apply(const TableDev T, const unsigned long long* keys, 
   }
 }
 
-// Compaction pass 1: every live key of the table is inserted again, with
-// its row and meta, into the fresh slot array `fresh` (all EMPTY), along the
-// same probe sequence; keys are distinct, so a CAS only ever loses to
-// another key.  A key that finds no EMPTY slot within max_probes sets *fail.
-__global__ void k_compact_rebuild(const TableDev T, Slot* fresh, int* fail) {
+// Compaction: every live key of the table is inserted again, with its row
+// and meta, into the fresh slot array `fresh` (all EMPTY), along the same
+// probe sequence; keys are distinct, so a CAS only ever loses to another key.
+// A key that finds no EMPTY slot within max_probes sets the header's flag
+// (the call then keeps the old slots and latches MT_EFULL).
+__global__ void k_compact_rebuild(const TableDev T, Slot* fresh) {
   const unsigned long long M = T.mask + 1;
   for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
        s += (unsigned long long)gridDim.x * blockDim.x) {
@@ -81,23 +82,11 @@ __global__ void k_compact_rebuild(const TableDev T, Slot* fresh, int* fail) {
       }
       h = (h + T.S) & T.mask;
     }
-    if (!placed) atomicExch(fail, 1);
+    if (!placed) {
+      atomicExch(&T.hdr->pad0, 1);
+      latch_error(T.hdr, MT_EFULL);
+    }
   }
-}
-
-// Compaction pass 2: the fresh slots replace the table's, unless a key did
-// not fit (then the table stays as it was and MT_EFULL is latched).
-__global__ void k_compact_commit(const TableDev T, const Slot* fresh, const int* fail) {
-  if (*fail) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) latch_error(T.hdr, MT_EFULL);
-    return;
-  }
-  const unsigned long long M = T.mask + 1;
-  const uint4* src = reinterpret_cast<const uint4*>(fresh);
-  uint4* dst = reinterpret_cast<uint4*>(T.slots);
-  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
-       s += (unsigned long long)gridDim.x * blockDim.x)
-    dst[s] = src[s];
 }
 
 // Import pass 1: find each key, or insert it like a lookup does (first
@@ -165,8 +154,9 @@ __global__ void k_import_write(const TableDev T, const int32_t* rows, long long 
   }
 }
 
-// Capacity expansion, pass 1: the new rows (old R .. new R - 1) join the
-// free list above the old free entries, and the free count grows with them.
+// Capacity expansion, pass 1: the new rows (old R .. new R - 1, the new row
+// segment) join the free list above the old free entries, and the free count
+// grows with them.
 __global__ void k_grow_rows(const TableDev T2, long long old_rows) {
   const long long added = T2.num_rows - old_rows;
   const long long top = T2.hdr->free_top;  // copied from the old header
@@ -315,21 +305,15 @@ cudaError_t launch_erase(const TableDev& T, const unsigned long long* keys, long
   return cudaGetLastError();
 }
 
-cudaError_t launch_compact(const TableDev& T, void* ws, cudaStream_t s) {
+cudaError_t launch_compact(const TableDev& T, Slot* fresh, cudaStream_t s) {
   const unsigned long long M = T.mask + 1;
-  Slot* fresh = static_cast<Slot*>(ws);
-  int* fail = reinterpret_cast<int*>(static_cast<char*>(ws) + M * sizeof(Slot));
   cudaError_t e = cudaMemsetAsync(fresh, 0xFF, M * sizeof(Slot), s);  // keys EMPTY
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(fail, 0, sizeof(int), s);
+  e = cudaMemsetAsync(&T.hdr->pad0, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_compact_rebuild", s);
-    k_compact_rebuild<<<grid_for((long long)M, 256, 32), 256, 0, s>>>(T, fresh, fail);
-  }
-  {
-    MT_LAUNCH("k_compact_commit", s);
-    k_compact_commit<<<grid_for((long long)M, 256, 32), 256, 0, s>>>(T, fresh, fail);
+    k_compact_rebuild<<<grid_for((long long)M, 256, 32), 256, 0, s>>>(T, fresh);
   }
   return cudaGetLastError();
 }
@@ -369,10 +353,12 @@ cudaError_t launch_import(const TableDev& T, const unsigned long long* keys, lon
   return cudaGetLastError();
 }
 
+// The new key store of T2: header and the old free list copied, slots
+// cleared, the new row segment's rows pushed, every live key re-inserted.
+// No row record is read or written.
 cudaError_t launch_grow(const TableDev& T, const TableDev& T2, cudaStream_t s) {
   cudaError_t e = cudaMemcpyAsync(T2.hdr, T.hdr, kHeaderBytes, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(T2.free_stack, T.free_stack, (size_t)T.num_rows * 4, cudaMemcpyDeviceToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(T2.rows, T.rows, (size_t)T.num_rows * T.rec_bytes, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(T2.slots, 0xFF, (size_t)(T2.mask + 1) * sizeof(Slot), s);  // keys EMPTY
   if (e != cudaSuccess) return e;
   if (T2.num_rows > T.num_rows) {
