@@ -726,7 +726,26 @@ def run_ours(args):
         M = 1 << wl.log2
         comp = {"ms": c_ms, "slots": M, "live": int(st_before["live"]),
                 "algorithmic_GB/s": 32.0 * M / (c_ms / 1e3) / 1e9,  # read every old slot, write every new one
-                "note": "mt_compact: live keys re-inserted into a fresh slot array that replaces the table's"}
+                "note": "mt_compact: live keys re-inserted into a spare slot array that becomes the table's "
+                        "(no copy back)"}
+
+    # -------- capacity expansion: twice the slots, rows unchanged (one call, after everything else) --------
+    grow = None
+    if ws == 1 and args.grow:
+        st_before = tab.stats()
+        M_old = 1 << wl.log2
+        torch.cuda.synchronize(dev)
+        g0 = time.perf_counter()
+        tab.grow(wl.log2 + 1, num_rows=tab.cfg.num_rows)  # synchronises
+        g_ms = (time.perf_counter() - g0) * 1e3
+        grow = {"ms_host_timed": g_ms, "slots_before": M_old, "slots_after": 2 * M_old,
+                "live": int(st_before["live"]),
+                "rows_moved": 0, "row_bytes_in_table": int(tab.cfg.num_rows) * (B + 8 * wl.dim),
+                "key_store_GB/s": (16.0 * M_old + 16.0 * 2 * M_old) / (g_ms / 1e3) / 1e9,
+                "note": "mt_table_grow: a new key store (old slots read, new slots cleared and filled); the rows "
+                        "stay in place, so the cost follows the slot count, not the row pool"}
+        if tab.stats()["live"] != st_before["live"]:
+            raise RuntimeError("capacity expansion lost keys")
 
     err = tab.error()
     if err != 0:
@@ -766,6 +785,7 @@ def run_ours(args):
         "cold_step": cold_stats,
         "pooled": pooled,
         "compaction": comp,
+        "grow": grow,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
@@ -873,6 +893,7 @@ def main():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--e2e", type=int, default=1, help="also time the step through host buffers (its own table)")
     ap.add_argument("--pooled", type=int, default=1, help="also time the pooled jagged-bag step (jagged workload)")
+    ap.add_argument("--grow", type=int, default=1, help="also time one capacity expansion at the end")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=150.0,

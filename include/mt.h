@@ -77,9 +77,10 @@ typedef void* mt_stream;
  *              Theorem 1).  Used mod M; it must be odd, which makes the
  *              sequence visit every slot.  An even S is MT_EINVAL.
  *  hash_seed   h0 = top n bits of splitmix64-finaliser(key ^ hash_seed).
- *  init_seed   fresh rows: column j = scale * (2q - 2^24) / 2^24 with q the
- *              top 24 bits of word j%4 of Philox4x64-10(counter (j/4,0,0,0),
- *              key (merged key, init_seed)); m = v = 0.
+ *  init_seed   fresh rows: column j = scale * (2q - 2^24) / 2^24 with q
+ *              24 bits of word (j/2)%4 of Philox4x64-10(counter (j/8,0,0,0),
+ *              key (merged key, init_seed)): bits 63..40 for an even j, bits
+ *              39..16 for an odd j; m = v = 0.
  *  init_scale  0 means fp32(1/sqrt(d)).
  *  num_rows    R, rows in the row pool; 0 means M.  1 <= R <= M. */
 typedef struct {
@@ -284,6 +285,117 @@ size_t mt_backward_pooled_workspace_bytes(const mt_table* t, int64_t n, int64_t 
 int mt_backward_adam_pooled(mt_table* t, const mt_lookup_result* res, int64_t n, const int64_t* bag_offsets,
                             int64_t num_bags, int mode, const float* dpooled, const mt_adam* hp, float* gsum_out,
                             void* ws, size_t ws_bytes, mt_stream stream);
+
+/* ---- automatic table merging ------------------------------------------------ */
+
+/* Feature tables merged into shared tables (MTGenRec TL;DR and abstract:
+ * automatic table merging, so a batch needs fewer lookups).  The pages give
+ * no grouping rule; this one is used: features whose tables have the same
+ * row shape (dim and row dtype) share a merged table, in order of first
+ * appearance, each feature keeping its own key space through its table id
+ * (0, 1, 2, ... in feature order; a merged table holds at most 255 features,
+ * more open another one of the same shape). */
+typedef struct {
+  uint32_t dim;       /* the feature table's embedding width */
+  uint32_t row_dtype; /* MT_F32 or MT_BF16 */
+  int64_t capacity;   /* keys the feature's table is expected to hold (>= 0) */
+} mt_feature_spec;
+
+typedef struct {
+  int32_t group;    /* the merged table the feature goes to */
+  uint8_t table_id; /* its table id there */
+  uint8_t pad[3];
+} mt_feature_placement;
+
+typedef struct {
+  uint32_t dim, row_dtype;
+  uint32_t log2_slots; /* the smallest n >= 1 with capacity <= max_load * 2^n */
+  int32_t num_features;
+  int64_t capacity;    /* the sum of its features' capacities */
+} mt_merge_group;
+
+/* Plan the merged tables of F features (1 <= F <= MT_MAX_FEATURES) with
+ * 0 < max_load <= 1: placement [F] and groups [F] (host) receive the plan,
+ * *num_groups the number of merged tables.  MT_EINVAL for a bad row shape, a
+ * negative capacity, or a group that would need more than 2^31 slots. */
+int mt_plan_merge(const mt_feature_spec* features, int F, double max_load, mt_feature_placement* placement,
+                  mt_merge_group* groups, int* num_groups);
+
+/* Workspace bytes mt_lookup_grouped needs for a batch of n IDs. */
+size_t mt_lookup_grouped_workspace_bytes(int64_t n);
+
+/* Lookup of one batch of F feature segments over the merged tables of a plan:
+ * the segments of the features placed in group g are routed, in feature
+ * order, into one batch for tables[g] (its feature offsets and table ids from
+ * the plan), and looked up there as mt_lookup does.
+ *  tables       host array [G] of the merged tables (rows of group g's shape).
+ *  ids          device int64 [n]; feat_offsets host int64 [F + 1] (0 .. n).
+ *  out_rows     host array [G] of device pointers [group_n[g], d_g] (entries
+ *               or the array may be NULL).
+ *  results      host array [G], each of capacity >= the group's IDs.
+ *  group_n      host int64 [G]: receives each group's number of IDs.
+ * The backward of group g is mt_backward_adam(tables[g], &results[g],
+ * group_n[g], ...) with that group's gradient rows. */
+int mt_lookup_grouped(mt_table* const* tables, int G, const mt_feature_placement* placement, const int64_t* ids,
+                      int64_t n, const int64_t* feat_offsets, int F, int insert_missing, void* const* out_rows,
+                      const mt_lookup_result* results, int64_t* group_n, void* ws, size_t ws_bytes,
+                      mt_stream stream);
+
+/* ---- sharded two-stage deduplication (G logical shards on one GPU) ------- */
+
+/* The distributed form of the lookup (MTGR section 5, Embedding Lookup:
+ * deduplicated IDs on both sides of the cross-device all-to-all; MTGenRec
+ * TL;DR: two-stage ID deduplication), with G logical ranks on one GPU.  Each
+ * rank r owns the keys whose owner(key) (a second hash of the key mapped to
+ * [0, G)) is r and keeps them in its shard table; each rank has its own
+ * batch.  Forward: stage-1 unique per rank; the (rank, owner) counts are read
+ * on the host (the sizes of a variable all-to-all); every rank writes its
+ * unique keys into the owners' receive buffers (the exchange, a device-local
+ * copy here); stage-2 unique, find/insert and gather at each owner; rows back
+ * to the ranks, and each rank expands them through its inverse.  Backward:
+ * per-rank sums per unique key, sums to the owners, per-key sums over the
+ * ranks and one Adam step on every shard.  The shards must share dim, row
+ * dtype, init seed and init scale (a key's row does not depend on its owner).
+ * These calls synchronise the stream (the exchange sizes are read on the
+ * host), so they cannot be captured in a CUDA graph. */
+#define MT_MAX_SHARDS 16
+typedef struct mt_shard_group mt_shard_group; /* opaque host handle */
+
+/* Group G distinct tables (1 <= G <= MT_MAX_SHARDS) as the shards of one logical table. */
+int mt_shard_group_create(mt_table* const* shards, int G, mt_shard_group** out);
+int mt_shard_group_destroy(mt_shard_group* g);
+
+/* Workspace bytes for batches of n[r] IDs (host int64 [G]); the lookup and its
+ * backward take the same workspace, which keeps the exchange layout between them. */
+size_t mt_shard_workspace_bytes(const mt_shard_group* g, const int64_t* n);
+
+/* Forward of one step of all G ranks.
+ *  ids          host array of G device pointers: rank r's IDs, int64 [n[r]].
+ *  n            host int64 [G].
+ *  feat_offsets host int64 [G * (F + 1)]: rank r's feature offsets (as in
+ *               mt_lookup); NULL means F = 1 for every rank.
+ *  table_ids    host uint8 [F] (< 255), shared by the ranks; NULL means 0.
+ *  out_rows     host array of G device pointers [n[r], d] (entries or the
+ *               array may be NULL: no rows for that rank).
+ *  results      host array of G mt_lookup_result: rank r's unique keys in
+ *               first-occurrence order of its own batch, inverse, counts,
+ *               ranks (nullable) and num_unique; unique_rows are set to -1
+ *               (the rows live in the owners' shards).
+ * The rows a rank receives equal what one table holding every key would give. */
+int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t* n, const int64_t* feat_offsets,
+                    const uint8_t* table_ids, int F, int insert_missing, void* const* out_rows,
+                    const mt_lookup_result* results, void* ws, size_t ws_bytes, mt_stream stream);
+
+/* Backward of the last mt_shard_lookup (same results and workspace): grads is a
+ * host array of G device pointers [n[r], d] of grad_dtype.  Every key's
+ * gradient is summed over all positions of all ranks (rank sums rounded to
+ * fp32, then summed exactly at the owner and rounded once), then one Adam step
+ * is applied by its owner; every shard's step counter advances once.
+ *  gsum_out  NULL, or a host array of G device pointers fp32 [U_r, d] (entries
+ *            may be NULL): rank r's unique keys' sums over all ranks. */
+int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, const void* const* grads,
+                           int grad_dtype, const mt_adam* hp, float* const* gsum_out, void* ws, size_t ws_bytes,
+                           mt_stream stream);
 
 /* ---- deletion ------------------------------------------------------------ */
 

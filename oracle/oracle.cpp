@@ -90,16 +90,18 @@ float bf16_value(uint16_t b) {
 // The value a row element holds in storage of the given dtype.
 float store_round(float x, int dtype) { return dtype == ORC_BF16 ? bf16_value(bf16_bits(x)) : x; }
 
-// Initial value of column j of the row of `key`.  Word j%4 of
-// Philox4x64-10(counter = (j/4, 0, 0, 0), key = (key, seed)) gives a 24-bit
-// integer q (its top 24 bits); (2q - 2^24) / 2^24 is exact in fp32 and lies in
-// [-1, 1); one multiply by `scale` is the only rounding.
+// Initial value of column j of the row of `key`.  Each 64-bit word of
+// Philox4x64-10(counter = (j/8, 0, 0, 0), key = (key, seed)) serves two
+// columns: word (j/2)%4 gives a 24-bit integer q from its bits 63..40 for an
+// even j and from its bits 39..16 for an odd j; (2q - 2^24) / 2^24 is exact
+// in fp32 and lies in [-1, 1); one multiply by `scale` is the only rounding.
 float init_value(uint64_t key, uint64_t seed, float scale, uint32_t j) {
   uint64_t k[2] = {key, seed};
-  uint64_t c[4] = {(uint64_t)(j / 4u), 0, 0, 0};
+  uint64_t c[4] = {(uint64_t)(j / 8u), 0, 0, 0};
   uint64_t w[4];
   philox4x64(c, k, w);
-  int32_t q = (int32_t)(w[j % 4u] >> 40);
+  const uint64_t word = w[(j / 2u) % 4u];
+  int32_t q = (int32_t)((j % 2u == 0u ? word >> 40 : word >> 16) & 0xFFFFFFu);
   float unit = (float)(2 * q - (1 << 24)) * (1.0f / 16777216.0f);
   return unit * scale;
 }

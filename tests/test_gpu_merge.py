@@ -1,0 +1,87 @@
+"""Automatic table merging on the GPU: features of dims {16, 32, 64} planned into merged tables, a batch's
+feature segments routed to them by mt_lookup_grouped, then per-table backward; every merged table matches an
+oracle table fed the same routed segments (unique keys, inverse, counts and rows bit-exact; Adam rows within
+the stated tolerances)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import update_merged_table_gb300 as mt
+from update_merged_table_gb300 import workloads as W
+from numerics import ATOL, RTOL, assert_rows_close  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+FEATURES = [(16, "f32", 4000), (32, "f32", 4000), (64, "bf16", 4000), (16, "f32", 4000), (64, "bf16", 4000),
+            (32, "f32", 4000)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from update_merged_table_gb300 import build_lib
+    build_lib.build()
+    mt.load_library()
+    oracle.build()
+
+
+def batch(seed, per=1500):
+    rng = np.random.default_rng(seed)
+    sizes = [per, per // 2, per, 0, per + 7, per // 3]  # one feature absent from this batch
+    parts = [W.zipf_ranks(rng, s, 1.1, 3000) - 1 for s in sizes]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    return np.concatenate(parts).astype(np.int64), offs
+
+
+def routed(ids, offs, placement, g):
+    """The segments of group g's features, in feature order, with offsets and table ids (the routing, by hand)."""
+    seg, o, t = [], [0], []
+    for f, (gg, tid) in enumerate(placement):
+        if gg != g:
+            continue
+        seg.append(ids[offs[f]:offs[f + 1]])
+        o.append(o[-1] + offs[f + 1] - offs[f])
+        t.append(tid)
+    return np.concatenate(seg), np.array(o, np.int64), np.array(t, np.uint8)
+
+
+def test_merged_tables_route_and_train():
+    mtabs = mt.MergedTables(FEATURES, max_load=0.5, init_seed=3)
+    assert [(g["dim"], g["row_dtype"], g["num_features"]) for g in mtabs.groups] == [
+        (16, "f32", 2), (32, "f32", 2), (64, "bf16", 2)]
+    refs = [oracle.Table(g["log2_slots"], g["dim"], row_dtype=oracle.BF16 if g["row_dtype"] == "bf16" else oracle.F32,
+                         init_seed=3) for g in mtabs.groups]
+    dev = mtabs.device
+    for step in range(3):
+        ids, offs = batch(step)
+        res = mtabs.lookup(torch.from_numpy(ids).to(dev), offs)
+        grads = []
+        for g, (r, ref) in enumerate(zip(res, refs)):
+            gids, goffs, gtids = routed(ids, offs, mtabs.placement, g)
+            want = ref.lookup(gids, goffs, gtids)
+            U = r.U
+            assert U == want["U"]
+            assert np.array_equal(r.unique_keys[:U].cpu().numpy().view(np.uint64), want["unique"])
+            assert np.array_equal(r.inverse[:r.n].cpu().numpy(), want["inverse"])
+            assert np.array_equal(r.counts[:U].cpu().numpy(), want["counts"])
+            assert np.array_equal(r.rows.float().cpu().numpy(), want["rows"])
+            assert (r.unique_keys[:U].cpu().numpy().view(np.uint64) >> np.uint64(56)).max() < 2  # two features each
+            grads.append(W.grads_normal(10 * step + g, r.n, mtabs.groups[g]["dim"]))
+        gsums = [t.backward_adam(r, torch.from_numpy(gr).to(dev), want_gsum=True)
+                 for t, r, gr in zip(mtabs.tables, res, grads)]
+        for g, (r, ref) in enumerate(zip(res, refs)):
+            ref_gsum = ref.backward_adam(grads[g], want_gsum=True)
+            np.testing.assert_allclose(gsums[g][:r.U].cpu().numpy(), ref_gsum, rtol=RTOL, atol=ATOL)
+            emb, m, v = mtabs.tables[g].read_rows(r.unique_rows[:r.U])
+            e2, m2, v2, pr = ref.get_rows(r.unique_keys[:r.U].cpu().numpy().view(np.uint64))
+            assert pr.all()
+            assert_rows_close(emb.cpu().numpy(), e2, mtabs.groups[g]["row_dtype"])
+            np.testing.assert_allclose(m.cpu().numpy(), m2, rtol=RTOL, atol=ATOL)
+    assert all(t.error() == 0 for t in mtabs.tables)
+
+
+def test_group_without_ids_in_the_batch():
+    mtabs = mt.MergedTables([(16, "f32", 100), (32, "f32", 100)], max_load=0.5)
+    ids = np.arange(50, dtype=np.int64)
+    res = mtabs.lookup(torch.from_numpy(ids).to(mtabs.device), [0, 50, 50])
+    assert res[0].U == 50 and res[1].n == 0 and res[1].U == 0

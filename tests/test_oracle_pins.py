@@ -167,8 +167,8 @@ def test_init_row_from_numpy_philox():
             seed = int(rng.integers(0, 2**63))
             want = np.zeros(dim, np.float32)
             for j in range(dim):
-                w = _numpy_philox_block([j // 4, 0, 0, 0], [key, seed])[j % 4]
-                q = int(w) >> 40
+                w = int(_numpy_philox_block([j // 8, 0, 0, 0], [key, seed])[(j // 2) % 4])
+                q = (w >> 40) if j % 2 == 0 else ((w >> 16) & 0xFFFFFF)
                 unit = np.float32((2 * q - (1 << 24)) / float(1 << 24))
                 want[j] = np.float32(unit * np.float32(scale))
             if dtype == oracle.BF16:

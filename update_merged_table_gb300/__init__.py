@@ -20,7 +20,7 @@ import os
 
 import numpy as np
 
-__all__ = ["Table", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "POOL_SUM", "POOL_MEAN",
+__all__ = ["Table", "ShardGroup", "MergedTables", "plan_merge", "LookupResult", "load_library", "MTError", "MT_F32", "MT_BF16", "POOL_SUM", "POOL_MEAN",
            "KEY_EMPTY", "KEY_TOMBSTONE",
            "ABI_FUNCTIONS", "profile_enable", "profile_report", "kernel_launches"]
 
@@ -90,6 +90,14 @@ ABI_FUNCTIONS = {
     "mt_backward_pooled_workspace_bytes": (_SZ, [_P, _I64, _I64]),
     "mt_backward_adam_pooled": (_I32, [_P, _P, _I64, _P, _I64, _I32, _P, _P, _P, _P, _SZ, _P]),
     "mt_backward_adam": (_I32, [_P, _P, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "mt_shard_group_create": (_I32, [_P, _I32, _P]),
+    "mt_shard_group_destroy": (_I32, [_P]),
+    "mt_shard_workspace_bytes": (_SZ, [_P, _P]),
+    "mt_shard_lookup": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "mt_shard_backward_adam": (_I32, [_P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
+    "mt_plan_merge": (_I32, [_P, _I32, ctypes.c_double, _P, _P, _P]),
+    "mt_lookup_grouped_workspace_bytes": (_SZ, [_I64]),
+    "mt_lookup_grouped": (_I32, [_P, _I32, _P, _P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
     "mt_erase_workspace_bytes": (_SZ, [_I64]),
     "mt_erase": (_I32, [_P, _P, _I64, _P, _P, _SZ, _P]),
     "mt_compact_workspace_bytes": (_SZ, [_P]),
@@ -107,6 +115,19 @@ ABI_FUNCTIONS = {
     "mt_profile_report": (_I32, [_P, _I32, _P, _I32]),
     "mt_kernel_launches": (_I64, []),
 }
+
+class _FeatureSpec(ctypes.Structure):
+    _fields_ = [("dim", ctypes.c_uint32), ("row_dtype", ctypes.c_uint32), ("capacity", ctypes.c_int64)]
+
+
+class _Placement(ctypes.Structure):
+    _fields_ = [("group", ctypes.c_int32), ("table_id", ctypes.c_uint8), ("pad", ctypes.c_uint8 * 3)]
+
+
+class _MergeGroup(ctypes.Structure):
+    _fields_ = [("dim", ctypes.c_uint32), ("row_dtype", ctypes.c_uint32), ("log2_slots", ctypes.c_uint32),
+                ("num_features", ctypes.c_int32), ("capacity", ctypes.c_int64)]
+
 
 class _KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
@@ -514,3 +535,160 @@ class Table:
     @property
     def step(self) -> int:
         return int(self.lib.mt_step(self.h))
+
+
+class ShardGroup:
+    """G tables as the shards of one logical table, driven as G logical ranks on one GPU
+    (``mt_shard_lookup`` / ``mt_shard_backward_adam``): each rank deduplicates its own batch, sends its
+    unique keys to their owners, the owners deduplicate again and serve the rows, and the rows come back."""
+
+    def __init__(self, shards):
+        self.lib = load_library()
+        self.shards = list(shards)
+        self.G = len(self.shards)
+        arr = (ctypes.c_void_p * self.G)(*[t.h.value for t in self.shards])
+        self.h = ctypes.c_void_p()
+        _check(self.lib.mt_shard_group_create(arr, self.G, ctypes.byref(self.h)), "mt_shard_group_create")
+        self.dim = self.shards[0].dim
+        self.device = self.shards[0].device
+        self._ws = None
+        self._last = None
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h and h.value:
+            try:
+                self.lib.mt_shard_group_destroy(h)
+            except Exception:  # pragma: no cover
+                pass
+            self.h = None
+
+    def lookup(self, ids, feat_offsets=None, table_ids=None, insert_missing: bool = True, gather: bool = True,
+               ranks: bool = True, stream=None):
+        """ids: G int64 CUDA tensors; feat_offsets: G host sequences of F+1 (or None).  Returns G LookupResults
+        (rows per rank; unique_rows are -1, the rows live in the owners' shards)."""
+        torch = _torch()
+        G = self.G
+        if len(ids) != G:
+            raise ValueError("one ID tensor per rank")
+        ns = np.array([int(x.numel()) for x in ids], dtype=np.int64)
+        for x in ids:
+            if x.dtype != torch.int64 or not x.is_cuda or not x.is_contiguous():
+                raise TypeError("ids must be contiguous int64 CUDA tensors")
+        res = [self.shards[r].new_result(int(ns[r]), gather=gather, ranks=ranks) for r in range(G)]
+        F = 1
+        fo_p = ti_p = None
+        if feat_offsets is not None:
+            fo = np.ascontiguousarray(np.concatenate([np.asarray(f, np.int64) for f in feat_offsets]), np.int64)
+            F = fo.size // G - 1
+            fo_p = fo.ctypes.data_as(ctypes.c_void_p)
+        if table_ids is not None:
+            ti = np.ascontiguousarray(table_ids, dtype=np.uint8)
+            ti_p = ti.ctypes.data_as(ctypes.c_void_p)
+        wsb = self.lib.mt_shard_workspace_bytes(self.h, ns.ctypes.data_as(ctypes.c_void_p))
+        if self._ws is None or self._ws.numel() < wsb:
+            self._ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=self.device)
+        ids_p = (ctypes.c_void_p * G)(*[x.data_ptr() if x.numel() else None for x in ids])
+        out_p = (ctypes.c_void_p * G)(*[(r.rows.data_ptr() if (gather and r.n) else None) for r in res])
+        st = (_Result * G)(*[r.as_struct() for r in res])
+        _check(self.lib.mt_shard_lookup(self.h, ids_p, ns.ctypes.data_as(ctypes.c_void_p), fo_p, ti_p, F,
+                                        int(bool(insert_missing)), out_p, st, self._ws.data_ptr(), self._ws.numel(),
+                                        _stream(stream)), "mt_shard_lookup")
+        self._last = res
+        return res
+
+    def backward_adam(self, res, grads, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
+                      eps: float = 1e-8, want_gsum: bool = False, stream=None):
+        """grads: G CUDA tensors [n_r, dim] (fp32 or bf16).  Returns per-rank fp32 sums [U_r, dim] over all
+        ranks if asked."""
+        torch = _torch()
+        G = self.G
+        gd = {torch.float32: MT_F32, torch.bfloat16: MT_BF16}.get(grads[0].dtype)
+        if gd is None or any(g.dtype != grads[0].dtype for g in grads):
+            raise TypeError("grads must all be float32 or all bfloat16")
+        for r in range(G):
+            if grads[r].shape != (res[r].n, self.dim) or not grads[r].is_cuda or not grads[r].is_contiguous():
+                raise ValueError("grads[r] must be a contiguous CUDA tensor [n_r, dim]")
+        gsum = None
+        gs_p = None
+        if want_gsum:
+            gsum = [torch.empty((max(int(r.U), 1), self.dim), dtype=torch.float32, device=self.device) for r in res]
+            gs_p = (ctypes.c_void_p * G)(*[g.data_ptr() for g in gsum])
+        hp = _Adam(lr, beta1, beta2, eps)
+        g_p = (ctypes.c_void_p * G)(*[g.data_ptr() if g.numel() else None for g in grads])
+        st = (_Result * G)(*[r.as_struct() for r in res])
+        _check(self.lib.mt_shard_backward_adam(self.h, st, g_p, gd, ctypes.byref(hp), gs_p, self._ws.data_ptr(),
+                                               self._ws.numel(), _stream(stream)), "mt_shard_backward_adam")
+        return gsum
+
+
+def plan_merge(features, max_load: float = 0.5):
+    """Automatic table merging (``mt_plan_merge``).  features: sequence of (dim, "f32"|"bf16", capacity).
+    Returns (placement, groups): placement[f] = (group, table_id); groups[g] = dict(dim, row_dtype,
+    log2_slots, num_features, capacity)."""
+    L = load_library()
+    F = len(features)
+    specs = (_FeatureSpec * max(F, 1))(*[_FeatureSpec(d, {"f32": MT_F32, "bf16": MT_BF16}[t], c)
+                                        for d, t, c in features])
+    pl = (_Placement * max(F, 1))()
+    gr = (_MergeGroup * max(F, 1))()
+    G = ctypes.c_int()
+    _check(L.mt_plan_merge(specs, F, float(max_load), pl, gr, ctypes.byref(G)), "mt_plan_merge")
+    placement = [(int(pl[f].group), int(pl[f].table_id)) for f in range(F)]
+    groups = [dict(dim=int(gr[g].dim), row_dtype="f32" if gr[g].row_dtype == MT_F32 else "bf16",
+                   log2_slots=int(gr[g].log2_slots), num_features=int(gr[g].num_features),
+                   capacity=int(gr[g].capacity)) for g in range(G.value)]
+    return placement, groups
+
+
+class MergedTables:
+    """The merged tables of a plan (``plan_merge``) and the lookup that routes a batch's feature segments
+    to them (``mt_lookup_grouped``); backward is per merged table."""
+
+    def __init__(self, features, max_load: float = 0.5, device=None, **table_kwargs):
+        self.lib = load_library()
+        self.placement, self.groups = plan_merge(features, max_load)
+        self.tables = [Table(g["log2_slots"], g["dim"], row_dtype=g["row_dtype"], device=device, **table_kwargs)
+                       for g in self.groups]
+        self.device = self.tables[0].device
+        self._pl = (_Placement * len(self.placement))(*[_Placement(g, t) for g, t in self.placement])
+        self._ws = None
+
+    def group_sizes(self, feat_offsets):
+        """IDs each merged table receives from a batch with these feature offsets."""
+        fo = np.asarray(feat_offsets, dtype=np.int64)
+        sizes = [0] * len(self.tables)
+        for f, (g, _) in enumerate(self.placement):
+            sizes[g] += int(fo[f + 1] - fo[f])
+        return sizes
+
+    def lookup(self, ids, feat_offsets, insert_missing: bool = True, gather: bool = True, stream=None):
+        """ids: int64 CUDA tensor [n]; feat_offsets: host sequence of F+1.  Returns one LookupResult per
+        merged table (its IDs are the batch's segments of its features, in feature order)."""
+        torch = _torch()
+        fo = np.ascontiguousarray(feat_offsets, dtype=np.int64)
+        F = fo.size - 1
+        if F != len(self.placement):
+            raise ValueError("one segment per planned feature")
+        n = int(ids.numel())
+        sizes = self.group_sizes(fo)
+        res = [t.new_result(sz, gather=gather) for t, sz in zip(self.tables, sizes)]
+        G = len(self.tables)
+        wsb = self.lib.mt_lookup_grouped_workspace_bytes(n)
+        if self._ws is None or self._ws.numel() < wsb:
+            self._ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=self.device)
+        tabs = (ctypes.c_void_p * G)(*[t.h.value for t in self.tables])
+        outs = (ctypes.c_void_p * G)(*[(r.rows.data_ptr() if (gather and r.n) else None) for r in res])
+        st = (_Result * G)(*[r.as_struct() for r in res])
+        gn = np.zeros(G, dtype=np.int64)
+        _check(self.lib.mt_lookup_grouped(tabs, G, self._pl, ids.data_ptr() if n else None, n,
+                                          fo.ctypes.data_as(ctypes.c_void_p), F, int(bool(insert_missing)), outs, st,
+                                          gn.ctypes.data_as(ctypes.c_void_p), self._ws.data_ptr(), self._ws.numel(),
+                                          _stream(stream)), "mt_lookup_grouped")
+        if list(gn) != sizes:
+            raise RuntimeError("group sizes disagree with the plan")
+        return res
+
+    def backward_adam(self, results, grads, **adam):
+        """grads: one CUDA tensor [n_g, dim_g] per merged table."""
+        return [t.backward_adam(r, g, **adam) for t, r, g in zip(self.tables, results, grads)]

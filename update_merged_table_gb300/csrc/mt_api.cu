@@ -30,6 +30,12 @@ struct mt_table {
   long long step;    // host-side count of backward calls
 };
 
+namespace mt {
+const TableDev& table_dev(const mt_table* t) { return t->dev; }
+mt_config table_cfg(const mt_table* t) { return t->cfg; }
+void table_count_step(mt_table* t) { t->step += 1; }
+}  // namespace mt
+
 namespace {
 
 using mt::align_up;
@@ -404,6 +410,9 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
     p.sc = reinterpret_cast<mt::ScSlot*>(w + L.sc);
     p.ss = L.ss;
     p.ulist_n = reinterpret_cast<uint32_t*>(w + L.ulist_n);
+    p.fresh_n = p.ulist_n + 1;
+    p.fresh_row = reinterpret_cast<int32_t*>(w + L.fresh_row);
+    p.fresh_key = reinterpret_cast<unsigned long long*>(w + L.fresh_key);
     p.ulist = reinterpret_cast<int32_t*>(w + L.ulist);
     p.sc_row = reinterpret_cast<int32_t*>(w + L.sc_row);
     p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);

@@ -82,7 +82,8 @@ __device__ __forceinline__ int warp_chunks(int c, int wc) { return c > kChunk ? 
 __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
   if (blockIdx.x == p.nblk) {  // the extra block: step counter and this step's Adam scalars
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && p.reduce_only) p.work[0] = 0;
+    if (threadIdx.x == 0 && !p.reduce_only) {
       p.T.hdr->step += 1;
       p.work[0] = 0;
       // the beta-power accumulators advance by one multiply each (in
@@ -667,7 +668,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
 #pragma unroll
           for (int j = 0; j < VEC / 2; ++j) gs[j] = add2(hi[j], lo[j]);
           if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
-          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
+          if (row >= 0 && !p.reduce_only) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
         } else {
           double* a = p.acc64 + (size_t)h * d + col;
 #pragma unroll
@@ -695,7 +696,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
 #pragma unroll
           for (int j = 0; j < VEC / 2; ++j) gs[j] = pk((float)__ldcg(a + 2 * j), (float)__ldcg(a + 2 * j + 1));
           if (p.gsum_out != nullptr) store_gsum(p.gsum_out, hinfo.x, d, col, gs, VEC);
-          if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
+          if (row >= 0 && !p.reduce_only) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
         }
       }
     }
@@ -781,7 +782,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
 #pragma unroll
       for (int j = 0; j < VEC / 2; ++j) gs[j] = add2(hi[j], lo[j]);
       if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
-      if (row >= 0) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
+      if (row >= 0 && !p.reduce_only) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
     }
     __syncwarp(team_mask);  // every lane is done with my_pos
 #pragma unroll

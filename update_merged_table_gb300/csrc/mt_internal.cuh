@@ -104,6 +104,7 @@ __device__ __forceinline__ unsigned long long load_key_relaxed(const unsigned lo
 // table view lives in kernel parameter space, which dynamic indexing would
 // copy to local memory).
 __device__ __forceinline__ char* row_ptr(const TableDev& T, int32_t row) {
+  if (T.nseg == 1) return T.seg_base[0] + (size_t)row * T.rec_bytes;  // a table that never grew its rows
   char* base = T.seg_base[0];
   long long first = 0;
 #pragma unroll
@@ -135,17 +136,19 @@ __device__ __forceinline__ void philox4x64_10(unsigned long long c0, unsigned lo
   out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-// Initial values of columns 4g .. 4g+3 of the row of `key`: the top 24 bits
-// q of each Philox word give (2q - 2^24) / 2^24 exactly; one fp32 multiply by
-// the scale is the only rounding.
-__device__ __forceinline__ void init_quad(const TableDev& T, unsigned long long key, uint32_t g, float v[4]) {
+// Initial values of columns 8g .. 8g+7 of the row of `key` from one
+// Philox4x64-10 block (counter (g, 0, 0, 0), key (merged key, init seed)):
+// word k serves columns 8g+2k (its bits 63..40) and 8g+2k+1 (bits 39..16).
+// Each 24-bit integer q gives (2q - 2^24) / 2^24 exactly; one fp32 multiply
+// by the scale is the only rounding.
+__device__ __forceinline__ void init_oct(const TableDev& T, unsigned long long key, uint32_t g, float v[8]) {
   unsigned long long w[4];
   philox4x64_10((unsigned long long)g, 0ull, 0ull, 0ull, key, T.init_seed, w);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    int q = (int)(w[k] >> 40);
-    float unit = (float)(2 * q - (1 << 24)) * (1.0f / 16777216.0f);
-    v[k] = __fmul_rn(unit, T.init_scale);
+    const int q0 = (int)(w[k] >> 40), q1 = (int)((w[k] >> 16) & 0xFFFFFFull);
+    v[2 * k] = __fmul_rn((float)(2 * q0 - (1 << 24)) * (1.0f / 16777216.0f), T.init_scale);
+    v[2 * k + 1] = __fmul_rn((float)(2 * q1 - (1 << 24)) * (1.0f / 16777216.0f), T.init_scale);
   }
 }
 
@@ -154,29 +157,24 @@ __device__ __forceinline__ void init_quad(const TableDev& T, unsigned long long 
 __device__ __forceinline__ void init_row_coop(const TableDev& T, int32_t row, unsigned long long key, int l, int nl) {
   char* rec = row_ptr(T, row);
   const uint32_t d = T.dim;
-  if (T.row_dtype == MT_F32) {
-    float4* e = reinterpret_cast<float4*>(rec);
-    for (uint32_t g = l; g < d / 4; g += nl) {
-      float v[4];
-      init_quad(T, key, g, v);
-      e[g] = make_float4(v[0], v[1], v[2], v[3]);
-    }
-  } else {
-    uint4* e = reinterpret_cast<uint4*>(rec);
-    for (uint32_t g8 = l; g8 < d / 8; g8 += nl) {
-      float a[4], b[4];
-      init_quad(T, key, 2 * g8, a);
-      init_quad(T, key, 2 * g8 + 1, b);
-      __nv_bfloat162 p0 = __floats2bfloat162_rn(a[0], a[1]);
-      __nv_bfloat162 p1 = __floats2bfloat162_rn(a[2], a[3]);
-      __nv_bfloat162 p2 = __floats2bfloat162_rn(b[0], b[1]);
-      __nv_bfloat162 p3 = __floats2bfloat162_rn(b[2], b[3]);
+  for (uint32_t g = l; g < (d + 7) / 8; g += nl) {
+    float v[8];
+    init_oct(T, key, g, v);
+    if (T.row_dtype == MT_F32) {
+      float4* e = reinterpret_cast<float4*>(rec) + 2 * g;
+      e[0] = make_float4(v[0], v[1], v[2], v[3]);
+      if (8 * g + 4 < d) e[1] = make_float4(v[4], v[5], v[6], v[7]);  // d is a multiple of 4
+    } else {
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(v[4], v[5]);
+      __nv_bfloat162 p3 = __floats2bfloat162_rn(v[6], v[7]);
       uint4 u;
       u.x = *reinterpret_cast<uint32_t*>(&p0);
       u.y = *reinterpret_cast<uint32_t*>(&p1);
       u.z = *reinterpret_cast<uint32_t*>(&p2);
       u.w = *reinterpret_cast<uint32_t*>(&p3);
-      e[g8] = u;
+      reinterpret_cast<uint4*>(rec)[g] = u;
     }
   }
   float4* mv = reinterpret_cast<float4*>(rec + T.emb_bytes);

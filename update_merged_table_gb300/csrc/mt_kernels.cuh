@@ -36,6 +36,8 @@ struct LookupParams {
   long long n;
   int F;
   int insert_missing;
+  int keys_in;            // 1: ids[] already hold merged keys (no encoding; sentinels are invalid)
+  int no_table;           // 1: deduplicate only; the table is not read (unique rows -1)
   long long feat_off[MT_MAX_FEATURES + 1];
   unsigned char table_ids[MT_MAX_FEATURES];
   void* out_rows;
@@ -49,6 +51,9 @@ struct LookupParams {
   ScSlot* sc;             // [ss] stage-2 scratch hash
   unsigned long long ss;  // scratch slots (>= n + 1; not a power of two)
   uint32_t* ulist_n;      // distinct keys listed so far, minus one
+  uint32_t* fresh_n;      // fresh rows listed so far, minus one (the word after ulist_n)
+  int32_t* fresh_row;     // [n] rows inserted by this lookup
+  unsigned long long* fresh_key;  // [n] their keys
   int32_t* ulist;         // [n] scratch slot of each distinct key, in claim order
   int32_t* sc_row;        // [ss] table row of the key in a slot (-1: none)
   int32_t* tile_L;        // [ntiles] tile-local uniques per tile
@@ -64,7 +69,8 @@ struct LookupParams {
 };
 
 struct LookupWsLayout {
-  size_t sc, ulist_n, ulist, sc_row, tile_L, tile_O, tile_pre, done, first_slot, lsslot, lidx, total;
+  size_t sc, ulist_n, ulist, fresh_row, fresh_key, sc_row, tile_L, tile_O, tile_pre, done, first_slot, lsslot, lidx,
+      total;
   size_t clear_bytes;  // bytes from the start of the workspace cleared to all ones per call
   unsigned long long ss;
   int ntiles;
@@ -94,6 +100,7 @@ struct BackwardParams {
   float lr, beta1, beta2, eps;
   float one_minus_b1, one_minus_b2;
   float* gsum_out;
+  int reduce_only;      // 1: gradient sums only; no Adam step and no step counter change
   // workspace
   int32_t* bsum;        // [nblk * 3] per scan block: sums of counts, heavy chunks, heavy uniques
   int32_t* boff;        // [(nblk + 1) * 3] exclusive offsets (+ totals)

@@ -24,14 +24,16 @@
 //             from the tile it lowers the first position of.
 //  k_resolve  one thread per distinct key, over the whole GPU: find the key in
 //             the table (odd-step probing) or insert it (first tombstone or
-//             EMPTY slot of its chain, rows popped once per block, fresh rows
-//             initialised by teams of lanes); note the key at its first
-//             position.  The last block to finish turns the per-tile counts
+//             EMPTY slot of its chain, rows popped once per block; fresh
+//             rows listed for k_expand); note the key at its first position.  The last block to finish turns the per-tile counts
 //             of first positions into tile offsets.
 //  k_number   per tile: the keys first seen in the tile take unique indices
 //             tile offset + their order inside the tile, i.e. first-occurrence
 //             order, and write the unique keys, rows and counts.
-//  k_expand   per tile: inverse index of every position.
+//  k_expand   per tile: inverse index of every position; then a share of the
+//             fresh rows is initialised (Philox-keyed values, m = v = 0) by
+//             teams of lanes, filling the issue slots of this latency-bound
+//             kernel.
 //  k_gather   the 16-byte vectorised row gather over the whole batch.
 // No kernel waits on another block.
 #include <atomic>
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   __shared__ int s_wbase;      // where the block's distinct keys go in the list
 
   const int tile = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const long long base = (long long)tile * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
 
@@ -148,8 +150,13 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
         const int mid = (lo + hi) >> 1;
         if (s_off[mid] <= i) lo = mid; else hi = mid;
       }
-      valid = id >= 0 && (unsigned long long)id < kIdLimit;
-      key = ((unsigned long long)s_tid[lo] << 56) | (unsigned long long)id;
+      if (p.keys_in) {  // a merged key as it is; table id 255 holds the sentinels
+        key = (unsigned long long)id;
+        valid = (key >> 56) != 0xFFull;
+      } else {
+        valid = id >= 0 && (unsigned long long)id < kIdLimit;
+        key = ((unsigned long long)s_tid[lo] << 56) | (unsigned long long)id;
+      }
       bad |= !valid;
     }
     if (valid) {
@@ -225,15 +232,22 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
     const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
     unsigned long long h = stage2_home(key, p.ss);
     bool won = false;
+    uint32_t seen_first = 0xFFFFFFFFu;  // a first position the slot already held (it only ever decreases)
     for (unsigned long long probe = 0; probe < p.ss; ++probe) {
-      const unsigned long long cur = atomicCAS(&p.sc[h].key, kEmpty, key);
+      // a plain load first: the hottest keys are claimed by nearly every tile, and an atomic on their
+      // slot would queue behind every other tile's at the L2
+      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h]));
+      unsigned long long cur = sv.x;
+      if (cur == kEmpty) cur = atomicCAS(&p.sc[h].key, kEmpty, key);
       if (cur == kEmpty || cur == key) {
         won = cur == kEmpty;
+        if (sv.x == key) seen_first = (uint32_t)(sv.y & 0xFFFFFFFFull);
         break;
       }
       h = h + 1 == p.ss ? 0ull : h + 1;
     }
-    const uint32_t prev_first = atomicMin(&p.sc[h].first, gpos);
+    // lower the key's first position only when this tile can (a later tile of a hot key cannot)
+    const uint32_t prev_first = gpos < seen_first ? atomicMin(&p.sc[h].first, gpos) : seen_first;
     const uint32_t before = atomicAdd(&p.sc[h].cnt, s_cnt[sl]) + 1u;  // the slot starts at "count - 1" = 2^32 - 1
     s_cnt[sl] = before;  // rank base of this tile's positions of the key
     p.lsslot[lb + li] = (int32_t)h;
@@ -270,18 +284,12 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
 __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
   __shared__ int s_need, s_nnew, s_avail;
   __shared__ long long s_rowbase;
-  __shared__ int32_t s_newrow[kThreadsR];
-  __shared__ unsigned long long s_newkey[kThreadsR];
   __shared__ int s_warp[kThreadsR / 32];
   __shared__ bool s_last;
 
   const int tid = threadIdx.x;
   const uint32_t U = *p.ulist_n + 1u;  // the counter starts at 2^32 - 1
   const uint32_t step = (uint32_t)p.T.hdr->step;
-  const uint32_t vecs = p.T.row_dtype == MT_F32 ? p.T.dim / 4 : p.T.dim / 8;
-  int team = 1;
-  while (team < 32 && team < (int)vecs) team <<= 1;
-  const int nteams = kThreadsR / team, my_team = tid / team, lt = tid % team;
 
   for (uint32_t b0 = blockIdx.x * kThreadsR; b0 < U; b0 += gridDim.x * kThreadsR) {  // block-uniform trip count
     const uint32_t idx = b0 + tid;
@@ -300,9 +308,9 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
       const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[slot]));
       key = sv.x;
       gfirst = (uint32_t)(sv.y & 0xFFFFFFFFull);
-      long long t_end, t_tomb;
-      const long long sidx = find_slot(p.T, key, &t_end, &t_tomb, &row);
-      if (sidx < 0 && p.insert_missing) {
+      long long t_end = 0, t_tomb = -1;
+      const long long sidx = p.no_table ? -1 : find_slot(p.T, key, &t_end, &t_tomb, &row);
+      if (sidx < 0 && p.insert_missing && !p.no_table) {
         // absent, and no other thread inserts it (its key is listed once):
         // take the first tombstone of its chain, else the EMPTY slot that
         // ended the chain, else the next free slot after them
@@ -336,9 +344,6 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
         row = p.T.free_stack[s_rowbase - 1 - q];
         p.T.slots[cs].row = row;
         p.T.slots[cs].meta = step;
-        const int w = atomicAdd(&s_nnew, 1);
-        s_newrow[w] = row;
-        s_newkey[w] = key;
       } else {
         atomicExch(&p.T.slots[cs].key, kTomb);  // give the slot back; the chain stays intact
         latch_error(p.T.hdr, MT_EFULL);
@@ -348,9 +353,16 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
       p.sc_row[slot] = row;
       p.first_slot[gfirst] = slot;
     }
+    // the block's fresh rows join the list k_expand initialises (one global atomic per block)
+    const bool fresh = claimed && q < s_avail;
+    const int w = fresh ? atomicAdd(&s_nnew, 1) : -1;
     __syncthreads();
-    const int nnew = s_nnew;
-    for (int w = my_team; w < nnew; w += nteams) init_row_coop(p.T, s_newrow[w], s_newkey[w], lt, team);
+    if (tid == 0 && s_nnew > 0) s_rowbase = (long long)(atomicAdd(p.fresh_n, (uint32_t)s_nnew) + 1u);  // from 2^32-1
+    __syncthreads();
+    if (fresh) {
+      p.fresh_row[s_rowbase + w] = row;
+      p.fresh_key[s_rowbase + w] = key;
+    }
     __syncthreads();
   }
 
@@ -433,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_number(const LookupParams p) {
 }
 
 // inverse[i] = unique index of position i (-1 for an invalid ID).
-__global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
+__global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
   __shared__ int32_t s_u[kTile];  // unique index of each tile-local unique
   const int tile = blockIdx.x, tid = threadIdx.x;
   const long long base = (long long)tile * kTile;
@@ -463,6 +475,17 @@ __global__ void __launch_bounds__(kThreads) k_expand(const LookupParams p) {
     const int lp = k * kThreads + tid;
     if (lp < cnt) p.inverse[base + lp] = li[k] == kNoIdx ? -1 : s_u[li[k]];
   }
+  // this block's share of the fresh rows: init(key), m = v = 0, one team of lanes per row (8 columns
+  // per lane and Philox block).  The arithmetic fills the issue slots this latency-bound kernel leaves.
+  const long long F = (long long)(uint32_t)(*p.fresh_n + 1u);  // the counter starts at 2^32 - 1
+  const long long per = (F + gridDim.x - 1) / gridDim.x;
+  const long long f0 = (long long)tile * per, f1 = min(f0 + per, F);
+  const int oct = (int)((p.T.dim + 7) / 8);
+  int team = 1;
+  while (team < 32 && team < oct) team <<= 1;
+  const int nteams = kThreads / team;
+  for (long long f = f0 + tid / team; f < f1; f += nteams)
+    init_row_coop(p.T, __ldcg(&p.fresh_row[f]), __ldcg(&p.fresh_key[f]), tid % team, team);
 }
 
 // out[i] = row of unique inverse[i] (zeros for an invalid ID or an absent
@@ -526,12 +549,14 @@ LookupWsLayout lookup_ws_layout(long long n) {
   };
   const size_t cap = (size_t)L.ntiles * kTile;
   L.sc = take(L.ss * sizeof(ScSlot));
-  L.ulist_n = off;  // right after the slots, then the tile counts: one memset clears all three
-  off += 16;
+  L.ulist_n = off;  // right after the slots (with the fresh-row counter), then the tile counts: one memset
+  off += 16;        // clears them all
   L.tile_O = off;
   L.clear_bytes = off + (size_t)L.ntiles * 4;
   take((size_t)L.ntiles * 4);
   L.ulist = take((size_t)(n > 0 ? n : 1) * 4);
+  L.fresh_row = take((size_t)(n > 0 ? n : 1) * 4);
+  L.fresh_key = take((size_t)(n > 0 ? n : 1) * 8);
   L.sc_row = take(L.ss * 4);
   L.tile_L = take((size_t)L.ntiles * 4);
   L.tile_pre = take((size_t)(L.ntiles + 1) * 4);
