@@ -1,9 +1,10 @@
 """Sharded two-stage deduplication: G logical ranks with one shard table each, on one GPU (through the C ABI).
 
 Each rank's unique keys, inverse and counts are its own batch's first-occurrence unique (bit-exact against
-the oracle); the rows a rank receives equal those of one table holding every key (bit-exact); the gradient
-sums over all ranks and the Adam-updated rows match one oracle table fed the concatenation of the ranks'
-batches (fp32 within 1e-5 relative + 1e-6 absolute; bf16 within one ulp); every key lives in one shard only.
+the oracle); the rows a rank receives equal those of one table holding every key (bit-exact before any
+training); the gradient sums over all ranks and the Adam-updated rows match one oracle table fed the
+concatenation of the ranks' batches (fp32 within 1e-5 relative + 1e-6 absolute; bf16 within one ulp: each
+rank's sum is rounded to fp32 before the owner adds them); every key lives in one shard only.
 """
 import numpy as np
 import pytest
@@ -67,7 +68,10 @@ def run_sharded(G, dim, row_dtype, steps, make_batch, log2=14):
         start = 0
         for r, b in enumerate(batches):
             want = r_all["rows"][start:start + b.n]
-            assert np.array_equal(res[r].rows.float().cpu().numpy(), want)
+            if step == 0:  # untrained rows: bit-exact
+                assert np.array_equal(res[r].rows.float().cpu().numpy(), want)
+            else:  # rows trained from two-stage sums (rank sums rounded once each): the stated tolerance
+                assert_rows_close(res[r].rows.float().cpu().numpy(), want, row_dtype)
             start += b.n
         # backward: every rank's gradients; the oracle sees them concatenated in the same order
         gs = [W.grads_normal(100 * step + r, b.n, dim) for r, b in enumerate(batches)]
@@ -80,11 +84,19 @@ def run_sharded(G, dim, row_dtype, steps, make_batch, log2=14):
             ref_gsum = ref.backward_adam(np.concatenate(gs), want_gsum=True)
         ukeys_all = r_all["unique"]
         pos = {int(k): i for i, k in enumerate(ukeys_all)}
+        # each rank's sum is rounded to fp32 before the owner adds them (exactly) and rounds once more: with
+        # S = sum of |g| over the key's positions, |error| <= 2^-24 * (S + |sum|) <= 2^-23 * S
+        gabs = np.abs(torch.cat(gt).float().numpy()).astype(np.float64)
+        S = np.zeros((ukeys_all.size, dim), np.float64)
+        np.add.at(S, r_all["inverse"], gabs)
         for r in range(G):
             U = res[r].U
             uk = res[r].unique_keys[:U].cpu().numpy().view(np.uint64)
-            want = ref_gsum[[pos[int(k)] for k in uk]]
-            np.testing.assert_allclose(gsum[r][:U].cpu().numpy(), want, rtol=RTOL, atol=ATOL)
+            idx = [pos[int(k)] for k in uk]
+            want = ref_gsum[idx]
+            got = gsum[r][:U].cpu().numpy()
+            bound = RTOL * np.abs(want) + ATOL + 2.0 ** -23 * S[idx]
+            assert (np.abs(got.astype(np.float64) - want) <= bound).all()
     # the trained rows, read back through another sharded lookup without inserts
     batches = [make_batch(steps - 1, r) for r in range(G)]
     res = grp.lookup([to_dev(b.ids) for b in batches], [b.feat_offsets for b in batches], batches[0].table_ids,

@@ -57,62 +57,86 @@ namespace {
 
 // Owner of a key: the high 32 bits of a second mix of the key, scaled to [0, G).
 __device__ __forceinline__ int owner_of(unsigned long long key, int G) {
-  return (int)(((mix64(key ^ 0xD6E8FEB86659FD93ull) >> 32) * (unsigned long long)G) >> 32);
+  const unsigned hi = (unsigned)(mix64(key ^ 0xD6E8FEB86659FD93ull) >> 32);
+  return (int)(((unsigned long long)hi * (unsigned)G) >> 32);
 }
 
 struct ShardOffsets {
   long long off[MT_MAX_SHARDS * MT_MAX_SHARDS];  // off[o * G + r]: where rank r's keys for owner o start
 };
 
-// counts[r * G + o] += keys of rank r owned by o (a block histogram, then one atomic per owner).
+// counts[r * G + o] += keys of rank r owned by o: per warp and owner one
+// ballot, and one atomic by the first lane that holds a key of that owner.
 __global__ void __launch_bounds__(256) k_shard_count(const unsigned long long* keys, long long U, int G, int r,
                                                      int32_t* counts) {
-  __shared__ int s_cnt[MT_MAX_SHARDS];
-  if (threadIdx.x < MT_MAX_SHARDS) s_cnt[threadIdx.x] = 0;
-  __syncthreads();
-  for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < U; u += (long long)gridDim.x * blockDim.x)
-    atomicAdd(&s_cnt[owner_of(keys[u], G)], 1);
-  __syncthreads();
-  if (threadIdx.x < G && s_cnt[threadIdx.x]) atomicAdd(&counts[r * G + threadIdx.x], s_cnt[threadIdx.x]);
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long u0 = (long long)blockIdx.x * blockDim.x; u0 < U; u0 += stride) {  // warp-uniform
+    const long long u = u0 + threadIdx.x;
+    const int o = u < U ? owner_of(keys[u], G) : -1;
+    for (int q = 0; q < G; ++q) {
+      const unsigned m = __ballot_sync(kFull, o == q);
+      if (m != 0 && lane == __ffs(m) - 1) atomicAdd(&counts[r * G + q], __popc(m));
+    }
+  }
 }
 
 // The exchange of keys: rank r writes each unique key into its owner's
 // receive buffer (order within a (rank, owner) segment unspecified) and
-// records where it went.
+// records where it went; the lanes of a warp with the same owner take
+// consecutive places with one atomic.
 __global__ void __launch_bounds__(256) k_shard_send(const unsigned long long* keys, long long U, int G, int r,
                                                     const ShardOffsets off, int32_t* cursor,
-                                                    unsigned long long* recv_keys, int32_t* perm) {
-  for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < U; u += (long long)gridDim.x * blockDim.x) {
-    const unsigned long long key = keys[u];
-    const int o = owner_of(key, G);
-    const long long slot = off.off[o * G + r] + atomicAdd(&cursor[r * G + o], 1);
-    recv_keys[slot] = key;
-    perm[u] = (int32_t)slot;
+                                                    unsigned long long* recv_keys, long long recv_cap, int32_t* perm,
+                                                    Header* hdr) {
+  const int lane = threadIdx.x & 31;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long u0 = (long long)blockIdx.x * blockDim.x; u0 < U; u0 += stride) {  // warp-uniform
+    const long long u = u0 + threadIdx.x;
+    const unsigned long long key = u < U ? keys[u] : 0ull;
+    const int o = u < U ? owner_of(key, G) : -1;
+    long long slot = -1;
+    for (int q = 0; q < G; ++q) {
+      const unsigned m = __ballot_sync(kFull, o == q);
+      if (m == 0) continue;
+      const int leader = __ffs(m) - 1;
+      int base = 0;
+      if (lane == leader) base = atomicAdd(&cursor[r * G + q], __popc(m));
+      base = __shfl_sync(kFull, base, leader);
+      if (o == q) slot = off.off[q * G + r] + base + __popc(m & ((1u << lane) - 1u));
+    }
+    if (slot >= recv_cap) {  // counts that disagree with the keys: reported, never written out of range
+      latch_error(hdr, MT_EINVAL);
+      slot = -1;
+    }
+    if (u < U) perm[u] = (int32_t)slot;
+    if (slot >= 0) recv_keys[slot] = key;
   }
 }
 
 // dst[i] = src[idx[i]] for rows of `vec16` 16-byte vectors (idx -1 or absent: zeros).
-__global__ void __launch_bounds__(256) k_shard_gather(const uint4* src, const int32_t* idx, long long n, int vec16,
-                                                      uint4* dst) {
+__global__ void __launch_bounds__(256) k_shard_gather(const uint4* src, long long src_rows, const int32_t* idx,
+                                                      long long n, int vec16, uint4* dst) {
   const long long total = n * vec16;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
     const long long i = it / vec16;
     const int v = (int)(it - i * vec16);
     const int32_t j = __ldg(&idx[i]);
-    dst[it] = j >= 0 ? __ldg(&src[(size_t)j * vec16 + v]) : make_uint4(0u, 0u, 0u, 0u);
+    dst[it] = (j >= 0 && j < src_rows) ? __ldg(&src[(size_t)j * vec16 + v]) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
 // dst[idx[i]] = src[i] for rows of `vec16` 16-byte vectors.
 __global__ void __launch_bounds__(256) k_shard_scatter(const uint4* src, const int32_t* idx, long long n, int vec16,
-                                                       uint4* dst) {
+                                                       uint4* dst, long long dst_rows) {
   const long long total = n * vec16;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
     const long long i = it / vec16;
     const int v = (int)(it - i * vec16);
-    dst[(size_t)__ldg(&idx[i]) * vec16 + v] = __ldg(&src[it]);
+    const int32_t j = __ldg(&idx[i]);
+    if (j >= 0 && j < dst_rows) dst[(size_t)j * vec16 + v] = __ldg(&src[it]);
   }
 }
 
@@ -121,10 +145,11 @@ __global__ void __launch_bounds__(256) k_shard_scatter(const uint4* src, const i
 // per-unique sums.
 __global__ void __launch_bounds__(256) k_shard_owner_unique(const unsigned long long* keys, const int32_t* perm,
                                                             long long U, int G, const ShardOffsets base,
-                                                            const int32_t* inv2, int32_t* out) {
+                                                            const int32_t* inv2, long long cap, int32_t* out) {
   for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < U; u += (long long)gridDim.x * blockDim.x) {
     const int o = owner_of(keys[u], G);
-    out[u] = (int32_t)(base.off[o] + __ldg(&inv2[perm[u]]));
+    const int32_t slot = perm[u];
+    out[u] = (slot >= 0 && slot < cap) ? (int32_t)(base.off[o] + __ldg(&inv2[slot])) : -1;
   }
 }
 
@@ -352,7 +377,8 @@ int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t*
     if (U[r] == 0) continue;
     MT_LAUNCH("k_shard_send", s);
     mt::k_shard_send<<<mt::grid_of(U[r]), 256, 0, s>>>(reinterpret_cast<const unsigned long long*>(results[r].unique_keys),
-                                                       U[r], G, r, off, cursor, recv_keys, perm + base[r]);
+                                                       U[r], G, r, off, cursor, recv_keys, t, perm + base[r],
+                                                       mt::table_dev(g->shards[r]).hdr);
   }
   // 4. stage 2 at every owner: dedup what arrived, find or insert in the shard, gather one row per received key
   char* recv_rows = w + L.recv_rows;
@@ -381,14 +407,14 @@ int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t*
     if (U[r] > 0) {
       MT_LAUNCH("k_shard_gather", s);
       mt::k_shard_gather<<<mt::grid_of(U[r] * vec16), 256, 0, s>>>(
-          reinterpret_cast<const uint4*>(recv_rows), perm + base[r], U[r], vec16,
+          reinterpret_cast<const uint4*>(recv_rows), t, perm + base[r], U[r], vec16,
           reinterpret_cast<uint4*>(uniq_rows + (size_t)base[r] * T0.emb_bytes));
     }
     if (out_rows != nullptr && out_rows[r] != nullptr && n[r] > 0) {
       MT_LAUNCH("k_shard_gather", s);
       mt::k_shard_gather<<<mt::grid_of(n[r] * vec16), 256, 0, s>>>(
-          reinterpret_cast<const uint4*>(uniq_rows + (size_t)base[r] * T0.emb_bytes), results[r].inverse, n[r], vec16,
-          static_cast<uint4*>(out_rows[r]));
+          reinterpret_cast<const uint4*>(uniq_rows + (size_t)base[r] * T0.emb_bytes), U[r], results[r].inverse, n[r],
+          vec16, static_cast<uint4*>(out_rows[r]));
     }
   }
   if (cudaGetLastError() != cudaSuccess) return MT_ECUDA;
@@ -485,7 +511,7 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
     MT_LAUNCH("k_shard_scatter", s);
     mt::k_shard_scatter<<<mt::grid_of(g->U[r] * gvec), 256, 0, s>>>(
         reinterpret_cast<const uint4*>(gsum + (size_t)g->rank_base[r] * d), perm + g->rank_base[r], g->U[r], gvec,
-        reinterpret_cast<uint4*>(recv_g));
+        reinterpret_cast<uint4*>(recv_g), g->ntot);
   }
   // 3. every owner: sums over the ranks per key, one Adam step on its shard (its step counter advances once)
   float* gsum2 = reinterpret_cast<float*>(w + L.gsum2);
@@ -513,11 +539,11 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
         MT_LAUNCH("k_shard_owner_unique", s);
         mt::k_shard_owner_unique<<<mt::grid_of(g->U[r]), 256, 0, s>>>(
             reinterpret_cast<const unsigned long long*>(results[r].unique_keys), perm + g->rank_base[r], g->U[r], G,
-            ob, reinterpret_cast<const int32_t*>(w + L.inv2), idx + g->rank_base[r]);
+            ob, reinterpret_cast<const int32_t*>(w + L.inv2), g->ntot, idx + g->rank_base[r]);
       }
       MT_LAUNCH("k_shard_gather", s);
       mt::k_shard_gather<<<mt::grid_of(g->U[r] * gvec), 256, 0, s>>>(
-          reinterpret_cast<const uint4*>(gsum2), idx + g->rank_base[r], g->U[r], gvec,
+          reinterpret_cast<const uint4*>(gsum2), g->ntot, idx + g->rank_base[r], g->U[r], gvec,
           reinterpret_cast<uint4*>(gsum_out[r]));
     }
   }
