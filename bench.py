@@ -225,11 +225,37 @@ def numa_cpus_for_gpu(pci_bus_id: str, sysfs: str = "/sys") -> tuple[set, str]:
     return cpus, "node 0 (no NUMA information for the GPU)" if cpus else "unbound"
 
 
+def gpu_pci_bus_id(dev_index: int):
+    """PCI bus id of the GPU torch calls `dev_index`: from torch's device properties where they carry it,
+    else from nvidia-smi, matched by the device UUID."""
+    import torch
+    props = torch.cuda.get_device_properties(dev_index)
+    for attr in ("pci_bus_id",):
+        v = getattr(props, attr, None)
+        if isinstance(v, str) and ":" in v:
+            return v
+    dom, bus, devn = (getattr(props, a, None) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id"))
+    if all(isinstance(x, int) for x in (dom, bus, devn)):
+        return f"{dom:08x}:{bus:02x}:{devn:02x}.0"
+    uuid = str(getattr(props, "uuid", "") or "")
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=uuid,pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout
+    except Exception:
+        return None
+    rows = [tuple(x.strip() for x in line.split(",")) for line in out.splitlines() if "," in line]
+    for u, b in rows:
+        if uuid and uuid.replace("GPU-", "") in u:
+            return b
+    return rows[dev_index][1] if dev_index < len(rows) else None
+
+
 def bind_to_gpu_numa_node(dev_index: int) -> str:
     """Run on the CPUs next to the GPU so pinned host buffers land in its NUMA node."""
     try:
-        import torch
-        bus = torch.cuda.get_device_properties(dev_index).pci_bus_id
+        bus = gpu_pci_bus_id(dev_index)
+        if bus is None:
+            return "unbound (no PCI bus id for the GPU)"
         cpus, how = numa_cpus_for_gpu(bus)
         avail = os.sched_getaffinity(0)
         cpus &= avail

@@ -225,37 +225,69 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   }
   __syncthreads();
   const size_t lb = (size_t)tile * kTile;
-  for (int li = tid; li < L; li += kThreadsA) {
-    const uint32_t it = s_item[li];
-    const uint32_t sl = it >> 16;
-    const unsigned long long key = s_key[sl];
-    const uint32_t gpos = (uint32_t)(base + (it & 0xFFFFu));
-    unsigned long long h = stage2_home(key, p.ss);
-    bool won = false;
-    uint32_t seen_first = 0xFFFFFFFFu;  // a first position the slot already held (it only ever decreases)
-    for (unsigned long long probe = 0; probe < p.ss; ++probe) {
+  // A thread's local uniques (at most kPPTA) go through each phase together, so their global round trips
+  // overlap: one plain load of each home slot, then the CAS of those found EMPTY, then the atomics.
+  uint32_t sl_[kPPTA], gpos_[kPPTA], seen_[kPPTA];
+  unsigned long long key_[kPPTA], h_[kPPTA], cur_[kPPTA];
+#pragma unroll
+  for (int k = 0; k < kPPTA; ++k) {
+    const int li = tid + k * kThreadsA;
+    if (li < L) {
+      const uint32_t it = s_item[li];
+      sl_[k] = it >> 16;
+      gpos_[k] = (uint32_t)(base + (it & 0xFFFFu));
+      key_[k] = s_key[sl_[k]];
+      h_[k] = stage2_home(key_[k], p.ss);
       // a plain load first: the hottest keys are claimed by nearly every tile, and an atomic on their
       // slot would queue behind every other tile's at the L2
-      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h]));
+      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h_[k]]));
+      cur_[k] = sv.x;
+      seen_[k] = sv.x == key_[k] ? (uint32_t)(sv.y & 0xFFFFFFFFull) : 0xFFFFFFFFu;  // it only ever decreases
+    }
+  }
+  bool won_[kPPTA];
+#pragma unroll
+  for (int k = 0; k < kPPTA; ++k) {
+    won_[k] = false;
+    if (tid + k * kThreadsA < L && cur_[k] == kEmpty) {
+      cur_[k] = atomicCAS(&p.sc[h_[k]].key, kEmpty, key_[k]);
+      won_[k] = cur_[k] == kEmpty;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPPTA; ++k) {  // the rare longer chains: probe on, one slot at a time
+    if (tid + k * kThreadsA >= L || won_[k] || cur_[k] == key_[k]) continue;
+    for (unsigned long long probe = 1; probe < p.ss; ++probe) {
+      h_[k] = h_[k] + 1 == p.ss ? 0ull : h_[k] + 1;
+      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h_[k]]));
       unsigned long long cur = sv.x;
-      if (cur == kEmpty) cur = atomicCAS(&p.sc[h].key, kEmpty, key);
-      if (cur == kEmpty || cur == key) {
-        won = cur == kEmpty;
-        if (sv.x == key) seen_first = (uint32_t)(sv.y & 0xFFFFFFFFull);
+      if (cur == kEmpty) cur = atomicCAS(&p.sc[h_[k]].key, kEmpty, key_[k]);
+      if (cur == kEmpty || cur == key_[k]) {
+        won_[k] = cur == kEmpty;
+        if (sv.x == key_[k]) seen_[k] = (uint32_t)(sv.y & 0xFFFFFFFFull);
         break;
       }
-      h = h + 1 == p.ss ? 0ull : h + 1;
     }
+  }
+  uint32_t prev_[kPPTA], before_[kPPTA];
+#pragma unroll
+  for (int k = 0; k < kPPTA; ++k) {
+    if (tid + k * kThreadsA >= L) continue;
     // lower the key's first position only when this tile can (a later tile of a hot key cannot)
-    const uint32_t prev_first = gpos < seen_first ? atomicMin(&p.sc[h].first, gpos) : seen_first;
-    const uint32_t before = atomicAdd(&p.sc[h].cnt, s_cnt[sl]) + 1u;  // the slot starts at "count - 1" = 2^32 - 1
-    s_cnt[sl] = before;  // rank base of this tile's positions of the key
-    p.lsslot[lb + li] = (int32_t)h;
-    if (gpos < prev_first) {
+    prev_[k] = gpos_[k] < seen_[k] ? atomicMin(&p.sc[h_[k]].first, gpos_[k]) : seen_[k];
+    before_[k] = atomicAdd(&p.sc[h_[k]].cnt, s_cnt[sl_[k]]) + 1u;  // the slot starts at "count - 1" = 2^32 - 1
+  }
+#pragma unroll
+  for (int k = 0; k < kPPTA; ++k) {
+    const int li = tid + k * kThreadsA;
+    if (li >= L) continue;
+    s_cnt[sl_[k]] = before_[k];  // rank base of this tile's positions of the key
+    p.lsslot[lb + li] = (int32_t)h_[k];
+    if (gpos_[k] < prev_[k]) {
       atomicAdd(&s_take, 1);
-      if (prev_first != 0xFFFFFFFFu) atomicAdd(&p.tile_O[prev_first / kTile], -1);
+      if (prev_[k] != 0xFFFFFFFFu) atomicAdd(&p.tile_O[prev_[k] / kTile], -1);
     }
-    if (won) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h;
+    if (won_[k]) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h_[k];
   }
   if (tid == 0) p.tile_L[tile] = L;
   __syncthreads();
