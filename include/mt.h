@@ -210,7 +210,7 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.
- *  - Every GPU that loads the library holds the array (4 MiB) until exit.
+ *  - Every GPU that loads the library holds the array (6 MiB) until exit.
  *  - All calls share the array: calls whose work overlaps on the GPU (other
  *    streams or host threads) race on it.  The array keeps the last call's
  *    contents; each call clears what it needs cleared.

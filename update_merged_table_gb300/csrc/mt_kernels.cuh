@@ -16,6 +16,7 @@ constexpr int kPPTA = kTile / kThreadsA; // positions per claim thread
 constexpr int kHS = 2 * kTile;           // shared-memory hash slots (backward fill)
 constexpr int kHSA = 3 * kTile / 2;      // shared-memory hash slots of stage 1 (load <= 2/3)
 constexpr int kThreadsR = 256;           // threads per resolve CTA (k_resolve)
+constexpr int kThreadsC = 256;           // threads per global-claim CTA (k_claim)
 constexpr uint16_t kNoIdx = 0xFFFF;
 
 // One slot of the stage-2 scratch hash.  The lookup clears the slots to all
@@ -52,6 +53,12 @@ struct LookupParams {
   unsigned long long ss;  // scratch slots (>= n + 1; not a power of two)
   uint32_t* ulist_n;      // distinct keys listed so far, minus one
   uint32_t* fresh_n;      // fresh rows listed so far, minus one (the word after ulist_n)
+  uint32_t* rec_n;        // tile-local uniques listed so far, minus one (the word after fresh_n)
+  ulonglong2* rec;        // [n] records {key, first position | count << 32}, each tile's together
+  int32_t* rec_slot;      // [n] scratch slot of each record's key
+  int32_t* rec_rb;        // [n] rank base of each record (positions of its key in records claimed before)
+  int32_t* tile_rec;      // [ntiles] where each tile's records start
+  uint16_t* lrank;        // [ntiles * kTile] rank of each position among its key's positions in the tile
   int32_t* fresh_row;     // [n] rows inserted by this lookup
   unsigned long long* fresh_key;  // [n] their keys
   int32_t* ulist;         // [n] scratch slot of each distinct key, in claim order
@@ -61,7 +68,6 @@ struct LookupParams {
   int32_t* tile_pre;      // [ntiles + 1] exclusive prefix of tile_O (written by the last k_resolve block)
   uint32_t* done;         // k_resolve blocks finished (zeroed by k_claim)
   int32_t* first_slot;    // [ntiles * kTile] scratch slot of the key first seen at each position, else -1
-  int32_t* lsslot;        // [ntiles * kTile] scratch slot of each tile-local unique
   uint16_t* lidx;         // [ntiles * kTile] tile-local unique of each position
   int ntiles;
   int resolve_grid;
@@ -69,8 +75,8 @@ struct LookupParams {
 };
 
 struct LookupWsLayout {
-  size_t sc, ulist_n, ulist, fresh_row, fresh_key, sc_row, tile_L, tile_O, tile_pre, done, first_slot, lsslot, lidx,
-      total;
+  size_t sc, ulist_n, ulist, rec, rec_slot, rec_rb, fresh_row, fresh_key, sc_row, tile_L, tile_O, tile_pre, done,
+      first_slot, tile_rec, lrank, lidx, total;
   size_t clear_bytes;  // bytes from the start of the workspace cleared to all ones per call
   unsigned long long ss;
   int ntiles;

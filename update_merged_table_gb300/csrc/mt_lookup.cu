@@ -11,29 +11,33 @@
 //
 // The unique keys come out in first-occurrence order.  Kernels, in launch
 // order (after one memset that clears the stage-2 scratch hash):
-//  k_claim    per tile of kTile positions: encode keys; stage 1: dedup inside
+//  k_local    stage 1, per tile of kTile positions: encode keys, dedup inside
 //             the tile with a shared-memory hash (first position, count and
-//             each position's rank among its key's positions); stage 2: each
-//             tile-local unique claims its key in the global scratch hash,
-//             lowers the key's first position there (atomicMin) and adds its
-//             count (the returned total is the rank base of the tile's
-//             positions, so the ranks are written here).  The one thread whose
-//             CAS put a key into the scratch hash lists the slot as a distinct
-//             key (one global atomic per block); the tile holding a key's
-//             first position so far counts the key, and takes the count over
-//             from the tile it lowers the first position of.
-//  k_resolve  one thread per distinct key, over the whole GPU: find the key in
-//             the table (odd-step probing) or insert it (first tombstone or
-//             EMPTY slot of its chain, rows popped once per block; fresh
-//             rows listed for k_expand); note the key at its first position.  The last block to finish turns the per-tile counts
-//             of first positions into tile offsets.
+//             each position's rank among its key's positions); every
+//             tile-local unique becomes one record {key, first position,
+//             count}, the tile's records stored together.
+//  k_claim    stage 2, one thread per record over the whole GPU: claim the
+//             key in the global scratch hash; one 64-bit atomic adds the
+//             record's count and returns the key's count and first position
+//             so far (the count is the rank base of the tile's positions);
+//             the first position is lowered only when this record can lower
+//             it.  The thread whose CAS put a key into the scratch hash lists
+//             it as a distinct key; the tile holding a key's first position so
+//             far counts the key, taking the count over from the tile whose
+//             first position it lowers.
+//  k_resolve  one thread per distinct key: find the key in the table
+//             (odd-step probing) or insert it (first tombstone or EMPTY slot
+//             of its chain, rows popped once per block; fresh rows listed for
+//             k_expand); note the key at its first position.  The last block
+//             to finish turns the per-tile counts of first positions into tile
+//             offsets.
 //  k_number   per tile: the keys first seen in the tile take unique indices
 //             tile offset + their order inside the tile, i.e. first-occurrence
 //             order, and write the unique keys, rows and counts.
-//  k_expand   per tile: inverse index of every position; then a share of the
-//             fresh rows is initialised (Philox-keyed values, m = v = 0) by
-//             teams of lanes, filling the issue slots of this latency-bound
-//             kernel.
+//  k_expand   per tile: inverse index and rank of every position; then a
+//             share of the fresh rows is initialised (Philox-keyed values,
+//             m = v = 0) by teams of lanes, filling the issue slots of this
+//             latency-bound kernel.
 //  k_gather   the 16-byte vectorised row gather over the whole batch.
 // No kernel waits on another block.
 #include <atomic>
@@ -86,7 +90,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 constexpr size_t kSmemA = kHSA * 8 + kHSA * 4 + kHSA * 4 + kTile * 4 + kTile * 2 + kTile * 2 +
                           (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
 
-__global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
+__global__ void __launch_bounds__(kThreadsA, 3) k_local(const LookupParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHSA] stage-1 hash keys
   uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHSA);             // [kHSA] first local position, then local index
@@ -98,9 +102,7 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
   __shared__ int s_warp[kThreadsA / 32];
   __shared__ int s_frange[2];  // features of the tile's first and last position
-  __shared__ int s_nwin;       // distinct keys this block put into the scratch hash
-  __shared__ int s_take;       // keys whose first position so far lies in this tile
-  __shared__ int s_wbase;      // where the block's distinct keys go in the list
+  __shared__ int s_rbase;      // where the tile's records start
 
   const int tile = blockIdx.x;
   const int tid = threadIdx.x;
@@ -207,112 +209,85 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_claim(const LookupParams p) {
   for (int lp = tid; lp < cnt; lp += kThreadsA) {
     const uint16_t sl = s_pslot[lp];
     p.lidx[base + lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
+    p.lrank[base + lp] = sl == kNoIdx ? (uint16_t)0 : s_lrank[lp];
     p.first_slot[base + lp] = -1;  // k_resolve notes each key at its first position
   }
-
-  // ---- stage 2: every local unique claims its key in the global scratch hash,
-  // lowers the key's first position and adds its count there.  The thread
-  // whose CAS put the key into the scratch hash is the only one in the grid to
-  // see it EMPTY; it lists the slot as a distinct key (the block's list goes
-  // out with one global atomic).  The tile that holds a key's first position
-  // so far counts the key; a tile that lowers the first position below
-  // another tile's takes the count over from it. ----
-  __syncthreads();  // s_min (local indices) is free from here: the block's new distinct keys are listed there
-  int32_t* s_win = reinterpret_cast<int32_t*>(s_min);  // [kHSA >= kTile]
+  // the tile's records, stored together (one global atomic per tile)
   if (tid == 0) {
-    s_nwin = 0;
-    s_take = 0;
+    s_rbase = L ? (int)(atomicAdd(p.rec_n, (uint32_t)L) + 1u) : 0;  // the counter starts at 2^32 - 1
+    p.tile_L[tile] = L;
+    p.tile_rec[tile] = s_rbase;
   }
   __syncthreads();
-  const size_t lb = (size_t)tile * kTile;
-  // A thread's local uniques (at most kPPTA) go through each phase together, so their global round trips
-  // overlap: one plain load of each home slot, then the CAS of those found EMPTY, then the atomics.
-  uint32_t sl_[kPPTA], gpos_[kPPTA], seen_[kPPTA];
-  unsigned long long key_[kPPTA], h_[kPPTA], cur_[kPPTA];
-#pragma unroll
-  for (int k = 0; k < kPPTA; ++k) {
-    const int li = tid + k * kThreadsA;
-    if (li < L) {
-      const uint32_t it = s_item[li];
-      sl_[k] = it >> 16;
-      gpos_[k] = (uint32_t)(base + (it & 0xFFFFu));
-      key_[k] = s_key[sl_[k]];
-      h_[k] = stage2_home(key_[k], p.ss);
-      // a plain load first: the hottest keys are claimed by nearly every tile, and an atomic on their
-      // slot would queue behind every other tile's at the L2
-      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h_[k]]));
-      cur_[k] = sv.x;
-      seen_[k] = sv.x == key_[k] ? (uint32_t)(sv.y & 0xFFFFFFFFull) : 0xFFFFFFFFu;  // it only ever decreases
-    }
-  }
-  bool won_[kPPTA];
-#pragma unroll
-  for (int k = 0; k < kPPTA; ++k) {
-    won_[k] = false;
-    if (tid + k * kThreadsA < L && cur_[k] == kEmpty) {
-      cur_[k] = atomicCAS(&p.sc[h_[k]].key, kEmpty, key_[k]);
-      won_[k] = cur_[k] == kEmpty;
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kPPTA; ++k) {  // the rare longer chains: probe on, one slot at a time
-    if (tid + k * kThreadsA >= L || won_[k] || cur_[k] == key_[k]) continue;
-    for (unsigned long long probe = 1; probe < p.ss; ++probe) {
-      h_[k] = h_[k] + 1 == p.ss ? 0ull : h_[k] + 1;
-      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h_[k]]));
-      unsigned long long cur = sv.x;
-      if (cur == kEmpty) cur = atomicCAS(&p.sc[h_[k]].key, kEmpty, key_[k]);
-      if (cur == kEmpty || cur == key_[k]) {
-        won_[k] = cur == kEmpty;
-        if (sv.x == key_[k]) seen_[k] = (uint32_t)(sv.y & 0xFFFFFFFFull);
-        break;
-      }
-    }
-  }
-  uint32_t prev_[kPPTA], before_[kPPTA];
-#pragma unroll
-  for (int k = 0; k < kPPTA; ++k) {
-    if (tid + k * kThreadsA >= L) continue;
-    // lower the key's first position only when this tile can (a later tile of a hot key cannot)
-    prev_[k] = gpos_[k] < seen_[k] ? atomicMin(&p.sc[h_[k]].first, gpos_[k]) : seen_[k];
-    before_[k] = atomicAdd(&p.sc[h_[k]].cnt, s_cnt[sl_[k]]) + 1u;  // the slot starts at "count - 1" = 2^32 - 1
-  }
-#pragma unroll
-  for (int k = 0; k < kPPTA; ++k) {
-    const int li = tid + k * kThreadsA;
-    if (li >= L) continue;
-    s_cnt[sl_[k]] = before_[k];  // rank base of this tile's positions of the key
-    p.lsslot[lb + li] = (int32_t)h_[k];
-    if (gpos_[k] < prev_[k]) {
-      atomicAdd(&s_take, 1);
-      if (prev_[k] != 0xFFFFFFFFu) atomicAdd(&p.tile_O[prev_[k] / kTile], -1);
-    }
-    if (won_[k]) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h_[k];
-  }
-  if (tid == 0) p.tile_L[tile] = L;
-  __syncthreads();
-  if (tid == 0) {
-    s_wbase = s_nwin ? (int)(atomicAdd(p.ulist_n, (uint32_t)s_nwin) + 1u) : 0;  // the counter starts at 2^32 - 1
-    if (s_take) atomicAdd(&p.tile_O[tile], s_take);
-  }
-  __syncthreads();
-  for (int w = tid; w < s_nwin; w += kThreadsA) p.ulist[s_wbase + w] = s_win[w];
-
-  if (p.ranks != nullptr) {
-    for (int lp = tid; lp < cnt; lp += kThreadsA) {
-      const uint16_t sl = s_pslot[lp];
-      p.ranks[base + lp] = sl == kNoIdx ? -1 : (int32_t)(s_cnt[sl] + s_lrank[lp]);
-    }
+  for (int li = tid; li < L; li += kThreadsA) {
+    const uint32_t it = s_item[li];
+    const uint32_t sl = it >> 16;
+    const ulonglong2 r = make_ulonglong2(s_key[sl], (unsigned long long)(uint32_t)(base + (it & 0xFFFFu)) |
+                                                       ((unsigned long long)s_cnt[sl] << 32));
+    __stcg(reinterpret_cast<ulonglong2*>(p.rec) + s_rbase + li, r);
   }
 }
 
-// One thread per distinct key, grid-stride over the list k_claim built.
-// Rows for inserted keys are popped from the free stack with one atomic per
-// block and iteration; a block's fresh rows are then initialised by teams of
-// lanes.  Every key is noted at its first position (first_slot) and counted
-// in the tile holding that position (tile_O).  The last block to finish
-// (counted on `done` after a fence) writes the exclusive prefix of tile_O and
-// the number of unique keys.
+// Stage 2: one thread per record {key, first position in its tile, count in
+// its tile}, over the whole GPU.  Each record's chain of global round trips is
+// short (a load of the key's home slot, a CAS when it is EMPTY, one 64-bit
+// atomic), and nothing waits on a block barrier in between.
+__global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
+  __shared__ int s_nwin, s_wbase;
+  __shared__ int32_t s_win[kThreadsC];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint32_t R = *p.rec_n + 1u;  // the counter starts at 2^32 - 1
+  for (uint32_t b0 = blockIdx.x * kThreadsC; b0 < R; b0 += gridDim.x * kThreadsC) {  // block-uniform trip count
+    const uint32_t r = b0 + tid;
+    const bool act = r < R;
+    if (tid == 0) s_nwin = 0;
+    __syncthreads();
+    bool won = false;
+    unsigned long long h = 0;
+    uint32_t gpos = 0, prev = 0xFFFFFFFFu;
+    if (act) {
+      const ulonglong2 rec = __ldcg(reinterpret_cast<const ulonglong2*>(p.rec) + r);
+      const unsigned long long key = rec.x;
+      gpos = (uint32_t)(rec.y & 0xFFFFFFFFull);
+      const uint32_t lcount = (uint32_t)(rec.y >> 32);
+      h = stage2_home(key, p.ss);
+      for (unsigned long long probe = 0; probe < p.ss; ++probe) {
+        // a plain load first: the hottest keys have a record from nearly every tile, and a CAS on their
+        // slot would queue behind every other tile's at the L2
+        unsigned long long cur = __ldcg(&p.sc[h].key);
+        if (cur == kEmpty) cur = atomicCAS(&p.sc[h].key, kEmpty, key);
+        if (cur == kEmpty || cur == key) {
+          won = cur == kEmpty;
+          break;
+        }
+        h = h + 1 == p.ss ? 0ull : h + 1;
+      }
+      // {first, count - 1} of the slot are one 64-bit word: adding the count to its high half returns both
+      const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h].first),
+                                               (unsigned long long)lcount << 32);
+      const uint32_t old_first = (uint32_t)(old & 0xFFFFFFFFull);
+      p.rec_rb[r] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before this record
+      p.rec_slot[r] = (int32_t)h;
+      // lower the key's first position only when this record can (the first position only decreases)
+      prev = gpos < old_first ? atomicMin(&p.sc[h].first, gpos) : old_first;
+    }
+    // a record that holds the key's first position so far counts the key for its tile
+    const bool take = act && gpos < prev;
+    const int t = (int)(gpos / kTile);
+    const int t0 = __shfl_sync(kFull, t, 0);
+    const unsigned same = __ballot_sync(kFull, take && t == t0);  // records of one tile are stored together
+    if (same && lane == __ffs(same) - 1) atomicAdd(&p.tile_O[t0], __popc(same));
+    if (take && t != t0) atomicAdd(&p.tile_O[t], 1);
+    if (take && prev != 0xFFFFFFFFu) atomicAdd(&p.tile_O[prev / kTile], -1);
+    if (won) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h;
+    __syncthreads();
+    if (tid == 0) s_wbase = s_nwin ? (int)(atomicAdd(p.ulist_n, (uint32_t)s_nwin) + 1u) : 0;  // from 2^32 - 1
+    __syncthreads();
+    if (tid < s_nwin) p.ulist[s_wbase + tid] = s_win[tid];
+    __syncthreads();  // s_nwin is reset by the next round
+  }
+}
+
 __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
   __shared__ int s_need, s_nnew, s_avail;
   __shared__ long long s_rowbase;
@@ -476,19 +451,22 @@ __global__ void __launch_bounds__(kThreads, 6) k_number(const LookupParams p) {
   }
 }
 
-// inverse[i] = unique index of position i (-1 for an invalid ID).
+// inverse[i] = unique index of position i (-1 for an invalid ID); ranks[i] =
+// the rank base of its tile's record + its rank inside the tile.
 __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
-  __shared__ int32_t s_u[kTile];  // unique index of each tile-local unique
+  __shared__ int32_t s_u[kTile];   // unique index of each tile-local unique
+  __shared__ int32_t s_rb[kTile];  // rank base of each tile-local unique
   const int tile = blockIdx.x, tid = threadIdx.x;
   const long long base = (long long)tile * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
   const int L = __ldg(&p.tile_L[tile]);
-  const size_t lb = (size_t)tile * kTile;
+  const int r0 = __ldg(&p.tile_rec[tile]);
   int32_t sl[kPPT];
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int l = k * kThreads + tid;
-    sl[k] = l < L ? __ldg(&p.lsslot[lb + l]) : -1;
+    sl[k] = l < L ? __ldcg(&p.rec_slot[r0 + l]) : -1;
+    if (l < L) s_rb[l] = __ldcg(&p.rec_rb[r0 + l]);
   }
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
@@ -506,6 +484,13 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
   for (int k = 0; k < kPPT; ++k) {
     const int lp = k * kThreads + tid;
     if (lp < cnt) p.inverse[base + lp] = li[k] == kNoIdx ? -1 : s_u[li[k]];
+  }
+  if (p.ranks != nullptr) {
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+      const int lp = k * kThreads + tid;
+      if (lp < cnt) p.ranks[base + lp] = li[k] == kNoIdx ? -1 : s_rb[li[k]] + (int32_t)__ldg(&p.lrank[base + lp]);
+    }
   }
   // this block's share of the fresh rows: init(key), m = v = 0, one team of lanes per row (8 columns
   // per lane and Philox block).  The arithmetic fills the issue slots this latency-bound kernel leaves.
@@ -587,6 +572,9 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.clear_bytes = off + (size_t)L.ntiles * 4;
   take((size_t)L.ntiles * 4);
   L.ulist = take((size_t)(n > 0 ? n : 1) * 4);
+  L.rec = take((size_t)(n > 0 ? n : 1) * 16);
+  L.rec_slot = take((size_t)(n > 0 ? n : 1) * 4);
+  L.rec_rb = take((size_t)(n > 0 ? n : 1) * 4);
   L.fresh_row = take((size_t)(n > 0 ? n : 1) * 4);
   L.fresh_key = take((size_t)(n > 0 ? n : 1) * 8);
   L.sc_row = take(L.ss * 4);
@@ -594,7 +582,8 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.tile_pre = take((size_t)(L.ntiles + 1) * 4);
   L.done = take(16);
   L.first_slot = take(cap * 4);
-  L.lsslot = take(cap * 4);
+  L.tile_rec = take((size_t)L.ntiles * 4);
+  L.lrank = take(cap * 2);
   L.lidx = take(cap * 2);
   L.total = off;
   return L;
@@ -604,29 +593,41 @@ cudaError_t launch_lookup(const LookupParams& p_in, cudaStream_t s) {
   if (p_in.n == 0) return cudaMemsetAsync(p_in.num_unique, 0, sizeof(long long), s);
   static std::atomic<int> gather_grid[kMaxDevices];   // 0: not set up on that device yet
   static std::atomic<int> resolve_slots[kMaxDevices];
+  static std::atomic<int> claim_slots[kMaxDevices];
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
   if (gather_grid[dev].load(std::memory_order_relaxed) == 0) {
-    cudaError_t e = cudaFuncSetAttribute(k_claim, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
+    cudaError_t e = cudaFuncSetAttribute(k_local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
     if (e != cudaSuccess) return e;
-    int sms = 0, per = 0, rper = 0;
+    int sms = 0, per = 0, rper = 0, cper = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, k_gather, 256, 0);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rper, k_resolve, kThreadsR, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cper, k_claim, kThreadsC, 0);
     resolve_slots[dev].store(sms * (rper > 0 ? rper : 1), std::memory_order_relaxed);
+    claim_slots[dev].store(sms * (cper > 0 ? cper : 1), std::memory_order_relaxed);
     gather_grid[dev].store(sms * (per > 0 ? per : 1), std::memory_order_relaxed);
   }
   LookupParams p = p_in;
-  const long long want = (p.n + kThreadsR - 1) / kThreadsR;  // blocks if every ID were distinct
-  const int slots = resolve_slots[dev].load(std::memory_order_relaxed);
-  p.resolve_grid = (int)(want < slots ? want : slots);
-  // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1), the distinct-key counter and the tile counts
-  // (both minus one): all ones
+  {
+    const long long want = (p.n + kThreadsR - 1) / kThreadsR;  // blocks if every ID were distinct
+    const int slots = resolve_slots[dev].load(std::memory_order_relaxed);
+    p.resolve_grid = (int)(want < slots ? want : slots);
+  }
+  const long long cwant = (p.n + kThreadsC - 1) / kThreadsC;
+  const int cslots = claim_slots[dev].load(std::memory_order_relaxed);
+  const int claim_grid = (int)(cwant < cslots ? cwant : cslots);
+  // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1), the list counters and the tile counts
+  // (all minus one): all ones
   cudaError_t e = cudaMemsetAsync(p.sc, 0xFF, p.clear_bytes, s);
   if (e != cudaSuccess) return e;
   {
+    MT_LAUNCH("k_local", s);
+    k_local<<<p.ntiles, kThreadsA, kSmemA, s>>>(p);
+  }
+  {
     MT_LAUNCH("k_claim", s);
-    k_claim<<<p.ntiles, kThreadsA, kSmemA, s>>>(p);
+    k_claim<<<claim_grid, kThreadsC, 0, s>>>(p);
   }
   {
     MT_LAUNCH("k_resolve", s);

@@ -24,7 +24,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = 4u << 20;  // 4 MiB: the lookup workspace for MT_LOOKUP_STATIC_MAX_IDS IDs
+constexpr size_t kStaticScratchBytes = 6u << 20;  // 6 MiB: the lookup workspace for MT_LOOKUP_STATIC_MAX_IDS IDs
 
 __device__ __align__(256) unsigned char g_lookup_scratch[kStaticScratchBytes];
 
