@@ -496,8 +496,9 @@ def pooled_run(args, tab, wl, dev, stream, first_seed: int):
     (mt_pool_forward) and the pooled backward + Adam (mt_backward_adam_pooled), on fresh batches, replayed as
     CUDA graphs with events between the two halves."""
     import torch
+    import update_merged_table_gb300 as mt
     steps = min(args.steps, 8)
-    seq = wl.steps(first_seed, steps)
+    seq = wl.steps(first_seed, steps + 1)  # the last batch: one eager pass for the per-kernel device times
     entries = []
     for j, (b, _) in enumerate(seq):
         U, _, _ = batch_stats(b)
@@ -519,6 +520,7 @@ def pooled_run(args, tab, wl, dev, stream, first_seed: int):
 
     # workspaces sized before capture (a capture must not allocate them)
     tab.reserve_workspaces(max(e["batch"].n for e in entries), max(e["Bg"] for e in entries))
+    prof_entry = entries.pop()
     torch.cuda.synchronize(dev)
     graphs = []
     for e in entries:
@@ -542,6 +544,13 @@ def pooled_run(args, tab, wl, dev, stream, first_seed: int):
     fwd_s = sum(a.elapsed_time(m_) for a, m_, _ in ev) / 1e3 / steps
     bwd_s = sum(m_.elapsed_time(z) for _, m_, z in ev) / 1e3 / steps
     new_keys = max(0.0, (tab.stats()["live"] - st0["live"]) / steps)
+    mt.profile_enable(True)
+    mt.profile_report(reset=True)
+    fwd(prof_entry)
+    bwd(prof_entry)
+    torch.cuda.synchronize(dev)
+    prof = mt.profile_report(reset=True)
+    mt.profile_enable(False)
     N = sum(e["batch"].n for e in entries) / steps
     U = sum(e["U"] for e in entries) / steps
     Bg = sum(e["Bg"] for e in entries) / steps
@@ -555,6 +564,7 @@ def pooled_run(args, tab, wl, dev, stream, first_seed: int):
                              "achieved": fwd_bytes / fwd_s / 1e9, "frac": fwd_bytes / fwd_s / 1e9 / peak},
             "roofline_bwd": {"bytes_per_step": bwd_bytes, "ms_per_step": bwd_s * 1e3,
                              "achieved": bwd_bytes / bwd_s / 1e9, "frac": bwd_bytes / bwd_s / 1e9 / peak},
+            "kernels_us": {k: round(1e3 * v[1] / v[0], 2) for k, v in prof.items()},
             "what": "lookup without the per-position gather + mean pooling of each (user, feature) bag; backward "
                     "of the pooling folded into the per-unique reduction + Adam (no per-position gradient rows)"}
 
@@ -596,7 +606,7 @@ def run_ours(args):
         e = dict(batch=b, U=U, H=H, NH=NH, erase=None, n_erase=0)
         e["ids_d"] = torch.from_numpy(b.ids).to(dev)
         e["grads_d"] = _device_grads(torch, dev, tdt[wl.grad], j, b.n, wl.dim)
-        e["res"] = tab.new_result(b.n, gather=True)
+        e["res"] = tab.new_result(b.n, gather=True, ranks=bool(args.ranks))
         if er is not None:
             e["erase"] = torch.from_numpy(er.astype(np.int64)).to(dev)
             e["n_erase"] = er.size
@@ -787,7 +797,7 @@ def run_ours(args):
                    "steps_cycle_fresh_batches": K > kf,
                    "step_sequence": (f"cold step 0 (seed 0) untimed, {args.warmup} warm-up steps on it, then timed "
                                      f"steps 1..{K} on fresh seeds" + (f" (cycling {kf} batches)" if K > kf else "")),
-                   "cuda_graph": bool(args.graph),
+                   "cuda_graph": bool(args.graph), "lookup_ranks": bool(args.ranks),
                    "l2": ("inputs larger than L2 (ids+grads+out ~0.5 GB per step), no flush" if args.config == 3
                           else "fresh batches every step; see the workload's sizes"),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", "host_binding": numa,
@@ -920,6 +930,9 @@ def main():
     ap.add_argument("--e2e", type=int, default=1, help="also time the step through host buffers (its own table)")
     ap.add_argument("--pooled", type=int, default=1, help="also time the pooled jagged-bag step (jagged workload)")
     ap.add_argument("--grow", type=int, default=1, help="also time one capacity expansion at the end")
+    ap.add_argument("--ranks", type=int, default=1,
+                    help="1: the lookup also returns per-position ranks (the backward groups positions with them); "
+                         "0: the backward groups positions itself")
     ap.add_argument("--graph", type=int, default=1, help="replay each step as a captured CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=150.0,

@@ -17,15 +17,19 @@
  *    unless a parameter says "host".  Device buffers passed here must be
  *    16-byte aligned; arenas and workspaces 256-byte aligned.
  *  - Calls are asynchronous and stream-ordered on `stream`, except
- *    mt_stats, mt_export and mt_get_error, which synchronise it.  One table
- *    must be used from one stream at a time.
+ *    mt_stats, mt_export, mt_get_error, mt_get_adam_state,
+ *    mt_set_adam_state, mt_table_grow, mt_compact and mt_shard_lookup, which
+ *    synchronise it (they read or publish host-side values).  One table must
+ *    be used from one stream at a time.
  *  - A negative return value is an error detected on the host; nothing has
  *    been enqueued.  Errors found on the device (an ID out of range, the
  *    probe limit or the row pool exhausted) latch the first code into a
  *    device error word that mt_stats / mt_get_error report; the affected
  *    positions get row -1 and zero output, and the call otherwise completes.
  *  - No kernel of this library waits on another block or another launch:
- *    every probe loop is bounded by the table's probe limit.
+ *    every probe loop is bounded by the table's probe limit, and where the
+ *    last block of a launch finishes a scan it only reads what the earlier
+ *    blocks published before they counted themselves done.
  */
 #ifndef MT_H
 #define MT_H

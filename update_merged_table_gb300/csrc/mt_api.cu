@@ -406,30 +406,7 @@ int mt_lookup(mt_table* t, const int64_t* ids, int64_t n, const int64_t* feat_of
   p.unique_rows = res->unique_rows;
   p.num_unique = reinterpret_cast<long long*>(res->num_unique);
   p.ranks = res->ranks;
-  if (n > 0) {
-    p.sc = reinterpret_cast<mt::ScSlot*>(w + L.sc);
-    p.ss = L.ss;
-    p.ulist_n = reinterpret_cast<uint32_t*>(w + L.ulist_n);
-    p.fresh_n = p.ulist_n + 1;
-    p.rec_n = p.ulist_n + 2;
-    p.rec = reinterpret_cast<ulonglong2*>(w + L.rec);
-    p.rec_slot = reinterpret_cast<int32_t*>(w + L.rec_slot);
-    p.rec_rb = reinterpret_cast<int32_t*>(w + L.rec_rb);
-    p.tile_rec = reinterpret_cast<int32_t*>(w + L.tile_rec);
-    p.lrank = reinterpret_cast<uint16_t*>(w + L.lrank);
-    p.fresh_row = reinterpret_cast<int32_t*>(w + L.fresh_row);
-    p.fresh_key = reinterpret_cast<unsigned long long*>(w + L.fresh_key);
-    p.ulist = reinterpret_cast<int32_t*>(w + L.ulist);
-    p.sc_row = reinterpret_cast<int32_t*>(w + L.sc_row);
-    p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
-    p.tile_O = reinterpret_cast<int32_t*>(w + L.tile_O);
-    p.tile_pre = reinterpret_cast<int32_t*>(w + L.tile_pre);
-    p.done = reinterpret_cast<uint32_t*>(w + L.done);
-    p.first_slot = reinterpret_cast<int32_t*>(w + L.first_slot);
-    p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
-    p.ntiles = L.ntiles;
-    p.clear_bytes = L.clear_bytes;
-  }
+  if (n > 0) mt::bind_lookup_ws(p, w, L);
   return cuda_status(mt::launch_lookup(p, as_stream(stream)));
 }
 

@@ -11,8 +11,8 @@ namespace mt {
 constexpr int kTile = 2048;              // positions per lookup tile (one CTA)
 constexpr int kThreads = 256;            // threads per lookup CTA (number, expand)
 constexpr int kPPT = kTile / kThreads;   // positions per thread
-constexpr int kThreadsA = 512;           // threads per claim CTA (k_claim)
-constexpr int kPPTA = kTile / kThreadsA; // positions per claim thread
+constexpr int kThreadsA = 512;           // threads per stage-1 CTA (k_local)
+constexpr int kPPTA = kTile / kThreadsA; // positions per stage-1 thread
 constexpr int kHS = 2 * kTile;           // shared-memory hash slots (backward fill)
 constexpr int kHSA = 3 * kTile / 2;      // shared-memory hash slots of stage 1 (load <= 2/3)
 constexpr int kThreadsR = 256;           // threads per resolve CTA (k_resolve)
@@ -22,8 +22,7 @@ constexpr uint16_t kNoIdx = 0xFFFF;
 // One slot of the stage-2 scratch hash.  The lookup clears the slots to all
 // ones, so a fresh slot holds key EMPTY, first = "none" and cnt = 2^32 - 1,
 // i.e. cnt stores (positions - 1): an atomicAdd of c returns (positions
-// added before) - 1.  After numbering, `first` is overwritten with the key's
-// unique index.
+// added before) - 1.  After numbering, `first` holds the key's unique index.
 struct __align__(16) ScSlot {
   unsigned long long key;
   uint32_t first;  // smallest position holding the key (atomicMin), then its unique index
@@ -64,24 +63,27 @@ struct LookupParams {
   int32_t* ulist;         // [n] scratch slot of each distinct key, in claim order
   int32_t* sc_row;        // [ss] table row of the key in a slot (-1: none)
   int32_t* tile_L;        // [ntiles] tile-local uniques per tile
-  int32_t* tile_O;        // [ntiles] keys whose first position lies in the tile, minus one (cleared to -1)
-  int32_t* tile_pre;      // [ntiles + 1] exclusive prefix of tile_O (written by the last k_resolve block)
-  uint32_t* done;         // k_resolve blocks finished (zeroed by k_claim)
-  int32_t* first_slot;    // [ntiles * kTile] scratch slot of the key first seen at each position, else -1
+  unsigned long long* owner_nb;  // [ntiles * kTile / 64] bit i clear: position i is its key's first (cleared
+                                 // to all ones)
+  uint16_t* wpre;         // [ntiles * kTile / 64] first positions in the tile before each 64-position word
+  int32_t* tile_pre;      // [ntiles + 1] first positions before each tile (its count, then the exclusive prefix)
+  uint32_t* done;         // k_prefix blocks finished (zeroed by k_local)
   uint16_t* lidx;         // [ntiles * kTile] tile-local unique of each position
   int ntiles;
   int resolve_grid;
-  size_t clear_bytes;     // bytes from sc on cleared to all ones per call (slots, counter, tile counts)
+  size_t clear_bytes;     // bytes from sc on cleared to all ones per call (slots, counters, first-position bits)
 };
 
 struct LookupWsLayout {
-  size_t sc, ulist_n, ulist, rec, rec_slot, rec_rb, fresh_row, fresh_key, sc_row, tile_L, tile_O, tile_pre, done,
-      first_slot, tile_rec, lrank, lidx, total;
+  size_t sc, ulist_n, ulist, rec, rec_slot, rec_rb, fresh_row, fresh_key, sc_row, tile_L, owner_nb, tile_pre, done,
+      wpre, tile_rec, lrank, lidx, total;
   size_t clear_bytes;  // bytes from the start of the workspace cleared to all ones per call
   unsigned long long ss;
   int ntiles;
 };
 LookupWsLayout lookup_ws_layout(long long n);
+// Points the workspace fields of p into w laid out as L (n > 0).
+void bind_lookup_ws(LookupParams& p, char* w, const LookupWsLayout& L);
 cudaError_t launch_lookup(const LookupParams& p, cudaStream_t s);
 
 // ---- backward ---------------------------------------------------------------

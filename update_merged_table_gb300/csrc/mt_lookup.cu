@@ -22,18 +22,20 @@
 //             so far (the count is the rank base of the tile's positions);
 //             the first position is lowered only when this record can lower
 //             it.  The thread whose CAS put a key into the scratch hash lists
-//             it as a distinct key; the tile holding a key's first position so
-//             far counts the key, taking the count over from the tile whose
-//             first position it lowers.
+//             it as a distinct key.
 //  k_resolve  one thread per distinct key: find the key in the table
 //             (odd-step probing) or insert it (first tombstone or EMPTY slot
 //             of its chain, rows popped once per block; fresh rows listed for
-//             k_expand); note the key at its first position.  The last block
-//             to finish turns the per-tile counts of first positions into tile
-//             offsets.
-//  k_number   per tile: the keys first seen in the tile take unique indices
-//             tile offset + their order inside the tile, i.e. first-occurrence
-//             order, and write the unique keys, rows and counts.
+//             k_expand); mark the key's first position in a bitmap of the
+//             batch's positions.
+//  k_prefix   per tile (a warp, a lane per 64-position word): first positions
+//             before each word of the tile; the last block to finish turns the
+//             tile counts into tile offsets.
+//  k_number   one thread per distinct key: its unique index is the number of
+//             first positions before its own (tile offset + word offset + a
+//             popcount), which is first-occurrence order; it writes the
+//             unique key, row and count and leaves the index in the scratch
+//             slot.
 //  k_expand   per tile: inverse index and rank of every position; then a
 //             share of the fresh rows is initialised (Philox-keyed values,
 //             m = v = 0) by teams of lanes, filling the issue slots of this
@@ -87,18 +89,15 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return r;
 }
 
-constexpr size_t kSmemA = kHSA * 8 + kHSA * 4 + kHSA * 4 + kTile * 4 + kTile * 2 + kTile * 2 +
-                          (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
+constexpr size_t kSmemA = kHSA * 8 + kHSA * 4 + kHSA * 4 + kTile * 2 + (MT_MAX_FEATURES + 1) * 8 + MT_MAX_FEATURES;
 
-__global__ void __launch_bounds__(kThreadsA, 3) k_local(const LookupParams p) {
+__global__ void __launch_bounds__(kThreadsA, 4) k_local(const LookupParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   unsigned long long* s_key = reinterpret_cast<unsigned long long*>(smem);  // [kHSA] stage-1 hash keys
   uint32_t* s_min = reinterpret_cast<uint32_t*>(s_key + kHSA);             // [kHSA] first local position, then local index
-  uint32_t* s_cnt = s_min + kHSA;                                          // [kHSA] positions per key, then rank base
-  uint32_t* s_item = s_cnt + kHSA;                                         // [kTile] (hash slot << 16) | first position of local unique l
-  uint16_t* s_pslot = reinterpret_cast<uint16_t*>(s_item + kTile);         // [kTile] hash slot of each position
-  uint16_t* s_lrank = s_pslot + kTile;                                     // [kTile] rank of each position inside the tile
-  long long* s_off = reinterpret_cast<long long*>(s_lrank + kTile);        // [F + 1]
+  uint32_t* s_cnt = s_min + kHSA;                                          // [kHSA] positions per key
+  uint16_t* s_pslot = reinterpret_cast<uint16_t*>(s_cnt + kHSA);           // [kTile] hash slot of each position
+  long long* s_off = reinterpret_cast<long long*>(s_pslot + kTile);        // [F + 1]
   unsigned char* s_tid = reinterpret_cast<unsigned char*>(s_off + MT_MAX_FEATURES + 1);  // [F]
   __shared__ int s_warp[kThreadsA / 32];
   __shared__ int s_frange[2];  // features of the tile's first and last position
@@ -161,6 +160,7 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_local(const LookupParams p) {
       }
       bad |= !valid;
     }
+    uint16_t rank = 0;
     if (valid) {
       uint32_t h = stage1_hash(key);
       for (int probe = 0; probe < kHSA; ++probe) {
@@ -169,11 +169,12 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_local(const LookupParams p) {
         h = h + 1 == (uint32_t)kHSA ? 0u : h + 1;
       }
       atomicMin(&s_min[h], (uint32_t)lp);
-      s_lrank[lp] = (uint16_t)atomicAdd(&s_cnt[h], 1u);
+      rank = (uint16_t)atomicAdd(&s_cnt[h], 1u);
       s_pslot[lp] = (uint16_t)h;
     } else if (in) {
       s_pslot[lp] = kNoIdx;
     }
+    if (in) p.lrank[base + lp] = rank;  // the position's rank among its key's positions in the tile
   }
   if (bad) latch_error(p.T.hdr, MT_EKEY);
   __syncthreads();
@@ -194,13 +195,23 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_local(const LookupParams p) {
   }
   int L;
   int l = block_exclusive_scan<kThreadsA>(c, s_warp, &L);  // every s_min read above precedes its barriers
+  // the tile's records, stored together (one global atomic per tile)
+  if (tid == 0) {
+    s_rbase = L ? (int)(atomicAdd(p.rec_n, (uint32_t)L) + 1u) : 0;  // the counter starts at 2^32 - 1
+    p.tile_L[tile] = L;
+    p.tile_rec[tile] = s_rbase;
+  }
+  __syncthreads();
+  const int rbase = s_rbase;
 #pragma unroll
   for (int k = 0; k < kPPTA; ++k) {
     if (flags & (1u << k)) {
       const int lp = tid * kPPTA + k;
       const uint16_t sl = s_pslot[lp];
       s_min[sl] = (uint32_t)l;
-      s_item[l] = ((uint32_t)sl << 16) | (uint32_t)lp;
+      const ulonglong2 r = make_ulonglong2(s_key[sl], (unsigned long long)(uint32_t)(base + lp) |
+                                                         ((unsigned long long)s_cnt[sl] << 32));
+      __stcg(reinterpret_cast<ulonglong2*>(p.rec) + rbase + l, r);
       ++l;
     }
   }
@@ -209,22 +220,6 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_local(const LookupParams p) {
   for (int lp = tid; lp < cnt; lp += kThreadsA) {
     const uint16_t sl = s_pslot[lp];
     p.lidx[base + lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
-    p.lrank[base + lp] = sl == kNoIdx ? (uint16_t)0 : s_lrank[lp];
-    p.first_slot[base + lp] = -1;  // k_resolve notes each key at its first position
-  }
-  // the tile's records, stored together (one global atomic per tile)
-  if (tid == 0) {
-    s_rbase = L ? (int)(atomicAdd(p.rec_n, (uint32_t)L) + 1u) : 0;  // the counter starts at 2^32 - 1
-    p.tile_L[tile] = L;
-    p.tile_rec[tile] = s_rbase;
-  }
-  __syncthreads();
-  for (int li = tid; li < L; li += kThreadsA) {
-    const uint32_t it = s_item[li];
-    const uint32_t sl = it >> 16;
-    const ulonglong2 r = make_ulonglong2(s_key[sl], (unsigned long long)(uint32_t)(base + (it & 0xFFFFu)) |
-                                                       ((unsigned long long)s_cnt[sl] << 32));
-    __stcg(reinterpret_cast<ulonglong2*>(p.rec) + s_rbase + li, r);
   }
 }
 
@@ -235,7 +230,7 @@ __global__ void __launch_bounds__(kThreadsA, 3) k_local(const LookupParams p) {
 __global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
   __shared__ int s_nwin, s_wbase;
   __shared__ int32_t s_win[kThreadsC];
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const uint32_t R = *p.rec_n + 1u;  // the counter starts at 2^32 - 1
   for (uint32_t b0 = blockIdx.x * kThreadsC; b0 < R; b0 += gridDim.x * kThreadsC) {  // block-uniform trip count
     const uint32_t r = b0 + tid;
@@ -244,41 +239,41 @@ __global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
     __syncthreads();
     bool won = false;
     unsigned long long h = 0;
-    uint32_t gpos = 0, prev = 0xFFFFFFFFu;
     if (act) {
       const ulonglong2 rec = __ldcg(reinterpret_cast<const ulonglong2*>(p.rec) + r);
       const unsigned long long key = rec.x;
-      gpos = (uint32_t)(rec.y & 0xFFFFFFFFull);
+      const uint32_t gpos = (uint32_t)(rec.y & 0xFFFFFFFFull);
       const uint32_t lcount = (uint32_t)(rec.y >> 32);
       h = stage2_home(key, p.ss);
+      uint32_t seen_first = 0xFFFFFFFFu;  // a first position the slot already held (it only ever decreases)
       for (unsigned long long probe = 0; probe < p.ss; ++probe) {
         // a plain load first: the hottest keys have a record from nearly every tile, and a CAS on their
         // slot would queue behind every other tile's at the L2
-        unsigned long long cur = __ldcg(&p.sc[h].key);
+        const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h]));
+        unsigned long long cur = sv.x;
         if (cur == kEmpty) cur = atomicCAS(&p.sc[h].key, kEmpty, key);
         if (cur == kEmpty || cur == key) {
           won = cur == kEmpty;
+          if (sv.x == key) seen_first = (uint32_t)(sv.y & 0xFFFFFFFFull);
           break;
         }
         h = h + 1 == p.ss ? 0ull : h + 1;
       }
-      // {first, count - 1} of the slot are one 64-bit word: adding the count to its high half returns both
-      const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h].first),
-                                               (unsigned long long)lcount << 32);
-      const uint32_t old_first = (uint32_t)(old & 0xFFFFFFFFull);
-      p.rec_rb[r] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before this record
+      uint32_t old_first = seen_first;
+      if (p.ranks != nullptr) {
+        // {first, count - 1} of the slot are one 64-bit word: adding the count to its high half returns
+        // both, the count being the rank base of this record's positions
+        const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h].first),
+                                                 (unsigned long long)lcount << 32);
+        old_first = (uint32_t)(old & 0xFFFFFFFFull);
+        p.rec_rb[r] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before this record
+      } else {
+        atomicAdd(&p.sc[h].cnt, lcount);  // no ranks asked for: the count alone, with no value returned
+      }
       p.rec_slot[r] = (int32_t)h;
       // lower the key's first position only when this record can (the first position only decreases)
-      prev = gpos < old_first ? atomicMin(&p.sc[h].first, gpos) : old_first;
+      if (gpos < old_first) atomicMin(&p.sc[h].first, gpos);
     }
-    // a record that holds the key's first position so far counts the key for its tile
-    const bool take = act && gpos < prev;
-    const int t = (int)(gpos / kTile);
-    const int t0 = __shfl_sync(kFull, t, 0);
-    const unsigned same = __ballot_sync(kFull, take && t == t0);  // records of one tile are stored together
-    if (same && lane == __ffs(same) - 1) atomicAdd(&p.tile_O[t0], __popc(same));
-    if (take && t != t0) atomicAdd(&p.tile_O[t], 1);
-    if (take && prev != 0xFFFFFFFFu) atomicAdd(&p.tile_O[prev / kTile], -1);
     if (won) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h;
     __syncthreads();
     if (tid == 0) s_wbase = s_nwin ? (int)(atomicAdd(p.ulist_n, (uint32_t)s_nwin) + 1u) : 0;  // from 2^32 - 1
@@ -291,8 +286,6 @@ __global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
 __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
   __shared__ int s_need, s_nnew, s_avail;
   __shared__ long long s_rowbase;
-  __shared__ int s_warp[kThreadsR / 32];
-  __shared__ bool s_last;
 
   const int tid = threadIdx.x;
   const uint32_t U = *p.ulist_n + 1u;  // the counter starts at 2^32 - 1
@@ -358,7 +351,7 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
     }
     if (act) {
       p.sc_row[slot] = row;
-      p.first_slot[gfirst] = slot;
+      atomicAnd(&p.owner_nb[gfirst >> 6], ~(1ull << (gfirst & 63)));  // the key's first position
     }
     // the block's fresh rows join the list k_expand initialises (one global atomic per block)
     const bool fresh = claimed && q < s_avail;
@@ -372,8 +365,29 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
     }
     __syncthreads();
   }
+}
 
-  // the last block to finish: tile offsets of the first-occurrence numbering
+// First positions per 64-position word and per tile, from the bits k_resolve
+// cleared: one warp per tile (a lane per word); the last block to finish turns
+// the tile counts into their exclusive prefix.
+__global__ void __launch_bounds__(kThreads) k_prefix(const LookupParams p) {
+  __shared__ int s_warp[kThreads / 32];
+  __shared__ bool s_last;
+  const int tid = threadIdx.x, lane = tid & 31;
+  static_assert(kTile == 64 * 32, "a warp's lanes cover one tile's words");
+  const int tile = blockIdx.x * (kThreads / 32) + (tid >> 5);
+  if (tile < p.ntiles) {
+    const int w = tile * 32 + lane;
+    const int c = __popcll(~__ldcg(&p.owner_nb[w]));
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    p.wpre[w] = (uint16_t)(x - c);
+    if (lane == 31) p.tile_pre[tile] = x;
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(p.done, 1u) == gridDim.x - 1;
@@ -381,16 +395,16 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
   if (!s_last) return;
   __threadfence();
   long long carry = 0;
-  for (int c0 = 0; c0 < p.ntiles; c0 += kThreadsR * 4) {
+  for (int c0 = 0; c0 < p.ntiles; c0 += kThreads * 4) {
     int v[4], sum = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int t = c0 + tid * 4 + k;
-      v[k] = t < p.ntiles ? __ldcg(&p.tile_O[t]) + 1 : 0;  // the counts start at -1
+      v[k] = t < p.ntiles ? __ldcg(&p.tile_pre[t]) : 0;
       sum += v[k];
     }
     int tot;
-    int run = (int)carry + block_exclusive_scan<kThreadsR>(sum, s_warp, &tot);
+    int run = (int)carry + block_exclusive_scan<kThreads>(sum, s_warp, &tot);  // its barriers order reads first
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int t = c0 + tid * 4 + k;
@@ -401,53 +415,28 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
   }
   if (tid == 0) {
     p.tile_pre[p.ntiles] = (int32_t)carry;
-    *p.num_unique = (long long)U;
+    *p.num_unique = (long long)carry;
   }
 }
 
-// The keys first seen in a tile take the unique indices tile offset + their
-// order inside the tile: first-occurrence order over the whole batch.
-__global__ void __launch_bounds__(kThreads, 6) k_number(const LookupParams p) {
-  __shared__ int s_warp[kThreads / 32];
-  const int tile = blockIdx.x, tid = threadIdx.x;
-  const long long base = (long long)tile * kTile;
-  const int cnt = (int)min((long long)kTile, p.n - base);
-  const int pre = __ldg(&p.tile_pre[tile]);
-
-  int32_t v[kPPT];  // positions tid*kPPT .. tid*kPPT + kPPT - 1, in order
-  if ((tid + 1) * kPPT <= cnt) {
-    const int4* src = reinterpret_cast<const int4*>(p.first_slot + base + tid * kPPT);
-#pragma unroll
-    for (int k = 0; k < kPPT / 4; ++k) {
-      const int4 w = __ldcg(src + k);
-      v[4 * k] = w.x;
-      v[4 * k + 1] = w.y;
-      v[4 * k + 2] = w.z;
-      v[4 * k + 3] = w.w;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < kPPT; ++k) {
-      const int lp = tid * kPPT + k;
-      v[k] = lp < cnt ? __ldcg(&p.first_slot[base + lp]) : -1;
-    }
-  }
-  int c = 0;
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) c += v[k] >= 0;
-  int tot;
-  int r = block_exclusive_scan<kThreads>(c, s_warp, &tot);
-#pragma unroll
-  for (int k = 0; k < kPPT; ++k) {  // about one key in six is first seen here: their loads run one by one
-    if (v[k] >= 0) {
-      const int u = pre + r++;
-      const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[v[k]]));
-      const int32_t row = __ldcg(&p.sc_row[v[k]]);
-      p.unique_keys[u] = sv.x;
-      p.unique_rows[u] = row;
-      p.counts[u] = (int32_t)((uint32_t)(sv.y >> 32) + 1u);
-      p.sc[v[k]].first = (uint32_t)u;  // from here on the slot holds the key's unique index
-    }
+// One thread per distinct key (the claim-order list): the key's unique index
+// is the number of first positions before its own (tile offset + word offset
+// + the bits before it in its word), i.e. first-occurrence order.  It writes
+// the key's unique entry and leaves the index in the scratch slot for
+// k_expand.
+__global__ void __launch_bounds__(kThreadsR) k_number(const LookupParams p) {
+  const uint32_t U = *p.ulist_n + 1u;  // the counter starts at 2^32 - 1
+  for (uint32_t idx = blockIdx.x * kThreadsR + threadIdx.x; idx < U; idx += gridDim.x * kThreadsR) {
+    const int32_t slot = __ldcg(&p.ulist[idx]);
+    const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[slot]));
+    const int32_t row = __ldcg(&p.sc_row[slot]);
+    const uint32_t g = (uint32_t)(sv.y & 0xFFFFFFFFull);
+    const unsigned long long below = ~__ldcg(&p.owner_nb[g >> 6]) & ((1ull << (g & 63)) - 1ull);
+    const int u = __ldcg(&p.tile_pre[g / kTile]) + (int)__ldcg(&p.wpre[g >> 6]) + __popcll(below);
+    p.unique_keys[u] = sv.x;
+    p.unique_rows[u] = row;
+    p.counts[u] = (int32_t)((uint32_t)(sv.y >> 32) + 1u);
+    p.sc[slot].first = (uint32_t)u;  // from here on the slot holds the key's unique index
   }
 }
 
@@ -466,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
   for (int k = 0; k < kPPT; ++k) {
     const int l = k * kThreads + tid;
     sl[k] = l < L ? __ldcg(&p.rec_slot[r0 + l]) : -1;
-    if (l < L) s_rb[l] = __ldcg(&p.rec_rb[r0 + l]);
+    if (l < L && p.ranks != nullptr) s_rb[l] = __ldcg(&p.rec_rb[r0 + l]);
   }
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
@@ -564,13 +553,13 @@ LookupWsLayout lookup_ws_layout(long long n) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  const size_t cap = (size_t)L.ntiles * kTile;
   L.sc = take(L.ss * sizeof(ScSlot));
-  L.ulist_n = off;  // right after the slots (with the fresh-row counter), then the tile counts: one memset
-  off += 16;        // clears them all
-  L.tile_O = off;
-  L.clear_bytes = off + (size_t)L.ntiles * 4;
-  take((size_t)L.ntiles * 4);
+  const size_t cap = (size_t)L.ntiles * kTile;
+  L.ulist_n = off;  // right after the slots (with the fresh-row and record counters), then the first-position
+  off += 16;        // bits: one memset clears them all
+  L.owner_nb = off;
+  L.clear_bytes = off + cap / 8;
+  take(cap / 8);
   L.ulist = take((size_t)(n > 0 ? n : 1) * 4);
   L.rec = take((size_t)(n > 0 ? n : 1) * 16);
   L.rec_slot = take((size_t)(n > 0 ? n : 1) * 4);
@@ -581,12 +570,37 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.tile_L = take((size_t)L.ntiles * 4);
   L.tile_pre = take((size_t)(L.ntiles + 1) * 4);
   L.done = take(16);
-  L.first_slot = take(cap * 4);
+  L.wpre = take(cap / 64 * 2);
   L.tile_rec = take((size_t)L.ntiles * 4);
   L.lrank = take(cap * 2);
   L.lidx = take(cap * 2);
   L.total = off;
   return L;
+}
+
+void bind_lookup_ws(LookupParams& p, char* w, const LookupWsLayout& L) {
+  p.sc = reinterpret_cast<ScSlot*>(w + L.sc);
+  p.ss = L.ss;
+  p.ulist_n = reinterpret_cast<uint32_t*>(w + L.ulist_n);
+  p.fresh_n = p.ulist_n + 1;
+  p.rec_n = p.ulist_n + 2;
+  p.rec = reinterpret_cast<ulonglong2*>(w + L.rec);
+  p.rec_slot = reinterpret_cast<int32_t*>(w + L.rec_slot);
+  p.rec_rb = reinterpret_cast<int32_t*>(w + L.rec_rb);
+  p.tile_rec = reinterpret_cast<int32_t*>(w + L.tile_rec);
+  p.lrank = reinterpret_cast<uint16_t*>(w + L.lrank);
+  p.fresh_row = reinterpret_cast<int32_t*>(w + L.fresh_row);
+  p.fresh_key = reinterpret_cast<unsigned long long*>(w + L.fresh_key);
+  p.ulist = reinterpret_cast<int32_t*>(w + L.ulist);
+  p.sc_row = reinterpret_cast<int32_t*>(w + L.sc_row);
+  p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
+  p.owner_nb = reinterpret_cast<unsigned long long*>(w + L.owner_nb);
+  p.wpre = reinterpret_cast<uint16_t*>(w + L.wpre);
+  p.tile_pre = reinterpret_cast<int32_t*>(w + L.tile_pre);
+  p.done = reinterpret_cast<uint32_t*>(w + L.done);
+  p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
+  p.ntiles = L.ntiles;
+  p.clear_bytes = L.clear_bytes;
 }
 
 cudaError_t launch_lookup(const LookupParams& p_in, cudaStream_t s) {
@@ -617,8 +631,8 @@ cudaError_t launch_lookup(const LookupParams& p_in, cudaStream_t s) {
   const long long cwant = (p.n + kThreadsC - 1) / kThreadsC;
   const int cslots = claim_slots[dev].load(std::memory_order_relaxed);
   const int claim_grid = (int)(cwant < cslots ? cwant : cslots);
-  // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1), the list counters and the tile counts
-  // (all minus one): all ones
+  // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1), the list counters (minus one) and the
+  // first-position bits (none set): all ones
   cudaError_t e = cudaMemsetAsync(p.sc, 0xFF, p.clear_bytes, s);
   if (e != cudaSuccess) return e;
   {
@@ -634,8 +648,12 @@ cudaError_t launch_lookup(const LookupParams& p_in, cudaStream_t s) {
     k_resolve<<<p.resolve_grid, kThreadsR, 0, s>>>(p);
   }
   {
+    MT_LAUNCH("k_prefix", s);
+    k_prefix<<<(p.ntiles + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, s>>>(p);
+  }
+  {
     MT_LAUNCH("k_number", s);
-    k_number<<<p.ntiles, kThreads, 0, s>>>(p);
+    k_number<<<p.resolve_grid, kThreadsR, 0, s>>>(p);
   }
   {
     MT_LAUNCH("k_expand", s);

@@ -11,9 +11,11 @@
 //
 // Kernels:
 //  k_pool         positions in chunks of kPoolChunk, a team of lanes per
-//                 chunk (VEC columns per lane), rows summed as exact fp32
-//                 pairs (TwoSum); a bag that lies inside one chunk is written
-//                 at once, the pieces of a longer bag meet in an fp64
+//                 chunk (one 16-byte vector of a row per lane, eight rows in
+//                 flight), rows summed as exact fp32 pairs (TwoSum); the
+//                 chunk's first bag comes from a team-wide multiway search of
+//                 the offsets; a bag that lies inside one chunk is written at
+//                 once, the pieces of a longer bag meet in an fp64
 //                 accumulator.
 //  k_pool_finish  bags split over chunks (and empty bags): rounded from the
 //                 fp64 accumulator.
@@ -36,17 +38,6 @@ __device__ __forceinline__ void two_sum1(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-// The bag holding position i: the last b with bo[b] <= i (-1 when i lies
-// before every bag; b may be >= B when it lies after all of them).
-__device__ __forceinline__ long long bag_of(const long long* bo, long long B, long long i) {
-  long long lo = -1, hi = B + 1;  // bo[lo] <= i < bo[hi] with bo[-1] = -inf, bo[B+1] = +inf
-  while (hi - lo > 1) {
-    const long long mid = (lo + hi) >> 1;
-    if (__ldg(&bo[mid]) <= i) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 // Round a bag's sum (or mean) from double to fp32 into out[b, col .. col + VEC).
 template <int VEC>
 __device__ __forceinline__ void store_pooled(const PoolParams& p, long long b, int col, const double* s, long long len) {
@@ -58,15 +49,15 @@ __device__ __forceinline__ void store_pooled(const PoolParams& p, long long b, i
   for (int q = 0; q < VEC / 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
 }
 
-// VEC columns of a stored row as fp32 (bf16 widens exactly).
+// A stored row's 16 bytes at a lane's columns as VEC fp32 values (bf16 widens exactly).
 template <int RD, int VEC>
-__device__ __forceinline__ void load_row_cols(const TableDev& T, int32_t row, int col, float v[VEC]) {
-  const char* rec = row_ptr(T, row);
+__device__ __forceinline__ void widen(const uint4 t, float v[VEC]) {
   if (RD == MT_F32) {
-    const float4 t = __ldg(reinterpret_cast<const float4*>(rec) + col / 4);
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    v[0] = __uint_as_float(t.x);
+    v[1] = __uint_as_float(t.y);
+    v[2] = __uint_as_float(t.z);
+    v[3] = __uint_as_float(t.w);
   } else {
-    const uint4 t = __ldg(reinterpret_cast<const uint4*>(rec) + col / 8);
     const uint32_t w[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -76,22 +67,48 @@ __device__ __forceinline__ void load_row_cols(const TableDev& T, int32_t row, in
   }
 }
 
+// The bag holding position x, searched by a whole team at once: the last b
+// with bo[b] <= x (-1 when x lies before every bag; b may be >= B when it lies
+// after all of them).  Each round the team's T lanes probe T points that cut
+// the open range (lo, hi) into T + 1 parts, so about log_(T+1)(B) rounds.  The
+// range shrinks every round and every probe lies in [0, B], also for offsets
+// that decrease.
+__device__ __forceinline__ long long bag_search(const long long* bo, long long B, long long x, int lt, int team,
+                                                unsigned team_mask, int team_base) {
+  const unsigned full = team == 32 ? kFull : (1u << team) - 1u;
+  long long lo = -1, hi = B + 1;  // bo[lo] <= x < bo[hi] with bo[-1] = -inf, bo[B+1] = +inf
+  while (hi - lo > 1) {
+    const long long span = hi - lo;
+    const long long m = lo + (span * (lt + 1)) / (team + 1);  // lo <= m < hi, non-decreasing in lt
+    const bool le = m == lo || __ldg(&bo[m]) <= x;
+    const unsigned bits = (__ballot_sync(team_mask, le) >> team_base) & full;
+    const int k = bits == full ? team : __ffs(~bits) - 1;  // the first probe above x
+    const long long nlo = lo + (span * k) / (team + 1);    // probe k - 1 (lo when k = 0)
+    hi = k == team ? hi : lo + (span * (k + 1)) / (team + 1);
+    lo = nlo;
+  }
+  return lo;
+}
+
 template <int RD>
-__global__ void __launch_bounds__(256) k_pool(const PoolParams p) {
-  constexpr int VEC = RD == MT_F32 ? 4 : 8;
-  constexpr int UNR = 32 / VEC;  // rows in flight per lane
+__global__ void __launch_bounds__(256, 2) k_pool(const PoolParams p) {
+  constexpr int VEC = RD == MT_F32 ? 4 : 8;  // columns per lane: one 16-byte load of a row
+  constexpr int UNR = 8;                     // rows in flight per lane
   __shared__ int32_t s_row[(256 >> kPoolMinTeamShift) * kPoolChunk];  // per team: the rows of its chunk
   const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
   const int lane = threadIdx.x & 31;
   const int lt = lane & (team - 1);
-  const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << (lane & ~(team - 1)));
+  const int team_base = lane & ~(team - 1);
+  const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << team_base);
   int32_t* my_row = s_row + (threadIdx.x >> team_shift) * kPoolChunk;
   const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
   const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
   const long long nchunks = (p.n + kPoolChunk - 1) / kPoolChunk;
   const long long U = *p.num_unique;
   const int d = (int)p.T.dim;
+  const long long B = p.num_bags;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
 
   for (long long c = gteam; c < nchunks; c += nteam) {  // uniform per team
     const long long p0 = c * kPoolChunk, p1 = min(p0 + kPoolChunk, p.n);
@@ -100,20 +117,21 @@ __global__ void __launch_bounds__(256) k_pool(const PoolParams p) {
       const int32_t u = __ldg(&p.inverse[p0 + q]);
       my_row[q] = (u >= 0 && u < U) ? __ldg(&p.unique_rows[u]) : -1;
     }
+    const long long b_first = bag_search(p.bag_offsets, B, p0, lt, team, team_mask, team_base);
+    const long long bo0 = __ldg(&p.bag_offsets[0]);
     __syncwarp(team_mask);
-    const long long b_first = bag_of(p.bag_offsets, p.num_bags, p0);
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + lt * VEC;
       const bool active = col < d;
       long long b = b_first < 0 ? 0 : b_first;
-      long long b_end = b < p.num_bags ? __ldg(&p.bag_offsets[b + 1]) : p1;
+      long long b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p1;
       float hi[VEC], lo[VEC];
 #pragma unroll
       for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.0f;
       // a bag's sum leaves the running pair: written out when the whole bag lies in this chunk, else added
       // to the bag's fp64 accumulator
       auto flush = [&](long long bb, long long bend) {
-        if (bb < 0 || bb >= p.num_bags || !active) return;
+        if (bb < 0 || bb >= B || !active) return;
         const long long bstart = __ldg(&p.bag_offsets[bb]);
         double s[VEC];
 #pragma unroll
@@ -129,37 +147,37 @@ __global__ void __launch_bounds__(256) k_pool(const PoolParams p) {
         for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.0f;
       };
       for (long long i0 = p0; i0 < p1; i0 += UNR) {
-        float v[UNR][VEC];
+        uint4 raw[UNR];  // every load of the round issued before the first add
 #pragma unroll
         for (int r = 0; r < UNR; ++r) {
           const long long i = i0 + r;
           const int32_t row = i < p1 ? my_row[i - p0] : -1;
-          if (active && row >= 0) load_row_cols<RD, VEC>(p.T, row, col, v[r]);
-          else {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) v[r][j] = 0.0f;
-          }
+          raw[r] = active && row >= 0 ? __ldg(reinterpret_cast<const uint4*>(row_ptr(p.T, row) + (size_t)col *
+                                                                              (RD == MT_F32 ? 4 : 2)))
+                                      : zero;
         }
 #pragma unroll
         for (int r = 0; r < UNR; ++r) {
           const long long i = i0 + r;
           if (i >= p1) break;
-          while (b < p.num_bags && i >= b_end) {  // position i starts a later bag
+          while (b < B && i >= b_end) {  // position i starts a later bag
             flush(b, b_end);
             ++b;
-            b_end = b < p.num_bags ? __ldg(&p.bag_offsets[b + 1]) : p1;
+            b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p1;
           }
-          if (b >= p.num_bags || (b_first < 0 && i < __ldg(&p.bag_offsets[0]))) continue;  // in no bag
+          if (b >= B || i < bo0) continue;  // in no bag
+          float v[VEC];
+          widen<RD, VEC>(raw[r], v);
 #pragma unroll
           for (int j = 0; j < VEC; ++j) {
             float s, e;
-            two_sum1(hi[j], v[r][j], s, e);
+            two_sum1(hi[j], v[j], s, e);
             hi[j] = s;
             lo[j] = __fadd_rn(lo[j], e);
           }
         }
       }
-      if (b < p.num_bags) flush(b, b_end);
+      if (b < B) flush(b, b_end);
     }
     __syncwarp(team_mask);  // my_row is refilled by the next chunk
   }

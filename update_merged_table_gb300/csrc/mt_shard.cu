@@ -226,30 +226,7 @@ mt::LookupParams lookup_params(const mt::TableDev& T, const long long* ids, long
   p.n = n;
   const mt::LookupWsLayout L = mt::lookup_ws_layout(n);
   char* w = static_cast<char*>(ws);
-  if (n > 0) {
-    p.sc = reinterpret_cast<mt::ScSlot*>(w + L.sc);
-    p.ss = L.ss;
-    p.ulist_n = reinterpret_cast<uint32_t*>(w + L.ulist_n);
-    p.fresh_n = p.ulist_n + 1;
-    p.rec_n = p.ulist_n + 2;
-    p.rec = reinterpret_cast<ulonglong2*>(w + L.rec);
-    p.rec_slot = reinterpret_cast<int32_t*>(w + L.rec_slot);
-    p.rec_rb = reinterpret_cast<int32_t*>(w + L.rec_rb);
-    p.tile_rec = reinterpret_cast<int32_t*>(w + L.tile_rec);
-    p.lrank = reinterpret_cast<uint16_t*>(w + L.lrank);
-    p.ulist = reinterpret_cast<int32_t*>(w + L.ulist);
-    p.fresh_row = reinterpret_cast<int32_t*>(w + L.fresh_row);
-    p.fresh_key = reinterpret_cast<unsigned long long*>(w + L.fresh_key);
-    p.sc_row = reinterpret_cast<int32_t*>(w + L.sc_row);
-    p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
-    p.tile_O = reinterpret_cast<int32_t*>(w + L.tile_O);
-    p.tile_pre = reinterpret_cast<int32_t*>(w + L.tile_pre);
-    p.done = reinterpret_cast<uint32_t*>(w + L.done);
-    p.first_slot = reinterpret_cast<int32_t*>(w + L.first_slot);
-    p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
-    p.ntiles = L.ntiles;
-    p.clear_bytes = L.clear_bytes;
-  }
+  if (n > 0) mt::bind_lookup_ws(p, w, L);
   return p;
 }
 
