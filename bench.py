@@ -648,6 +648,10 @@ def run_ours(args):
     graphs = None
     launches_per_step = None
     if args.graph:
+        # every workspace sized for the largest batch first: a capture must not replace a buffer that graphs
+        # captured before it still use
+        tab.reserve_workspaces(max(e["batch"].n for e in pool + prof_pool))
+        torch.cuda.synchronize(dev)
         graphs = []
         l0 = mt.kernel_launches()
         for e in pool:
@@ -706,9 +710,9 @@ def run_ours(args):
     tot_ids, tot_secs = aggregate(float(n_ids), secs)
 
     # -------- per-kernel device times: an eager pass over further fresh steps --------
+    pst0 = tab.stats()
     mt.profile_enable(True)
     mt.profile_report(reset=True)
-    pst0 = tab.stats()
     for e in prof_pool:
         fwd_call(e)
         bwd_call(e)

@@ -610,3 +610,33 @@ def test_full_size_online_churn():
             np.testing.assert_allclose(m.cpu().numpy()[pr], m2[pr], rtol=RTOL, atol=ATOL)
             np.testing.assert_allclose(v.cpu().numpy()[pr], v2[pr], rtol=RTOL, atol=1e-9)
     assert tab.error() == 0 and ref.error == 0
+
+
+def test_graph_capture_needs_reserved_workspaces():
+    """A lookup captured in a CUDA graph must not grow a workspace (graphs captured earlier keep the old
+    buffer's address); after reserve_workspaces the captured lookup replays to the eager result."""
+    tab = mt.Table(14, 16)
+    small = to_dev(np.arange(100, dtype=np.int64))
+    ids = np.random.default_rng(3).integers(0, 3000, size=6000).astype(np.int64)
+    big = to_dev(ids)
+    tab.lookup(small)  # workspaces sized for 100 IDs
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    res = tab.new_result(ids.size)
+    with pytest.raises(RuntimeError, match="reserve_workspaces"):
+        with torch.cuda.graph(torch.cuda.CUDAGraph(), stream=s):
+            tab.lookup(big, result=res)
+    tab.reserve_workspaces(ids.size)
+    eager = tab.lookup(big)  # inserts the keys
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tab.lookup(big, result=res)
+    g.replay()
+    torch.cuda.synchronize()
+    U = eager.U
+    assert res.U == U
+    assert torch.equal(res.unique_keys[:U], eager.unique_keys[:U])
+    assert torch.equal(res.inverse, eager.inverse)
+    assert torch.equal(res.counts[:U], eager.counts[:U])
+    assert torch.equal(res.rows, eager.rows)
+    assert tab.error() == 0

@@ -283,6 +283,11 @@ class Table:
         torch = _torch()
         buf = self._ws.get(kind)
         if buf is None or buf.numel() < nbytes:
+            if torch.cuda.is_current_stream_capturing():
+                # graphs captured earlier hold the old buffer's address, and a later capture may return the
+                # freed buffer to the driver: they would replay on unmapped memory
+                raise RuntimeError(f"the {kind} workspace would have to grow during CUDA graph capture; call "
+                                   "reserve_workspaces() with the largest batch before capturing")
             buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
             self._ws[kind] = buf
         return buf

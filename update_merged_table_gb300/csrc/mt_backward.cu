@@ -177,7 +177,6 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   int hch = ex[1] + s_base[1];
   int hv = ex[2] + s_base[2];
   const int HWC = s_tot[1];
-  const int d = (int)p.T.dim;
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
     const long long u = u0 + k;
@@ -287,45 +286,6 @@ __global__ void __launch_bounds__(kThreads) k_bw_fill(const BackwardParams p) {
 }
 
 // ---- reduction + Adam -------------------------------------------------------
-
-// ---- packed fp32 pairs ---------------------------------------------------------
-// Two adjacent columns travel in one 64-bit register (low half: the even
-// column) and are combined by the paired fp32 instructions (add/sub
-// .rn.f32x2): each half is rounded to nearest on its own, exactly like the
-// scalar __fadd_rn/__fsub_rn, at one instruction per pair.  Only additions
-// and subtractions are paired: with no product in the chain nothing can be
-// fused, so TwoSum stays exact.
-typedef unsigned long long f32x2;
-
-__device__ __forceinline__ f32x2 pk(float lo, float hi) {
-  f32x2 d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-  return d;
-}
-__device__ __forceinline__ float2 upk(f32x2 a) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a));
-  return r;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-// Two bf16 in one word (low half: the even column) widened to fp32 (exact).
-__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
-
-// s + e = a + b exactly, per half (Knuth's TwoSum).
-__device__ __forceinline__ void two_sum(f32x2 a, f32x2 b, f32x2& s, f32x2& e) {
-  s = add2(a, b);
-  const f32x2 bb = sub2(s, a);
-  e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
-}
 
 // Add x and y (two rows' pairs) to the running pair (hi, lo), which carries
 // the sum with about twice fp32's precision: the two rows' TwoSum does not
@@ -624,9 +584,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
   int* my_pos = s_pos + (threadIdx.x >> team_shift) * kTeamShare;
   const int d = (int)p.T.dim;
   const int col0 = lt * VEC;
-  const long long U = *p.num_unique;
   const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
-  const long long light_end = (long long)HWC + (U - p.boff[(size_t)p.nblk * 3 + 2]);
 
   // ---- heavy warp-chunks, handed to warps one at a time (they differ in size) ----
   for (;;) {
@@ -718,10 +676,8 @@ __global__ void __launch_bounds__(256, 3) k_bw_light_reduce(const BackwardParams
 
   const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
-  const int tpw = 32 >> team_shift;  // teams per warp
   const int lane = threadIdx.x & 31;
   const int lt = lane & (team - 1);
-  const int tiw = lane >> team_shift;  // team index in the warp
   const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << (lane & ~(team - 1)));
   int* my_pos = s_pos + (threadIdx.x >> team_shift) * kChunk;
   const int d = (int)p.T.dim;

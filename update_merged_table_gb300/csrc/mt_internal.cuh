@@ -246,4 +246,44 @@ __device__ __forceinline__ long long find_slot(const TableDev& T, unsigned long 
 struct LookupWs;
 struct BackwardWs;
 
+// ---- packed fp32 pairs -------------------------------------------------------
+// Two adjacent columns travel in one 64-bit register (low half: the even
+// column) and are combined by the paired fp32 instructions (add/sub
+// .rn.f32x2): each half is rounded to nearest on its own, exactly like the
+// scalar __fadd_rn/__fsub_rn, at one instruction per pair.  Only additions
+// and subtractions are paired: with no product in the chain nothing can be
+// fused, so TwoSum stays exact.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pk(float lo, float hi) {
+  f32x2 d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float2 upk(f32x2 a) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(a));
+  return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Two bf16 in one word (low half: the even column) widened to fp32 (exact).
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
+
+// s + e = a + b exactly, per half (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(f32x2 a, f32x2 b, f32x2& s, f32x2& e) {
+  s = add2(a, b);
+  const f32x2 bb = sub2(s, a);
+  e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
+}
+
+
 }  // namespace mt

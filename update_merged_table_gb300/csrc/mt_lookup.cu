@@ -224,64 +224,108 @@ __global__ void __launch_bounds__(kThreadsA, 4) k_local(const LookupParams p) {
 }
 
 // Stage 2: one thread per record {key, first position in its tile, count in
-// its tile}, over the whole GPU.  Each record's chain of global round trips is
-// short (a load of the key's home slot, a CAS when it is EMPTY, one 64-bit
-// atomic), and nothing waits on a block barrier in between.
+// its tile}, two records per thread in flight, over the whole GPU.  Each
+// record's chain of global round trips is short (a load of the key's home
+// slot, a CAS when it is EMPTY, one 64-bit atomic), and nothing waits on a
+// block barrier in between: the block's distinct keys collect in shared
+// memory and are listed once at the end (or once per round when the block's
+// share of records could overflow that buffer).
+constexpr int kClaimILP = 2;     // records per thread per round
+constexpr int kWinCap = 4096;    // distinct keys a block holds before listing them
+
+// Claims `key` in the scratch hash from slot h whose contents sv were loaded
+// already: the first slot holding the key or EMPTY (then CASed).  Returns
+// whether this call put the key there; *first_seen is the first position
+// the slot held when it was seen with the key (EMPTY: none).
+__device__ __forceinline__ bool claim_from(const LookupParams& p, unsigned long long key, unsigned long long& h,
+                                           ulonglong2 sv, uint32_t* first_seen) {
+  *first_seen = 0xFFFFFFFFu;
+  for (unsigned long long probe = 0; probe < p.ss; ++probe) {
+    unsigned long long cur = sv.x;
+    // a plain load first: the hottest keys have a record from nearly every tile, and a CAS on their
+    // slot would queue behind every other tile's at the L2
+    if (cur == kEmpty) cur = atomicCAS(&p.sc[h].key, kEmpty, key);
+    if (cur == kEmpty) return true;
+    if (cur == key) {
+      if (sv.x == key) *first_seen = (uint32_t)(sv.y & 0xFFFFFFFFull);
+      return false;
+    }
+    h = h + 1 == p.ss ? 0ull : h + 1;
+    sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h]));
+  }
+  return false;  // not reached: the scratch hash has more slots than records
+}
+
+// Lists the block's distinct keys held in s_win (call with the whole block).
+__device__ __forceinline__ void list_winners(const LookupParams& p, int32_t* s_win, int* s_nwin, int* s_wbase) {
+  __syncthreads();
+  const int nwin = *s_nwin;
+  if (threadIdx.x == 0 && nwin > 0) *s_wbase = (int)(atomicAdd(p.ulist_n, (uint32_t)nwin) + 1u);  // from 2^32 - 1
+  __syncthreads();
+  for (int i = threadIdx.x; i < nwin; i += kThreadsC) p.ulist[*s_wbase + i] = s_win[i];
+  __syncthreads();
+  if (threadIdx.x == 0) *s_nwin = 0;
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
   __shared__ int s_nwin, s_wbase;
-  __shared__ int32_t s_win[kThreadsC];
+  __shared__ int32_t s_win[kWinCap];
   const int tid = threadIdx.x;
   const uint32_t R = *p.rec_n + 1u;  // the counter starts at 2^32 - 1
-  for (uint32_t b0 = blockIdx.x * kThreadsC; b0 < R; b0 += gridDim.x * kThreadsC) {  // block-uniform trip count
-    const uint32_t r = b0 + tid;
-    const bool act = r < R;
-    if (tid == 0) s_nwin = 0;
-    __syncthreads();
-    bool won = false;
-    unsigned long long h = 0;
-    if (act) {
-      const ulonglong2 rec = __ldcg(reinterpret_cast<const ulonglong2*>(p.rec) + r);
-      const unsigned long long key = rec.x;
-      const uint32_t gpos = (uint32_t)(rec.y & 0xFFFFFFFFull);
-      const uint32_t lcount = (uint32_t)(rec.y >> 32);
-      h = stage2_home(key, p.ss);
-      uint32_t seen_first = 0xFFFFFFFFu;  // a first position the slot already held (it only ever decreases)
-      for (unsigned long long probe = 0; probe < p.ss; ++probe) {
-        // a plain load first: the hottest keys have a record from nearly every tile, and a CAS on their
-        // slot would queue behind every other tile's at the L2
-        const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h]));
-        unsigned long long cur = sv.x;
-        if (cur == kEmpty) cur = atomicCAS(&p.sc[h].key, kEmpty, key);
-        if (cur == kEmpty || cur == key) {
-          won = cur == kEmpty;
-          if (sv.x == key) seen_first = (uint32_t)(sv.y & 0xFFFFFFFFull);
-          break;
-        }
-        h = h + 1 == p.ss ? 0ull : h + 1;
+  const uint32_t span = kThreadsC * kClaimILP;
+  const uint32_t stride = gridDim.x * span;
+  const uint32_t first = blockIdx.x * span;
+  const uint32_t rounds = first < R ? (R - first + stride - 1) / stride : 0u;
+  const bool list_each_round = (unsigned long long)rounds * span > (unsigned long long)kWinCap;  // block-uniform
+  if (tid == 0) s_nwin = 0;
+  __syncthreads();
+  for (uint32_t b0 = first; b0 < R; b0 += stride) {
+    uint32_t r[kClaimILP], gpos[kClaimILP], lcount[kClaimILP];
+    unsigned long long key[kClaimILP], h[kClaimILP];
+    ulonglong2 sv[kClaimILP];
+#pragma unroll
+    for (int k = 0; k < kClaimILP; ++k) {
+      r[k] = b0 + k * kThreadsC + tid;
+      key[k] = kEmpty;
+      if (r[k] < R) {
+        const ulonglong2 rec = __ldcg(reinterpret_cast<const ulonglong2*>(p.rec) + r[k]);
+        key[k] = rec.x;
+        gpos[k] = (uint32_t)(rec.y & 0xFFFFFFFFull);
+        lcount[k] = (uint32_t)(rec.y >> 32);
       }
-      uint32_t old_first = seen_first;
+    }
+#pragma unroll
+    for (int k = 0; k < kClaimILP; ++k)
+      if (r[k] < R) {
+        h[k] = stage2_home(key[k], p.ss);
+        sv[k] = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h[k]]));
+      }
+#pragma unroll
+    for (int k = 0; k < kClaimILP; ++k) {
+      if (r[k] >= R) continue;
+      uint32_t old_first;
+      const bool won = claim_from(p, key[k], h[k], sv[k], &old_first);
       if (p.ranks != nullptr) {
         // {first, count - 1} of the slot are one 64-bit word: adding the count to its high half returns
         // both, the count being the rank base of this record's positions
-        const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h].first),
-                                                 (unsigned long long)lcount << 32);
+        const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h[k]].first),
+                                                 (unsigned long long)lcount[k] << 32);
         old_first = (uint32_t)(old & 0xFFFFFFFFull);
-        p.rec_rb[r] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before this record
+        p.rec_rb[r[k]] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before
       } else {
-        atomicAdd(&p.sc[h].cnt, lcount);  // no ranks asked for: the count alone, with no value returned
+        atomicAdd(&p.sc[h[k]].cnt, lcount[k]);  // no ranks asked for: the count alone, no value returned
       }
-      p.rec_slot[r] = (int32_t)h;
+      p.rec_slot[r[k]] = (int32_t)h[k];
       // lower the key's first position only when this record can (the first position only decreases)
-      if (gpos < old_first) atomicMin(&p.sc[h].first, gpos);
+      if (gpos[k] < old_first) atomicMin(&p.sc[h[k]].first, gpos[k]);
+      if (won) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h[k];
     }
-    if (won) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h;
-    __syncthreads();
-    if (tid == 0) s_wbase = s_nwin ? (int)(atomicAdd(p.ulist_n, (uint32_t)s_nwin) + 1u) : 0;  // from 2^32 - 1
-    __syncthreads();
-    if (tid < s_nwin) p.ulist[s_wbase + tid] = s_win[tid];
-    __syncthreads();  // s_nwin is reset by the next round
+    if (list_each_round) list_winners(p, s_win, &s_nwin, &s_wbase);
   }
+  if (!list_each_round) list_winners(p, s_win, &s_nwin, &s_wbase);
 }
+
 
 __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
   __shared__ int s_need, s_nnew, s_avail;
@@ -425,18 +469,38 @@ __global__ void __launch_bounds__(kThreads) k_prefix(const LookupParams p) {
 // the key's unique entry and leaves the index in the scratch slot for
 // k_expand.
 __global__ void __launch_bounds__(kThreadsR) k_number(const LookupParams p) {
+  constexpr int ILP = 2;  // keys per thread in flight: every load of both before any store
   const uint32_t U = *p.ulist_n + 1u;  // the counter starts at 2^32 - 1
-  for (uint32_t idx = blockIdx.x * kThreadsR + threadIdx.x; idx < U; idx += gridDim.x * kThreadsR) {
-    const int32_t slot = __ldcg(&p.ulist[idx]);
-    const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[slot]));
-    const int32_t row = __ldcg(&p.sc_row[slot]);
-    const uint32_t g = (uint32_t)(sv.y & 0xFFFFFFFFull);
-    const unsigned long long below = ~__ldcg(&p.owner_nb[g >> 6]) & ((1ull << (g & 63)) - 1ull);
-    const int u = __ldcg(&p.tile_pre[g / kTile]) + (int)__ldcg(&p.wpre[g >> 6]) + __popcll(below);
-    p.unique_keys[u] = sv.x;
-    p.unique_rows[u] = row;
-    p.counts[u] = (int32_t)((uint32_t)(sv.y >> 32) + 1u);
-    p.sc[slot].first = (uint32_t)u;  // from here on the slot holds the key's unique index
+  for (uint32_t i0 = blockIdx.x * kThreadsR * ILP + threadIdx.x; i0 < U; i0 += gridDim.x * kThreadsR * ILP) {
+    int32_t slot[ILP], row[ILP];
+    ulonglong2 sv[ILP];
+#pragma unroll
+    for (int k = 0; k < ILP; ++k) {
+      const uint32_t idx = i0 + k * kThreadsR;
+      slot[k] = idx < U ? __ldcg(&p.ulist[idx]) : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < ILP; ++k)
+      if (slot[k] >= 0) {
+        sv[k] = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[slot[k]]));
+        row[k] = __ldcg(&p.sc_row[slot[k]]);
+      }
+    int u[ILP];
+#pragma unroll
+    for (int k = 0; k < ILP; ++k)
+      if (slot[k] >= 0) {
+        const uint32_t g = (uint32_t)(sv[k].y & 0xFFFFFFFFull);
+        const unsigned long long below = ~__ldcg(&p.owner_nb[g >> 6]) & ((1ull << (g & 63)) - 1ull);
+        u[k] = __ldcg(&p.tile_pre[g / kTile]) + (int)__ldcg(&p.wpre[g >> 6]) + __popcll(below);
+      }
+#pragma unroll
+    for (int k = 0; k < ILP; ++k)
+      if (slot[k] >= 0) {
+        p.unique_keys[u[k]] = sv[k].x;
+        p.unique_rows[u[k]] = row[k];
+        p.counts[u[k]] = (int32_t)((uint32_t)(sv[k].y >> 32) + 1u);
+        p.sc[slot[k]].first = (uint32_t)u[k];  // from here on the slot holds the key's unique index
+      }
   }
 }
 
@@ -628,7 +692,7 @@ cudaError_t launch_lookup(const LookupParams& p_in, cudaStream_t s) {
     const int slots = resolve_slots[dev].load(std::memory_order_relaxed);
     p.resolve_grid = (int)(want < slots ? want : slots);
   }
-  const long long cwant = (p.n + kThreadsC - 1) / kThreadsC;
+  const long long cwant = (p.n + kThreadsC * kClaimILP - 1) / (kThreadsC * kClaimILP);
   const int cslots = claim_slots[dev].load(std::memory_order_relaxed);
   const int claim_grid = (int)(cwant < cslots ? cwant : cslots);
   // scratch slots (key EMPTY, first "none", count - 1 = 2^32 - 1), the list counters (minus one) and the

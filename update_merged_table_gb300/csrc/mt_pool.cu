@@ -11,8 +11,9 @@
 //
 // Kernels:
 //  k_pool         positions in chunks of kPoolChunk, a team of lanes per
-//                 chunk (one 16-byte vector of a row per lane, eight rows in
-//                 flight), rows summed as exact fp32 pairs (TwoSum); the
+//                 chunk (one 16-byte vector of a row per lane, four rows in
+//                 flight), rows summed as exact fp32 pairs (TwoSum on the
+//                 paired fp32 instructions, two columns each); the
 //                 chunk's first bag comes from a team-wide multiway search of
 //                 the offsets; a bag that lies inside one chunk is written at
 //                 once, the pieces of a longer bag meet in an fp64
@@ -31,13 +32,6 @@ namespace {
 constexpr int kPoolChunk = 64;        // positions per chunk (one team)
 constexpr int kPoolMinTeamShift = 2;  // teams of at least 4 lanes
 
-// s + e = a + b exactly (Knuth's TwoSum).
-__device__ __forceinline__ void two_sum1(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-
 // Round a bag's sum (or mean) from double to fp32 into out[b, col .. col + VEC).
 template <int VEC>
 __device__ __forceinline__ void store_pooled(const PoolParams& p, long long b, int col, const double* s, long long len) {
@@ -47,24 +41,6 @@ __device__ __forceinline__ void store_pooled(const PoolParams& p, long long b, i
   float4* dst = reinterpret_cast<float4*>(p.out + (size_t)b * p.T.dim + col);
 #pragma unroll
   for (int q = 0; q < VEC / 4; ++q) dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-}
-
-// A stored row's 16 bytes at a lane's columns as VEC fp32 values (bf16 widens exactly).
-template <int RD, int VEC>
-__device__ __forceinline__ void widen(const uint4 t, float v[VEC]) {
-  if (RD == MT_F32) {
-    v[0] = __uint_as_float(t.x);
-    v[1] = __uint_as_float(t.y);
-    v[2] = __uint_as_float(t.z);
-    v[3] = __uint_as_float(t.w);
-  } else {
-    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[2 * q] = __uint_as_float(w[q] << 16);
-      v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
-    }
-  }
 }
 
 // The bag holding position x, searched by a whole team at once: the last b
@@ -91,9 +67,10 @@ __device__ __forceinline__ long long bag_search(const long long* bo, long long B
 }
 
 template <int RD>
-__global__ void __launch_bounds__(256, 2) k_pool(const PoolParams p) {
+__global__ void __launch_bounds__(256, 3) k_pool(const PoolParams p) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;  // columns per lane: one 16-byte load of a row
-  constexpr int UNR = 8;                     // rows in flight per lane
+  constexpr int NP = VEC / 2;                // column pairs per lane
+  constexpr int UNR = 4;                     // rows in flight per lane
   __shared__ int32_t s_row[(256 >> kPoolMinTeamShift) * kPoolChunk];  // per team: the rows of its chunk
   const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
@@ -109,71 +86,86 @@ __global__ void __launch_bounds__(256, 2) k_pool(const PoolParams p) {
   const int d = (int)p.T.dim;
   const long long B = p.num_bags;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  // an offset relative to the chunk start, clamped to [0, kPoolChunk + 1]
+  auto rel = [](long long x, long long p0) -> int {
+    const long long r = x - p0;
+    return r < 0 ? 0 : (r > kPoolChunk ? kPoolChunk + 1 : (int)r);
+  };
 
   for (long long c = gteam; c < nchunks; c += nteam) {  // uniform per team
-    const long long p0 = c * kPoolChunk, p1 = min(p0 + kPoolChunk, p.n);
+    const long long p0 = c * kPoolChunk;
+    const int cnt = (int)min((long long)kPoolChunk, p.n - p0);
     // the chunk's rows (-1: nothing to add)
-    for (int q = lt; q < p1 - p0; q += team) {
+    for (int q = lt; q < cnt; q += team) {
       const int32_t u = __ldg(&p.inverse[p0 + q]);
       my_row[q] = (u >= 0 && u < U) ? __ldg(&p.unique_rows[u]) : -1;
     }
     const long long b_first = bag_search(p.bag_offsets, B, p0, lt, team, team_mask, team_base);
-    const long long bo0 = __ldg(&p.bag_offsets[0]);
+    // positions before the first bag belong to none
+    const int q_skip = b_first < 0 && B > 0 ? rel(__ldg(&p.bag_offsets[0]), p0) : 0;
     __syncwarp(team_mask);
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + lt * VEC;
       const bool active = col < d;
       long long b = b_first < 0 ? 0 : b_first;
-      long long b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p1;
-      float hi[VEC], lo[VEC];
+      long long b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p0 + cnt;
+      int q_end = rel(b_end, p0);
+      f32x2 hi[NP], lo[NP];
 #pragma unroll
-      for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.0f;
-      // a bag's sum leaves the running pair: written out when the whole bag lies in this chunk, else added
-      // to the bag's fp64 accumulator
+      for (int j = 0; j < NP; ++j) hi[j] = lo[j] = 0ull;
+      // a bag's sum leaves the running pair, one column pair at a time: written out (rounded once) when
+      // the whole bag lies in this chunk, else added to the bag's fp64 accumulator
       auto flush = [&](long long bb, long long bend) {
         if (bb < 0 || bb >= B || !active) return;
         const long long bstart = __ldg(&p.bag_offsets[bb]);
-        double s[VEC];
+        const bool whole = bstart >= p0 && bend <= p0 + cnt && bend > bstart;
+        const double len = (double)(bend - bstart);
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) s[j] = (double)hi[j] + (double)lo[j];
-        if (bstart >= p0 && bend <= p1 && bend > bstart) {
-          store_pooled<VEC>(p, bb, col, s, bend - bstart);
-        } else {
-          double* a = p.acc + (size_t)bb * d + col;
-#pragma unroll
-          for (int j = 0; j < VEC; ++j) atomicAdd(a + j, s[j]);
+        for (int j = 0; j < NP; ++j) {
+          const float2 h = upk(hi[j]), l = upk(lo[j]);
+          const double s0 = (double)h.x + (double)l.x, s1 = (double)h.y + (double)l.y;
+          if (whole) {
+            const bool mean = p.mode == MT_POOL_MEAN;
+            *reinterpret_cast<float2*>(p.out + (size_t)bb * d + col + 2 * j) =
+                make_float2((float)(mean ? s0 / len : s0), (float)(mean ? s1 / len : s1));
+          } else {
+            double* a = p.acc + (size_t)bb * d + col + 2 * j;
+            atomicAdd(a, s0);
+            atomicAdd(a + 1, s1);
+          }
+          hi[j] = lo[j] = 0ull;
         }
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) hi[j] = lo[j] = 0.0f;
       };
-      for (long long i0 = p0; i0 < p1; i0 += UNR) {
+      for (int q0 = 0; q0 < cnt; q0 += UNR) {
         uint4 raw[UNR];  // every load of the round issued before the first add
 #pragma unroll
         for (int r = 0; r < UNR; ++r) {
-          const long long i = i0 + r;
-          const int32_t row = i < p1 ? my_row[i - p0] : -1;
+          const int q = q0 + r;
+          const int32_t row = q < cnt ? my_row[q] : -1;
           raw[r] = active && row >= 0 ? __ldg(reinterpret_cast<const uint4*>(row_ptr(p.T, row) + (size_t)col *
                                                                               (RD == MT_F32 ? 4 : 2)))
                                       : zero;
         }
 #pragma unroll
         for (int r = 0; r < UNR; ++r) {
-          const long long i = i0 + r;
-          if (i >= p1) break;
-          while (b < B && i >= b_end) {  // position i starts a later bag
+          const int q = q0 + r;
+          if (q >= cnt) break;
+          while (q >= q_end && b < B) {  // position q starts a later bag
             flush(b, b_end);
             ++b;
-            b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p1;
+            b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p0 + cnt;
+            q_end = rel(b_end, p0);
           }
-          if (b >= B || i < bo0) continue;  // in no bag
-          float v[VEC];
-          widen<RD, VEC>(raw[r], v);
+          if (b >= B || q < q_skip) continue;  // in no bag
+          const uint32_t w[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) {
-            float s, e;
-            two_sum1(hi[j], v[j], s, e);
+          for (int j = 0; j < NP; ++j) {
+            const f32x2 x = RD == MT_F32 ? pk(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1]))
+                                         : bf16x2_to_f32x2(w[j]);
+            f32x2 s, e;
+            two_sum(hi[j], x, s, e);
             hi[j] = s;
-            lo[j] = __fadd_rn(lo[j], e);
+            lo[j] = add2(lo[j], e);
           }
         }
       }
