@@ -146,3 +146,15 @@ def test_full_size_pooled_jagged():
     for s, mode in ((0, "mean"), (1, "sum")):
         b = W.jagged_batch(s)
         pooled_step(tab, ref, b, jagged_bags(b), mode, 90 + s, "bf16")
+
+
+@pytest.mark.parametrize("dim,row_dtype", [(4, "f32"), (32, "bf16"), (128, "f32"), (512, "bf16"), (1024, "f32")])
+def test_pooled_team_shapes(dim, row_dtype):
+    """Row shapes that give every team size (4 to 32 lanes) and several column groups per lane (d = 512 bf16,
+    d = 1024 fp32), on jagged bags with sum and mean pooling, against the oracle."""
+    tab = mt.Table(14, dim, row_dtype=row_dtype)
+    ref = oracle.Table(14, dim, row_dtype=oracle.BF16 if row_dtype == "bf16" else oracle.F32)
+    b = W.jagged_batch(11, users=24)
+    bo = jagged_bags(b)
+    for s, mode in enumerate(("sum", "mean")):
+        pooled_step(tab, ref, b, bo, mode, 300 + s, row_dtype)

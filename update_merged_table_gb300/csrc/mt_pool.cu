@@ -11,7 +11,7 @@
 //
 // Kernels:
 //  k_pool         positions in chunks of kPoolChunk, a team of lanes per
-//                 chunk (one 16-byte vector of a row per lane, four rows in
+//                 chunk (one 16-byte vector of a row per lane, two rows in
 //                 flight), rows summed as exact fp32 pairs (TwoSum on the
 //                 paired fp32 instructions, two columns each); the
 //                 chunk's first bag comes from a team-wide multiway search of
@@ -67,10 +67,10 @@ __device__ __forceinline__ long long bag_search(const long long* bo, long long B
 }
 
 template <int RD>
-__global__ void __launch_bounds__(256, 3) k_pool(const PoolParams p) {
+__global__ void __launch_bounds__(256, 4) k_pool(const PoolParams p) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;  // columns per lane: one 16-byte load of a row
   constexpr int NP = VEC / 2;                // column pairs per lane
-  constexpr int UNR = 4;                     // rows in flight per lane
+  constexpr int UNR = 2;                     // rows in flight per lane
   __shared__ int32_t s_row[(256 >> kPoolMinTeamShift) * kPoolChunk];  // per team: the rows of its chunk
   const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
@@ -79,47 +79,49 @@ __global__ void __launch_bounds__(256, 3) k_pool(const PoolParams p) {
   const int team_base = lane & ~(team - 1);
   const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << team_base);
   int32_t* my_row = s_row + (threadIdx.x >> team_shift) * kPoolChunk;
-  const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
-  const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
-  const long long nchunks = (p.n + kPoolChunk - 1) / kPoolChunk;
-  const long long U = *p.num_unique;
+  // positions, bags and unique indices fit in int (the entry point admits n, B < 2^31)
+  const int n = (int)p.n;
+  const int B = (int)p.num_bags;
+  const int U = (int)*p.num_unique;
   const int d = (int)p.T.dim;
-  const long long B = p.num_bags;
+  const int nchunks = (n + kPoolChunk - 1) / kPoolChunk;
+  const int gteam = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> team_shift);
+  const int nteam = (int)((gridDim.x * blockDim.x) >> team_shift);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  // an offset relative to the chunk start, clamped to [0, kPoolChunk + 1]
-  auto rel = [](long long x, long long p0) -> int {
+  // a bag offset relative to the chunk start p0, clamped to [-1, kPoolChunk + 1]: the comparisons with
+  // the chunk's positions [0, cnt) stay exact
+  auto rel = [](long long x, int p0) -> int {
     const long long r = x - p0;
-    return r < 0 ? 0 : (r > kPoolChunk ? kPoolChunk + 1 : (int)r);
+    return r < 0 ? -1 : (r > kPoolChunk ? kPoolChunk + 1 : (int)r);
   };
 
-  for (long long c = gteam; c < nchunks; c += nteam) {  // uniform per team
-    const long long p0 = c * kPoolChunk;
-    const int cnt = (int)min((long long)kPoolChunk, p.n - p0);
+  for (int c = gteam; c < nchunks; c += nteam) {  // uniform per team
+    const int p0 = c * kPoolChunk;
+    const int cnt = min(kPoolChunk, n - p0);
     // the chunk's rows (-1: nothing to add)
     for (int q = lt; q < cnt; q += team) {
       const int32_t u = __ldg(&p.inverse[p0 + q]);
       my_row[q] = (u >= 0 && u < U) ? __ldg(&p.unique_rows[u]) : -1;
     }
-    const long long b_first = bag_search(p.bag_offsets, B, p0, lt, team, team_mask, team_base);
+    const int b_first = (int)bag_search(p.bag_offsets, B, p0, lt, team, team_mask, team_base);
     // positions before the first bag belong to none
     const int q_skip = b_first < 0 && B > 0 ? rel(__ldg(&p.bag_offsets[0]), p0) : 0;
     __syncwarp(team_mask);
     for (int c0 = 0; c0 < d; c0 += team * VEC) {
       const int col = c0 + lt * VEC;
       const bool active = col < d;
-      long long b = b_first < 0 ? 0 : b_first;
-      long long b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p0 + cnt;
-      int q_end = rel(b_end, p0);
+      int b = b_first < 0 ? 0 : b_first;
+      int q_end = b < B ? rel(__ldg(&p.bag_offsets[b + 1]), p0) : cnt;  // end of bag b, chunk-relative
       f32x2 hi[NP], lo[NP];
 #pragma unroll
       for (int j = 0; j < NP; ++j) hi[j] = lo[j] = 0ull;
-      // a bag's sum leaves the running pair, one column pair at a time: written out (rounded once) when
-      // the whole bag lies in this chunk, else added to the bag's fp64 accumulator
-      auto flush = [&](long long bb, long long bend) {
+      // bag bb (ending at chunk-relative re) leaves the running pair, one column pair at a time: written out
+      // (rounded once) when the whole bag lies in this chunk, else added to its fp64 accumulator
+      auto flush = [&](int bb, int re) {
         if (bb < 0 || bb >= B || !active) return;
-        const long long bstart = __ldg(&p.bag_offsets[bb]);
-        const bool whole = bstart >= p0 && bend <= p0 + cnt && bend > bstart;
-        const double len = (double)(bend - bstart);
+        const int rs = rel(__ldg(&p.bag_offsets[bb]), p0);
+        const bool whole = rs >= 0 && re <= cnt && re > rs;
+        const double len = (double)(re - rs);
 #pragma unroll
         for (int j = 0; j < NP; ++j) {
           const float2 h = upk(hi[j]), l = upk(lo[j]);
@@ -151,10 +153,9 @@ __global__ void __launch_bounds__(256, 3) k_pool(const PoolParams p) {
           const int q = q0 + r;
           if (q >= cnt) break;
           while (q >= q_end && b < B) {  // position q starts a later bag
-            flush(b, b_end);
+            flush(b, q_end);
             ++b;
-            b_end = b < B ? __ldg(&p.bag_offsets[b + 1]) : p0 + cnt;
-            q_end = rel(b_end, p0);
+            q_end = b < B ? rel(__ldg(&p.bag_offsets[b + 1]), p0) : cnt;
           }
           if (b >= B || q < q_skip) continue;  // in no bag
           const uint32_t w[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(256, 3) k_pool(const PoolParams p) {
           }
         }
       }
-      if (b < B) flush(b, b_end);
+      if (b < B) flush(b, q_end);
     }
     __syncwarp(team_mask);  // my_row is refilled by the next chunk
   }
