@@ -786,16 +786,37 @@ def run_ours(args):
         tab.compact()  # first call allocates its workspace
         torch.cuda.synchronize(dev)
         cc0, cc1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        mt.profile_enable(True)
+        mt.profile_report(reset=True)
         cc0.record(stream)
         tab.compact()
         cc1.record(stream)
         torch.cuda.synchronize(dev)
+        cp = mt.profile_report(reset=True)
+        mt.profile_enable(False)
         c_ms = cc0.elapsed_time(cc1)
+        k_ms = cp["k_compact_rebuild"][1] if "k_compact_rebuild" in cp else None
         M = 1 << wl.log2
-        comp = {"ms": c_ms, "slots": M, "live": int(st_before["live"]),
+        comp = {"ms": c_ms, "kernel_ms": k_ms, "slots": M, "live": int(st_before["live"]),
                 "algorithmic_GB/s": 32.0 * M / (c_ms / 1e3) / 1e9,  # read every old slot, write every new one
-                "note": "mt_compact: live keys re-inserted into a spare slot array that becomes the table's "
-                        "(no copy back)"}
+                "note": "mt_compact (one call: clear the spare slot array, re-insert the live keys into it, swap); "
+                        "kernel_ms is the re-insert kernel alone"}
+
+    # -------- occupancy statistics: one scan of the key store (the kernel's own device time) --------
+    stats_leg = None
+    if ws == 1:
+        tab.stats()
+        mt.profile_enable(True)
+        mt.profile_report(reset=True)
+        tab.stats()
+        sp = mt.profile_report(reset=True)
+        mt.profile_enable(False)
+        if "k_stats" in sp:
+            s_ms = sp["k_stats"][1] / sp["k_stats"][0]
+            M = 1 << wl.log2
+            stats_leg = {"kernel_ms": s_ms, "slots": M, "algorithmic_GB/s": 16.0 * M / (s_ms / 1e3) / 1e9,
+                         "frac": 16.0 * M / (s_ms / 1e3) / 1e9 / peak,
+                         "note": "mt_stats: one read of every 16-byte slot (live, tombstones, probe-index histogram)"}
 
     # -------- capacity expansion: twice the slots, rows unchanged (one call, after everything else) --------
     grow = None
@@ -803,15 +824,21 @@ def run_ours(args):
         st_before = tab.stats()
         M_old = 1 << wl.log2
         torch.cuda.synchronize(dev)
+        mt.profile_enable(True)
+        mt.profile_report(reset=True)
         g0 = time.perf_counter()
         tab.grow(wl.log2 + 1, num_rows=tab.cfg.num_rows)  # synchronises
         g_ms = (time.perf_counter() - g0) * 1e3
-        grow = {"ms_host_timed": g_ms, "slots_before": M_old, "slots_after": 2 * M_old,
+        gp = mt.profile_report(reset=True)
+        mt.profile_enable(False)
+        grow = {"ms_host_timed": g_ms, "kernels_ms": {k: v[1] for k, v in gp.items()},
+                "slots_before": M_old, "slots_after": 2 * M_old,
                 "live": int(st_before["live"]),
                 "rows_moved": 0, "row_bytes_in_table": int(tab.cfg.num_rows) * (B + 8 * wl.dim),
                 "key_store_GB/s": (16.0 * M_old + 16.0 * 2 * M_old) / (g_ms / 1e3) / 1e9,
                 "note": "mt_table_grow: a new key store (old slots read, new slots cleared and filled); the rows "
-                        "stay in place, so the cost follows the slot count, not the row pool"}
+                        "stay in place, so the cost follows the slot count, not the row pool; ms_host_timed includes "
+                        "allocating the new key store and row segment"}
         if tab.stats()["live"] != st_before["live"]:
             raise RuntimeError("capacity expansion lost keys")
 
@@ -853,6 +880,7 @@ def run_ours(args):
         "cold_step": cold_stats,
         "pooled": pooled,
         "compaction": comp,
+        "stats": stats_leg,
         "grow": grow,
         "e2e": e2e,
         "gpu_launches": int(launches),

@@ -16,13 +16,14 @@
 //             each position's rank among its key's positions); every
 //             tile-local unique becomes one record {key, first position,
 //             count}, the tile's records stored together.
-//  k_claim    stage 2, one thread per record over the whole GPU: claim the
-//             key in the global scratch hash; one 64-bit atomic adds the
-//             record's count and returns the key's count and first position
-//             so far (the count is the rank base of the tile's positions);
-//             the first position is lowered only when this record can lower
-//             it.  The thread whose CAS put a key into the scratch hash lists
-//             it as a distinct key.
+//  k_claim    stage 2, one thread per record over the whole GPU: a new key
+//             is installed in the global scratch hash by one 128-bit CAS
+//             with its record's first position and count; a present key gets
+//             one 64-bit atomic that adds the record's count and returns the
+//             key's count and first position so far (the count is the rank
+//             base of the tile's positions), and an atomicMin only when the
+//             record lowers the first position.  The thread that installed a
+//             key lists it as a distinct key.
 //  k_resolve  one thread per distinct key: find the key in the table
 //             (odd-step probing) or insert it (first tombstone or EMPTY slot
 //             of its chain, rows popped once per block; fresh rows listed for
@@ -225,34 +226,61 @@ __global__ void __launch_bounds__(kThreadsA, 4) k_local(const LookupParams p) {
 
 // Stage 2: one thread per record {key, first position in its tile, count in
 // its tile}, two records per thread in flight, over the whole GPU.  Each
-// record's chain of global round trips is short (a load of the key's home
-// slot, a CAS when it is EMPTY, one 64-bit atomic), and nothing waits on a
-// block barrier in between: the block's distinct keys collect in shared
+// record's chain of global round trips is short: a load of the key's home
+// slot, then either one 128-bit CAS that installs a new key with its first
+// position and count, or one 64-bit atomic that adds to a present key (and an
+// atomicMin when the record lowers the key's first position).  Nothing waits
+// on a block barrier in between: the block's distinct keys collect in shared
 // memory and are listed once at the end (or once per round when the block's
 // share of records could overflow that buffer).
 constexpr int kClaimILP = 2;     // records per thread per round
 constexpr int kWinCap = 4096;    // distinct keys a block holds before listing them
 
+// 128-bit compare-and-swap of a whole scratch slot (sm_90 and later): returns the slot's previous contents.
+__device__ __forceinline__ ulonglong2 cas_slot(ScSlot* slot, ulonglong2 expect, ulonglong2 desired) {
+  ulonglong2 old;
+  asm volatile(
+      "{\n\t"
+      ".reg .b128 d, e, v;\n\t"
+      "mov.b128 e, {%2, %3};\n\t"
+      "mov.b128 v, {%4, %5};\n\t"
+      "atom.global.cas.b128 d, [%6], e, v;\n\t"
+      "mov.b128 {%0, %1}, d;\n\t"
+      "}"
+      : "=l"(old.x), "=l"(old.y)
+      : "l"(expect.x), "l"(expect.y), "l"(desired.x), "l"(desired.y), "l"(slot)
+      : "memory");
+  return old;
+}
+
 // Claims `key` in the scratch hash from slot h whose contents sv were loaded
-// already: the first slot holding the key or EMPTY (then CASed).  Returns
-// whether this call put the key there; *first_seen is the first position
-// the slot held when it was seen with the key (EMPTY: none).
-__device__ __forceinline__ bool claim_from(const LookupParams& p, unsigned long long key, unsigned long long& h,
-                                           ulonglong2 sv, uint32_t* first_seen) {
-  *first_seen = 0xFFFFFFFFu;
+// already: the first slot holding the key, or an EMPTY one, which a single
+// 128-bit CAS fills with the key, the record's first position and its count
+// at once.  Returns whether this call put the key there (its record's rank
+// base is then 0 and nothing is left to add); otherwise *first_seen is the
+// first position the slot held when it was seen with the key.
+__device__ __forceinline__ bool claim_from(const LookupParams& p, unsigned long long key, uint32_t gpos,
+                                           uint32_t lcount, unsigned long long& h, ulonglong2 sv,
+                                           uint32_t* first_seen) {
+  // a fresh slot: key EMPTY, first "none", count - 1 = 2^32 - 1 (the memset); {first, count - 1} change
+  // only after a key is in the slot
+  const ulonglong2 fresh = make_ulonglong2(kEmpty, ~0ull);
+  const ulonglong2 mine = make_ulonglong2(key, (unsigned long long)gpos | ((unsigned long long)(lcount - 1u) << 32));
   for (unsigned long long probe = 0; probe < p.ss; ++probe) {
-    unsigned long long cur = sv.x;
     // a plain load first: the hottest keys have a record from nearly every tile, and a CAS on their
     // slot would queue behind every other tile's at the L2
-    if (cur == kEmpty) cur = atomicCAS(&p.sc[h].key, kEmpty, key);
-    if (cur == kEmpty) return true;
-    if (cur == key) {
-      if (sv.x == key) *first_seen = (uint32_t)(sv.y & 0xFFFFFFFFull);
+    if (sv.x == kEmpty) {
+      sv = cas_slot(&p.sc[h], fresh, mine);
+      if (sv.x == kEmpty) return true;  // the slot was fresh: it now holds this record
+    }
+    if (sv.x == key) {
+      *first_seen = (uint32_t)(sv.y & 0xFFFFFFFFull);
       return false;
     }
     h = h + 1 == p.ss ? 0ull : h + 1;
     sv = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[h]));
   }
+  *first_seen = 0u;
   return false;  // not reached: the scratch hash has more slots than records
 }
 
@@ -305,21 +333,25 @@ __global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
     for (int k = 0; k < kClaimILP; ++k) {
       if (r[k] >= R) continue;
       uint32_t old_first;
-      const bool won = claim_from(p, key[k], h[k], sv[k], &old_first);
-      if (p.ranks != nullptr) {
-        // {first, count - 1} of the slot are one 64-bit word: adding the count to its high half returns
-        // both, the count being the rank base of this record's positions
-        const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h[k]].first),
-                                                 (unsigned long long)lcount[k] << 32);
-        old_first = (uint32_t)(old & 0xFFFFFFFFull);
-        p.rec_rb[r[k]] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before
+      const bool won = claim_from(p, key[k], gpos[k], lcount[k], h[k], sv[k], &old_first);
+      if (won) {
+        if (p.ranks != nullptr) p.rec_rb[r[k]] = 0;  // the key's first record: no positions before it
+        s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h[k];
       } else {
-        atomicAdd(&p.sc[h[k]].cnt, lcount[k]);  // no ranks asked for: the count alone, no value returned
+        if (p.ranks != nullptr) {
+          // {first, count - 1} of the slot are one 64-bit word: adding the count to its high half returns
+          // both, the count being the rank base of this record's positions
+          const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h[k]].first),
+                                                   (unsigned long long)lcount[k] << 32);
+          old_first = (uint32_t)(old & 0xFFFFFFFFull);
+          p.rec_rb[r[k]] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before
+        } else {
+          atomicAdd(&p.sc[h[k]].cnt, lcount[k]);  // no ranks asked for: the count alone, no value returned
+        }
+        // lower the key's first position only when this record can (the first position only decreases)
+        if (gpos[k] < old_first) atomicMin(&p.sc[h[k]].first, gpos[k]);
       }
       p.rec_slot[r[k]] = (int32_t)h[k];
-      // lower the key's first position only when this record can (the first position only decreases)
-      if (gpos[k] < old_first) atomicMin(&p.sc[h[k]].first, gpos[k]);
-      if (won) s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h[k];
     }
     if (list_each_round) list_winners(p, s_win, &s_nwin, &s_wbase);
   }

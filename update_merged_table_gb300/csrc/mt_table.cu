@@ -60,33 +60,41 @@ __global__ void k_erase_apply(const TableDev T, const unsigned long long* keys, 
   }
 }
 
-// Compaction: every live key of the table is inserted again, with its row
-// and meta, into the fresh slot array `fresh` (all EMPTY), along the same
-// probe sequence; keys are distinct, so a CAS only ever loses to another key.
-// A key that finds no EMPTY slot within max_probes sets the header's flag
-// (the call then keeps the old slots and latches MT_EFULL).
-__global__ void k_compact_rebuild(const TableDev T, Slot* fresh) {
-  const unsigned long long M = T.mask + 1;
+// Every live key of src's slots, with its row and meta, inserted into `slots`
+// (all EMPTY) along its probe sequence in table `dst`: one old slot per
+// thread and loop trip, many threads (one CAS each in flight beats several
+// per thread here, measured).  Keys are distinct, so a CAS only ever loses to
+// another key.  A key that finds no EMPTY slot within dst's probe limit sets
+// dst's header flag (and latches MT_EFULL when latch_full).
+__device__ __forceinline__ void reinsert_live(const TableDev& src, const TableDev& dst, Slot* slots, bool latch_full) {
+  const unsigned long long M = src.mask + 1;
   for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
        s += (unsigned long long)gridDim.x * blockDim.x) {
-    const Slot old = T.slots[s];
+    const Slot old = src.slots[s];
     if (old.key == kEmpty || old.key == kTomb) continue;
-    unsigned long long h = home_slot(T, old.key);
+    unsigned long long h = home_slot(dst, old.key);
     bool placed = false;
-    for (uint32_t t = 0; t < T.max_probes; ++t) {
-      if (atomicCAS(&fresh[h].key, kEmpty, old.key) == kEmpty) {
-        fresh[h].row = old.row;
-        fresh[h].meta = old.meta;
+    for (uint32_t t = 0; t < dst.max_probes; ++t) {
+      if (atomicCAS(&slots[h].key, kEmpty, old.key) == kEmpty) {
+        slots[h].row = old.row;
+        slots[h].meta = old.meta;
         placed = true;
         break;
       }
-      h = (h + T.S) & T.mask;
+      h = (h + dst.S) & dst.mask;
     }
     if (!placed) {
-      atomicExch(&T.hdr->pad0, 1);
-      latch_error(T.hdr, MT_EFULL);
+      atomicExch(&dst.hdr->pad0, 1);
+      if (latch_full) latch_error(dst.hdr, MT_EFULL);
     }
   }
+}
+
+// Compaction: every live key of the table inserted again into the fresh slot
+// array `fresh` along the same probe sequence (a key that does not fit makes
+// the call keep the old slots and latch MT_EFULL).
+__global__ void __launch_bounds__(256) k_compact_rebuild(const TableDev T, Slot* fresh) {
+  reinsert_live(T, T, fresh, true);
 }
 
 // Import pass 1: find each key, or insert it like a lookup does (first
@@ -171,27 +179,17 @@ __global__ void k_grow_top(const TableDev T2, long long old_rows) {
 
 // Capacity expansion, pass 2: every live key of the old slots is inserted
 // into the new (all EMPTY) slots along its probe sequence in the new table.
-__global__ void k_grow_rebuild(const TableDev T, const TableDev T2) {
-  const unsigned long long M = T.mask + 1;
-  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
-       s += (unsigned long long)gridDim.x * blockDim.x) {
-    const Slot old = T.slots[s];
-    if (old.key == kEmpty || old.key == kTomb) continue;
-    unsigned long long h = home_slot(T2, old.key);
-    bool placed = false;
-    for (uint32_t t = 0; t < T2.max_probes; ++t) {
-      if (atomicCAS(&T2.slots[h].key, kEmpty, old.key) == kEmpty) {
-        T2.slots[h].row = old.row;
-        T2.slots[h].meta = old.meta;
-        placed = true;
-        break;
-      }
-      h = (h + T2.S) & T2.mask;
-    }
-    if (!placed) atomicExch(&T2.hdr->pad0, 1);
-  }
+__global__ void __launch_bounds__(256) k_grow_rebuild(const TableDev T, const TableDev T2) {
+  reinsert_live(T, T2, T2.slots, false);
 }
 
+// One pass over the slots: live keys, tombstones, total displacement and the
+// probe-index histogram.  Nearly every key of a healthy table sits at a small
+// probe index, so the first kStatRegBins indices are counted in registers and
+// summed per warp (shared-memory atomics on one bin would serialise); longer
+// chains go to shared memory.  Four streaming slot loads per thread in flight.
+constexpr int kStatRegBins = 8;
+constexpr int kStatUnroll = 4;
 __global__ void __launch_bounds__(256) k_stats(const TableDev T) {
   __shared__ unsigned long long s_hist[MT_HIST_BINS];
   __shared__ unsigned long long s_live, s_tomb, s_disp;
@@ -199,19 +197,39 @@ __global__ void __launch_bounds__(256) k_stats(const TableDev T) {
   if (threadIdx.x == 0) s_live = s_tomb = s_disp = 0;
   __syncthreads();
   unsigned long long live = 0, tomb = 0, disp = 0;
+  uint32_t c[kStatRegBins];
+#pragma unroll
+  for (int j = 0; j < kStatRegBins; ++j) c[j] = 0;
   const unsigned long long M = T.mask + 1;
-  for (unsigned long long s = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s < M;
-       s += (unsigned long long)gridDim.x * blockDim.x) {
-    const unsigned long long key = T.slots[s].key;
-    if (key == kTomb) {
-      ++tomb;
-    } else if (key != kEmpty) {
-      ++live;
-      // slot = h0 + t*S (mod M)  =>  t = (slot - h0) * S^-1 (mod M)
-      const unsigned long long t = ((s - home_slot(T, key)) & T.mask) * T.Sinv & T.mask;
-      disp += t;
-      atomicAdd(&s_hist[t < MT_HIST_BINS - 1 ? t : MT_HIST_BINS - 1], 1ull);
+  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+  for (unsigned long long s0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; s0 < M;
+       s0 += stride * kStatUnroll) {
+    unsigned long long key[kStatUnroll];
+#pragma unroll
+    for (int k = 0; k < kStatUnroll; ++k) {
+      const unsigned long long s = s0 + k * stride;
+      key[k] = s < M ? __ldcs(&T.slots[s].key) : kEmpty;
     }
+#pragma unroll
+    for (int k = 0; k < kStatUnroll; ++k) {
+      if (key[k] == kTomb) {
+        ++tomb;
+      } else if (key[k] != kEmpty) {
+        ++live;
+        // slot = h0 + t*S (mod M)  =>  t = (slot - h0) * S^-1 (mod M)
+        const unsigned long long s = s0 + k * stride;
+        const unsigned long long t = ((s - home_slot(T, key[k])) & T.mask) * T.Sinv & T.mask;
+        disp += t;
+#pragma unroll
+        for (int j = 0; j < kStatRegBins; ++j) c[j] += t == (unsigned long long)j;
+        if (t >= (unsigned long long)kStatRegBins) atomicAdd(&s_hist[t < MT_HIST_BINS - 1 ? t : MT_HIST_BINS - 1], 1ull);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kStatRegBins; ++j) {
+    const unsigned w = __reduce_add_sync(kFull, c[j]);
+    if ((threadIdx.x & 31) == 0 && w) atomicAdd(&s_hist[j], (unsigned long long)w);
   }
   atomicAdd(&s_live, live);
   atomicAdd(&s_tomb, tomb);
@@ -323,7 +341,7 @@ cudaError_t launch_stats(const TableDev& T, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_stats", s);
-    k_stats<<<grid_for((long long)(T.mask + 1), 256, 32), 256, 0, s>>>(T);
+    k_stats<<<grid_for((long long)(T.mask + 1) / kStatUnroll, 256, 4), 256, 0, s>>>(T);  // all resident
   }
   return cudaGetLastError();
 }
