@@ -677,7 +677,8 @@ def run_ours(args):
     if args.graph:
         # every workspace sized for the largest batch first: a capture must not replace a buffer that graphs
         # captured before it still use
-        tab.reserve_workspaces(max(e["batch"].n for e in pool + prof_pool))
+        tab.reserve_workspaces(max(e["batch"].n for e in pool + prof_pool),
+                               n_erase=max(e["n_erase"] for e in pool + prof_pool))
         torch.cuda.synchronize(dev)
         graphs = []
         l0 = mt.kernel_launches()

@@ -397,11 +397,13 @@ class Table:
                "mt_backward_adam_pooled")
         return gsum
 
-    def reserve_workspaces(self, n: int, num_bags: int = 0):
-        """Allocate every workspace a batch of n IDs (and num_bags pooled bags) needs, so that later calls
-        (for instance under CUDA graph capture) allocate nothing."""
+    def reserve_workspaces(self, n: int, num_bags: int = 0, n_erase: int = 0):
+        """Allocate every workspace a batch of n IDs (num_bags pooled bags, n_erase keys to erase) needs, so
+        that later calls (for instance under CUDA graph capture) allocate nothing."""
         self._workspace("lookup", self.lib.mt_lookup_workspace_bytes(self.h, n))
         self._workspace("backward", self.lib.mt_backward_workspace_bytes(self.h, n))
+        if n_erase:
+            self._workspace("erase", self.lib.mt_erase_workspace_bytes(n_erase))
         if num_bags:
             self._workspace("pool", self.lib.mt_pool_workspace_bytes(self.h, num_bags))
             self._workspace("backward_pooled", self.lib.mt_backward_pooled_workspace_bytes(self.h, n, num_bags))

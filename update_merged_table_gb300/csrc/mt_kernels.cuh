@@ -22,11 +22,12 @@ constexpr uint16_t kNoIdx = 0xFFFF;
 // One slot of the stage-2 scratch hash.  The lookup clears the slots to all
 // ones, so a fresh slot holds key EMPTY, first = "none" and cnt = 2^32 - 1,
 // i.e. cnt stores (positions - 1): an atomicAdd of c returns (positions
-// added before) - 1.  After numbering, `first` holds the key's unique index.
+// added before) - 1.  After numbering, `first` holds the key's unique index
+// and `cnt` its table row.
 struct __align__(16) ScSlot {
   unsigned long long key;
   uint32_t first;  // smallest position holding the key (atomicMin), then its unique index
-  uint32_t cnt;    // positions holding the key, minus one
+  uint32_t cnt;    // positions holding the key, minus one; then its table row
 };
 static_assert(sizeof(ScSlot) == 16, "scratch slot is 16 bytes");
 
@@ -66,6 +67,7 @@ struct LookupParams {
   unsigned long long* owner_nb;  // [ntiles * kTile / 64] bit i clear: position i is its key's first (cleared
                                  // to all ones)
   uint16_t* wpre;         // [ntiles * kTile / 64] first positions in the tile before each 64-position word
+  int32_t* prow;          // [ntiles * kTile] table row of each position (-1: none), for the gather
   int32_t* tile_pre;      // [ntiles + 1] first positions before each tile (its count, then the exclusive prefix)
   uint32_t* done;         // k_prefix blocks finished (zeroed by k_local)
   uint16_t* lidx;         // [ntiles * kTile] tile-local unique of each position
@@ -76,7 +78,7 @@ struct LookupParams {
 
 struct LookupWsLayout {
   size_t sc, ulist_n, ulist, rec, rec_slot, rec_rb, fresh_row, fresh_key, sc_row, tile_L, owner_nb, tile_pre, done,
-      wpre, tile_rec, lrank, lidx, total;
+      wpre, prow, tile_rec, lrank, lidx, total;
   size_t clear_bytes;  // bytes from the start of the workspace cleared to all ones per call
   unsigned long long ss;
   int ntiles;

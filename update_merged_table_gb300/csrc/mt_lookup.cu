@@ -35,10 +35,10 @@
 //  k_number   one thread per distinct key: its unique index is the number of
 //             first positions before its own (tile offset + word offset + a
 //             popcount), which is first-occurrence order; it writes the
-//             unique key, row and count and leaves the index in the scratch
-//             slot.
-//  k_expand   per tile: inverse index and rank of every position; then a
-//             share of the fresh rows is initialised (Philox-keyed values,
+//             unique key, row and count and leaves the index and the row in
+//             the scratch slot.
+//  k_expand   per tile: inverse index, rank and table row of every position;
+//             then a share of the fresh rows is initialised (Philox-keyed values,
 //             m = v = 0) by teams of lanes, filling the issue slots of this
 //             latency-bound kernel.
 //  k_gather   the 16-byte vectorised row gather over the whole batch.
@@ -498,8 +498,8 @@ __global__ void __launch_bounds__(kThreads) k_prefix(const LookupParams p) {
 // One thread per distinct key (the claim-order list): the key's unique index
 // is the number of first positions before its own (tile offset + word offset
 // + the bits before it in its word), i.e. first-occurrence order.  It writes
-// the key's unique entry and leaves the index in the scratch slot for
-// k_expand.
+// the key's unique entry and leaves the index and the table row in the
+// scratch slot for k_expand.
 __global__ void __launch_bounds__(kThreadsR) k_number(const LookupParams p) {
   constexpr int ILP = 2;  // keys per thread in flight: every load of both before any store
   const uint32_t U = *p.ulist_n + 1u;  // the counter starts at 2^32 - 1
@@ -531,7 +531,9 @@ __global__ void __launch_bounds__(kThreadsR) k_number(const LookupParams p) {
         p.unique_keys[u[k]] = sv[k].x;
         p.unique_rows[u[k]] = row[k];
         p.counts[u[k]] = (int32_t)((uint32_t)(sv[k].y >> 32) + 1u);
-        p.sc[slot[k]].first = (uint32_t)u[k];  // from here on the slot holds the key's unique index
+        // from here on the slot's {first, count - 1} word holds {unique index, table row}: one load for k_expand
+        *reinterpret_cast<unsigned long long*>(&p.sc[slot[k]].first) =
+            (unsigned long long)(uint32_t)u[k] | ((unsigned long long)(uint32_t)row[k] << 32);
       }
   }
 }
@@ -541,6 +543,7 @@ __global__ void __launch_bounds__(kThreadsR) k_number(const LookupParams p) {
 __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
   __shared__ int32_t s_u[kTile];   // unique index of each tile-local unique
   __shared__ int32_t s_rb[kTile];  // rank base of each tile-local unique
+  __shared__ int32_t s_row[kTile];  // table row of each tile-local unique (when the lookup gathers)
   const int tile = blockIdx.x, tid = threadIdx.x;
   const long long base = (long long)tile * kTile;
   const int cnt = (int)min((long long)kTile, p.n - base);
@@ -553,10 +556,15 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
     sl[k] = l < L ? __ldcg(&p.rec_slot[r0 + l]) : -1;
     if (l < L && p.ranks != nullptr) s_rb[l] = __ldcg(&p.rec_rb[r0 + l]);
   }
+  const bool gather = p.out_rows != nullptr;
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int l = k * kThreads + tid;
-    if (l < L) s_u[l] = (int32_t)__ldcg(&p.sc[sl[k]].first);
+    if (l < L) {
+      const unsigned long long ur = __ldcg(reinterpret_cast<const unsigned long long*>(&p.sc[sl[k]].first));
+      s_u[l] = (int32_t)(uint32_t)(ur & 0xFFFFFFFFull);
+      s_row[l] = (int32_t)(uint32_t)(ur >> 32);
+    }
   }
   __syncthreads();
   uint16_t li[kPPT];
@@ -569,6 +577,13 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
   for (int k = 0; k < kPPT; ++k) {
     const int lp = k * kThreads + tid;
     if (lp < cnt) p.inverse[base + lp] = li[k] == kNoIdx ? -1 : s_u[li[k]];
+  }
+  if (gather) {  // the gather then reads each position's row directly
+#pragma unroll
+    for (int k = 0; k < kPPT; ++k) {
+      const int lp = k * kThreads + tid;
+      if (lp < cnt) p.prow[base + lp] = li[k] == kNoIdx ? -1 : s_row[li[k]];
+    }
   }
   if (p.ranks != nullptr) {
 #pragma unroll
@@ -590,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
     init_row_coop(p.T, __ldcg(&p.fresh_row[f]), __ldcg(&p.fresh_key[f]), tid % team, team);
 }
 
-// out[i] = row of unique inverse[i] (zeros for an invalid ID or an absent
+// out[i] = row prow[i] of position i (zeros for an invalid ID or an absent
 // key): 16-byte items (position, vector), consecutive threads on consecutive
 // items; each round a block covers kGatherILP * blockDim contiguous items
 // (kGatherILP independent items in flight per thread), and the blocks stride
@@ -613,8 +628,7 @@ __global__ void __launch_bounds__(256) k_gather(const LookupParams p) {
       row[k] = -1;
       if (it < total) {
         const long long i = vshift >= 0 ? (it >> vshift) : it / vec16;
-        const int32_t u = __ldg(&p.inverse[i]);
-        if (u >= 0) row[k] = __ldg(&p.unique_rows[u]);
+        row[k] = __ldg(&p.prow[i]);
       }
     }
     uint4 v[kGatherILP];
@@ -667,6 +681,7 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.tile_pre = take((size_t)(L.ntiles + 1) * 4);
   L.done = take(16);
   L.wpre = take(cap / 64 * 2);
+  L.prow = take(cap * 4);
   L.tile_rec = take((size_t)L.ntiles * 4);
   L.lrank = take(cap * 2);
   L.lidx = take(cap * 2);
@@ -692,6 +707,7 @@ void bind_lookup_ws(LookupParams& p, char* w, const LookupWsLayout& L) {
   p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
   p.owner_nb = reinterpret_cast<unsigned long long*>(w + L.owner_nb);
   p.wpre = reinterpret_cast<uint16_t*>(w + L.wpre);
+  p.prow = reinterpret_cast<int32_t*>(w + L.prow);
   p.tile_pre = reinterpret_cast<int32_t*>(w + L.tile_pre);
   p.done = reinterpret_cast<uint32_t*>(w + L.done);
   p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
