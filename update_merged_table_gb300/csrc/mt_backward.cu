@@ -71,6 +71,26 @@ __device__ __forceinline__ void block_scan3(const int v[3], int ex[3], int tot[3
   __syncthreads();
 }
 
+// Block totals of three ints per thread (every thread receives them).  Contains __syncthreads.
+template <int NT>
+__device__ __forceinline__ void block_total3(const int v[3], int tot[3], int (*s_warp)[NT / 32]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    const int w = __reduce_add_sync(kFull, v[c]);
+    if (lane == 0) s_warp[c][warp] = w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    int t = 0;
+#pragma unroll
+    for (int q = 0; q < NT / 32; ++q) t += s_warp[c][q];
+    tot[c] = t;
+  }
+  __syncthreads();
+}
+
 // A unique with more than kChunk positions is "heavy": it is reduced in
 // warp-chunks of p.warp_chunk positions, each by one whole warp.
 __device__ __forceinline__ int warp_chunks(int c, int wc) { return c > kChunk ? (c + wc - 1) / wc : 0; }
@@ -113,8 +133,8 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
     v[1] += warp_chunks(c[k], p.warp_chunk);
     v[2] += c[k] > kChunk;
   }
-  int ex[3], tot[3];
-  block_scan3<kScanThreads>(v, ex, tot, s_warp);
+  int tot[3];
+  block_total3<kScanThreads>(v, tot, s_warp);
   if (threadIdx.x < 3) p.bsum[(size_t)blockIdx.x * 3 + threadIdx.x] = tot[threadIdx.x];
 }
 
@@ -132,38 +152,38 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   __shared__ int s_tot[3];
   const long long U = *p.num_unique;
   const int b = blockIdx.x;
-  {  // block offsets: sums over blocks < b; totals over all blocks
-    int pre[3] = {0, 0, 0}, all[3] = {0, 0, 0};
-    for (int q = threadIdx.x; q < p.nblk; q += kScanThreads) {
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        const int x = __ldg(&p.bsum[(size_t)q * 3 + c]);
-        all[c] += x;
-        if (q < b) pre[c] += x;
-      }
-    }
-    int ex[3], tot[3];
-    block_scan3<kScanThreads>(pre, ex, tot, s_warp);
-    if (threadIdx.x == 0) {
-      for (int c = 0; c < 3; ++c) s_base[c] = tot[c];
-    }
-    block_scan3<kScanThreads>(all, ex, tot, s_warp);
-    if (threadIdx.x == 0) {
-      for (int c = 0; c < 3; ++c) s_tot[c] = tot[c];
-      if (b == 0) {  // totals for the reduce kernels
-        for (int c = 0; c < 3; ++c) p.boff[(size_t)p.nblk * 3 + c] = tot[c];
-      }
-    }
-    __syncthreads();
-  }
-  if ((long long)b * kScanTile >= U) return;  // uniform over the block
   const long long u0 = (long long)b * kScanTile + (long long)threadIdx.x * kUPT;
-  int c[kUPT], rows[kUPT];  // every load in flight before the scan and the stores
+  int c[kUPT], rows[kUPT];  // the block's own uniques: loaded together with the block sums below
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
     c[k] = u0 + k < U ? __ldg(&p.counts[u0 + k]) : 0;
     rows[k] = u0 + k < U ? __ldg(&p.unique_rows[u0 + k]) : -1;
   }
+  {  // block offsets: sums over blocks < b; totals over all blocks
+    int pre[3] = {0, 0, 0}, all[3] = {0, 0, 0};
+    for (int q = threadIdx.x; q < p.nblk; q += kScanThreads) {
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc) {
+        const int x = __ldg(&p.bsum[(size_t)q * 3 + cc]);
+        all[cc] += x;
+        if (q < b) pre[cc] += x;
+      }
+    }
+    int tot[3];
+    block_total3<kScanThreads>(pre, tot, s_warp);
+    if (threadIdx.x == 0) {
+      for (int cc = 0; cc < 3; ++cc) s_base[cc] = tot[cc];
+    }
+    block_total3<kScanThreads>(all, tot, s_warp);
+    if (threadIdx.x == 0) {
+      for (int cc = 0; cc < 3; ++cc) s_tot[cc] = tot[cc];
+      if (b == 0) {  // totals for the reduce kernels
+        for (int cc = 0; cc < 3; ++cc) p.boff[(size_t)p.nblk * 3 + cc] = tot[cc];
+      }
+    }
+    __syncthreads();
+  }
+  if ((long long)b * kScanTile >= U) return;  // uniform over the block
   int v[3] = {0, 0, 0};
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
