@@ -98,3 +98,29 @@ def test_numa_binding_gpu_memory_node_takes_nearest_cpu_node(tmp_path):
                        distance={4: [80, 40, 80, 80, 10]})
     cpus, how = bench.numa_cpus_for_gpu("0009:01:00.0", root)
     assert cpus == set(range(72, 144)) and "nearest" in how
+
+
+def test_kernel_sources_and_traffic_digests(tmp_path, monkeypatch):
+    """Every kernel named in the committed traffic file is found in its own source file, and counters whose
+    recorded digest differs from the sources' are not used."""
+    import os
+    assert os.path.basename(bench.kernel_source("k_bw_light_reduce")) == "mt_backward.cu"
+    assert os.path.basename(bench.kernel_source("k_claim")) == "mt_lookup.cu"
+    assert bench.kernel_source("no_such_kernel") is None
+    assert bench.source_digest("k_claim") != bench.source_digest("k_bw_light_reduce")
+    # a traffic file with one current and one stale entry
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "kernel_traffic.txt").write_text(
+        "# comment\n"
+        f"k_bw_light_reduce 250.0 {bench.source_digest('k_bw_light_reduce')}\n"
+        "k_gather 97.0 0000000000000000\n")
+    src = tmp_path / "update_merged_table_gb300"
+    src.symlink_to(os.path.join(bench.ROOT, "update_merged_table_gb300"))
+    (tmp_path / "include").symlink_to(os.path.join(bench.ROOT, "include"))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.committed_traffic("k_bw_light_reduce") == (250.0, "profiles/kernel_traffic.txt")
+    value, why = bench.committed_traffic("k_gather")
+    assert value is None and "other sources" in why
+    value, why = bench.committed_traffic("k_expand")
+    assert value is None and "no counters" in why
