@@ -121,7 +121,7 @@ def run_sharded(G, dim, row_dtype, steps, make_batch, log2=14):
     assert all(s.step == steps for s in shards) and all(s.error() == 0 for s in shards)
 
 
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
 def test_sharded_merged_batches(G):
     """8 merged feature tables per rank, dim 16 fp32, two steps."""
     run_sharded(G, 16, "f32", 2, lambda step, r: W.merged_batch(1000 * step + r, per_table=512))
