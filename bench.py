@@ -509,6 +509,143 @@ def jagged_bag_offsets(b) -> np.ndarray:
     return np.concatenate([f * T + b.user_offsets[:-1] for f in range(F)] + [[F * T]]).astype(np.int64)
 
 
+def shard_run(args, wl, dev, stream, tdt):
+    """Sharded two-stage deduplication: G logical ranks on one GPU, each with its own jagged batch and one shard
+    table (the keys it owns).  A step is mt_shard_lookup (stage-1 unique per rank, owner partition, exchange,
+    stage-2 unique + find/insert + gather at the owners, rows back, expand) and mt_shard_backward_adam (per-rank
+    sums to the owners, owner sums, Adam).  The lookup reads the exchange sizes on the host, as a variable
+    all-to-all does, so the step runs eagerly (no graph)."""
+    import torch
+    import update_merged_table_gb300 as mt
+    G = args.shard
+    log2 = wl.log2 - 1  # the shards share the keys of G batches
+    shards = [mt.Table(log2, wl.dim, row_dtype=wl.row, hash_seed=r, device=dev) for r in range(G)]
+    grp = mt.ShardGroup(shards)
+    steps = min(args.steps, 8)
+    nstep = args.warmup + steps
+    batches = [[wl.batch(2000 + j * G + r)[0] for r in range(G)] for j in range(nstep)]
+    ids = [[torch.from_numpy(b.ids).to(dev) for b in row] for row in batches]
+    grads = [[_device_grads(torch, dev, tdt[wl.grad], 3000 + j * G + r, b.n, wl.dim) for r, b in enumerate(row)]
+             for j, row in enumerate(batches)]
+    stats = [[batch_stats(b) for b in row] for row in batches]
+
+    def step(j):
+        row = batches[j]
+        res = grp.lookup(ids[j], [b.feat_offsets for b in row], row[0].table_ids)
+        ev_m.record(stream)
+        grp.backward_adam(res, grads[j])
+
+    for j in range(args.warmup):
+        ev_m = torch.cuda.Event(enable_timing=True)
+        step(j)
+    torch.cuda.synchronize(dev)
+    live0 = sum(s.stats()["live"] for s in shards)
+    fwd_ms = bwd_ms = 0.0
+    for j in range(args.warmup, nstep):
+        e0, ev_m, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        step(j)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        fwd_ms += e0.elapsed_time(ev_m)
+        bwd_ms += ev_m.elapsed_time(e1)
+    live1 = sum(s.stats()["live"] for s in shards)
+    if any(s.error() != 0 for s in shards):
+        raise RuntimeError("device error in the sharded leg")
+    N = sum(b.n for j in range(args.warmup, nstep) for b in batches[j]) / steps
+    U = sum(st[0] for j in range(args.warmup, nstep) for st in stats[j]) / steps  # per-rank uniques, summed
+    new_keys = max(0.0, (live1 - live0) / steps)
+    B, Gb, d = wl.row_bytes, wl.grad_bytes, wl.dim
+    # the compulsory bytes of G ranks each with its own batch (the exchange's own traffic is not counted)
+    fwd_bytes = 8 * N + 4 * N + U * (8 + 16) + U * B + N * B + new_keys * (16 + B + 8 * d)
+    bwd_bytes = N * Gb + 4 * N + U * (4 + 2 * B + 16 * d)
+    peak, _ = measured_hbm_peak()
+    f_s, b_s = fwd_ms / steps / 1e3, bwd_ms / steps / 1e3
+    return {"G": G, "steps": steps, "ids_per_step": N, "rank_uniques_per_step": U, "new_keys_per_step": new_keys,
+            "ids_per_s": N / (f_s + b_s), "fwd_ms": f_s * 1e3, "bwd_ms": b_s * 1e3,
+            "roofline_fwd": {"bytes_per_step": fwd_bytes, "achieved": fwd_bytes / f_s / 1e9,
+                             "frac": fwd_bytes / f_s / 1e9 / peak},
+            "roofline_bwd": {"bytes_per_step": bwd_bytes, "achieved": bwd_bytes / b_s / 1e9,
+                             "frac": bwd_bytes / b_s / 1e9 / peak},
+            "what": "mt_shard_lookup + mt_shard_backward_adam over G logical ranks on one GPU (each a full jagged "
+                    "batch of its own), eager: the lookup reads the exchange sizes on the host"}
+
+
+def merged_run(args, dev, stream):
+    """Automatic table merging with mixed row shapes: the 8 features of the merged-tables workload (vocab 1e4 to
+    1e6, Zipf 0.8 to 1.3), 2^17 IDs each, given row dims 16, 16, 16, 32, 32, 32, 64, 64 (fp32); the planner puts
+    them into three merged tables.  A step is mt_lookup_grouped (every feature segment routed to its table) and
+    one mt_backward_adam per merged table, replayed as CUDA graphs on fresh batches."""
+    import torch
+    import update_merged_table_gb300 as mt
+    dims = [16, 16, 16, 32, 32, 32, 64, 64]
+    per = 1 << 17
+    features = [(dims[k], "f32", W.merged_vocab(k)) for k in range(len(dims))]
+    mtabs = mt.MergedTables(features, max_load=0.5, device=dev)
+    steps = min(args.steps, 8)
+    nstep = 1 + args.warmup + steps
+    batches = [W.merged_batch(4000 + j, per_table=per) for j in range(nstep)]
+    ids = [torch.from_numpy(b.ids).to(dev) for b in batches]
+    sizes = mtabs.group_sizes(batches[0].feat_offsets)
+    grads = [[_device_grads(torch, dev, torch.float32, 5000 + 10 * j + g, sizes[g], mtabs.groups[g]["dim"])
+              for g in range(len(sizes))] for j in range(nstep)]
+
+    def fwd(j):
+        return mtabs.lookup(ids[j], batches[j].feat_offsets)
+
+    for j in range(1 + args.warmup):  # cold step and warm-up, eager (they also size every workspace)
+        mtabs.backward_adam(fwd(j), grads[j])
+    for t, sz in zip(mtabs.tables, sizes):
+        t.reserve_workspaces(sz)
+    torch.cuda.synchronize(dev)
+    live0 = [t.stats()["live"] for t in mtabs.tables]
+    graphs = []
+    for j in range(1 + args.warmup, nstep):
+        gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf, stream=stream):
+            res = fwd(j)
+        with torch.cuda.graph(gb, stream=stream):
+            mtabs.backward_adam(res, grads[j])
+        graphs.append((gf, gb))
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in graphs]
+    for (gf, gb), (a, m_, z) in zip(graphs, ev):
+        a.record(stream)
+        gf.replay()
+        m_.record(stream)
+        gb.replay()
+        z.record(stream)
+    torch.cuda.synchronize(dev)
+    f_s = sum(a.elapsed_time(m_) for a, m_, _ in ev) / 1e3 / steps
+    b_s = sum(m_.elapsed_time(z) for _, m_, z in ev) / 1e3 / steps
+    live1 = [t.stats()["live"] for t in mtabs.tables]
+    if any(t.error() != 0 for t in mtabs.tables):
+        raise RuntimeError("device error in the merged-tables leg")
+    N = float(sum(sizes))
+    # per merged table: its IDs, uniques and row bytes (the same compulsory bytes as the single-table step)
+    fwd_bytes = bwd_bytes = 0.0
+    fo = batches[-1].feat_offsets
+    for g, grp in enumerate(mtabs.groups):
+        B = grp["dim"] * 4
+        d = grp["dim"]
+        segs = [f for f, (gg, _) in enumerate(mtabs.placement) if gg == g]
+        keys = np.concatenate([(np.uint64(mtabs.placement[f][1]) << np.uint64(56)) |
+                               batches[-1].ids[fo[f]:fo[f + 1]].astype(np.uint64) for f in segs])
+        Ng, Ug = float(keys.size), float(np.unique(keys).size)
+        new_g = max(0.0, (live1[g] - live0[g]) / steps)
+        fwd_bytes += 12 * Ng + Ug * (24 + B) + Ng * B + new_g * (16 + B + 8 * d)
+        bwd_bytes += Ng * B + 4 * Ng + Ug * (4 + 2 * B + 16 * d)
+    new_keys = max(0.0, (sum(live1) - sum(live0)) / steps)
+    peak, _ = measured_hbm_peak()
+    return {"tables": [(g["dim"], g["row_dtype"], g["num_features"], g["log2_slots"]) for g in mtabs.groups],
+            "ids_per_step": N, "new_keys_per_step": new_keys, "steps": steps,
+            "ids_per_s": N / (f_s + b_s), "fwd_ms": f_s * 1e3, "bwd_ms": b_s * 1e3,
+            "roofline_fwd": {"bytes_per_step": fwd_bytes, "frac": fwd_bytes / f_s / 1e9 / peak},
+            "roofline_bwd": {"bytes_per_step": bwd_bytes, "frac": bwd_bytes / b_s / 1e9 / peak},
+            "what": "mt_lookup_grouped over the planner's three merged tables (dims 16, 32, 64) + one backward and "
+                    "Adam per table, CUDA graphs, fresh batches"}
+
+
 def queue_ahead(torch, stream, steps: int):
     """Keep the GPU busy for about 2 ms (+ 0.5 ms per step) before an eager pass with per-kernel events, so that
     the host enqueues the pass's launches ahead of the GPU: a kernel's start event and the kernel then run back
@@ -780,6 +917,12 @@ def run_ours(args):
     # -------- pooled jagged bags (sum/mean of each user's rows per feature) on further fresh steps --------
     pooled = pooled_run(args, tab, wl, dev, stream, 1 + kf + nprof) if (args.config == 3 and args.pooled) else None
 
+    # -------- sharded two-stage dedup: G logical ranks, each with a batch and a shard table of its own --------
+    sharded = shard_run(args, wl, dev, stream, tdt) if (args.config == 3 and args.shard > 1 and ws == 1) else None
+
+    # -------- automatic table merging with mixed row shapes: the grouped lookup over the planner's tables --------
+    merged = merged_run(args, dev, stream) if (args.config == 3 and args.merged and ws == 1) else None
+
     # -------- tombstone compaction of the key store (one call, outside the step) --------
     comp = None
     if ws == 1:
@@ -880,6 +1023,8 @@ def run_ours(args):
                        f"({p_new:.0f} new keys per step)",
         "cold_step": cold_stats,
         "pooled": pooled,
+        "sharded": sharded,
+        "merged": merged,
         "compaction": comp,
         "stats": stats_leg,
         "grow": grow,
@@ -991,6 +1136,10 @@ def main():
     ap.add_argument("--e2e", type=int, default=1, help="also time the step through host buffers (its own table)")
     ap.add_argument("--pooled", type=int, default=1, help="also time the pooled jagged-bag step (jagged workload)")
     ap.add_argument("--grow", type=int, default=1, help="also time one capacity expansion at the end")
+    ap.add_argument("--merged", type=int, default=1,
+                    help="also time the grouped lookup over planner-merged tables of dims 16/32/64 (with config 3)")
+    ap.add_argument("--shard", type=int, default=2,
+                    help="also time the sharded two-stage dedup with this many logical ranks (jagged workload; 0: no)")
     ap.add_argument("--ranks", type=int, default=1,
                     help="1: the lookup also returns per-position ranks (the backward groups positions with them); "
                          "0: the backward groups positions itself")
