@@ -55,10 +55,9 @@ struct LookupParams {
   uint32_t* fresh_n;      // fresh rows listed so far, minus one (the word after ulist_n)
   uint32_t* rec_n;        // tile-local uniques listed so far, minus one (the word after fresh_n)
   ulonglong2* rec;        // [n] records {key, first position | count << 32}, each tile's together
-  int32_t* rec_slot;      // [n] scratch slot of each record's key
-  int32_t* rec_rb;        // [n] rank base of each record (positions of its key in records claimed before)
+  int2* rec_sr;           // [n] {scratch slot of the record's key, rank base (positions of the key in records
+                          // claimed before)}
   int32_t* tile_rec;      // [ntiles] where each tile's records start
-  uint16_t* lrank;        // [ntiles * kTile] rank of each position among its key's positions in the tile
   int32_t* fresh_row;     // [n] rows inserted by this lookup
   unsigned long long* fresh_key;  // [n] their keys
   int32_t* ulist;         // [n] scratch slot of each distinct key, in claim order
@@ -70,15 +69,16 @@ struct LookupParams {
   int32_t* prow;          // [ntiles * kTile] table row of each position (-1: none), for the gather
   int32_t* tile_pre;      // [ntiles + 1] first positions before each tile (its count, then the exclusive prefix)
   uint32_t* done;         // k_prefix blocks finished (zeroed by k_local)
-  uint16_t* lidx;         // [ntiles * kTile] tile-local unique of each position
+  uint32_t* llr;          // [ntiles * kTile] per position: tile-local unique (low half, 0xFFFF: invalid ID) |
+                          // rank among its key's positions in the tile (high half)
   int ntiles;
   int resolve_grid;
   size_t clear_bytes;     // bytes from sc on cleared to all ones per call (slots, counters, first-position bits)
 };
 
 struct LookupWsLayout {
-  size_t sc, ulist_n, ulist, rec, rec_slot, rec_rb, fresh_row, fresh_key, sc_row, tile_L, owner_nb, tile_pre, done,
-      wpre, prow, tile_rec, lrank, lidx, total;
+  size_t sc, ulist_n, ulist, rec, rec_sr, fresh_row, fresh_key, sc_row, tile_L, owner_nb, tile_pre, done,
+      wpre, prow, tile_rec, llr, total;
   size_t clear_bytes;  // bytes from the start of the workspace cleared to all ones per call
   unsigned long long ss;
   int ntiles;

@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kThreadsA, 4) k_local(const LookupParams p) {
 
   // ---- encode + stage 1 (tile-local dedup: first position, count, rank) ----
   bool bad = false;
+  uint32_t rk[kPPTA];    // each position's rank, stored with its local index at the end
   long long idv[kPPTA];  // every ID load in flight before the shared-memory work
 #pragma unroll
   for (int k = 0; k < kPPTA; ++k) {
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(kThreadsA, 4) k_local(const LookupParams p) {
     } else if (in) {
       s_pslot[lp] = kNoIdx;
     }
-    if (in) p.lrank[base + lp] = rank;  // the position's rank among its key's positions in the tile
+    rk[k] = rank;  // the position's rank among its key's positions in the tile
   }
   if (bad) latch_error(p.T.hdr, MT_EKEY);
   __syncthreads();
@@ -218,9 +219,13 @@ __global__ void __launch_bounds__(kThreadsA, 4) k_local(const LookupParams p) {
   }
   __syncthreads();
 
-  for (int lp = tid; lp < cnt; lp += kThreadsA) {
-    const uint16_t sl = s_pslot[lp];
-    p.lidx[base + lp] = sl == kNoIdx ? kNoIdx : (uint16_t)s_min[sl];
+#pragma unroll
+  for (int k = 0; k < kPPTA; ++k) {  // the positions this thread hashed: {local index, rank} in one word
+    const int lp = k * kThreadsA + tid;
+    if (lp < cnt) {
+      const uint16_t sl = s_pslot[lp];
+      p.llr[base + lp] = (sl == kNoIdx ? (uint32_t)kNoIdx : s_min[sl]) | (rk[k] << 16);
+    }
   }
 }
 
@@ -334,8 +339,8 @@ __global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
       if (r[k] >= R) continue;
       uint32_t old_first;
       const bool won = claim_from(p, key[k], gpos[k], lcount[k], h[k], sv[k], &old_first);
+      int32_t rb = 0;  // the key's first record: no positions before it
       if (won) {
-        if (p.ranks != nullptr) p.rec_rb[r[k]] = 0;  // the key's first record: no positions before it
         s_win[atomicAdd(&s_nwin, 1)] = (int32_t)h[k];
       } else {
         if (p.ranks != nullptr) {
@@ -344,14 +349,14 @@ __global__ void __launch_bounds__(kThreadsC) k_claim(const LookupParams p) {
           const unsigned long long old = atomicAdd(reinterpret_cast<unsigned long long*>(&p.sc[h[k]].first),
                                                    (unsigned long long)lcount[k] << 32);
           old_first = (uint32_t)(old & 0xFFFFFFFFull);
-          p.rec_rb[r[k]] = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before
+          rb = (int32_t)((uint32_t)(old >> 32) + 1u);  // positions of the key added before
         } else {
           atomicAdd(&p.sc[h[k]].cnt, lcount[k]);  // no ranks asked for: the count alone, no value returned
         }
         // lower the key's first position only when this record can (the first position only decreases)
         if (gpos[k] < old_first) atomicMin(&p.sc[h[k]].first, gpos[k]);
       }
-      p.rec_slot[r[k]] = (int32_t)h[k];
+      p.rec_sr[r[k]] = make_int2((int32_t)h[k], rb);  // one 8-byte store: the record's slot and rank base
     }
     if (list_each_round) list_winners(p, s_win, &s_nwin, &s_wbase);
   }
@@ -553,8 +558,9 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int l = k * kThreads + tid;
-    sl[k] = l < L ? __ldcg(&p.rec_slot[r0 + l]) : -1;
-    if (l < L && p.ranks != nullptr) s_rb[l] = __ldcg(&p.rec_rb[r0 + l]);
+    const int2 sr = l < L ? __ldcg(&p.rec_sr[r0 + l]) : make_int2(-1, 0);
+    sl[k] = sr.x;
+    if (l < L) s_rb[l] = sr.y;
   }
   const bool gather = p.out_rows != nullptr;
 #pragma unroll
@@ -567,11 +573,13 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
     }
   }
   __syncthreads();
-  uint16_t li[kPPT];
+  uint16_t li[kPPT], lr[kPPT];
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
     const int lp = k * kThreads + tid;
-    li[k] = lp < cnt ? __ldg(&p.lidx[base + lp]) : kNoIdx;
+    const uint32_t w = lp < cnt ? __ldg(&p.llr[base + lp]) : (uint32_t)kNoIdx;
+    li[k] = (uint16_t)(w & 0xFFFFu);
+    lr[k] = (uint16_t)(w >> 16);
   }
 #pragma unroll
   for (int k = 0; k < kPPT; ++k) {
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 5) k_expand(const LookupParams p) {
 #pragma unroll
     for (int k = 0; k < kPPT; ++k) {
       const int lp = k * kThreads + tid;
-      if (lp < cnt) p.ranks[base + lp] = li[k] == kNoIdx ? -1 : s_rb[li[k]] + (int32_t)__ldg(&p.lrank[base + lp]);
+      if (lp < cnt) p.ranks[base + lp] = li[k] == kNoIdx ? -1 : s_rb[li[k]] + (int32_t)lr[k];
     }
   }
   // this block's share of the fresh rows: init(key), m = v = 0, one team of lanes per row (8 columns
@@ -672,8 +680,7 @@ LookupWsLayout lookup_ws_layout(long long n) {
   take(cap / 8);
   L.ulist = take((size_t)(n > 0 ? n : 1) * 4);
   L.rec = take((size_t)(n > 0 ? n : 1) * 16);
-  L.rec_slot = take((size_t)(n > 0 ? n : 1) * 4);
-  L.rec_rb = take((size_t)(n > 0 ? n : 1) * 4);
+  L.rec_sr = take((size_t)(n > 0 ? n : 1) * 8);
   L.fresh_row = take((size_t)(n > 0 ? n : 1) * 4);
   L.fresh_key = take((size_t)(n > 0 ? n : 1) * 8);
   L.sc_row = take(L.ss * 4);
@@ -683,8 +690,7 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.wpre = take(cap / 64 * 2);
   L.prow = take(cap * 4);
   L.tile_rec = take((size_t)L.ntiles * 4);
-  L.lrank = take(cap * 2);
-  L.lidx = take(cap * 2);
+  L.llr = take(cap * 4);
   L.total = off;
   return L;
 }
@@ -696,10 +702,8 @@ void bind_lookup_ws(LookupParams& p, char* w, const LookupWsLayout& L) {
   p.fresh_n = p.ulist_n + 1;
   p.rec_n = p.ulist_n + 2;
   p.rec = reinterpret_cast<ulonglong2*>(w + L.rec);
-  p.rec_slot = reinterpret_cast<int32_t*>(w + L.rec_slot);
-  p.rec_rb = reinterpret_cast<int32_t*>(w + L.rec_rb);
+  p.rec_sr = reinterpret_cast<int2*>(w + L.rec_sr);
   p.tile_rec = reinterpret_cast<int32_t*>(w + L.tile_rec);
-  p.lrank = reinterpret_cast<uint16_t*>(w + L.lrank);
   p.fresh_row = reinterpret_cast<int32_t*>(w + L.fresh_row);
   p.fresh_key = reinterpret_cast<unsigned long long*>(w + L.fresh_key);
   p.ulist = reinterpret_cast<int32_t*>(w + L.ulist);
@@ -710,7 +714,7 @@ void bind_lookup_ws(LookupParams& p, char* w, const LookupWsLayout& L) {
   p.prow = reinterpret_cast<int32_t*>(w + L.prow);
   p.tile_pre = reinterpret_cast<int32_t*>(w + L.tile_pre);
   p.done = reinterpret_cast<uint32_t*>(w + L.done);
-  p.lidx = reinterpret_cast<uint16_t*>(w + L.lidx);
+  p.llr = reinterpret_cast<uint32_t*>(w + L.llr);
   p.ntiles = L.ntiles;
   p.clear_bytes = L.clear_bytes;
 }
