@@ -61,7 +61,7 @@ struct LookupParams {
   int32_t* fresh_row;     // [n] rows inserted by this lookup
   unsigned long long* fresh_key;  // [n] their keys
   int32_t* ulist;         // [n] scratch slot of each distinct key, in claim order
-  int32_t* sc_row;        // [ss] table row of the key in a slot (-1: none)
+  int32_t* urow;          // [n] table row of each distinct key (-1: none), beside ulist
   int32_t* tile_L;        // [ntiles] tile-local uniques per tile
   unsigned long long* owner_nb;  // [ntiles * kTile / 64] bit i clear: position i is its key's first (cleared
                                  // to all ones)
@@ -77,7 +77,7 @@ struct LookupParams {
 };
 
 struct LookupWsLayout {
-  size_t sc, ulist_n, ulist, rec, rec_sr, fresh_row, fresh_key, sc_row, tile_L, owner_nb, tile_pre, done,
+  size_t sc, ulist_n, ulist, rec, rec_sr, fresh_row, fresh_key, urow, tile_L, owner_nb, tile_pre, done,
       wpre, prow, tile_rec, llr, total;
   size_t clear_bytes;  // bytes from the start of the workspace cleared to all ones per call
   unsigned long long ss;

@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kThreadsR) k_resolve(const LookupParams p) {
       }
     }
     if (act) {
-      p.sc_row[slot] = row;
+      p.urow[idx] = row;  // beside the key's entry of the list: k_number reads both in order
       atomicAnd(&p.owner_nb[gfirst >> 6], ~(1ull << (gfirst & 63)));  // the key's first position
     }
     // the block's fresh rows join the list k_expand initialises (one global atomic per block)
@@ -515,13 +515,11 @@ __global__ void __launch_bounds__(kThreadsR) k_number(const LookupParams p) {
     for (int k = 0; k < ILP; ++k) {
       const uint32_t idx = i0 + k * kThreadsR;
       slot[k] = idx < U ? __ldcg(&p.ulist[idx]) : -1;
+      row[k] = idx < U ? __ldcg(&p.urow[idx]) : -1;
     }
 #pragma unroll
     for (int k = 0; k < ILP; ++k)
-      if (slot[k] >= 0) {
-        sv[k] = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[slot[k]]));
-        row[k] = __ldcg(&p.sc_row[slot[k]]);
-      }
+      if (slot[k] >= 0) sv[k] = __ldcg(reinterpret_cast<const ulonglong2*>(&p.sc[slot[k]]));
     int u[ILP];
 #pragma unroll
     for (int k = 0; k < ILP; ++k)
@@ -683,7 +681,7 @@ LookupWsLayout lookup_ws_layout(long long n) {
   L.rec_sr = take((size_t)(n > 0 ? n : 1) * 8);
   L.fresh_row = take((size_t)(n > 0 ? n : 1) * 4);
   L.fresh_key = take((size_t)(n > 0 ? n : 1) * 8);
-  L.sc_row = take(L.ss * 4);
+  L.urow = take((size_t)(n > 0 ? n : 1) * 4);
   L.tile_L = take((size_t)L.ntiles * 4);
   L.tile_pre = take((size_t)(L.ntiles + 1) * 4);
   L.done = take(16);
@@ -707,7 +705,7 @@ void bind_lookup_ws(LookupParams& p, char* w, const LookupWsLayout& L) {
   p.fresh_row = reinterpret_cast<int32_t*>(w + L.fresh_row);
   p.fresh_key = reinterpret_cast<unsigned long long*>(w + L.fresh_key);
   p.ulist = reinterpret_cast<int32_t*>(w + L.ulist);
-  p.sc_row = reinterpret_cast<int32_t*>(w + L.sc_row);
+  p.urow = reinterpret_cast<int32_t*>(w + L.urow);
   p.tile_L = reinterpret_cast<int32_t*>(w + L.tile_L);
   p.owner_nb = reinterpret_cast<unsigned long long*>(w + L.owner_nb);
   p.wpre = reinterpret_cast<uint16_t*>(w + L.wpre);
