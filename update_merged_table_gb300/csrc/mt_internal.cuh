@@ -210,35 +210,81 @@ __device__ __forceinline__ void push_row_warp(const TableDev& T, unsigned mask, 
   T.free_stack[old + rank] = row;
 }
 
+// One probe of find_slot: 1 = the key is in slot s (sv holds it), -1 = an
+// EMPTY slot ends the chain, 0 = go on (a tombstone is noted at probe t).
+__device__ __forceinline__ int probe_one(unsigned long long key, const ulonglong2& sv, uint32_t t, long long* first_tomb) {
+  if (sv.x == key) return 1;
+  if (sv.x == kEmpty) return -1;
+  if (sv.x == kTomb && *first_tomb < 0) *first_tomb = t;
+  return 0;
+}
+
 // Find `key` along its probe sequence h_t = (h0 + t*S) mod M (MTGenRec,
 // Theorem 1).  Returns the slot index, or -1 when an EMPTY slot or the probe
 // limit ends the chain first.  *t_end receives the probe index where the
 // search stopped, *t_tomb the first tombstone's probe index (or -1) and
-// *row the row of a found key.  Each probe is one 16-byte load from L2.
-__device__ __forceinline__ long long find_slot(const TableDev& T, unsigned long long key, long long* t_end,
-                                               long long* t_tomb, int32_t* row) {
-  unsigned long long s = home_slot(T, key);
+// *row the row of a found key.  Each probe is one 16-byte load from L2;
+// with S = 1, the probes after the first come four adjacent slots at a time.
+// find_slot_from starts with the home slot s and its contents sv already
+// loaded.
+__device__ __forceinline__ long long find_slot_from(const TableDev& T, unsigned long long key, unsigned long long s,
+                                                    ulonglong2 sv, long long* t_end, long long* t_tomb,
+                                                    int32_t* row) {
   long long first_tomb = -1;
-  for (uint32_t t = 0; t < T.max_probes; ++t) {
-    const ulonglong2 sv = __ldcg(reinterpret_cast<const ulonglong2*>(&T.slots[s]));
-    const unsigned long long k = sv.x;
-    if (k == key) {
-      *t_end = t;
+  uint32_t t = 0;
+  if (T.max_probes > 0) {
+    const int r = probe_one(key, sv, 0, &first_tomb);
+    if (r != 0) {
+      *t_end = 0;
       *t_tomb = first_tomb;
-      *row = (int32_t)(uint32_t)(sv.y & 0xFFFFFFFFull);
-      return (long long)s;
+      if (r > 0) *row = (int32_t)(uint32_t)(sv.y & 0xFFFFFFFFull);
+      return r > 0 ? (long long)s : -1;
     }
-    if (k == kEmpty) {
-      *t_end = t;
-      *t_tomb = first_tomb;
-      return -1;
-    }
-    if (k == kTomb && first_tomb < 0) first_tomb = t;
+    t = 1;
     s = (s + T.S) & T.mask;
+  }
+  if (T.S == 1 && T.mask >= 3) {
+    // linear probing: the rest of the chain in aligned groups of four adjacent slots (64 bytes of one line),
+    // each group's slots loaded together and checked in probe order
+    while (t < T.max_probes) {
+      const unsigned long long g0 = s & ~3ull;
+      const ulonglong2* gp = reinterpret_cast<const ulonglong2*>(&T.slots[g0]);
+      const ulonglong2 q0 = __ldcg(gp), q1 = __ldcg(gp + 1), q2 = __ldcg(gp + 2), q3 = __ldcg(gp + 3);
+      for (unsigned long long j = s - g0; j < 4 && t < T.max_probes; ++j, ++t) {
+        const ulonglong2 q = j == 0 ? q0 : (j == 1 ? q1 : (j == 2 ? q2 : q3));
+        const int r = probe_one(key, q, t, &first_tomb);
+        if (r != 0) {
+          *t_end = t;
+          *t_tomb = first_tomb;
+          if (r > 0) *row = (int32_t)(uint32_t)(q.y & 0xFFFFFFFFull);
+          return r > 0 ? (long long)(g0 + j) : -1;
+        }
+      }
+      s = (g0 + 4) & T.mask;
+    }
+  } else {
+    for (; t < T.max_probes; ++t) {
+      sv = __ldcg(reinterpret_cast<const ulonglong2*>(&T.slots[s]));
+      const int r = probe_one(key, sv, t, &first_tomb);
+      if (r != 0) {
+        *t_end = t;
+        *t_tomb = first_tomb;
+        if (r > 0) *row = (int32_t)(uint32_t)(sv.y & 0xFFFFFFFFull);
+        return r > 0 ? (long long)s : -1;
+      }
+      s = (s + T.S) & T.mask;
+    }
   }
   *t_end = T.max_probes;
   *t_tomb = first_tomb;
   return -1;
+}
+
+// Find `key` from its home slot (loading it first).
+__device__ __forceinline__ long long find_slot(const TableDev& T, unsigned long long key, long long* t_end,
+                                               long long* t_tomb, int32_t* row) {
+  const unsigned long long s = home_slot(T, key);
+  return find_slot_from(T, key, s, __ldcg(reinterpret_cast<const ulonglong2*>(&T.slots[s])), t_end, t_tomb, row);
 }
 
 // ---- host-side launchers (defined in the kernel files) --------------------
