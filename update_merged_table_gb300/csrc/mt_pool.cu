@@ -180,23 +180,27 @@ __global__ void __launch_bounds__(256, 4) k_pool(const PoolParams p) {
 // its fp64 accumulator, an empty bag zeros.  Offsets that decrease or leave
 // [0, n] latch MT_EINVAL (the bag is then written as zeros).
 __global__ void __launch_bounds__(256) k_pool_finish(const PoolParams p) {
-  const int d = (int)p.T.dim;
-  const long long total = p.num_bags * d;
+  const int d4 = (int)p.T.dim / 4;  // four columns per item (d is a multiple of 4)
+  const long long total = p.num_bags * d4;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
-    const long long b = it / d;
-    const int j = (int)(it - b * d);
+    const long long b = it / d4;
+    const int j4 = (int)(it - b * d4);
     const long long s = __ldg(&p.bag_offsets[b]), e = __ldg(&p.bag_offsets[b + 1]);
     const bool bad = s < 0 || e < s || e > p.n;
-    if (bad && j == 0) latch_error(p.T.hdr, MT_EINVAL);
+    if (bad && j4 == 0) latch_error(p.T.hdr, MT_EINVAL);
     const bool one_chunk = !bad && e > s && s / kPoolChunk == (e - 1) / kPoolChunk;
     if (one_chunk) continue;  // written by k_pool
-    float o = 0.0f;
+    float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (!bad && e > s) {
-      const double a = __ldcg(&p.acc[(size_t)b * d + j]);
-      o = (float)(p.mode == MT_POOL_MEAN ? a / (double)(e - s) : a);
+      const double2* a = reinterpret_cast<const double2*>(p.acc + (size_t)b * p.T.dim) + 2 * j4;
+      const double2 a0 = __ldcg(a), a1 = __ldcg(a + 1);
+      const bool mean = p.mode == MT_POOL_MEAN;
+      const double len = (double)(e - s);
+      o = make_float4((float)(mean ? a0.x / len : a0.x), (float)(mean ? a0.y / len : a0.y),
+                      (float)(mean ? a1.x / len : a1.x), (float)(mean ? a1.y / len : a1.y));
     }
-    p.out[(size_t)b * d + j] = o;
+    reinterpret_cast<float4*>(p.out + (size_t)b * p.T.dim)[j4] = o;
   }
 }
 
@@ -221,13 +225,16 @@ __global__ void __launch_bounds__(256) k_pos_bag(const long long* bo, long long 
 // gradient every position of a mean-pooled bag receives).
 __global__ void __launch_bounds__(256) k_pool_scale(const long long* bo, long long B, int d, const float* dpooled,
                                                     float* dscaled) {
-  const long long total = B * d;
+  const int d4 = d / 4;  // four columns per item (d is a multiple of 4)
+  const long long total = B * d4;
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < total;
        it += (long long)gridDim.x * blockDim.x) {
-    const long long b = it / d;
+    const long long b = it / d4;
     const long long len = __ldg(&bo[b + 1]) - __ldg(&bo[b]);
     const float s = len > 0 ? __frcp_rn((float)len) : 1.0f;
-    dscaled[it] = __fmul_rn(__ldg(&dpooled[it]), s);
+    const float4 g = __ldg(reinterpret_cast<const float4*>(dpooled) + it);
+    reinterpret_cast<float4*>(dscaled)[it] =
+        make_float4(__fmul_rn(g.x, s), __fmul_rn(g.y, s), __fmul_rn(g.z, s), __fmul_rn(g.w, s));
   }
 }
 
@@ -247,7 +254,7 @@ cudaError_t launch_pool(const PoolParams& p, cudaStream_t s) {
   }
   {
     MT_LAUNCH("k_pool_finish", s);
-    k_pool_finish<<<grid_for(p.num_bags * p.T.dim, 256, 16), 256, 0, s>>>(p);
+    k_pool_finish<<<grid_for(p.num_bags * p.T.dim / 4, 256, 16), 256, 0, s>>>(p);
   }
   return cudaGetLastError();
 }
@@ -265,7 +272,7 @@ cudaError_t launch_pool_scale(const long long* bo, long long B, int d, const flo
                               cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   MT_LAUNCH("k_pool_scale", s);
-  k_pool_scale<<<grid_for(B * d, 256, 16), 256, 0, s>>>(bo, B, d, dpooled, dscaled);
+  k_pool_scale<<<grid_for(B * d / 4, 256, 16), 256, 0, s>>>(bo, B, d, dpooled, dscaled);
   return cudaGetLastError();
 }
 
