@@ -209,17 +209,7 @@ int run_backward(mt_table* t, const mt_lookup_result* res, int64_t n, const void
   p.one_minus_b1 = (float)(1.0 - (double)hp->beta1);
   p.one_minus_b2 = (float)(1.0 - (double)hp->beta2);
   p.gsum_out = gsum_out;
-  p.bsum = reinterpret_cast<int32_t*>(w + L.bsum);
-  p.boff = reinterpret_cast<int32_t*>(w + L.boff);
-  p.seg = reinterpret_cast<int2*>(w + L.seg);
-  p.chunks = reinterpret_cast<int4*>(w + L.chunks);
-  p.heavy_info = reinterpret_cast<int4*>(w + L.heavy_info);
-  p.pos_sorted = reinterpret_cast<int32_t*>(w + L.pos_sorted);
-  p.acc64 = reinterpret_cast<double*>(w + L.acc64);
-  p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
-  p.work = reinterpret_cast<int32_t*>(w + L.work);
-  p.nblk = L.nblk;
-  p.ntiles = L.ntiles;
+  mt::bind_backward_ws(p, w, L);
   p.team_shift = mt::backward_team_shift(t->cfg.dim, (int)t->cfg.row_dtype);
   p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
   const int rc = cuda_status(mt::launch_backward(p, stream));

@@ -9,15 +9,15 @@
 // bias correction.
 //
 // Kernels, in launch order:
-//  k_bw_blocksum     per block of uniques: sums of positions, of heavy
-//                    warp-chunks and of heavy uniques (more than kChunk
-//                    positions); one extra block advances the table's step
-//                    counter and beta powers and computes the Adam scalars.
-//  k_bw_offsets      per unique: {segment start, count}; per light unique one chunk
-//                    descriptor, per heavy unique its warp-chunk descriptors
-//                    and zeroed fp64 accumulators (each block sums the block
-//                    totals before it itself).
-//  k_bw_scatter      positions grouped by unique: segment start + the rank
+//  k_bw_plan         per block of uniques (after a memset of four counters):
+//                    each unique's segment {start, count}, a chunk descriptor
+//                    per light unique, a record per heavy unique (more than
+//                    kChunk positions); each block reserves its ranges with
+//                    one atomic per counter.  One extra block advances the
+//                    table's step counter and beta powers and computes the
+//                    Adam scalars.
+//  k_bw_scatter      heavy uniques' warp-chunk descriptors and zeroed fp64
+//                    accumulators; positions grouped by unique: segment start + the rank
 //                    the lookup recorded (k_bw_fill re-groups them with a
 //                    shared-memory hash when the lookup kept no ranks).
 //  k_bw_heavy_reduce heavy uniques: a warp per warp-chunk, 16 gradient rows
@@ -71,36 +71,23 @@ __device__ __forceinline__ void block_scan3(const int v[3], int ex[3], int tot[3
   __syncthreads();
 }
 
-// Block totals of three ints per thread (every thread receives them).  Contains __syncthreads.
-template <int NT>
-__device__ __forceinline__ void block_total3(const int v[3], int tot[3], int (*s_warp)[NT / 32]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int c = 0; c < 3; ++c) {
-    const int w = __reduce_add_sync(kFull, v[c]);
-    if (lane == 0) s_warp[c][warp] = w;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int c = 0; c < 3; ++c) {
-    int t = 0;
-#pragma unroll
-    for (int q = 0; q < NT / 32; ++q) t += s_warp[c][q];
-    tot[c] = t;
-  }
-  __syncthreads();
-}
-
 // A unique with more than kChunk positions is "heavy": it is reduced in
 // warp-chunks of p.warp_chunk positions, each by one whole warp.
 __device__ __forceinline__ int warp_chunks(int c, int wc) { return c > kChunk ? (c + wc - 1) / wc : 0; }
 
-// Sums over a block of uniques: positions, chunks of heavy (multi-chunk)
-// uniques, heavy uniques.  The block after the last one advances the
-// table's step counter and beta-power accumulators and computes the step's
-// Adam scalars.
-__global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardParams p) {
+// The grouping plan, one block per kScanTile uniques: each unique gets a
+// segment of pos_sorted (its count of positions), and either one team-chunk
+// descriptor (light) or a heavy record whose warp-chunks k_bw_scatter writes.
+// Segments only need to be disjoint, so each block reserves its ranges with
+// one atomic per counter (positions, heavy warp-chunks, heavy uniques) and
+// places its uniques by a block scan: no pass over the other blocks' sums.
+// Light unique u's descriptor is chunks[light0 + u].  The block after the last one advances the table's step
+// counter and beta-power accumulators and computes the step's Adam scalars.
+constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_plan
+
+__global__ void __launch_bounds__(kScanThreads) k_bw_plan(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
+  __shared__ int s_base[4];
   if (blockIdx.x == p.nblk) {  // the extra block: step counter and this step's Adam scalars
     if (threadIdx.x == 0 && p.reduce_only) p.work[0] = 0;
     if (threadIdx.x == 0 && !p.reduce_only) {
@@ -119,71 +106,15 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_blocksum(const BackwardPara
     return;
   }
   const long long U = *p.num_unique;
-  const long long u0 = (long long)blockIdx.x * kScanTile + threadIdx.x;
-  int c[kScanTile / kScanThreads];  // every load in flight before the sums
-#pragma unroll
-  for (int k = 0; k < kScanTile / kScanThreads; ++k) {
-    const long long u = u0 + (long long)k * kScanThreads;
-    c[k] = u < U ? __ldg(&p.counts[u]) : 0;
-  }
-  int v[3] = {0, 0, 0};
-#pragma unroll
-  for (int k = 0; k < kScanTile / kScanThreads; ++k) {
-    v[0] += c[k];
-    v[1] += warp_chunks(c[k], p.warp_chunk);
-    v[2] += c[k] > kChunk;
-  }
-  int tot[3];
-  block_total3<kScanThreads>(v, tot, s_warp);
-  if (threadIdx.x < 3) p.bsum[(size_t)blockIdx.x * 3 + threadIdx.x] = tot[threadIdx.x];
-}
-
-constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_offsets
-
-// Per unique: {segment start, count}.  A light unique gets its team-chunk
-// descriptor {start, end, row, u} at HWC + its rank among light uniques (HWC
-// = warp-chunks of all heavy uniques, which come first); a heavy unique gets
-// {u, warp-chunks, segment start, first chunk}, its warp-chunk descriptors,
-// zeroed fp64 accumulators and arrival count.  Each block adds up the sums
-// of the blocks before it itself (they are few), so no scan launch is needed.
-__global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParams p) {
-  __shared__ int s_warp[3][kScanThreads / 32];
-  __shared__ int s_base[3];
-  __shared__ int s_tot[3];
-  const long long U = *p.num_unique;
-  const int b = blockIdx.x;
-  const long long u0 = (long long)b * kScanTile + (long long)threadIdx.x * kUPT;
-  int c[kUPT], rows[kUPT];  // the block's own uniques: loaded together with the block sums below
+  const long long ub = (long long)blockIdx.x * kScanTile;
+  if (ub >= U) return;  // the grid is sized for every ID distinct
+  const long long u0 = ub + (long long)threadIdx.x * kUPT;
+  int c[kUPT], rows[kUPT];
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
     c[k] = u0 + k < U ? __ldg(&p.counts[u0 + k]) : 0;
     rows[k] = u0 + k < U ? __ldg(&p.unique_rows[u0 + k]) : -1;
   }
-  {  // block offsets: sums over blocks < b; totals over all blocks
-    int pre[3] = {0, 0, 0}, all[3] = {0, 0, 0};
-    for (int q = threadIdx.x; q < p.nblk; q += kScanThreads) {
-#pragma unroll
-      for (int cc = 0; cc < 3; ++cc) {
-        const int x = __ldg(&p.bsum[(size_t)q * 3 + cc]);
-        all[cc] += x;
-        if (q < b) pre[cc] += x;
-      }
-    }
-    int tot[3];
-    block_total3<kScanThreads>(pre, tot, s_warp);
-    if (threadIdx.x == 0) {
-      for (int cc = 0; cc < 3; ++cc) s_base[cc] = tot[cc];
-    }
-    block_total3<kScanThreads>(all, tot, s_warp);
-    if (threadIdx.x == 0) {
-      for (int cc = 0; cc < 3; ++cc) s_tot[cc] = tot[cc];
-      if (b == 0) {  // totals for the reduce kernels
-        for (int cc = 0; cc < 3; ++cc) p.boff[(size_t)p.nblk * 3 + cc] = tot[cc];
-      }
-    }
-    __syncthreads();
-  }
-  if ((long long)b * kScanTile >= U) return;  // uniform over the block
   int v[3] = {0, 0, 0};
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
@@ -193,19 +124,24 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   }
   int ex[3], tot[3];
   block_scan3<kScanThreads>(v, ex, tot, s_warp);
+  if (threadIdx.x == 0) {
+    s_base[0] = atomicAdd(&p.ctr[0], tot[0]);
+    s_base[1] = atomicAdd(&p.ctr[1], tot[1]);
+    s_base[2] = atomicAdd(&p.ctr[2], tot[2]);
+  }
+  __syncthreads();
   int seg = ex[0] + s_base[0];
   int hch = ex[1] + s_base[1];
   int hv = ex[2] + s_base[2];
-  const int HWC = s_tot[1];
 #pragma unroll
   for (int k = 0; k < kUPT; ++k) {
     const long long u = u0 + k;
     if (u >= U) break;
     p.seg[u] = make_int2(seg, c[k]);
-    const int row = rows[k];
-    if (c[k] <= kChunk) {
-      p.chunks[HWC + (int)(u - hv)] = make_int4(seg, seg + c[k], row, (int)u);
-    } else {
+    // the team-chunks stay in unique order (the light reduce runs measurably faster so); a heavy unique
+    // leaves an empty one there
+    p.chunks[p.light0 + u] = c[k] <= kChunk ? make_int4(seg, seg + c[k], rows[k], (int)u) : make_int4(0, 0, -1, -1);
+    if (c[k] > kChunk) {
       const int nw = warp_chunks(c[k], p.warp_chunk);
       p.heavy_info[hv] = make_int4((int)u, nw, seg, hch);  // its warp-chunks are written by the grouping kernel
       ++hv;
@@ -215,13 +151,14 @@ __global__ void __launch_bounds__(kScanThreads) k_bw_offsets(const BackwardParam
   }
 }
 
+
 // Warp-chunk descriptors of the heavy uniques, a warp per heavy unique over
 // the whole grid (the hottest IDs are seen first, so their uniques cluster
 // in the first offsets block); a unique with several warp-chunks also gets
 // its fp64 accumulator and arrival count cleared.  Called by every thread of
 // the grouping kernels before they group.
 __device__ __forceinline__ void write_heavy_chunks(const BackwardParams& p) {
-  const int H = p.boff[(size_t)p.nblk * 3 + 2];
+  const int H = __ldcg(&p.ctr[2]);
   const int d = (int)p.T.dim;
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -591,7 +528,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
   extern __shared__ __align__(16) uint4 dsmem[];  // [kHeavyStages][HS][Q][256] ring, then positions
   uint4* ring = dsmem + threadIdx.x;
   int* s_pos = reinterpret_cast<int*>(dsmem + (HS > 0 ? kHeavyStages * HS * Q * 256 : 0));
-  const float step_size = __int_as_float(__ldg(&p.work[2]));  // set by k_bw_blocksum
+  const float step_size = __int_as_float(__ldg(&p.work[2]));  // set by k_bw_plan
   const float inv_sqrt_bc2 = __int_as_float(__ldg(&p.work[3]));
 
   const int team_shift = p.team_shift;
@@ -604,7 +541,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
   int* my_pos = s_pos + (threadIdx.x >> team_shift) * kTeamShare;
   const int d = (int)p.T.dim;
   const int col0 = lt * VEC;
-  const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
+  const int HWC = __ldcg(&p.ctr[1]);
 
   // ---- heavy warp-chunks, handed to warps one at a time (they differ in size) ----
   for (;;) {
@@ -693,7 +630,7 @@ __global__ void __launch_bounds__(256, (RD == MT_F32 && GD == MT_F32) ? 4 : 3) k
   constexpr int VEC = RD == MT_F32 ? 4 : 8;
   constexpr int UNR = 16 / GradRaw<GD, VEC>::W;  // gradient rows in flight per lane (16 raw words)
   __shared__ int s_pos[kMaxTeams * kChunk];
-  const float step_size = __int_as_float(__ldg(&p.work[2]));  // set by k_bw_blocksum
+  const float step_size = __int_as_float(__ldg(&p.work[2]));  // set by k_bw_plan
   const float inv_sqrt_bc2 = __int_as_float(__ldg(&p.work[3]));
 
   const int team_shift = p.team_shift;
@@ -704,9 +641,7 @@ __global__ void __launch_bounds__(256, (RD == MT_F32 && GD == MT_F32) ? 4 : 3) k
   int* my_pos = s_pos + (threadIdx.x >> team_shift) * kChunk;
   const int d = (int)p.T.dim;
   const int col0 = lt * VEC;
-  const long long U = *p.num_unique;
-  const int HWC = p.boff[(size_t)p.nblk * 3 + 1];
-  const long long light_end = (long long)HWC + (U - p.boff[(size_t)p.nblk * 3 + 2]);
+  const long long light_end = (long long)p.light0 + *p.num_unique;  // heavy uniques' entries are empty
 
   const long long gteam = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> team_shift;
   const long long nteam = ((long long)gridDim.x * blockDim.x) >> team_shift;
@@ -716,7 +651,7 @@ __global__ void __launch_bounds__(256, (RD == MT_F32 && GD == MT_F32) ? 4 : 3) k
   // the positions of the next one are in flight into registers and its Adam
   // row and gradient rows are being pulled into L2.
   constexpr int kPosRegs = kChunk >> kMinTeamShift;  // positions per lane of one team-chunk
-  long long c = HWC + gteam;
+  long long c = p.light0 + gteam;
   int4 dsc = c < light_end ? __ldg(&p.chunks[c]) : make_int4(0, 0, -1, 0);
   if (c < light_end) {
     for (int q = lt; q < dsc.y - dsc.x; q += team) my_pos[q] = valid_pos(p, __ldg(&p.pos_sorted[dsc.x + q]));
@@ -759,7 +694,7 @@ __global__ void __launch_bounds__(256, (RD == MT_F32 && GD == MT_F32) ? 4 : 3) k
       f32x2 gs[VEC / 2];
 #pragma unroll
       for (int j = 0; j < VEC / 2; ++j) gs[j] = add2(hi[j], lo[j]);
-      if (p.gsum_out != nullptr) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
+      if (p.gsum_out != nullptr && dsc.w >= 0) store_gsum(p.gsum_out, dsc.w, d, col, gs, VEC);
       if (row >= 0 && !p.reduce_only) adam_cols<RD, VEC>(p, row, col, gs, step_size, inv_sqrt_bc2);
     }
     __syncwarp(team_mask);  // every lane is done with my_pos
@@ -834,10 +769,12 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
     return o;
   };
   const size_t nn = (size_t)(n > 0 ? n : 1);
-  L.bsum = take((size_t)L.nblk * 3 * 4);
-  L.boff = take(((size_t)L.nblk + 1) * 3 * 4);
+  // a heavy unique has more than kChunk positions and at most count / 64 + 1 warp-chunks (a warp-chunk holds
+  // at least 64 positions), so n / 21 + 2 bounds the heavy warp-chunks
+  L.light0 = (int)(n / 21 + 2);
+  L.ctr = take(16);
   L.seg = take(nn * 8);
-  L.chunks = take(nn * 16);
+  L.chunks = take(((size_t)L.light0 + nn) * 16);
   L.heavy_info = take((size_t)L.heavy_cap * 16);
   L.pos_sorted = take(nn * 4);
   L.acc64 = take((size_t)L.heavy_cap * dim * 8);
@@ -847,14 +784,26 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
   return L;
 }
 
+void bind_backward_ws(BackwardParams& p, char* w, const BackwardWsLayout& L) {
+  p.ctr = reinterpret_cast<int32_t*>(w + L.ctr);
+  p.seg = reinterpret_cast<int2*>(w + L.seg);
+  p.chunks = reinterpret_cast<int4*>(w + L.chunks);
+  p.heavy_info = reinterpret_cast<int4*>(w + L.heavy_info);
+  p.pos_sorted = reinterpret_cast<int32_t*>(w + L.pos_sorted);
+  p.acc64 = reinterpret_cast<double*>(w + L.acc64);
+  p.arrive = reinterpret_cast<int32_t*>(w + L.arrive);
+  p.work = reinterpret_cast<int32_t*>(w + L.work);
+  p.nblk = L.nblk;
+  p.light0 = L.light0;
+  p.ntiles = L.ntiles;
+}
+
 cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(p.ctr, 0, 4 * sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
   {
-    MT_LAUNCH("k_bw_blocksum", s);
-    k_bw_blocksum<<<p.nblk + 1, kScanThreads, 0, s>>>(p);  // + the block that sets up the step
-  }
-  {
-    MT_LAUNCH("k_bw_offsets", s);
-    k_bw_offsets<<<p.nblk, kScanThreads, 0, s>>>(p);
+    MT_LAUNCH("k_bw_plan", s);
+    k_bw_plan<<<p.nblk + 1, kScanThreads, 0, s>>>(p);  // + the block that sets up the step
   }
   if (p.ntiles > 0 && p.ranks != nullptr) {
     MT_LAUNCH("k_bw_scatter", s);

@@ -112,28 +112,32 @@ struct BackwardParams {
   float* gsum_out;
   int reduce_only;      // 1: gradient sums only; no Adam step and no step counter change
   // workspace
-  int32_t* bsum;        // [nblk * 3] per scan block: sums of counts, heavy chunks, heavy uniques
-  int32_t* boff;        // [(nblk + 1) * 3] exclusive offsets (+ totals)
+  int32_t* ctr;         // [4] positions, heavy warp-chunks and heavy uniques placed so far (zeroed per call;
+                        //     their totals once k_bw_plan is done)
   int2* seg;            // [n] {segment start, count} of each unique; the fill advances the start to the end
-  int4* chunks;         // [n] descriptors {start, end, row, u or -(heavy index + 1)}: the warp-chunks of
-                        //     heavy uniques (more than kChunk positions) first, then one team-chunk per light unique
+  int4* chunks;         // [light0 + n] descriptors {start, end, row, u or -(heavy index + 1)}: the warp-chunks of
+                        //     heavy uniques (more than kChunk positions) from 0; unique u's team-chunk at
+                        //     light0 + u (empty, {0, 0, -1, -1}, for a heavy unique)
   int4* heavy_info;     // [heavy_cap] {u, warp-chunks, segment start, first chunk} of each heavy unique
   int32_t* pos_sorted;  // [n] positions grouped by unique
   double* acc64;        // [heavy_cap * d] cross-chunk sums of heavy uniques
   int32_t* arrive;      // [heavy_cap] chunks finished per heavy unique
   int32_t* work;        // [4] heavy warp-chunks handed out (zeroed per call), -, step_size and inv_sqrt_bc2 (fp32 bits)
   int nblk;
+  int light0;           // where the light uniques' team-chunks start in chunks (bounds the heavy warp-chunks)
   int ntiles;
   int team_shift;       // log2 lanes per team (one team covers VEC columns per lane)
   int warp_chunk;       // positions per heavy warp-chunk: kTeamShare x teams per warp
 };
 
 struct BackwardWsLayout {
-  size_t bsum, boff, seg, chunks, heavy_info, pos_sorted, acc64, arrive, work, total;
+  size_t ctr, seg, chunks, heavy_info, pos_sorted, acc64, arrive, work, total;
   long long heavy_cap;
-  int nblk, ntiles;
+  int nblk, ntiles, light0;
 };
 BackwardWsLayout backward_ws_layout(long long n, uint32_t dim);
+// Points the workspace fields of p into w laid out as L.
+void bind_backward_ws(BackwardParams& p, char* w, const BackwardWsLayout& L);
 int backward_team_shift(uint32_t dim, int row_dtype);
 cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s);
 

@@ -465,17 +465,7 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
     p.one_minus_b2 = (float)(1.0 - (double)hp->beta2);
     p.gsum_out = out;
     p.reduce_only = reduce_only;
-    p.bsum = reinterpret_cast<int32_t*>(scratch + BL.bsum);
-    p.boff = reinterpret_cast<int32_t*>(scratch + BL.boff);
-    p.seg = reinterpret_cast<int2*>(scratch + BL.seg);
-    p.chunks = reinterpret_cast<int4*>(scratch + BL.chunks);
-    p.heavy_info = reinterpret_cast<int4*>(scratch + BL.heavy_info);
-    p.pos_sorted = reinterpret_cast<int32_t*>(scratch + BL.pos_sorted);
-    p.acc64 = reinterpret_cast<double*>(scratch + BL.acc64);
-    p.arrive = reinterpret_cast<int32_t*>(scratch + BL.arrive);
-    p.work = reinterpret_cast<int32_t*>(scratch + BL.work);
-    p.nblk = BL.nblk;
-    p.ntiles = BL.ntiles;
+    mt::bind_backward_ws(p, scratch, BL);
     p.team_shift = mt::backward_team_shift(T.dim, T.row_dtype);
     p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
     return mt::launch_backward(p, s) == cudaSuccess ? MT_OK : MT_ECUDA;
