@@ -769,9 +769,9 @@ BackwardWsLayout backward_ws_layout(long long n, uint32_t dim) {
     return o;
   };
   const size_t nn = (size_t)(n > 0 ? n : 1);
-  // a heavy unique has more than kChunk positions and at most count / 64 + 1 warp-chunks (a warp-chunk holds
-  // at least 64 positions), so n / 21 + 2 bounds the heavy warp-chunks
-  L.light0 = (int)(n / 21 + 2);
+  // a heavy unique has more than kChunk positions and at most count / kTeamShare + 1 warp-chunks (a warp-chunk
+  // holds kTeamShare positions per team, one team or more), so this bounds the heavy warp-chunks
+  L.light0 = (int)(n / kTeamShare + n / (kChunk + 1) + 2);
   L.ctr = take(16);
   L.seg = take(nn * 8);
   L.chunks = take(((size_t)L.light0 + nn) * 16);
