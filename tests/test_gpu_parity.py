@@ -433,6 +433,33 @@ def test_integer_grads_sum_exactly():
     assert np.array_equal(gsum[:r["U"]].cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("n_unique", [2049, 4096])
+@pytest.mark.parametrize("row_dtype,dim", [("f32", 32), ("bf16", 64)])
+def test_grouping_plan_boundaries(n_unique, row_dtype, dim):
+    """The backward's grouping at its boundaries: keys with 31 | 32 | 33 positions (a light unique has at
+    most 32), 255 | 256 | 257 and 513 (one heavy warp-chunk holds 256 positions at these dims), filled with
+    single-position keys up to a unique count one past, or exactly at, the end of a 2048-unique block of the
+    grouping plan.  Positions are shuffled, gradients are integers (so every sum is exact and compared bit
+    for bit), then a second step with normal gradients checks Adam."""
+    rng = np.random.default_rng(n_unique + dim)
+    special = [1, 2, 31, 32, 33, 255, 256, 257, 513, 1000]
+    counts = special + [1] * (n_unique - len(special))
+    ids = np.repeat(np.arange(n_unique, dtype=np.int64) * 7919 + 11, counts)
+    b = W.single_feature(ids[rng.permutation(ids.size)])
+    tab = mt.Table(16, dim, row_dtype=row_dtype)
+    ref = oracle.Table(16, dim, row_dtype=oracle.BF16 if row_dtype == "bf16" else oracle.F32)
+    res = tab.lookup(to_dev(b.ids), b.feat_offsets, b.table_ids)
+    r = ref.lookup(b.ids, b.feat_offsets, b.table_ids)
+    compare_lookup(res, r)
+    assert r["U"] == n_unique
+    g = W.grads_small_int(7, b.n, dim)
+    gsum = tab.backward_adam(res, to_dev(g), want_gsum=True)
+    want = ref.backward_adam(g, want_gsum=True)
+    assert np.array_equal(gsum[:n_unique].cpu().numpy(), want)
+    compare_after_adam(tab, res, ref, r, row_dtype)
+    run_steps(tab, ref, [b], row_dtype=row_dtype, grad_dtype="f32", seed0=41)
+
+
 # ---------------------------------------------------------------------------
 # full size, in the launch configuration the benchmark times
 # ---------------------------------------------------------------------------
