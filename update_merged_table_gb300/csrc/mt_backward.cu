@@ -9,7 +9,7 @@
 // bias correction.
 //
 // Kernels, in launch order:
-//  k_bw_plan         per block of uniques (after a memset of four counters):
+//  k_bw_plan         per block of uniques (after a memset of three counters):
 //                    each unique's segment {start, count}, a chunk descriptor
 //                    per light unique, a record per heavy unique (more than
 //                    kChunk positions); each block reserves its ranges with
@@ -87,7 +87,7 @@ constexpr int kUPT = kScanTile / kScanThreads;  // uniques per thread in k_bw_pl
 
 __global__ void __launch_bounds__(kScanThreads) k_bw_plan(const BackwardParams p) {
   __shared__ int s_warp[3][kScanThreads / 32];
-  __shared__ int s_base[4];
+  __shared__ int s_base[3];
   if (blockIdx.x == p.nblk) {  // the extra block: step counter and this step's Adam scalars
     if (threadIdx.x == 0 && p.reduce_only) p.work[0] = 0;
     if (threadIdx.x == 0 && !p.reduce_only) {
@@ -799,7 +799,7 @@ void bind_backward_ws(BackwardParams& p, char* w, const BackwardWsLayout& L) {
 }
 
 cudaError_t launch_backward(const BackwardParams& p, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(p.ctr, 0, 4 * sizeof(int32_t), s);
+  cudaError_t e = cudaMemsetAsync(p.ctr, 0, 3 * sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
   {
     MT_LAUNCH("k_bw_plan", s);

@@ -112,7 +112,7 @@ struct BackwardParams {
   float* gsum_out;
   int reduce_only;      // 1: gradient sums only; no Adam step and no step counter change
   // workspace
-  int32_t* ctr;         // [4] positions, heavy warp-chunks and heavy uniques placed so far (zeroed per call;
+  int32_t* ctr;         // [3] positions, heavy warp-chunks and heavy uniques placed so far (zeroed per call;
                         //     their totals once k_bw_plan is done)
   int2* seg;            // [n] {segment start, count} of each unique; the fill advances the start to the end
   int4* chunks;         // [light0 + n] descriptors {start, end, row, u or -(heavy index + 1)}: the warp-chunks of
