@@ -575,7 +575,8 @@ def merged_run(args, dev, stream):
     """Automatic table merging with mixed row shapes: the 8 features of the merged-tables workload (vocab 1e4 to
     1e6, Zipf 0.8 to 1.3), 2^17 IDs each, given row dims 16, 16, 16, 32, 32, 32, 64, 64 (fp32); the planner puts
     them into three merged tables.  A step is mt_lookup_grouped (every feature segment routed to its table) and
-    one mt_backward_adam per merged table, replayed as CUDA graphs on fresh batches."""
+    mt_backward_adam_grouped (each merged table's backward and Adam), the tables side by side on side streams,
+    replayed as CUDA graphs on fresh batches."""
     import torch
     import update_merged_table_gb300 as mt
     dims = [16, 16, 16, 32, 32, 32, 64, 64]
@@ -593,10 +594,8 @@ def merged_run(args, dev, stream):
     def fwd(j):
         return mtabs.lookup(ids[j], batches[j].feat_offsets)
 
-    for j in range(1 + args.warmup):  # cold step and warm-up, eager (they also size every workspace)
+    for j in range(1 + args.warmup):  # cold step and warm-up, eager (they also size the grouped workspaces)
         mtabs.backward_adam(fwd(j), grads[j])
-    for t, sz in zip(mtabs.tables, sizes):
-        t.reserve_workspaces(sz)
     torch.cuda.synchronize(dev)
     live0 = [t.stats()["live"] for t in mtabs.tables]
     graphs = []
@@ -642,8 +641,8 @@ def merged_run(args, dev, stream):
             "ids_per_s": N / (f_s + b_s), "fwd_ms": f_s * 1e3, "bwd_ms": b_s * 1e3,
             "roofline_fwd": {"bytes_per_step": fwd_bytes, "frac": fwd_bytes / f_s / 1e9 / peak},
             "roofline_bwd": {"bytes_per_step": bwd_bytes, "frac": bwd_bytes / b_s / 1e9 / peak},
-            "what": "mt_lookup_grouped over the planner's three merged tables (dims 16, 32, 64) + one backward and "
-                    "Adam per table, CUDA graphs, fresh batches"}
+            "what": "mt_lookup_grouped over the planner's three merged tables (dims 16, 32, 64) + "
+                    "mt_backward_adam_grouped, the tables side by side on side streams, CUDA graphs, fresh batches"}
 
 
 def queue_ahead(torch, stream, steps: int):

@@ -325,8 +325,9 @@ typedef struct {
 int mt_plan_merge(const mt_feature_spec* features, int F, double max_load, mt_feature_placement* placement,
                   mt_merge_group* groups, int* num_groups);
 
-/* Workspace bytes mt_lookup_grouped needs for a batch of n IDs. */
-size_t mt_lookup_grouped_workspace_bytes(int64_t n);
+/* Workspace bytes mt_lookup_grouped needs for a batch of n IDs in F feature
+ * segments, however the features split it among the groups. */
+size_t mt_lookup_grouped_workspace_bytes(int64_t n, int F);
 
 /* Lookup of one batch of F feature segments over the merged tables of a plan:
  * the segments of the features placed in group g are routed, in feature
@@ -338,12 +339,33 @@ size_t mt_lookup_grouped_workspace_bytes(int64_t n);
  *               or the array may be NULL).
  *  results      host array [G], each of capacity >= the group's IDs.
  *  group_n      host int64 [G]: receives each group's number of IDs.
+ * When more than one group receives IDs, the groups run side by side on the
+ * library's own side streams of the current device (up to four, created on
+ * the first such call and kept until the process exits): they wait for the
+ * work enqueued on `stream` before the call, and work enqueued on `stream`
+ * after the call waits for all of them, also when the call returns an error.
+ * Under stream capture this records parallel branches of the graph.
  * The backward of group g is mt_backward_adam(tables[g], &results[g],
- * group_n[g], ...) with that group's gradient rows. */
+ * group_n[g], ...) with that group's gradient rows, or all groups at once with
+ * mt_backward_adam_grouped. */
 int mt_lookup_grouped(mt_table* const* tables, int G, const mt_feature_placement* placement, const int64_t* ids,
                       int64_t n, const int64_t* feat_offsets, int F, int insert_missing, void* const* out_rows,
                       const mt_lookup_result* results, int64_t* group_n, void* ws, size_t ws_bytes,
                       mt_stream stream);
+
+/* Workspace bytes mt_backward_adam_grouped needs: the groups' backward
+ * workspaces (mt_backward_workspace_bytes(tables[g], group_n[g])) side by side. */
+size_t mt_backward_grouped_workspace_bytes(mt_table* const* tables, int G, const int64_t* group_n);
+
+/* mt_backward_adam of every group of a grouped lookup: group g's call gets
+ * tables[g], &results[g], group_n[g], grads[g] (device [group_n[g], d_g] of
+ * grad_dtype) and gsum_out[g] (gsum_out may be NULL; so may its entries), and
+ * the groups run side by side as in mt_lookup_grouped.  The tables must be
+ * distinct (each call advances its table's step counter).  Every group's
+ * arguments are checked before anything is enqueued. */
+int mt_backward_adam_grouped(mt_table* const* tables, int G, const mt_lookup_result* results, const int64_t* group_n,
+                             const void* const* grads, int grad_dtype, const mt_adam* hp, float* const* gsum_out,
+                             void* ws, size_t ws_bytes, mt_stream stream);
 
 /* ---- sharded two-stage deduplication (G logical shards on one GPU) ------- */
 

@@ -159,3 +159,39 @@ def test_product_path_has_no_oracle_or_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text, f
+
+
+def test_grouped_lookup_workspace_covers_any_split(lib):
+    """The grouped lookup gives each group its own lookup workspace; the size it asks for covers the routed
+    IDs plus the groups' workspaces for any split of the batch into F feature segments and groups."""
+    import numpy as np
+    rng = np.random.default_rng(0)
+    table = ctypes.c_void_p(16)  # the workspace-size query only checks the handle is not NULL
+
+    def align(x):
+        return (x + 255) // 256 * 256
+
+    for n in (1, 100, 2047, 4096, 65536, 1 << 20, 3_000_000):
+        for _ in range(25):
+            F = int(rng.integers(1, mt.MAX_FEATURES + 1))
+            cuts = np.sort(rng.integers(0, n + 1, F - 1))
+            sizes = np.diff(np.concatenate([[0], cuts, [n]]))
+            need = align(n * 8) + sum(align(lib.mt_lookup_workspace_bytes(table, int(s))) for s in sizes if s > 0)
+            assert lib.mt_lookup_grouped_workspace_bytes(n, F) >= need, (n, sizes)
+    for F in (2, 17, mt.MAX_FEATURES):  # every group one ID past a tile: the most rounding per group
+        sizes = [2049] * F
+        n = sum(sizes)
+        need = align(n * 8) + sum(align(lib.mt_lookup_workspace_bytes(table, s)) for s in sizes)
+        assert lib.mt_lookup_grouped_workspace_bytes(n, F) >= need, F
+    assert lib.mt_lookup_grouped_workspace_bytes(10, 0) == 0
+    assert lib.mt_lookup_grouped_workspace_bytes(10, mt.MAX_FEATURES + 1) == 0
+
+
+def test_grouped_backward_rejects_bad_arguments_on_host(lib):
+    res = (ctypes.c_byte * 64)()
+    gn = (ctypes.c_int64 * 1)(0)
+    assert lib.mt_backward_grouped_workspace_bytes(None, 1, gn) == 0
+    assert lib.mt_backward_adam_grouped(None, 1, res, gn, None, mt.MT_F32, None, None, None, 0, None) == mt.MT_EINVAL
+    tabs = (ctypes.c_void_p * 1)(None)
+    assert lib.mt_backward_adam_grouped(tabs, 1, res, gn, None, mt.MT_F32, None, None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_backward_adam_grouped(tabs, 0, res, gn, None, mt.MT_F32, None, None, None, 0, None) == mt.MT_EINVAL

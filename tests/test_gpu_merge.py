@@ -67,8 +67,11 @@ def test_merged_tables_route_and_train():
             assert np.array_equal(r.rows.float().cpu().numpy(), want["rows"])
             assert (r.unique_keys[:U].cpu().numpy().view(np.uint64) >> np.uint64(56)).max() < 2  # two features each
             grads.append(W.grads_normal(10 * step + g, r.n, mtabs.groups[g]["dim"]))
-        gsums = [t.backward_adam(r, torch.from_numpy(gr).to(dev), want_gsum=True)
-                 for t, r, gr in zip(mtabs.tables, res, grads)]
+        dgrads = [torch.from_numpy(gr).to(dev) for gr in grads]
+        if step < 2:  # all tables' steps side by side (mt_backward_adam_grouped)
+            gsums = mtabs.backward_adam(res, dgrads, want_gsum=True)
+        else:  # one table at a time
+            gsums = [t.backward_adam(r, gr, want_gsum=True) for t, r, gr in zip(mtabs.tables, res, dgrads)]
         for g, (r, ref) in enumerate(zip(res, refs)):
             ref_gsum = ref.backward_adam(grads[g], want_gsum=True)
             np.testing.assert_allclose(gsums[g][:r.U].cpu().numpy(), ref_gsum, rtol=RTOL, atol=ATOL)
@@ -85,3 +88,7 @@ def test_group_without_ids_in_the_batch():
     ids = np.arange(50, dtype=np.int64)
     res = mtabs.lookup(torch.from_numpy(ids).to(mtabs.device), [0, 50, 50])
     assert res[0].U == 50 and res[1].n == 0 and res[1].U == 0
+    grads = [torch.ones((50, 16), device=mtabs.device), torch.empty((0, 32), device=mtabs.device)]
+    gs = mtabs.backward_adam(res, grads, want_gsum=True)
+    assert torch.equal(gs[0][:50].cpu(), torch.ones(50, 16))
+    assert [t.step for t in mtabs.tables] == [1, 1] and all(t.error() == 0 for t in mtabs.tables)

@@ -96,8 +96,10 @@ ABI_FUNCTIONS = {
     "mt_shard_lookup": (_I32, [_P, _P, _P, _P, _P, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "mt_shard_backward_adam": (_I32, [_P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "mt_plan_merge": (_I32, [_P, _I32, ctypes.c_double, _P, _P, _P]),
-    "mt_lookup_grouped_workspace_bytes": (_SZ, [_I64]),
+    "mt_lookup_grouped_workspace_bytes": (_SZ, [_I64, _I32]),
     "mt_lookup_grouped": (_I32, [_P, _I32, _P, _P, _I64, _P, _I32, _I32, _P, _P, _P, _P, _SZ, _P]),
+    "mt_backward_grouped_workspace_bytes": (_SZ, [_P, _I32, _P]),
+    "mt_backward_adam_grouped": (_I32, [_P, _I32, _P, _P, _P, _I32, _P, _P, _P, _SZ, _P]),
     "mt_erase_workspace_bytes": (_SZ, [_I64]),
     "mt_erase": (_I32, [_P, _P, _I64, _P, _P, _SZ, _P]),
     "mt_compact_workspace_bytes": (_SZ, [_P]),
@@ -650,7 +652,7 @@ def plan_merge(features, max_load: float = 0.5):
 
 class MergedTables:
     """The merged tables of a plan (``plan_merge``) and the lookup that routes a batch's feature segments
-    to them (``mt_lookup_grouped``); backward is per merged table."""
+    to them (``mt_lookup_grouped``); the backward runs every merged table's step (``mt_backward_adam_grouped``)."""
 
     def __init__(self, features, max_load: float = 0.5, device=None, **table_kwargs):
         self.lib = load_library()
@@ -659,7 +661,7 @@ class MergedTables:
                        for g in self.groups]
         self.device = self.tables[0].device
         self._pl = (_Placement * len(self.placement))(*[_Placement(g, t) for g, t in self.placement])
-        self._ws = None
+        self._ws = {}
 
     def group_sizes(self, feat_offsets):
         """IDs each merged table receives from a batch with these feature offsets."""
@@ -681,21 +683,56 @@ class MergedTables:
         sizes = self.group_sizes(fo)
         res = [t.new_result(sz, gather=gather) for t, sz in zip(self.tables, sizes)]
         G = len(self.tables)
-        wsb = self.lib.mt_lookup_grouped_workspace_bytes(n)
-        if self._ws is None or self._ws.numel() < wsb:
-            self._ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=self.device)
+        ws = self._workspace("lookup", self.lib.mt_lookup_grouped_workspace_bytes(n, F))
         tabs = (ctypes.c_void_p * G)(*[t.h.value for t in self.tables])
         outs = (ctypes.c_void_p * G)(*[(r.rows.data_ptr() if (gather and r.n) else None) for r in res])
         st = (_Result * G)(*[r.as_struct() for r in res])
         gn = np.zeros(G, dtype=np.int64)
         _check(self.lib.mt_lookup_grouped(tabs, G, self._pl, ids.data_ptr() if n else None, n,
                                           fo.ctypes.data_as(ctypes.c_void_p), F, int(bool(insert_missing)), outs, st,
-                                          gn.ctypes.data_as(ctypes.c_void_p), self._ws.data_ptr(), self._ws.numel(),
+                                          gn.ctypes.data_as(ctypes.c_void_p), ws.data_ptr(), ws.numel(),
                                           _stream(stream)), "mt_lookup_grouped")
         if list(gn) != sizes:
             raise RuntimeError("group sizes disagree with the plan")
         return res
 
-    def backward_adam(self, results, grads, **adam):
-        """grads: one CUDA tensor [n_g, dim_g] per merged table."""
-        return [t.backward_adam(r, g, **adam) for t, r, g in zip(self.tables, results, grads)]
+    def _workspace(self, kind: str, nbytes: int):
+        torch = _torch()
+        buf = self._ws.get(kind)
+        if buf is None or buf.numel() < nbytes:
+            if torch.cuda.is_current_stream_capturing():
+                raise RuntimeError(f"the grouped {kind} workspace would have to grow during CUDA graph capture; "
+                                   "run one eager step with the largest batch before capturing")
+            buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self._ws[kind] = buf
+        return buf
+
+    def backward_adam(self, results, grads, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
+                      eps: float = 1e-8, want_gsum: bool = False, stream=None):
+        """grads: one CUDA tensor [n_g, dim_g] per merged table, all float32 or all bfloat16
+        (``mt_backward_adam_grouped``: the tables' backward steps run side by side).  Returns one gradient-sum
+        tensor (or None) per table."""
+        torch = _torch()
+        G = len(self.tables)
+        if len(results) != G or len(grads) != G:
+            raise ValueError("one lookup result and one gradient tensor per merged table")
+        gd = {torch.float32: MT_F32, torch.bfloat16: MT_BF16}.get(grads[0].dtype)
+        if gd is None or any(g.dtype != grads[0].dtype for g in grads):
+            raise TypeError("grads must all be float32 or all bfloat16")
+        for t, r, g in zip(self.tables, results, grads):
+            if g.shape != (r.n, t.dim) or not g.is_cuda or not g.is_contiguous():
+                raise ValueError("grads[g] must be a contiguous CUDA tensor [n_g, dim_g]")
+        gsums = [torch.empty((max(r.n, 1), t.dim), dtype=torch.float32, device=self.device) if want_gsum else None
+                 for t, r in zip(self.tables, results)]
+        tabs = (ctypes.c_void_p * G)(*[t.h.value for t in self.tables])
+        gn = np.asarray([r.n for r in results], dtype=np.int64)
+        ws = self._workspace("backward", self.lib.mt_backward_grouped_workspace_bytes(
+            tabs, G, gn.ctypes.data_as(ctypes.c_void_p)))
+        st = (_Result * G)(*[r.as_struct() for r in results])
+        gp = (ctypes.c_void_p * G)(*[(g.data_ptr() if r.n else None) for g, r in zip(grads, results)])
+        gs = (ctypes.c_void_p * G)(*[_ptr(x) for x in gsums]) if want_gsum else None
+        hp = _Adam(lr, beta1, beta2, eps)
+        _check(self.lib.mt_backward_adam_grouped(tabs, G, st, gn.ctypes.data_as(ctypes.c_void_p), gp, gd,
+                                                 ctypes.byref(hp), gs, ws.data_ptr(), ws.numel(), _stream(stream)),
+               "mt_backward_adam_grouped")
+        return gsums

@@ -236,6 +236,23 @@ PooledLayout pooled_layout(const mt_table* t, int64_t n, int64_t num_bags) {
 
 }  // namespace
 
+namespace mt {
+// The host checks mt_lookup and mt_backward_adam make on a group's own
+// arguments before enqueuing anything: the grouped calls run them for every
+// group first, so that an error still leaves nothing enqueued.
+int lookup_group_status(const mt_lookup_result* res, const void* out_rows) {
+  if (!valid_result(res)) return MT_EINVAL;
+  if (out_rows != nullptr && !aligned(out_rows, 16)) return MT_EINVAL;
+  return MT_OK;
+}
+int backward_group_status(const mt_table* t, const mt_lookup_result* res, int64_t n, const void* grads,
+                          int grad_dtype, const mt_adam* hp, const float* gsum_out) {
+  if (t == nullptr || n < 0 || n > 0x7FFFFFFF) return MT_EINVAL;
+  if (n > 0 && (grads == nullptr || !aligned(grads, 16))) return MT_EINVAL;
+  return check_backward(t, res, grad_dtype, hp, gsum_out);
+}
+}  // namespace mt
+
 extern "C" {
 
 int mt_abi_version(void) { return MT_ABI_VERSION; }

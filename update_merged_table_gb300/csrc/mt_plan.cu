@@ -8,11 +8,16 @@
 // inside it each keeps its own key space through its table id (the merged key
 // (table_id << 56) | id).
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "mt_kernels.cuh"
 
 namespace mt {
+int lookup_group_status(const mt_lookup_result* res, const void* out_rows);
+int backward_group_status(const mt_table* t, const mt_lookup_result* res, int64_t n, const void* grads,
+                          int grad_dtype, const mt_adam* hp, const float* gsum_out);
+
 namespace {
 
 constexpr int kRouteSegs = 64;  // segments per routing launch (kernel parameter space)
@@ -34,6 +39,75 @@ __global__ void __launch_bounds__(256) k_route(const long long* ids, long long* 
       dst[i] = __ldg(&src[i]);
   }
 }
+
+// The merged tables are independent, and each one's lookup (or backward) is
+// a chain of small latency-bound launches: the groups run side by side on the
+// library's side streams, forked from the caller's stream by an event and
+// joined back into it before the call returns (under stream capture this
+// becomes parallel branches of the graph).
+constexpr int kSideStreams = 4;
+std::mutex g_side_mu;
+cudaStream_t g_side[kMaxDevices][kSideStreams] = {};
+
+// The side streams of the current device, created on first use (non-blocking).
+cudaError_t side_streams(cudaStream_t* out) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  for (int k = 0; k < kSideStreams; ++k) {
+    if (g_side[dev][k] == nullptr) {
+      const cudaError_t e = cudaStreamCreateWithFlags(&g_side[dev][k], cudaStreamNonBlocking);
+      if (e != cudaSuccess) return e;
+    }
+    out[k] = g_side[dev][k];
+  }
+  return cudaSuccess;
+}
+
+// Work enqueued on side[0 .. k) from now on waits for everything enqueued on s so far.
+cudaError_t fork_streams(cudaStream_t s, const cudaStream_t* side, int k) {
+  cudaEvent_t ev;
+  cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  e = cudaEventRecord(ev, s);
+  for (int i = 0; i < k && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(side[i], ev, 0);
+  cudaEventDestroy(ev);  // released once the waits are resolved
+  return e;
+}
+
+// Work enqueued on s from now on waits for everything enqueued on side[0 .. k) so far.
+cudaError_t join_streams(cudaStream_t s, const cudaStream_t* side, int k) {
+  cudaError_t first = cudaSuccess;
+  for (int i = 0; i < k; ++i) {
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) {
+      e = cudaEventRecord(ev, side[i]);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev, 0);
+      cudaEventDestroy(ev);
+    }
+    if (first == cudaSuccess) first = e;
+  }
+  return first;
+}
+
+// Where group g's work goes: its own side stream when several groups have
+// work, else the caller's stream.
+struct GroupStreams {
+  cudaStream_t caller;
+  cudaStream_t side[kSideStreams];
+  int used = 0;  // side streams forked
+  cudaError_t begin(cudaStream_t s, int active) {
+    caller = s;
+    if (active < 2) return cudaSuccess;
+    const cudaError_t e = side_streams(side);
+    if (e != cudaSuccess) return e;
+    used = active < kSideStreams ? active : kSideStreams;
+    return fork_streams(s, side, used);
+  }
+  cudaStream_t stream(int slot) const { return used ? side[slot % used] : caller; }
+  cudaError_t end() { return used ? join_streams(caller, side, used) : cudaSuccess; }
+};
 
 }  // namespace
 }  // namespace mt
@@ -81,9 +155,14 @@ int mt_plan_merge(const mt_feature_spec* features, int F, double max_load, mt_fe
   return MT_OK;
 }
 
-size_t mt_lookup_grouped_workspace_bytes(int64_t n) {
-  if (n < 0 || n > 0x7FFFFFFF) return 0;
-  return mt::align_up((size_t)(n > 0 ? n : 1) * 8, 256) + mt::lookup_ws_layout(n).total;
+size_t mt_lookup_grouped_workspace_bytes(int64_t n, int F) {
+  if (n < 0 || n > 0x7FFFFFFF || F < 1 || F > MT_MAX_FEATURES) return 0;
+  // the routed IDs, then one lookup workspace per group with IDs (at most min(F, n) of them).  Split into
+  // groups, a batch needs at most one more tile, one more scratch-hash rounding and one more set of array
+  // alignments per group: the workspace of a one-ID lookup.
+  const long long groups = n < F ? n : F;
+  return mt::align_up((size_t)(n > 0 ? n : 1) * 8, 256) + mt::align_up(mt::lookup_ws_layout(n).total, 256) +
+         (size_t)groups * mt::align_up(mt::lookup_ws_layout(1).total, 256);
 }
 
 int mt_lookup_grouped(mt_table* const* tables, int G, const mt_feature_placement* placement, const int64_t* ids,
@@ -100,18 +179,41 @@ int mt_lookup_grouped(mt_table* const* tables, int G, const mt_feature_placement
   }
   for (int g = 0; g < G; ++g)
     if (tables[g] == nullptr) return MT_EINVAL;
-  if (ws == nullptr || ws_bytes < mt_lookup_grouped_workspace_bytes(n) || ((uintptr_t)ws % 256) != 0)
-    return MT_ENOSPACE;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  long long* routed = static_cast<long long*>(ws);
-  void* lws = static_cast<char*>(ws) + mt::align_up((size_t)(n > 0 ? n : 1) * 8, 256);
-  const size_t lws_bytes = ws_bytes - mt::align_up((size_t)(n > 0 ? n : 1) * 8, 256);
+  if (ws == nullptr || ((uintptr_t)ws % 256) != 0) return MT_ENOSPACE;
+  // each group's IDs, its slice of the routed IDs and its own lookup workspace (the groups run side by side)
+  std::vector<long long> ng(G, 0), rbase(G, 0);
+  std::vector<size_t> wso(G, 0), wsz(G, 0);
+  for (int f = 0; f < F; ++f) ng[placement[f].group] += feat_offsets[f + 1] - feat_offsets[f];
+  size_t off = mt::align_up((size_t)(n > 0 ? n : 1) * 8, 256);
+  long long rb = 0;
+  int active = 0;
   for (int g = 0; g < G; ++g) {
-    // the group's features in batch order, their segments routed into one contiguous batch
+    rbase[g] = rb;
+    rb += ng[g];
+    if (ng[g] > 0) {
+      wsz[g] = mt::lookup_ws_layout(ng[g]).total;
+      wso[g] = off;
+      off = mt::align_up(off + wsz[g], 256);
+      ++active;
+    }
+  }
+  if (ws_bytes < off) return MT_ENOSPACE;
+  for (int g = 0; g < G; ++g) {
+    const int st = mt::lookup_group_status(&results[g], out_rows ? out_rows[g] : nullptr);
+    if (st != MT_OK) return st;
+  }
+  long long* routed = static_cast<long long*>(ws);
+  mt::GroupStreams gs;
+  if (gs.begin(reinterpret_cast<cudaStream_t>(stream), active) != cudaSuccess) return MT_ECUDA;
+  int rc = MT_OK, slot = 0;
+  for (int g = 0; g < G && rc == MT_OK; ++g) {
+    const cudaStream_t s = ng[g] > 0 ? gs.stream(slot++) : gs.caller;
+    // the group's features in batch order, their segments routed into its slice of the routed IDs
     std::vector<int64_t> offs(1, 0);
     std::vector<uint8_t> tids;
     mt::RouteSegs segs;
     std::memset(&segs, 0, sizeof(segs));
+    long long* dst = routed + rbase[g];
     for (int f = 0; f < F; ++f) {
       if (placement[f].group != g) continue;
       const long long len = feat_offsets[f + 1] - feat_offsets[f];
@@ -121,7 +223,7 @@ int mt_lookup_grouped(mt_table* const* tables, int G, const mt_feature_placement
         segs.len[segs.count] = len;
         if (++segs.count == mt::kRouteSegs) {
           MT_LAUNCH("k_route", s);
-          mt::k_route<<<dim3(64, mt::kRouteSegs), 256, 0, s>>>(reinterpret_cast<const long long*>(ids), routed, segs);
+          mt::k_route<<<dim3(64, mt::kRouteSegs), 256, 0, s>>>(reinterpret_cast<const long long*>(ids), dst, segs);
           segs.count = 0;
         }
       }
@@ -130,21 +232,67 @@ int mt_lookup_grouped(mt_table* const* tables, int G, const mt_feature_placement
     }
     if (segs.count > 0) {
       MT_LAUNCH("k_route", s);
-      mt::k_route<<<dim3(64, segs.count), 256, 0, s>>>(reinterpret_cast<const long long*>(ids), routed, segs);
+      mt::k_route<<<dim3(64, segs.count), 256, 0, s>>>(reinterpret_cast<const long long*>(ids), dst, segs);
     }
-    if (cudaGetLastError() != cudaSuccess) return MT_ECUDA;
-    const int64_t ng = offs.back();
-    group_n[g] = ng;
+    if (cudaGetLastError() != cudaSuccess) {
+      rc = MT_ECUDA;
+      break;
+    }
+    group_n[g] = ng[g];
     if (tids.empty()) {  // no feature of this batch goes to the group: an empty lookup
       offs.push_back(0);
       tids.push_back(0);
     }
-    const int rc = mt_lookup(tables[g], reinterpret_cast<const int64_t*>(routed), ng, offs.data(), tids.data(),
-                             (int)tids.size(), insert_missing, out_rows ? out_rows[g] : nullptr, &results[g], lws,
-                             lws_bytes, stream);
-    if (rc != MT_OK) return rc;
+    rc = mt_lookup(tables[g], reinterpret_cast<const int64_t*>(dst), ng[g], offs.data(), tids.data(),
+                   (int)tids.size(), insert_missing, out_rows ? out_rows[g] : nullptr, &results[g],
+                   ng[g] > 0 ? static_cast<char*>(ws) + wso[g] : nullptr, wsz[g], reinterpret_cast<mt_stream>(s));
   }
-  return MT_OK;
+  // every group's work is ordered before the caller's later work, also after an error
+  if (gs.end() != cudaSuccess && rc == MT_OK) rc = MT_ECUDA;
+  return rc;
+}
+
+size_t mt_backward_grouped_workspace_bytes(mt_table* const* tables, int G, const int64_t* group_n) {
+  if (tables == nullptr || group_n == nullptr || G < 1) return 0;
+  size_t off = 0;
+  for (int g = 0; g < G; ++g) {
+    if (tables[g] == nullptr || group_n[g] < 0) return 0;
+    off = mt::align_up(off + mt_backward_workspace_bytes(tables[g], group_n[g]), 256);
+  }
+  return off > 0 ? off : 256;
+}
+
+int mt_backward_adam_grouped(mt_table* const* tables, int G, const mt_lookup_result* results, const int64_t* group_n,
+                             const void* const* grads, int grad_dtype, const mt_adam* hp, float* const* gsum_out,
+                             void* ws, size_t ws_bytes, mt_stream stream) {
+  if (tables == nullptr || results == nullptr || group_n == nullptr || grads == nullptr || G < 1) return MT_EINVAL;
+  for (int g = 0; g < G; ++g)
+    if (tables[g] == nullptr || group_n[g] < 0) return MT_EINVAL;
+  if (ws == nullptr || ((uintptr_t)ws % 256) != 0 || ws_bytes < mt_backward_grouped_workspace_bytes(tables, G, group_n))
+    return MT_ENOSPACE;
+  for (int g = 0; g < G; ++g) {
+    for (int q = 0; q < g; ++q)  // the tables must be distinct: each call advances its table's step
+      if (tables[q] == tables[g]) return MT_EINVAL;
+    const int st = mt::backward_group_status(tables[g], &results[g], group_n[g], grads[g], grad_dtype, hp,
+                                             gsum_out ? gsum_out[g] : nullptr);
+    if (st != MT_OK) return st;
+  }
+  int active = 0;
+  for (int g = 0; g < G; ++g) active += group_n[g] > 0;
+  mt::GroupStreams gs;
+  if (gs.begin(reinterpret_cast<cudaStream_t>(stream), active) != cudaSuccess) return MT_ECUDA;
+  int rc = MT_OK, slot = 0;
+  size_t off = 0;
+  for (int g = 0; g < G && rc == MT_OK; ++g) {
+    const size_t need = mt_backward_workspace_bytes(tables[g], group_n[g]);
+    const cudaStream_t s = group_n[g] > 0 ? gs.stream(slot++) : gs.caller;
+    rc = mt_backward_adam(tables[g], &results[g], group_n[g], grads[g], grad_dtype, hp,
+                          gsum_out ? gsum_out[g] : nullptr, static_cast<char*>(ws) + off, need,
+                          reinterpret_cast<mt_stream>(s));
+    off = mt::align_up(off + need, 256);
+  }
+  if (gs.end() != cudaSuccess && rc == MT_OK) rc = MT_ECUDA;
+  return rc;
 }
 
 }  // extern "C"
