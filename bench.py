@@ -400,7 +400,8 @@ def _prefill(torch, tab, wl, dev):
 def e2e_run(args, dev, stream, tdt):
     """The same step sequence through the public API with HOST buffers, on a table of its own: a cold
     step, warm-up steps, then K fresh steps, each copying its IDs and gradients from pinned host memory
-    (step j + 1's copies on a copy stream while step j computes) and reading its unique count back."""
+    (step j + 1's copies on a copy stream while step j computes), running its calls (captured as a CUDA
+    graph before timing) and reading its unique count back."""
     import torch
     import update_merged_table_gb300 as mt
     wl = Workload(args.config, args.users, args.log2_slots)
@@ -444,6 +445,27 @@ def e2e_run(args, dev, stream, tdt):
     torch.cuda.synchronize(dev)
     link_gbs = (ids0.numel() * 8 + g0.numel() * g0.element_size()) / (la.elapsed_time(lb) / 1e3) / 1e9
 
+    # each step's public-API calls (lookup, backward with Adam, erase) captured once as a CUDA graph on its
+    # slot's device buffers, as a training loop would run them: per step the timed loop then issues the copies
+    # from pinned host memory, one graph replay and the read-back, so the host's own per-call overhead does
+    # not sit between the copies
+    tab.reserve_workspaces(nmax, n_erase=max((h[3].numel() for h in host if h[3] is not None), default=0))
+    torch.cuda.synchronize(dev)
+    graphs = []
+    for j, (b, ids_h, g_h, er_h) in enumerate(host):
+        s = slots[j % 2]
+        big = s["big"]
+        res = mt.LookupResult(big.unique_keys[:b.n], big.inverse[:b.n], big.counts[:b.n], big.unique_rows[:b.n],
+                              big.num_unique, big.rows[:b.n], b.n, big.ranks[:b.n])
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            tab.lookup(s["ids"][:b.n], b.feat_offsets, b.table_ids, result=res)
+            tab.backward_adam(res, s["grads"][:b.n])
+            if er_h is not None:
+                tab.erase(s["erase"][:er_h.numel()], want_found=False)
+        graphs.append((gr, res))
+    torch.cuda.synchronize(dev)
+
     used = [None, None]
     landed = [None, None]
 
@@ -472,13 +494,8 @@ def e2e_run(args, dev, stream, tdt):
         b, ids_h, g_h, er_h = host[j]
         stream.wait_event(landed[k])
         s = slots[k]
-        big = s["big"]
-        res = mt.LookupResult(big.unique_keys[:b.n], big.inverse[:b.n], big.counts[:b.n], big.unique_rows[:b.n],
-                              big.num_unique, big.rows[:b.n], b.n, big.ranks[:b.n])
-        tab.lookup(s["ids"][:b.n], b.feat_offsets, b.table_ids, result=res)
-        tab.backward_adam(res, s["grads"][:b.n])
-        if er_h is not None:
-            tab.erase(s["erase"][:er_h.numel()], want_found=False)
+        gr, res = graphs[j]
+        gr.replay()  # on `stream`, the current stream
         s["u_h"].copy_(res.num_unique, non_blocking=True)
         used[k] = torch.cuda.Event()
         used[k].record(stream)
@@ -493,10 +510,11 @@ def e2e_run(args, dev, stream, tdt):
     tot, mx = aggregate(float(ids_done), secs)
     out = {"value": tot / mx, "unit": UNIT, "h2d_bytes_per_step": h2d // ke, "d2h_bytes_per_step": d2h // ke,
            "steps": ke, "h2d_GB/s_effective": h2d / secs / 1e9, "h2d_GB/s_link": link_gbs,
-           "what": "mt_lookup + mt_backward_adam through the Python binding, inputs copied from pinned host "
-                   "memory inside the timed region; the unique count read back each step; a table of its own "
+           "what": "mt_lookup + mt_backward_adam through the Python binding, each step's calls captured as a "
+                   "CUDA graph before timing; inputs copied from pinned host memory inside the timed region (one "
+                   "step ahead, on a copy stream); the unique count read back each step; a table of its own "
                    "running the same cold, warm-up and fresh steps"}
-    del tab, host, slots
+    del tab, host, slots, graphs
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
     return out
