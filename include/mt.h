@@ -333,7 +333,7 @@ size_t mt_lookup_grouped_workspace_bytes(int64_t n, int F);
  * the segments of the features placed in group g are routed, in feature
  * order, into one batch for tables[g] (its feature offsets and table ids from
  * the plan), and looked up there as mt_lookup does.
- *  tables       host array [G] of the merged tables (rows of group g's shape).
+ *  tables       host array [G] of distinct merged tables (rows of group g's shape).
  *  ids          device int64 [n]; feat_offsets host int64 [F + 1] (0 .. n).
  *  out_rows     host array [G] of device pointers [group_n[g], d_g] (entries
  *               or the array may be NULL).

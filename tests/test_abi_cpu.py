@@ -195,3 +195,16 @@ def test_grouped_backward_rejects_bad_arguments_on_host(lib):
     tabs = (ctypes.c_void_p * 1)(None)
     assert lib.mt_backward_adam_grouped(tabs, 1, res, gn, None, mt.MT_F32, None, None, None, 0, None) == mt.MT_EINVAL
     assert lib.mt_backward_adam_grouped(tabs, 0, res, gn, None, mt.MT_F32, None, None, None, 0, None) == mt.MT_EINVAL
+
+
+def test_grouped_lookup_rejects_a_table_in_two_groups(lib):
+    """The groups' lookups run side by side, so one table may not serve two groups (checked on the host,
+    before any handle is used)."""
+    t = ctypes.c_void_p(16)
+    tabs = (ctypes.c_void_p * 2)(t, t)
+    pl = (ctypes.c_int32 * 2)(0, 0)  # one feature: group 0, table id 0
+    fo = (ctypes.c_int64 * 2)(0, 0)
+    res = (ctypes.c_byte * 256)()
+    gn = (ctypes.c_int64 * 2)()
+    ws = ctypes.c_void_p(4096)
+    assert lib.mt_lookup_grouped(tabs, 2, pl, None, 0, fo, 1, 1, None, res, gn, ws, 1 << 20, None) == mt.MT_EINVAL

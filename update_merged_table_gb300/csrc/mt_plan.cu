@@ -177,8 +177,11 @@ int mt_lookup_grouped(mt_table* const* tables, int G, const mt_feature_placement
     if (feat_offsets[f + 1] < feat_offsets[f]) return MT_EINVAL;
     if (placement[f].group < 0 || placement[f].group >= G || placement[f].table_id == 0xFF) return MT_EINVAL;
   }
-  for (int g = 0; g < G; ++g)
+  for (int g = 0; g < G; ++g) {
     if (tables[g] == nullptr) return MT_EINVAL;
+    for (int q = 0; q < g; ++q)  // distinct tables: the groups' lookups run side by side
+      if (tables[q] == tables[g]) return MT_EINVAL;
+  }
   if (ws == nullptr || ((uintptr_t)ws % 256) != 0) return MT_ENOSPACE;
   // each group's IDs, its slice of the routed IDs and its own lookup workspace (the groups run side by side)
   std::vector<long long> ng(G, 0), rbase(G, 0);
