@@ -504,6 +504,10 @@ __device__ __forceinline__ void accumulate_async(const BackwardParams& p, const 
   cp_async_wait<0>();  // nothing of this call stays in flight
 }
 
+// fp32 gradient matrices up to this size stay in L2 while the heavy kernel
+// reads them (a pooled backward's bag rows): read into registers there.
+constexpr unsigned long long kL2GradBytes = 16ull << 20;
+
 // Rows per ring stage of the heavy kernel (0: keep rows in registers) and
 // stages per ring: 16-byte pieces per lane and row x rows x stages = 16.
 constexpr int kHeavyStages = 4;
@@ -542,6 +546,7 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
   const int d = (int)p.T.dim;
   const int col0 = lt * VEC;
   const int HWC = __ldcg(&p.ctr[1]);
+  const bool l2_rows = (unsigned long long)p.grad_rows * (unsigned long long)d * 4ull <= kL2GradBytes;
 
   // ---- heavy warp-chunks, handed to warps one at a time (they differ in size) ----
   for (;;) {
@@ -565,8 +570,17 @@ __global__ void __launch_bounds__(256, 3) k_bw_heavy_reduce(const BackwardParams
         __syncwarp(team_mask);
       }
       if (active) {
-        if (HS > 0) accumulate_async<GD, VEC, (HS > 0 ? HS : 1), kHeavyStages>(p, my_pos, te - tb, d, col, ring, hi, lo);
-        else accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
+        if constexpr (HS > 0 && GD == MT_F32) {
+          // fp32 gradient rows few enough to stay in L2 (a pooled backward's bag rows): read into
+          // registers, since the ring's two copies and two shared-memory reads per row and lane would
+          // throttle the memory-instruction pipe instead
+          if (l2_rows) accumulate<GD, VEC, 2>(p, my_pos, te - tb, d, col, hi, lo);
+          else accumulate_async<GD, VEC, HS, kHeavyStages>(p, my_pos, te - tb, d, col, ring, hi, lo);
+        } else if constexpr (HS > 0) {
+          accumulate_async<GD, VEC, HS, kHeavyStages>(p, my_pos, te - tb, d, col, ring, hi, lo);
+        } else {
+          accumulate<GD, VEC, UNR>(p, my_pos, te - tb, d, col, hi, lo);
+        }
       }
       for (int o = team; o < 32; o <<= 1) {
 #pragma unroll
