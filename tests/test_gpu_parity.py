@@ -130,6 +130,16 @@ def test_bf16_rows_fp32_grads_and_fp32_rows_bf16_grads():
     run_steps(tab, ref, [b, b], row_dtype="f32", grad_dtype="bf16")
 
 
+def test_bf16_rows_fp32_grads_past_l2():
+    """bf16 rows with fp32 gradients whose matrix is too large to stay in L2 (> 16 MB): the heavy uniques'
+    rows go through the shared-memory ring, not the register path small fp32 matrices take."""
+    batches = [W.jagged_batch(s, users=256, lengths_seed=s) for s in range(2)]
+    assert all(b.n * 64 * 4 > (16 << 20) for b in batches)
+    tab = mt.Table(19, 64, row_dtype="bf16")
+    ref = oracle.Table(19, 64, row_dtype=oracle.BF16)
+    run_steps(tab, ref, batches, row_dtype="bf16", grad_dtype="f32")
+
+
 def test_large_keyspace_prefilled():
     """Zipf(1.05) over a 2^32 key space, dim 128 fp32, table prefilled to load 0.7."""
     log2 = 16
