@@ -92,3 +92,75 @@ def test_group_without_ids_in_the_batch():
     gs = mtabs.backward_adam(res, grads, want_gsum=True)
     assert torch.equal(gs[0][:50].cpu(), torch.ones(50, 16))
     assert [t.step for t in mtabs.tables] == [1, 1] and all(t.error() == 0 for t in mtabs.tables)
+
+
+def test_more_groups_than_side_streams():
+    """Six merged tables (six row shapes): more groups than the library's four side streams, so groups share
+    streams; every table still matches its oracle table, lookup and a grouped backward step."""
+    feats = [(8, "f32", 3000), (16, "f32", 3000), (24, "f32", 3000), (32, "f32", 3000), (48, "f32", 3000),
+             (64, "bf16", 3000)]
+    mtabs = mt.MergedTables(feats, max_load=0.5, init_seed=5)
+    assert len(mtabs.groups) == 6
+    refs = [oracle.Table(g["log2_slots"], g["dim"], row_dtype=oracle.BF16 if g["row_dtype"] == "bf16" else oracle.F32,
+                         init_seed=5) for g in mtabs.groups]
+    rng = np.random.default_rng(11)
+    sizes = [900, 1300, 700, 1100, 500, 1600]
+    ids = np.concatenate([W.zipf_ranks(rng, s, 1.1, 2500) - 1 for s in sizes]).astype(np.int64)
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    dev = mtabs.device
+    for step in range(2):
+        res = mtabs.lookup(torch.from_numpy(ids).to(dev), offs)
+        grads, wants = [], []
+        for g, (r, ref) in enumerate(zip(res, refs)):
+            gids, goffs, gtids = routed(ids, offs, mtabs.placement, g)
+            want = ref.lookup(gids, goffs, gtids)
+            assert r.U == want["U"]
+            assert np.array_equal(r.inverse[:r.n].cpu().numpy(), want["inverse"])
+            assert np.array_equal(r.rows.float().cpu().numpy(), want["rows"])
+            grads.append(W.grads_normal(50 * step + g, r.n, mtabs.groups[g]["dim"]))
+        gsums = mtabs.backward_adam(res, [torch.from_numpy(x).to(dev) for x in grads], want_gsum=True)
+        for g, (r, ref) in enumerate(zip(res, refs)):
+            np.testing.assert_allclose(gsums[g][:r.U].cpu().numpy(), ref.backward_adam(grads[g], want_gsum=True),
+                                       rtol=RTOL, atol=ATOL)
+    assert all(t.error() == 0 for t in mtabs.tables) and [t.step for t in mtabs.tables] == [2] * 6
+
+
+def test_grouped_calls_replay_as_cuda_graphs():
+    """The grouped lookup and backward captured as CUDA graphs (their side streams become parallel branches)
+    and replayed give the same tables as the same calls made eagerly on a twin."""
+    eager = mt.MergedTables(FEATURES, max_load=0.5, init_seed=9)
+    graphed = mt.MergedTables(FEATURES, max_load=0.5, init_seed=9)
+    dev = eager.device
+    batches = [batch(20 + j) for j in range(3)]
+    ids = [torch.from_numpy(i).to(dev) for i, _ in batches]
+    grads = [[torch.from_numpy(W.grads_normal(70 + 5 * j + g, sz, eager.groups[g]["dim"])).to(dev)
+              for g, sz in enumerate(eager.group_sizes(o))] for j, (_, o) in enumerate(batches)]
+    # step 0 eager on both (it also sizes every workspace); steps 1 and 2: eager against graph replays
+    for m in (eager, graphed):
+        m.backward_adam(m.lookup(ids[0], batches[0][1]), grads[0])
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    for j in (1, 2):
+        gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf, stream=stream):
+            res = graphed.lookup(ids[j], batches[j][1])
+        with torch.cuda.graph(gb, stream=stream):
+            graphed.backward_adam(res, grads[j])
+        graphs.append((gf, gb, res))
+    for j, (gf, gb, res) in zip((1, 2), graphs):
+        want = eager.lookup(ids[j], batches[j][1])
+        eager.backward_adam(want, grads[j])
+        gf.replay()
+        gb.replay()
+        torch.cuda.synchronize()
+        for r, w in zip(res, want):
+            assert r.U == w.U
+            assert torch.equal(r.unique_keys[:r.U], w.unique_keys[:w.U])
+            assert torch.equal(r.inverse[:r.n], w.inverse[:w.n])
+            assert torch.equal(r.rows, w.rows)
+    for te, tg in zip(eager.tables, graphed.tables):
+        k_e, _ = te.export()
+        k_g, _ = tg.export()
+        assert np.array_equal(np.sort(k_e.cpu().numpy()), np.sort(k_g.cpu().numpy()))
+        assert te.step == tg.step == 3 and te.error() == 0 and tg.error() == 0
