@@ -209,6 +209,43 @@ inline int current_device() {
   return d;
 }
 
+// ---- side streams ---------------------------------------------------------------
+
+// Independent tables (merged groups, logical ranks) each run a chain of small
+// latency-bound launches: they run side by side on the library's side streams
+// of the current device (created on first use, kept until exit), forked from
+// the caller's stream by an event and joined back into it before the call
+// returns (under stream capture: parallel branches of the graph).
+constexpr int kSideStreams = 4;
+cudaError_t side_streams(cudaStream_t* out);
+// Work enqueued on side[0 .. k) from now on waits for everything enqueued on s so far.
+cudaError_t fork_streams(cudaStream_t s, const cudaStream_t* side, int k);
+// Work enqueued on s from now on waits for everything enqueued on side[0 .. k) so far.
+cudaError_t join_streams(cudaStream_t s, const cudaStream_t* side, int k);
+
+// Where the work of the i-th table with work goes: a side stream when several
+// tables have work, else the caller's stream.
+struct GroupStreams {
+  cudaStream_t caller = nullptr;
+  cudaStream_t side[kSideStreams] = {};
+  int used = 0;  // side streams forked
+  cudaError_t begin(cudaStream_t s, int active) {
+    caller = s;
+    used = 0;
+    if (active < 2) return cudaSuccess;
+    const cudaError_t e = side_streams(side);
+    if (e != cudaSuccess) return e;
+    used = active < kSideStreams ? active : kSideStreams;
+    return fork_streams(s, side, used);
+  }
+  cudaStream_t stream(int slot) const { return used ? side[slot % used] : caller; }
+  cudaError_t end() {
+    const cudaError_t e = used ? join_streams(caller, side, used) : cudaSuccess;
+    used = 0;
+    return e;
+  }
+};
+
 // Streaming multiprocessors of the current device (queried once per device).
 int sm_count();
 

@@ -40,16 +40,13 @@ __global__ void __launch_bounds__(256) k_route(const long long* ids, long long* 
   }
 }
 
-// The merged tables are independent, and each one's lookup (or backward) is
-// a chain of small latency-bound launches: the groups run side by side on the
-// library's side streams, forked from the caller's stream by an event and
-// joined back into it before the call returns (under stream capture this
-// becomes parallel branches of the graph).
-constexpr int kSideStreams = 4;
+}  // namespace
+
+// The library's side streams (one set per device, kept until exit) and the
+// event fork/join that orders them with the caller's stream.
 std::mutex g_side_mu;
 cudaStream_t g_side[kMaxDevices][kSideStreams] = {};
 
-// The side streams of the current device, created on first use (non-blocking).
 cudaError_t side_streams(cudaStream_t* out) {
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
@@ -64,7 +61,6 @@ cudaError_t side_streams(cudaStream_t* out) {
   return cudaSuccess;
 }
 
-// Work enqueued on side[0 .. k) from now on waits for everything enqueued on s so far.
 cudaError_t fork_streams(cudaStream_t s, const cudaStream_t* side, int k) {
   cudaEvent_t ev;
   cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
@@ -75,7 +71,6 @@ cudaError_t fork_streams(cudaStream_t s, const cudaStream_t* side, int k) {
   return e;
 }
 
-// Work enqueued on s from now on waits for everything enqueued on side[0 .. k) so far.
 cudaError_t join_streams(cudaStream_t s, const cudaStream_t* side, int k) {
   cudaError_t first = cudaSuccess;
   for (int i = 0; i < k; ++i) {
@@ -91,25 +86,6 @@ cudaError_t join_streams(cudaStream_t s, const cudaStream_t* side, int k) {
   return first;
 }
 
-// Where group g's work goes: its own side stream when several groups have
-// work, else the caller's stream.
-struct GroupStreams {
-  cudaStream_t caller;
-  cudaStream_t side[kSideStreams];
-  int used = 0;  // side streams forked
-  cudaError_t begin(cudaStream_t s, int active) {
-    caller = s;
-    if (active < 2) return cudaSuccess;
-    const cudaError_t e = side_streams(side);
-    if (e != cudaSuccess) return e;
-    used = active < kSideStreams ? active : kSideStreams;
-    return fork_streams(s, side, used);
-  }
-  cudaStream_t stream(int slot) const { return used ? side[slot % used] : caller; }
-  cudaError_t end() { return used ? join_streams(caller, side, used) : cudaSuccess; }
-};
-
-}  // namespace
 }  // namespace mt
 
 extern "C" {

@@ -158,7 +158,11 @@ struct ShardLayout {
       gsum2, idx, scratch, total;
 };
 
-ShardLayout shard_layout(long long ntot, long long nmax, uint32_t dim, uint32_t rec_emb_bytes) {
+// The scratch holds one lookup (or backward) workspace per rank, or per owner,
+// side by side: their batches add up to at most ntot IDs, and splitting a
+// batch costs at most one tile's workspace per part (a tile's rounding, the
+// scratch hash's rounding, the arrays' alignment).
+ShardLayout shard_layout(int G, long long ntot, long long nmax, uint32_t dim, uint32_t rec_emb_bytes) {
   ShardLayout L{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -185,7 +189,8 @@ ShardLayout shard_layout(long long ntot, long long nmax, uint32_t dim, uint32_t 
   L.idx = take(nt * 4);
   const long long big = ntot > nmax ? ntot : nmax;
   const size_t lw = lookup_ws_layout(big).total, bw = backward_ws_layout(big, dim).total;
-  L.scratch = take(lw > bw ? lw : bw);
+  const size_t lt = lookup_ws_layout(kTile).total, bt = backward_ws_layout(kTile, dim).total;
+  L.scratch = take(align_up(lw > bw ? lw : bw, 256) + (size_t)G * align_up(lt > bt ? lt : bt, 256));
   L.total = off;
   return L;
 }
@@ -266,7 +271,7 @@ size_t mt_shard_workspace_bytes(const mt_shard_group* g, const int64_t* n) {
   long long base[MT_MAX_SHARDS], ntot, nmax;
   if (!batch_sizes(g, n, base, &ntot, &nmax)) return 0;
   const mt::TableDev& T = mt::table_dev(g->shards[0]);
-  return mt::shard_layout(ntot, nmax, T.dim, T.emb_bytes).total;
+  return mt::shard_layout(g->G, ntot, nmax, T.dim, T.emb_bytes).total;
 }
 
 int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t* n, const int64_t* feat_offsets,
@@ -279,7 +284,7 @@ int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t*
   if (feat_offsets == nullptr) F = 1;
   if (F < 1 || F > MT_MAX_FEATURES) return MT_EINVAL;
   const mt::TableDev& T0 = mt::table_dev(g->shards[0]);
-  const mt::ShardLayout L = mt::shard_layout(ntot, nmax, T0.dim, T0.emb_bytes);
+  const mt::ShardLayout L = mt::shard_layout(G, ntot, nmax, T0.dim, T0.emb_bytes);
   if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return MT_ENOSPACE;
   for (int r = 0; r < G; ++r) {
     const mt_lookup_result& R = results[r];
@@ -297,31 +302,62 @@ int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t*
   char* scratch = w + L.scratch;
   g->have_lookup = false;
 
-  // 1. stage 1 on every rank: dedup only (first occurrence), no table access
-  for (int r = 0; r < G; ++r) {
-    mt::LookupParams p = lookup_params(mt::table_dev(g->shards[r]), reinterpret_cast<const long long*>(ids[r]), n[r],
-                                       scratch);
-    p.F = F;
-    if (feat_offsets == nullptr) {
-      p.feat_off[0] = 0;
-      p.feat_off[1] = n[r];
-    } else {
+  if (feat_offsets != nullptr) {  // every rank's feature offsets are checked before anything is enqueued
+    for (int r = 0; r < G; ++r) {
       const int64_t* fo = feat_offsets + (size_t)r * (F + 1);
       if (fo[0] != 0 || fo[F] != n[r]) return MT_EINVAL;
-      for (int f = 0; f <= F; ++f) {
-        if (f > 0 && fo[f] < fo[f - 1]) return MT_EINVAL;
-        p.feat_off[f] = fo[f];
-      }
+      for (int f = 1; f <= F; ++f)
+        if (fo[f] < fo[f - 1]) return MT_EINVAL;
     }
-    for (int f = 0; f < F; ++f) p.table_ids[f] = tid[f];
-    p.no_table = 1;
-    p.unique_keys = reinterpret_cast<unsigned long long*>(results[r].unique_keys);
-    p.inverse = results[r].inverse;
-    p.counts = results[r].counts;
-    p.unique_rows = results[r].unique_rows;
-    p.num_unique = reinterpret_cast<long long*>(results[r].num_unique);
-    p.ranks = results[r].ranks;
-    if (mt::launch_lookup(p, s) != cudaSuccess) return MT_ECUDA;
+  }
+  const size_t scratch_bytes = L.total - L.scratch;
+  // each rank's (or owner's) own slice of the scratch: offsets of lookup workspaces side by side
+  auto lookup_slices = [&](const long long* sizes, size_t* off) -> bool {
+    size_t o = 0;
+    for (int r = 0; r < G; ++r) {
+      off[r] = o;
+      if (sizes[r] > 0) o = align_up(o + mt::lookup_ws_layout(sizes[r]).total, 256);
+    }
+    return o <= scratch_bytes;
+  };
+  size_t soff[MT_MAX_SHARDS];
+  long long nn[MT_MAX_SHARDS];
+  int active = 0;
+  for (int r = 0; r < G; ++r) {
+    nn[r] = n[r];
+    active += n[r] > 0;
+  }
+  if (!lookup_slices(nn, soff)) return MT_ENOSPACE;
+
+  // 1. stage 1 on every rank, the ranks side by side: dedup only (first occurrence), no table access
+  {
+    mt::GroupStreams gs;
+    if (gs.begin(s, active) != cudaSuccess) return MT_ECUDA;
+    int rc = MT_OK, slot = 0;
+    for (int r = 0; r < G && rc == MT_OK; ++r) {
+      const cudaStream_t sr = n[r] > 0 ? gs.stream(slot++) : s;
+      mt::LookupParams p = lookup_params(mt::table_dev(g->shards[r]), reinterpret_cast<const long long*>(ids[r]),
+                                         n[r], scratch + soff[r]);
+      p.F = F;
+      if (feat_offsets == nullptr) {
+        p.feat_off[0] = 0;
+        p.feat_off[1] = n[r];
+      } else {
+        const int64_t* fo = feat_offsets + (size_t)r * (F + 1);
+        for (int f = 0; f <= F; ++f) p.feat_off[f] = fo[f];
+      }
+      for (int f = 0; f < F; ++f) p.table_ids[f] = tid[f];
+      p.no_table = 1;
+      p.unique_keys = reinterpret_cast<unsigned long long*>(results[r].unique_keys);
+      p.inverse = results[r].inverse;
+      p.counts = results[r].counts;
+      p.unique_rows = results[r].unique_rows;
+      p.num_unique = reinterpret_cast<long long*>(results[r].num_unique);
+      p.ranks = results[r].ranks;
+      if (mt::launch_lookup(p, sr) != cudaSuccess) rc = MT_ECUDA;
+    }
+    if (gs.end() != cudaSuccess && rc == MT_OK) rc = MT_ECUDA;  // joined also after an error
+    if (rc != MT_OK) return rc;
   }
   // 2. the partition counts, read on the host as the sizes of the exchange
   long long U[MT_MAX_SHARDS];
@@ -362,26 +398,38 @@ int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t*
                                                        U[r], G, r, off, cursor, recv_keys, t, perm + base[r],
                                                        mt::table_dev(g->shards[r]).hdr);
   }
-  // 4. stage 2 at every owner: dedup what arrived, find or insert in the shard, gather one row per received key
+  // 4. stage 2 at every owner, the owners side by side: dedup what arrived, find or insert in the shard, gather
+  //    one row per received key
   char* recv_rows = w + L.recv_rows;
   const int vec16 = (int)(T0.emb_bytes / 16);
-  for (int o = 0; o < G; ++o) {
-    const long long rb = recv_base[o];
-    mt::LookupParams p = lookup_params(mt::table_dev(g->shards[o]), reinterpret_cast<const long long*>(recv_keys + rb),
-                                       N[o], scratch);
-    p.F = 1;
-    p.feat_off[0] = 0;
-    p.feat_off[1] = N[o];
-    p.keys_in = 1;
-    p.insert_missing = insert_missing ? 1 : 0;
-    p.out_rows = recv_rows + (size_t)rb * T0.emb_bytes;
-    p.unique_keys = reinterpret_cast<unsigned long long*>(w + L.uk2) + rb;
-    p.inverse = reinterpret_cast<int32_t*>(w + L.inv2) + rb;
-    p.counts = reinterpret_cast<int32_t*>(w + L.cnt2) + rb;
-    p.unique_rows = reinterpret_cast<int32_t*>(w + L.rows2) + rb;
-    p.num_unique = reinterpret_cast<long long*>(w + L.nu2) + o;
-    p.ranks = reinterpret_cast<int32_t*>(w + L.rank2) + rb;
-    if (mt::launch_lookup(p, s) != cudaSuccess) return MT_ECUDA;
+  {
+    if (!lookup_slices(N, soff)) return MT_ENOSPACE;
+    int owners = 0;
+    for (int o = 0; o < G; ++o) owners += N[o] > 0;
+    mt::GroupStreams gs;
+    if (gs.begin(s, owners) != cudaSuccess) return MT_ECUDA;
+    int rc = MT_OK, slot = 0;
+    for (int o = 0; o < G && rc == MT_OK; ++o) {
+      const cudaStream_t so = N[o] > 0 ? gs.stream(slot++) : s;
+      const long long rb = recv_base[o];
+      mt::LookupParams p = lookup_params(mt::table_dev(g->shards[o]), reinterpret_cast<const long long*>(recv_keys + rb),
+                                         N[o], scratch + soff[o]);
+      p.F = 1;
+      p.feat_off[0] = 0;
+      p.feat_off[1] = N[o];
+      p.keys_in = 1;
+      p.insert_missing = insert_missing ? 1 : 0;
+      p.out_rows = recv_rows + (size_t)rb * T0.emb_bytes;
+      p.unique_keys = reinterpret_cast<unsigned long long*>(w + L.uk2) + rb;
+      p.inverse = reinterpret_cast<int32_t*>(w + L.inv2) + rb;
+      p.counts = reinterpret_cast<int32_t*>(w + L.cnt2) + rb;
+      p.unique_rows = reinterpret_cast<int32_t*>(w + L.rows2) + rb;
+      p.num_unique = reinterpret_cast<long long*>(w + L.nu2) + o;
+      p.ranks = reinterpret_cast<int32_t*>(w + L.rank2) + rb;
+      if (mt::launch_lookup(p, so) != cudaSuccess) rc = MT_ECUDA;
+    }
+    if (gs.end() != cudaSuccess && rc == MT_OK) rc = MT_ECUDA;
+    if (rc != MT_OK) return rc;
   }
   // 5. rows back to the ranks, then each rank expands them to its positions
   char* uniq_rows = w + L.uniq_rows;
@@ -430,7 +478,7 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
     if (gsum_out != nullptr && gsum_out[r] != nullptr && !aligned(gsum_out[r], 16)) return MT_EINVAL;
   }
   const mt::TableDev& T0 = mt::table_dev(g->shards[0]);
-  const mt::ShardLayout L = mt::shard_layout(g->ntot, nmax, T0.dim, T0.emb_bytes);
+  const mt::ShardLayout L = mt::shard_layout(G, g->ntot, nmax, T0.dim, T0.emb_bytes);
   if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return MT_ENOSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
@@ -442,7 +490,7 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
   const int32_t* perm = reinterpret_cast<const int32_t*>(w + L.perm);
 
   auto run = [&](mt_table* shard, const mt_lookup_result& R, long long n, const void* gr, int gd, float* out,
-                 int reduce_only) -> int {
+                 int reduce_only, char* scr, cudaStream_t st) -> int {
     const mt::TableDev& T = mt::table_dev(shard);
     const mt::BackwardWsLayout BL = mt::backward_ws_layout(n, T.dim);
     mt::BackwardParams p;
@@ -465,16 +513,40 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
     p.one_minus_b2 = (float)(1.0 - (double)hp->beta2);
     p.gsum_out = out;
     p.reduce_only = reduce_only;
-    mt::bind_backward_ws(p, scratch, BL);
+    mt::bind_backward_ws(p, scr, BL);
     p.team_shift = mt::backward_team_shift(T.dim, T.row_dtype);
     p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
-    return mt::launch_backward(p, s) == cudaSuccess ? MT_OK : MT_ECUDA;
+    return mt::launch_backward(p, st) == cudaSuccess ? MT_OK : MT_ECUDA;
   };
+  // each rank's (or owner's) own slice of the scratch: offsets of backward workspaces side by side
+  const size_t scratch_bytes = L.total - L.scratch;
+  // (an owner that received nothing still runs its backward, which advances its step counter, so every one
+  // gets a slice)
+  auto backward_slices = [&](const long long* sizes, size_t* off, int* active) -> bool {
+    size_t o = 0;
+    *active = 0;
+    for (int r = 0; r < G; ++r) {
+      off[r] = o;
+      o = align_up(o + mt::backward_ws_layout(sizes[r], T0.dim).total, 256);
+      *active += sizes[r] > 0;
+    }
+    return o <= scratch_bytes;
+  };
+  size_t soff[MT_MAX_SHARDS];
+  int active = 0;
 
-  // 1. every rank: per-unique sums of its positions' gradients (no Adam)
-  for (int r = 0; r < G; ++r) {
-    if (g->n[r] == 0) continue;
-    const int rc = run(g->shards[r], results[r], g->n[r], grads[r], grad_dtype, gsum + (size_t)g->rank_base[r] * d, 1);
+  // 1. every rank, the ranks side by side: per-unique sums of its positions' gradients (no Adam)
+  {
+    if (!backward_slices(g->n, soff, &active)) return MT_ENOSPACE;
+    mt::GroupStreams gs;
+    if (gs.begin(s, active) != cudaSuccess) return MT_ECUDA;
+    int rc = MT_OK, slot = 0;
+    for (int r = 0; r < G && rc == MT_OK; ++r) {
+      if (g->n[r] == 0) continue;
+      rc = run(g->shards[r], results[r], g->n[r], grads[r], grad_dtype, gsum + (size_t)g->rank_base[r] * d, 1,
+               scratch + soff[r], gs.stream(slot++));
+    }
+    if (gs.end() != cudaSuccess && rc == MT_OK) rc = MT_ECUDA;  // joined also after an error
     if (rc != MT_OK) return rc;
   }
   // 2. the sums go to the owners (the exchange of the forward, reversed)
@@ -485,20 +557,30 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
         reinterpret_cast<const uint4*>(gsum + (size_t)g->rank_base[r] * d), perm + g->rank_base[r], g->U[r], gvec,
         reinterpret_cast<uint4*>(recv_g), g->ntot);
   }
-  // 3. every owner: sums over the ranks per key, one Adam step on its shard (its step counter advances once)
+  // 3. every owner, the owners side by side: sums over the ranks per key, one Adam step on its shard (its step
+  //    counter advances once)
   float* gsum2 = reinterpret_cast<float*>(w + L.gsum2);
-  for (int o = 0; o < G; ++o) {
-    const long long rb = g->recv_base[o];
-    mt_lookup_result R2;
-    R2.unique_keys = reinterpret_cast<uint64_t*>(w + L.uk2) + rb;
-    R2.inverse = reinterpret_cast<int32_t*>(w + L.inv2) + rb;
-    R2.counts = reinterpret_cast<int32_t*>(w + L.cnt2) + rb;
-    R2.unique_rows = reinterpret_cast<int32_t*>(w + L.rows2) + rb;
-    R2.num_unique = reinterpret_cast<int64_t*>(w + L.nu2) + o;
-    R2.ranks = reinterpret_cast<int32_t*>(w + L.rank2) + rb;
-    const int rc = run(g->shards[o], R2, g->N[o], recv_g + (size_t)rb * d, MT_F32, gsum2 + (size_t)rb * d, 0);
+  {
+    if (!backward_slices(g->N, soff, &active)) return MT_ENOSPACE;
+    mt::GroupStreams gs;
+    if (gs.begin(s, active) != cudaSuccess) return MT_ECUDA;
+    int rc = MT_OK, slot = 0;
+    for (int o = 0; o < G && rc == MT_OK; ++o) {
+      const long long rb = g->recv_base[o];
+      mt_lookup_result R2;
+      R2.unique_keys = reinterpret_cast<uint64_t*>(w + L.uk2) + rb;
+      R2.inverse = reinterpret_cast<int32_t*>(w + L.inv2) + rb;
+      R2.counts = reinterpret_cast<int32_t*>(w + L.cnt2) + rb;
+      R2.unique_rows = reinterpret_cast<int32_t*>(w + L.rows2) + rb;
+      R2.num_unique = reinterpret_cast<int64_t*>(w + L.nu2) + o;
+      R2.ranks = reinterpret_cast<int32_t*>(w + L.rank2) + rb;
+      const cudaStream_t so = g->N[o] > 0 ? gs.stream(slot++) : s;
+      rc = run(g->shards[o], R2, g->N[o], recv_g + (size_t)rb * d, MT_F32, gsum2 + (size_t)rb * d, 0,
+               scratch + soff[o], so);
+      if (rc == MT_OK) mt::table_count_step(g->shards[o]);
+    }
+    if (gs.end() != cudaSuccess && rc == MT_OK) rc = MT_ECUDA;
     if (rc != MT_OK) return rc;
-    mt::table_count_step(g->shards[o]);
   }
   // 4. asked for: each rank's per-unique sums over all ranks, from the owners
   if (gsum_out != nullptr) {
