@@ -407,7 +407,10 @@ size_t mt_shard_workspace_bytes(const mt_shard_group* g, const int64_t* n);
  *               first-occurrence order of its own batch, inverse, counts,
  *               ranks (nullable) and num_unique; unique_rows are set to -1
  *               (the rows live in the owners' shards).
- * The rows a rank receives equal what one table holding every key would give. */
+ * The rows a rank receives equal what one table holding every key would give.
+ * The ranks' stage-1 lookups, and then the owners' stage-2 lookups, run side by
+ * side on the library's side streams (as in mt_lookup_grouped), joined back
+ * into `stream`; the host reads of the exchange sizes synchronise it. */
 int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t* n, const int64_t* feat_offsets,
                     const uint8_t* table_ids, int F, int insert_missing, void* const* out_rows,
                     const mt_lookup_result* results, void* ws, size_t ws_bytes, mt_stream stream);
@@ -416,7 +419,9 @@ int mt_shard_lookup(mt_shard_group* g, const int64_t* const* ids, const int64_t*
  * host array of G device pointers [n[r], d] of grad_dtype.  Every key's
  * gradient is summed over all positions of all ranks (rank sums rounded to
  * fp32, then summed exactly at the owner and rounded once), then one Adam step
- * is applied by its owner; every shard's step counter advances once.
+ * is applied by its owner; every shard's step counter advances once.  The
+ * ranks' sums, and then the owners' Adam steps, run side by side on the side
+ * streams, joined back into `stream`.
  *  gsum_out  NULL, or a host array of G device pointers fp32 [U_r, d] (entries
  *            may be NULL): rank r's unique keys' sums over all ranks. */
 int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, const void* const* grads,
