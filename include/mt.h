@@ -340,11 +340,14 @@ size_t mt_lookup_grouped_workspace_bytes(int64_t n, int F);
  *  results      host array [G], each of capacity >= the group's IDs.
  *  group_n      host int64 [G]: receives each group's number of IDs.
  * When more than one group receives IDs, the groups run side by side on the
- * library's own side streams of the current device (up to four, created on
- * the first such call and kept until the process exits): they wait for the
- * work enqueued on `stream` before the call, and work enqueued on `stream`
- * after the call waits for all of them, also when the call returns an error.
- * Under stream capture this records parallel branches of the graph.
+ * library's own side streams of the current device: up to four per host
+ * thread, so that calls from different threads (or one thread's stream
+ * capture) never share one; a thread's streams are created on its first such
+ * call, go back to a pool when it exits and are kept until the process exits.
+ * They wait for the work enqueued on `stream` before the call, and work
+ * enqueued on `stream` after the call waits for all of them, also when the
+ * call returns an error.  Under stream capture this records parallel branches
+ * of the graph.
  * The backward of group g is mt_backward_adam(tables[g], &results[g],
  * group_n[g], ...) with that group's gradient rows, or all groups at once with
  * mt_backward_adam_grouped. */

@@ -164,3 +164,57 @@ def test_grouped_calls_replay_as_cuda_graphs():
         k_g, _ = tg.export()
         assert np.array_equal(np.sort(k_e.cpu().numpy()), np.sort(k_g.cpu().numpy()))
         assert te.step == tg.step == 3 and te.error() == 0 and tg.error() == 0
+
+
+def test_grouped_calls_from_two_host_threads():
+    """Two host threads run grouped lookups and backward steps at the same time, each on its own merged tables
+    and its own stream (each thread has its own side streams); every result and every table equals the same
+    steps run one thread after the other on twin tables."""
+    import threading
+
+    def run(mtabs, steps, seed0, out):
+        s = torch.cuda.Stream(device=mtabs.device)
+        with torch.cuda.stream(s):
+            for j in range(steps):
+                ids, offs = batch(seed0 + j)
+                res = mtabs.lookup(torch.from_numpy(ids).to(mtabs.device), offs)
+                grads = [torch.from_numpy(W.grads_normal(seed0 + 7 * j + g, sz, mtabs.groups[g]["dim"])).to(mtabs.device)
+                         for g, sz in enumerate(mtabs.group_sizes(offs))]
+                mtabs.backward_adam(res, grads)
+                out.append([(r.U, r.unique_keys[:r.U].clone(), r.inverse[:r.n].clone(), r.rows.clone()) for r in res])
+        s.synchronize()
+
+    seeds = (40, 60)
+    twins = [mt.MergedTables(FEATURES, max_load=0.5, init_seed=s) for s in seeds]
+    want = [[], []]
+    for k in range(2):
+        run(twins[k], 3, seeds[k], want[k])
+    tabs = [mt.MergedTables(FEATURES, max_load=0.5, init_seed=s) for s in seeds]
+    got = [[], []]
+    errs = []
+
+    def worker(k):
+        try:
+            run(tabs[k], 3, seeds[k], got[k])
+        except Exception as e:  # surfaced below
+            errs.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errs, errs
+    torch.cuda.synchronize()
+    for k in range(2):
+        assert len(got[k]) == len(want[k]) == 3
+        for gs, ws in zip(got[k], want[k]):
+            for (gu, gk, gi, gr), (wu, wk, wi, wr) in zip(gs, ws):
+                assert gu == wu and torch.equal(gk, wk) and torch.equal(gi, wi) and torch.equal(gr, wr)
+        for tg, tw in zip(tabs[k].tables, twins[k].tables):
+            kg, rg = tg.export()
+            kw, rw = tw.export()
+            og, ow = torch.argsort(kg), torch.argsort(kw)
+            assert torch.equal(kg[og], kw[ow])
+            assert torch.equal(tg.read_rows(rg[og])[0], tw.read_rows(rw[ow])[0])
+            assert tg.step == tw.step == 3 and tg.error() == 0 and tw.error() == 0

@@ -100,6 +100,33 @@ def test_pooled_fp32_edge_bags():
         ref.error  # noqa: B018
 
 
+@pytest.mark.parametrize("dim,row_dtype", [(16, "f32"), (64, "bf16")])
+def test_pooled_many_small_and_empty_bags(dim, row_dtype):
+    """Bags of 0 to 3 positions (far more than 32 bags meet one chunk, so the kernel walks several windows of
+    offsets), runs of empty bags on chunk boundaries, bags that end exactly on a boundary, one long bag over
+    several chunks and positions after the last bag, for sum and mean."""
+    rng = np.random.default_rng(21)
+    n = 3000
+    ids = rng.integers(0, 700, size=n).astype(np.int64)
+    lens = rng.choice([0, 0, 1, 2, 3], size=700)
+    bo = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)  # ends near position 1050
+    tail = bo[-1]
+    extra = [128 * k for k in range(tail // 128 + 1, tail // 128 + 4) for _ in range(3)]  # empties on boundaries
+    bo = np.concatenate([bo, np.maximum(extra, tail), [2000, 2000, 2600]]).astype(np.int64)
+    assert (np.diff(bo) >= 0).all() and bo[-1] < n
+    tab = mt.Table(13, dim, row_dtype=row_dtype)
+    ref = oracle.Table(13, dim, row_dtype=oracle.BF16 if row_dtype == "bf16" else oracle.F32)
+    b = W.single_feature(ids)
+    res = tab.lookup(to_dev(b.ids), gather=False)
+    ref.lookup(b.ids, gather=False)
+    for mode in ("sum", "mean"):
+        got = tab.pool_forward(res, to_dev(bo), mode=mode).cpu().numpy()
+        want = ref.pool_forward(bo, mode=1 if mode == "mean" else 0)
+        np.testing.assert_allclose(got, want, rtol=RTOL, atol=ATOL)
+        assert not got[np.diff(bo) == 0].any()  # empty bags are zeros
+    assert tab.error() == 0 and ref.error == 0
+
+
 def test_pooled_backward_equals_expanded_backward():
     """The pooled backward (sum) equals the per-position backward fed the bag gradients expanded to their
     positions, bit for bit: the same rows are summed in the same order."""

@@ -213,9 +213,10 @@ inline int current_device() {
 
 // Independent tables (merged groups, logical ranks) each run a chain of small
 // latency-bound launches: they run side by side on the library's side streams
-// of the current device (created on first use, kept until exit), forked from
-// the caller's stream by an event and joined back into it before the call
-// returns (under stream capture: parallel branches of the graph).
+// of the current device and host thread (created on first use, pooled when the
+// thread exits, never destroyed), forked from the caller's stream by an event
+// and joined back into it before the call returns (under stream capture:
+// parallel branches of the graph).
 constexpr int kSideStreams = 4;
 cudaError_t side_streams(cudaStream_t* out);
 // Work enqueued on side[0 .. k) from now on waits for everything enqueued on s so far.

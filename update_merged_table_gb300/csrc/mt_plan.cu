@@ -42,22 +42,63 @@ __global__ void __launch_bounds__(256) k_route(const long long* ids, long long* 
 
 }  // namespace
 
-// The library's side streams (one set per device, kept until exit) and the
-// event fork/join that orders them with the caller's stream.
-std::mutex g_side_mu;
-cudaStream_t g_side[kMaxDevices][kSideStreams] = {};
+// The library's side streams: one set of kSideStreams per device and host
+// thread, so that a call on one thread (or a stream capture it is making)
+// never enqueues onto a stream that another thread's call is using.  When a
+// thread exits, its sets go back to a pool that later threads draw from;
+// streams are never destroyed.  The pool and its lock are never freed, so a
+// thread may exit at any point of the process's shutdown.
+namespace {
+struct SideSet {
+  cudaStream_t s[kSideStreams];
+};
+std::mutex& side_pool_mu() {
+  static std::mutex* m = new std::mutex;
+  return *m;
+}
+std::vector<SideSet>* side_pool() {  // [kMaxDevices]
+  static std::vector<SideSet>* v = new std::vector<SideSet>[kMaxDevices];
+  return v;
+}
+struct ThreadSides {
+  SideSet set[kMaxDevices] = {};
+  bool have[kMaxDevices] = {};
+  ~ThreadSides() {
+    std::lock_guard<std::mutex> lk(side_pool_mu());
+    for (int d = 0; d < kMaxDevices; ++d)
+      if (have[d]) side_pool()[d].push_back(set[d]);
+  }
+};
+thread_local ThreadSides t_sides;
+}  // namespace
 
 cudaError_t side_streams(cudaStream_t* out) {
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_side_mu);
-  for (int k = 0; k < kSideStreams; ++k) {
-    if (g_side[dev][k] == nullptr) {
-      const cudaError_t e = cudaStreamCreateWithFlags(&g_side[dev][k], cudaStreamNonBlocking);
-      if (e != cudaSuccess) return e;
+  ThreadSides& ts = t_sides;
+  if (!ts.have[dev]) {
+    SideSet x{};
+    bool pooled = false;
+    {
+      std::lock_guard<std::mutex> lk(side_pool_mu());
+      std::vector<SideSet>& v = side_pool()[dev];
+      if (!v.empty()) {
+        x = v.back();
+        v.pop_back();
+        pooled = true;
+      }
     }
-    out[k] = g_side[dev][k];
+    for (int k = 0; k < kSideStreams && !pooled; ++k) {
+      const cudaError_t e = cudaStreamCreateWithFlags(&x.s[k], cudaStreamNonBlocking);
+      if (e != cudaSuccess) {
+        for (int q = 0; q < k; ++q) cudaStreamDestroy(x.s[q]);
+        return e;
+      }
+    }
+    ts.set[dev] = x;
+    ts.have[dev] = true;
   }
+  for (int k = 0; k < kSideStreams; ++k) out[k] = ts.set[dev].s[k];
   return cudaSuccess;
 }
 

@@ -10,13 +10,14 @@
 // ever written.
 //
 // Kernels:
-//  k_pool         positions in chunks of kPoolChunk, a team of lanes per
-//                 chunk (one 16-byte vector of a row per lane, two rows in
-//                 flight), rows summed as exact fp32 pairs (TwoSum on the
-//                 paired fp32 instructions, two columns each); the
-//                 chunk's first bag comes from a team-wide multiway search of
-//                 the offsets; a bag that lies inside one chunk is written at
-//                 once, the pieces of a longer bag meet in an fp64
+//  k_pool         a warp per chunk of kPoolChunk positions: the chunk's row
+//                 indices fetched in one round, its first bag by a warp-wide
+//                 multiway search of the offsets; each bag's positions split
+//                 over the warp's sub-teams (one 16-byte vector of a row per
+//                 lane), rows summed as exact fp32 pairs (TwoSum on the paired
+//                 fp32 instructions, two columns each) and the sub-teams'
+//                 pairs joined by TwoSums; a bag that lies inside one chunk is
+//                 written at once, the pieces of a longer bag meet in an fp64
 //                 accumulator.
 //  k_pool_finish  bags split over chunks (and empty bags): rounded from the
 //                 fp64 accumulator.
@@ -29,8 +30,9 @@ namespace mt {
 
 namespace {
 
-constexpr int kPoolChunk = 64;        // positions per chunk (one team)
-constexpr int kPoolMinTeamShift = 2;  // teams of at least 4 lanes
+constexpr int kPoolChunk = 128;                // positions per chunk (one warp)
+constexpr int kPoolRows = kPoolChunk / 32;     // row indices each lane fetches per chunk
+constexpr int kPoolUnroll = 4;                 // rows in flight per lane
 
 // Round a bag's sum (or mean) from double to fp32 into out[b, col .. col + VEC).
 template <int VEC>
@@ -66,27 +68,38 @@ __device__ __forceinline__ long long bag_search(const long long* bo, long long B
   return lo;
 }
 
+// A warp per chunk of kPoolChunk positions.  The warp fetches the chunk's
+// row indices in one round (kPoolRows positions per lane, inverse and then
+// unique_rows, into shared memory) while it searches for the chunk's first
+// bag, then walks the bags that meet the chunk with a window of 32 offsets
+// held one per lane.  A bag's positions in the chunk are split over the
+// warp's S = 32 / team sub-teams (position q goes to sub-team q mod S), each
+// lane adding one 16-byte vector of a row per position, kPoolUnroll rows in
+// flight, as exact fp32 pairs (TwoSum on the paired instructions).  The
+// sub-teams' pairs meet by a butterfly of TwoSums, and sub-team 0 writes the
+// bag when the whole bag lies in the chunk, else adds it to the bag's fp64
+// accumulator.  A pair's exact sum is rounded to fp32 by one fp32 add
+// (correctly rounded); only the mean divides, in double.
 template <int RD>
 __global__ void __launch_bounds__(256, 4) k_pool(const PoolParams p) {
   constexpr int VEC = RD == MT_F32 ? 4 : 8;  // columns per lane: one 16-byte load of a row
   constexpr int NP = VEC / 2;                // column pairs per lane
-  constexpr int UNR = 2;                     // rows in flight per lane
-  __shared__ int32_t s_row[(256 >> kPoolMinTeamShift) * kPoolChunk];  // per team: the rows of its chunk
+  __shared__ int32_t s_row[256 / 32][kPoolChunk];  // per warp: the rows of its chunk (-1: nothing to add)
+  const int lane = threadIdx.x & 31;
   const int team_shift = p.team_shift;
   const int team = 1 << team_shift;
-  const int lane = threadIdx.x & 31;
   const int lt = lane & (team - 1);
-  const int team_base = lane & ~(team - 1);
-  const unsigned team_mask = team == 32 ? kFull : (((1u << team) - 1u) << team_base);
-  int32_t* my_row = s_row + (threadIdx.x >> team_shift) * kPoolChunk;
+  const int sub = lane >> team_shift;  // sub-team
+  const int S = 32 >> team_shift;      // sub-teams per warp
+  int32_t* my_row = s_row[threadIdx.x >> 5];
   // positions, bags and unique indices fit in int (the entry point admits n, B < 2^31)
   const int n = (int)p.n;
   const int B = (int)p.num_bags;
   const int U = (int)*p.num_unique;
   const int d = (int)p.T.dim;
   const int nchunks = (n + kPoolChunk - 1) / kPoolChunk;
-  const int gteam = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> team_shift);
-  const int nteam = (int)((gridDim.x * blockDim.x) >> team_shift);
+  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int nw = (int)((gridDim.x * blockDim.x) >> 5);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   // a bag offset relative to the chunk start p0, clamped to [-1, kPoolChunk + 1]: the comparisons with
   // the chunk's positions [0, cnt) stay exact
@@ -94,85 +107,109 @@ __global__ void __launch_bounds__(256, 4) k_pool(const PoolParams p) {
     const long long r = x - p0;
     return r < 0 ? -1 : (r > kPoolChunk ? kPoolChunk + 1 : (int)r);
   };
+  // lane k's entry of the offsets window based at bag w: bo[w + k] relative to p0 (bo[-1] = -inf,
+  // bo[i > B] = +inf)
+  auto window = [&](int w, int p0) -> int {
+    const int i = w + lane;
+    return i < 0 ? -1 : (i <= B ? rel(__ldg(&p.bag_offsets[i]), p0) : kPoolChunk + 1);
+  };
 
-  for (int c = gteam; c < nchunks; c += nteam) {  // uniform per team
+  for (int c = gw; c < nchunks; c += nw) {  // uniform per warp
     const int p0 = c * kPoolChunk;
     const int cnt = min(kPoolChunk, n - p0);
-    // the chunk's rows (-1: nothing to add)
-    for (int q = lt; q < cnt; q += team) {
-      const int32_t u = __ldg(&p.inverse[p0 + q]);
-      my_row[q] = (u >= 0 && u < U) ? __ldg(&p.unique_rows[u]) : -1;
+    int32_t inv[kPoolRows];
+#pragma unroll
+    for (int k = 0; k < kPoolRows; ++k) {
+      const int q = k * 32 + lane;
+      inv[k] = q < cnt ? __ldg(&p.inverse[p0 + q]) : -1;
     }
-    const int b_first = (int)bag_search(p.bag_offsets, B, p0, lt, team, team_mask, team_base);
-    // positions before the first bag belong to none
-    const int q_skip = b_first < 0 && B > 0 ? rel(__ldg(&p.bag_offsets[0]), p0) : 0;
-    __syncwarp(team_mask);
-    for (int c0 = 0; c0 < d; c0 += team * VEC) {
-      const int col = c0 + lt * VEC;
-      const bool active = col < d;
-      int b = b_first < 0 ? 0 : b_first;
-      int q_end = b < B ? rel(__ldg(&p.bag_offsets[b + 1]), p0) : cnt;  // end of bag b, chunk-relative
-      f32x2 hi[NP], lo[NP];
+    int b = (int)bag_search(p.bag_offsets, B, p0, lane, 32, kFull, 0);  // the chunk's first bag (-1: none yet)
 #pragma unroll
-      for (int j = 0; j < NP; ++j) hi[j] = lo[j] = 0ull;
-      // bag bb (ending at chunk-relative re) leaves the running pair, one column pair at a time: written out
-      // (rounded once) when the whole bag lies in this chunk, else added to its fp64 accumulator
-      auto flush = [&](int bb, int re) {
-        if (bb < 0 || bb >= B || !active) return;
-        const int rs = rel(__ldg(&p.bag_offsets[bb]), p0);
-        const bool whole = rs >= 0 && re <= cnt && re > rs;
+    for (int k = 0; k < kPoolRows; ++k) {
+      const int q = k * 32 + lane;
+      if (q < cnt) my_row[q] = (inv[k] >= 0 && inv[k] < U) ? __ldg(&p.unique_rows[inv[k]]) : -1;
+    }
+    int w0 = b;
+    int win = window(w0, p0);
+    __syncwarp();
+    // bag b covers the chunk's positions [qs, qe); b = -1 holds the positions before the first bag
+    for (int qs = 0; qs < cnt && b < B; ++b) {
+      if (b + 1 - w0 > 31) {  // the window is used up: the next 32 offsets
+        w0 = b;
+        win = window(w0, p0);
+      }
+      const int rs = __shfl_sync(kFull, win, b - w0);      // start of bag b, chunk-relative
+      const int re = __shfl_sync(kFull, win, b + 1 - w0);  // its end
+      const int qe = min(max(re, qs), cnt);
+      if (b >= 0 && qe > qs) {
+        const bool whole = rs >= 0 && re <= cnt && re > rs;  // the whole bag lies in this chunk
         const double len = (double)(re - rs);
+        for (int c0 = 0; c0 < d; c0 += team * VEC) {
+          const int col = c0 + lt * VEC;
+          const bool active = col < d;
+          f32x2 hi[NP], lo[NP];
 #pragma unroll
-        for (int j = 0; j < NP; ++j) {
-          const float2 h = upk(hi[j]), l = upk(lo[j]);
-          const double s0 = (double)h.x + (double)l.x, s1 = (double)h.y + (double)l.y;
-          if (whole) {
-            const bool mean = p.mode == MT_POOL_MEAN;
-            *reinterpret_cast<float2*>(p.out + (size_t)bb * d + col + 2 * j) =
-                make_float2((float)(mean ? s0 / len : s0), (float)(mean ? s1 / len : s1));
-          } else {
-            double* a = p.acc + (size_t)bb * d + col + 2 * j;
-            atomicAdd(a, s0);
-            atomicAdd(a + 1, s1);
+          for (int j = 0; j < NP; ++j) hi[j] = lo[j] = 0ull;
+          for (int q0 = qs + sub; q0 < qe; q0 += S * kPoolUnroll) {
+            uint4 raw[kPoolUnroll];  // every load of the round issued before the first add
+#pragma unroll
+            for (int r = 0; r < kPoolUnroll; ++r) {
+              const int q = q0 + r * S;
+              const int32_t row = q < qe ? my_row[q] : -1;
+              raw[r] = active && row >= 0 ? __ldg(reinterpret_cast<const uint4*>(row_ptr(p.T, row) + (size_t)col *
+                                                                                  (RD == MT_F32 ? 4 : 2)))
+                                          : zero;  // adding zero leaves a pair exactly as it is
+            }
+#pragma unroll
+            for (int r = 0; r < kPoolUnroll; ++r) {
+              const uint32_t w[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+#pragma unroll
+              for (int j = 0; j < NP; ++j) {
+                const f32x2 x = RD == MT_F32 ? pk(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1]))
+                                             : bf16x2_to_f32x2(w[j]);
+                f32x2 s, e;
+                two_sum(hi[j], x, s, e);
+                hi[j] = s;
+                lo[j] = add2(lo[j], e);
+              }
+            }
           }
-          hi[j] = lo[j] = 0ull;
-        }
-      };
-      for (int q0 = 0; q0 < cnt; q0 += UNR) {
-        uint4 raw[UNR];  // every load of the round issued before the first add
+          // the sub-teams' pairs meet: lane l and lane l ^ o hold the same columns
+          for (int o = team; o < 32; o <<= 1) {
 #pragma unroll
-        for (int r = 0; r < UNR; ++r) {
-          const int q = q0 + r;
-          const int32_t row = q < cnt ? my_row[q] : -1;
-          raw[r] = active && row >= 0 ? __ldg(reinterpret_cast<const uint4*>(row_ptr(p.T, row) + (size_t)col *
-                                                                              (RD == MT_F32 ? 4 : 2)))
-                                      : zero;
-        }
-#pragma unroll
-        for (int r = 0; r < UNR; ++r) {
-          const int q = q0 + r;
-          if (q >= cnt) break;
-          while (q >= q_end && b < B) {  // position q starts a later bag
-            flush(b, q_end);
-            ++b;
-            q_end = b < B ? rel(__ldg(&p.bag_offsets[b + 1]), p0) : cnt;
+            for (int j = 0; j < NP; ++j) {
+              const f32x2 oh = __shfl_xor_sync(kFull, hi[j], o), ol = __shfl_xor_sync(kFull, lo[j], o);
+              f32x2 s, e;
+              two_sum(hi[j], oh, s, e);
+              hi[j] = s;
+              lo[j] = add2(add2(lo[j], ol), e);
+            }
           }
-          if (b >= B || q < q_skip) continue;  // in no bag
-          const uint32_t w[4] = {raw[r].x, raw[r].y, raw[r].z, raw[r].w};
+          if (sub == 0 && active) {
 #pragma unroll
-          for (int j = 0; j < NP; ++j) {
-            const f32x2 x = RD == MT_F32 ? pk(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1]))
-                                         : bf16x2_to_f32x2(w[j]);
-            f32x2 s, e;
-            two_sum(hi[j], x, s, e);
-            hi[j] = s;
-            lo[j] = add2(lo[j], e);
+            for (int j = 0; j < NP; ++j) {
+              const float2 h = upk(hi[j]), l = upk(lo[j]);
+              if (whole && p.mode != MT_POOL_MEAN) {  // the exact sum h + l, rounded once
+                *reinterpret_cast<float2*>(p.out + (size_t)b * d + col + 2 * j) =
+                    make_float2(__fadd_rn(h.x, l.x), __fadd_rn(h.y, l.y));
+                continue;
+              }
+              const double s0 = (double)h.x + (double)l.x, s1 = (double)h.y + (double)l.y;
+              if (whole) {
+                *reinterpret_cast<float2*>(p.out + (size_t)b * d + col + 2 * j) =
+                    make_float2((float)(s0 / len), (float)(s1 / len));
+              } else {
+                double* a = p.acc + (size_t)b * d + col + 2 * j;
+                atomicAdd(a, s0);
+                atomicAdd(a + 1, s1);
+              }
+            }
           }
         }
       }
-      if (b < B) flush(b, q_end);
+      qs = qe;
     }
-    __syncwarp(team_mask);  // my_row is refilled by the next chunk
+    __syncwarp();  // my_row is refilled by the next chunk
   }
 }
 
@@ -246,9 +283,8 @@ cudaError_t launch_pool(const PoolParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (p.n > 0) {
     const long long chunks = (p.n + kPoolChunk - 1) / kPoolChunk;
-    const long long teams_per_block = 256 >> p.team_shift;
     MT_LAUNCH("k_pool", s);
-    const int grid = grid_for(chunks * (256 / teams_per_block), 256, 16);
+    const int grid = grid_for(chunks * 32, 256, 16);  // a warp per chunk
     if (p.T.row_dtype == MT_F32) k_pool<MT_F32><<<grid, 256, 0, s>>>(p);
     else k_pool<MT_BF16><<<grid, 256, 0, s>>>(p);
   }
