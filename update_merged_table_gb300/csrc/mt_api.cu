@@ -20,6 +20,23 @@ int sm_count() {
   }
   return v;
 }
+
+// Positions per heavy warp-chunk of a backward over n positions.  A team's
+// share stays at most kTeamShare (its positions are staged in shared memory)
+// and a warp-chunk at least kTeamShare positions, so that no batch makes more
+// warp-chunks than the workspace layout counts (n / kTeamShare + one per
+// heavy key).  Within that range the warp-chunk covers n / (6 x SMs)
+// positions: long enough to amortise its start and its fp64 partial sums
+// (batches of 0.26M and more keep the longest), short enough that a small
+// batch's hottest key is not one warp's serial chain (a 4096-ID batch put its
+// hottest key's few hundred positions in one 512-position warp-chunk).
+int heavy_warp_chunk(long long n, int team_shift) {
+  const long long tpw = 32 >> team_shift;  // teams per warp
+  const long long parts = (long long)sm_count() * 6;
+  long long wc = (n + parts - 1) / parts;
+  wc = (wc + tpw - 1) / tpw * tpw;
+  return (int)std::max<long long>(kTeamShare, std::min<long long>(wc, kTeamShare * tpw));
+}
 }  // namespace mt
 
 struct mt_table {
@@ -211,7 +228,7 @@ int run_backward(mt_table* t, const mt_lookup_result* res, int64_t n, const void
   p.gsum_out = gsum_out;
   mt::bind_backward_ws(p, w, L);
   p.team_shift = mt::backward_team_shift(t->cfg.dim, (int)t->cfg.row_dtype);
-  p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
+  p.warp_chunk = mt::heavy_warp_chunk(n, p.team_shift);
   const int rc = cuda_status(mt::launch_backward(p, stream));
   if (rc == MT_OK) t->step += 1;
   return rc;

@@ -35,6 +35,7 @@ namespace mt {
 const TableDev& table_dev(const mt_table* t);
 mt_config table_cfg(const mt_table* t);
 void table_count_step(mt_table* t);
+int heavy_warp_chunk(long long n, int team_shift);
 }  // namespace mt
 
 struct mt_shard_group {
@@ -515,7 +516,7 @@ int mt_shard_backward_adam(mt_shard_group* g, const mt_lookup_result* results, c
     p.reduce_only = reduce_only;
     mt::bind_backward_ws(p, scr, BL);
     p.team_shift = mt::backward_team_shift(T.dim, T.row_dtype);
-    p.warp_chunk = mt::kTeamShare * (32 >> p.team_shift);
+    p.warp_chunk = mt::heavy_warp_chunk(p.n, p.team_shift);
     return mt::launch_backward(p, st) == cudaSuccess ? MT_OK : MT_ECUDA;
   };
   // each rank's (or owner's) own slice of the scratch: offsets of backward workspaces side by side
