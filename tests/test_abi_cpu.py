@@ -208,3 +208,26 @@ def test_grouped_lookup_rejects_a_table_in_two_groups(lib):
     gn = (ctypes.c_int64 * 2)()
     ws = ctypes.c_void_p(4096)
     assert lib.mt_lookup_grouped(tabs, 2, pl, None, 0, fo, 1, 1, None, res, gn, ws, 1 << 20, None) == mt.MT_EINVAL
+
+
+def test_pooled_and_sharded_calls_reject_bad_handles_on_host(lib):
+    """The pooled-bag and sharded entry points refuse missing handles, sizes and modes before any device
+    call (no GPU here)."""
+    r = mt._Result(0, 0, 0, 0, 0)
+    assert lib.mt_pool_workspace_bytes(None, 10) == 0
+    assert lib.mt_pool_forward(None, ctypes.byref(r), 0, None, 1, mt.POOL_SUM, None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_backward_pooled_workspace_bytes(None, 10, 10) == 0
+    assert lib.mt_backward_adam_pooled(None, ctypes.byref(r), 0, None, 1, mt.POOL_SUM, None, None, None, None, 0,
+                                       None) == mt.MT_EINVAL
+    out = ctypes.c_void_p(1)
+    assert lib.mt_shard_group_create(None, 2, ctypes.byref(out)) == mt.MT_EINVAL and out.value is None
+    shards = (ctypes.c_void_p * 2)(None, None)
+    assert lib.mt_shard_group_create(shards, 0, ctypes.byref(out)) == mt.MT_EINVAL
+    max_shards = int(re.search(r"#define MT_MAX_SHARDS (\d+)", open(os.path.join(ROOT, "include", "mt.h")).read()).group(1))
+    assert lib.mt_shard_group_create(shards, max_shards + 1, ctypes.byref(out)) == mt.MT_EINVAL
+    assert lib.mt_shard_group_create(shards, 2, None) == mt.MT_EINVAL
+    assert lib.mt_shard_group_destroy(None) == mt.MT_EINVAL
+    n = (ctypes.c_int64 * 2)(10, 10)
+    assert lib.mt_shard_workspace_bytes(None, n) == 0
+    assert lib.mt_shard_lookup(None, None, n, None, None, 1, 1, None, None, None, 0, None) == mt.MT_EINVAL
+    assert lib.mt_shard_backward_adam(None, None, None, mt.MT_F32, None, None, None, 0, None) == mt.MT_EINVAL
